@@ -1,0 +1,281 @@
+"""Plain fp64 CPU oracle of the dropless MoE layer forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library: the arithmetic lives in ``moe_oracle.c`` (plain loops,
+fp64 on exactly widened bf16 inputs); this module only compiles it with gcc,
+marshals numpy arrays and chains the stages in the order the pages give
+("MoE & MLA operators", sec. 2.1: router -> permute -> grouped GEMM ->
+combine; "Dropless and grouped GEMM", sec. 1: routed + shared).
+
+Array conventions (numpy):
+  bf16 tensors are passed as their uint16 bit patterns; x [T, d],
+  Wg [d, E], W1/W3 [E, d, de], W2 [E, de, d], Ws1/Ws3 [d, ds], Ws2 [ds, d];
+  bias float32 [E]; topk_idx int32 [T, k]; gates float64.
+
+Pinned by ``tests/test_oracle_pins.py`` against the padding worked example
+("Dropless and grouped GEMM", sec. 3), the ledger figures, brute-force
+routing, a stable library argsort, closed-form softmax identities, the
+textbook dense SwiGLU MLP (k = 1, E = 1) and the exact permute/direct
+equivalence ("MoE & MLA operators", sec. 2.3).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I, LL, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+            sig = {
+                "or_bf16_to_double": (D, [ctypes.c_uint16]),
+                "or_round_bf16": (D, [D]),
+                "or_double_to_bf16_bits": (ctypes.c_uint16, [D]),
+                "or_router_logits": (None, [I, I, I, P, P, P, P]),
+                "or_route": (I, [I, I, I, I, I, P, P, P, P]),
+                "or_rows_capacity": (LL, [LL, I, I]),
+                "or_blocks_capacity": (LL, [LL, I, I]),
+                "or_build_offsets": (I, [LL, I, I, P, P, P, P, P, P, P, P, P]),
+                "or_permute": (None, [LL, I, I, P, P, P]),
+                "or_grouped_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P]),
+                "or_expert_rows": (I, [I, I, I, I, P, P, P, P, P, P, P, P]),
+                "or_shared_expert": (I, [I, I, I, P, P, P, P, P, P]),
+                "or_combine": (None, [I, I, I, P, P, P, P]),
+                "or_direct_layer": (I, [I, P, I, I, I, I, P, P, P, P, P, P, P, P]),
+                "or_round_bf16_array": (None, [LL, P, P]),
+                "or_num_threads": (I, []),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc, what):
+    if rc == 1:
+        raise ValueError(f"oracle {what}: invalid argument")
+    if rc == 2:
+        raise ValueError(f"oracle {what}: expert id out of range")
+
+
+def num_threads() -> int:
+    return int(_L().or_num_threads())
+
+
+# ---------------------------------------------------------------- bf16 ----
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest bf16 value (ties to even), returned as fp64."""
+    a = _c(v, np.float64)
+    out = np.empty_like(a)
+    _L().or_round_bf16_array(a.size, _p(a), _p(out))
+    return out
+
+
+# --------------------------------------------------------------- stages ----
+def rows_capacity(A: int, E: int, P: int) -> int:
+    return int(_L().or_rows_capacity(A, E, P))
+
+
+def blocks_capacity(A: int, E: int, P: int) -> int:
+    return int(_L().or_blocks_capacity(A, E, P))
+
+
+def router_logits(x, Wg, bias=None) -> np.ndarray:
+    x = _c(x, np.uint16)
+    Wg = _c(Wg, np.uint16)
+    T, d = x.shape
+    E = Wg.shape[1]
+    assert Wg.shape[0] == d
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), np.float64)
+    _L().or_router_logits(T, d, E, _p(x), _p(Wg), _p(b), _p(out))
+    return out
+
+
+def route(logits, k: int, n_groups: int = 0, topk_groups: int = 0):
+    """Top-k (optionally group-limited) routing -> (idx int32 [T,k],
+    gates fp64 [T,k], margin fp64 [T])."""
+    lg = _c(logits, np.float64)
+    T, E = lg.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    m = np.empty((T,), np.float64)
+    _check(_L().or_route(T, E, k, n_groups, topk_groups, _p(lg), _p(idx), _p(w), _p(m)), "route")
+    return idx, w, m
+
+
+def build_offsets(topk_idx, topk_w, E: int, P: int) -> dict:
+    idx = _c(topk_idx, np.int32).reshape(-1)
+    A = idx.size
+    w = None if topk_w is None else _c(topk_w, np.float64).reshape(-1)
+    R = rows_capacity(A, E, P)
+    NB = blocks_capacity(A, E, P)
+    counts = np.empty(E, np.int32)
+    po = np.empty(E + 1, np.int32)
+    meta = np.empty((NB, 3), np.int32)
+    nb = np.zeros(1, np.int32)
+    perm_row = np.empty(A, np.int32)
+    row_src = np.empty(R, np.int32)
+    row_gate = np.empty(R, np.float64)
+    _check(_L().or_build_offsets(A, E, P, _p(idx), _p(w), _p(counts), _p(po), _p(meta), _p(nb),
+                                 _p(perm_row), _p(row_src), _p(row_gate)), "build_offsets")
+    n = int(nb[0])
+    return dict(counts=counts, padded_offsets=po, block_metadata=meta[:n].copy(), num_blocks=n,
+                perm_row=perm_row, row_src=row_src, row_gate=row_gate, rows_capacity=R,
+                blocks_capacity=NB)
+
+
+def permute(x, row_src, k: int) -> np.ndarray:
+    """x_perm [R, d] uint16; pad rows are zero here (the method leaves them
+    unspecified and never reads them)."""
+    x = _c(x, np.uint16)
+    rs = _c(row_src, np.int32)
+    R = rs.size
+    d = x.shape[1]
+    out = np.zeros((R, d), np.uint16)
+    _L().or_permute(R, d, k, _p(x), _p(rs), _p(out))
+    return out
+
+
+def grouped_experts(x_perm, W1, W3, W2, block_metadata, row_gate):
+    """h [R, de] and y [R, d] in fp64 over the whole padded layout; pad rows
+    stay NaN."""
+    xp = _c(x_perm, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    W2 = _c(W2, np.uint16)
+    E, d, de = W1.shape
+    meta = _c(block_metadata, np.int32)
+    rg = _c(row_gate, np.float64)
+    R = xp.shape[0]
+    h = np.full((R, de), np.nan)
+    y = np.full((R, d), np.nan)
+    _check(_L().or_grouped_experts(d, de, E, meta.shape[0], _p(meta), _p(xp), _p(W1), _p(W3),
+                                   _p(W2), _p(rg), _p(h), _p(y)), "grouped_experts")
+    return h, y
+
+
+def expert_rows(xrows, experts, gates, W1, W3, W2):
+    """h [n, de], y [n, d] for a compact list of (row, expert, gate)."""
+    xr = _c(xrows, np.uint16)
+    ex = _c(experts, np.int32)
+    g = _c(gates, np.float64)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    W2 = _c(W2, np.uint16)
+    E, d, de = W1.shape
+    n = ex.size
+    h = np.empty((n, de))
+    y = np.empty((n, d))
+    _check(_L().or_expert_rows(n, d, de, E, _p(xr), _p(ex), _p(g), _p(W1), _p(W3), _p(W2), _p(h),
+                               _p(y)), "expert_rows")
+    return h, y
+
+
+def shared_expert(xrows, Ws1, Ws3, Ws2):
+    xr = _c(xrows, np.uint16)
+    Ws1 = _c(Ws1, np.uint16)
+    Ws3 = _c(Ws3, np.uint16)
+    Ws2 = _c(Ws2, np.uint16)
+    n, d = xr.shape
+    ds = Ws1.shape[1]
+    hs = np.empty((n, ds))
+    ys = np.empty((n, d))
+    _check(_L().or_shared_expert(n, d, ds, _p(xr), _p(Ws1), _p(Ws3), _p(Ws2), _p(hs), _p(ys)),
+           "shared_expert")
+    return hs, ys
+
+
+def combine(y, perm_row, k: int, ys=None) -> np.ndarray:
+    yy = _c(y, np.float64)
+    pr = _c(perm_row, np.int32)
+    T = pr.size // k
+    d = yy.shape[1]
+    s = None if ys is None else _c(ys, np.float64)
+    out = np.empty((T, d))
+    _L().or_combine(T, d, k, _p(yy), _p(pr), _p(s), _p(out))
+    return out
+
+
+def direct_layer(tokens, x, W1, W3, W2, topk_idx, topk_w, ys_rows=None) -> np.ndarray:
+    tok = _c(tokens, np.int32)
+    x = _c(x, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W3 = _c(W3, np.uint16)
+    W2 = _c(W2, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_w, np.float64)
+    E, d, de = W1.shape
+    k = idx.shape[1]
+    s = None if ys_rows is None else _c(ys_rows, np.float64)
+    out = np.empty((tok.size, d))
+    _check(_L().or_direct_layer(tok.size, _p(tok), d, de, E, k, _p(x), _p(W1), _p(W3), _p(W2),
+                                _p(idx), _p(w), _p(s), _p(out)), "direct_layer")
+    return out
+
+
+# ---------------------------------------------------------- whole layer ----
+def layer_forward(inp: dict, cfg) -> dict:
+    """Whole layer through the padded layout (router, offsets, permute,
+    grouped experts, shared expert, combine), every intermediate returned.
+    ``inp`` holds numpy arrays (see module doc); a pre-routed input carries
+    topk_idx / topk_w instead of Wg."""
+    if inp.get("topk_idx") is None:
+        logits = router_logits(inp["x"], inp["Wg"], inp.get("bias"))
+        idx, w, margin = route(logits, cfg.k, cfg.n_groups, cfg.topk_groups)
+    else:
+        logits, margin = None, None
+        idx = _c(inp["topk_idx"], np.int32)
+        w = _c(inp["topk_w"], np.float64)
+    off = build_offsets(idx, w, cfg.E, cfg.pad)
+    x_perm = permute(inp["x"], off["row_src"], cfg.k)
+    h, y = grouped_experts(x_perm, inp["W1"], inp["W3"], inp["W2"], off["block_metadata"],
+                           off["row_gate"])
+    hs = ys = None
+    if cfg.d_shared:
+        hs, ys = shared_expert(inp["x"], inp["Ws1"], inp["Ws3"], inp["Ws2"])
+    out = combine(y, off["perm_row"], cfg.k, ys)
+    return dict(logits=logits, topk_idx=idx, topk_w=w, margin=margin, x_perm=x_perm, h=h, y=y,
+                hs=hs, ys=ys, out=out, **off)

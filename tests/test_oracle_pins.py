@@ -1,0 +1,352 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a worked
+example printed on the pages (tests/golden/), brute force over all subsets,
+a library routine (numpy stable argsort, numpy matmul, torch's bf16
+conversion), a closed form, or the exact permute/direct equivalence that the
+TileLang page states.  A plausible mistake in the oracle (a dropped bias, a
+wrong sign in silu, a transposed weight, an off-by-one in the padding, an
+unstable segment order, a wrong tie-break) fails at least one of them.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routing_permute_grouped_gb300 import ledger
+from tests.helpers import bits, rand_bf16
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [float(v) if "." in v else int(v) for v in rest]
+    return vals
+
+
+# ------------------------------------------------------------- bf16 --------
+def test_bf16_widen_matches_torch():
+    x = torch.randn(4096) * 10
+    b = x.to(torch.bfloat16)
+    np.testing.assert_array_equal(oracle.bf16_to_f64(bits(b)), b.to(torch.float64).numpy())
+
+
+def test_bf16_rounding_matches_torch_rne():
+    # every fp32 value converts to bf16 with round-to-nearest-even in torch;
+    # the oracle rounds the same (exactly representable) value from fp64
+    g = torch.Generator().manual_seed(3)
+    f = torch.cat([torch.randn(20000, generator=g) * s for s in (1e-3, 1.0, 1e4)])
+    # exact ties: bf16 value + half an ulp
+    base = torch.randn(2000, generator=g).to(torch.bfloat16).to(torch.float32)
+    ulp_half = torch.ldexp(torch.ones_like(base), torch.frexp(base).exponent - 9)
+    f = torch.cat([f, base + ulp_half, base - ulp_half])
+    ref = f.to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(f.to(torch.float64).numpy())
+    np.testing.assert_array_equal(got, ref)
+
+
+# ---------------------------------------------------------- offsets --------
+def _prerouted_idx(counts, seed=0):
+    labels = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])
+    rng = np.random.default_rng(seed)
+    return labels[rng.permutation(labels.size)]
+
+
+def test_padding_worked_example():
+    gd = _golden("padding_dropless_sec3.txt")
+    counts = gd["counts"]
+    P = gd["pad"][0]
+    off = oracle.build_offsets(_prerouted_idx(counts), None, len(counts), P)
+    assert off["counts"].tolist() == counts
+    sizes = np.diff(off["padded_offsets"]).tolist()
+    assert sizes == gd["padded"]
+    assert [s - c for s, c in zip(sizes, counts)] == gd["pad_rows"]
+    assert off["padded_offsets"][-1] == gd["total_rows"][0]
+    assert off["padded_offsets"][-1] - sum(counts) == gd["total_pad"][0]
+    meta = off["block_metadata"]
+    per_expert = [int((meta[:, 0] == e).sum()) for e in range(len(counts))]
+    assert per_expert == gd["blocks"]
+    assert off["num_blocks"] == sum(gd["blocks"])
+    last_e0 = meta[meta[:, 0] == 0][-1]
+    assert last_e0[2] == gd["last_block_valid_e0"][0]
+    assert last_e0[1] == 169 * 128
+    # the bound of sec. 3: < P pad rows per expert
+    assert max(gd["pad_rows"]) <= P - 1 and sum(gd["pad_rows"]) <= len(counts) * (P - 1)
+
+
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_offsets_invariants_and_stable_order(P, seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 40))
+    T, k = int(rng.integers(1, 700)), int(rng.integers(1, 5))
+    # skewed, some experts empty
+    p = rng.dirichlet(np.full(E, 0.3))
+    idx = rng.choice(E, size=T * k, p=p).astype(np.int32)
+    w = rng.random(T * k)
+    off = oracle.build_offsets(idx, w, E, P)
+    c, po = off["counts"], off["padded_offsets"]
+    assert c.sum() == T * k
+    assert np.array_equal(c, np.bincount(idx, minlength=E))
+    s = np.diff(po)
+    assert (s % P == 0).all() and ((s - c) >= 0).all() and ((s - c) <= P - 1).all()
+    assert ((c == 0) == (s == 0)).all()
+    # stable order: inside a segment, ascending assignment index == numpy's
+    # stable argsort of the expert ids
+    order = np.argsort(idx, kind="stable")
+    expect_row = np.empty(T * k, np.int64)
+    pos = 0
+    for e in range(E):
+        seg = order[pos:pos + c[e]]
+        expect_row[seg] = po[e] + np.arange(c[e])
+        pos += c[e]
+    assert np.array_equal(off["perm_row"], expect_row)
+    rs = off["row_src"]
+    assert rs.size == T * k + E * (P - 1)
+    valid = rs >= 0
+    assert valid.sum() == T * k
+    assert np.array_equal(rs[off["perm_row"]], np.arange(T * k))
+    assert np.array_equal(off["row_gate"][off["perm_row"]], w)
+    assert (off["row_gate"][~valid] == 0).all()
+    # block table: ascending expert then m, heights P, valid_m = min(P, rest)
+    meta = off["block_metadata"]
+    assert off["num_blocks"] == int(np.sum(-(-c // P)))
+    assert off["num_blocks"] <= (T * k) // P + E
+    exp_meta = [[e, po[e] + m, min(P, c[e] - m)] for e in range(E) for m in range(0, c[e], P)]
+    assert meta.tolist() == exp_meta
+
+
+def test_offsets_decode_block_is_exact():
+    # "Dropless and grouped GEMM", sec. 10: 128 rows per expert is exactly one
+    # block of 128 with no padding
+    off = oracle.build_offsets(_prerouted_idx([128, 128, 0, 128]), None, 4, 128)
+    assert np.diff(off["padded_offsets"]).tolist() == [128, 128, 0, 128]
+    assert off["block_metadata"].tolist() == [[0, 0, 128], [1, 128, 128], [3, 256, 128]]
+
+
+def test_offsets_rejects_bad_expert():
+    with pytest.raises(ValueError):
+        oracle.build_offsets(np.array([0, 5], np.int32), None, 4, 128)
+
+
+# ------------------------------------------------------------ router -------
+def test_router_logits_match_library_matmul():
+    x = rand_bf16((37, 96), seed=1)
+    Wg = rand_bf16((96, 12), std=0.1, seed=2)
+    bias = np.random.default_rng(0).normal(0, 0.5, 12).astype(np.float32)
+    ref = oracle.bf16_to_f64(x) @ oracle.bf16_to_f64(Wg) + bias.astype(np.float64)
+    np.testing.assert_allclose(oracle.router_logits(x, Wg, bias), ref, rtol=1e-13, atol=1e-13)
+
+
+def _brute_topk(l, k, n_groups, topk_groups):
+    E = l.size
+    elig = list(range(E))
+    if n_groups:
+        gsz = E // n_groups
+        gs = [l[g * gsz:(g + 1) * gsz].max() for g in range(n_groups)]
+        best = max(itertools.combinations(range(n_groups), topk_groups),
+                   key=lambda c: sum(gs[g] for g in c))
+        elig = [e for e in range(E) if e // gsz in best]
+    best = max(itertools.combinations(elig, k), key=lambda c: sum(l[e] for e in c))
+    return sorted(best, key=lambda e: -l[e])
+
+
+@pytest.mark.parametrize("case", [(8, 2, 0, 0), (8, 3, 4, 2), (6, 1, 0, 0), (8, 4, 2, 1),
+                                  (8, 8, 0, 0), (8, 5, 4, 3)])
+def test_route_brute_force(case):
+    E, k, ng, tg = case
+    rng = np.random.default_rng(E * 100 + k * 10 + ng)
+    lg = rng.normal(size=(8, E))
+    idx, w, m = oracle.route(lg, k, ng, tg)
+    for t in range(8):
+        assert idx[t].tolist() == _brute_topk(lg[t], k, ng, tg)
+    # gates: softmax over the chosen logits == softmax over all E experts,
+    # renormalised over the chosen ones
+    p = np.exp(lg - lg.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    sel = np.take_along_axis(p, idx.astype(np.int64), 1)
+    np.testing.assert_allclose(w, sel / sel.sum(1, keepdims=True), rtol=1e-12)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-14)
+    # closed form of the ratio between two gates
+    np.testing.assert_allclose(w[:, 0] / w[:, -1],
+                               np.exp(np.take_along_axis(lg, idx[:, :1].astype(np.int64), 1)[:, 0] -
+                                      np.take_along_axis(lg, idx[:, -1:].astype(np.int64), 1)[:, 0]),
+                               rtol=1e-12)
+    assert (m > 0).all()
+
+
+def test_route_ties_go_to_lower_index():
+    lg = np.array([[1.0, 3.0, 3.0, 0.5, 3.0]])
+    idx, w, m = oracle.route(lg, 2)
+    assert idx.tolist() == [[1, 2]]
+    assert m[0] == 0.0
+    lg = np.array([[5.0, 0.0, 0.0, 5.0]])  # two groups with equal score
+    idx, _, _ = oracle.route(lg, 1, 2, 1)
+    assert idx.tolist() == [[0]]
+
+
+def test_group_limit_excludes_experts():
+    # expert 3 has the second-highest logit but its group (1) loses to group 0
+    # (max 9) and group 2 (max 8) when only 2 of 3 groups are kept
+    lg = np.array([[9.0, -5, 7.5, 7.6, -1, -1, 8.0, 1.0, 2.0]])
+    idx, _, _ = oracle.route(lg, 2, 3, 2)
+    assert idx.tolist() == [[0, 6]]
+    idx, _, _ = oracle.route(lg, 2)
+    assert idx.tolist() == [[0, 6]]
+    idx, _, _ = oracle.route(lg, 3, 3, 2)
+    assert idx.tolist() == [[0, 6, 2]]
+
+
+# ------------------------------------------------------ expert / layer -----
+class _Cfg:
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def _textbook_swiglu(x, W1, W3, W2):
+    """Dense SwiGLU MLP with library matmuls; h rounded to bf16."""
+    xf = oracle.bf16_to_f64(x)
+    g = xf @ oracle.bf16_to_f64(W1)
+    u = xf @ oracle.bf16_to_f64(W3)
+    h = oracle.round_bf16(g / (1.0 + np.exp(-g)) * u)
+    return h, h @ oracle.bf16_to_f64(W2)
+
+
+def test_moe_with_one_expert_is_dense_swiglu():
+    # k = 1, E = 1: every token goes to expert 0 with gate 1, so the layer is
+    # the dense SwiGLU MLP of the textbook
+    T, d, de = 150, 64, 96
+    x = rand_bf16((T, d), seed=5)
+    W1 = rand_bf16((1, d, de), std=d ** -0.5, seed=6)
+    W3 = rand_bf16((1, d, de), std=d ** -0.5, seed=7)
+    W2 = rand_bf16((1, de, d), std=de ** -0.5, seed=8)
+    Wg = rand_bf16((d, 1), std=d ** -0.5, seed=9)
+    cfg = _Cfg(k=1, E=1, n_groups=0, topk_groups=0, pad=128, d_shared=0)
+    res = oracle.layer_forward(dict(x=x, Wg=Wg, bias=None, W1=W1, W3=W3, W2=W2), cfg)
+    h_ref, y_ref = _textbook_swiglu(x, W1[0], W3[0], W2[0])
+    assert (res["topk_w"] == 1.0).all()
+    np.testing.assert_allclose(res["out"], y_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(res["h"][res["perm_row"]], h_ref)
+
+
+def test_shared_expert_is_dense_swiglu():
+    T, d, ds = 40, 64, 32
+    x = rand_bf16((T, d), seed=11)
+    Ws1 = rand_bf16((d, ds), std=0.125, seed=12)
+    Ws3 = rand_bf16((d, ds), std=0.125, seed=13)
+    Ws2 = rand_bf16((ds, d), std=0.17, seed=14)
+    hs, ys = oracle.shared_expert(x, Ws1, Ws3, Ws2)
+    h_ref, y_ref = _textbook_swiglu(x, Ws1, Ws3, Ws2)
+    np.testing.assert_array_equal(hs, h_ref)
+    np.testing.assert_allclose(ys, y_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_silu_sign_and_gate_scaling():
+    # silu(g) * u with g = u: h = g^2 sigmoid(g) is >= 0; a flipped sign in
+    # silu or a swapped gate/up weight gives negative values
+    d, de = 32, 16
+    x = rand_bf16((20, d), seed=21)
+    W = rand_bf16((1, d, de), std=0.2, seed=22)
+    W2 = rand_bf16((1, de, d), std=0.2, seed=23)
+    h, y = oracle.expert_rows(x, np.zeros(20, np.int32), np.full(20, 0.5), W, W, W2)
+    assert (h >= 0).all()
+    h1, y1 = oracle.expert_rows(x, np.zeros(20, np.int32), np.full(20, 1.0), W, W, W2)
+    np.testing.assert_allclose(y, 0.5 * y1, rtol=1e-15)
+    # gate and up are not interchangeable: silu(g) u != silu(u) g
+    W3 = rand_bf16((1, d, de), std=0.2, seed=24)
+    ha, _ = oracle.expert_rows(x, np.zeros(20, np.int32), np.ones(20), W, W3, W2)
+    hb, _ = oracle.expert_rows(x, np.zeros(20, np.int32), np.ones(20), W3, W, W2)
+    assert not np.array_equal(ha, hb)
+    h_ref, _ = _textbook_swiglu(x, W[0], W3[0], W2[0])
+    np.testing.assert_array_equal(ha, h_ref)
+
+
+@pytest.mark.parametrize("ng,tg,ds,P", [(0, 0, 0, 128), (4, 2, 48, 128), (0, 0, 48, 64)])
+def test_permute_combine_equals_direct_evaluation(ng, tg, ds, P):
+    # "MoE & MLA operators", sec. 2.3: permute -> per-assignment expert ->
+    # scatter-reduce equals evaluating each token's chosen experts directly,
+    # with a maximum error of exactly 0
+    T, d, de, E, k = 300, 64, 32, 8, 3
+    x = rand_bf16((T, d), seed=31)
+    inp = dict(x=x, Wg=rand_bf16((d, E), std=d ** -0.5, seed=32),
+               bias=np.random.default_rng(1).normal(0, 0.5, E).astype(np.float32),
+               W1=rand_bf16((E, d, de), std=d ** -0.5, seed=33),
+               W3=rand_bf16((E, d, de), std=d ** -0.5, seed=34),
+               W2=rand_bf16((E, de, d), std=de ** -0.5, seed=35))
+    if ds:
+        inp.update(Ws1=rand_bf16((d, ds), std=d ** -0.5, seed=36),
+                   Ws3=rand_bf16((d, ds), std=d ** -0.5, seed=37),
+                   Ws2=rand_bf16((ds, d), std=ds ** -0.5, seed=38))
+    cfg = _Cfg(k=k, E=E, n_groups=ng, topk_groups=tg, pad=P, d_shared=ds)
+    res = oracle.layer_forward(inp, cfg)
+    direct = oracle.direct_layer(np.arange(T), x, inp["W1"], inp["W3"], inp["W2"],
+                                 res["topk_idx"], res["topk_w"], res["ys"])
+    assert np.array_equal(res["out"], direct)
+    # the permuted rows really are copies of their token rows
+    rs = res["row_src"]
+    v = rs >= 0
+    assert np.array_equal(res["x_perm"][v], x[rs[v] // k])
+    # pad rows of y are never produced, and never needed by combine
+    assert np.isnan(res["y"][~v]).all()
+
+
+def test_direct_evaluation_detects_wrong_layout():
+    # plant a layout mistake in the oracle's own tables (swap two rows of
+    # perm_row): the equivalence check above must catch it
+    T, d, de, E, k = 50, 32, 16, 4, 2
+    x = rand_bf16((T, d), seed=41)
+    W1 = rand_bf16((E, d, de), std=0.2, seed=42)
+    W3 = rand_bf16((E, d, de), std=0.2, seed=43)
+    W2 = rand_bf16((E, de, d), std=0.2, seed=44)
+    Wg = rand_bf16((d, E), std=0.2, seed=45)
+    cfg = _Cfg(k=k, E=E, n_groups=0, topk_groups=0, pad=128, d_shared=0)
+    res = oracle.layer_forward(dict(x=x, Wg=Wg, bias=None, W1=W1, W3=W3, W2=W2), cfg)
+    pr = res["perm_row"].copy()
+    flat = res["topk_idx"].reshape(-1)
+    a = 0  # token 0; b: an assignment of another token with another expert
+    b = int(np.flatnonzero((flat != flat[0]) & (np.arange(flat.size) // k != 0))[0])
+    pr[a], pr[b] = pr[b], pr[a]
+    bad = oracle.combine(res["y"], pr, k)
+    direct = oracle.direct_layer(np.arange(T), x, W1, W3, W2, res["topk_idx"], res["topk_w"])
+    assert not np.array_equal(bad, direct)
+
+
+# ------------------------------------------------------------ ledgers ------
+def test_ledger_figures_of_the_pages():
+    g = _golden("ledger_pages.txt")
+    d, de = 7168, 2048
+    assert round(ledger.expert_flops_per_row(d, de) / 1e6, 2) == g["expert_flops_per_row_mflop"][0]
+    assert round(ledger.routed_flops(65536, d, de) / 1e12, 3) == g["routed_tflop_65536_rows"][0]
+    assert round(ledger.routed_flops(65792, d, de) / 1e12, 3) == g["routed_tflop_65792_rows"][0]
+    assert round(ledger.routed_flops(98304, d, de) / 1e12, 3) == g["routed_tflop_98304_rows"][0]
+    assert round(4 * ledger.routed_flops(65792, d, de) / 1e12, 3) == g["ungrouped_tflop_65792x4"][0]
+    gib = 2.0 ** 30
+    assert round(8192 * d * 2 / gib, 2) == g["mem_x_gib"][0]
+    assert round(65792 * d * 2 / gib, 2) == g["mem_recv_x_gib"][0]
+    assert round(65792 * 2 * de * 2 / gib, 2) == g["mem_h13_gib"][0]
+    assert round(65792 * de * 2 / gib, 2) == g["mem_h_gib"][0]
+    assert round(65792 * d * 2 / gib, 2) == g["mem_y_gib"][0]
+    T, E, k = 8192, 8, 4
+    assert round(ledger.router_flops(T, d, E) / 1e9, 2) == g["router_gflop"][0]
+    assert round(ledger.router_intensity(T, d, E), 1) == g["router_ai"][0]
+    assert ledger.permute_bytes_page(T, k, d) / 2 ** 20 == g["permute_mib"][0]
+    assert round(ledger.routed_flops(T * k, d, de) / 1e12, 2) == g["grouped_tflop"][0]
+    gb = ledger.grouped_gemm_bytes_page(T * k, E, d, de)
+    assert round(gb / 1e9, 2) == g["grouped_gb"][0]
+    assert round(ledger.routed_flops(T * k, d, de) / gb) == g["grouped_ai"][0]
+    assert ledger.permute_combine_bytes_page(T, k, d) / gib == g["permute_combine_gib"][0]
+    assert round(ledger.single_expert_intensity(16, d, de), 1) == g["single_expert_ai_16"][0]
+    assert round(ledger.single_expert_intensity(512, d, de)) == g["single_expert_ai_512"][0]
+    gd = _golden("padding_dropless_sec3.txt")
+    assert ledger.padded_rows(gd["counts"], 128) == gd["total_rows"][0]
+    assert round(100 * ledger.padding_waste(gd["counts"], 128), 2) == 0.39
