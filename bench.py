@@ -1,0 +1,459 @@
+"""Benchmark of the dropless MoE layer forward pass on GB300.
+
+Default workload (one GPU): T=8192 tokens, d=7168, d_e=2048, E=8 routed
+SwiGLU experts, top-4, per-expert logit bias N(0, 0.5), one shared expert of
+width 2048 (the pages' fused-MoE default shape).  A step is one whole layer
+forward: router -> offsets -> permute -> grouped GEMMs -> shared expert ->
+combine, on synthetic seeded inputs already resident in HBM.
+
+Prints one JSON line:
+  value    useful TFLOP/s of the layer (routed rows without padding + shared
+           expert), aggregated over ranks; replicas only for N > 1
+  e2e      the same metric through MoeLayer.forward with the token rows copied
+           from pinned host memory and the output copied back every step
+  roofline the grouped-GEMM stage (GEMM1 + SwiGLU, GEMM2 + gate) against the
+           measured bf16 tensor peak
+  stages   per-stage milliseconds and the permute / combine HBM GB/s
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload
+
+``--impl reference`` times the CPU oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from routing_permute_grouped_gb300 import ledger, synth  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    except OSError:
+        p = dict(FALLBACK)
+        p["source"] = "fallback"
+        return p
+
+
+# ------------------------------------------------------------ clocks ------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------- distributed ----
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(v: float, world: int) -> float:
+    """Maximum of a host value over all ranks (the slowest rank sets the
+    job time)."""
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ oracle ------
+def oracle_sample_tflops(shape, inp_host: dict, n_tokens: int):
+    """fp64 CPU oracle on n_tokens tokens of the workload: router for those
+    tokens, their routed experts (direct per-token evaluation) and the shared
+    expert.  Returns (useful TFLOP/s, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    tok = np.arange(n_tokens, dtype=np.int32)
+    x = bits(inp_host["x"][:n_tokens])
+    t0 = time.perf_counter()
+    if inp_host.get("Wg") is not None:
+        bias = None if inp_host.get("bias") is None else inp_host["bias"].numpy()
+        lg = oracle.router_logits(x, bits(inp_host["Wg"]), bias)
+        idx, w, _ = oracle.route(lg, shape.k, shape.n_groups, shape.topk_groups)
+    else:
+        idx = inp_host["topk_idx"][:n_tokens].numpy()
+        w = inp_host["topk_w"][:n_tokens].double().numpy()
+    ys = None
+    if shape.d_shared:
+        _, ys = oracle.shared_expert(x, bits(inp_host["Ws1"]), bits(inp_host["Ws3"]),
+                                     bits(inp_host["Ws2"]))
+    oracle.direct_layer(np.arange(n_tokens, dtype=np.int32), x, bits(inp_host["W1"]),
+                        bits(inp_host["W3"]), bits(inp_host["W2"]), idx, w, ys)
+    dt = time.perf_counter() - t0
+    flops = ledger.layer_useful_flops(n_tokens, shape.k, shape.d, shape.d_e, shape.d_shared)
+    if inp_host.get("Wg") is not None:
+        flops += ledger.router_flops(n_tokens, shape.d, shape.E)
+    return flops / dt / 1e12, dt, oracle.num_threads()
+
+
+def host_inputs(shape):
+    """CPU copies of the workload (seeded; same generator as the GPU run)."""
+    return synth.make_inputs(shape, device="cpu")
+
+
+# -------------------------------------------------------- reference arm ---
+def run_reference(args, shape, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    inp = host_inputs(shape)
+    n_tok = max(1, oracle.num_threads())  # one token per oracle thread per step
+    for _ in range(args.warmup):
+        oracle_sample_tflops(shape, inp, n_tok)
+    t0 = time.perf_counter()
+    flops = 0
+    threads = 1
+    for _ in range(args.steps):
+        _, _, threads = oracle_sample_tflops(shape, inp, n_tok)
+        flops += ledger.layer_useful_flops(n_tok, shape.k, shape.d, shape.d_e, shape.d_shared)
+        flops += ledger.router_flops(n_tok, shape.d, shape.E) if not shape.prerouted else 0
+    dt = time.perf_counter() - t0
+    val = flops / dt / 1e12
+    sample = (f"{n_tok} token(s) of the workload per step (router, routed experts, shared "
+              f"expert), {n_tok} oracle threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(shape),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "MoE layer fwd useful TFLOP/s (bf16, fp32 accumulate)"
+
+
+def config_dict(shape):
+    return {"workload": f"{shape.name}: T={shape.T} d={shape.d} d_e={shape.d_e} E={shape.E} "
+                        f"k={shape.k} groups={shape.n_groups}/{shape.topk_groups} "
+                        f"pad={shape.pad} shared={shape.d_shared}",
+            "l2": "inputs larger than L2 (expert weights and permuted rows exceed 129 MB)",
+            "parallelism": "replicas"}
+
+
+# -------------------------------------------------------------- ours ------
+def run_ours(args, shape, rank, world, local):
+    import routing_permute_grouped_gb300 as moe
+    from routing_permute_grouped_gb300 import build as moe_build
+
+    moe_build.build()
+    moe.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.make_inputs(shape, device=dev)
+    cfg = moe.config_of(shape)
+    layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
+                         bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
+                         Ws2=inp.get("Ws2"))
+    x = inp["x"]
+    out = torch.empty_like(x)
+    L = layer.layout
+    ws = layer.ws
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    T, k, E, d, de, ds = shape.T, shape.k, shape.E, shape.d, shape.d_e, shape.d_shared
+    A, R, NB = shape.A, shape.rows_capacity, shape.blocks_capacity
+    buf = layer.buffer
+    topk_idx = buf("topk_idx", i32, (T, k)) if not shape.prerouted else inp["topk_idx"]
+    topk_w = buf("topk_w", f32, (T, k)) if not shape.prerouted else inp["topk_w"]
+    counts, po = buf("counts", i32, (E,)), buf("padded_offsets", i32, (E + 1,))
+    meta, nb = buf("block_metadata", i32, (NB, 3)), buf("num_blocks", i32, (1,))
+    perm_row, row_src = buf("perm_row", i32, (A,)), buf("row_src", i32, (R,))
+    row_gate = buf("row_gate", f32, (R,))
+    x_perm, h, y = buf("x_perm", bf, (R, d)), buf("h", bf, (R, de)), buf("y", bf, (R, d))
+    hs = buf("hs", bf, (T, ds)) if ds else None
+    ys = buf("ys", bf, (T, d)) if ds else None
+    status_word = buf("status", i32, (1,))
+    offs_ws = ws[L["status"]:L["topk_idx"]]
+
+    stage_names = ["route", "offsets", "permute", "grouped_gemm", "shared", "combine"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        if not shape.prerouted:
+            moe.moe_route(cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w)
+        if ev is not None:
+            ev[1].record()
+        moe.moe_build_offsets(cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src,
+                              row_gate, offs_ws)
+        if ev is not None:
+            ev[2].record()
+        moe.moe_permute(cfg, x, perm_row, x_perm)
+        if ev is not None:
+            ev[3].record()
+        moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, row_gate, h, y,
+                                    status_word)
+        if ev is not None:
+            ev[4].record()
+        if ds:
+            moe.moe_shared_expert(cfg, x, layer.Ws13, layer.Ws2_t, hs, ys, status_word)
+        if ev is not None:
+            ev[5].record()
+        moe.moe_combine(cfg, y, perm_row, ys, out)
+        if ev is not None:
+            ev[6].record()
+
+    launches_per_step = (0 if shape.prerouted else 1) + 3 + 1 + 2 + (2 if ds else 0) + 1
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    # device-timed region: K steps; every stage bracketed by CUDA events on
+    # the stream the kernels run on (torch's current stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms_total = t_start.elapsed_time(t_end)
+    ms_max = reduce_max(ms_total, world)
+    stage_ms = {n: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
+                for j, n in enumerate(stage_names)}
+
+    counts_h = counts.cpu().tolist()
+    useful = ledger.layer_useful_flops(T, k, d, de, ds)
+    flops_job = reduce_sum(useful * args.steps, world)
+    value = flops_job / (ms_max / 1e3) / 1e12
+    st = layer.device_status()
+    if st:
+        raise RuntimeError(f"device status bits {st:#x}")
+
+    # e2e through the public API with host buffers
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty_like(x)
+    topk_kw = {}
+    if shape.prerouted:
+        idx_host = inp["topk_idx"].cpu().pin_memory()
+        w_host = inp["topk_w"].cpu().pin_memory()
+        idx_dev, w_dev = torch.empty_like(inp["topk_idx"]), torch.empty_like(inp["topk_w"])
+        topk_kw = dict(topk_idx=idx_dev, topk_w=w_dev)
+    h2d = x_host.numel() * 2 + (idx_host.numel() * 8 if shape.prerouted else 0)
+    d2h = out_host.numel() * 2
+    e2e_steps = max(1, min(args.steps, 100))
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        if shape.prerouted:
+            idx_dev.copy_(idx_host, non_blocking=True)
+            w_dev.copy_(w_host, non_blocking=True)
+        layer(x_dev, out_dev, **topk_kw)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+
+    pk = peaks()
+    gemm_flops = ledger.routed_flops(A, d, de)
+    gemm_ach = gemm_flops / (stage_ms["grouped_gemm"] / 1e3) / 1e12
+    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    perm_bytes = ledger.permute_bytes_alg(T, k, d)
+    comb_bytes = ledger.combine_bytes_alg(T, k, d, bool(ds))
+    perm_gbs = perm_bytes / (stage_ms["permute"] / 1e3) / 1e9
+    comb_gbs = comb_bytes / (stage_ms["combine"] / 1e3) / 1e9
+    traffic = recorded_traffic("grouped_gemm", shape.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(shape),
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
+                     "achieved": gemm_ach, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": gemm_ach / peak_t, "peak_source": pk["source"] + " sustained bf16",
+                     "traffic": traffic},
+        "stages": {"ms": {n: round(v, 4) for n, v in stage_ms.items()},
+                   "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],
+                   "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm_gbs"],
+                   "expert_counts": counts_h,
+                   "padded_rows": ledger.padded_rows(counts_h, shape.pad)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
+        # calibrate to ~15 s of oracle work
+        tf1, dt1, _ = oracle_sample_tflops(shape, host, 2)
+        n = max(2, min(shape.T, int(2 * 15.0 / max(dt1, 1e-3))))
+        tf, dt, threads = oracle_sample_tflops(shape, host, n)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {n} tokens of the workload: router, routed "
+                                          f"experts and shared expert ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    from routing_permute_grouped_gb300 import build as moe_build
+
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_digest") != moe_build._digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="default", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    shape = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape, rank, world)
+    else:
+        run_ours(args, shape, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) dropless MoE layer forward pass.
+ *
+ * One layer = router (GEMM + softmax + top-k, optionally group-limited)
+ *           -> per-expert counts / padded offsets / block table
+ *           -> permute (token rows into expert order)
+ *           -> grouped SwiGLU expert GEMMs (+ dense shared expert)
+ *           -> combine (sum back into token order).
+ * The decomposition is the four-stage one of "MoE & MLA operators" (TileLang
+ * tutorial), sec. 2.1, with the shared expert of "Dropless and grouped GEMM",
+ * sec. 1 added to the routed result.
+ *
+ * Conventions for every entry point
+ *  - Pointers named as device buffers are device pointers owned by the caller;
+ *    the library never allocates, frees or keeps them.  bf16 tensors are
+ *    passed as `void *` (IEEE bfloat16, 2 bytes per element), row-major.
+ *  - `stream` is a cudaStream_t passed as `void *` (NULL = legacy default
+ *    stream).  Every call only enqueues work on it and returns; nothing
+ *    synchronises with the host, and no launch size depends on routed data:
+ *    kernels read the number of blocks from device memory and size their
+ *    grids from static upper bounds.
+ *  - Argument errors return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before
+ *    anything is enqueued.  A failed launch returns MOE_ERR_CUDA.  Data errors
+ *    that only the device can see (an expert id outside [0, E), a wait that
+ *    timed out) set a word in the workspace, readable with
+ *    moe_get_device_status().
+ *  - A call with T == 0 enqueues nothing and returns MOE_OK.
+ *  - Requirements on shapes: d % 128 == 0, d_e % 128 == 0,
+ *    d_shared % 128 == 0 (or 0), 1 <= E <= 256, 1 <= k <= 8, pad_multiple 64
+ *    or 128, group-limited routing needs E % n_groups == 0,
+ *    n_groups <= 32 and topk_groups * (E / n_groups) >= k.  Routing also needs
+ *    k <= E; pre-routed input (moe_build_offsets) may repeat an expert.
+ *
+ * Derived sizes (all host-computable from the config, never from the data):
+ *    A      = T * k                       routed assignments
+ *    R_max  = A + E * (pad_multiple - 1)  padded-row capacity
+ *    NB_max = A / pad_multiple + E        block capacity
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent config */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid MoE, but a shape this build does not run */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_DEVICE_CHECK = 5  /* the device flagged bad data or a timed-out wait */
+} moe_status_t;
+
+/* Device error bits reported by moe_get_device_status(). */
+#define MOE_DEVERR_EXPERT_RANGE 0x1u /* an expert id outside [0, E) was skipped */
+#define MOE_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel gave up */
+
+typedef struct {
+    int32_t T;            /* tokens */
+    int32_t d;            /* model width */
+    int32_t d_e;          /* routed expert width */
+    int32_t E;            /* routed experts */
+    int32_t k;            /* experts per token */
+    int32_t n_groups;     /* expert groups for group-limited routing, 0 = none */
+    int32_t topk_groups;  /* groups kept per token when n_groups > 0 */
+    int32_t pad_multiple; /* segment padding multiple P: 64 or 128 */
+    int32_t d_shared;     /* shared expert width, 0 = no shared expert */
+} moe_config_t;
+
+/* Packed weights as produced by the moe_pack_* calls (device pointers). */
+typedef struct {
+    const void *Wg_t;   /* router weight, K-major: bf16 [E, d] */
+    const float *bias;  /* per-expert logit bias fp32 [E], or NULL */
+    const void *W13;    /* routed gate/up weights: bf16 [E, 2*d_e, d] */
+    const void *W2;     /* routed down weights, K-major: bf16 [E, d, d_e] */
+    const void *Ws13;   /* shared gate/up: bf16 [2*d_shared, d], or NULL */
+    const void *Ws2;    /* shared down, K-major: bf16 [d, d_shared], or NULL */
+} moe_weights_t;
+
+/* Offsets (bytes) of every intermediate inside the moe_layer_fwd workspace,
+ * so a caller can read them back.  All offsets are multiples of 1024. */
+typedef struct {
+    size_t total;
+    size_t status;         /* uint32 device error word + build scratch */
+    size_t topk_idx;       /* int32 [T, k] */
+    size_t topk_w;         /* fp32 [T, k] */
+    size_t counts;         /* int32 [E] */
+    size_t padded_offsets; /* int32 [E + 1] */
+    size_t block_metadata; /* int32 [NB_max, 3] */
+    size_t num_blocks;     /* int32 [1] */
+    size_t perm_row;       /* int32 [A] */
+    size_t row_src;        /* int32 [R_max] */
+    size_t row_gate;       /* fp32 [R_max] */
+    size_t x_perm;         /* bf16 [R_max, d] */
+    size_t h;              /* bf16 [R_max, d_e] */
+    size_t y;              /* bf16 [R_max, d] */
+    size_t hs;             /* bf16 [T, d_shared] */
+    size_t ys;             /* bf16 [T, d] */
+} moe_workspace_layout_t;
+
+/* ---------------------------------------------------------------- sizes -- */
+
+/* Validates cfg (same rules as every call).  Returns MOE_OK or an error. */
+moe_status_t moe_check_config(const moe_config_t *cfg);
+
+/* Bytes of the moe_layer_fwd workspace; 0 if cfg is invalid. */
+size_t moe_workspace_size(const moe_config_t *cfg);
+
+/* Fills *layout with the moe_layer_fwd workspace layout. */
+moe_status_t moe_workspace_layout(const moe_config_t *cfg, moe_workspace_layout_t *layout);
+
+/* Bytes of the scratch that moe_build_offsets needs (status word + per-chunk
+ * expert counts); 0 if cfg is invalid. */
+size_t moe_offsets_workspace_size(const moe_config_t *cfg);
+
+/* ------------------------------------------------------------- packing -- */
+
+/* Router weight W_g [d, E] (the orientation of "MoE & MLA operators",
+ * sec. 2.2: logits = x[T,d] @ W_g[d,E]) -> Wg_t [E, d] (K-major).  One-time
+ * weight preparation, not part of the forward pass. */
+moe_status_t moe_pack_router(int32_t d, int32_t E, const void *Wg, void *Wg_t, void *stream);
+
+/* Expert weights W1 (gate), W3 (up) [E, d, de] and W2 (down) [E, de, d] ->
+ * W13 [E, 2*de, d] and W2_t [E, d, de], both K-major.  Inside W13 the gate
+ * and up rows are interleaved per 128 output columns: rows
+ * [256 j, 256 j + 128) hold gate columns [128 j, 128 j + 128) and rows
+ * [256 j + 128, 256 j + 256) the matching up columns, so that one 256-wide
+ * GEMM tile produces both halves of 128 SwiGLU outputs.  Gate and up share one
+ * read of the activations ("MoE & MLA operators", sec. 2.4(c); "Dropless and
+ * grouped GEMM", sec. 4 step 7: gate and up concatenated).  E = 1 packs a
+ * shared expert.  Requires de % 128 == 0, d % 128 == 0. */
+moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void *W1, const void *W3,
+                              const void *W2, void *W13, void *W2_t, void *stream);
+
+/* ----------------------------------------------------------- the stages -- */
+
+/* a1. Router ("MoE & MLA operators", sec. 2.2): logits = x Wg + bias,
+ * optionally restricted to the topk_groups best expert groups (group score =
+ * the group's largest logit), top-k by logit (ties to the lower index), gates
+ * = softmax over the k chosen logits.
+ *   x        bf16 [T, d]          device, read
+ *   Wg_t     bf16 [E, d]          device, read (moe_pack_router)
+ *   bias     fp32 [E] or NULL     device, read
+ *   topk_idx int32 [T, k]         device, written, descending logit order
+ *   topk_w   fp32 [T, k]          device, written
+ * Tensor cores compute the GEMM (fp32 accumulate); top-k runs in the
+ * epilogue, one token row per thread. */
+moe_status_t moe_route(const moe_config_t *cfg, const void *x, const void *Wg_t,
+                       const float *bias, int32_t *topk_idx, float *topk_w, void *stream);
+
+/* a2. Counts, padded offsets and the block table ("MoE & MLA operators",
+ * sec. 2.3: padded offsets with padding_M = 128 and
+ * block_metadata[total_m_blocks, 3] = [expert, m_start, valid_m]; "Dropless
+ * and grouped GEMM", sec. 3: each segment rounded up to a multiple of 128,
+ * sec. 5: segments in ascending expert order, the tile count computed on the
+ * device).  Padded size of a segment = ceil(count / P) * P.
+ *   topk_idx       int32 [A]        device, read (A = T*k, a = t*k + j)
+ *   topk_w         fp32 [A] or NULL device, read (NULL = weight 1)
+ *   counts         int32 [E]        device, written
+ *   padded_offsets int32 [E + 1]    device, written (exclusive prefix sum)
+ *   block_metadata int32 [NB_max,3] device, written: rows [0, num_blocks)
+ *                                   = [expert, first padded row, valid rows]
+ *   num_blocks     int32 [1]        device, written
+ *   perm_row       int32 [A]        device, written: padded row of assignment a
+ *                                   (-1 if its expert id was out of range)
+ *   row_src        int32 [R_max]    device, written: assignment of a padded
+ *                                   row, -1 for pad rows
+ *   row_gate       fp32 [R_max]     device, written: routing weight of a
+ *                                   padded row, 0 for pad rows
+ *   ws, ws_bytes   scratch >= moe_offsets_workspace_size(cfg), device
+ * Rows of a segment keep ascending assignment order, so the result is
+ * deterministic.  An expert id outside [0, E) is skipped and flagged with
+ * MOE_DEVERR_EXPERT_RANGE in the status word at the start of ws. */
+moe_status_t moe_build_offsets(const moe_config_t *cfg, const int32_t *topk_idx,
+                               const float *topk_w, int32_t *counts, int32_t *padded_offsets,
+                               int32_t *block_metadata, int32_t *num_blocks, int32_t *perm_row,
+                               int32_t *row_src, float *row_gate, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/* a3. Permute ("MoE & MLA operators", sec. 2.3: a data-dependent gather of
+ * token rows into expert order): x_perm[perm_row[t*k + j]] = x[t].  Each
+ * token row is read once and written k times with 16-byte accesses; pad rows
+ * of x_perm are not written.
+ *   x        bf16 [T, d]      device, read
+ *   perm_row int32 [A]        device, read (negative entries are skipped)
+ *   x_perm   bf16 [R_max, d]  device, written */
+moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
+                         void *x_perm, void *stream);
+
+/* a4 + a5. Grouped SwiGLU expert GEMMs over the block table ("MoE & MLA
+ * operators", sec. 2.4; "Dropless and grouped GEMM", sec. 5: one tile reads
+ * exactly one expert's weights, the tile list lives on the device):
+ *   h[r] = bf16( silu(x_perm[r] W1[e]) * (x_perm[r] W3[e]) )
+ *   y[r] = bf16( row_gate[r] * (h[r] W2[e]) )
+ * for every valid row r of every block [e, m_start, valid_m].  tcgen05 MMAs
+ * with fp32 accumulators in tensor memory, operands staged by TMA; SwiGLU is
+ * fused into the first GEMM's epilogue and the routing weight into the
+ * second's ("MoE & MLA operators", sec. 2.5: output * expert weight in the
+ * GEMM epilogue).  Pad rows of h and y are not written.
+ *   x_perm         bf16 [R_max, d]     device, read
+ *   W13, W2_t      packed weights      device, read (moe_pack_experts)
+ *   block_metadata int32 [NB_max, 3]   device, read
+ *   num_blocks     int32 [1]           device, read (never copied to the host)
+ *   row_gate       fp32 [R_max] or NULL (NULL = 1)
+ *   h              bf16 [R_max, d_e]   device, written
+ *   y              bf16 [R_max, d]     device, written
+ *   status         uint32 [1] device error word, or NULL */
+moe_status_t moe_grouped_gemm_swiglu(const moe_config_t *cfg, const void *x_perm, const void *W13,
+                                     const void *W2_t, const int32_t *block_metadata,
+                                     const int32_t *num_blocks, const float *row_gate, void *h,
+                                     void *y, uint32_t *status, void *stream);
+
+/* a6. Dense shared expert ("Dropless and grouped GEMM", sec. 1: it reads the
+ * original token rows, with no permute and no group sizes):
+ *   hs = bf16( silu(x Ws1) * (x Ws3) ),  ys = bf16( hs Ws2 )
+ * on the same tcgen05 kernels with a dense tile list.
+ *   x bf16 [T, d], Ws13/Ws2_t packed (moe_pack_experts with E = 1),
+ *   hs bf16 [T, d_shared], ys bf16 [T, d]; status as above. */
+moe_status_t moe_shared_expert(const moe_config_t *cfg, const void *x, const void *Ws13,
+                               const void *Ws2_t, void *hs, void *ys, uint32_t *status,
+                               void *stream);
+
+/* a7. Combine ("MoE & MLA operators", sec. 2.5 and 6.4: k-way sum back into
+ * token order in a fixed order, with wide accumulation):
+ *   out[t] = bf16( sum_{j=0..k-1} y[perm_row[t*k + j]] + shared_out[t] )
+ * summed in fp32 in exactly that order, one rounding at the end.  Pad rows
+ * are never read; a negative perm_row entry contributes nothing.
+ *   y bf16 [R_max, d], perm_row int32 [A], shared_out bf16 [T, d] or NULL,
+ *   out bf16 [T, d]; all device. */
+moe_status_t moe_combine(const moe_config_t *cfg, const void *y, const int32_t *perm_row,
+                         const void *shared_out, void *out, void *stream);
+
+/* --------------------------------------------------------- whole layer -- */
+
+/* The whole forward pass of one layer: a1 .. a7 enqueued on one stream,
+ * no host synchronisation.  ws must hold moe_workspace_size(cfg) bytes
+ * (layout in moe_workspace_layout); its intermediates stay readable after
+ * the call.  Requires w->Wg_t; w->Ws13/Ws2 when cfg->d_shared > 0.
+ *   x bf16 [T, d], out bf16 [T, d]; all device. */
+moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
+                           void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* The same layer for pre-routed input: the router is skipped and the given
+ * routing (topk_idx int32 [T, k], topk_w fp32 [T, k], device) is used as is;
+ * an expert may repeat within a token.  ("Dropless and grouped GEMM", sec. 4:
+ * the rows that reach a card arrive already routed.) */
+moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_t *w,
+                                     const void *x, const int32_t *topk_idx, const float *topk_w,
+                                     void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------- diagnostics -- */
+
+/* Synchronises `stream`, reads the uint32 device error word at the start of
+ * ws (a moe_layer_fwd workspace or a moe_build_offsets scratch) into
+ * *bits (may be NULL) and clears it.  Returns MOE_OK if it was 0, else
+ * MOE_ERR_DEVICE_CHECK.  This is the only call that synchronises; it is meant
+ * for checking, not for the hot path. */
+moe_status_t moe_get_device_status(void *ws, uint32_t *bits, void *stream);
+
+/* Static description of a status code. */
+const char *moe_status_string(moe_status_t s);
+
+/* Thread-local text of the last error seen by this thread (argument or CUDA
+ * error detail), "" if none. */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,303 @@
+"""GB300 (sm_103a) dropless MoE layer forward pass: Python binding.
+
+Every compute step runs in the CUDA library ``_build/libmoe_gb300.so``
+(C ABI in ``include/moe.h``); this module only marshals torch tensors into
+pointers, sizes and streams.  There is no fallback: if the library is not
+built, every call raises.  Build it with ``routing_permute_grouped_gb300.build.build()``
+(or ``__graft_entry__.build()``).
+
+Functions carry the names of the C entry points and take the same
+arguments, with torch CUDA tensors in place of device pointers and an
+optional ``stream`` (default: torch's current stream).  ``MoeLayer`` is the
+user-facing object: it packs the weights once, owns a workspace and runs the
+whole layer with one call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoeError", "MoeConfig", "MoeWeights", "MoeLayer", "config_of", "load",
+    "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
+    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_permute",
+    "moe_grouped_gemm_swiglu", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
+    "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string",
+]
+
+MOE_OK = 0
+DEVERR_EXPERT_RANGE = 0x1
+DEVERR_TIMEOUT = 0x2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"moe status {status}: {detail}")
+        self.status = status
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d", "d_e", "E", "k", "n_groups", "topk_groups", "pad_multiple", "d_shared")]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("Wg_t", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("W13", ctypes.c_void_p),
+                ("W2", ctypes.c_void_p), ("Ws13", ctypes.c_void_p), ("Ws2", ctypes.c_void_p)]
+
+
+_LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
+                  "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
+                  "y", "hs", "ys")
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in _LAYOUT_FIELDS]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the built CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path} is missing "
+                          "(run routing_permute_grouped_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    CP = ctypes.POINTER(MoeConfig)
+    sigs = {
+        "moe_check_config": (ctypes.c_int, [CP]),
+        "moe_workspace_size": (SZ, [CP]),
+        "moe_workspace_layout": (ctypes.c_int, [CP, ctypes.POINTER(_Layout)]),
+        "moe_offsets_workspace_size": (SZ, [CP]),
+        "moe_pack_router": (ctypes.c_int, [I32, I32, P, P, P]),
+        "moe_pack_experts": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P]),
+        "moe_route": (ctypes.c_int, [CP, P, P, P, P, P, P]),
+        "moe_build_offsets": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
+        "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P]),
+        "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
+        "moe_combine": (ctypes.c_int, [CP, P, P, P, P, P]),
+        "moe_layer_fwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, SZ, P]),
+        "moe_layer_fwd_prerouted": (ctypes.c_int,
+                                    [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ, P]),
+        "moe_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "moe_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        lib = load()
+        raise MoeError(status, f"{lib.moe_status_string(status).decode()}: "
+                               f"{lib.moe_last_error().decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def config_of(shape=None, **kw) -> MoeConfig:
+    """MoeConfig from a synth.MoeShape (or keyword fields)."""
+    if shape is not None:
+        kw = dict(T=shape.T, d=shape.d, d_e=shape.d_e, E=shape.E, k=shape.k,
+                  n_groups=shape.n_groups, topk_groups=shape.topk_groups,
+                  pad_multiple=shape.pad, d_shared=shape.d_shared, **kw)
+    kw.setdefault("n_groups", 0)
+    kw.setdefault("topk_groups", 0)
+    kw.setdefault("pad_multiple", 128)
+    kw.setdefault("d_shared", 0)
+    return MoeConfig(**kw)
+
+
+# ------------------------------------------------------------- sizes ------
+def moe_check_config(cfg: MoeConfig) -> None:
+    _check(load().moe_check_config(ctypes.byref(cfg)))
+
+
+def moe_workspace_size(cfg: MoeConfig) -> int:
+    return int(load().moe_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_workspace_layout(cfg: MoeConfig) -> dict:
+    L = _Layout()
+    _check(load().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)))
+    return {n: int(getattr(L, n)) for n in _LAYOUT_FIELDS}
+
+
+def moe_offsets_workspace_size(cfg: MoeConfig) -> int:
+    return int(load().moe_offsets_workspace_size(ctypes.byref(cfg)))
+
+
+# ----------------------------------------------------------- packing ------
+def moe_pack_router(Wg: torch.Tensor, Wg_t: torch.Tensor, stream=None) -> None:
+    d, E = Wg.shape
+    _check(load().moe_pack_router(d, E, _ptr(Wg), _ptr(Wg_t), _stream(stream)))
+
+
+def moe_pack_experts(W1, W3, W2, W13, W2_t, stream=None) -> None:
+    E, d, de = W1.shape
+    _check(load().moe_pack_experts(E, d, de, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(W13), _ptr(W2_t),
+                                   _stream(stream)))
+
+
+# ------------------------------------------------------------ stages ------
+def moe_route(cfg, x, Wg_t, bias, topk_idx, topk_w, stream=None) -> None:
+    _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg_t), _ptr(bias), _ptr(topk_idx),
+                            _ptr(topk_w), _stream(stream)))
+
+
+def moe_build_offsets(cfg, topk_idx, topk_w, counts, padded_offsets, block_metadata, num_blocks,
+                      perm_row, row_src, row_gate, ws, stream=None) -> None:
+    _check(load().moe_build_offsets(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(padded_offsets),
+        _ptr(block_metadata), _ptr(num_blocks), _ptr(perm_row), _ptr(row_src), _ptr(row_gate),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_permute(cfg, x, perm_row, x_perm, stream=None) -> None:
+    _check(load().moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(perm_row), _ptr(x_perm),
+                              _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate, h, y,
+                            status=None, stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
+        _ptr(num_blocks), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
+
+
+def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:
+    _check(load().moe_shared_expert(ctypes.byref(cfg), _ptr(x), _ptr(Ws13), _ptr(Ws2_t), _ptr(hs),
+                                    _ptr(ys), _ptr(status), _stream(stream)))
+
+
+def moe_combine(cfg, y, perm_row, shared_out, out, stream=None) -> None:
+    _check(load().moe_combine(ctypes.byref(cfg), _ptr(y), _ptr(perm_row), _ptr(shared_out),
+                              _ptr(out), _stream(stream)))
+
+
+def moe_layer_fwd(cfg, weights: MoeWeights, x, out, ws, stream=None) -> None:
+    _check(load().moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(out),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_fwd_prerouted(cfg, weights: MoeWeights, x, topk_idx, topk_w, out, ws,
+                            stream=None) -> None:
+    _check(load().moe_layer_fwd_prerouted(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(out),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error bits."""
+    bits = ctypes.c_uint32(0)
+    st = load().moe_get_device_status(_ptr(ws), ctypes.byref(bits), _stream(stream))
+    if st not in (MOE_OK, 5):
+        _check(st)
+    return int(bits.value)
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+# --------------------------------------------------------- the layer ------
+class MoeLayer:
+    """One dropless MoE layer on the current CUDA device.
+
+    Packs the weights once (``moe_pack_router`` / ``moe_pack_experts``) and
+    owns a workspace sized for ``T`` tokens.  ``forward(x)`` runs
+    ``moe_layer_fwd`` (or the pre-routed variant) on the current stream.
+    Weights use the pages' orientation: Wg [d, E], W1/W3 [E, d, d_e],
+    W2 [E, d_e, d], shared Ws1/Ws3 [d, d_s], Ws2 [d_s, d]; all bf16 CUDA
+    tensors; bias fp32 [E] or None.
+    """
+
+    def __init__(self, cfg: MoeConfig, W1, W3, W2, Wg=None, bias=None, Ws1=None, Ws3=None, Ws2=None,
+                 stream=None):
+        moe_check_config(cfg)
+        self.cfg = cfg
+        dev = W1.device
+        E, d, de = W1.shape
+        self.W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device=dev)
+        self.W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device=dev)
+        moe_pack_experts(W1, W3, W2, self.W13, self.W2_t, stream)
+        self.Wg_t = None
+        if Wg is not None:
+            self.Wg_t = torch.empty((E, d), dtype=torch.bfloat16, device=dev)
+            moe_pack_router(Wg, self.Wg_t, stream)
+        self.bias = None if bias is None else bias.to(device=dev, dtype=torch.float32).contiguous()
+        self.Ws13 = self.Ws2_t = None
+        if cfg.d_shared:
+            ds = cfg.d_shared
+            self.Ws13 = torch.empty((1, 2 * ds, d), dtype=torch.bfloat16, device=dev)
+            self.Ws2_t = torch.empty((1, d, ds), dtype=torch.bfloat16, device=dev)
+            moe_pack_experts(Ws1.unsqueeze(0).contiguous(), Ws3.unsqueeze(0).contiguous(),
+                             Ws2.unsqueeze(0).contiguous(), self.Ws13, self.Ws2_t, stream)
+        self.weights = MoeWeights(
+            Wg_t=None if self.Wg_t is None else self.Wg_t.data_ptr(),
+            bias=None if self.bias is None else self.bias.data_ptr(),
+            W13=self.W13.data_ptr(), W2=self.W2_t.data_ptr(),
+            Ws13=None if self.Ws13 is None else self.Ws13.data_ptr(),
+            Ws2=None if self.Ws2_t is None else self.Ws2_t.data_ptr())
+        self.layout = moe_workspace_layout(cfg)
+        self.ws = torch.empty(self.layout["total"], dtype=torch.uint8, device=dev)
+        self.ws[:256].zero_()
+
+    def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None):
+        if out is None:
+            out = torch.empty_like(x)
+        if topk_idx is None:
+            moe_layer_fwd(self.cfg, self.weights, x, out, self.ws, stream)
+        else:
+            moe_layer_fwd_prerouted(self.cfg, self.weights, x, topk_idx, topk_w, out, self.ws,
+                                    stream)
+        return out
+
+    __call__ = forward
+
+    def buffer(self, name: str, dtype, shape) -> torch.Tensor:
+        """A view of one intermediate of the workspace (see moe_workspace_layout)."""
+        off = self.layout[name]
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def device_status(self, stream=None) -> int:
+        return moe_get_device_status(self.ws, stream)

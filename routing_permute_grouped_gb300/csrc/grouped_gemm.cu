@@ -1,0 +1,494 @@
+// grouped_gemm.cu -- persistent tcgen05 grouped GEMM over the block table.
+//
+// One kernel serves the three tensor-core stages of the layer:
+//   router  : logits = x Wg^T (+ bias) and top-k in the epilogue
+//   GEMM1   : [g | u] = x_perm W13[e]^T, h = bf16(silu(g) * u)
+//   GEMM2   : y = bf16(row_gate * (h W2[e]^T))
+// The work list is the block table [expert, m_start, valid_m] built on the
+// device ("MoE & MLA operators", sec. 2.3; "Dropless and grouped GEMM",
+// sec. 5: a tile reads exactly one expert's weights, the tile count lives in
+// device memory and the host never learns the per-expert sizes).  A tile is
+// one 128-row block x one BN-column panel; tiles are numbered block-major with
+// the N panel fastest, so the CTAs running at the same time share the A block
+// and one expert's weights in L2.
+//
+// CTA = 6 warps, one CTA per SM, persistent over tiles:
+//   warp 0      TMA producer: A and B tiles (64 K-columns, 128-byte swizzle)
+//               into a ring of shared-memory stages guarded by mbarriers
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
+//               (M=128, N=BN, K=16) into one of two TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per
+//               thread), fused SwiGLU / gate / top-k, stores to global memory
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1.  Every wait is bounded; on a timeout the CTA flags the status word,
+// drains what it has in flight and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
+constexpr int kThreads = 192;
+constexpr uint32_t kDevErrTimeout = 0x2u;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                     : (2 * BN <= 256) ? 256 : 512;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+    static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
+    static_assert(STAGES >= 2, "need at least two stages");
+};
+
+struct TileInfo {
+    int e, m0, vm, nb;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
+    TileInfo ti;
+    const int mb = t / a.n_tiles;
+    ti.nb = t - mb * a.n_tiles;
+    if (a.block_metadata) {
+        ti.e = __ldg(a.block_metadata + 3 * mb + 0);
+        ti.m0 = __ldg(a.block_metadata + 3 * mb + 1);
+        ti.vm = __ldg(a.block_metadata + 3 * mb + 2);
+    } else {
+        ti.e = 0;
+        ti.m0 = mb * BM;
+        ti.vm = min(BM, a.dense_rows - ti.m0);
+    }
+    return ti;
+}
+
+__device__ __forceinline__ float bf16_bits_lo(uint32_t v) { return __uint_as_float(v << 16); }
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+// ----------------------------------------------------------- epilogues --
+
+// GEMM1: columns [0, 128) of the tile are gate, [128, 256) up, for the 128
+// SwiGLU outputs [nb*128, nb*128 + 128) of row m0 + row.
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                           int row) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const bool valid = row < ti.vm;
+    __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * 128;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + c * 32, g);
+        tmem_ld32(taddr + 128 + c * 32, u);
+        tmem_ld_wait();
+        if (valid) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                p[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        }
+    }
+}
+
+// GEMM2: y = bf16(gate * acc) for the BN output columns of the tile.
+template <int BN>
+__device__ __forceinline__ void epi_gate(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                         int row) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const bool valid = row < ti.vm;
+    const float gate = (valid && a.row_gate) ? __ldg(a.row_gate + ti.m0 + row) : 1.0f;
+    __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                p[i] = pack_bf16x2(gate * __uint_as_float(v[2 * i]), gate * __uint_as_float(v[2 * i + 1]));
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        }
+    }
+}
+
+// Router: the thread owns token m0 + row and its E logits (TMEM columns
+// [0, E)).  Group-limited routing keeps the topk_groups groups with the
+// largest maximum logit; top-k runs over the eligible experts in ascending
+// index order with strict comparisons, so the lower index wins a tie; the
+// gates are a softmax over the k chosen logits.
+template <int BN>
+__device__ __forceinline__ void epi_router(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                           int row) {
+    const int E = a.E, k = a.k;
+    const int token = ti.m0 + row;
+    const bool valid = row < ti.vm;
+    uint32_t gmask = 0xFFFFFFFFu;
+    int gsz = E;
+    if (a.n_groups > 0) {
+        gsz = E / a.n_groups;
+        float gs[32];
+#pragma unroll
+        for (int g = 0; g < 32; ++g) gs[g] = -FLT_MAX;
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = c * 16 + i;
+                if (e < E) {
+                    const float l = __uint_as_float(v[i]) + (a.bias ? __ldg(a.bias + e) : 0.0f);
+                    const int g = e / gsz;
+                    gs[g] = fmaxf(gs[g], l);
+                }
+            }
+        }
+        gmask = 0;
+        for (int r = 0; r < a.topk_groups; ++r) {
+            int bi = -1;
+            float bv = -FLT_MAX;
+            for (int g = 0; g < a.n_groups; ++g) {
+                if (gmask & (1u << g)) continue;
+                if (bi < 0 || gs[g] > bv) {
+                    bi = g;
+                    bv = gs[g];
+                }
+            }
+            gmask |= 1u << bi;
+        }
+    }
+    float tv[8];
+    int ti_[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        tv[s] = -FLT_MAX;
+        ti_[s] = -1;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e = c * 16 + i;
+            if (e < E && ((gmask >> (e / gsz)) & 1u)) {
+                float cv = __uint_as_float(v[i]) + (a.bias ? __ldg(a.bias + e) : 0.0f);
+                int ci = e;
+                bool shifting = false;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    if (s < k && (shifting || ti_[s] < 0 || cv > tv[s])) {
+                        const float tf = tv[s];
+                        const int tii = ti_[s];
+                        tv[s] = cv;
+                        ti_[s] = ci;
+                        cv = tf;
+                        ci = tii;
+                        shifting = true;
+                    }
+                }
+            }
+        }
+    }
+    if (valid) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < k) sum += expf(tv[s] - tv[0]);
+        const float inv = 1.0f / sum;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            if (s < k) {
+                a.topk_idx[(int64_t)token * k + s] = ti_[s];
+                a.topk_w[(int64_t)token * k + s] = expf(tv[s] - tv[0]) * inv;
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------- kernel --
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+    using C = GemmCfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* tfull = bars + 2 * S;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_holder + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull + i, 1);
+            mbar_init(tempty + i, 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    int nblocks;
+    if (args.block_metadata) {
+        nblocks = *args.num_blocks;  // produced by an earlier kernel on this stream
+        nblocks = max(0, min(nblocks, args.nb_cap));
+    } else {
+        nblocks = (args.dense_rows + BM - 1) / BM;
+    }
+    const int total = nblocks * args.n_tiles;
+    bool timed_out = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_par = 0;  // stages armed and not yet seen consumed
+            for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+                const TileInfo ti = decode_tile(args, t);
+                const int brow = ti.e * args.b_rows_per_expert + ti.nb * BN;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
+                        timed_out = true;
+                        break;
+                    }
+                    armed &= ~(1u << s);
+                    mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+                    tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, ti.m0, full + s);
+                    tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * BK, brow, full + s);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (timed_out || *abort_flag) {
+                *abort_flag = 1;
+                // let the copies already issued land before the CTA exits
+                for (int i = 0; i < S; ++i)
+                    if (armed & (1u << i)) {
+                        volatile uint32_t never = 0;
+                        (void)mbar_wait(full + i, (armed_par >> i) & 1u, &never);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool issued = false;
+            for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+                if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(full + s, ph, abort_flag)) {
+                        timed_out = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * C::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        mma_bf16(d_tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
+                                 idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    mma_commit(empty + s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (timed_out) break;
+                mma_commit(tfull + acc);
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            if ((timed_out || *abort_flag) && issued) {
+                *abort_flag = 1;
+                // wait for the MMAs in flight before tensor memory is freed
+                mma_commit(drain);
+                volatile uint32_t never = 0;
+                (void)mbar_wait(drain, 0, &never);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(args, t);
+            // tcgen05.ld is warp-collective: the whole warp proceeds or stops
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
+            if (!ok) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            if constexpr (EPI == kEpiSwiGLU) {
+                epi_swiglu(args, ti, taddr, row);
+            } else if constexpr (EPI == kEpiGate) {
+                epi_gate<BN>(args, ti, taddr, row);
+            } else {
+                epi_router<BN>(args, ti, taddr, row);
+            }
+            tc_fence_before();
+            mbar_arrive(tempty + acc);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+        if (timed_out) *abort_flag = 1;
+    }
+
+    if (timed_out && args.status) atomicOr(args.status, kDevErrTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host --
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled encode_fn() {
+    static PFN_encodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_encodeTiled>(p);
+    }
+    return fn;
+}
+
+// K-major bf16 matrix [rows, K] as a 2D tensor map with a {64, box_rows}
+// box and the 128-byte swizzle; out-of-range rows read as zero.
+static bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+    PFN_encodeTiled enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
+                            int max_tiles, cudaStream_t stream) {
+    using C = GemmCfg<BN>;
+    static bool attr_done[64] = {};  // per device (small device counts)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm<BN, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    int grid = num_sms();
+    if (max_tiles < grid) grid = max_tiles;
+    if (grid <= 0) return cudaSuccess;
+    k_grouped_gemm<BN, EPI><<<grid, kThreads, C::SMEM, stream>>>(tA, tB, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,
+                                int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
+                                cudaStream_t stream) {
+    CUtensorMap tA, tB;
+    if (!make_tmap(&tA, A, rowsA, K, BM) || !make_tmap(&tB, B, rowsB, K, bn))
+        return cudaErrorInvalidValue;
+    if (epi == kEpiSwiGLU) {
+        if (bn == 256) return launch_t<256, kEpiSwiGLU>(tA, tB, args, max_tiles, stream);
+    } else if (epi == kEpiGate) {
+        if (bn == 256) return launch_t<256, kEpiGate>(tA, tB, args, max_tiles, stream);
+        if (bn == 128) return launch_t<128, kEpiGate>(tA, tB, args, max_tiles, stream);
+    } else if (epi == kEpiRouter) {
+        switch (bn) {
+            case 16: return launch_t<16, kEpiRouter>(tA, tB, args, max_tiles, stream);
+            case 32: return launch_t<32, kEpiRouter>(tA, tB, args, max_tiles, stream);
+            case 64: return launch_t<64, kEpiRouter>(tA, tB, args, max_tiles, stream);
+            case 128: return launch_t<128, kEpiRouter>(tA, tB, args, max_tiles, stream);
+            case 256: return launch_t<256, kEpiRouter>(tA, tB, args, max_tiles, stream);
+            default: break;
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the translation units of the library
+// (launchers and the GEMM problem description).  Not part of the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Device-side description of one grouped-GEMM launch.  The tile list is
+// either the block table written by the offsets stage (block_metadata +
+// num_blocks, both in device memory) or, when block_metadata is null, a
+// dense list of ceil(dense_rows / 128) blocks of expert 0.
+struct GemmArgs {
+    const int32_t* block_metadata;  // [nb_cap, 3] or null
+    const int32_t* num_blocks;      // [1] or null
+    int32_t nb_cap;                 // capacity of the block table
+    int32_t dense_rows;             // rows when block_metadata is null
+    int32_t n_tiles;                // N / BN
+    int32_t k_blocks;               // K / 64
+    int32_t b_rows_per_expert;      // rows of the packed B operand per expert
+    void* out;                      // bf16 output
+    int64_t ldo;                    // output row stride (elements)
+    const float* row_gate;          // per padded row (gate epilogue), may be null
+    uint32_t* status;               // device error word, may be null
+    // router epilogue
+    const float* bias;
+    int32_t E, k, n_groups, topk_groups;
+    int32_t* topk_idx;
+    float* topk_w;
+};
+
+enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2 };
+
+// Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
+// [rowsB, K] bf16 (K-major), tile N = bn.  Returns a cudaError_t.
+cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,
+                                int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
+                                cudaStream_t stream);
+
+cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t A, int E, int P,
+                           int64_t R_max, int32_t* counts, int32_t* padded_offsets,
+                           int32_t* block_metadata, int32_t* num_blocks, int32_t* perm_row,
+                           int32_t* row_src, float* row_gate, uint32_t* status,
+                           int32_t* chunk_scratch, cudaStream_t stream);
+int64_t offsets_num_chunks(int64_t A);
+
+cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,
+                           int k, cudaStream_t stream);
+cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,
+                           void* out, int T, int d, int k, cudaStream_t stream);
+
+// out[c, r] = in[r, c] with the output row of column c remapped by `mode`:
+// 0: row c; 1: gate rows of W13; 2: up rows of W13.  Batched over `batch`.
+cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols, int64_t in_bstride,
+                                  int64_t out_bstride, int out_ld, int mode, int batch,
+                                  cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace moe

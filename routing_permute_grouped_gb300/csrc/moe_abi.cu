@@ -1,0 +1,436 @@
+// moe_abi.cu -- the extern "C" entry points declared in include/moe.h:
+// argument validation, the workspace layout, and the launch sequence of the
+// layer on the caller's stream.  No entry point allocates memory or waits for
+// the device, except moe_get_device_status().
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+static thread_local std::string g_last_error;
+
+static moe_status_t fail(moe_status_t s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+static moe_status_t cuda_fail(cudaError_t e, const char* where) {
+    return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+int num_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+static inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Sizes {
+    int64_t A, R, NB, chunks;
+};
+
+static Sizes sizes_of(const moe_config_t& c) {
+    Sizes s;
+    s.A = static_cast<int64_t>(c.T) * c.k;
+    s.R = s.A + static_cast<int64_t>(c.E) * (c.pad_multiple - 1);
+    s.NB = s.A / c.pad_multiple + c.E;
+    s.chunks = offsets_num_chunks(s.A);
+    return s;
+}
+
+// Shape rules shared by every entry point.  `routed` adds the rule k <= E
+// and the group-limit rules, which only the router needs.
+static moe_status_t check_cfg(const moe_config_t* c, bool routed) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+    if (c->T < 0 || c->d <= 0 || c->d_e <= 0 || c->E <= 0 || c->k <= 0)
+        return fail(MOE_ERR_INVALID_ARG, "T must be >= 0 and d, d_e, E, k > 0");
+    if (c->d % 128) return fail(MOE_ERR_UNSUPPORTED, "d = %d is not a multiple of 128", c->d);
+    if (c->d_e % 128) return fail(MOE_ERR_UNSUPPORTED, "d_e = %d is not a multiple of 128", c->d_e);
+    if (c->d_shared < 0 || c->d_shared % 128)
+        return fail(MOE_ERR_UNSUPPORTED, "d_shared = %d must be 0 or a multiple of 128", c->d_shared);
+    if (c->E > 256) return fail(MOE_ERR_UNSUPPORTED, "E = %d > 256", c->E);
+    if (c->k > 8) return fail(MOE_ERR_UNSUPPORTED, "k = %d > 8", c->k);
+    if (c->pad_multiple != 64 && c->pad_multiple != 128)
+        return fail(MOE_ERR_UNSUPPORTED, "pad_multiple = %d must be 64 or 128", c->pad_multiple);
+    const int64_t A = static_cast<int64_t>(c->T) * c->k;
+    if (A + static_cast<int64_t>(c->E) * c->pad_multiple > (1ll << 30))
+        return fail(MOE_ERR_UNSUPPORTED, "T*k too large for 32-bit row indices");
+    if (routed) {
+        if (c->k > c->E) return fail(MOE_ERR_INVALID_ARG, "k = %d > E = %d", c->k, c->E);
+        if (c->n_groups < 0) return fail(MOE_ERR_INVALID_ARG, "n_groups < 0");
+        if (c->n_groups > 0) {
+            if (c->n_groups > 32 || c->E % c->n_groups)
+                return fail(MOE_ERR_INVALID_ARG, "n_groups = %d must divide E and be <= 32",
+                            c->n_groups);
+            if (c->topk_groups <= 0 || c->topk_groups > c->n_groups)
+                return fail(MOE_ERR_INVALID_ARG, "topk_groups = %d outside [1, n_groups]",
+                            c->topk_groups);
+            if (c->topk_groups * (c->E / c->n_groups) < c->k)
+                return fail(MOE_ERR_INVALID_ARG, "topk_groups * (E / n_groups) < k");
+        }
+    }
+    return MOE_OK;
+}
+
+static moe_workspace_layout_t layout_of(const moe_config_t& c) {
+    const Sizes s = sizes_of(c);
+    moe_workspace_layout_t L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    L.status = take(256 + static_cast<size_t>(s.chunks) * c.E * 4);
+    L.topk_idx = take(s.A * 4);
+    L.topk_w = take(s.A * 4);
+    L.counts = take(static_cast<size_t>(c.E) * 4);
+    L.padded_offsets = take(static_cast<size_t>(c.E + 1) * 4);
+    L.block_metadata = take(static_cast<size_t>(s.NB) * 12);
+    L.num_blocks = take(4);
+    L.perm_row = take(s.A * 4);
+    L.row_src = take(s.R * 4);
+    L.row_gate = take(s.R * 4);
+    L.x_perm = take(static_cast<size_t>(s.R) * c.d * 2);
+    L.h = take(static_cast<size_t>(s.R) * c.d_e * 2);
+    L.y = take(static_cast<size_t>(s.R) * c.d * 2);
+    L.hs = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d_shared : 0) * 2);
+    L.ys = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
+    L.total = off;
+    return L;
+}
+
+static size_t offsets_ws_bytes(const moe_config_t& c) {
+    return 256 + static_cast<size_t>(sizes_of(c).chunks) * c.E * 4;
+}
+
+static int router_bn(int E) {
+    if (E <= 16) return 16;
+    if (E <= 32) return 32;
+    if (E <= 64) return 64;
+    if (E <= 128) return 128;
+    return 256;
+}
+
+// ------------------------------------------------------------- stages --
+
+static moe_status_t do_route(const moe_config_t& c, const void* x, const void* Wg_t,
+                             const float* bias, int32_t* topk_idx, float* topk_w,
+                             cudaStream_t st) {
+    GemmArgs a{};
+    a.dense_rows = c.T;
+    a.n_tiles = 1;
+    a.k_blocks = c.d / 64;
+    a.b_rows_per_expert = 0;
+    a.bias = bias;
+    a.E = c.E;
+    a.k = c.k;
+    a.n_groups = c.n_groups;
+    a.topk_groups = c.topk_groups;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    const int tiles = (c.T + 127) / 128;
+    cudaError_t e = launch_grouped_gemm(kEpiRouter, router_bn(c.E), x, c.T, Wg_t, c.E, c.d, a,
+                                        tiles, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router GEMM");
+}
+
+static moe_status_t do_offsets(const moe_config_t& c, const int32_t* topk_idx, const float* topk_w,
+                               int32_t* counts, int32_t* po, int32_t* meta, int32_t* nb,
+                               int32_t* perm_row, int32_t* row_src, float* row_gate, void* ws,
+                               cudaStream_t st) {
+    const Sizes s = sizes_of(c);
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    cudaError_t e = launch_offsets(topk_idx, topk_w, s.A, c.E, c.pad_multiple, s.R, counts, po,
+                                   meta, nb, perm_row, row_src, row_gate,
+                                   reinterpret_cast<uint32_t*>(w8),
+                                   reinterpret_cast<int32_t*>(w8 + 256), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "offsets kernels");
+}
+
+static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const void* W13,
+                               const void* W2_t, const int32_t* meta, const int32_t* nb,
+                               const float* row_gate, void* h, void* y, uint32_t* status,
+                               cudaStream_t st) {
+    const Sizes s = sizes_of(c);
+    GemmArgs a{};
+    a.block_metadata = meta;
+    a.num_blocks = nb;
+    a.nb_cap = static_cast<int32_t>(s.NB);
+    a.status = status;
+    // GEMM1: N = 2*d_e (gate/up interleaved), K = d
+    a.n_tiles = (2 * c.d_e) / 256;
+    a.k_blocks = c.d / 64;
+    a.b_rows_per_expert = 2 * c.d_e;
+    a.out = h;
+    a.ldo = c.d_e;
+    cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x_perm, s.R, W13,
+                                        static_cast<int64_t>(c.E) * 2 * c.d_e, c.d, a,
+                                        static_cast<int>(s.NB * a.n_tiles), st);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 (gate/up + SwiGLU)");
+    // GEMM2: N = d, K = d_e
+    const int bn2 = (c.d % 256 == 0) ? 256 : 128;
+    a.n_tiles = c.d / bn2;
+    a.k_blocks = c.d_e / 64;
+    a.b_rows_per_expert = c.d;
+    a.out = y;
+    a.ldo = c.d;
+    a.row_gate = row_gate;
+    e = launch_grouped_gemm(kEpiGate, bn2, h, s.R, W2_t, static_cast<int64_t>(c.E) * c.d, c.d_e, a,
+                            static_cast<int>(s.NB * a.n_tiles), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2 (down + gate)");
+}
+
+static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
+                              const void* Ws2_t, void* hs, void* ys, uint32_t* status,
+                              cudaStream_t st) {
+    GemmArgs a{};
+    a.dense_rows = c.T;
+    a.status = status;
+    a.n_tiles = (2 * c.d_shared) / 256;
+    a.k_blocks = c.d / 64;
+    a.b_rows_per_expert = 0;
+    a.out = hs;
+    a.ldo = c.d_shared;
+    const int mblocks = (c.T + 127) / 128;
+    cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
+                                        mblocks * a.n_tiles, st);
+    if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
+    const int bn2 = (c.d % 256 == 0) ? 256 : 128;
+    a.n_tiles = c.d / bn2;
+    a.k_blocks = c.d_shared / 64;
+    a.out = ys;
+    a.ldo = c.d;
+    e = launch_grouped_gemm(kEpiGate, bn2, hs, c.T, Ws2_t, c.d, c.d_shared, a,
+                            mblocks * a.n_tiles, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "shared GEMM2");
+}
+
+static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                          const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
+                          size_t ws_bytes, cudaStream_t st) {
+    const bool routed = pre_idx == nullptr;
+    moe_status_t r = check_cfg(cfg, routed);
+    if (r != MOE_OK) return r;
+    const moe_config_t& c = *cfg;
+    if (!w || !x || !out) return fail(MOE_ERR_INVALID_ARG, "null weights, x or out");
+    if (!w->W13 || !w->W2) return fail(MOE_ERR_INVALID_ARG, "null routed expert weights");
+    if (routed && !w->Wg_t) return fail(MOE_ERR_INVALID_ARG, "null router weight");
+    if (!routed && !pre_w) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
+    if (c.d_shared && (!w->Ws13 || !w->Ws2))
+        return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared expert weights");
+    const moe_workspace_layout_t L = layout_of(c);
+    if (!ws || ws_bytes < L.total)
+        return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
+    if (c.T == 0) return MOE_OK;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    auto at = [&](size_t o) { return static_cast<void*>(b + o); };
+    uint32_t* status = static_cast<uint32_t*>(at(L.status));
+    int32_t* topk_idx = static_cast<int32_t*>(at(L.topk_idx));
+    float* topk_w = static_cast<float*>(at(L.topk_w));
+    if (routed) {
+        r = do_route(c, x, w->Wg_t, w->bias, topk_idx, topk_w, st);
+        if (r != MOE_OK) return r;
+    } else {
+        topk_idx = const_cast<int32_t*>(pre_idx);
+        topk_w = const_cast<float*>(pre_w);
+    }
+    int32_t* meta = static_cast<int32_t*>(at(L.block_metadata));
+    int32_t* nb = static_cast<int32_t*>(at(L.num_blocks));
+    int32_t* perm_row = static_cast<int32_t*>(at(L.perm_row));
+    float* row_gate = static_cast<float*>(at(L.row_gate));
+    r = do_offsets(c, topk_idx, topk_w, static_cast<int32_t*>(at(L.counts)),
+                   static_cast<int32_t*>(at(L.padded_offsets)), meta, nb, perm_row,
+                   static_cast<int32_t*>(at(L.row_src)), row_gate, at(L.status), st);
+    if (r != MOE_OK) return r;
+    cudaError_t e = launch_permute(x, perm_row, at(L.x_perm), c.T, c.d, c.k, st);
+    if (e != cudaSuccess) return cuda_fail(e, "permute");
+    r = do_experts(c, at(L.x_perm), w->W13, w->W2, meta, nb, row_gate, at(L.h), at(L.y), status, st);
+    if (r != MOE_OK) return r;
+    const void* shared = nullptr;
+    if (c.d_shared) {
+        r = do_shared(c, x, w->Ws13, w->Ws2, at(L.hs), at(L.ys), status, st);
+        if (r != MOE_OK) return r;
+        shared = at(L.ys);
+    }
+    e = launch_combine(at(L.y), perm_row, shared, out, c.T, c.d, c.k, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_check_config(const moe_config_t* cfg) { return check_cfg(cfg, false); }
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+    if (check_cfg(cfg, false) != MOE_OK) return 0;
+    return layout_of(*cfg).total;
+}
+
+moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!layout) return fail(MOE_ERR_INVALID_ARG, "layout is NULL");
+    *layout = layout_of(*cfg);
+    return MOE_OK;
+}
+
+size_t moe_offsets_workspace_size(const moe_config_t* cfg) {
+    if (check_cfg(cfg, false) != MOE_OK) return 0;
+    return offsets_ws_bytes(*cfg);
+}
+
+moe_status_t moe_pack_router(int32_t d, int32_t E, const void* Wg, void* Wg_t, void* stream) {
+    if (d <= 0 || E <= 0 || !Wg || !Wg_t) return fail(MOE_ERR_INVALID_ARG, "bad router pack args");
+    cudaError_t e = launch_pack_transpose(Wg, Wg_t, d, E, 0, 0, d, 0, 1,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack router");
+}
+
+moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void* W1, const void* W3,
+                              const void* W2, void* W13, void* W2_t, void* stream) {
+    if (E <= 0 || d <= 0 || de <= 0 || !W1 || !W3 || !W2 || !W13 || !W2_t)
+        return fail(MOE_ERR_INVALID_ARG, "bad expert pack args");
+    if (d % 128 || de % 128) return fail(MOE_ERR_UNSUPPORTED, "d and de must be multiples of 128");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t dd = d, dde = de;
+    cudaError_t e = launch_pack_transpose(W1, W13, d, de, dd * dde, 2 * dde * dd, d, 1, E, st);
+    if (e == cudaSuccess) e = launch_pack_transpose(W3, W13, d, de, dd * dde, 2 * dde * dd, d, 2, E, st);
+    if (e == cudaSuccess) e = launch_pack_transpose(W2, W2_t, de, d, dde * dd, dd * dde, de, 0, E, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack experts");
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg_t, const float* bias,
+                       int32_t* topk_idx, float* topk_w, void* stream) {
+    moe_status_t r = check_cfg(cfg, true);
+    if (r != MOE_OK) return r;
+    if (!x || !Wg_t || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_route(*cfg, x, Wg_t, bias, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_build_offsets(const moe_config_t* cfg, const int32_t* topk_idx,
+                               const float* topk_w, int32_t* counts, int32_t* padded_offsets,
+                               int32_t* block_metadata, int32_t* num_blocks, int32_t* perm_row,
+                               int32_t* row_src, float* row_gate, void* ws, size_t ws_bytes,
+                               void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!topk_idx || !counts || !padded_offsets || !block_metadata || !num_blocks || !perm_row ||
+        !row_src || !row_gate)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    const size_t need = offsets_ws_bytes(*cfg);
+    if (!ws || ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "offsets scratch of %zu bytes, %zu needed", ws_bytes, need);
+    if (cfg->T == 0) return MOE_OK;
+    return do_offsets(*cfg, topk_idx, topk_w, counts, padded_offsets, block_metadata, num_blocks,
+                      perm_row, row_src, row_gate, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* perm_row,
+                         void* x_perm, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x || !perm_row || !x_perm) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    cudaError_t e = launch_permute(x, perm_row, x_perm, cfg->T, cfg->d, cfg->k,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute");
+}
+
+moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm, const void* W13,
+                                     const void* W2_t, const int32_t* block_metadata,
+                                     const int32_t* num_blocks, const float* row_gate, void* h,
+                                     void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x_perm || !W13 || !W2_t || !block_metadata || !num_blocks || !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate, h, y, status,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const void* Ws13,
+                               const void* Ws2_t, void* hs, void* ys, uint32_t* status,
+                               void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (!x || !Ws13 || !Ws2_t || !hs || !ys) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_shared(*cfg, x, Ws13, Ws2_t, hs, ys, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y, const int32_t* perm_row,
+                         const void* shared_out, void* out, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!y || !perm_row || !out) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    cudaError_t e = launch_combine(y, perm_row, shared_out, out, cfg->T, cfg->d, cfg->k,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
+}
+
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                           void* out, void* ws, size_t ws_bytes, void* stream) {
+    return layer(cfg, w, x, nullptr, nullptr, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer_fwd_prerouted(const moe_config_t* cfg, const moe_weights_t* w,
+                                     const void* x, const int32_t* topk_idx, const float* topk_w,
+                                     void* out, void* ws, size_t ws_bytes, void* stream) {
+    if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "null pre-routed indices");
+    return layer(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_get_device_status(void* ws, uint32_t* bits, void* stream) {
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "ws is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && v) e = cudaMemsetAsync(ws, 0, sizeof v, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (bits) *bits = v;
+    return v ? fail(MOE_ERR_DEVICE_CHECK, "device status bits 0x%x", v) : MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// permute_combine.cu -- the two zero-FLOP stages of the layer, both bound by
+// HBM bandwidth ("MoE & MLA operators", sec. 2.3 and 2.5).
+//
+// permute: token-major scatter.  A warp owns one token: it reads the token's
+//          row once with 16-byte loads and writes it to the k padded rows
+//          perm_row[t*k + j] with 16-byte stores.  Bytes per token:
+//          d*2 read + k*d*2 written.
+// combine: a warp owns one token: it reads the k routed rows y[perm_row[...]]
+//          (and the shared-expert row) 16 bytes at a time, sums in fp32 in
+//          the fixed order j = 0..k-1 then shared, and writes one bf16 row
+//          (sec. 6.4: fixed summation order, wide accumulation, no atomics).
+//          Bytes per token: (k + 1 [+1]) * d * 2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kPCWarps = 8;  // warps per CTA
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_permute(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
+              uint4* __restrict__ x_perm, int T, int nvec, int k) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kPCWarps + warp;
+    if (t >= T) return;
+    int rows[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(perm_row + (int64_t)t * k + j) : -1;
+    const uint4* src = x + (int64_t)t * nvec;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 buf[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + u * 32;
+            if (v < nvec) buf[u] = __ldg(src + v);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (rows[j] < 0) continue;
+            uint4* dst = x_perm + (int64_t)rows[j] * nvec;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32;
+                if (v < nvec) dst[v] = buf[u];
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ perm_row,
+              const uint4* __restrict__ shared_out, uint4* __restrict__ out, int T, int nvec, int k) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kPCWarps + warp;
+    if (t >= T) return;
+    int rows[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(perm_row + (int64_t)t * k + j) : -1;
+    for (int v = lane; v < nvec; v += 32) {
+        uint4 in[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (rows[j] >= 0) in[j] = __ldg(y + (int64_t)rows[j] * nvec + v);
+        uint4 sh = make_uint4(0, 0, 0, 0);
+        if (shared_out) sh = __ldg(shared_out + (int64_t)t * nvec + v);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (rows[j] >= 0) add_bf16x8(acc, in[j]);
+        if (shared_out) add_bf16x8(acc, sh);
+        uint4 o;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+        o.x = *reinterpret_cast<uint32_t*>(&p0);
+        o.y = *reinterpret_cast<uint32_t*>(&p1);
+        o.z = *reinterpret_cast<uint32_t*>(&p2);
+        o.w = *reinterpret_cast<uint32_t*>(&p3);
+        out[(int64_t)t * nvec + v] = o;
+    }
+}
+
+cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,
+                           int k, cudaStream_t stream) {
+    const int nvec = d / 8;
+    const int grid = (T + kPCWarps - 1) / kPCWarps;
+    k_permute<<<grid, kPCWarps * 32, 0, stream>>>(static_cast<const uint4*>(x), perm_row,
+                                                  static_cast<uint4*>(x_perm), T, nvec, k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,
+                           void* out, int T, int d, int k, cudaStream_t stream) {
+    const int nvec = d / 8;
+    const int grid = (T + kPCWarps - 1) / kPCWarps;
+    k_combine<<<grid, kPCWarps * 32, 0, stream>>>(static_cast<const uint4*>(y), perm_row,
+                                                  static_cast<const uint4*>(shared_out),
+                                                  static_cast<uint4*>(out), T, nvec, k);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

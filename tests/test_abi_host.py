@@ -1,0 +1,111 @@
+"""CPU tests of the C ABI: the library builds, loads and exports every entry
+point that include/moe.h declares, and the host-side argument checks return
+their errors before anything is enqueued (no GPU is touched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import routing_permute_grouped_gb300 as moe
+from routing_permute_grouped_gb300 import build as moe_build
+from routing_permute_grouped_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "moe_layer_fwd" in names and "moe_build_offsets" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+
+
+def test_status_strings(lib):
+    assert moe.moe_status_string(0) == "ok"
+    assert "workspace" in moe.moe_status_string(3)
+
+
+def _cfg(**kw):
+    base = dict(T=256, d=512, d_e=256, E=8, k=2)
+    base.update(kw)
+    return moe.config_of(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=500), 2), (dict(d_e=200), 2), (dict(E=300), 2), (dict(k=9, E=16), 2),
+    (dict(pad_multiple=32), 2), (dict(d_shared=100), 2), (dict(T=-1), 1), (dict(E=0), 1),
+])
+def test_check_config_rejects(lib, kw, status):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_check_config(_cfg(**kw))
+    assert ei.value.status == status
+
+
+@pytest.mark.parametrize("kw", [dict(k=5, E=4), dict(n_groups=3, E=8), dict(n_groups=4, topk_groups=1, k=3),
+                                dict(n_groups=4, topk_groups=5)])
+def test_route_rejects_before_launch(lib, kw):
+    cfg = _cfg(**kw)
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the checks fail first
+    st = lib.moe_route(ctypes.byref(cfg), fake, fake, None, fake, fake, None)
+    assert st == 1
+
+
+def test_workspace_sizes_follow_the_capacities(lib):
+    for name in ("tiny", "default", "prerouted", "decode", "imbalance_x2_p64"):
+        s = synth.WORKLOADS[name]
+        cfg = moe.config_of(s)
+        L = moe.moe_workspace_layout(cfg)
+        assert L["total"] == moe.moe_workspace_size(cfg)
+        R = s.A + s.E * (s.pad - 1)
+        assert L["h"] - L["x_perm"] >= R * s.d * 2
+        assert L["y"] - L["h"] >= R * s.d_e * 2
+        offs = [L[n] for n in ("status", "topk_idx", "topk_w", "counts", "padded_offsets",
+                               "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate",
+                               "x_perm", "h", "y", "hs", "ys")]
+        assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
+
+
+def test_layer_rejects_small_workspace_and_nulls(lib):
+    cfg = _cfg()
+    fake = ctypes.c_void_p(0x1000)
+    w = moe.MoeWeights(Wg_t=0x1000, bias=None, W13=0x1000, W2=0x1000, Ws13=None, Ws2=None)
+    need = moe.moe_workspace_size(cfg)
+    assert lib.moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(w), fake, fake, fake, need - 1, None) == 3
+    assert lib.moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(w), None, fake, fake, need, None) == 1
+    w2 = moe.MoeWeights(Wg_t=None, bias=None, W13=0x1000, W2=0x1000, Ws13=None, Ws2=None)
+    assert lib.moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(w2), fake, fake, fake, need, None) == 1
+    cfg_s = _cfg(d_shared=256)
+    need_s = moe.moe_workspace_size(cfg_s)
+    assert lib.moe_layer_fwd(ctypes.byref(cfg_s), ctypes.byref(w), fake, fake, fake, need_s, None) == 1
+    assert "shared" in lib.moe_last_error().decode()
+
+
+def test_offsets_scratch_checked(lib):
+    cfg = _cfg()
+    fake = ctypes.c_void_p(0x1000)
+    need = moe.moe_offsets_workspace_size(cfg)
+    assert need >= 256 + cfg.E * 4
+    st = lib.moe_build_offsets(ctypes.byref(cfg), fake, None, fake, fake, fake, fake, fake, fake,
+                               fake, fake, need - 4, None)
+    assert st == 3
+
+
+def test_empty_batch_is_a_noop(lib):
+    cfg = _cfg(T=0)
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.moe_permute(ctypes.byref(cfg), fake, fake, fake, None) == 0
+    assert lib.moe_combine(ctypes.byref(cfg), fake, fake, None, fake, None) == 0
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, fake, fake, None) == 0

@@ -1,0 +1,309 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Routing indices, counts, offsets, the block table and the permutation must
+be bit-exact (the inputs are redrawn until every routing decision has a
+fp64 margin >= 1e-3, so fp32 logits decide the same way); permuted rows are
+bit-exact copies; floating outputs must have a relative Frobenius error
+<= 5e-3 and a max error <= 3e-2 * max|ref|.  Shapes span several tiles in
+M, N and K, ragged tails, empty experts, padding 64 and 128, group-limited
+routing, a router width that is not a power of two, and a model width that
+is not a multiple of 256.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import routing_permute_grouped_gb300 as moe
+from routing_permute_grouped_gb300 import build as moe_build
+from routing_permute_grouped_gb300 import synth
+from routing_permute_grouped_gb300.synth import MoeShape
+from tests.helpers import bits, enforce_margin, oracle_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 5e-3
+MAX_REL = 3e-2
+
+SHAPES = {
+    "tiny": synth.WORKLOADS["tiny"],
+    "small_default": MoeShape("small_default", T=777, d=1024, d_e=384, E=8, k=4, bias_std=0.5,
+                              d_shared=256, seed=77),
+    "small_decode": MoeShape("small_decode", T=37, d=512, d_e=256, E=64, k=8, n_groups=8,
+                             topk_groups=4, d_shared=128, seed=78),
+    "small_prerouted": MoeShape("small_prerouted", T=300, d=512, d_e=256, E=4, k=8,
+                                prerouted=(900, 321, 1000, 179), seed=79),
+    "small_imbalance_p64": MoeShape("small_imbalance_p64", T=2000, d=512, d_e=256, E=64, k=6,
+                                    pad=64, zipf_target=2.0, seed=80),
+    "small_e100_d384": MoeShape("small_e100_d384", T=300, d=384, d_e=128, E=100, k=3,
+                                bias_std=0.3, seed=81),
+}
+ZIPF_S = {"small_imbalance_p64": 1.0}
+
+_cache = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU parity tests need a CUDA device")
+    moe_build.build()
+    moe.load()
+
+
+def prepared(name):
+    """(shape, CPU inputs after the margin filter, oracle result)."""
+    if name not in _cache:
+        shape = SHAPES[name]
+        inp = synth.make_inputs(shape, zipf_s=ZIPF_S.get(name))
+        enforce_margin(inp, shape)
+        ref = oracle.layer_forward(oracle_inputs(inp), shape)
+        _cache[name] = (shape, inp, ref)
+    return _cache[name]
+
+
+def cuda(t):
+    return None if t is None else t.cuda().contiguous()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, what
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / (nref if nref > 0 else 1.0)
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    bound = MAX_REL * (np.abs(ref).max() if ref.size else 0.0)
+    assert rel <= REL_FRO, f"{what}: relative Frobenius error {rel:.3e}"
+    assert mx <= bound + 1e-30, f"{what}: max error {mx:.3e} > {bound:.3e}"
+
+
+def make_layer(shape, inp):
+    cfg = moe.config_of(shape)
+    layer = moe.MoeLayer(cfg, cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]),
+                         Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")),
+                         Ws1=cuda(inp.get("Ws1")), Ws3=cuda(inp.get("Ws3")),
+                         Ws2=cuda(inp.get("Ws2")))
+    return cfg, layer
+
+
+# ---------------------------------------------------------------- layer ----
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_layer_matches_oracle(name):
+    shape, inp, ref = prepared(name)
+    cfg, layer = make_layer(shape, inp)
+    x = cuda(inp["x"])
+    if shape.prerouted:
+        out = layer(x, topk_idx=cuda(inp["topk_idx"]), topk_w=cuda(inp["topk_w"]))
+    else:
+        out = layer(x)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    T, k, E, d, de = shape.T, shape.k, shape.E, shape.d, shape.d_e
+    A, R, NB = shape.A, shape.rows_capacity, shape.blocks_capacity
+    i32 = torch.int32
+    if not shape.prerouted:
+        gidx = layer.buffer("topk_idx", i32, (T, k)).cpu().numpy()
+        assert np.array_equal(gidx, ref["topk_idx"])
+        gw = layer.buffer("topk_w", torch.float32, (T, k)).cpu().double().numpy()
+        np.testing.assert_allclose(gw, ref["topk_w"], rtol=0, atol=2e-5)
+    assert np.array_equal(layer.buffer("counts", i32, (E,)).cpu().numpy(), ref["counts"])
+    assert np.array_equal(layer.buffer("padded_offsets", i32, (E + 1,)).cpu().numpy(),
+                          ref["padded_offsets"])
+    nb = int(layer.buffer("num_blocks", i32, (1,)).item())
+    assert nb == ref["num_blocks"]
+    meta = layer.buffer("block_metadata", i32, (NB, 3)).cpu().numpy()[:nb]
+    assert np.array_equal(meta, ref["block_metadata"])
+    assert np.array_equal(layer.buffer("perm_row", i32, (A,)).cpu().numpy(), ref["perm_row"])
+    assert np.array_equal(layer.buffer("row_src", i32, (R,)).cpu().numpy(), ref["row_src"])
+    rg = layer.buffer("row_gate", torch.float32, (R,)).cpu().double().numpy()
+    np.testing.assert_allclose(rg, ref["row_gate"], rtol=0, atol=2e-5)
+    valid = ref["row_src"] >= 0
+    xp = bits(layer.buffer("x_perm", torch.bfloat16, (R, d)).cpu())
+    assert np.array_equal(xp[valid], ref["x_perm"][valid])
+    h = f64(layer.buffer("h", torch.bfloat16, (R, de)))
+    assert_close(h[valid], ref["h"][valid], "h")
+    y = f64(layer.buffer("y", torch.bfloat16, (R, d)))
+    assert_close(y[valid], ref["y"][valid], "y")
+    if shape.d_shared:
+        assert_close(f64(layer.buffer("ys", torch.bfloat16, (T, d))), ref["ys"], "shared ys")
+    assert_close(f64(out), ref["out"], "out")
+
+
+def test_layer_is_deterministic():
+    shape, inp, _ = prepared("small_default")
+    cfg, layer = make_layer(shape, inp)
+    x = cuda(inp["x"])
+    a = layer(x).clone()
+    b = layer(x).clone()
+    assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------- stages ----
+@pytest.mark.parametrize("name", ["tiny", "small_decode", "small_e100_d384", "small_imbalance_p64"])
+def test_route_stage(name):
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    Wg_t = torch.empty((shape.E, shape.d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_router(cuda(inp["Wg"]), Wg_t)
+    idx = torch.full((shape.T, shape.k), -7, dtype=torch.int32, device="cuda")
+    w = torch.zeros((shape.T, shape.k), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(w.cpu().double().numpy(), ref["topk_w"], rtol=0, atol=2e-5)
+
+
+def _offsets_case(idx, w, E, P):
+    T, k = idx.shape
+    cfg = moe.config_of(T=T, d=128, d_e=128, E=E, k=k, pad_multiple=P)
+    A = T * k
+    R = A + E * (P - 1)
+    NB = A // P + E
+    dev = "cuda"
+    out = dict(counts=torch.full((E,), -5, dtype=torch.int32, device=dev),
+               padded_offsets=torch.full((E + 1,), -5, dtype=torch.int32, device=dev),
+               block_metadata=torch.full((NB, 3), -5, dtype=torch.int32, device=dev),
+               num_blocks=torch.full((1,), -5, dtype=torch.int32, device=dev),
+               perm_row=torch.full((A,), -5, dtype=torch.int32, device=dev),
+               row_src=torch.full((R,), -5, dtype=torch.int32, device=dev),
+               row_gate=torch.full((R,), -5.0, dtype=torch.float32, device=dev))
+    ws = torch.zeros(moe.moe_offsets_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    moe.moe_build_offsets(cfg, cuda(torch.as_tensor(idx)), cuda(torch.as_tensor(w)),
+                          out["counts"], out["padded_offsets"], out["block_metadata"],
+                          out["num_blocks"], out["perm_row"], out["row_src"], out["row_gate"], ws)
+    status = moe.moe_get_device_status(ws)
+    return {kk: v.cpu().numpy() for kk, v in out.items()}, status
+
+
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("case", ["uniform", "skewed_empty", "one_expert", "worked_example", "exact_blocks"])
+def test_build_offsets_stage(P, case):
+    rng = np.random.default_rng(hash(case) % 1000 + P)
+    if case == "uniform":
+        E, T, k = 8, 4097, 4  # several chunks, ragged tail
+        idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    elif case == "skewed_empty":
+        E, T, k = 256, 1111, 8
+        p = rng.dirichlet(np.full(E, 0.05))
+        idx = rng.choice(E, size=(T, k), p=p).astype(np.int32)
+    elif case == "one_expert":
+        E, T, k = 5, 3000, 1
+        idx = np.full((T, k), 3, np.int32)
+    elif case == "worked_example":
+        # "Dropless and grouped GEMM", sec. 3 sizes, 8192 tokens x top-8
+        sizes = [21733, 15004, 17982, 10817]
+        lab = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(sizes)])
+        idx = lab[rng.permutation(lab.size)].reshape(8192, 8)
+        E = 4
+    else:
+        E, T, k = 4, 128, 4  # 128 rows per expert: one exact block each at P=128
+        idx = np.repeat(np.arange(4, dtype=np.int32)[None, :], T, 0)
+    w = rng.random(idx.shape).astype(np.float32)
+    got, status = _offsets_case(idx, w, E, P)
+    assert status == 0
+    ref = oracle.build_offsets(idx, w.astype(np.float64), E, P)
+    for key in ("counts", "padded_offsets", "perm_row", "row_src"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert int(got["num_blocks"][0]) == ref["num_blocks"]
+    assert np.array_equal(got["block_metadata"][:ref["num_blocks"]], ref["block_metadata"])
+    assert np.array_equal(got["row_gate"].astype(np.float64), ref["row_gate"])
+    if case == "worked_example" and P == 128:
+        assert got["padded_offsets"].tolist() == [0, 21760, 36864, 54912, 65792]
+        assert int(got["num_blocks"][0]) == 514
+
+
+def test_build_offsets_flags_bad_expert_ids():
+    idx = np.array([[0, 1], [9, 2], [3, -1], [1, 1]], np.int32)
+    w = np.ones(idx.shape, np.float32)
+    got, status = _offsets_case(idx, w, 4, 128)
+    assert status & moe.DEVERR_EXPERT_RANGE
+    assert got["perm_row"][2] == -1 and got["perm_row"][5] == -1
+    assert got["counts"].tolist() == [1, 3, 1, 1]
+    # the valid assignments keep the oracle's layout of the valid ids
+    ok = np.array([0, 1, 3, 4, 6, 7])
+    assert (got["row_src"][got["perm_row"][ok]] == ok).all()
+
+
+@pytest.mark.parametrize("name", ["small_default", "small_prerouted"])
+def test_permute_stage(name):
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    R = shape.rows_capacity
+    x_perm = torch.zeros((R, shape.d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, cuda(inp["x"]), cuda(torch.as_tensor(ref["perm_row"])), x_perm)
+    got = bits(x_perm.cpu())
+    valid = ref["row_src"] >= 0
+    assert np.array_equal(got[valid], ref["x_perm"][valid])
+    assert (got[~valid] == 0).all()  # pad rows untouched
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_default", "small_imbalance_p64", "small_e100_d384"])
+def test_grouped_gemm_stage(name):
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    E, d, de, R, NB = shape.E, shape.d, shape.d_e, shape.rows_capacity, shape.blocks_capacity
+    W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device="cuda")
+    W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), W13, W2_t)
+    meta = np.zeros((NB, 3), np.int32)
+    meta[:ref["num_blocks"]] = ref["block_metadata"]
+    gate32 = ref["row_gate"].astype(np.float32)
+    x_perm = torch.from_numpy(ref["x_perm"].view(np.int16)).view(torch.bfloat16).cuda()
+    h = torch.zeros((R, de), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, cuda(torch.from_numpy(meta)),
+                                cuda(torch.tensor([ref["num_blocks"]], dtype=torch.int32)),
+                                cuda(torch.from_numpy(gate32)), h, y, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    eh, ey = oracle.grouped_experts(ref["x_perm"], bits(inp["W1"]), bits(inp["W3"]),
+                                    bits(inp["W2"]), ref["block_metadata"],
+                                    gate32.astype(np.float64))
+    valid = ref["row_src"] >= 0
+    assert_close(f64(h)[valid], eh[valid], "h")
+    assert_close(f64(y)[valid], ey[valid], "y")
+    # pad rows are never written
+    assert (f64(y)[~valid] == 0).all() and (f64(h)[~valid] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["small_default", "small_decode"])
+def test_shared_expert_stage(name):
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    d, ds, T = shape.d, shape.d_shared, shape.T
+    Ws13 = torch.empty((1, 2 * ds, d), dtype=torch.bfloat16, device="cuda")
+    Ws2_t = torch.empty((1, d, ds), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(inp["Ws1"]).unsqueeze(0).contiguous(),
+                         cuda(inp["Ws3"]).unsqueeze(0).contiguous(),
+                         cuda(inp["Ws2"]).unsqueeze(0).contiguous(), Ws13, Ws2_t)
+    hs = torch.empty((T, ds), dtype=torch.bfloat16, device="cuda")
+    ys = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_shared_expert(cfg, cuda(inp["x"]), Ws13, Ws2_t, hs, ys)
+    assert_close(f64(hs), ref["hs"], "hs")
+    assert_close(f64(ys), ref["ys"], "ys")
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_combine_stage(shared):
+    shape, inp, ref = prepared("small_default")
+    cfg = moe.config_of(shape)
+    R, d, T = shape.rows_capacity, shape.d, shape.T
+    g = torch.Generator().manual_seed(5)
+    y = torch.randn((R, d), generator=g).to(torch.bfloat16)
+    ys = torch.randn((T, d), generator=g).to(torch.bfloat16) if shared else None
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(cfg, cuda(y), cuda(torch.as_tensor(ref["perm_row"])), cuda(ys), out)
+    expect = oracle.combine(oracle.bf16_to_f64(bits(y)), ref["perm_row"], shape.k,
+                            None if ys is None else oracle.bf16_to_f64(bits(ys)))
+    got = f64(out)
+    # fp32 sum of at most k+1 bf16 values, one rounding: within one bf16 ulp
+    ulp = np.ldexp(1.0, np.frexp(np.abs(expect))[1] - 8)
+    assert (np.abs(got - expect) <= ulp).all()
+    assert np.mean(got == oracle.round_bf16(expect)) > 0.999
