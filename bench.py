@@ -406,9 +406,12 @@ def run_ours(args, shape, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
-        # calibrate to ~15 s of oracle work
-        tf1, dt1, _ = oracle_sample_tflops(shape, host, 2)
-        n = max(2, min(shape.T, int(2 * 15.0 / max(dt1, 1e-3))))
+        # calibrate to ~15 s of oracle work: one token per thread first
+        import oracle
+
+        n0 = max(1, oracle.num_threads())
+        _, dt1, _ = oracle_sample_tflops(shape, host, n0)
+        n = max(n0, min(shape.T, n0 * int(round(15.0 / max(dt1, 1e-3)))))
         tf, dt, threads = oracle_sample_tflops(shape, host, n)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {n} tokens of the workload: router, routed "
