@@ -181,6 +181,32 @@ moe_status_t moe_build_offsets(const moe_config_t *cfg, const int32_t *topk_idx,
                                int32_t *row_src, float *row_gate, void *ws, size_t ws_bytes,
                                void *stream);
 
+/* Allocation-free variant of moe_build_offsets (the pages have no
+ * counterpart; this exists for callers of this library).  Some callers cannot
+ * allocate device memory where they run this stage: work recorded into a
+ * CUDA graph may not call allocation routines during stream capture, and some
+ * serving runtimes only hand out memory from a pool reserved at start-up.
+ * This call takes the same inputs and outputs as moe_build_offsets but no
+ * scratch: its per-chunk counts live in a 64 KiB array in the library's own
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *   status  uint32 [1] device word that collects MOE_DEVERR_EXPERT_RANGE, or
+ *           NULL to leave bad expert ids unreported
+ * Limits: ceil(T*k / 2048) * E * 4 <= 65536 bytes (T*k <= 131072 at E = 256);
+ * larger configs return MOE_ERR_WORKSPACE before anything is enqueued.
+ * The first call on a device looks up the array's device address (with that
+ * device current), so make that first call before any stream capture begins.
+ * All calls share the one array and it keeps the last call's contents (none
+ * of it needs to start at zero); calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race on it and must be
+ * ordered by the caller. */
+moe_status_t moe_build_offsets_noalloc(const moe_config_t *cfg, const int32_t *topk_idx,
+                                       const float *topk_w, int32_t *counts,
+                                       int32_t *padded_offsets, int32_t *block_metadata,
+                                       int32_t *num_blocks, int32_t *perm_row, int32_t *row_src,
+                                       float *row_gate, uint32_t *status, void *stream);
+
 /* a3. Permute ("MoE & MLA operators", sec. 2.3: a data-dependent gather of
  * token rows into expert order): x_perm[perm_row[t*k + j]] = x[t].  Each
  * token row is read once and written k times with 16-byte accesses; pad rows

@@ -25,7 +25,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "MoeConfig", "MoeWeights", "MoeLayer", "config_of", "load",
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
-    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_permute",
+    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string",
 ]
@@ -88,6 +88,7 @@ def load():
         "moe_pack_experts": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P]),
         "moe_route": (ctypes.c_int, [CP, P, P, P, P, P, P]),
         "moe_build_offsets": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_build_offsets_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
         "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P]),
         "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
@@ -186,6 +187,19 @@ def moe_build_offsets(cfg, topk_idx, topk_w, counts, padded_offsets, block_metad
         ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(padded_offsets),
         _ptr(block_metadata), _ptr(num_blocks), _ptr(perm_row), _ptr(row_src), _ptr(row_gate),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_build_offsets_noalloc(cfg, topk_idx, topk_w, counts, padded_offsets, block_metadata,
+                              num_blocks, perm_row, row_src, row_gate, status=None,
+                              stream=None) -> None:
+    """moe_build_offsets without a caller-provided scratch: for callers that
+    cannot allocate device memory here (stream capture, fixed memory pools).
+    The scratch is a fixed array inside the library; see include/moe.h for its
+    size limit and for why overlapping calls must be ordered."""
+    _check(load().moe_build_offsets_noalloc(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(padded_offsets),
+        _ptr(block_metadata), _ptr(num_blocks), _ptr(perm_row), _ptr(row_src), _ptr(row_gate),
+        _ptr(status), _stream(stream)))
 
 
 def moe_permute(cfg, x, perm_row, x_perm, stream=None) -> None:

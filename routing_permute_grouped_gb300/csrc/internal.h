@@ -58,4 +58,10 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
 
 int num_sms();
 
+constexpr int kMaxDevices = 64;
+
+// Records a printf-style message as this thread's last error (read by
+// moe_last_error) and returns `status` unchanged.
+int record_error(int status, const char* fmt, ...);
+
 }  // namespace moe

@@ -25,6 +25,16 @@ static moe_status_t fail(moe_status_t s, const char* fmt, ...) {
     return s;
 }
 
+int record_error(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
     return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }

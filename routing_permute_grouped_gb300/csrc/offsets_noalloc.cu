@@ -1,0 +1,84 @@
+// offsets_noalloc.cu -- an allocation-free variant of moe_build_offsets.
+//
+// moe_build_offsets needs a small device scratch (per-chunk expert counts)
+// that its caller allocates.  Some callers cannot allocate device memory at
+// the point where they run this stage: code that is being recorded into a
+// CUDA graph (allocation calls are not allowed during stream capture), and
+// runtimes that hand out memory only from a pool reserved at start-up and
+// forbid any allocation on the serving path.  This variant keeps its
+// scratch in a fixed-size array in the library's own device memory instead,
+// so the caller passes inputs and outputs only.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+// The per-chunk counts of the offsets kernels (int32 [chunks, E]).  Every
+// GPU that loads the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+static __device__ __align__(256) unsigned char g_offsets_scratch[kNoAllocScratchBytes];
+
+// Device address of g_offsets_scratch on the current device.  In host code
+// the symbol name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+static void* noalloc_scratch(int dev, cudaError_t* err) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    *err = cudaSuccess;
+    if (addr[dev]) return addr[dev];
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_offsets_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+    return p;
+}
+
+#define set_last_error(status, ...) static_cast<moe_status_t>(record_error(status, __VA_ARGS__))
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_build_offsets_noalloc(const moe_config_t* cfg, const int32_t* topk_idx,
+                                                  const float* topk_w, int32_t* counts,
+                                                  int32_t* padded_offsets, int32_t* block_metadata,
+                                                  int32_t* num_blocks, int32_t* perm_row,
+                                                  int32_t* row_src, float* row_gate,
+                                                  uint32_t* status, void* stream) {
+    moe_status_t r = moe_check_config(cfg);
+    if (r != MOE_OK) return r;
+    if (!topk_idx || !counts || !padded_offsets || !block_metadata || !num_blocks || !perm_row ||
+        !row_src || !row_gate)
+        return set_last_error(MOE_ERR_INVALID_ARG, "null pointer");
+    const int64_t A = static_cast<int64_t>(cfg->T) * cfg->k;
+    const size_t need = static_cast<size_t>(offsets_num_chunks(A)) * cfg->E * 4;
+    if (need > kNoAllocScratchBytes)
+        return set_last_error(MOE_ERR_WORKSPACE,
+                              "allocation-free offsets need %zu bytes of scratch; the static "
+                              "scratch holds %zu (T*k <= %lld at this E)",
+                              need, kNoAllocScratchBytes,
+                              static_cast<long long>(kNoAllocScratchBytes / 4 / cfg->E) * 2048);
+    if (cfg->T == 0) return MOE_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_last_error(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_last_error(MOE_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+    void* scratch = noalloc_scratch(dev, &e);
+    if (!scratch)
+        return set_last_error(MOE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    // Nothing in the scratch has to start at zero: the histogram pass writes
+    // every [chunk, expert] count before the scan and the scatter read them.
+    const int64_t R = A + static_cast<int64_t>(cfg->E) * (cfg->pad_multiple - 1);
+    e = launch_offsets(topk_idx, topk_w, A, cfg->E, cfg->pad_multiple, R, counts, padded_offsets,
+                       block_metadata, num_blocks, perm_row, row_src, row_gate, status,
+                       static_cast<int32_t*>(scratch), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return set_last_error(MOE_ERR_CUDA, "offsets kernels: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}
