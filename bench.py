@@ -249,7 +249,12 @@ def run_ours(args, shape, rank, world, local):
     moe_build.build()
     moe.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = synth.make_inputs(shape, device=dev)
+    # token rows, router weight and routing on the host (the same draws as the
+    # tests and the Zipf calibration), expert weights drawn on the GPU
+    inp = synth.make_inputs(shape, device="cpu", weights_device=dev)
+    for key in ("x", "Wg", "bias", "topk_idx", "topk_w"):
+        if inp.get(key) is not None:
+            inp[key] = inp[key].to(dev)
     cfg = moe.config_of(shape)
     layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
                          bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),

@@ -114,7 +114,10 @@ def normal_bf16(shape, std: float, base: int, name: str, device="cpu", chunk_dim
 
 
 def zipf_s_table() -> dict:
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "zipf_s.json")
+    """Zipf exponents per imbalance workload, as stored by
+    tests/golden/make_zipf_s.py (bisection on the oracle's routing counts)."""
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tests",
+                        "golden", "zipf_s.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
