@@ -27,7 +27,7 @@ __all__ = [
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
     "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
-    "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string",
+    "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
 ]
 
 MOE_OK = 0
@@ -315,3 +315,64 @@ class MoeLayer:
 
     def device_status(self, stream=None) -> int:
         return moe_get_device_status(self.ws, stream)
+
+
+class HostPipeline:
+    """Runs a MoeLayer on token batches held in pinned host memory.
+
+    Each submitted batch is copied to the device, run through the layer and
+    copied back; the copies of neighbouring batches overlap the layer's
+    compute (three streams: copy-in, compute, copy-out, with ``depth``
+    device buffers in rotation).  ``synchronize()`` waits for every submitted
+    batch.  The layer's own workspace is reused batch after batch, so layer
+    calls stay ordered on the compute stream.
+    """
+
+    def __init__(self, layer: MoeLayer, depth: int = 2):
+        T, d = layer.cfg.T, layer.cfg.d
+        dev = layer.ws.device
+        self.layer = layer
+        self.depth = depth
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_run = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.x_dev = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.o_dev = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.ev_in = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_run = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_out = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+        self.i = 0
+
+    def submit(self, x_host: torch.Tensor, out_host: torch.Tensor, topk_idx=None, topk_w=None):
+        k = self.i % self.depth
+        self.i += 1
+        if self.used[k]:
+            self.s_in.wait_event(self.ev_run[k])    # x buffer no longer read
+            self.s_run.wait_event(self.ev_out[k])   # out buffer copied back
+        self.used[k] = True
+        with torch.cuda.stream(self.s_in):
+            self.x_dev[k].copy_(x_host, non_blocking=True)
+            if topk_idx is not None and not topk_idx.is_cuda:
+                # pre-routed batches carry their routing from the host too
+                if not hasattr(self, "idx_dev"):
+                    self.idx_dev = [torch.empty_like(topk_idx, device=self.x_dev[0].device)
+                                    for _ in range(self.depth)]
+                    self.w_dev = [torch.empty_like(topk_w, device=self.x_dev[0].device)
+                                  for _ in range(self.depth)]
+                self.idx_dev[k].copy_(topk_idx, non_blocking=True)
+                self.w_dev[k].copy_(topk_w, non_blocking=True)
+                topk_idx, topk_w = self.idx_dev[k], self.w_dev[k]
+            self.ev_in[k].record(self.s_in)
+        self.s_run.wait_event(self.ev_in[k])
+        self.layer.forward(self.x_dev[k], self.o_dev[k], topk_idx=topk_idx, topk_w=topk_w,
+                           stream=self.s_run)
+        self.ev_run[k].record(self.s_run)
+        self.s_out.wait_event(self.ev_run[k])
+        with torch.cuda.stream(self.s_out):
+            out_host.copy_(self.o_dev[k], non_blocking=True)
+            self.ev_out[k].record(self.s_out)
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_run, self.s_out):
+            s.synchronize()

@@ -53,27 +53,52 @@ struct GemmCfg {
     static_assert(STAGES >= 2, "need at least two stages");
 };
 
+// One tile = 128 rows [m0, m0 + 128) of the A operand for one expert, of
+// which rows [lo, hi) (relative to m0) are stored.  With 128-row blocks a
+// tile is one block.  With 64-row blocks a tile is the 128-row window of the
+// padded buffer that holds the block: two blocks of one expert in the same
+// window share one tile (the second block's tile is skipped), and a window
+// whose halves belong to two experts is visited once per expert, each visit
+// storing only its own rows.
 struct TileInfo {
-    int e, m0, vm, nb;
+    int e, m0, lo, hi, nb;
+    bool skip;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int nblocks) {
     TileInfo ti;
     const int mb = t / a.n_tiles;
     ti.nb = t - mb * a.n_tiles;
-    if (a.block_metadata) {
-        ti.e = __ldg(a.block_metadata + 3 * mb + 0);
-        ti.m0 = __ldg(a.block_metadata + 3 * mb + 1);
-        ti.vm = __ldg(a.block_metadata + 3 * mb + 2);
-    } else {
+    ti.skip = false;
+    if (!a.block_metadata) {
         ti.e = 0;
         ti.m0 = mb * BM;
-        ti.vm = min(BM, a.dense_rows - ti.m0);
+        ti.lo = 0;
+        ti.hi = min(BM, a.dense_rows - ti.m0);
+        return ti;
+    }
+    const int32_t* bm = a.block_metadata;
+    ti.e = __ldg(bm + 3 * mb + 0);
+    const int start = __ldg(bm + 3 * mb + 1);
+    const int valid = __ldg(bm + 3 * mb + 2);
+    if (!a.pair64) {
+        ti.m0 = start;
+        ti.lo = 0;
+        ti.hi = valid;
+        return ti;
+    }
+    const int win = start >> 7;
+    ti.m0 = win << 7;
+    ti.lo = start - ti.m0;
+    ti.hi = ti.lo + valid;
+    if (mb > 0 && (__ldg(bm + 3 * (mb - 1) + 1) >> 7) == win && __ldg(bm + 3 * (mb - 1)) == ti.e) {
+        ti.skip = true;  // covered by the previous block's tile
+    } else if (mb + 1 < nblocks && (__ldg(bm + 3 * (mb + 1) + 1) >> 7) == win &&
+               __ldg(bm + 3 * (mb + 1)) == ti.e) {
+        ti.hi += __ldg(bm + 3 * (mb + 1) + 2);
     }
     return ti;
 }
-
-__device__ __forceinline__ float bf16_bits_lo(uint32_t v) { return __uint_as_float(v << 16); }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
@@ -84,7 +109,7 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
                                            int row) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    const bool valid = row < ti.vm;
+    const bool valid = row >= ti.lo && row < ti.hi;
     __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * 128;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -112,7 +137,7 @@ template <int BN>
 __device__ __forceinline__ void epi_gate(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
                                          int row) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    const bool valid = row < ti.vm;
+    const bool valid = row >= ti.lo && row < ti.hi;
     const float gate = (valid && a.row_gate) ? __ldg(a.row_gate + ti.m0 + row) : 1.0f;
     __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * BN;
 #pragma unroll 1
@@ -142,7 +167,7 @@ __device__ __forceinline__ void epi_router(const GemmArgs& a, const TileInfo& ti
                                            int row) {
     const int E = a.E, k = a.k;
     const int token = ti.m0 + row;
-    const bool valid = row < ti.vm;
+    const bool valid = row >= ti.lo && row < ti.hi;
     uint32_t gmask = 0xFFFFFFFFu;
     int gsz = E;
     if (a.n_groups > 0) {
@@ -291,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // stages armed and not yet seen consumed
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, t);
+                const TileInfo ti = decode_tile(args, t, nblocks);
+                if (ti.skip) continue;
                 const int brow = ti.e * args.b_rows_per_expert + ti.nb * BN;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
@@ -330,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t aph = 0;
             bool issued = false;
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+                if (decode_tile(args, t, nblocks).skip) continue;
                 if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag)) {
                     timed_out = true;
                     break;
@@ -376,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile(args, t);
+            const TileInfo ti = decode_tile(args, t, nblocks);
+            if (ti.skip) continue;
             // tcgen05.ld is warp-collective: the whole warp proceeds or stops
             const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
             if (!ok) {

@@ -15,6 +15,7 @@ struct GemmArgs {
     const int32_t* block_metadata;  // [nb_cap, 3] or null
     const int32_t* num_blocks;      // [1] or null
     int32_t nb_cap;                 // capacity of the block table
+    int32_t pair64;                 // blocks are 64 rows: tile on the 128-row grid
     int32_t dense_rows;             // rows when block_metadata is null
     int32_t n_tiles;                // N / BN
     int32_t k_blocks;               // K / 64

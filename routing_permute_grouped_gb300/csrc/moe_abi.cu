@@ -185,6 +185,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.block_metadata = meta;
     a.num_blocks = nb;
     a.nb_cap = static_cast<int32_t>(s.NB);
+    a.pair64 = c.pad_multiple == 64;
     a.status = status;
     // GEMM1: N = 2*d_e (gate/up interleaved), K = d
     a.n_tiles = (2 * c.d_e) / 256;

@@ -307,3 +307,33 @@ def test_combine_stage(shared):
     ulp = np.ldexp(1.0, np.frexp(np.abs(expect))[1] - 8)
     assert (np.abs(got - expect) <= ulp).all()
     assert np.mean(got == oracle.round_bf16(expect)) > 0.999
+
+
+def test_host_pipeline_matches_layer():
+    # batches in pinned host memory through HostPipeline == the layer on
+    # device tensors (same kernels, deterministic order: bit-identical)
+    shape, inp, _ = prepared("small_default")
+    cfg, layer = make_layer(shape, inp)
+    g = torch.Generator().manual_seed(9)
+    xs = [inp["x"]] + [torch.randn(inp["x"].shape, generator=g).to(torch.bfloat16)
+                       for _ in range(4)]
+    xs_host = [x.pin_memory() for x in xs]
+    outs = [torch.empty_like(x).pin_memory() for x in xs]
+    pipe = moe.HostPipeline(layer)
+    for x, o in zip(xs_host, outs):
+        pipe.submit(x, o)
+    pipe.synchronize()
+    for x, o in zip(xs, outs):
+        ref = layer(cuda(x)).cpu()
+        assert torch.equal(o, ref)
+
+
+def test_host_pipeline_prerouted():
+    shape, inp, ref = prepared("small_prerouted")
+    cfg, layer = make_layer(shape, inp)
+    x = inp["x"].pin_memory()
+    o = torch.empty_like(x).pin_memory()
+    pipe = moe.HostPipeline(layer)
+    pipe.submit(x, o, topk_idx=inp["topk_idx"].pin_memory(), topk_w=inp["topk_w"].pin_memory())
+    pipe.synchronize()
+    assert_close(o.double().numpy(), ref["out"], "out")
