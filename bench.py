@@ -295,8 +295,8 @@ def run_ours(args, shape, rank, world, local):
         moe.moe_permute(cfg, x, perm_row, x_perm)
         if ev is not None:
             ev[3].record()
-        moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, row_gate, h, y,
-                                    status_word)
+        moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate, h,
+                                    y, status_word)
         if ev is not None:
             ev[4].record()
         if ds:

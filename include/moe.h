@@ -223,7 +223,9 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *
  *   h[r] = bf16( silu(x_perm[r] W1[e]) * (x_perm[r] W3[e]) )
  *   y[r] = bf16( row_gate[r] * (h[r] W2[e]) )
  * for every valid row r of every block [e, m_start, valid_m].  tcgen05 MMAs
- * with fp32 accumulators in tensor memory, operands staged by TMA; SwiGLU is
+ * with fp32 accumulators in tensor memory, issued on CTA pairs
+ * (cta_group::2: a 256-row tile whose B operand is split between the two
+ * SMs), operands staged by TMA; SwiGLU is
  * fused into the first GEMM's epilogue and the routing weight into the
  * second's ("MoE & MLA operators", sec. 2.5: output * expert weight in the
  * GEMM epilogue).  Pad rows of h and y are not written.
@@ -231,14 +233,18 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *
  *   W13, W2_t      packed weights      device, read (moe_pack_experts)
  *   block_metadata int32 [NB_max, 3]   device, read
  *   num_blocks     int32 [1]           device, read (never copied to the host)
+ *   padded_offsets int32 [E + 1]       device, read: segment starts, so that a
+ *                                      CTA pair takes an expert's blocks two
+ *                                      (P = 128) or four (P = 64) at a time
  *   row_gate       fp32 [R_max] or NULL (NULL = 1)
  *   h              bf16 [R_max, d_e]   device, written
  *   y              bf16 [R_max, d]     device, written
  *   status         uint32 [1] device error word, or NULL */
 moe_status_t moe_grouped_gemm_swiglu(const moe_config_t *cfg, const void *x_perm, const void *W13,
                                      const void *W2_t, const int32_t *block_metadata,
-                                     const int32_t *num_blocks, const float *row_gate, void *h,
-                                     void *y, uint32_t *status, void *stream);
+                                     const int32_t *num_blocks, const int32_t *padded_offsets,
+                                     const float *row_gate, void *h, void *y, uint32_t *status,
+                                     void *stream);
 
 /* a6. Dense shared expert ("Dropless and grouped GEMM", sec. 1: it reads the
  * original token rows, with no permute and no group sizes):

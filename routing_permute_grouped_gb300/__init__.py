@@ -90,7 +90,7 @@ def load():
         "moe_build_offsets": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_build_offsets_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
-        "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P]),
+        "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
         "moe_combine": (ctypes.c_int, [CP, P, P, P, P, P]),
         "moe_layer_fwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, SZ, P]),
@@ -207,11 +207,12 @@ def moe_permute(cfg, x, perm_row, x_perm, stream=None) -> None:
                               _stream(stream)))
 
 
-def moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate, h, y,
-                            status=None, stream=None) -> None:
+def moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets,
+                            row_gate, h, y, status=None, stream=None) -> None:
     _check(load().moe_grouped_gemm_swiglu(
         ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
-        _ptr(num_blocks), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
+        _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status),
+        _stream(stream)))
 
 
 def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:

@@ -438,6 +438,269 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------ CTA-pair (2-SM) kernel --
+//
+// The same grouped GEMM on CTA pairs (clusters of 2): one tcgen05.mma with
+// cta_group::2 computes a 256 x BN tile whose A rows are split between the
+// two CTAs (128 each) and whose B tile is split along N (BN/2 rows each), so
+// each SM stages only half of the B operand.  The even CTA issues the MMAs;
+// both CTAs run a TMA producer (completions counted on the even CTA's
+// barriers) and an epilogue over their own 128 accumulator rows.
+//
+// A unit of work is a 256-row visit of one expert's segment: visits start at
+// every 256th row of the segment (from padded_offsets), so the blocks of one
+// expert are taken two (P = 128) or four (P = 64) at a time; rows of a visit
+// past the segment's valid rows are computed but never stored.  Only real
+// visits are enumerated, so the round-robin over CTA pairs stays balanced.
+
+struct PairTile {
+    int e, m0, hi, nb;  // rows [m0, m0 + hi) of the visit are valid
+};
+
+// Visits of expert e are numbered from vpref[e] (exclusive prefix over the
+// experts of ceil(blocks_e / (256 / P))); block i of expert e is block
+// padded_offsets[e] / P + i of the table, so a visit maps to its first block
+// without any search of the table itself.
+__device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const int* vpref) {
+    PairTile p;
+    const int v = t / a.n_tiles;
+    p.nb = t - v * a.n_tiles;
+    if (!a.block_metadata) {
+        p.e = 0;
+        p.m0 = v * 256;
+        p.hi = min(256, a.dense_rows - p.m0);
+        return p;
+    }
+    int lo = 0, hi = a.n_experts;  // largest e with vpref[e] <= v
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (vpref[mid] <= v) lo = mid; else hi = mid;
+    }
+    p.e = lo;
+    const int per = 256 / a.block_rows;
+    const int mb = __ldg(a.padded_offsets + lo) / a.block_rows + (v - vpref[lo]) * per;
+    const int32_t* bm = a.block_metadata;
+    p.m0 = __ldg(bm + 3 * mb + 1);
+    p.hi = __ldg(bm + 3 * mb + 2);
+    const int bend = __ldg(a.padded_offsets + lo + 1) / a.block_rows;  // next expert's first block
+    for (int j = 1; j < per && mb + j < bend; ++j) p.hi += __ldg(bm + 3 * (mb + j) + 2);
+    return p;
+}
+
+template <int BN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    constexpr int BH = BN / 2;  // B rows staged by each CTA
+    constexpr int A_BYTES = BM * BK * 2;
+    constexpr int B_BYTES = BH * BK * 2;
+    constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
+    constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+    static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * B_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* tfull = bars + 2 * S;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_holder + 1;
+    int* vpref = reinterpret_cast<int*>(bars + 64);  // [E + 1]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull + i, 1);
+            mbar_init(tempty + i, 8);  // one arrival per epilogue warp of both CTAs
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    if (warp == 2 && args.block_metadata) {
+        // per-expert visit counts from the segment sizes, exclusive warp scan
+        const int per = 256 / args.block_rows;
+        int running = 0;
+        for (int base = 0; base < args.n_experts; base += 32) {
+            const int e = base + lane;
+            int nv = 0;
+            if (e < args.n_experts) {
+                const int nblk = (__ldg(args.padded_offsets + e + 1) - __ldg(args.padded_offsets + e)) /
+                                 args.block_rows;
+                nv = (nblk + per - 1) / per;
+            }
+            int x = nv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (e < args.n_experts) vpref[e] = running + x - nv;
+            running += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+        if (lane == 0) vpref[args.n_experts] = running;
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int nvisits = args.block_metadata ? vpref[args.n_experts] : (args.dense_rows + 255) / 256;
+    const int total = nvisits * args.n_tiles;
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    bool timed_out = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_par = 0;
+            for (int t = cluster; t < total && !timed_out; t += nclusters) {
+                const PairTile p = decode_pair(args, t, vpref);
+                const int arow = p.m0 + BM * static_cast<int>(rank);
+                const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
+                        timed_out = true;
+                        break;
+                    }
+                    armed &= ~(1u << s);
+                    const uint32_t full_leader = mapa_shared(smem_u32(full + s), 0);
+                    if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
+                    tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
+                    tma_load_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if ((timed_out || *abort_flag) && leader) {
+                *abort_flag = 1;
+                for (int i = 0; i < S; ++i)
+                    if (armed & (1u << i)) {
+                        volatile uint32_t never = 0;
+                        (void)mbar_wait(full + i, (armed_par >> i) & 1u, &never);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool issued = false;
+            for (int t = cluster; t < total && !timed_out; t += nclusters) {
+                if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(full + s, ph, abort_flag)) {
+                        timed_out = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + kk * 32),
+                                      sdesc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    mma_commit_pair(empty + s, 0x3);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (timed_out) break;
+                mma_commit_pair(tfull + acc, 0x3);
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            if ((timed_out || *abort_flag) && issued) {
+                *abort_flag = 1;
+                mma_commit_pair(drain, 0x1);
+                volatile uint32_t never = 0;
+                (void)mbar_wait(drain, 0, &never);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = cluster; t < total; t += nclusters) {
+            const PairTile p = decode_pair(args, t, vpref);
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
+            if (!ok) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            TileInfo ti;
+            ti.e = p.e;
+            ti.nb = p.nb;
+            ti.m0 = p.m0 + BM * static_cast<int>(rank);
+            ti.lo = 0;
+            ti.hi = min(BM, p.hi - BM * static_cast<int>(rank));
+            ti.skip = false;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            if constexpr (EPI == kEpiSwiGLU) {
+                epi_swiglu(args, ti, taddr, row);
+            } else {
+                epi_gate<BN>(args, ti, taddr, row);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + acc), 0));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+        if (timed_out) *abort_flag = 1;
+    }
+
+    if (timed_out && args.status) atomicOr(args.status, kDevErrTimeout);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its pair may still touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ---------------------------------------------------------------- host --
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -495,12 +758,52 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
     return cudaGetLastError();
 }
 
+template <int BN, int EPI>
+static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
+                                 int max_visits, cudaStream_t stream) {
+    constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
+    constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
+    constexpr int SMEM = 1024 + S * STAGE_BYTES + 512 + 4 * 260;
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!max_clusters[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_pair<BN, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = SMEM;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<BN, EPI>, &cfg);
+        if (e != cudaSuccess || n <= 0) n = num_sms() / 2;
+        max_clusters[dev] = n;
+    }
+    int clusters = max_clusters[dev];
+    if (max_visits < clusters) clusters = max_visits;
+    if (clusters <= 0) return cudaSuccess;
+    k_grouped_gemm_pair<BN, EPI><<<2 * clusters, kThreads, SMEM, stream>>>(tA, tB, args);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,
                                 int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
                                 cudaStream_t stream) {
     CUtensorMap tA, tB;
-    if (!make_tmap(&tA, A, rowsA, K, BM) || !make_tmap(&tB, B, rowsB, K, bn))
+    const bool pair = epi != kEpiRouter;
+    if (!make_tmap(&tA, A, rowsA, K, BM) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
         return cudaErrorInvalidValue;
+    if (pair) {
+        if (epi == kEpiSwiGLU && bn == 256)
+            return launch_pair_t<256, kEpiSwiGLU>(tA, tB, args, max_tiles, stream);
+        if (epi == kEpiGate && bn == 256)
+            return launch_pair_t<256, kEpiGate>(tA, tB, args, max_tiles, stream);
+        if (epi == kEpiGate && bn == 128)
+            return launch_pair_t<128, kEpiGate>(tA, tB, args, max_tiles, stream);
+        return cudaErrorInvalidValue;
+    }
     if (epi == kEpiSwiGLU) {
         if (bn == 256) return launch_t<256, kEpiSwiGLU>(tA, tB, args, max_tiles, stream);
     } else if (epi == kEpiGate) {

@@ -178,14 +178,17 @@ static moe_status_t do_offsets(const moe_config_t& c, const int32_t* topk_idx, c
 
 static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const void* W13,
                                const void* W2_t, const int32_t* meta, const int32_t* nb,
-                               const float* row_gate, void* h, void* y, uint32_t* status,
-                               cudaStream_t st) {
+                               const int32_t* po, const float* row_gate, void* h, void* y,
+                               uint32_t* status, cudaStream_t st) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
     a.block_metadata = meta;
     a.num_blocks = nb;
     a.nb_cap = static_cast<int32_t>(s.NB);
     a.pair64 = c.pad_multiple == 64;
+    a.padded_offsets = po;
+    a.block_rows = c.pad_multiple;
+    a.n_experts = c.E;
     a.status = status;
     // GEMM1: N = 2*d_e (gate/up interleaved), K = d
     a.n_tiles = (2 * c.d_e) / 256;
@@ -216,12 +219,13 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     GemmArgs a{};
     a.dense_rows = c.T;
     a.status = status;
+    a.block_rows = 256;
     a.n_tiles = (2 * c.d_shared) / 256;
     a.k_blocks = c.d / 64;
     a.b_rows_per_expert = 0;
     a.out = hs;
     a.ldo = c.d_shared;
-    const int mblocks = (c.T + 127) / 128;
+    const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
                                         mblocks * a.n_tiles, st);
     if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
@@ -274,7 +278,9 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     if (r != MOE_OK) return r;
     cudaError_t e = launch_permute(x, perm_row, at(L.x_perm), c.T, c.d, c.k, st);
     if (e != cudaSuccess) return cuda_fail(e, "permute");
-    r = do_experts(c, at(L.x_perm), w->W13, w->W2, meta, nb, row_gate, at(L.h), at(L.y), status, st);
+    r = do_experts(c, at(L.x_perm), w->W13, w->W2, meta, nb,
+                   static_cast<const int32_t*>(at(L.padded_offsets)), row_gate, at(L.h), at(L.y),
+                   status, st);
     if (r != MOE_OK) return r;
     const void* shared = nullptr;
     if (c.d_shared) {
@@ -372,15 +378,16 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
 
 moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm, const void* W13,
                                      const void* W2_t, const int32_t* block_metadata,
-                                     const int32_t* num_blocks, const float* row_gate, void* h,
-                                     void* y, uint32_t* status, void* stream) {
+                                     const int32_t* num_blocks, const int32_t* padded_offsets,
+                                     const float* row_gate, void* h, void* y, uint32_t* status,
+                                     void* stream) {
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
-    if (!x_perm || !W13 || !W2_t || !block_metadata || !num_blocks || !h || !y)
+    if (!x_perm || !W13 || !W2_t || !block_metadata || !num_blocks || !padded_offsets || !h || !y)
         return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
-    return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate, h, y, status,
-                      static_cast<cudaStream_t>(stream));
+    return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
+                      h, y, status, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const void* Ws13,

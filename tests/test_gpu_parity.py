@@ -251,8 +251,11 @@ def test_grouped_gemm_stage(name):
     W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device="cuda")
     W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device="cuda")
     moe.moe_pack_experts(cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), W13, W2_t)
-    meta = np.zeros((NB, 3), np.int32)
+    # entries past num_blocks are stale: fill them with plausible-looking rows
+    # of the real table, which the kernels must never use
+    meta = np.resize(ref["block_metadata"], (NB, 3)).astype(np.int32)
     meta[:ref["num_blocks"]] = ref["block_metadata"]
+    meta[ref["num_blocks"]:, 1] += 128
     gate32 = ref["row_gate"].astype(np.float32)
     x_perm = torch.from_numpy(ref["x_perm"].view(np.int16)).view(torch.bfloat16).cuda()
     h = torch.zeros((R, de), dtype=torch.bfloat16, device="cuda")
@@ -260,6 +263,7 @@ def test_grouped_gemm_stage(name):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     moe.moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, cuda(torch.from_numpy(meta)),
                                 cuda(torch.tensor([ref["num_blocks"]], dtype=torch.int32)),
+                                cuda(torch.from_numpy(ref["padded_offsets"])),
                                 cuda(torch.from_numpy(gate32)), h, y, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
