@@ -233,10 +233,11 @@ def run_reference(args, shape, rank, world):
 METRIC = "MoE layer fwd useful TFLOP/s (bf16, fp32 accumulate)"
 
 
-def config_dict(shape):
+def config_dict(shape, permute="separate"):
     return {"workload": f"{shape.name}: T={shape.T} d={shape.d} d_e={shape.d_e} E={shape.E} "
                         f"k={shape.k} groups={shape.n_groups}/{shape.topk_groups} "
                         f"pad={shape.pad} shared={shape.d_shared}",
+            "permute": permute,
             "l2": "inputs larger than L2 (expert weights and permuted rows exceed 129 MB)",
             "parallelism": "replicas"}
 
@@ -292,11 +293,16 @@ def run_ours(args, shape, rank, world, local):
                               row_gate, offs_ws)
         if ev is not None:
             ev[2].record()
-        moe.moe_permute(cfg, x, perm_row, x_perm)
+        if args.permute == "separate":
+            moe.moe_permute(cfg, x, perm_row, x_perm)
         if ev is not None:
             ev[3].record()
-        moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate, h,
-                                    y, status_word)
+        if args.permute == "separate":
+            moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate,
+                                        h, y, status_word)
+        else:
+            moe.moe_grouped_gemm_swiglu_gather(cfg, x, row_src, layer.W13, layer.W2_t, meta, nb, po,
+                                               row_gate, h, y, status_word)
         if ev is not None:
             ev[4].record()
         if ds:
@@ -307,7 +313,8 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[6].record()
 
-    launches_per_step = (0 if shape.prerouted else 1) + 3 + 1 + 2 + (2 if ds else 0) + 1
+    launches_per_step = ((0 if shape.prerouted else 1) + 3 + (1 if args.permute == "separate" else 0)
+                         + 2 + (2 if ds else 0) + 1)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -386,7 +393,7 @@ def run_ours(args, shape, rank, world, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_dict(shape),
+        "data": "synthetic", "config": config_dict(shape, args.permute),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -442,6 +449,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--permute", choices=["separate", "fused"], default="separate",
+                    help="permute as its own kernel, or fused into GEMM1's A load")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     shape = synth.WORKLOADS[args.workload]

@@ -246,6 +246,21 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t *cfg, const void *x_perm
                                      const float *row_gate, void *h, void *y, uint32_t *status,
                                      void *stream);
 
+/* a3 + a4 + a5 fused: the grouped GEMMs of moe_grouped_gemm_swiglu with the
+ * permute folded into GEMM1's A load ("Dropless and grouped GEMM", sec. 4:
+ * gather the token rows by index instead of materialising the k copies).
+ * Padded row r of expert e's segment reads x[row_src[r] / k]; pad rows read
+ * zeros.  No x_perm buffer is read or written.
+ *   x       bf16 [T, d]     device, read
+ *   row_src int32 [R_max]   device, read (moe_build_offsets)
+ * Other arguments and outputs as moe_grouped_gemm_swiglu. */
+moe_status_t moe_grouped_gemm_swiglu_gather(const moe_config_t *cfg, const void *x,
+                                            const int32_t *row_src, const void *W13,
+                                            const void *W2_t, const int32_t *block_metadata,
+                                            const int32_t *num_blocks,
+                                            const int32_t *padded_offsets, const float *row_gate,
+                                            void *h, void *y, uint32_t *status, void *stream);
+
 /* a6. Dense shared expert ("Dropless and grouped GEMM", sec. 1: it reads the
  * original token rows, with no permute and no group sizes):
  *   hs = bf16( silu(x Ws1) * (x Ws3) ),  ys = bf16( hs Ws2 )

@@ -26,7 +26,7 @@ __all__ = [
     "MoeError", "MoeConfig", "MoeWeights", "MoeLayer", "config_of", "load",
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
     "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
-    "moe_grouped_gemm_swiglu", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
+    "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
 ]
 
@@ -91,6 +91,7 @@ def load():
         "moe_build_offsets_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
         "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
+        "moe_grouped_gemm_swiglu_gather": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
         "moe_combine": (ctypes.c_int, [CP, P, P, P, P, P]),
         "moe_layer_fwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, SZ, P]),
@@ -211,6 +212,15 @@ def moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, 
                             row_gate, h, y, status=None, stream=None) -> None:
     _check(load().moe_grouped_gemm_swiglu(
         ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
+        _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status),
+        _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_gather(cfg, x, row_src, W13, W2_t, block_metadata, num_blocks,
+                                   padded_offsets, row_gate, h, y, status=None,
+                                   stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu_gather(
+        ctypes.byref(cfg), _ptr(x), _ptr(row_src), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
         _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status),
         _stream(stream)))
 

@@ -487,8 +487,11 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
     return p;
 }
 
-template <int BN, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// GATHER: the A rows are gathered from the token rows by a seventh warp
+// (the permute fused into GEMM1's A load) instead of being loaded by TMA from
+// the permuted buffer.
+template <int BN, int EPI, bool GATHER>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? kThreads + 32 : kThreads, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
     constexpr int BH = BN / 2;  // B rows staged by each CTA
@@ -520,7 +523,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(full + i, 1);
+            // the even CTA's producer (+ the A gatherers of both CTAs)
+            mbar_init(full + i, GATHER ? 3 : 1);
             mbar_init(empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -586,8 +590,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     armed &= ~(1u << s);
                     const uint32_t full_leader = mapa_shared(smem_u32(full + s), 0);
-                    if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
-                    tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
+                    if (leader) mbar_arrive_expect_tx(full + s, GATHER ? 2 * B_BYTES : 2 * STAGE_BYTES);
+                    if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
                     tma_load_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -654,7 +658,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(drain, 0, &never);
             }
         }
-    } else {
+    } else if (GATHER && warp == 6) {
+        // -------------------------------------------------- A-row gatherer
+        // Lane l copies rows l, l+32, l+64, l+96 of this CTA's half of the
+        // visit: padded row r reads token row row_src[r] / k; rows past the
+        // visit's valid rows are zero-filled.  The 16-byte chunk c of row r
+        // goes to chunk c ^ (r % 8) (the 128-byte swizzle that TMA would
+        // apply).  A stage is reported to the even CTA LAG stages later, once
+        // its copies have completed and been made visible to the async proxy.
+        constexpr int LAG = 4;
+        static_assert(LAG < S, "the gatherer must not wait on its own unreported stages");
+        const char* xg = static_cast<const char*>(args.gather_x);
+        const int64_t row_bytes = static_cast<int64_t>(args.k_blocks) * BK * 2;
+        int s = 0;
+        uint32_t ph = 0;
+        int n = 0;
+        for (int t = cluster; t < total && !timed_out; t += nclusters) {
+            const PairTile p = decode_pair(args, t, vpref);
+            const char* src[4];
+            uint32_t nbytes[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int rr = BM * static_cast<int>(rank) + lane + 32 * j;  // row in the visit
+                if (rr < p.hi) {
+                    const int a = __ldg(args.row_src + p.m0 + rr);
+                    src[j] = xg + static_cast<int64_t>(a / args.gather_k) * row_bytes;
+                    nbytes[j] = 16;
+                } else {
+                    src[j] = xg;
+                    nbytes[j] = 0;
+                }
+            }
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty + s, ph ^ 1u, abort_flag));
+                if (!ok) {
+                    timed_out = true;
+                    break;
+                }
+                const uint32_t sbase = smem_u32(sA + s * A_BYTES);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane + 32 * j;
+                    const uint32_t rowbase = sbase + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        cp_async_16(rowbase + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4),
+                                    src[j] + kb * 128 + c * 16, nbytes[j]);
+                }
+                cp_async_commit();
+                ++n;
+                if (n > LAG) {
+                    cp_async_wait<LAG>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(full + (n - 1 - LAG) % S), 0));
+                }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && !timed_out)
+            for (int i = max(0, n - LAG); i < n; ++i)
+                mbar_arrive_cluster(mapa_shared(smem_u32(full + i % S), 0));
+        if (timed_out) *abort_flag = 1;
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;
@@ -758,9 +830,10 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
     return cudaGetLastError();
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool GATHER>
 static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
                                  int max_visits, cudaStream_t stream) {
+    constexpr int NT = GATHER ? kThreads + 32 : kThreads;
     constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
     constexpr int SMEM = 1024 + S * STAGE_BYTES + 512 + 4 * 260;
@@ -769,22 +842,22 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
     cudaGetDevice(&dev);
     if (dev >= 64) return cudaErrorInvalidDevice;
     if (!max_clusters[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_pair<BN, EPI>,
+        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_pair<BN, EPI, GATHER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(NT, 1, 1);
         cfg.dynamicSmemBytes = SMEM;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<BN, EPI>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<BN, EPI, GATHER>, &cfg);
         if (e != cudaSuccess || n <= 0) n = num_sms() / 2;
         max_clusters[dev] = n;
     }
     int clusters = max_clusters[dev];
     if (max_visits < clusters) clusters = max_visits;
     if (clusters <= 0) return cudaSuccess;
-    k_grouped_gemm_pair<BN, EPI><<<2 * clusters, kThreads, SMEM, stream>>>(tA, tB, args);
+    k_grouped_gemm_pair<BN, EPI, GATHER><<<2 * clusters, NT, SMEM, stream>>>(tA, tB, args);
     return cudaGetLastError();
 }
 
@@ -797,11 +870,13 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
         return cudaErrorInvalidValue;
     if (pair) {
         if (epi == kEpiSwiGLU && bn == 256)
-            return launch_pair_t<256, kEpiSwiGLU>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, args, max_tiles, stream);
+        if (epi == kEpiSwiGLUGather && bn == 256)
+            return launch_pair_t<256, kEpiSwiGLU, true>(tA, tB, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 256)
-            return launch_pair_t<256, kEpiGate>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<256, kEpiGate, false>(tA, tB, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 128)
-            return launch_pair_t<128, kEpiGate>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<128, kEpiGate, false>(tA, tB, args, max_tiles, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == kEpiSwiGLU) {

@@ -19,6 +19,11 @@ struct GemmArgs {
     const int32_t* padded_offsets;  // [E + 1] segment starts (CTA-pair kernel)
     int32_t block_rows;             // rows per block of the table (P)
     int32_t n_experts;              // E (CTA-pair kernel)
+    // A rows gathered from token rows (permute fused into GEMM1's A load):
+    // padded row r reads gather_x[row_src[r] / gather_k], pad rows read zeros
+    const void* gather_x;
+    const int32_t* row_src;
+    int32_t gather_k;
     int32_t dense_rows;             // rows when block_metadata is null
     int32_t n_tiles;                // N / BN
     int32_t k_blocks;               // K / 64
@@ -34,7 +39,7 @@ struct GemmArgs {
     float* topk_w;
 };
 
-enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2 };
+enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 3 };
 
 // Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
 // [rowsB, K] bf16 (K-major), tile N = bn.  Returns a cudaError_t.

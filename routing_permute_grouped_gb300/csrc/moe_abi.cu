@@ -176,10 +176,14 @@ static moe_status_t do_offsets(const moe_config_t& c, const int32_t* topk_idx, c
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "offsets kernels");
 }
 
+// GEMM1 reads its A rows either from the permuted buffer x_perm (TMA) or,
+// when x_perm is null, straight from the token rows x through row_src (the
+// permute fused into the A load).
 static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const void* W13,
                                const void* W2_t, const int32_t* meta, const int32_t* nb,
                                const int32_t* po, const float* row_gate, void* h, void* y,
-                               uint32_t* status, cudaStream_t st) {
+                               uint32_t* status, cudaStream_t st, const void* x = nullptr,
+                               const int32_t* row_src = nullptr) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
     a.block_metadata = meta;
@@ -196,7 +200,12 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.b_rows_per_expert = 2 * c.d_e;
     a.out = h;
     a.ldo = c.d_e;
-    cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x_perm, s.R, W13,
+    const bool gather = x_perm == nullptr;
+    a.gather_x = x;
+    a.row_src = row_src;
+    a.gather_k = c.k;
+    cudaError_t e = launch_grouped_gemm(gather ? kEpiSwiGLUGather : kEpiSwiGLU, 256,
+                                        gather ? x : x_perm, gather ? c.T : s.R, W13,
                                         static_cast<int64_t>(c.E) * 2 * c.d_e, c.d, a,
                                         static_cast<int>(s.NB * a.n_tiles), st);
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 (gate/up + SwiGLU)");
@@ -388,6 +397,22 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
     if (cfg->T == 0) return MOE_OK;
     return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
                       h, y, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_gemm_swiglu_gather(const moe_config_t* cfg, const void* x,
+                                            const int32_t* row_src, const void* W13,
+                                            const void* W2_t, const int32_t* block_metadata,
+                                            const int32_t* num_blocks,
+                                            const int32_t* padded_offsets, const float* row_gate,
+                                            void* h, void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x || !row_src || !W13 || !W2_t || !block_metadata || !num_blocks || !padded_offsets ||
+        !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts(*cfg, nullptr, W13, W2_t, block_metadata, num_blocks, padded_offsets,
+                      row_gate, h, y, status, static_cast<cudaStream_t>(stream), x, row_src);
 }
 
 moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const void* Ws13,

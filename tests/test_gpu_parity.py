@@ -341,3 +341,35 @@ def test_host_pipeline_prerouted():
     pipe.submit(x, o, topk_idx=inp["topk_idx"].pin_memory(), topk_w=inp["topk_w"].pin_memory())
     pipe.synchronize()
     assert_close(o.double().numpy(), ref["out"], "out")
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_default", "small_imbalance_p64", "small_e100_d384",
+                                  "small_prerouted"])
+def test_grouped_gemm_gather_stage(name):
+    # the permute fused into GEMM1's A load: token rows gathered through
+    # row_src must give the same h and y as the oracle's permuted layout
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    E, d, de, R, NB = shape.E, shape.d, shape.d_e, shape.rows_capacity, shape.blocks_capacity
+    W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device="cuda")
+    W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), W13, W2_t)
+    meta = np.resize(ref["block_metadata"], (NB, 3)).astype(np.int32)
+    meta[:ref["num_blocks"]] = ref["block_metadata"]
+    gate32 = ref["row_gate"].astype(np.float32)
+    h = torch.zeros((R, de), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_swiglu_gather(
+        cfg, cuda(inp["x"]), cuda(torch.from_numpy(ref["row_src"])), W13, W2_t,
+        cuda(torch.from_numpy(meta)), cuda(torch.tensor([ref["num_blocks"]], dtype=torch.int32)),
+        cuda(torch.from_numpy(ref["padded_offsets"])), cuda(torch.from_numpy(gate32)), h, y, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    eh, ey = oracle.grouped_experts(ref["x_perm"], bits(inp["W1"]), bits(inp["W3"]),
+                                    bits(inp["W2"]), ref["block_metadata"],
+                                    gate32.astype(np.float64))
+    valid = ref["row_src"] >= 0
+    assert_close(f64(h)[valid], eh[valid], "h")
+    assert_close(f64(y)[valid], ey[valid], "y")
+    assert (f64(y)[~valid] == 0).all() and (f64(h)[~valid] == 0).all()
