@@ -487,11 +487,11 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
     return p;
 }
 
-// GATHER: the A rows are gathered from the token rows by a seventh warp
-// (the permute fused into GEMM1's A load) instead of being loaded by TMA from
-// the permuted buffer.
+// GATHER: the A rows are gathered from the token rows with TMA gather4 (the
+// permute fused into GEMM1's A load) instead of a tile load from the
+// permuted buffer.
 template <int BN, int EPI, bool GATHER>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? kThreads + 32 : kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
     constexpr int BH = BN / 2;  // B rows staged by each CTA
@@ -523,8 +523,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? kThreads + 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            // the even CTA's producer (+ the A gatherers of both CTAs)
-            mbar_init(full + i, GATHER ? 3 : 1);
+            mbar_init(full + i, 1);  // the even CTA's producer (+ transaction bytes)
             mbar_init(empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -574,41 +573,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? kThreads + 
     bool timed_out = false;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t armed = 0, armed_par = 0;
-            for (int t = cluster; t < total && !timed_out; t += nclusters) {
-                const PairTile p = decode_pair(args, t, vpref);
-                const int arow = p.m0 + BM * static_cast<int>(rank);
-                const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
-                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
-                        timed_out = true;
-                        break;
-                    }
+        // ---------------------------------------------------- TMA producer
+        // Lane 0 loads the B half (and the A tile from the permuted buffer);
+        // in the gather variant every lane also gathers 4 of this CTA's 128
+        // A rows straight from the token rows (row_src[r] / k) with one
+        // gather4 per k-step (4 rows x 128 bytes at offset 512 * lane of the
+        // 128-byte-swizzled A stage).
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t armed = 0, armed_par = 0;
+        for (int t = cluster; t < total && !timed_out; t += nclusters) {
+            const PairTile p = decode_pair(args, t, vpref);
+            const int arow = p.m0 + BM * static_cast<int>(rank);
+            const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
+            int grow[4] = {0, 0, 0, 0};
+            if (GATHER) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int rr = BM * static_cast<int>(rank) + 4 * lane + j;  // row in the visit
+                    // rows past the visit's valid rows are computed but never
+                    // stored: any in-range token row will do
+                    if (rr < p.hi) grow[j] = __ldg(args.row_src + p.m0 + rr) / args.gather_k;
+                }
+            }
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(empty + s, ph ^ 1u, abort_flag);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) {
+                    timed_out = true;
+                    break;
+                }
+                const uint32_t full_leader = mapa_shared(smem_u32(full + s), 0);
+                if (lane == 0) {
                     armed &= ~(1u << s);
-                    const uint32_t full_leader = mapa_shared(smem_u32(full + s), 0);
-                    if (leader) mbar_arrive_expect_tx(full + s, GATHER ? 2 * B_BYTES : 2 * STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
                     if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
                     tma_load_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                }
+                if (GATHER)
+                    tma_gather4_pair(smem_u32(sA + s * A_BYTES) + lane * 512u, &tmA, kb * BK, grow[0],
+                                     grow[1], grow[2], grow[3], full_leader);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-            if ((timed_out || *abort_flag) && leader) {
-                *abort_flag = 1;
-                for (int i = 0; i < S; ++i)
-                    if (armed & (1u << i)) {
-                        volatile uint32_t never = 0;
-                        (void)mbar_wait(full + i, (armed_par >> i) & 1u, &never);
-                    }
-            }
+        }
+        if (lane == 0 && (timed_out || *abort_flag) && leader) {
+            *abort_flag = 1;
+            for (int i = 0; i < S; ++i)
+                if (armed & (1u << i)) {
+                    volatile uint32_t never = 0;
+                    (void)mbar_wait(full + i, (armed_par >> i) & 1u, &never);
+                }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
@@ -658,74 +678,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? kThreads + 
                 (void)mbar_wait(drain, 0, &never);
             }
         }
-    } else if (GATHER && warp == 6) {
-        // -------------------------------------------------- A-row gatherer
-        // Lane l copies rows l, l+32, l+64, l+96 of this CTA's half of the
-        // visit: padded row r reads token row row_src[r] / k; rows past the
-        // visit's valid rows are zero-filled.  The 16-byte chunk c of row r
-        // goes to chunk c ^ (r % 8) (the 128-byte swizzle that TMA would
-        // apply).  A stage is reported to the even CTA LAG stages later, once
-        // its copies have completed and been made visible to the async proxy.
-        constexpr int LAG = 4;
-        static_assert(LAG < S, "the gatherer must not wait on its own unreported stages");
-        const char* xg = static_cast<const char*>(args.gather_x);
-        const int64_t row_bytes = static_cast<int64_t>(args.k_blocks) * BK * 2;
-        int s = 0;
-        uint32_t ph = 0;
-        int n = 0;
-        for (int t = cluster; t < total && !timed_out; t += nclusters) {
-            const PairTile p = decode_pair(args, t, vpref);
-            const char* src[4];
-            uint32_t nbytes[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int rr = BM * static_cast<int>(rank) + lane + 32 * j;  // row in the visit
-                if (rr < p.hi) {
-                    const int a = __ldg(args.row_src + p.m0 + rr);
-                    src[j] = xg + static_cast<int64_t>(a / args.gather_k) * row_bytes;
-                    nbytes[j] = 16;
-                } else {
-                    src[j] = xg;
-                    nbytes[j] = 0;
-                }
-            }
-            for (int kb = 0; kb < args.k_blocks; ++kb) {
-                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty + s, ph ^ 1u, abort_flag));
-                if (!ok) {
-                    timed_out = true;
-                    break;
-                }
-                const uint32_t sbase = smem_u32(sA + s * A_BYTES);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = lane + 32 * j;
-                    const uint32_t rowbase = sbase + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        cp_async_16(rowbase + ((static_cast<uint32_t>(c) ^ (r & 7)) << 4),
-                                    src[j] + kb * 128 + c * 16, nbytes[j]);
-                }
-                cp_async_commit();
-                ++n;
-                if (n > LAG) {
-                    cp_async_wait<LAG>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(full + (n - 1 - LAG) % S), 0));
-                }
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && !timed_out)
-            for (int i = max(0, n - LAG); i < n; ++i)
-                mbar_arrive_cluster(mapa_shared(smem_u32(full + i % S), 0));
-        if (timed_out) *abort_flag = 1;
     } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;
@@ -833,7 +785,7 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
 template <int BN, int EPI, bool GATHER>
 static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
                                  int max_visits, cudaStream_t stream) {
-    constexpr int NT = GATHER ? kThreads + 32 : kThreads;
+    constexpr int NT = kThreads;
     constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
     constexpr int SMEM = 1024 + S * STAGE_BYTES + 512 + 4 * 260;
@@ -866,7 +818,8 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
                                 cudaStream_t stream) {
     CUtensorMap tA, tB;
     const bool pair = epi != kEpiRouter;
-    if (!make_tmap(&tA, A, rowsA, K, BM) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
+    const int a_box = epi == kEpiSwiGLUGather ? 1 : BM;  // gather4 reads one-row boxes
+    if (!make_tmap(&tA, A, rowsA, K, a_box) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
         return cudaErrorInvalidValue;
     if (pair) {
         if (epi == kEpiSwiGLU && bn == 256)

@@ -225,6 +225,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
         : "memory");
 }
 
+
+// Gather four rows r0..r3 of a 2D tensor (box {64 columns, 1 row}) into 4
+// consecutive 128-byte rows of shared memory, completing on an mbarrier that
+// may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const CUtensorMap* tm, int32_t x0,
+                                                 int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                                 uint32_t bar_cluster_addr) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(bar_cluster_addr)
+        : "memory");
+}
+
 // Tensor memory shared by a CTA pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
