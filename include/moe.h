@@ -308,6 +308,13 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
  * for checking, not for the hot path. */
 moe_status_t moe_get_device_status(void *ws, uint32_t *bits, void *stream);
 
+/* Self-test of the failure path: one kernel waits on an mbarrier that nothing
+ * signals, using the bounded wait of every kernel in this library, gives up
+ * after limit_ns (0 < limit_ns <= 10 s) and sets MOE_DEVERR_TIMEOUT in the
+ * device word *status.  The GPU context stays usable afterwards.  No fault,
+ * trap or hang is involved. */
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, uint32_t *status, void *stream);
+
 /* Static description of a status code. */
 const char *moe_status_string(moe_status_t s);
 

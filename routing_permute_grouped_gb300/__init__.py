@@ -98,6 +98,7 @@ def load():
         "moe_layer_fwd_prerouted": (ctypes.c_int,
                                     [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ, P]),
         "moe_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_last_error": (ctypes.c_char_p, []),
     }
@@ -254,6 +255,10 @@ def moe_get_device_status(ws, stream=None) -> int:
     if st not in (MOE_OK, 5):
         _check(st)
     return int(bits.value)
+
+
+def moe_selftest_wait_timeout(limit_ns: int, status, stream=None) -> None:
+    _check(load().moe_selftest_wait_timeout(limit_ns, _ptr(status), _stream(stream)))
 
 
 def moe_status_string(status: int) -> str:

@@ -67,6 +67,8 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
 
 int num_sms();
 
+cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
+
 constexpr int kMaxDevices = 64;
 
 // Records a printf-style message as this thread's last error (read by

@@ -462,6 +462,13 @@ moe_status_t moe_get_device_status(void* ws, uint32_t* bits, void* stream) {
     return v ? fail(MOE_ERR_DEVICE_CHECK, "device status bits 0x%x", v) : MOE_OK;
 }
 
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, uint32_t* status, void* stream) {
+    if (!status || limit_ns == 0 || limit_ns > 10000000000ull)
+        return fail(MOE_ERR_INVALID_ARG, "status must be non-null and 0 < limit_ns <= 10 s");
+    cudaError_t e = launch_wait_selftest(limit_ns, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "wait self-test");
+}
+
 const char* moe_status_string(moe_status_t s) {
     switch (s) {
         case MOE_OK: return "ok";

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -93,6 +94,26 @@ __global__ void __launch_bounds__(kPCWarps * 32)
         o.w = *reinterpret_cast<uint32_t*>(&p3);
         out[(int64_t)t * nvec + v] = o;
     }
+}
+
+// Waits on an mbarrier that nothing ever signals, with the bounded wait that
+// every kernel of the library uses; after limit_ns it records a timeout in
+// *status and returns, leaving the context usable.
+__global__ void k_wait_selftest(uint64_t limit_ns, uint32_t* status) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicOr(status, 0x2u);
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t stream) {
+    k_wait_selftest<<<1, 32, 0, stream>>>(limit_ns, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,

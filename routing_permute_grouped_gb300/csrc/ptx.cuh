@@ -57,7 +57,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // (without completing the wait) when *abort becomes non-zero or after
 // kWaitLimitNs; the caller then unwinds.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile uint32_t* abort) {
+                                          const volatile uint32_t* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -65,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }

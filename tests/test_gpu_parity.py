@@ -373,3 +373,21 @@ def test_grouped_gemm_gather_stage(name):
     assert_close(f64(h)[valid], eh[valid], "h")
     assert_close(f64(y)[valid], ey[valid], "y")
     assert (f64(y)[~valid] == 0).all() and (f64(h)[~valid] == 0).all()
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    # a kernel waits on a barrier that nothing signals: the bounded wait gives
+    # up, the timeout bit is set, and the next work on the stream runs normally
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    moe.moe_selftest_wait_timeout(50_000_000, status)  # 50 ms
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert int(status.item()) & moe.DEVERR_TIMEOUT
+    shape, inp, ref = prepared("tiny")
+    cfg, layer = make_layer(shape, inp)
+    out = layer(cuda(inp["x"]))
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert_close(f64(out), ref["out"], "out after a timed-out kernel")
