@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // past the segment's valid rows are computed but never stored.  Only real
 // visits are enumerated, so the round-robin over CTA pairs stays balanced.
 
-constexpr int kSched = 4;        // tile-id slots between the scheduler and the roles
+constexpr int kSched = 8;        // tile-id slots between the scheduler and the roles
 constexpr int kSchedTakers = 10; // MMA lane + 8 epilogue warps + the odd CTA's producer
 
 struct PairTile {
@@ -592,25 +592,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         uint32_t armed = 0, armed_par = 0;
+        // The even CTA's lane 0 picks the tiles and publishes each one a tile
+        // ahead of its use to every role of both CTAs, so no role waits on the
+        // cross-CTA hand-off at a tile boundary; the odd CTA's producer takes
+        // the ids like the other roles.
+        auto publish = [&](int it) -> int {  // even CTA, lane 0; -1 = abort
+            const int slot = it % kSched;
+            if (!mbar_wait_cluster(sempty + slot, ((it / kSched) & 1u) ^ 1u, abort_flag)) return -2;
+            const int next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
+                                               : cluster + it * nclusters;
+            const int t = next < total ? next : -1;
+            sched_tile[slot] = t;
+            st_cluster_u32(mapa_shared(smem_u32((const void*)(sched_tile + slot)), 1),
+                           static_cast<uint32_t>(t));
+            mbar_arrive(sfull + slot);
+            mbar_arrive_cluster(mapa_shared(smem_u32(sfull + slot), 1));
+            return t;
+        };
+        int next_t = 0;
+        if (lane == 0 && leader) next_t = publish(0);
         for (int it = 0; !timed_out; ++it) {
-            // the even CTA's lane 0 picks the next tile and publishes it to
-            // every role of both CTAs; the odd CTA's producer takes it
             int t = -1;
             bool ok = true;
             if (lane == 0) {
                 const int slot = it % kSched;
                 const uint32_t par = (it / kSched) & 1u;
                 if (leader) {
-                    ok = mbar_wait_cluster(sempty + slot, par ^ 1u, abort_flag);
-                    if (ok) {
-                        const int next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
-                                                           : cluster + it * nclusters;
-                        t = next < total ? next : -1;
-                        sched_tile[slot] = t;
-                        st_cluster_u32(mapa_shared(smem_u32((const void*)(sched_tile + slot)), 1),
-                                       static_cast<uint32_t>(t));
-                        mbar_arrive(sfull + slot);
-                        mbar_arrive_cluster(mapa_shared(smem_u32(sfull + slot), 1));
+                    t = next_t;
+                    ok = t != -2;
+                    if (ok && t >= 0) {
+                        next_t = publish(it + 1);
+                        ok = next_t != -2;
                     }
                 } else {
                     ok = mbar_wait_cluster(sfull + slot, par, abort_flag);
