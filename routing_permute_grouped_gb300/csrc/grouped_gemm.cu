@@ -697,7 +697,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool issued = false;
             for (int it = 0; !timed_out; ++it) {
                 const int slot = it % kSched;
-                if (!mbar_wait_cluster(sfull + slot, (it / kSched) & 1u, abort_flag)) {
+                // published by this CTA's producer: a CTA-scope wait suffices
+                if (!mbar_wait(sfull + slot, (it / kSched) & 1u, abort_flag)) {
                     timed_out = true;
                     break;
                 }
@@ -753,7 +754,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool got = true;
             if (lane == 0) {
                 const int slot = it % kSched;
-                got = mbar_wait_cluster(sfull + slot, (it / kSched) & 1u, abort_flag);
+                const uint32_t par = (it / kSched) & 1u;
+                got = leader ? mbar_wait(sfull + slot, par, abort_flag)
+                             : mbar_wait_cluster(sfull + slot, par, abort_flag);
                 if (got) {
                     t = sched_tile[slot];
                     mbar_arrive_cluster(mapa_shared(smem_u32(sempty + slot), 0));
