@@ -85,7 +85,7 @@ typedef struct {
  * so a caller can read them back.  All offsets are multiples of 1024. */
 typedef struct {
     size_t total;
-    size_t status;         /* uint32 device error word, tile counters, build scratch */
+    size_t status;         /* uint32 device error word + build scratch */
     size_t topk_idx;       /* int32 [T, k] */
     size_t topk_w;         /* fp32 [T, k] */
     size_t counts;         /* int32 [E] */
@@ -283,18 +283,11 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y, const int32_t *
 
 /* --------------------------------------------------------- whole layer -- */
 
-/* The whole forward pass of one layer, a1 .. a7, with no host
- * synchronisation.  ws must hold moe_workspace_size(cfg) bytes (layout in
- * moe_workspace_layout); its intermediates stay readable after the call.
- * Requires w->Wg_t; w->Ws13/Ws2 when cfg->d_shared > 0.
- *   x bf16 [T, d], out bf16 [T, d]; all device.
- * The shared expert reads only the token rows, so it is forked onto a
- * library-owned side stream (one per device, created with its two events on
- * the first call that needs it: make that call before any stream capture)
- * and runs beside the routing chain; the combine waits for it on `stream`.
- * Work ordered after the call on `stream` sees every result.  The grouped
- * GEMMs take tiles from counters in the workspace, reset at the start of
- * each call, so two calls that share one workspace must not overlap. */
+/* The whole forward pass of one layer: a1 .. a7 enqueued on one stream,
+ * no host synchronisation.  ws must hold moe_workspace_size(cfg) bytes
+ * (layout in moe_workspace_layout); its intermediates stay readable after
+ * the call.  Requires w->Wg_t; w->Ws13/Ws2 when cfg->d_shared > 0.
+ *   x bf16 [T, d], out bf16 [T, d]; all device. */
 moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
                            void *out, void *ws, size_t ws_bytes, void *stream);
 

@@ -453,9 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // past the segment's valid rows are computed but never stored.  Only real
 // visits are enumerated, so the round-robin over CTA pairs stays balanced.
 
-constexpr int kSched = 8;        // tile-id slots between the scheduler and the roles
-constexpr int kSchedTakers = 10; // MMA lane + 8 epilogue warps + the odd CTA's producer
-
 struct PairTile {
     int e, m0, hi, nb;  // rows [m0, m0 + hi) of the visit are valid
 };
@@ -515,11 +512,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* tfull = bars + 2 * S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* sfull = drain + 1;         // [kSched] tile id published (both CTAs)
-    uint64_t* sempty = sfull + kSched;   // [kSched] tile id taken by all roles (even CTA)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sempty + kSched);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = tmem_holder + 1;
-    volatile int* sched_tile = reinterpret_cast<volatile int*>(tmem_holder + 2);  // [kSched]
     int* vpref = reinterpret_cast<int*>(bars + 64);  // [E + 1]
 
     const int warp = threadIdx.x >> 5;
@@ -537,10 +531,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(tempty + i, 8);  // one arrival per epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
-        for (int i = 0; i < kSched; ++i) {
-            mbar_init(sfull + i, 1);
-            mbar_init(sempty + i, kSchedTakers);
-        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -592,53 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         uint32_t armed = 0, armed_par = 0;
-        // The even CTA's lane 0 picks the tiles and publishes each one a tile
-        // ahead of its use to every role of both CTAs, so no role waits on the
-        // cross-CTA hand-off at a tile boundary; the odd CTA's producer takes
-        // the ids like the other roles.
-        auto publish = [&](int it) -> int {  // even CTA, lane 0; -1 = abort
-            const int slot = it % kSched;
-            if (!mbar_wait_cluster(sempty + slot, ((it / kSched) & 1u) ^ 1u, abort_flag)) return -2;
-            const int next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
-                                               : cluster + it * nclusters;
-            const int t = next < total ? next : -1;
-            sched_tile[slot] = t;
-            st_cluster_u32(mapa_shared(smem_u32((const void*)(sched_tile + slot)), 1),
-                           static_cast<uint32_t>(t));
-            mbar_arrive(sfull + slot);
-            mbar_arrive_cluster(mapa_shared(smem_u32(sfull + slot), 1));
-            return t;
-        };
-        int next_t = 0;
-        if (lane == 0 && leader) next_t = publish(0);
-        for (int it = 0; !timed_out; ++it) {
-            int t = -1;
-            bool ok = true;
-            if (lane == 0) {
-                const int slot = it % kSched;
-                const uint32_t par = (it / kSched) & 1u;
-                if (leader) {
-                    t = next_t;
-                    ok = t != -2;
-                    if (ok && t >= 0) {
-                        next_t = publish(it + 1);
-                        ok = next_t != -2;
-                    }
-                } else {
-                    ok = mbar_wait_cluster(sfull + slot, par, abort_flag);
-                    if (ok) {
-                        t = sched_tile[slot];
-                        mbar_arrive_cluster(mapa_shared(smem_u32(sempty + slot), 0));
-                    }
-                }
-            }
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            t = __shfl_sync(0xFFFFFFFFu, t, 0);
-            if (!ok) {
-                timed_out = true;
-                break;
-            }
-            if (t < 0) break;
+        for (int t = cluster; t < total && !timed_out; t += nclusters) {
             const PairTile p = decode_pair(args, t, vpref);
             const int arow = p.m0 + BM * static_cast<int>(rank);
             const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
@@ -695,16 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t aph = 0;
             bool issued = false;
-            for (int it = 0; !timed_out; ++it) {
-                const int slot = it % kSched;
-                // published by this CTA's producer: a CTA-scope wait suffices
-                if (!mbar_wait(sfull + slot, (it / kSched) & 1u, abort_flag)) {
-                    timed_out = true;
-                    break;
-                }
-                const int t = sched_tile[slot];
-                mbar_arrive(sempty + slot);
-                if (t < 0) break;
+            for (int t = cluster; t < total && !timed_out; t += nclusters) {
                 if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag)) {
                     timed_out = true;
                     break;
@@ -749,26 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
-        for (int it = 0;; ++it) {
-            int t = -1;
-            bool got = true;
-            if (lane == 0) {
-                const int slot = it % kSched;
-                const uint32_t par = (it / kSched) & 1u;
-                got = leader ? mbar_wait(sfull + slot, par, abort_flag)
-                             : mbar_wait_cluster(sfull + slot, par, abort_flag);
-                if (got) {
-                    t = sched_tile[slot];
-                    mbar_arrive_cluster(mapa_shared(smem_u32(sempty + slot), 0));
-                }
-            }
-            got = __shfl_sync(0xFFFFFFFFu, got, 0);
-            t = __shfl_sync(0xFFFFFFFFu, t, 0);
-            if (!got) {
-                timed_out = true;
-                break;
-            }
-            if (t < 0) break;
+        for (int t = cluster; t < total; t += nclusters) {
             const PairTile p = decode_pair(args, t, vpref);
             const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
             if (!ok) {
@@ -868,7 +784,7 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
 
 template <int BN, int EPI, bool GATHER>
 static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
-                                 int max_visits, cudaStream_t stream, int cluster_cap) {
+                                 int max_visits, cudaStream_t stream) {
     constexpr int NT = kThreads;
     constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
@@ -891,7 +807,6 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
         max_clusters[dev] = n;
     }
     int clusters = max_clusters[dev];
-    if (cluster_cap > 0 && cluster_cap < clusters) clusters = cluster_cap;
     if (max_visits < clusters) clusters = max_visits;
     if (clusters <= 0) return cudaSuccess;
     k_grouped_gemm_pair<BN, EPI, GATHER><<<2 * clusters, NT, SMEM, stream>>>(tA, tB, args);
@@ -900,7 +815,7 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
 
 cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,
                                 int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
-                                cudaStream_t stream, int cluster_cap) {
+                                cudaStream_t stream) {
     CUtensorMap tA, tB;
     const bool pair = epi != kEpiRouter;
     const int a_box = epi == kEpiSwiGLUGather ? 1 : BM;  // gather4 reads one-row boxes
@@ -908,13 +823,13 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
         return cudaErrorInvalidValue;
     if (pair) {
         if (epi == kEpiSwiGLU && bn == 256)
-            return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, args, max_tiles, stream, cluster_cap);
+            return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, args, max_tiles, stream);
         if (epi == kEpiSwiGLUGather && bn == 256)
-            return launch_pair_t<256, kEpiSwiGLU, true>(tA, tB, args, max_tiles, stream, cluster_cap);
+            return launch_pair_t<256, kEpiSwiGLU, true>(tA, tB, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 256)
-            return launch_pair_t<256, kEpiGate, false>(tA, tB, args, max_tiles, stream, cluster_cap);
+            return launch_pair_t<256, kEpiGate, false>(tA, tB, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 128)
-            return launch_pair_t<128, kEpiGate, false>(tA, tB, args, max_tiles, stream, cluster_cap);
+            return launch_pair_t<128, kEpiGate, false>(tA, tB, args, max_tiles, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == kEpiSwiGLU) {

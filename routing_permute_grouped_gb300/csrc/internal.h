@@ -24,9 +24,6 @@ struct GemmArgs {
     const void* gather_x;
     const int32_t* row_src;
     int32_t gather_k;
-    // tile counter (zero at launch) for dynamic scheduling over CTA pairs;
-    // null = static round-robin
-    int32_t* tile_counter;
     int32_t dense_rows;             // rows when block_metadata is null
     int32_t n_tiles;                // N / BN
     int32_t k_blocks;               // K / 64
@@ -46,11 +43,9 @@ enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 
 
 // Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
 // [rowsB, K] bf16 (K-major), tile N = bn.  Returns a cudaError_t.
-// cluster_cap > 0 limits the CTA-pair kernels to that many pairs (leaving
-// SMs to kernels running concurrently on other streams).
 cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,
                                 int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
-                                cudaStream_t stream, int cluster_cap = 0);
+                                cudaStream_t stream);
 
 cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t A, int E, int P,
                            int64_t R_max, int32_t* counts, int32_t* padded_offsets,

@@ -6,7 +6,6 @@
 
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 #include "../../include/moe.h"
@@ -129,11 +128,6 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c) {
     return L;
 }
 
-// Byte offset, inside the status region of the layer workspace, of the four
-// tile counters of the grouped GEMMs (the status word is at 0, the offsets
-// scratch at 256).
-constexpr size_t kCounterOffset = 64;
-
 static size_t offsets_ws_bytes(const moe_config_t& c) {
     return 256 + static_cast<size_t>(sizes_of(c).chunks) * c.E * 4;
 }
@@ -189,10 +183,9 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
                                const void* W2_t, const int32_t* meta, const int32_t* nb,
                                const int32_t* po, const float* row_gate, void* h, void* y,
                                uint32_t* status, cudaStream_t st, const void* x = nullptr,
-                               const int32_t* row_src = nullptr, int32_t* counters = nullptr) {
+                               const int32_t* row_src = nullptr) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
-    a.tile_counter = counters;
     a.block_metadata = meta;
     a.num_blocks = nb;
     a.nb_cap = static_cast<int32_t>(s.NB);
@@ -224,7 +217,6 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.out = y;
     a.ldo = c.d;
     a.row_gate = row_gate;
-    a.tile_counter = counters ? counters + 1 : nullptr;
     e = launch_grouped_gemm(kEpiGate, bn2, h, s.R, W2_t, static_cast<int64_t>(c.E) * c.d, c.d_e, a,
                             static_cast<int>(s.NB * a.n_tiles), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2 (down + gate)");
@@ -232,9 +224,8 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
 
 static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
                               const void* Ws2_t, void* hs, void* ys, uint32_t* status,
-                              cudaStream_t st, int32_t* counters = nullptr, int cluster_cap = 0) {
+                              cudaStream_t st) {
     GemmArgs a{};
-    a.tile_counter = counters;
     a.dense_rows = c.T;
     a.status = status;
     a.block_rows = 256;
@@ -245,48 +236,17 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     a.ldo = c.d_shared;
     const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
-                                        mblocks * a.n_tiles, st, cluster_cap);
+                                        mblocks * a.n_tiles, st);
     if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_shared / 64;
     a.out = ys;
     a.ldo = c.d;
-    a.tile_counter = counters ? counters + 1 : nullptr;
     e = launch_grouped_gemm(kEpiGate, bn2, hs, c.T, Ws2_t, c.d, c.d_shared, a,
-                            mblocks * a.n_tiles, st, cluster_cap);
+                            mblocks * a.n_tiles, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "shared GEMM2");
 }
-
-// A non-blocking side stream and two events per device, created on first
-// use: the layer forks the shared expert onto it (the shared expert reads
-// only the token rows, so it runs while the routing chain runs) and joins
-// before the combine.
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-static std::mutex g_side_mu;
-static SideStream g_side[kMaxDevices];
-
-static moe_status_t side_stream(SideStream** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
-    SideStream& ss = g_side[dev];
-    if (!ss.stream) {
-        e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(e, "creating the side stream");
-    }
-    *out = &ss;
-    return MOE_OK;
-}
-
-// Pairs of CTAs left to the routing chain while the shared expert runs beside it.
-constexpr int kRoutingPairs = 16;
 
 static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
                           const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
@@ -308,27 +268,8 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     uint8_t* b = static_cast<uint8_t*>(ws);
     auto at = [&](size_t o) { return static_cast<void*>(b + o); };
     uint32_t* status = static_cast<uint32_t*>(at(L.status));
-    int32_t* counters = reinterpret_cast<int32_t*>(b + L.status + kCounterOffset);  // 4 tile counters
     int32_t* topk_idx = static_cast<int32_t*>(at(L.topk_idx));
     float* topk_w = static_cast<float*>(at(L.topk_w));
-    cudaError_t e = cudaMemsetAsync(counters, 0, 4 * sizeof(int32_t), st);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the tile counters");
-    std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
-    SideStream* side = nullptr;
-    if (c.d_shared) {
-        lock.lock();  // the fork/join events are shared by all calls on this device
-        r = side_stream(&side);
-        if (r != MOE_OK) return r;
-        e = cudaEventRecord(side->fork, st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-        if (e != cudaSuccess) return cuda_fail(e, "forking the shared expert");
-        const int cap = max(1, num_sms() / 2 - kRoutingPairs);
-        r = do_shared(c, x, w->Ws13, w->Ws2, at(L.hs), at(L.ys), status, side->stream, counters + 2,
-                      cap);
-        if (r != MOE_OK) return r;
-        e = cudaEventRecord(side->join, side->stream);
-        if (e != cudaSuccess) return cuda_fail(e, "recording the shared expert");
-    }
     if (routed) {
         r = do_route(c, x, w->Wg_t, w->bias, topk_idx, topk_w, st);
         if (r != MOE_OK) return r;
@@ -344,16 +285,16 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
                    static_cast<int32_t*>(at(L.padded_offsets)), meta, nb, perm_row,
                    static_cast<int32_t*>(at(L.row_src)), row_gate, at(L.status), st);
     if (r != MOE_OK) return r;
-    e = launch_permute(x, perm_row, at(L.x_perm), c.T, c.d, c.k, st);
+    cudaError_t e = launch_permute(x, perm_row, at(L.x_perm), c.T, c.d, c.k, st);
     if (e != cudaSuccess) return cuda_fail(e, "permute");
     r = do_experts(c, at(L.x_perm), w->W13, w->W2, meta, nb,
                    static_cast<const int32_t*>(at(L.padded_offsets)), row_gate, at(L.h), at(L.y),
-                   status, st, nullptr, nullptr, counters);
+                   status, st);
     if (r != MOE_OK) return r;
     const void* shared = nullptr;
     if (c.d_shared) {
-        e = cudaStreamWaitEvent(st, side->join, 0);
-        if (e != cudaSuccess) return cuda_fail(e, "joining the shared expert");
+        r = do_shared(c, x, w->Ws13, w->Ws2, at(L.hs), at(L.ys), status, st);
+        if (r != MOE_OK) return r;
         shared = at(L.ys);
     }
     e = launch_combine(at(L.y), perm_row, shared, out, c.T, c.d, c.k, st);
