@@ -60,39 +60,64 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
     }
 }
 
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+    uint4 o;
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&p0);
+    o.y = *reinterpret_cast<uint32_t*>(&p1);
+    o.z = *reinterpret_cast<uint32_t*>(&p2);
+    o.w = *reinterpret_cast<uint32_t*>(&p3);
+    return o;
+}
+
+// Each lane handles two 16-byte vectors per iteration, so up to 2 * (K + 1)
+// independent loads are in flight per lane before the first add; K is a
+// template parameter so the load buffers take only the registers they need.
+template <int K>
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ perm_row,
-              const uint4* __restrict__ shared_out, uint4* __restrict__ out, int T, int nvec, int k) {
+              const uint4* __restrict__ shared_out, uint4* __restrict__ out, int T, int nvec) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
-    int rows[8];
+    int rows[K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(perm_row + (int64_t)t * k + j) : -1;
-    for (int v = lane; v < nvec; v += 32) {
-        uint4 in[8];
+    for (int j = 0; j < K; ++j) rows[j] = __ldg(perm_row + (int64_t)t * K + j);
+    for (int v0 = lane; v0 < nvec; v0 += 64) {
+        const int v1 = v0 + 32;
+        const bool has1 = v1 < nvec;
+        uint4 in0[K], in1[K];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (rows[j] >= 0) in[j] = __ldg(y + (int64_t)rows[j] * nvec + v);
-        uint4 sh = make_uint4(0, 0, 0, 0);
-        if (shared_out) sh = __ldg(shared_out + (int64_t)t * nvec + v);
-        float acc[8];
+        for (int j = 0; j < K; ++j) {
+            if (rows[j] >= 0) {
+                const uint4* src = y + (int64_t)rows[j] * nvec;
+                in0[j] = __ldg(src + v0);
+                if (has1) in1[j] = __ldg(src + v1);
+            }
+        }
+        uint4 sh0 = make_uint4(0, 0, 0, 0), sh1 = make_uint4(0, 0, 0, 0);
+        if (shared_out) {
+            sh0 = __ldg(shared_out + (int64_t)t * nvec + v0);
+            if (has1) sh1 = __ldg(shared_out + (int64_t)t * nvec + v1);
+        }
+        float a0[8], a1[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) a0[i] = a1[i] = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (rows[j] >= 0) add_bf16x8(acc, in[j]);
-        if (shared_out) add_bf16x8(acc, sh);
-        uint4 o;
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
-        __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
-        o.x = *reinterpret_cast<uint32_t*>(&p0);
-        o.y = *reinterpret_cast<uint32_t*>(&p1);
-        o.z = *reinterpret_cast<uint32_t*>(&p2);
-        o.w = *reinterpret_cast<uint32_t*>(&p3);
-        out[(int64_t)t * nvec + v] = o;
+        for (int j = 0; j < K; ++j)
+            if (rows[j] >= 0) {
+                add_bf16x8(a0, in0[j]);
+                if (has1) add_bf16x8(a1, in1[j]);
+            }
+        if (shared_out) {
+            add_bf16x8(a0, sh0);
+            add_bf16x8(a1, sh1);
+        }
+        __stcs(out + (int64_t)t * nvec + v0, pack_bf16x8(a0));
+        if (has1) __stcs(out + (int64_t)t * nvec + v1, pack_bf16x8(a1));
     }
 }
 
@@ -129,9 +154,17 @@ cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* s
                            void* out, int T, int d, int k, cudaStream_t stream) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    k_combine<<<grid, kPCWarps * 32, 0, stream>>>(static_cast<const uint4*>(y), perm_row,
-                                                  static_cast<const uint4*>(shared_out),
-                                                  static_cast<uint4*>(out), T, nvec, k);
+    const uint4* y4 = static_cast<const uint4*>(y);
+    const uint4* s4 = static_cast<const uint4*>(shared_out);
+    uint4* o4 = static_cast<uint4*>(out);
+    switch (k) {
+#define MOE_COMBINE_K(KK) \
+    case KK: k_combine<KK><<<grid, kPCWarps * 32, 0, stream>>>(y4, perm_row, s4, o4, T, nvec); break;
+        MOE_COMBINE_K(1) MOE_COMBINE_K(2) MOE_COMBINE_K(3) MOE_COMBINE_K(4)
+        MOE_COMBINE_K(5) MOE_COMBINE_K(6) MOE_COMBINE_K(7) MOE_COMBINE_K(8)
+#undef MOE_COMBINE_K
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
