@@ -582,6 +582,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         uint32_t armed = 0, armed_par = 0;
+        // an expert's weight panels are re-read by every visit of that
+        // expert: keep them in L2 ahead of the streamed activation rows
+        const uint64_t keep = l2_policy_evict_last();
         for (int t = cluster; t < total && !timed_out; t += nclusters) {
             const PairTile p = decode_pair(args, t, vpref);
             const int arow = p.m0 + BM * static_cast<int>(rank);
@@ -609,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     armed &= ~(1u << s);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
                     if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
-                    tma_load_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader);
+                    tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader, keep);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                 }

@@ -241,6 +241,25 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const CUtens
         : "memory");
 }
 
+
+// L2 cache policy that keeps the lines it loads resident in preference to
+// others (for operands that many CTAs re-read over the kernel's lifetime).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* smem_dst, const CUtensorMap* tm,
+                                                      int32_t x0, int32_t y0,
+                                                      uint32_t bar_cluster_addr, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x0), "r"(y0), "r"(bar_cluster_addr), "l"(policy)
+        : "memory");
+}
+
 // Tensor memory shared by a CTA pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
