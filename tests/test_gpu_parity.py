@@ -391,3 +391,63 @@ def test_bounded_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert layer.device_status() == 0
     assert_close(f64(out), ref["out"], "out after a timed-out kernel")
+
+
+def test_layer_captures_into_a_cuda_graph():
+    # the whole layer enqueues kernels only (no host sync, no allocation), so
+    # it can be recorded once and replayed: the replay equals the eager call
+    shape, inp, ref = prepared("small_default")
+    cfg, layer = make_layer(shape, inp)
+    x = cuda(inp["x"])
+    out = torch.empty_like(x)
+    eager = layer(x).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(x, out, stream=s)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer(x, out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    x.copy_(cuda(torch.flip(inp["x"], dims=[0])))  # new tokens, same graph
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, layer(x).clone())
+
+
+EDGE = {
+    "one_token": MoeShape("one_token", T=1, d=256, d_e=128, E=8, k=2, d_shared=128, seed=91),
+    "k_equals_E": MoeShape("k_equals_E", T=130, d=256, d_e=128, E=4, k=4, seed=92),
+    "single_expert": MoeShape("single_expert", T=300, d=384, d_e=256, E=1, k=1, seed=93),
+    "hot_expert": MoeShape("hot_expert", T=700, d=256, d_e=128, E=16, k=2, bias_std=0.0, seed=94),
+    "groups_keep_one": MoeShape("groups_keep_one", T=200, d=256, d_e=128, E=32, k=4, n_groups=4,
+                                topk_groups=1, seed=95),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_case_layers(name):
+    shape = EDGE[name]
+    inp = synth.make_inputs(shape)
+    if name == "hot_expert":
+        # a large bias sends every token's first choice to expert 3
+        inp["bias"] = torch.zeros(shape.E)
+        inp["bias"][3] = 50.0
+    enforce_margin(inp, shape)
+    ref = oracle.layer_forward(oracle_inputs(inp), shape)
+    cfg, layer = make_layer(shape, inp)
+    out = layer(cuda(inp["x"]))
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    T, k, E = shape.T, shape.k, shape.E
+    assert np.array_equal(layer.buffer("topk_idx", torch.int32, (T, k)).cpu().numpy(),
+                          ref["topk_idx"])
+    assert np.array_equal(layer.buffer("counts", torch.int32, (E,)).cpu().numpy(), ref["counts"])
+    if name == "hot_expert":
+        assert ref["counts"][3] == T
+    assert_close(f64(out), ref["out"], "out")
