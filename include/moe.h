@@ -100,6 +100,7 @@ typedef struct {
     size_t y;              /* bf16 [R_max, d] */
     size_t hs;             /* bf16 [T, d_shared] */
     size_t ys;             /* bf16 [T, d] */
+    size_t router_partial; /* fp32 [S, T, E] split-K router logits (S > 1 only) */
 } moe_workspace_layout_t;
 
 /* ---------------------------------------------------------------- sizes -- */
@@ -287,7 +288,11 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y, const int32_t *
  * no host synchronisation.  ws must hold moe_workspace_size(cfg) bytes
  * (layout in moe_workspace_layout); its intermediates stay readable after
  * the call.  Requires w->Wg_t; w->Ws13/Ws2 when cfg->d_shared > 0.
- *   x bf16 [T, d], out bf16 [T, d]; all device. */
+ *   x bf16 [T, d], out bf16 [T, d]; all device.
+ * When the batch has too few 128-token tiles to fill the GPU (decode sizes),
+ * the router GEMM splits K into up to 16 slices whose fp32 partial logits
+ * (workspace region router_partial) a second kernel sums in slice order
+ * before the top-k; otherwise it is the single kernel of moe_route. */
 moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
                            void *out, void *ws, size_t ws_bytes, void *stream);
 

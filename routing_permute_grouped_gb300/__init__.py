@@ -53,7 +53,7 @@ class MoeWeights(ctypes.Structure):
 
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
                   "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
-                  "y", "hs", "ys")
+                  "y", "hs", "ys", "router_partial")
 
 
 class _Layout(ctypes.Structure):

@@ -254,6 +254,26 @@ __device__ __forceinline__ void epi_router(const GemmArgs& a, const TileInfo& ti
     }
 }
 
+// Split-K router: fp32 partial logits of this K slice for the token rows of
+// the tile, columns [0, E).
+template <int BN>
+__device__ __forceinline__ void epi_partial(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                            int row) {
+    const bool valid = row >= ti.lo && row < ti.hi;
+    float* dst = a.partial + (static_cast<int64_t>(ti.nb) * a.dense_rows + ti.m0 + row) * a.E;
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (c * 16 + i < a.E) dst[c * 16 + i] = __uint_as_float(v[i]);
+        }
+    }
+}
+
 // -------------------------------------------------------------- kernel --
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -318,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
                 const TileInfo ti = decode_tile(args, t, nblocks);
                 if (ti.skip) continue;
-                const int brow = ti.e * args.b_rows_per_expert + ti.nb * BN;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                const bool split = EPI == kEpiPartial;
+                const int brow = split ? 0 : ti.e * args.b_rows_per_expert + ti.nb * BN;
+                const int kb0 = split ? ti.nb * args.k_per_split : 0;
+                const int kb1 = split ? min(kb0 + args.k_per_split, args.k_blocks) : args.k_blocks;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
                         timed_out = true;
                         break;
@@ -356,14 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t aph = 0;
             bool issued = false;
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-                if (decode_tile(args, t, nblocks).skip) continue;
+                const TileInfo ti = decode_tile(args, t, nblocks);
+                if (ti.skip) continue;
+                const int kb0 = EPI == kEpiPartial ? ti.nb * args.k_per_split : 0;
+                const int kb1 = EPI == kEpiPartial ? min(kb0 + args.k_per_split, args.k_blocks)
+                                                   : args.k_blocks;
                 if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag)) {
                     timed_out = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full + s, ph, abort_flag)) {
                         timed_out = true;
                         break;
@@ -374,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         mma_bf16(d_tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
-                                 idesc, (kb | kk) != 0 ? 1u : 0u);
+                                 idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
                     mma_commit(empty + s);
@@ -418,6 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epi_swiglu(args, ti, taddr, row);
             } else if constexpr (EPI == kEpiGate) {
                 epi_gate<BN>(args, ti, taddr, row);
+            } else if constexpr (EPI == kEpiPartial) {
+                epi_partial<BN>(args, ti, taddr, row);
             } else {
                 epi_router<BN>(args, ti, taddr, row);
             }
@@ -820,7 +849,7 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
                                 int64_t rowsB, int64_t K, const GemmArgs& args, int max_tiles,
                                 cudaStream_t stream) {
     CUtensorMap tA, tB;
-    const bool pair = epi != kEpiRouter;
+    const bool pair = epi != kEpiRouter && epi != kEpiPartial;
     const int a_box = epi == kEpiSwiGLUGather ? 1 : BM;  // gather4 reads one-row boxes
     if (!make_tmap(&tA, A, rowsA, K, a_box) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
         return cudaErrorInvalidValue;
@@ -840,6 +869,15 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
     } else if (epi == kEpiGate) {
         if (bn == 256) return launch_t<256, kEpiGate>(tA, tB, args, max_tiles, stream);
         if (bn == 128) return launch_t<128, kEpiGate>(tA, tB, args, max_tiles, stream);
+    } else if (epi == kEpiPartial) {
+        switch (bn) {
+            case 16: return launch_t<16, kEpiPartial>(tA, tB, args, max_tiles, stream);
+            case 32: return launch_t<32, kEpiPartial>(tA, tB, args, max_tiles, stream);
+            case 64: return launch_t<64, kEpiPartial>(tA, tB, args, max_tiles, stream);
+            case 128: return launch_t<128, kEpiPartial>(tA, tB, args, max_tiles, stream);
+            case 256: return launch_t<256, kEpiPartial>(tA, tB, args, max_tiles, stream);
+            default: break;
+        }
     } else if (epi == kEpiRouter) {
         switch (bn) {
             case 16: return launch_t<16, kEpiRouter>(tA, tB, args, max_tiles, stream);

@@ -24,6 +24,11 @@ struct GemmArgs {
     const void* gather_x;
     const int32_t* row_src;
     int32_t gather_k;
+    // split-K router (kEpiPartial): tile nb covers k-blocks
+    // [nb * k_per_split, (nb + 1) * k_per_split); fp32 partial logits go to
+    // partial[(nb * dense_rows + row) * E + e]
+    int32_t k_per_split;
+    float* partial;
     int32_t dense_rows;             // rows when block_metadata is null
     int32_t n_tiles;                // N / BN
     int32_t k_blocks;               // K / 64
@@ -39,7 +44,7 @@ struct GemmArgs {
     float* topk_w;
 };
 
-enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 3 };
+enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 3, kEpiPartial = 4 };
 
 // Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
 // [rowsB, K] bf16 (K-major), tile N = bn.  Returns a cudaError_t.
@@ -66,6 +71,12 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
                                   cudaStream_t stream);
 
 int num_sms();
+
+// Sums S fp32 partial-logit slices in slice order, adds the bias and does the
+// (group-limited) top-k and softmax of each token.
+cudaError_t launch_router_reduce(const float* partial, int S, int T, int E, int k, int n_groups,
+                                 int topk_groups, const float* bias, int32_t* topk_idx,
+                                 float* topk_w, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 

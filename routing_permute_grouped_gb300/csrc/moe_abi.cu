@@ -100,6 +100,19 @@ static moe_status_t check_cfg(const moe_config_t* c, bool routed) {
     return MOE_OK;
 }
 
+// K slices of the layer's router GEMM: enough 128-token tiles x slices to
+// cover the GPU (about 128 CTAs) when the batch is small, at most 16, and
+// never an empty slice.  1 = the fused single-kernel router.
+static int router_splits(const moe_config_t& c) {
+    const int m_tiles = (c.T + 127) / 128;
+    const int k_blocks = c.d / 64;
+    int S = m_tiles > 0 ? 128 / m_tiles : 1;
+    S = S < 1 ? 1 : (S > 16 ? 16 : S);
+    if (S > k_blocks) S = k_blocks;
+    const int per = (k_blocks + S - 1) / S;
+    return (k_blocks + per - 1) / per;
+}
+
 static moe_workspace_layout_t layout_of(const moe_config_t& c) {
     const Sizes s = sizes_of(c);
     moe_workspace_layout_t L{};
@@ -124,6 +137,8 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c) {
     L.y = take(static_cast<size_t>(s.R) * c.d * 2);
     L.hs = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d_shared : 0) * 2);
     L.ys = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
+    const int S = router_splits(c);
+    L.router_partial = take(S > 1 ? static_cast<size_t>(S) * c.T * c.E * 4 : 0);
     L.total = off;
     return L;
 }
@@ -161,6 +176,29 @@ static moe_status_t do_route(const moe_config_t& c, const void* x, const void* W
     cudaError_t e = launch_grouped_gemm(kEpiRouter, router_bn(c.E), x, c.T, Wg_t, c.E, c.d, a,
                                         tiles, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router GEMM");
+}
+
+// The layer's router: fused (top-k in the GEMM epilogue) when the batch
+// fills the GPU, otherwise split-K partial logits + a reduce/top-k kernel.
+static moe_status_t do_route_layer(const moe_config_t& c, const void* x, const void* Wg_t,
+                                   const float* bias, int32_t* topk_idx, float* topk_w,
+                                   float* partial, cudaStream_t st) {
+    const int S = router_splits(c);
+    if (S <= 1) return do_route(c, x, Wg_t, bias, topk_idx, topk_w, st);
+    GemmArgs a{};
+    a.dense_rows = c.T;
+    a.n_tiles = S;
+    a.k_blocks = c.d / 64;
+    a.k_per_split = (a.k_blocks + S - 1) / S;
+    a.E = c.E;
+    a.partial = partial;
+    const int tiles = ((c.T + 127) / 128) * S;
+    cudaError_t e = launch_grouped_gemm(kEpiPartial, router_bn(c.E), x, c.T, Wg_t, c.E, c.d, a,
+                                        tiles, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router GEMM (split K)");
+    e = launch_router_reduce(partial, S, c.T, c.E, c.k, c.n_groups, c.topk_groups, bias, topk_idx,
+                             topk_w, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router reduce");
 }
 
 static moe_status_t do_offsets(const moe_config_t& c, const int32_t* topk_idx, const float* topk_w,
@@ -271,7 +309,8 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     int32_t* topk_idx = static_cast<int32_t*>(at(L.topk_idx));
     float* topk_w = static_cast<float*>(at(L.topk_w));
     if (routed) {
-        r = do_route(c, x, w->Wg_t, w->bias, topk_idx, topk_w, st);
+        r = do_route_layer(c, x, w->Wg_t, w->bias, topk_idx, topk_w,
+                           static_cast<float*>(at(L.router_partial)), st);
         if (r != MOE_OK) return r;
     } else {
         topk_idx = const_cast<int32_t*>(pre_idx);
