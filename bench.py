@@ -278,6 +278,8 @@ def run_ours(args, shape, rank, world, local):
     hs = buf("hs", bf, (T, ds)) if ds else None
     ys = buf("ys", bf, (T, d)) if ds else None
     status_word = buf("status", i32, (1,))
+    nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
+    router_partial = buf("router_partial", f32, (nsplit,)) if nsplit else None
     offs_ws = ws[L["status"]:L["topk_idx"]]
 
     stage_names = ["route", "offsets", "permute", "grouped_gemm", "shared", "combine"]
@@ -286,7 +288,8 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[0].record()
         if not shape.prerouted:
-            moe.moe_route(cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w)
+            # the router the layer runs: split-K for small batches
+            moe.moe_route_splitk(cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w, router_partial)
         if ev is not None:
             ev[1].record()
         moe.moe_build_offsets(cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src,
@@ -313,10 +316,11 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[6].record()
 
-    # kernels per layer forward: router, 3 offsets kernels, permute (or none
-    # when fused), 2 routed GEMMs, 2 shared-expert GEMMs, combine
-    launches_per_step = ((0 if shape.prerouted else 1) + 3 + (1 if args.permute == "separate" else 0)
-                         + 2 + (2 if ds else 0) + 1)
+    # kernels per layer forward: router (2 when split-K), 3 offsets kernels,
+    # permute (or none when fused), 2 routed GEMMs, 2 shared-expert GEMMs,
+    # combine
+    launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + 3
+                         + (1 if args.permute == "separate" else 0) + 2 + (2 if ds else 0) + 1)
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():

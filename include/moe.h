@@ -153,6 +153,19 @@ moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void *W1, 
 moe_status_t moe_route(const moe_config_t *cfg, const void *x, const void *Wg_t,
                        const float *bias, int32_t *topk_idx, float *topk_w, void *stream);
 
+/* a1 for small batches: the router GEMM with K split into S slices (S from
+ * the config: enough slices that the 128-token tiles x slices cover the GPU,
+ * at most 16) writes fp32 partial logits to `partial`; a second kernel sums
+ * them in slice order, adds the bias and does the same group-limited top-k
+ * and softmax as moe_route.  Returns the same outputs as moe_route.  When
+ * moe_route_splitk_scratch_size(cfg) is 0 (the batch already fills the GPU)
+ * it runs moe_route's single kernel and ignores `partial`.
+ *   partial  fp32 [S, T, E] device scratch, partial_bytes >= the size above */
+size_t moe_route_splitk_scratch_size(const moe_config_t *cfg);
+moe_status_t moe_route_splitk(const moe_config_t *cfg, const void *x, const void *Wg_t,
+                              const float *bias, int32_t *topk_idx, float *topk_w, float *partial,
+                              size_t partial_bytes, void *stream);
+
 /* a2. Counts, padded offsets and the block table ("MoE & MLA operators",
  * sec. 2.3: padded offsets with padding_M = 128 and
  * block_metadata[total_m_blocks, 3] = [expert, m_start, valid_m]; "Dropless

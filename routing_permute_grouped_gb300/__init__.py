@@ -25,7 +25,8 @@ from . import build as _build
 __all__ = [
     "MoeError", "MoeConfig", "MoeWeights", "MoeLayer", "config_of", "load",
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
-    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
+    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_route_splitk",
+    "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
 ]
@@ -87,6 +88,8 @@ def load():
         "moe_pack_router": (ctypes.c_int, [I32, I32, P, P, P]),
         "moe_pack_experts": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P]),
         "moe_route": (ctypes.c_int, [CP, P, P, P, P, P, P]),
+        "moe_route_splitk_scratch_size": (SZ, [CP]),
+        "moe_route_splitk": (ctypes.c_int, [CP, P, P, P, P, P, P, SZ, P]),
         "moe_build_offsets": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_build_offsets_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
@@ -181,6 +184,17 @@ def moe_pack_experts(W1, W3, W2, W13, W2_t, stream=None) -> None:
 def moe_route(cfg, x, Wg_t, bias, topk_idx, topk_w, stream=None) -> None:
     _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg_t), _ptr(bias), _ptr(topk_idx),
                             _ptr(topk_w), _stream(stream)))
+
+
+def moe_route_splitk_scratch_size(cfg) -> int:
+    return int(load().moe_route_splitk_scratch_size(ctypes.byref(cfg)))
+
+
+def moe_route_splitk(cfg, x, Wg_t, bias, topk_idx, topk_w, partial, stream=None) -> None:
+    nbytes = 0 if partial is None else partial.numel() * partial.element_size()
+    _check(load().moe_route_splitk(ctypes.byref(cfg), _ptr(x), _ptr(Wg_t), _ptr(bias),
+                                   _ptr(topk_idx), _ptr(topk_w), _ptr(partial), nbytes,
+                                   _stream(stream)))
 
 
 def moe_build_offsets(cfg, topk_idx, topk_w, counts, padded_offsets, block_metadata, num_blocks,

@@ -395,6 +395,27 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg_t,
     return do_route(*cfg, x, Wg_t, bias, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_route_splitk_scratch_size(const moe_config_t* cfg) {
+    if (check_cfg(cfg, true) != MOE_OK) return 0;
+    const int S = router_splits(*cfg);
+    return S > 1 ? static_cast<size_t>(S) * cfg->T * cfg->E * 4 : 0;
+}
+
+moe_status_t moe_route_splitk(const moe_config_t* cfg, const void* x, const void* Wg_t,
+                              const float* bias, int32_t* topk_idx, float* topk_w, float* partial,
+                              size_t partial_bytes, void* stream) {
+    moe_status_t r = check_cfg(cfg, true);
+    if (r != MOE_OK) return r;
+    if (!x || !Wg_t || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    const size_t need = moe_route_splitk_scratch_size(cfg);
+    if (need && (!partial || partial_bytes < need))
+        return fail(MOE_ERR_WORKSPACE, "split-K router scratch of %zu bytes, %zu needed",
+                    partial_bytes, need);
+    if (cfg->T == 0) return MOE_OK;
+    return do_route_layer(*cfg, x, Wg_t, bias, topk_idx, topk_w, partial,
+                          static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_build_offsets(const moe_config_t* cfg, const int32_t* topk_idx,
                                const float* topk_w, int32_t* counts, int32_t* padded_offsets,
                                int32_t* block_metadata, int32_t* num_blocks, int32_t* perm_row,

@@ -157,6 +157,15 @@ def test_route_stage(name):
     moe.moe_route(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(w.cpu().double().numpy(), ref["topk_w"], rtol=0, atol=2e-5)
+    # the split-K router (partial logits + reduce/top-k kernel) decides the same
+    nbytes = moe.moe_route_splitk_scratch_size(cfg)
+    assert nbytes > 0  # these batches are small enough to split
+    partial = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    idx.fill_(-7)
+    w.zero_()
+    moe.moe_route_splitk(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w, partial)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(w.cpu().double().numpy(), ref["topk_w"], rtol=0, atol=2e-5)
 
 
 def _offsets_case(idx, w, E, P):
