@@ -316,10 +316,11 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[6].record()
 
-    # kernels per layer forward: router (2 when split-K), 3 offsets kernels,
+    # kernels per layer forward: router (2 when split-K), offsets (1 or 3),
     # permute (or none when fused), 2 routed GEMMs, 2 shared-expert GEMMs,
     # combine
-    launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + 3
+    offsets_launches = 1 if A <= 4096 else 3  # one-CTA offsets kernel for small batches
+    launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
                          + (1 if args.permute == "separate" else 0) + 2 + (2 if ds else 0) + 1)
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 

@@ -14,7 +14,8 @@
 //                    perm_row, row_src, row_gate
 // Ranks depend only on the assignment order, never on atomic ordering, so the
 // permutation is deterministic and rows of a segment stay in ascending
-// assignment order.
+// assignment order.  Batches of at most 4096 assignments run all three steps
+// in one CTA (one launch).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -166,11 +167,136 @@ __global__ void __launch_bounds__(kScatterThreads)
     }
 }
 
+// Small batches (A <= kSmallA): the three steps above in one CTA of 1024
+// threads, so a decode step pays one launch instead of three.
+constexpr int kSmallA = 4096;
+constexpr int kSmallThreads = 1024;
+
+__global__ void __launch_bounds__(kSmallThreads)
+    k_offsets_small(const int32_t* __restrict__ idx, const float* __restrict__ w, int A, int E, int P,
+                    int64_t R_max, int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets,
+                    int32_t* __restrict__ block_metadata, int32_t* __restrict__ num_blocks,
+                    int32_t* __restrict__ perm_row, int32_t* __restrict__ row_src,
+                    float* __restrict__ row_gate, uint32_t* status) {
+    constexpr int W = kSmallThreads / 32;
+    __shared__ int hist[kMaxE];
+    __shared__ int s_size[kMaxE];
+    __shared__ int s_nblk[kMaxE];
+    __shared__ int running[kMaxE];
+    __shared__ int wcnt[W][kMaxE];
+    __shared__ int s_total[2];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = tid; e < E; e += blockDim.x) {
+        hist[e] = 0;
+        for (int i = 0; i < W; ++i) wcnt[i][e] = 0;
+    }
+    __syncthreads();
+    bool bad = false;
+    for (int a = tid; a < A; a += blockDim.x) {
+        const int e = __ldg(idx + a);
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[e], 1);
+        else
+            bad = true;
+    }
+    if (bad && status) atomicOr(status, kDevErrExpert);
+    __syncthreads();
+    int cnt = 0;
+    if (tid < E) {
+        cnt = hist[tid];
+        s_size[tid] = ((cnt + P - 1) / P) * P;
+        s_nblk[tid] = (cnt + P - 1) / P;
+    }
+    __syncthreads();
+    for (int off = 1; off < E; off <<= 1) {
+        int vs = 0, vb = 0;
+        if (tid < E && tid >= off) {
+            vs = s_size[tid - off];
+            vb = s_nblk[tid - off];
+        }
+        __syncthreads();
+        if (tid < E && tid >= off) {
+            s_size[tid] += vs;
+            s_nblk[tid] += vb;
+        }
+        __syncthreads();
+    }
+    if (tid == E - 1) {
+        s_total[0] = s_size[tid];
+        s_total[1] = s_nblk[tid];
+    }
+    __syncthreads();
+    if (tid < E) {
+        const int size = ((cnt + P - 1) / P) * P;
+        const int nblk = (cnt + P - 1) / P;
+        const int po = s_size[tid] - size;
+        const int b0 = s_nblk[tid] - nblk;
+        counts[tid] = cnt;
+        padded_offsets[tid] = po;
+        if (tid == E - 1) padded_offsets[E] = s_total[0];
+        running[tid] = po;
+        for (int i = 0; i < nblk; ++i) {
+            block_metadata[3 * (b0 + i) + 0] = tid;
+            block_metadata[3 * (b0 + i) + 1] = po + i * P;
+            block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
+        }
+        for (int r = po + cnt; r < po + size; ++r) {
+            row_src[r] = -1;
+            row_gate[r] = 0.0f;
+        }
+    }
+    if (tid == 0) *num_blocks = s_total[1];
+    for (int64_t r = s_total[0] + tid; r < R_max; r += blockDim.x) {
+        row_src[r] = -1;
+        row_gate[r] = 0.0f;
+    }
+    __syncthreads();
+    // stable ranks, 1024 assignments at a time in assignment order
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = 0; base < A; base += kSmallThreads) {
+        const int a = base + tid;
+        int e = -1;
+        if (a < A) {
+            e = __ldg(idx + a);
+            if (e < 0 || e >= E) {
+                perm_row[a] = -1;
+                e = -1;
+            }
+        }
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & lt_mask);
+        const bool leader = rank == 0;
+        if (e >= 0 && leader) wcnt[warp][e] = __popc(peers);
+        __syncthreads();
+        if (e >= 0) {
+            int off = 0;
+            for (int i = 0; i < warp; ++i) off += wcnt[i][e];
+            const int r = running[e] + off + rank;
+            perm_row[a] = r;
+            row_src[r] = a;
+            row_gate[r] = w ? __ldg(w + a) : 1.0f;
+        }
+        __syncthreads();
+        if (e >= 0 && leader) {
+            atomicAdd(&running[e], __popc(peers));
+            wcnt[warp][e] = 0;
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t A, int E, int P,
                            int64_t R_max, int32_t* counts, int32_t* padded_offsets,
                            int32_t* block_metadata, int32_t* num_blocks, int32_t* perm_row,
                            int32_t* row_src, float* row_gate, uint32_t* status,
                            int32_t* chunk_scratch, cudaStream_t stream) {
+    if (A <= kSmallA) {
+        k_offsets_small<<<1, kSmallThreads, 0, stream>>>(topk_idx, topk_w, static_cast<int>(A), E, P,
+                                                         R_max, counts, padded_offsets,
+                                                         block_metadata, num_blocks, perm_row,
+                                                         row_src, row_gate, status);
+        return cudaGetLastError();
+    }
     const int n_chunks = static_cast<int>(offsets_num_chunks(A));
     if (n_chunks > 0) {
         k_chunk_hist<<<n_chunks, kScatterThreads, 0, stream>>>(topk_idx, A, E, chunk_scratch,
