@@ -35,6 +35,7 @@ namespace moe {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
+constexpr int kOutStageBytes = 4 * 2 * 4096;  // pair-kernel epilogue staging
 constexpr int kThreads = 192;
 constexpr uint32_t kDevErrTimeout = 0x2u;
 
@@ -516,13 +517,77 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
     return p;
 }
 
+// Epilogue of the pair kernel with coalesced output: a warp whose 32 rows are
+// all valid stages each 32 x 64 box of bf16 outputs in shared memory (the
+// 128-byte swizzle the store tensor map expects) and writes it with one TMA
+// bulk store; the two 4 KB staging buffers of the warp alternate.  Warps with
+// any row past the visit's valid rows take the per-thread path, which stores
+// valid rows only.
+template <int BN, int EPI>
+__device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                         int q, int lane, uint8_t* stage, const CUtensorMap* tmOut,
+                                         int& buf) {
+    const int row = q * 32 + lane;
+    if (q * 32 + 32 > ti.hi) {
+        if constexpr (EPI == kEpiSwiGLU) epi_swiglu(a, ti, taddr, row);
+        else epi_gate<BN>(a, ti, taddr, row);
+        return;
+    }
+    constexpr int NCH = EPI == kEpiSwiGLU ? 2 : BN / 64;  // 64-column output boxes
+    const int col0 = EPI == kEpiSwiGLU ? ti.nb * 128 : ti.nb * BN;
+    const float gate = (EPI == kEpiGate && a.row_gate) ? __ldg(a.row_gate + ti.m0 + row) : 1.0f;
+#pragma unroll 1
+    for (int c = 0; c < NCH; ++c) {
+        if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+        __syncwarp();
+        uint8_t* sb = stage + buf * 4096 + lane * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t p[16];
+            if constexpr (EPI == kEpiSwiGLU) {
+                uint32_t g[32], u[32];
+                tmem_ld32(taddr + c * 64 + half * 32, g);
+                tmem_ld32(taddr + 128 + c * 64 + half * 32, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                    const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                    p[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+                }
+            } else {
+                uint32_t v[32];
+                tmem_ld32(taddr + c * 64 + half * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    p[i] = pack_bf16x2(gate * __uint_as_float(v[2 * i]), gate * __uint_as_float(v[2 * i + 1]));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int chunk = half * 4 + j;  // 16-byte chunk of the 128-byte row
+                *reinterpret_cast<uint4*>(sb + ((chunk ^ (lane & 7)) << 4)) =
+                    make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmOut, stage + buf * 4096, col0 + c * 64, ti.m0 + q * 32);
+            bulk_commit();
+        }
+        buf ^= 1;
+    }
+}
+
 // GATHER: the A rows are gathered from the token rows with TMA gather4 (the
 // permute fused into GEMM1's A load) instead of a tile load from the
 // permuted buffer.
 template <int BN, int EPI, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
     constexpr int BH = BN / 2;  // B rows staged by each CTA
     constexpr int A_BYTES = BM * BK * 2;
     constexpr int B_BYTES = BH * BK * 2;
@@ -535,7 +600,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * B_BYTES);
+    uint8_t* sOut = sB + S * B_BYTES;  // 4 epilogue warps x 2 x 4 KB staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kOutStageBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* tfull = bars + 2 * S;
@@ -565,6 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (threadIdx.x == 32) tma_prefetch_desc(&tmOut);
     if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
     if (warp == 2 && args.block_metadata) {
         // per-expert visit counts from the segment sizes, exclusive warp scan
@@ -714,6 +781,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        uint8_t* stage = sOut + (warp - 2) * 8192;
+        int buf = 0;
         int acc = 0;
         uint32_t aph = 0;
         for (int t = cluster; t < total; t += nclusters) {
@@ -733,17 +802,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ti.skip = false;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if constexpr (EPI == kEpiSwiGLU) {
-                epi_swiglu(args, ti, taddr, row);
-            } else {
-                epi_gate<BN>(args, ti, taddr, row);
-            }
+            (void)row;
+            epi_pair<BN, EPI>(args, ti, taddr, q, lane, stage, &tmOut, buf);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + acc), 0));
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();  // staged stores done before shared memory goes
         if (timed_out) *abort_flag = 1;
     }
 
@@ -779,19 +846,26 @@ static PFN_encodeTiled encode_fn() {
     return fn;
 }
 
-// K-major bf16 matrix [rows, K] as a 2D tensor map with a {64, box_rows}
-// box and the 128-byte swizzle; out-of-range rows read as zero.
-static bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a
+// {box_cols, box_rows} box and the 128-byte swizzle; out-of-range rows read
+// as zero.
+static bool make_tmap_box(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t cols, int box_cols,
+                          int box_rows) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// K-major operand [rows, K]: {64, box_rows} boxes.
+static bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+    return make_tmap_box(tm, ptr, rows, K, BK, box_rows);
 }
 
 template <int BN, int EPI>
@@ -815,12 +889,13 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
 }
 
 template <int BN, int EPI, bool GATHER>
-static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
-                                 int max_visits, cudaStream_t stream) {
+static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tO,
+                                 const GemmArgs& args, int max_visits, cudaStream_t stream) {
     constexpr int NT = kThreads;
     constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
-    constexpr int SMEM = 1024 + S * STAGE_BYTES + 512 + 4 * 260;
+    constexpr int SMEM = 1024 + S * STAGE_BYTES + kOutStageBytes + 512 + 4 * 260;
+    static_assert(SMEM <= 232448, "shared memory budget");
     static int max_clusters[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -841,7 +916,7 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
     int clusters = max_clusters[dev];
     if (max_visits < clusters) clusters = max_visits;
     if (clusters <= 0) return cudaSuccess;
-    k_grouped_gemm_pair<BN, EPI, GATHER><<<2 * clusters, NT, SMEM, stream>>>(tA, tB, args);
+    k_grouped_gemm_pair<BN, EPI, GATHER><<<2 * clusters, NT, SMEM, stream>>>(tA, tB, tO, args);
     return cudaGetLastError();
 }
 
@@ -854,14 +929,17 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
     if (!make_tmap(&tA, A, rowsA, K, a_box) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
         return cudaErrorInvalidValue;
     if (pair) {
+        // the output as a [rows, ldo] bf16 tensor for the staged TMA stores
+        CUtensorMap tO;
+        if (!make_tmap_box(&tO, args.out, args.out_rows, args.ldo, 64, 32)) return cudaErrorInvalidValue;
         if (epi == kEpiSwiGLU && bn == 256)
-            return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, tO, args, max_tiles, stream);
         if (epi == kEpiSwiGLUGather && bn == 256)
-            return launch_pair_t<256, kEpiSwiGLU, true>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<256, kEpiSwiGLU, true>(tA, tB, tO, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 256)
-            return launch_pair_t<256, kEpiGate, false>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<256, kEpiGate, false>(tA, tB, tO, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 128)
-            return launch_pair_t<128, kEpiGate, false>(tA, tB, args, max_tiles, stream);
+            return launch_pair_t<128, kEpiGate, false>(tA, tB, tO, args, max_tiles, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == kEpiSwiGLU) {

@@ -35,6 +35,7 @@ struct GemmArgs {
     int32_t b_rows_per_expert;      // rows of the packed B operand per expert
     void* out;                      // bf16 output
     int64_t ldo;                    // output row stride (elements)
+    int64_t out_rows;               // rows of the output tensor
     const float* row_gate;          // per padded row (gate epilogue), may be null
     uint32_t* status;               // device error word, may be null
     // router epilogue

@@ -238,6 +238,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.b_rows_per_expert = 2 * c.d_e;
     a.out = h;
     a.ldo = c.d_e;
+    a.out_rows = s.R;
     const bool gather = x_perm == nullptr;
     a.gather_x = x;
     a.row_src = row_src;
@@ -272,6 +273,7 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     a.b_rows_per_expert = 0;
     a.out = hs;
     a.ldo = c.d_shared;
+    a.out_rows = c.T;
     const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
                                         mblocks * a.n_tiles, st);
