@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    pdl_wait();  // inputs written by earlier kernels are visible from here on
 
     int nblocks;
     if (args.block_metadata) {
@@ -615,6 +617,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -633,6 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 32) tma_prefetch_desc(&tmOut);
     if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    pdl_wait();  // inputs written by earlier kernels are visible from here on
     if (warp == 2 && args.block_metadata) {
         // per-expert visit counts from the segment sizes, exclusive warp scan
         const int per = 256 / args.block_rows;
@@ -884,8 +888,8 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
     int grid = num_sms();
     if (max_tiles < grid) grid = max_tiles;
     if (grid <= 0) return cudaSuccess;
-    k_grouped_gemm<BN, EPI><<<grid, kThreads, C::SMEM, stream>>>(tA, tB, args);
-    return cudaGetLastError();
+    return launch_pdl(k_grouped_gemm<BN, EPI>, dim3(grid), dim3(kThreads), C::SMEM, stream, tA, tB,
+                      args);
 }
 
 template <int BN, int EPI, bool GATHER>
@@ -916,8 +920,8 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
     int clusters = max_clusters[dev];
     if (max_visits < clusters) clusters = max_visits;
     if (clusters <= 0) return cudaSuccess;
-    k_grouped_gemm_pair<BN, EPI, GATHER><<<2 * clusters, NT, SMEM, stream>>>(tA, tB, tO, args);
-    return cudaGetLastError();
+    return launch_pdl(k_grouped_gemm_pair<BN, EPI, GATHER>, dim3(2 * clusters), dim3(NT), SMEM, stream,
+                      tA, tB, tO, args);
 }
 
 cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, const void* B,

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -33,6 +34,8 @@ int64_t offsets_num_chunks(int64_t A) { return (A + kChunk - 1) / kChunk; }
 __global__ void __launch_bounds__(kScatterThreads)
     k_chunk_hist(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __restrict__ chunk_counts,
                  uint32_t* status) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int hist[kMaxE];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -57,6 +60,8 @@ __global__ void __launch_bounds__(kScanThreads)
            int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets,
            int32_t* __restrict__ block_metadata, int32_t* __restrict__ num_blocks,
            int32_t* __restrict__ row_src, float* __restrict__ row_gate) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_size[kMaxE];
     __shared__ int s_nblk[kMaxE];
     __shared__ int s_total[2];
@@ -122,6 +127,8 @@ __global__ void __launch_bounds__(kScatterThreads)
     k_chunk_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int E,
                     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_row,
                     int32_t* __restrict__ row_src, float* __restrict__ row_gate) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int W = kScatterThreads / 32;
     __shared__ int running[kMaxE];
     __shared__ int wcnt[W][kMaxE];
@@ -178,6 +185,8 @@ __global__ void __launch_bounds__(kSmallThreads)
                     int32_t* __restrict__ block_metadata, int32_t* __restrict__ num_blocks,
                     int32_t* __restrict__ perm_row, int32_t* __restrict__ row_src,
                     float* __restrict__ row_gate, uint32_t* status) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int W = kSmallThreads / 32;
     __shared__ int hist[kMaxE];
     __shared__ int s_size[kMaxE];
@@ -291,24 +300,25 @@ cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t
                            int32_t* row_src, float* row_gate, uint32_t* status,
                            int32_t* chunk_scratch, cudaStream_t stream) {
     if (A <= kSmallA) {
-        k_offsets_small<<<1, kSmallThreads, 0, stream>>>(topk_idx, topk_w, static_cast<int>(A), E, P,
-                                                         R_max, counts, padded_offsets,
-                                                         block_metadata, num_blocks, perm_row,
-                                                         row_src, row_gate, status);
-        return cudaGetLastError();
+        return launch_pdl(k_offsets_small, dim3(1), dim3(kSmallThreads), 0, stream, topk_idx, topk_w,
+                          static_cast<int>(A), E, P, R_max, counts, padded_offsets, block_metadata,
+                          num_blocks, perm_row, row_src, row_gate, status);
     }
     const int n_chunks = static_cast<int>(offsets_num_chunks(A));
     if (n_chunks > 0) {
-        k_chunk_hist<<<n_chunks, kScatterThreads, 0, stream>>>(topk_idx, A, E, chunk_scratch,
-                                                              status);
+        cudaError_t e = launch_pdl(k_chunk_hist, dim3(n_chunks), dim3(kScatterThreads), 0, stream,
+                                   topk_idx, A, E, chunk_scratch, status);
+        if (e != cudaSuccess) return e;
     }
-    k_scan<<<1, kScanThreads, 0, stream>>>(n_chunks, E, P, R_max, chunk_scratch, counts,
-                                           padded_offsets, block_metadata, num_blocks, row_src,
-                                           row_gate);
+    cudaError_t e = launch_pdl(k_scan, dim3(1), dim3(kScanThreads), 0, stream, n_chunks, E, P,
+                               R_max, chunk_scratch, counts, padded_offsets, block_metadata,
+                               num_blocks, row_src, row_gate);
+    if (e != cudaSuccess) return e;
     if (n_chunks > 0) {
-        k_chunk_scatter<<<n_chunks, kScatterThreads, 0, stream>>>(topk_idx, topk_w, A, E,
-                                                                 chunk_scratch, perm_row, row_src,
-                                                                 row_gate);
+        e = launch_pdl(k_chunk_scatter, dim3(n_chunks), dim3(kScatterThreads), 0, stream, topk_idx,
+                       topk_w, A, E, static_cast<const int32_t*>(chunk_scratch), perm_row, row_src,
+                       row_gate);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

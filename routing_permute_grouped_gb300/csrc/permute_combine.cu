@@ -24,6 +24,8 @@ constexpr int kUnroll = 4;
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_permute(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
               uint4* __restrict__ x_perm, int T, int nvec, int k) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
@@ -80,6 +82,8 @@ template <int K>
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ perm_row,
               const uint4* __restrict__ shared_out, uint4* __restrict__ out, int T, int nvec) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
@@ -145,9 +149,9 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
                            int k, cudaStream_t stream) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    k_permute<<<grid, kPCWarps * 32, 0, stream>>>(static_cast<const uint4*>(x), perm_row,
-                                                  static_cast<uint4*>(x_perm), T, nvec, k);
-    return cudaGetLastError();
+    return launch_pdl(k_permute, dim3(grid), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm), T, nvec,
+                      k);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,
@@ -159,7 +163,8 @@ cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* s
     uint4* o4 = static_cast<uint4*>(out);
     switch (k) {
 #define MOE_COMBINE_K(KK) \
-    case KK: k_combine<KK><<<grid, kPCWarps * 32, 0, stream>>>(y4, perm_row, s4, o4, T, nvec); break;
+    case KK: return launch_pdl(k_combine<KK>, dim3(grid), dim3(kPCWarps * 32), 0, stream, y4, perm_row, \
+                               s4, o4, T, nvec);
         MOE_COMBINE_K(1) MOE_COMBINE_K(2) MOE_COMBINE_K(3) MOE_COMBINE_K(4)
         MOE_COMBINE_K(5) MOE_COMBINE_K(6) MOE_COMBINE_K(7) MOE_COMBINE_K(8)
 #undef MOE_COMBINE_K

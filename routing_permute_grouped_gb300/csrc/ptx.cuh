@@ -12,6 +12,14 @@ namespace moe {
 // hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled, and wait until every earlier kernel has completed and its
+// memory is visible (a no-op for a kernel launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -15,6 +15,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -38,6 +39,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
                     int topk_groups, const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
                     float* __restrict__ topk_w) {
     __shared__ float s_logit[kReduceWarps][256];
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kReduceWarps + warp;
     if (t >= T) return;
@@ -120,9 +123,8 @@ cudaError_t launch_router_reduce(const float* partial, int S, int T, int E, int 
                                  float* topk_w, cudaStream_t stream) {
     if (E > 256 || k > 8 || (n_groups > 32)) return cudaErrorInvalidValue;
     const int grid = (T + kReduceWarps - 1) / kReduceWarps;
-    k_router_reduce<<<grid, kReduceWarps * 32, 0, stream>>>(partial, S, T, E, k, n_groups,
-                                                            topk_groups, bias, topk_idx, topk_w);
-    return cudaGetLastError();
+    return launch_pdl(k_router_reduce, dim3(grid), dim3(kReduceWarps * 32), 0, stream, partial, S, T,
+                      E, k, n_groups, topk_groups, bias, topk_idx, topk_w);
 }
 
 }  // namespace moe
