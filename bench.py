@@ -406,8 +406,21 @@ def run_ours(args, shape, rank, world, local):
 
     pk = peaks()
     gemm_flops = ledger.routed_flops(A, d, de)
-    gemm_ach = gemm_flops / (stage_ms["grouped_gemm"] / 1e3) / 1e12
+    active = sum(1 for c in counts_h if c > 0)
+    gemm_bytes = ledger.grouped_gemm_bytes_alg(A, active, d, de)
+    gemm_s = stage_ms["grouped_gemm"] / 1e3
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # the stage is tensor-bound when its FLOP per byte exceeds the machine
+    # balance (measured bf16 FLOP/s over measured HBM bytes/s), else HBM-bound
+    hbm_bound = gemm_flops / gemm_bytes < peak_t * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": gemm_bytes / gemm_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "peak_source": pk["source"] + " copy bandwidth"}
+    else:
+        roof = {"bound": "tensor", "achieved": gemm_flops / gemm_s / 1e12, "peak": peak_t,
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " sustained bf16"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["algorithmic"] = {"flop": gemm_flops, "bytes": gemm_bytes, "active_experts": active}
     perm_bytes = ledger.permute_bytes_alg(T, k, d)
     comb_bytes = ledger.combine_bytes_alg(T, k, d, bool(ds))
     perm_gbs = perm_bytes / (stage_ms["permute"] / 1e3) / 1e9
@@ -422,11 +435,9 @@ def run_ours(args, shape, rank, world, local):
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "tensor", "kernel": "grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
-                     "timing": "stage pass: CUDA events around moe_grouped_gemm_swiglu",
-                     "achieved": gemm_ach, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": gemm_ach / peak_t, "peak_source": pk["source"] + " sustained bf16",
-                     "traffic": traffic},
+        "roofline": dict(roof, kernel="grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
+                         timing="stage pass: CUDA events around moe_grouped_gemm_swiglu",
+                         traffic=traffic),
         "stages": {"ms": {n: round(v, 4) for n, v in stage_ms.items()},
                    "serial_sum_ms": round(sum(stage_ms.values()), 4),
                    "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],

@@ -350,3 +350,11 @@ def test_ledger_figures_of_the_pages():
     gd = _golden("padding_dropless_sec3.txt")
     assert ledger.padded_rows(gd["counts"], 128) == gd["total_rows"][0]
     assert round(100 * ledger.padding_waste(gd["counts"], 128), 2) == 0.39
+
+
+def test_grouped_gemm_algorithmic_bytes():
+    # default shape: 1.913 GB = x_perm + y (2 x 470 MB) + h twice (2 x 134 MB)
+    # + the weights of all 8 experts (705 MB)
+    b = ledger.grouped_gemm_bytes_alg(8192 * 4, 8, 7168, 2048)
+    assert round(b / 1e9, 3) == 1.913
+    assert ledger.grouped_gemm_bytes_alg(0, 3, 64, 32) == 2 * 3 * 3 * 64 * 32
