@@ -1,24 +1,27 @@
-// grouped_gemm.cu -- persistent tcgen05 grouped GEMM over the block table.
+// grouped_gemm.cu -- the tensor-core stages of the layer, tcgen05 + TMA:
 //
-// One kernel serves the three tensor-core stages of the layer:
-//   router  : logits = x Wg^T (+ bias) and top-k in the epilogue
-//   GEMM1   : [g | u] = x_perm W13[e]^T, h = bf16(silu(g) * u)
-//   GEMM2   : y = bf16(row_gate * (h W2[e]^T))
-// The work list is the block table [expert, m_start, valid_m] built on the
-// device ("MoE & MLA operators", sec. 2.3; "Dropless and grouped GEMM",
+//   k_grouped_gemm       one CTA per SM, M = 128 x N = BN tiles (BN = E
+//                        rounded up to 16..256): the router, logits = x Wg^T
+//                        (+ bias) with top-k in the epilogue, or fp32
+//                        partial logits of one K slice (split-K router)
+//   k_grouped_gemm_pair  CTA pairs (cta_group::2, M = 256 x N = 256): the
+//                        grouped expert GEMMs over the block table
+//                          GEMM1: [g | u] = x_perm W13[e]^T, h = bf16(silu(g) u)
+//                          GEMM2: y = bf16(row_gate * (h W2[e]^T))
+//                        and the dense shared expert on a dense tile list
+//
+// The expert work list is the block table [expert, m_start, valid_m] built on
+// the device ("MoE & MLA operators", sec. 2.3; "Dropless and grouped GEMM",
 // sec. 5: a tile reads exactly one expert's weights, the tile count lives in
-// device memory and the host never learns the per-expert sizes).  A tile is
-// one 128-row block x one BN-column panel; tiles are numbered block-major with
-// the N panel fastest, so the CTAs running at the same time share the A block
-// and one expert's weights in L2.
+// device memory and the host never learns the per-expert sizes).
 //
-// CTA = 6 warps, one CTA per SM, persistent over tiles:
+// Both kernels are persistent and warp-specialised (6 warps per CTA):
 //   warp 0      TMA producer: A and B tiles (64 K-columns, 128-byte swizzle)
 //               into a ring of shared-memory stages guarded by mbarriers
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
-//               (M=128, N=BN, K=16) into one of two TMEM accumulators
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per
-//               thread), fused SwiGLU / gate / top-k, stores to global memory
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma into one
+//               of two TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               fused SwiGLU / gate / top-k, stores to global memory
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every wait is bounded; on a timeout the CTA flags the status word,
 // drains what it has in flight and returns.
@@ -54,50 +57,24 @@ struct GemmCfg {
     static_assert(STAGES >= 2, "need at least two stages");
 };
 
-// One tile = 128 rows [m0, m0 + 128) of the A operand for one expert, of
-// which rows [lo, hi) (relative to m0) are stored.  With 128-row blocks a
-// tile is one block.  With 64-row blocks a tile is the 128-row window of the
-// padded buffer that holds the block: two blocks of one expert in the same
-// window share one tile (the second block's tile is skipped), and a window
-// whose halves belong to two experts is visited once per expert, each visit
-// storing only its own rows.
+// One tile of the 1-CTA kernel: 128 token rows [m0, m0 + 128) of the dense
+// router GEMM, of which rows [lo, hi) (relative to m0) exist, and column panel
+// (or, for the split-K router, K slice) nb.  The pair kernel's epilogue uses
+// the same record for its 128-row half of a visit.
 struct TileInfo {
     int e, m0, lo, hi, nb;
     bool skip;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t, int nblocks) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int t) {
     TileInfo ti;
     const int mb = t / a.n_tiles;
     ti.nb = t - mb * a.n_tiles;
     ti.skip = false;
-    if (!a.block_metadata) {
-        ti.e = 0;
-        ti.m0 = mb * BM;
-        ti.lo = 0;
-        ti.hi = min(BM, a.dense_rows - ti.m0);
-        return ti;
-    }
-    const int32_t* bm = a.block_metadata;
-    ti.e = __ldg(bm + 3 * mb + 0);
-    const int start = __ldg(bm + 3 * mb + 1);
-    const int valid = __ldg(bm + 3 * mb + 2);
-    if (!a.pair64) {
-        ti.m0 = start;
-        ti.lo = 0;
-        ti.hi = valid;
-        return ti;
-    }
-    const int win = start >> 7;
-    ti.m0 = win << 7;
-    ti.lo = start - ti.m0;
-    ti.hi = ti.lo + valid;
-    if (mb > 0 && (__ldg(bm + 3 * (mb - 1) + 1) >> 7) == win && __ldg(bm + 3 * (mb - 1)) == ti.e) {
-        ti.skip = true;  // covered by the previous block's tile
-    } else if (mb + 1 < nblocks && (__ldg(bm + 3 * (mb + 1) + 1) >> 7) == win &&
-               __ldg(bm + 3 * (mb + 1)) == ti.e) {
-        ti.hi += __ldg(bm + 3 * (mb + 1) + 2);
-    }
+    ti.e = 0;
+    ti.m0 = mb * BM;
+    ti.lo = 0;
+    ti.hi = min(BM, a.dense_rows - ti.m0);
     return ti;
 }
 
@@ -322,14 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
     pdl_wait();  // inputs written by earlier kernels are visible from here on
 
-    int nblocks;
-    if (args.block_metadata) {
-        nblocks = *args.num_blocks;  // produced by an earlier kernel on this stream
-        nblocks = max(0, min(nblocks, args.nb_cap));
-    } else {
-        nblocks = (args.dense_rows + BM - 1) / BM;
-    }
-    const int total = nblocks * args.n_tiles;
+    const int total = ((args.dense_rows + BM - 1) / BM) * args.n_tiles;
     bool timed_out = false;
 
     if (warp == 0) {
@@ -339,8 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;  // stages armed and not yet seen consumed
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, t, nblocks);
-                if (ti.skip) continue;
+                const TileInfo ti = decode_tile(args, t);
                 const bool split = EPI == kEpiPartial;
                 const int brow = split ? 0 : ti.e * args.b_rows_per_expert + ti.nb * BN;
                 const int kb0 = split ? ti.nb * args.k_per_split : 0;
@@ -382,8 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t aph = 0;
             bool issued = false;
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
-                const TileInfo ti = decode_tile(args, t, nblocks);
-                if (ti.skip) continue;
+                const TileInfo ti = decode_tile(args, t);
                 const int kb0 = EPI == kEpiPartial ? ti.nb * args.k_per_split : 0;
                 const int kb1 = EPI == kEpiPartial ? min(kb0 + args.k_per_split, args.k_blocks)
                                                    : args.k_blocks;
@@ -433,8 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile(args, t, nblocks);
-            if (ti.skip) continue;
+            const TileInfo ti = decode_tile(args, t);
             // tcgen05.ld is warp-collective: the whole warp proceeds or stops
             const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
             if (!ok) {
@@ -444,11 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if constexpr (EPI == kEpiSwiGLU) {
-                epi_swiglu(args, ti, taddr, row);
-            } else if constexpr (EPI == kEpiGate) {
-                epi_gate<BN>(args, ti, taddr, row);
-            } else if constexpr (EPI == kEpiPartial) {
+            if constexpr (EPI == kEpiPartial) {
                 epi_partial<BN>(args, ti, taddr, row);
             } else {
                 epi_router<BN>(args, ti, taddr, row);
@@ -946,12 +909,7 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
             return launch_pair_t<128, kEpiGate, false>(tA, tB, tO, args, max_tiles, stream);
         return cudaErrorInvalidValue;
     }
-    if (epi == kEpiSwiGLU) {
-        if (bn == 256) return launch_t<256, kEpiSwiGLU>(tA, tB, args, max_tiles, stream);
-    } else if (epi == kEpiGate) {
-        if (bn == 256) return launch_t<256, kEpiGate>(tA, tB, args, max_tiles, stream);
-        if (bn == 128) return launch_t<128, kEpiGate>(tA, tB, args, max_tiles, stream);
-    } else if (epi == kEpiPartial) {
+    if (epi == kEpiPartial) {
         switch (bn) {
             case 16: return launch_t<16, kEpiPartial>(tA, tB, args, max_tiles, stream);
             case 32: return launch_t<32, kEpiPartial>(tA, tB, args, max_tiles, stream);

@@ -37,7 +37,6 @@ struct GemmArgs {
     const int32_t* block_metadata;  // [nb_cap, 3] or null
     const int32_t* num_blocks;      // [1] or null
     int32_t nb_cap;                 // capacity of the block table
-    int32_t pair64;                 // blocks are 64 rows: tile on the 128-row grid
     const int32_t* padded_offsets;  // [E + 1] segment starts (CTA-pair kernel)
     int32_t block_rows;             // rows per block of the table (P)
     int32_t n_experts;              // E (CTA-pair kernel)

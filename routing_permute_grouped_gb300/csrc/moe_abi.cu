@@ -227,7 +227,6 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.block_metadata = meta;
     a.num_blocks = nb;
     a.nb_cap = static_cast<int32_t>(s.NB);
-    a.pair64 = c.pad_multiple == 64;
     a.padded_offsets = po;
     a.block_rows = c.pad_multiple;
     a.n_experts = c.E;
