@@ -11,7 +11,10 @@ combine; "Dropless and grouped GEMM", sec. 1: routed + shared).
 Array conventions (numpy):
   bf16 tensors are passed as their uint16 bit patterns; x [T, d],
   Wg [d, E], W1/W3 [E, d, de], W2 [E, de, d], Ws1/Ws3 [d, ds], Ws2 [ds, d];
-  bias float32 [E]; topk_idx int32 [T, k]; gates float64.
+  bias float32 [E]; topk_idx int32 [T, k]; gates float64;
+  e4m3 weights as uint8 codes in the layout of the bf16 matrix they stand
+  for, with float32 scales per output channel (Q1/Q3 [E, d, de] with S1/S3
+  [E, de], Q2 [E, de, d] with S2 [E, d]).
 
 Pinned by ``tests/test_oracle_pins.py`` against the padding worked example
 ("Dropless and grouped GEMM", sec. 3), the ledger figures, brute-force
@@ -70,6 +73,13 @@ def _L():
                 "or_direct_layer": (I, [I, P, I, I, I, I, P, P, P, P, P, P, P, P]),
                 "or_round_bf16_array": (None, [LL, P, P]),
                 "or_num_threads": (I, []),
+                "or_e4m3_to_double": (D, [ctypes.c_uint8]),
+                "or_double_to_e4m3": (ctypes.c_uint8, [D]),
+                "or_quantize_e4m3_columns": (None, [I, I, P, P, P]),
+                "or_quantize_e4m3_batch": (None, [I, I, I, P, P, P]),
+                "or_expert_rows_w8": (I, [I, I, I, I] + [P] * 11),
+                "or_e4m3_to_double_array": (None, [LL, P, P]),
+                "or_double_to_e4m3_array": (None, [LL, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -256,12 +266,89 @@ def direct_layer(tokens, x, W1, W3, W2, topk_idx, topk_w, ys_rows=None) -> np.nd
     return out
 
 
+# ------------------------------------------------ fp8 (e4m3) weights ----
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact value of e4m3 codes (uint8); NaN for the two NaN codes."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _L().or_e4m3_to_double_array(c.size, _p(c), _p(out))
+    return out
+
+
+def round_e4m3(v: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code (uint8) of each value, ties to even, saturating at
+    448."""
+    a = _c(v, np.float64)
+    out = np.empty(a.shape, np.uint8)
+    _L().or_double_to_e4m3_array(a.size, _p(a), _p(out))
+    return out
+
+
+def quantize_e4m3(W) -> tuple:
+    """Per-output-channel e4m3 quantization of bf16 matrices W [..., K, N]
+    (column n = output channel n) -> (codes uint8 [..., K, N], scales
+    float32 [..., N])."""
+    W = _c(W, np.uint16)
+    K, N = W.shape[-2:]
+    batch = int(np.prod(W.shape[:-2], dtype=np.int64)) if W.ndim > 2 else 1
+    q = np.empty(W.shape, np.uint8)
+    s = np.empty(W.shape[:-2] + (N,), np.float32)
+    _L().or_quantize_e4m3_batch(batch, K, N, _p(W), _p(q), _p(s))
+    return q, s
+
+
+def quantize_experts(inp: dict) -> dict:
+    """e4m3 codes and scales of the routed expert weights W1, W3, W2."""
+    Q1, S1 = quantize_e4m3(inp["W1"])
+    Q3, S3 = quantize_e4m3(inp["W3"])
+    Q2, S2 = quantize_e4m3(inp["W2"])
+    return dict(Q1=Q1, S1=S1, Q3=Q3, S3=S3, Q2=Q2, S2=S2)
+
+
+def expert_rows_w8(xrows, experts, gates, q: dict):
+    """expert_rows with e4m3 weights q = quantize_experts(...)."""
+    xr = _c(xrows, np.uint16)
+    ex = _c(experts, np.int32)
+    g = _c(gates, np.float64)
+    Q1, Q3, Q2 = (_c(q[n], np.uint8) for n in ("Q1", "Q3", "Q2"))
+    S1, S3, S2 = (_c(q[n], np.float32) for n in ("S1", "S3", "S2"))
+    E, d, de = Q1.shape
+    n = ex.size
+    h = np.empty((n, de))
+    y = np.empty((n, d))
+    _check(_L().or_expert_rows_w8(n, d, de, E, _p(xr), _p(ex), _p(g), _p(Q1), _p(S1), _p(Q3),
+                                  _p(S3), _p(Q2), _p(S2), _p(h), _p(y)), "expert_rows_w8")
+    return h, y
+
+
+def grouped_experts_w8(x_perm, q: dict, block_metadata, row_gate):
+    """grouped_experts with e4m3 weights: every valid row of the block table
+    through its expert; pad rows stay NaN."""
+    xp = _c(x_perm, np.uint16)
+    meta = _c(block_metadata, np.int32).reshape(-1, 3)
+    rows = [np.arange(m0, m0 + vm) for _, m0, vm in meta]
+    rows = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+    experts = np.concatenate([np.full(vm, e, np.int32) for e, _, vm in meta]) if len(meta) else \
+        np.zeros(0, np.int32)
+    E, d, de = q["Q1"].shape
+    R = xp.shape[0]
+    h = np.full((R, de), np.nan)
+    y = np.full((R, d), np.nan)
+    if rows.size:
+        hh, yy = expert_rows_w8(xp[rows], experts, _c(row_gate, np.float64)[rows], q)
+        h[rows] = hh
+        y[rows] = yy
+    return h, y
+
+
 # ---------------------------------------------------------- whole layer ----
 def layer_forward(inp: dict, cfg) -> dict:
     """Whole layer through the padded layout (router, offsets, permute,
     grouped experts, shared expert, combine), every intermediate returned.
     ``inp`` holds numpy arrays (see module doc); a pre-routed input carries
-    topk_idx / topk_w instead of Wg."""
+    topk_idx / topk_w instead of Wg; an input that also carries the e4m3
+    codes and scales of ``quantize_experts`` runs the routed experts on
+    them."""
     if inp.get("topk_idx") is None:
         logits = router_logits(inp["x"], inp["Wg"], inp.get("bias"))
         idx, w, margin = route(logits, cfg.k, cfg.n_groups, cfg.topk_groups)
@@ -271,8 +358,11 @@ def layer_forward(inp: dict, cfg) -> dict:
         w = _c(inp["topk_w"], np.float64)
     off = build_offsets(idx, w, cfg.E, cfg.pad)
     x_perm = permute(inp["x"], off["row_src"], cfg.k)
-    h, y = grouped_experts(x_perm, inp["W1"], inp["W3"], inp["W2"], off["block_metadata"],
-                           off["row_gate"])
+    if inp.get("Q1") is not None:  # e4m3 routed expert weights
+        h, y = grouped_experts_w8(x_perm, inp, off["block_metadata"], off["row_gate"])
+    else:
+        h, y = grouped_experts(x_perm, inp["W1"], inp["W3"], inp["W2"], off["block_metadata"],
+                               off["row_gate"])
     hs = ys = None
     if cfg.d_shared:
         hs, ys = shared_expert(inp["x"], inp["Ws1"], inp["Ws3"], inp["Ws2"])

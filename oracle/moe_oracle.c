@@ -26,6 +26,10 @@
  *  - same page, sec. 3: each segment rounds up to a multiple of 128, at most
  *    127 pad rows per expert; sec. 5: segments are laid out in ascending
  *    expert order and a tile reads exactly one expert's weights.
+ *  - fp8 expert weights: "MoE & MLA operators", sec. 6.1 (one byte per
+ *    weight) and "Dropless and grouped GEMM", sec. 12 (the scale multiplies
+ *    the product when one scale covers the whole contraction): e4m3 codes
+ *    with one fp32 scale per output channel.
  *
  * Readings where the pages are silent or disagree (each one is listed with
  * its reason in the design notes of the repository):
@@ -35,7 +39,9 @@
  *  - the group score is the maximum logit inside the group;
  *  - the routing weight is a softmax over the k selected logits (the same
  *    value as a softmax over all E followed by renormalisation);
- *  - the gate multiplies the down-projection result before the sum.
+ *  - the gate multiplies the down-projection result before the sum;
+ *  - fp8 weights: scale = amax / 448 per output channel, codes by
+ *    round-to-nearest-even of the fp32 quotient, saturating at 448.
  */
 #include <math.h>
 #include <stdint.h>
@@ -425,6 +431,171 @@ int or_shared_expert(int n, int d, int ds, const uint16_t *xrows, const uint16_t
         free(hy);
     }
     return bad ? OR_ERR_ARG : OR_OK;
+}
+
+/* ------------------------------------------------ fp8 (e4m3) expert weights -- */
+/*
+ * Weight-only fp8: a routed expert matrix is kept as 8-bit e4m3 codes with one
+ * fp32 scale per output channel, and the weight it stands for is exactly
+ * e4m3(q) * s.  "MoE & MLA operators", sec. 6.1 counts expert weights at one
+ * byte per element (fp8 weights, b = 1); "Dropless and grouped GEMM", sec. 12
+ * says the scale may be applied after the matmul when one scale covers the
+ * whole contraction, which is the case for a per-output-channel scale.
+ *
+ * e4m3 (the OCP 8-bit float, E4M3 variant without infinities): a sign bit,
+ * 4 exponent bits with bias 7 and 3 mantissa bits.  Exponent field 0 holds
+ * the subnormals m * 2^-9; exponent 15 with mantissa 7 is NaN; the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ */
+double or_e4m3_to_double(uint8_t code)
+{
+    int e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return (code & 0x80) ? -v : v;
+}
+
+/* The e4m3 code nearest to v, ties to the even code; magnitudes of 448 and
+ * more give 448 (the saturating conversion); NaN gives 0x7F.  The value is
+ * put on the grid of 4 significant bits (quantum 2^-9 at the bottom) with
+ * nearbyint, i.e. round-half-even in the default rounding mode, and encoded. */
+uint8_t or_double_to_e4m3(double v)
+{
+    if (v != v) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 4;      /* quantum of 4 significant bits */
+    if (q < -9) q = -9;
+    double r = ldexp(nearbyint(ldexp(a, -q)), q); /* <= 448 since a < 448 */
+    if (r == 0.0) return sign;
+    if (r <= ldexp(1.0, -6)) /* subnormal (2^-6 itself encodes as field 1, m 0) */
+        return sign | (uint8_t)(int)ldexp(r, 9);
+    int re;
+    double f = frexp(r, &re); /* r = (2f) * 2^(re - 1), 2f in [1, 2) */
+    int m = (int)((2.0 * f - 1.0) * 8.0);
+    return sign | (uint8_t)((re - 1 + 7) << 3) | (uint8_t)m;
+}
+
+/* Per-output-channel quantization of one matrix stored [K][N] (row i is input
+ * i, column n is output channel n), from bf16 bit patterns:
+ *   amax[n] = max_i |W[i][n]|                   (exact: bf16 fits fp32)
+ *   s[n]    = fp32(amax[n] / 448), 1 when amax[n] = 0
+ *   q[i][n] = code nearest to fp32(W[i][n] / s[n])
+ * Both divisions are single-precision IEEE divisions: the integer codes are
+ * decided in fp32. */
+void or_quantize_e4m3_columns(int K, int N, const uint16_t *W, uint8_t *q, float *s)
+{
+    for (int n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            float w = (float)or_bf16_to_double(W[(size_t)i * N + n]);
+            if (fabsf(w) > amax) amax = fabsf(w);
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        s[n] = sc;
+        for (int i = 0; i < K; ++i) {
+            float w = (float)or_bf16_to_double(W[(size_t)i * N + n]);
+            float ratio = w / sc;
+            q[(size_t)i * N + n] = or_double_to_e4m3((double)ratio);
+        }
+    }
+}
+
+/* The same quantization for `batch` matrices of [K][N] stored back to back. */
+void or_quantize_e4m3_batch(int batch, int K, int N, const uint16_t *W, uint8_t *q, float *s)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < batch; ++b)
+        or_quantize_e4m3_columns(K, N, W + (size_t)b * K * N, q + (size_t)b * K * N,
+                                 s + (size_t)b * N);
+}
+
+/* expert_row with e4m3 weights: Q1/Q3 [d][de] with scales S1/S3 [de], Q2
+ * [de][d] with scales S2 [d]; every weight is e4m3(q) * s formed in fp64, so
+ * the arithmetic is that of expert_row on the dequantized matrices. */
+static void expert_row_w8(int d, int de, const uint16_t *x, const uint8_t *Q1, const float *S1,
+                          const uint8_t *Q3, const float *S3, const uint8_t *Q2, const float *S2,
+                          double gate, const double *dec, double *acc_g, double *acc_u,
+                          double *h_out, double *y)
+{
+    for (int j = 0; j < de; ++j) acc_g[j] = acc_u[j] = 0.0;
+    for (int i = 0; i < d; ++i) {
+        double xi = or_bf16_to_double(x[i]);
+        const uint8_t *q1 = Q1 + (size_t)i * de;
+        const uint8_t *q3 = Q3 + (size_t)i * de;
+        for (int j = 0; j < de; ++j) {
+            acc_g[j] += xi * (dec[q1[j]] * (double)S1[j]);
+            acc_u[j] += xi * (dec[q3[j]] * (double)S3[j]);
+        }
+    }
+    for (int j = 0; j < de; ++j) {
+        double g = acc_g[j];
+        double silu = g / (1.0 + exp(-g));
+        acc_g[j] = or_round_bf16(silu * acc_u[j]);
+        if (h_out) h_out[j] = acc_g[j];
+    }
+    for (int n = 0; n < d; ++n) y[n] = 0.0;
+    for (int j = 0; j < de; ++j) {
+        double hj = acc_g[j];
+        const uint8_t *q2 = Q2 + (size_t)j * d;
+        for (int n = 0; n < d; ++n) y[n] += hj * (dec[q2[n]] * (double)S2[n]);
+    }
+    for (int n = 0; n < d; ++n) y[n] *= gate;
+}
+
+/* or_expert_rows with e4m3 expert weights: Q1/Q3 [E][d][de], S1/S3 [E][de],
+ * Q2 [E][de][d], S2 [E][d]. */
+int or_expert_rows_w8(int n, int d, int de, int E, const uint16_t *xrows, const int32_t *experts,
+                      const double *gates, const uint8_t *Q1, const float *S1, const uint8_t *Q3,
+                      const float *S3, const uint8_t *Q2, const float *S2, double *h, double *y)
+{
+    for (int i = 0; i < n; ++i)
+        if (experts[i] < 0 || experts[i] >= E) return OR_ERR_DATA;
+    double dec[256];
+    for (int c = 0; c < 256; ++c) dec[c] = or_e4m3_to_double((uint8_t)c);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *ag = (double *)malloc(sizeof(double) * (size_t)de);
+        double *au = (double *)malloc(sizeof(double) * (size_t)de);
+        double *hy = (double *)malloc(sizeof(double) * (size_t)de);
+        if (!ag || !au || !hy) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int i = 0; i < n; ++i) {
+                size_t e = (size_t)experts[i];
+                expert_row_w8(d, de, xrows + (size_t)i * d, Q1 + e * d * de, S1 + e * de,
+                              Q3 + e * d * de, S3 + e * de, Q2 + e * de * d, S2 + e * d, gates[i],
+                              dec, ag, au, hy, y + (size_t)i * d);
+                if (h) memcpy(h + (size_t)i * de, hy, sizeof(double) * (size_t)de);
+            }
+        }
+        free(ag);
+        free(au);
+        free(hy);
+    }
+    return bad ? OR_ERR_ARG : OR_OK;
+}
+
+/* Element-wise e4m3 decode / encode of arrays (test helpers). */
+void or_e4m3_to_double_array(long long n, const uint8_t *in, double *out)
+{
+    for (long long i = 0; i < n; ++i) out[i] = or_e4m3_to_double(in[i]);
+}
+
+void or_double_to_e4m3_array(long long n, const double *in, uint8_t *out)
+{
+    for (long long i = 0; i < n; ++i) out[i] = or_double_to_e4m3(in[i]);
 }
 
 /* ------------------------------------------------------------- combine -- */
