@@ -58,6 +58,7 @@ typedef enum {
 /* Device error bits reported by moe_get_device_status(). */
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* an expert id outside [0, E) was skipped */
 #define MOE_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel gave up */
+#define MOE_DEVERR_F16_RANGE 0x4u    /* e4m3 path: an activation beyond f16's range */
 
 typedef struct {
     int32_t T;            /* tokens */
@@ -81,6 +82,22 @@ typedef struct {
     const void *Ws2;    /* shared down, K-major: bf16 [d, d_shared], or NULL */
 } moe_weights_t;
 
+/* e4m3 expert weights as produced by moe_pack_experts_fp8 (device pointers):
+ * the K-major layouts of moe_weights_t with one byte per weight, and one fp32
+ * scale per weight row (output channel).  The router stays bf16. */
+typedef struct {
+    const void *Wg_t;    /* router weight, K-major: bf16 [E, d] */
+    const float *bias;   /* per-expert logit bias fp32 [E], or NULL */
+    const void *W13q;    /* routed gate/up codes: e4m3 [E, 2*d_e, d] */
+    const float *s13;    /* their scales: fp32 [E, 2*d_e] */
+    const void *W2q;     /* routed down codes, K-major: e4m3 [E, d, d_e] */
+    const float *s2;     /* fp32 [E, d] */
+    const void *Ws13q;   /* shared gate/up codes: e4m3 [2*d_shared, d], or NULL */
+    const float *ss13;   /* fp32 [2*d_shared] */
+    const void *Ws2q;    /* shared down codes: e4m3 [d, d_shared], or NULL */
+    const float *ss2;    /* fp32 [d] */
+} moe_weights_fp8_t;
+
 /* Offsets (bytes) of every intermediate inside the moe_layer_fwd workspace,
  * so a caller can read them back.  All offsets are multiples of 1024. */
 typedef struct {
@@ -101,6 +118,8 @@ typedef struct {
     size_t hs;             /* bf16 [T, d_shared] */
     size_t ys;             /* bf16 [T, d] */
     size_t router_partial; /* fp32 [S, T, E] split-K router logits (S > 1 only) */
+    size_t x16;            /* f16 [T, d] token rows for the shared expert
+                              (moe_layer_fwd_fp8 with d_shared > 0 only) */
 } moe_workspace_layout_t;
 
 /* ---------------------------------------------------------------- sizes -- */
@@ -136,6 +155,19 @@ moe_status_t moe_pack_router(int32_t d, int32_t E, const void *Wg, void *Wg_t, v
  * shared expert.  Requires de % 128 == 0, d % 128 == 0. */
 moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void *W1, const void *W3,
                               const void *W2, void *W13, void *W2_t, void *stream);
+
+/* The same packing into e4m3 codes with one fp32 scale per output channel
+ * ("MoE & MLA operators", sec. 6.1: fp8 expert weights, one byte each;
+ * "Dropless and grouped GEMM", sec. 12: a scale that covers the whole
+ * contraction is applied after the matmul).  For output channel c of a
+ * matrix: scale = amax_c / 448 (IEEE fp32 division; 1 for an all-zero
+ * channel) and code = the e4m3 value nearest to fp32(w / scale), ties to even,
+ * saturating at 448.  Codes go where moe_pack_experts puts the bf16 values
+ * (W13q [E, 2*de, d], W2q [E, d, de]); scales follow the packed rows
+ * (s13 [E, 2*de], s2 [E, d]).  E = 1 packs a shared expert. */
+moe_status_t moe_pack_experts_fp8(int32_t E, int32_t d, int32_t de, const void *W1,
+                                  const void *W3, const void *W2, void *W13q, float *s13,
+                                  void *W2q, float *s2, void *stream);
 
 /* ----------------------------------------------------------- the stages -- */
 
@@ -231,6 +263,16 @@ moe_status_t moe_build_offsets_noalloc(const moe_config_t *cfg, const int32_t *t
 moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
                          void *x_perm, void *stream);
 
+/* a3 for the e4m3-weight path: the same scatter writing f16 rows (x_perm16
+ * [R_max, d]); every bf16 value is copied exactly when its magnitude is in
+ * [2^-17, 65504] or zero (smaller magnitudes round to a multiple of 2^-24);
+ * a finite value beyond f16's range sets MOE_DEVERR_F16_RANGE in *status.
+ *   x16     f16 [T, d] device, written (the dense copy for the shared
+ *           expert), or NULL
+ *   status  uint32 [1] device word, or NULL */
+moe_status_t moe_permute_f16(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
+                             void *x_perm16, void *x16, uint32_t *status, void *stream);
+
 /* a4 + a5. Grouped SwiGLU expert GEMMs over the block table ("MoE & MLA
  * operators", sec. 2.4; "Dropless and grouped GEMM", sec. 5: one tile reads
  * exactly one expert's weights, the tile list lives on the device):
@@ -259,6 +301,36 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t *cfg, const void *x_perm
                                      const int32_t *num_blocks, const int32_t *padded_offsets,
                                      const float *row_gate, void *h, void *y, uint32_t *status,
                                      void *stream);
+
+/* a4 + a5 for blocks with few rows (decode): the same h and y as
+ * moe_grouped_gemm_swiglu from a second kernel that swaps the operands.  A
+ * tile multiplies 256 weight rows of one expert (two M = 128 tcgen05 MMAs)
+ * by the block's valid token rows (the MMA's N, valid_m rounded up to 16), so
+ * an expert with two rows costs its weight bytes, not a 128-row tile
+ * ("Dropless and grouped GEMM", sec. 10: the decode layout, valid rows per
+ * expert with the block table as work list).  Tiles are (panel, block) pairs;
+ * padded_offsets is not needed.  Arguments as moe_grouped_gemm_swiglu. */
+moe_status_t moe_grouped_gemm_swiglu_skinny(const moe_config_t *cfg, const void *x_perm,
+                                            const void *W13, const void *W2_t,
+                                            const int32_t *block_metadata,
+                                            const int32_t *num_blocks, const float *row_gate,
+                                            void *h, void *y, uint32_t *status, void *stream);
+
+/* a4 + a5 with e4m3 expert weights (moe_pack_experts_fp8), on the kernel of
+ * moe_grouped_gemm_swiglu_skinny: converter warps widen each staged e4m3
+ * panel to f16 (exact) for f16 x f16 -> fp32 MMAs, and the epilogues apply the
+ * channel scales to the fp32 accumulators:
+ *   h[r] = bf16( silu(s13_g * (x W1q)) * (s13_u * (x W3q)) )  stored as f16
+ *   y[r] = bf16( row_gate[r] * s2 * (h W2q) )
+ *   x_perm16 f16 [R_max, d] (moe_permute_f16), h16 f16 [R_max, d_e] holding
+ *   the bf16-rounded values, y bf16 [R_max, d]; other arguments as
+ *   moe_grouped_gemm_swiglu_skinny.  h values beyond f16's range set
+ *   MOE_DEVERR_F16_RANGE. */
+moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t *cfg, const void *x_perm16,
+                                         const void *W13q, const float *s13, const void *W2q,
+                                         const float *s2, const int32_t *block_metadata,
+                                         const int32_t *num_blocks, const float *row_gate,
+                                         void *h16, void *y, uint32_t *status, void *stream);
 
 /* a3 + a4 + a5 fused: the grouped GEMMs of moe_grouped_gemm_swiglu with the
  * permute folded into GEMM1's A load ("Dropless and grouped GEMM", sec. 4:
@@ -305,7 +377,11 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y, const int32_t *
  * When the batch has too few 128-token tiles to fill the GPU (decode sizes),
  * the router GEMM splits K into up to 16 slices whose fp32 partial logits
  * (workspace region router_partial) a second kernel sums in slice order
- * before the top-k; otherwise it is the single kernel of moe_route. */
+ * before the top-k; otherwise it is the single kernel of moe_route.
+ * When the mean rows per expert, T*k/E, is at most 32 the expert GEMMs run
+ * on the kernel of moe_grouped_gemm_swiglu_skinny, with the shared expert's
+ * tiles appended to the same two launches; otherwise on the CTA-pair kernel
+ * of moe_grouped_gemm_swiglu followed by moe_shared_expert. */
 moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
                            void *out, void *ws, size_t ws_bytes, void *stream);
 
@@ -316,6 +392,23 @@ moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, cons
 moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_t *w,
                                      const void *x, const int32_t *topk_idx, const float *topk_w,
                                      void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* The layer with e4m3 expert weights (routed and shared): router and
+ * offsets as moe_layer_fwd, then moe_permute_f16 (x_perm and, with a shared
+ * expert, x16 regions of the workspace), the e4m3 grouped GEMMs with the
+ * shared expert's tiles in the same two launches, and the combine.  The
+ * workspace is the moe_layer_fwd one (moe_workspace_size); x_perm, h and hs
+ * hold f16 there.  Requires w->W13q/s13/W2q/s2, w->Wg_t, and the shared codes
+ * and scales when d_shared > 0.  Bits of the device status word as above,
+ * plus MOE_DEVERR_F16_RANGE. */
+moe_status_t moe_layer_fwd_fp8(const moe_config_t *cfg, const moe_weights_fp8_t *w,
+                               const void *x, void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_layer_fwd_fp8 for pre-routed input (as moe_layer_fwd_prerouted). */
+moe_status_t moe_layer_fwd_fp8_prerouted(const moe_config_t *cfg, const moe_weights_fp8_t *w,
+                                         const void *x, const int32_t *topk_idx,
+                                         const float *topk_w, void *out, void *ws,
+                                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------- diagnostics -- */
 

@@ -305,6 +305,24 @@ def quantize_experts(inp: dict) -> dict:
     return dict(Q1=Q1, S1=S1, Q3=Q3, S3=S3, Q2=Q2, S2=S2)
 
 
+def quantize_shared(inp: dict) -> dict:
+    """e4m3 codes and scales of the shared expert Ws1, Ws3 [d, ds], Ws2 [ds, d]."""
+    Q1, S1 = quantize_e4m3(inp["Ws1"])
+    Q3, S3 = quantize_e4m3(inp["Ws3"])
+    Q2, S2 = quantize_e4m3(inp["Ws2"])
+    return dict(Qs1=Q1, Ss1=S1, Qs3=Q3, Ss3=S3, Qs2=Q2, Ss2=S2)
+
+
+def shared_expert_w8(xrows, qs: dict):
+    """The shared expert with e4m3 weights: the routed evaluation with one
+    expert and gate 1 (the arithmetic of shared_expert on the dequantized
+    matrices)."""
+    n = np.asarray(xrows).shape[0]
+    q = dict(Q1=qs["Qs1"][None], S1=qs["Ss1"][None], Q3=qs["Qs3"][None], S3=qs["Ss3"][None],
+             Q2=qs["Qs2"][None], S2=qs["Ss2"][None])
+    return expert_rows_w8(xrows, np.zeros(n, np.int32), np.ones(n), q)
+
+
 def expert_rows_w8(xrows, experts, gates, q: dict):
     """expert_rows with e4m3 weights q = quantize_experts(...)."""
     xr = _c(xrows, np.uint16)
@@ -347,8 +365,8 @@ def layer_forward(inp: dict, cfg) -> dict:
     grouped experts, shared expert, combine), every intermediate returned.
     ``inp`` holds numpy arrays (see module doc); a pre-routed input carries
     topk_idx / topk_w instead of Wg; an input that also carries the e4m3
-    codes and scales of ``quantize_experts`` runs the routed experts on
-    them."""
+    codes and scales of ``quantize_experts`` (``quantize_shared``) runs the
+    routed (shared) experts on them."""
     if inp.get("topk_idx") is None:
         logits = router_logits(inp["x"], inp["Wg"], inp.get("bias"))
         idx, w, margin = route(logits, cfg.k, cfg.n_groups, cfg.topk_groups)
@@ -364,7 +382,9 @@ def layer_forward(inp: dict, cfg) -> dict:
         h, y = grouped_experts(x_perm, inp["W1"], inp["W3"], inp["W2"], off["block_metadata"],
                                off["row_gate"])
     hs = ys = None
-    if cfg.d_shared:
+    if cfg.d_shared and inp.get("Qs1") is not None:  # e4m3 shared expert weights
+        hs, ys = shared_expert_w8(inp["x"], inp)
+    elif cfg.d_shared:
         hs, ys = shared_expert(inp["x"], inp["Ws1"], inp["Ws3"], inp["Ws2"])
     out = combine(y, off["perm_row"], cfg.k, ys)
     return dict(logits=logits, topk_idx=idx, topk_w=w, margin=margin, x_perm=x_perm, h=h, y=y,

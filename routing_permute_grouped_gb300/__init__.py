@@ -29,11 +29,14 @@ __all__ = [
     "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
+    "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_f16", "moe_grouped_gemm_swiglu_skinny",
+    "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
 ]
 
 MOE_OK = 0
 DEVERR_EXPERT_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
+DEVERR_F16_RANGE = 0x4
 
 
 class MoeError(RuntimeError):
@@ -52,9 +55,14 @@ class MoeWeights(ctypes.Structure):
                 ("W2", ctypes.c_void_p), ("Ws13", ctypes.c_void_p), ("Ws2", ctypes.c_void_p)]
 
 
+class MoeWeightsFp8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("Wg_t", "bias", "W13q", "s13", "W2q", "s2", "Ws13q", "ss13", "Ws2q", "ss2")]
+
+
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
                   "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
-                  "y", "hs", "ys", "router_partial")
+                  "y", "hs", "ys", "router_partial", "x16")
 
 
 class _Layout(ctypes.Structure):
@@ -100,6 +108,13 @@ def load():
         "moe_layer_fwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, SZ, P]),
         "moe_layer_fwd_prerouted": (ctypes.c_int,
                                     [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ, P]),
+        "moe_pack_experts_fp8": (ctypes.c_int, [I32, I32, I32] + [P] * 8),
+        "moe_permute_f16": (ctypes.c_int, [CP] + [P] * 6),
+        "moe_grouped_gemm_swiglu_skinny": (ctypes.c_int, [CP] + [P] * 10),
+        "moe_grouped_gemm_swiglu_fp8": (ctypes.c_int, [CP] + [P] * 12),
+        "moe_layer_fwd_fp8": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P, SZ, P]),
+        "moe_layer_fwd_fp8_prerouted": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P,
+                                                       P, P, SZ, P]),
         "moe_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -180,6 +195,12 @@ def moe_pack_experts(W1, W3, W2, W13, W2_t, stream=None) -> None:
                                    _stream(stream)))
 
 
+def moe_pack_experts_fp8(W1, W3, W2, W13q, s13, W2q, s2, stream=None) -> None:
+    E, d, de = W1.shape
+    _check(load().moe_pack_experts_fp8(E, d, de, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(W13q),
+                                       _ptr(s13), _ptr(W2q), _ptr(s2), _stream(stream)))
+
+
 # ------------------------------------------------------------ stages ------
 def moe_route(cfg, x, Wg_t, bias, topk_idx, topk_w, stream=None) -> None:
     _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg_t), _ptr(bias), _ptr(topk_idx),
@@ -240,6 +261,26 @@ def moe_grouped_gemm_swiglu_gather(cfg, x, row_src, W13, W2_t, block_metadata, n
         _stream(stream)))
 
 
+def moe_permute_f16(cfg, x, perm_row, x_perm16, x16=None, status=None, stream=None) -> None:
+    _check(load().moe_permute_f16(ctypes.byref(cfg), _ptr(x), _ptr(perm_row), _ptr(x_perm16),
+                                  _ptr(x16), _ptr(status), _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_skinny(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate,
+                                   h, y, status=None, stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu_skinny(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
+        _ptr(num_blocks), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_fp8(cfg, x_perm16, W13q, s13, W2q, s2, block_metadata, num_blocks,
+                                row_gate, h16, y, status=None, stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu_fp8(
+        ctypes.byref(cfg), _ptr(x_perm16), _ptr(W13q), _ptr(s13), _ptr(W2q), _ptr(s2),
+        _ptr(block_metadata), _ptr(num_blocks), _ptr(row_gate), _ptr(h16), _ptr(y), _ptr(status),
+        _stream(stream)))
+
+
 def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:
     _check(load().moe_shared_expert(ctypes.byref(cfg), _ptr(x), _ptr(Ws13), _ptr(Ws2_t), _ptr(hs),
                                     _ptr(ys), _ptr(status), _stream(stream)))
@@ -258,6 +299,18 @@ def moe_layer_fwd(cfg, weights: MoeWeights, x, out, ws, stream=None) -> None:
 def moe_layer_fwd_prerouted(cfg, weights: MoeWeights, x, topk_idx, topk_w, out, ws,
                             stream=None) -> None:
     _check(load().moe_layer_fwd_prerouted(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(out),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_fwd_fp8(cfg, weights: MoeWeightsFp8, x, out, ws, stream=None) -> None:
+    _check(load().moe_layer_fwd_fp8(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(out),
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_fwd_fp8_prerouted(cfg, weights: MoeWeightsFp8, x, topk_idx, topk_w, out, ws,
+                                stream=None) -> None:
+    _check(load().moe_layer_fwd_fp8_prerouted(
         ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(out),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -288,15 +341,21 @@ class MoeLayer:
     ``moe_layer_fwd`` (or the pre-routed variant) on the current stream.
     Weights use the pages' orientation: Wg [d, E], W1/W3 [E, d, d_e],
     W2 [E, d_e, d], shared Ws1/Ws3 [d, d_s], Ws2 [d_s, d]; all bf16 CUDA
-    tensors; bias fp32 [E] or None.
+    tensors; bias fp32 [E] or None.  ``fp8=True`` packs the routed and shared
+    expert weights as e4m3 codes with per-output-channel scales
+    (``moe_pack_experts_fp8``) and runs ``moe_layer_fwd_fp8``.
     """
 
     def __init__(self, cfg: MoeConfig, W1, W3, W2, Wg=None, bias=None, Ws1=None, Ws3=None, Ws2=None,
-                 stream=None):
+                 stream=None, fp8: bool = False):
         moe_check_config(cfg)
         self.cfg = cfg
+        self.fp8 = fp8
         dev = W1.device
         E, d, de = W1.shape
+        if fp8:
+            self._init_fp8(cfg, W1, W3, W2, Wg, bias, Ws1, Ws3, Ws2, stream)
+            return
         self.W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device=dev)
         self.W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device=dev)
         moe_pack_experts(W1, W3, W2, self.W13, self.W2_t, stream)
@@ -318,14 +377,56 @@ class MoeLayer:
             W13=self.W13.data_ptr(), W2=self.W2_t.data_ptr(),
             Ws13=None if self.Ws13 is None else self.Ws13.data_ptr(),
             Ws2=None if self.Ws2_t is None else self.Ws2_t.data_ptr())
+        self._init_ws(cfg, dev)
+
+    def _init_ws(self, cfg, dev):
         self.layout = moe_workspace_layout(cfg)
         self.ws = torch.empty(self.layout["total"], dtype=torch.uint8, device=dev)
         self.ws[:256].zero_()
 
+    def _init_fp8(self, cfg, W1, W3, W2, Wg, bias, Ws1, Ws3, Ws2, stream):
+        dev = W1.device
+        E, d, de = W1.shape
+
+        def pack(w1, w3, w2, n, width):
+            q13 = torch.empty((n, 2 * width, d), dtype=torch.uint8, device=dev)
+            s13 = torch.empty((n, 2 * width), dtype=torch.float32, device=dev)
+            q2 = torch.empty((n, d, width), dtype=torch.uint8, device=dev)
+            s2 = torch.empty((n, d), dtype=torch.float32, device=dev)
+            moe_pack_experts_fp8(w1, w3, w2, q13, s13, q2, s2, stream)
+            return q13, s13, q2, s2
+
+        self.W13q, self.s13, self.W2q, self.s2 = pack(W1, W3, W2, E, de)
+        self.Wg_t = None
+        if Wg is not None:
+            self.Wg_t = torch.empty((E, d), dtype=torch.bfloat16, device=dev)
+            moe_pack_router(Wg, self.Wg_t, stream)
+        self.bias = None if bias is None else bias.to(device=dev, dtype=torch.float32).contiguous()
+        self.Ws13q = self.ss13 = self.Ws2q = self.ss2 = None
+        if cfg.d_shared:
+            self.Ws13q, self.ss13, self.Ws2q, self.ss2 = pack(
+                Ws1.unsqueeze(0).contiguous(), Ws3.unsqueeze(0).contiguous(),
+                Ws2.unsqueeze(0).contiguous(), 1, cfg.d_shared)
+
+        def p(t):
+            return None if t is None else t.data_ptr()
+
+        self.weights = MoeWeightsFp8(
+            Wg_t=p(self.Wg_t), bias=p(self.bias), W13q=p(self.W13q), s13=p(self.s13),
+            W2q=p(self.W2q), s2=p(self.s2), Ws13q=p(self.Ws13q), ss13=p(self.ss13),
+            Ws2q=p(self.Ws2q), ss2=p(self.ss2))
+        self._init_ws(cfg, dev)
+
     def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None):
         if out is None:
             out = torch.empty_like(x)
-        if topk_idx is None:
+        if self.fp8:
+            if topk_idx is None:
+                moe_layer_fwd_fp8(self.cfg, self.weights, x, out, self.ws, stream)
+            else:
+                moe_layer_fwd_fp8_prerouted(self.cfg, self.weights, x, topk_idx, topk_w, out,
+                                            self.ws, stream)
+        elif topk_idx is None:
             moe_layer_fwd(self.cfg, self.weights, x, out, self.ws, stream)
         else:
             moe_layer_fwd_prerouted(self.cfg, self.weights, x, topk_idx, topk_w, out, self.ws,

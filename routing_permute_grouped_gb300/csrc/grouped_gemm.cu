@@ -116,7 +116,7 @@ __device__ __forceinline__ void epi_gate(const GemmArgs& a, const TileInfo& ti, 
                                          int row) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     const bool valid = row >= ti.lo && row < ti.hi;
-    const float gate = (valid && a.row_gate) ? __ldg(a.row_gate + ti.m0 + row) : 1.0f;
+    const float gate = (valid && a.row_gate) ? ld_dep(a.row_gate + ti.m0 + row) : 1.0f;
     __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * BN;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -162,7 +162,7 @@ __device__ __forceinline__ void epi_router(const GemmArgs& a, const TileInfo& ti
             for (int i = 0; i < 16; ++i) {
                 const int e = c * 16 + i;
                 if (e < E) {
-                    const float l = __uint_as_float(v[i]) + (a.bias ? __ldg(a.bias + e) : 0.0f);
+                    const float l = __uint_as_float(v[i]) + (a.bias ? ld_dep(a.bias + e) : 0.0f);
                     const int g = e / gsz;
                     gs[g] = fmaxf(gs[g], l);
                 }
@@ -198,7 +198,7 @@ __device__ __forceinline__ void epi_router(const GemmArgs& a, const TileInfo& ti
         for (int i = 0; i < 16; ++i) {
             const int e = c * 16 + i;
             if (e < E && ((gmask >> (e / gsz)) & 1u)) {
-                float cv = __uint_as_float(v[i]) + (a.bias ? __ldg(a.bias + e) : 0.0f);
+                float cv = __uint_as_float(v[i]) + (a.bias ? ld_dep(a.bias + e) : 0.0f);
                 int ci = e;
                 bool shifting = false;
 #pragma unroll
@@ -473,12 +473,12 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
     }
     p.e = lo;
     const int per = 256 / a.block_rows;
-    const int mb = __ldg(a.padded_offsets + lo) / a.block_rows + (v - vpref[lo]) * per;
+    const int mb = ld_dep(a.padded_offsets + lo) / a.block_rows + (v - vpref[lo]) * per;
     const int32_t* bm = a.block_metadata;
-    p.m0 = __ldg(bm + 3 * mb + 1);
-    p.hi = __ldg(bm + 3 * mb + 2);
-    const int bend = __ldg(a.padded_offsets + lo + 1) / a.block_rows;  // next expert's first block
-    for (int j = 1; j < per && mb + j < bend; ++j) p.hi += __ldg(bm + 3 * (mb + j) + 2);
+    p.m0 = ld_dep(bm + 3 * mb + 1);
+    p.hi = ld_dep(bm + 3 * mb + 2);
+    const int bend = ld_dep(a.padded_offsets + lo + 1) / a.block_rows;  // next expert's first block
+    for (int j = 1; j < per && mb + j < bend; ++j) p.hi += ld_dep(bm + 3 * (mb + j) + 2);
     return p;
 }
 
@@ -500,7 +500,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
     }
     constexpr int NCH = EPI == kEpiSwiGLU ? 2 : BN / 64;  // 64-column output boxes
     const int col0 = EPI == kEpiSwiGLU ? ti.nb * 128 : ti.nb * BN;
-    const float gate = (EPI == kEpiGate && a.row_gate) ? __ldg(a.row_gate + ti.m0 + row) : 1.0f;
+    const float gate = (EPI == kEpiGate && a.row_gate) ? ld_dep(a.row_gate + ti.m0 + row) : 1.0f;
 #pragma unroll 1
     for (int c = 0; c < NCH; ++c) {
         if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
@@ -608,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int e = base + lane;
             int nv = 0;
             if (e < args.n_experts) {
-                const int nblk = (__ldg(args.padded_offsets + e + 1) - __ldg(args.padded_offsets + e)) /
+                const int nblk = (ld_dep(args.padded_offsets + e + 1) - ld_dep(args.padded_offsets + e)) /
                                  args.block_rows;
                 nv = (nblk + per - 1) / per;
             }
@@ -659,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int rr = BM * static_cast<int>(rank) + 4 * lane + j;  // row in the visit
                     // rows past the visit's valid rows are computed but never
                     // stored: any in-range token row will do
-                    if (rr < p.hi) grow[j] = __ldg(args.row_src + p.m0 + rr) / args.gather_k;
+                    if (rr < p.hi) grow[j] = ld_dep(args.row_src + p.m0 + rr) / args.gather_k;
                 }
             }
             for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -826,6 +826,21 @@ static bool make_tmap_box(CUtensorMap* tm, const void* ptr, int64_t rows, int64_
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_2d(void* tmap, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
+                        int dtype, int box_cols, int box_rows, bool swizzle128) {
+    PFN_encodeTiled enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(static_cast<CUtensorMap*>(tmap), static_cast<CUtensorMapDataType>(dtype), 2,
+                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

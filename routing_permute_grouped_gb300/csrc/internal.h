@@ -94,6 +94,63 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
 
 int num_sms();
 
+// Device-side description of one launch of the small-M (swapped-operand)
+// grouped GEMM.  A tile multiplies 256 rows of one expert's K-major weight
+// matrix (panel p of that expert) by the token rows of one block of the
+// table (at most 128); tiles of the dense shared expert (chunks of 128 token
+// rows) follow the routed tiles when s_rows > 0.
+struct SkinnyArgs {
+    const int32_t* block_metadata;  // [nb_cap, 3] [expert, m_start, valid_m]
+    const int32_t* num_blocks;      // [1]
+    int32_t nb_cap;                 // capacity of the block table
+    int32_t n_experts;              // valid expert ids are [0, n_experts)
+    int32_t n_panels;               // routed panels of 256 weight rows per block
+    int32_t rows_per_expert;        // weight rows per expert (2 d_e or d)
+    int32_t k_blocks;               // routed K / 64
+    void* out;                      // routed output [out_rows, ldo] (bf16, or f16 h)
+    int64_t ldo;
+    int64_t out_rows;
+    const float* row_gate;          // routed gate per padded row (gate epilogue), may be null
+    const float* scale;             // e4m3 weights: fp32 scale per weight row
+    // shared expert (dense tiles after the routed ones)
+    int32_t s_rows;                 // token rows (0 = no shared tiles)
+    int32_t s_panels;
+    int32_t s_rows_per_expert;      // weight rows of the shared matrix
+    int32_t s_k_blocks;
+    void* s_out;                    // [s_rows, s_ldo]
+    int64_t s_ldo;
+    const float* s_scale;
+    uint32_t* status;               // device error word, may be null
+};
+
+// Small-M grouped GEMM (epi = kEpiSwiGLU or kEpiGate).  W / Ws: weights
+// [rows, K] K-major, bf16 or (fp8) e4m3 codes; X / Xs: token rows [rows, K],
+// bf16 or (fp8) f16.  max_tiles bounds the tile count (grid size).
+cudaError_t launch_grouped_gemm_skinny(int epi, bool fp8, const void* W, int64_t rowsW,
+                                       const void* X, int64_t rowsX, int64_t K, const void* Ws,
+                                       int64_t rowsWs, const void* Xs, int64_t rowsXs, int64_t Ks,
+                                       const SkinnyArgs& args, int max_tiles, cudaStream_t stream);
+
+// 2D tensor map of a row-major [rows, cols] matrix of elem_bytes-wide
+// elements (dtype: a CUtensorMapDataType value) with a {box_cols, box_rows}
+// box, the 128-byte swizzle or none.  False if the driver refuses it.
+bool make_tensor_map_2d(void* tmap, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
+                        int dtype, int box_cols, int box_rows, bool swizzle128);
+
+// e4m3 packing: per-output-channel scales of W [batch][rows][cols] (column c
+// = output channel c), written to scale[b * scale_bstride + packed_row(c,
+// mode)]; then the codes of the transposed matrix at out[packed_row(c,
+// mode) * out_ld + r].
+cudaError_t launch_pack_fp8(const void* in, uint8_t* out, float* scale, int rows, int cols,
+                            int64_t in_bstride, int64_t out_bstride, int64_t scale_bstride,
+                            int out_ld, int mode, int batch, cudaStream_t stream);
+
+// Permute into f16 rows (exact copies of the bf16 values in f16's range);
+// x16, if not null, also receives the dense f16 copy of every token row.
+// Values beyond f16's range set bit 0x4 of *status.
+cudaError_t launch_permute_f16(const void* x, const int32_t* perm_row, void* x_perm16, void* x16,
+                               int T, int d, int k, uint32_t* status, cudaStream_t stream);
+
 // Sums S fp32 partial-logit slices in slice order, adds the bias and does the
 // (group-limited) top-k and softmax of each token.
 cudaError_t launch_router_reduce(const float* partial, int S, int T, int E, int k, int n_groups,

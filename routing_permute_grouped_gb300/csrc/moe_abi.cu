@@ -139,6 +139,7 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c) {
     L.ys = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
     const int S = router_splits(c);
     L.router_partial = take(S > 1 ? static_cast<size_t>(S) * c.T * c.E * 4 : 0);
+    L.x16 = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
     L.total = off;
     return L;
 }
@@ -260,6 +261,79 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2 (down + gate)");
 }
 
+// The expert GEMMs on the swapped-operand kernel for blocks with few rows,
+// bf16 weights or (fp8) e4m3 codes with per-row scales.  When Ws13 is given
+// and d_shared > 0, the shared expert's dense tiles (token rows Xs) are
+// appended to the same two launches.
+static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const void* X,
+                                      const void* W13, const float* s13, const void* W2,
+                                      const float* s2, const int32_t* meta, const int32_t* nb,
+                                      const float* row_gate, void* h, void* y, uint32_t* status,
+                                      cudaStream_t st, const void* Xs = nullptr,
+                                      const void* Ws13 = nullptr, const float* ss13 = nullptr,
+                                      const void* Ws2 = nullptr, const float* ss2 = nullptr,
+                                      void* hs = nullptr, void* ys = nullptr) {
+    const Sizes s = sizes_of(c);
+    const bool shared = c.d_shared > 0 && Ws13 != nullptr;
+    const int64_t chunks = (static_cast<int64_t>(c.T) + 127) / 128;
+    SkinnyArgs a{};
+    a.block_metadata = meta;
+    a.num_blocks = nb;
+    a.nb_cap = static_cast<int32_t>(s.NB);
+    a.n_experts = c.E;
+    a.status = status;
+    a.out_rows = s.R;
+    // GEMM1: panels of 128 gate + 128 up rows, K = d
+    a.n_panels = c.d_e / 128;
+    a.rows_per_expert = 2 * c.d_e;
+    a.k_blocks = c.d / 64;
+    a.out = h;
+    a.ldo = c.d_e;
+    a.scale = s13;
+    if (shared) {
+        a.s_rows = c.T;
+        a.s_panels = c.d_shared / 128;
+        a.s_rows_per_expert = 2 * c.d_shared;
+        a.s_k_blocks = c.d / 64;
+        a.s_out = hs;
+        a.s_ldo = c.d_shared;
+        a.s_scale = ss13;
+    }
+    int64_t tiles = s.NB * a.n_panels + (shared ? chunks * a.s_panels : 0);
+    cudaError_t e = launch_grouped_gemm_skinny(
+        kEpiSwiGLU, fp8, W13, static_cast<int64_t>(c.E) * 2 * c.d_e, X, s.R, c.d, Ws13,
+        2 * static_cast<int64_t>(c.d_shared), Xs, c.T, c.d, a,
+        static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1, small-M kernel");
+    // GEMM2: panels of 256 output rows, K = d_e (d_shared for the shared tiles)
+    a.n_panels = (c.d + 255) / 256;
+    a.rows_per_expert = c.d;
+    a.k_blocks = c.d_e / 64;
+    a.out = y;
+    a.ldo = c.d;
+    a.row_gate = row_gate;
+    a.scale = s2;
+    if (shared) {
+        a.s_panels = (c.d + 255) / 256;
+        a.s_rows_per_expert = c.d;
+        a.s_k_blocks = c.d_shared / 64;
+        a.s_out = ys;
+        a.s_ldo = c.d;
+        a.s_scale = ss2;
+    }
+    tiles = s.NB * a.n_panels + (shared ? chunks * a.s_panels : 0);
+    e = launch_grouped_gemm_skinny(kEpiGate, fp8, W2, static_cast<int64_t>(c.E) * c.d, h, s.R, c.d_e,
+                                   Ws2, c.d, hs, c.T, c.d_shared, a,
+                                   static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2, small-M kernel");
+}
+
+// The small-M kernel serves the layer when the mean rows per expert is small
+// enough that 128-row tiles would mostly multiply padding.
+static bool use_skinny(const moe_config_t& c) {
+    return static_cast<int64_t>(c.T) * c.k <= 32ll * c.E;
+}
+
 static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
                               const void* Ws2_t, void* hs, void* ys, uint32_t* status,
                               cudaStream_t st) {
@@ -287,57 +361,118 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "shared GEMM2");
 }
 
-static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
-                          const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
-                          size_t ws_bytes, cudaStream_t st) {
-    const bool routed = pre_idx == nullptr;
-    moe_status_t r = check_cfg(cfg, routed);
-    if (r != MOE_OK) return r;
-    const moe_config_t& c = *cfg;
-    if (!w || !x || !out) return fail(MOE_ERR_INVALID_ARG, "null weights, x or out");
-    if (!w->W13 || !w->W2) return fail(MOE_ERR_INVALID_ARG, "null routed expert weights");
-    if (routed && !w->Wg_t) return fail(MOE_ERR_INVALID_ARG, "null router weight");
-    if (!routed && !pre_w) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
-    if (c.d_shared && (!w->Ws13 || !w->Ws2))
-        return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared expert weights");
-    const moe_workspace_layout_t L = layout_of(c);
-    if (!ws || ws_bytes < L.total)
-        return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, L.total);
-    if (c.T == 0) return MOE_OK;
-    uint8_t* b = static_cast<uint8_t*>(ws);
-    auto at = [&](size_t o) { return static_cast<void*>(b + o); };
-    uint32_t* status = static_cast<uint32_t*>(at(L.status));
-    int32_t* topk_idx = static_cast<int32_t*>(at(L.topk_idx));
-    float* topk_w = static_cast<float*>(at(L.topk_w));
-    if (routed) {
-        r = do_route_layer(c, x, w->Wg_t, w->bias, topk_idx, topk_w,
-                           static_cast<float*>(at(L.router_partial)), st);
+// Pointers into a layer workspace.
+struct LayerBufs {
+    const moe_workspace_layout_t L;
+    uint8_t* b;
+    void* at(size_t o) const { return static_cast<void*>(b + o); }
+    uint32_t* status() const { return static_cast<uint32_t*>(at(L.status)); }
+    int32_t* meta() const { return static_cast<int32_t*>(at(L.block_metadata)); }
+    int32_t* nb() const { return static_cast<int32_t*>(at(L.num_blocks)); }
+    int32_t* perm_row() const { return static_cast<int32_t*>(at(L.perm_row)); }
+    float* row_gate() const { return static_cast<float*>(at(L.row_gate)); }
+    const int32_t* po() const { return static_cast<const int32_t*>(at(L.padded_offsets)); }
+};
+
+// The front of the layer shared by both weight formats: the router (or the
+// given routing) and the offsets stage.
+static moe_status_t layer_front(const moe_config_t& c, const void* Wg_t, const float* bias,
+                                const void* x, const int32_t* pre_idx, const float* pre_w,
+                                const LayerBufs& B, cudaStream_t st) {
+    int32_t* topk_idx = static_cast<int32_t*>(B.at(B.L.topk_idx));
+    float* topk_w = static_cast<float*>(B.at(B.L.topk_w));
+    if (!pre_idx) {
+        moe_status_t r = do_route_layer(c, x, Wg_t, bias, topk_idx, topk_w,
+                                        static_cast<float*>(B.at(B.L.router_partial)), st);
         if (r != MOE_OK) return r;
     } else {
         topk_idx = const_cast<int32_t*>(pre_idx);
         topk_w = const_cast<float*>(pre_w);
     }
-    int32_t* meta = static_cast<int32_t*>(at(L.block_metadata));
-    int32_t* nb = static_cast<int32_t*>(at(L.num_blocks));
-    int32_t* perm_row = static_cast<int32_t*>(at(L.perm_row));
-    float* row_gate = static_cast<float*>(at(L.row_gate));
-    r = do_offsets(c, topk_idx, topk_w, static_cast<int32_t*>(at(L.counts)),
-                   static_cast<int32_t*>(at(L.padded_offsets)), meta, nb, perm_row,
-                   static_cast<int32_t*>(at(L.row_src)), row_gate, at(L.status), st);
+    return do_offsets(c, topk_idx, topk_w, static_cast<int32_t*>(B.at(B.L.counts)),
+                      static_cast<int32_t*>(B.at(B.L.padded_offsets)), B.meta(), B.nb(),
+                      B.perm_row(), static_cast<int32_t*>(B.at(B.L.row_src)), B.row_gate(),
+                      B.at(B.L.status), st);
+}
+
+static moe_status_t check_layer_args(const moe_config_t* cfg, bool routed, const void* Wg_t,
+                                     const void* x, const float* pre_w, void* out, void* ws,
+                                     size_t ws_bytes) {
+    moe_status_t r = check_cfg(cfg, routed);
     if (r != MOE_OK) return r;
-    cudaError_t e = launch_permute(x, perm_row, at(L.x_perm), c.T, c.d, c.k, st);
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "null x or out");
+    if (routed && !Wg_t) return fail(MOE_ERR_INVALID_ARG, "null router weight");
+    if (!routed && !pre_w) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
+    const size_t need = layout_of(*cfg).total;
+    if (!ws || ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
+    return MOE_OK;
+}
+
+static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                          const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
+                          size_t ws_bytes, cudaStream_t st) {
+    if (!w) return fail(MOE_ERR_INVALID_ARG, "null weights");
+    moe_status_t r = check_layer_args(cfg, pre_idx == nullptr, w->Wg_t, x, pre_w, out, ws, ws_bytes);
+    if (r != MOE_OK) return r;
+    const moe_config_t& c = *cfg;
+    if (!w->W13 || !w->W2) return fail(MOE_ERR_INVALID_ARG, "null routed expert weights");
+    if (c.d_shared && (!w->Ws13 || !w->Ws2))
+        return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared expert weights");
+    if (c.T == 0) return MOE_OK;
+    const LayerBufs B{layout_of(c), static_cast<uint8_t*>(ws)};
+    const moe_workspace_layout_t& L = B.L;
+    r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
+    if (r != MOE_OK) return r;
+    cudaError_t e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
     if (e != cudaSuccess) return cuda_fail(e, "permute");
-    r = do_experts(c, at(L.x_perm), w->W13, w->W2, meta, nb,
-                   static_cast<const int32_t*>(at(L.padded_offsets)), row_gate, at(L.h), at(L.y),
-                   status, st);
-    if (r != MOE_OK) return r;
-    const void* shared = nullptr;
-    if (c.d_shared) {
-        r = do_shared(c, x, w->Ws13, w->Ws2, at(L.hs), at(L.ys), status, st);
+    const void* shared = c.d_shared ? B.at(L.ys) : nullptr;
+    if (use_skinny(c)) {
+        r = do_experts_skinny(c, false, B.at(L.x_perm), w->W13, nullptr, w->W2, nullptr, B.meta(),
+                              B.nb(), B.row_gate(), B.at(L.h), B.at(L.y), B.status(), st, x,
+                              c.d_shared ? w->Ws13 : nullptr, nullptr, w->Ws2, nullptr, B.at(L.hs),
+                              B.at(L.ys));
         if (r != MOE_OK) return r;
-        shared = at(L.ys);
+    } else {
+        r = do_experts(c, B.at(L.x_perm), w->W13, w->W2, B.meta(), B.nb(), B.po(), B.row_gate(),
+                       B.at(L.h), B.at(L.y), B.status(), st);
+        if (r != MOE_OK) return r;
+        if (c.d_shared) {
+            r = do_shared(c, x, w->Ws13, w->Ws2, B.at(L.hs), B.at(L.ys), B.status(), st);
+            if (r != MOE_OK) return r;
+        }
     }
-    e = launch_combine(at(L.y), perm_row, shared, out, c.T, c.d, c.k, st);
+    e = launch_combine(B.at(L.y), B.perm_row(), shared, out, c.T, c.d, c.k, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
+}
+
+static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* w, const void* x,
+                              const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
+                              size_t ws_bytes, cudaStream_t st) {
+    if (!w) return fail(MOE_ERR_INVALID_ARG, "null weights");
+    moe_status_t r = check_layer_args(cfg, pre_idx == nullptr, w->Wg_t, x, pre_w, out, ws, ws_bytes);
+    if (r != MOE_OK) return r;
+    const moe_config_t& c = *cfg;
+    if (!w->W13q || !w->s13 || !w->W2q || !w->s2)
+        return fail(MOE_ERR_INVALID_ARG, "null routed expert codes or scales");
+    if (c.d_shared && (!w->Ws13q || !w->ss13 || !w->Ws2q || !w->ss2))
+        return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared expert codes or scales");
+    if (c.T == 0) return MOE_OK;
+    const LayerBufs B{layout_of(c), static_cast<uint8_t*>(ws)};
+    const moe_workspace_layout_t& L = B.L;
+    r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
+    if (r != MOE_OK) return r;
+    void* x16 = c.d_shared ? B.at(L.x16) : nullptr;
+    cudaError_t e = launch_permute_f16(x, B.perm_row(), B.at(L.x_perm), x16, c.T, c.d, c.k,
+                                       B.status(), st);
+    if (e != cudaSuccess) return cuda_fail(e, "permute (f16)");
+    r = do_experts_skinny(c, true, B.at(L.x_perm), w->W13q, w->s13, w->W2q, w->s2, B.meta(), B.nb(),
+                          B.row_gate(), B.at(L.h), B.at(L.y), B.status(), st, x16,
+                          c.d_shared ? w->Ws13q : nullptr, w->ss13, w->Ws2q, w->ss2, B.at(L.hs),
+                          B.at(L.ys));
+    if (r != MOE_OK) return r;
+    e = launch_combine(B.at(L.y), B.perm_row(), c.d_shared ? B.at(L.ys) : nullptr, out, c.T, c.d,
+                       c.k, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
 }
 
@@ -385,6 +520,23 @@ moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void* W1, 
     if (e == cudaSuccess) e = launch_pack_transpose(W3, W13, d, de, dd * dde, 2 * dde * dd, d, 2, E, st);
     if (e == cudaSuccess) e = launch_pack_transpose(W2, W2_t, de, d, dde * dd, dd * dde, de, 0, E, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack experts");
+}
+
+moe_status_t moe_pack_experts_fp8(int32_t E, int32_t d, int32_t de, const void* W1, const void* W3,
+                                  const void* W2, void* W13q, float* s13, void* W2q, float* s2,
+                                  void* stream) {
+    if (E <= 0 || d <= 0 || de <= 0 || !W1 || !W3 || !W2 || !W13q || !s13 || !W2q || !s2)
+        return fail(MOE_ERR_INVALID_ARG, "bad e4m3 expert pack args");
+    if (d % 128 || de % 128) return fail(MOE_ERR_UNSUPPORTED, "d and de must be multiples of 128");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t dd = d, dde = de;
+    uint8_t* q13 = static_cast<uint8_t*>(W13q);
+    uint8_t* q2 = static_cast<uint8_t*>(W2q);
+    cudaError_t e = launch_pack_fp8(W1, q13, s13, d, de, dd * dde, 2 * dde * dd, 2 * dde, d, 1, E, st);
+    if (e == cudaSuccess)
+        e = launch_pack_fp8(W3, q13, s13, d, de, dd * dde, 2 * dde * dd, 2 * dde, d, 2, E, st);
+    if (e == cudaSuccess) e = launch_pack_fp8(W2, q2, s2, de, d, dde * dd, dd * dde, dd, de, 0, E, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack experts (e4m3)");
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg_t, const float* bias,
@@ -460,6 +612,45 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
                       h, y, status, static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_permute_f16(const moe_config_t* cfg, const void* x, const int32_t* perm_row,
+                             void* x_perm16, void* x16, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x || !perm_row || !x_perm16) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    cudaError_t e = launch_permute_f16(x, perm_row, x_perm16, x16, cfg->T, cfg->d, cfg->k, status,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute (f16)");
+}
+
+moe_status_t moe_grouped_gemm_swiglu_skinny(const moe_config_t* cfg, const void* x_perm,
+                                            const void* W13, const void* W2_t,
+                                            const int32_t* block_metadata,
+                                            const int32_t* num_blocks, const float* row_gate,
+                                            void* h, void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x_perm || !W13 || !W2_t || !block_metadata || !num_blocks || !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts_skinny(*cfg, false, x_perm, W13, nullptr, W2_t, nullptr, block_metadata,
+                             num_blocks, row_gate, h, y, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t* cfg, const void* x_perm16,
+                                         const void* W13q, const float* s13, const void* W2q,
+                                         const float* s2, const int32_t* block_metadata,
+                                         const int32_t* num_blocks, const float* row_gate,
+                                         void* h16, void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x_perm16 || !W13q || !s13 || !W2q || !s2 || !block_metadata || !num_blocks || !h16 || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts_skinny(*cfg, true, x_perm16, W13q, s13, W2q, s2, block_metadata, num_blocks,
+                             row_gate, h16, y, status, static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_grouped_gemm_swiglu_gather(const moe_config_t* cfg, const void* x,
                                             const int32_t* row_src, const void* W13,
                                             const void* W2_t, const int32_t* block_metadata,
@@ -508,6 +699,21 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t* cfg, const moe_weights_
                                      void* out, void* ws, size_t ws_bytes, void* stream) {
     if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "null pre-routed indices");
     return layer(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* w, const void* x,
+                               void* out, void* ws, size_t ws_bytes, void* stream) {
+    return layer_fp8(cfg, w, x, nullptr, nullptr, out, ws, ws_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer_fwd_fp8_prerouted(const moe_config_t* cfg, const moe_weights_fp8_t* w,
+                                         const void* x, const int32_t* topk_idx,
+                                         const float* topk_w, void* out, void* ws,
+                                         size_t ws_bytes, void* stream) {
+    if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "null pre-routed indices");
+    return layer_fp8(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_get_device_status(void* ws, uint32_t* bits, void* stream) {

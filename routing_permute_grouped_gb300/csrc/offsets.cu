@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kScatterThreads)
     const int64_t a1 = min(A, a0 + kChunk);
     bool bad = false;
     for (int64_t a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
-        const int e = __ldg(idx + a);
+        const int e = ld_dep(idx + a);
         if (e >= 0 && e < E)
             atomicAdd(&hist[e], 1);
         else
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kScatterThreads)
         const int64_t a = base + threadIdx.x;
         int e = -1;
         if (a < a1) {
-            e = __ldg(idx + a);
+            e = ld_dep(idx + a);
             if (e < 0 || e >= E) {
                 perm_row[a] = -1;  // flagged by the histogram pass
                 e = -1;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kScatterThreads)
             const int r = running[e] + off + rank;
             perm_row[a] = r;
             row_src[r] = static_cast<int32_t>(a);
-            row_gate[r] = w ? __ldg(w + a) : 1.0f;
+            row_gate[r] = w ? ld_dep(w + a) : 1.0f;
         }
         __syncthreads();
         if (e >= 0 && leader) {
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     __syncthreads();
     bool bad = false;
     for (int a = tid; a < A; a += blockDim.x) {
-        const int e = __ldg(idx + a);
+        const int e = ld_dep(idx + a);
         if (e >= 0 && e < E)
             atomicAdd(&hist[e], 1);
         else
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kSmallThreads)
         const int a = base + tid;
         int e = -1;
         if (a < A) {
-            e = __ldg(idx + a);
+            e = ld_dep(idx + a);
             if (e < 0 || e >= E) {
                 perm_row[a] = -1;
                 e = -1;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kSmallThreads)
             const int r = running[e] + off + rank;
             perm_row[a] = r;
             row_src[r] = a;
-            row_gate[r] = w ? __ldg(w + a) : 1.0f;
+            row_gate[r] = w ? ld_dep(w + a) : 1.0f;
         }
         __syncthreads();
         if (e >= 0 && leader) {

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -48,6 +49,65 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
     k_pack_transpose<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(in),
                                                  static_cast<__nv_bfloat16*>(out), rows, cols,
                                                  in_bstride, out_bstride, out_ld, mode);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------- e4m3 weights --
+// Per-output-channel scale of in [rows, cols] (column c = output channel c):
+// amax over the column (exact in fp32), scale = amax / 448 by an IEEE
+// single-precision division, 1 for an all-zero column.  One thread per
+// column, rows walked in order (coalesced across the warp).
+__global__ void k_col_scale(const __nv_bfloat16* __restrict__ in, float* __restrict__ scale,
+                            int rows, int cols, int64_t in_bstride, int64_t scale_bstride,
+                            int mode) {
+    const int b = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    const __nv_bfloat16* src = in + b * in_bstride + c;
+    float amax = 0.0f;
+    for (int r = 0; r < rows; ++r) amax = fmaxf(amax, fabsf(__bfloat162float(src[(int64_t)r * cols])));
+    scale[b * scale_bstride + packed_row(c, mode)] = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+// Codes of the transposed matrix: out[packed_row(c), r] = e4m3(in[r, c] /
+// scale[c]), the quotient an IEEE single-precision division and the code its
+// nearest e4m3 value (ties to even, saturating).  32x32 tiles through shared
+// memory as in k_pack_transpose.
+__global__ void k_pack_quant(const __nv_bfloat16* __restrict__ in, uint8_t* __restrict__ out,
+                             const float* __restrict__ scale, int rows, int cols,
+                             int64_t in_bstride, int64_t out_bstride, int64_t scale_bstride,
+                             int out_ld, int mode) {
+    __shared__ float tile[32][33];
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const __nv_bfloat16* src = in + b * in_bstride;
+    uint8_t* dst = out + b * out_bstride;
+    const float* sc = scale + b * scale_bstride;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = __bfloat162float(src[(int64_t)r * cols + c]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) {
+            const int64_t pr = packed_row(c, mode);
+            dst[pr * out_ld + r] = f32_to_e4m3(__fdiv_rn(tile[threadIdx.x][i], __ldg(sc + pr)));
+        }
+    }
+}
+
+cudaError_t launch_pack_fp8(const void* in, uint8_t* out, float* scale, int rows, int cols,
+                            int64_t in_bstride, int64_t out_bstride, int64_t scale_bstride,
+                            int out_ld, int mode, int batch, cudaStream_t stream) {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
+    k_col_scale<<<dim3((cols + 127) / 128, batch), 128, 0, stream>>>(src, scale, rows, cols, in_bstride,
+                                                                      scale_bstride, mode);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
+    k_pack_quant<<<grid, dim3(32, 8), 0, stream>>>(src, out, scale, rows, cols, in_bstride, out_bstride,
+                                                   scale_bstride, out_ld, mode);
     return cudaGetLastError();
 }
 

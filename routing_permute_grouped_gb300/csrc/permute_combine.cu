@@ -11,6 +11,7 @@
 //          (sec. 6.4: fixed summation order, wide accumulation, no atomics).
 //          Bytes per token: (k + 1 [+1]) * d * 2.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -31,14 +32,14 @@ __global__ void __launch_bounds__(kPCWarps * 32)
     if (t >= T) return;
     int rows[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? __ldg(perm_row + (int64_t)t * k + j) : -1;
+    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
     const uint4* src = x + (int64_t)t * nvec;
     for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
         uint4 buf[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int v = v0 + u * 32;
-            if (v < nvec) buf[u] = __ldg(src + v);
+            if (v < nvec) buf[u] = ld_dep(src + v);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -51,6 +52,66 @@ __global__ void __launch_bounds__(kPCWarps * 32)
             }
         }
     }
+}
+
+// Eight bf16 values -> eight f16 values (exact for magnitudes in [2^-17,
+// 65504] and zero); sets ovf for a finite value past f16's range.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v, bool& ovf) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        ovf |= (fabsf(lo) >= 65520.0f && !isinf(lo)) || (fabsf(hi) >= 65520.0f && !isinf(hi));
+        const __half2 h = __floats2half2_rn(lo, hi);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The permute of the e4m3-weight path: the same token-major scatter, each row
+// written as f16; x16 (if given) also receives the token's dense f16 row for
+// the shared expert.
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_permute_f16(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
+                  uint4* __restrict__ x_perm, uint4* __restrict__ x16, int T, int nvec, int k,
+                  uint32_t* status) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kPCWarps + warp;
+    if (t >= T) return;
+    int rows[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
+    const uint4* src = x + (int64_t)t * nvec;
+    bool ovf = false;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 buf[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + u * 32;
+            if (v < nvec) buf[u] = bf16x8_to_f16x8(ld_dep(src + v), ovf);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (rows[j] < 0) continue;
+            uint4* dst = x_perm + (int64_t)rows[j] * nvec;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32;
+                if (v < nvec) dst[v] = buf[u];
+            }
+        }
+        if (x16) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32;
+                if (v < nvec) x16[(int64_t)t * nvec + v] = buf[u];
+            }
+        }
+    }
+    if (ovf && status) atomicOr(status, 0x4u);
 }
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
@@ -89,7 +150,7 @@ __global__ void __launch_bounds__(kPCWarps * 32)
     if (t >= T) return;
     int rows[K];
 #pragma unroll
-    for (int j = 0; j < K; ++j) rows[j] = __ldg(perm_row + (int64_t)t * K + j);
+    for (int j = 0; j < K; ++j) rows[j] = ld_dep(perm_row + (int64_t)t * K + j);
     for (int v0 = lane; v0 < nvec; v0 += 64) {
         const int v1 = v0 + 32;
         const bool has1 = v1 < nvec;
@@ -98,14 +159,14 @@ __global__ void __launch_bounds__(kPCWarps * 32)
         for (int j = 0; j < K; ++j) {
             if (rows[j] >= 0) {
                 const uint4* src = y + (int64_t)rows[j] * nvec;
-                in0[j] = __ldg(src + v0);
-                if (has1) in1[j] = __ldg(src + v1);
+                in0[j] = ld_dep(src + v0);
+                if (has1) in1[j] = ld_dep(src + v1);
             }
         }
         uint4 sh0 = make_uint4(0, 0, 0, 0), sh1 = make_uint4(0, 0, 0, 0);
         if (shared_out) {
-            sh0 = __ldg(shared_out + (int64_t)t * nvec + v0);
-            if (has1) sh1 = __ldg(shared_out + (int64_t)t * nvec + v1);
+            sh0 = ld_dep(shared_out + (int64_t)t * nvec + v0);
+            if (has1) sh1 = ld_dep(shared_out + (int64_t)t * nvec + v1);
         }
         float a0[8], a1[8];
 #pragma unroll
@@ -152,6 +213,15 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
     return launch_pdl(k_permute, dim3(grid), dim3(kPCWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm), T, nvec,
                       k);
+}
+
+cudaError_t launch_permute_f16(const void* x, const int32_t* perm_row, void* x_perm16, void* x16,
+                               int T, int d, int k, uint32_t* status, cudaStream_t stream) {
+    const int nvec = d / 8;
+    const int grid = (T + kPCWarps - 1) / kPCWarps;
+    return launch_pdl(k_permute_f16, dim3(grid), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm16),
+                      static_cast<uint4*>(x16), T, nvec, k, status);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,

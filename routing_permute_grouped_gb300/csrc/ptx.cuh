@@ -20,6 +20,17 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Load of data that an earlier kernel of the stream wrote.  Every kernel of
+// the library is launched with programmatic dependent launch, so it may start
+// while that kernel still runs; the read-only path (ld.global.nc, __ldg)
+// assumes data fixed for the whole life of the kernel, and such a load is not
+// kept behind griddepcontrol.wait.  A coherent load issued after pdl_wait()
+// sees the finished data.
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T* p) {
+    return __ldcg(p);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -144,6 +155,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with f16 A and B (format code 0 in bits [7,10) and [10,13)).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, M = 128, N from idesc, K = 16.
@@ -347,6 +363,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 codes (low byte = first element) -> two f16 values (low half =
+// first element).  Exact: every e4m3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+    return r;
+}
+
+// Nearest e4m3 code of v, ties to even, saturating at +-448.
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return static_cast<uint8_t>(r & 0xFFu);  // the second source lands in the low byte
 }
 
 }  // namespace moe

@@ -51,8 +51,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
         l[i] = -FLT_MAX;
         if (e < E) {
             float v = 0.0f;
-            for (int sl = 0; sl < S; ++sl) v += __ldg(partial + (static_cast<int64_t>(sl) * T + t) * E + e);
-            if (bias) v += __ldg(bias + e);
+            for (int sl = 0; sl < S; ++sl) v += ld_dep(partial + (static_cast<int64_t>(sl) * T + t) * E + e);
+            if (bias) v += ld_dep(bias + e);
             l[i] = v;
             s_logit[warp][e] = v;
         }

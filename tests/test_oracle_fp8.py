@@ -186,3 +186,18 @@ def test_grouped_w8_matches_rows_w8():
     assert np.array_equal(y[off["perm_row"]], yr) and np.array_equal(h[off["perm_row"]], hr)
     pad = off["row_src"] < 0
     assert np.all(np.isnan(y[pad]))
+
+
+def test_shared_w8_equals_one_expert_rows():
+    """The e4m3 shared expert is the one-expert routed evaluation with gate 1,
+    and with exactly representable weights it equals the bf16 shared expert."""
+    rng = np.random.default_rng(4)
+    d, ds, n = 64, 48, 5
+    Ws1 = _representable_matrix(rng, d, ds)[0]
+    Ws3 = _representable_matrix(rng, d, ds)[0]
+    Ws2 = _representable_matrix(rng, ds, d)[0]
+    x = _bf16_bits(rng.standard_normal((n, d)).astype(np.float32))
+    qs = oracle.quantize_shared(dict(Ws1=Ws1, Ws3=Ws3, Ws2=Ws2))
+    h8, y8 = oracle.shared_expert_w8(x, qs)
+    h16, y16 = oracle.shared_expert(x, Ws1, Ws3, Ws2)
+    assert np.array_equal(h8, h16) and np.array_equal(y8, y16)
