@@ -17,6 +17,8 @@ Prints one JSON line:
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload
 
 ``--impl reference`` times the CPU oracle as the reference arm.
+``--weights fp8`` runs the layer with e4m3 expert weights (per-output-channel
+fp32 scales; moe_layer_fwd_fp8) instead of bf16 ones.
 """
 from __future__ import annotations
 
@@ -222,7 +224,7 @@ def run_reference(args, shape, rank, world):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_dict(shape),
+        "data": "synthetic", "config": config_dict(shape, weights=args.weights),
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -231,13 +233,14 @@ def run_reference(args, shape, rank, world):
 
 
 METRIC = "MoE layer fwd useful TFLOP/s (bf16, fp32 accumulate)"
+METRIC_FP8 = "MoE layer fwd useful TFLOP/s (e4m3 expert weights, fp32 accumulate)"
 
 
-def config_dict(shape, permute="separate"):
+def config_dict(shape, permute="separate", weights="bf16"):
     return {"workload": f"{shape.name}: T={shape.T} d={shape.d} d_e={shape.d_e} E={shape.E} "
                         f"k={shape.k} groups={shape.n_groups}/{shape.topk_groups} "
                         f"pad={shape.pad} shared={shape.d_shared}",
-            "permute": permute,
+            "permute": permute, "expert_weights": weights,
             "l2": "inputs larger than L2 (expert weights and permuted rows exceed 129 MB)",
             "parallelism": "replicas"}
 
@@ -257,9 +260,12 @@ def run_ours(args, shape, rank, world, local):
         if inp.get(key) is not None:
             inp[key] = inp[key].to(dev)
     cfg = moe.config_of(shape)
+    fp8 = args.weights == "fp8"
+    if fp8 and args.permute != "separate":
+        raise SystemExit("--weights fp8 runs with the separate permute")
     layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
                          bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
-                         Ws2=inp.get("Ws2"))
+                         Ws2=inp.get("Ws2"), fp8=fp8)
     x = inp["x"]
     out = torch.empty_like(x)
     L = layer.layout
@@ -274,9 +280,15 @@ def run_ours(args, shape, rank, world, local):
     meta, nb = buf("block_metadata", i32, (NB, 3)), buf("num_blocks", i32, (1,))
     perm_row, row_src = buf("perm_row", i32, (A,)), buf("row_src", i32, (R,))
     row_gate = buf("row_gate", f32, (R,))
-    x_perm, h, y = buf("x_perm", bf, (R, d)), buf("h", bf, (R, de)), buf("y", bf, (R, d))
-    hs = buf("hs", bf, (T, ds)) if ds else None
+    act = torch.float16 if fp8 else bf  # the e4m3 path keeps activations in f16
+    x_perm, h, y = buf("x_perm", act, (R, d)), buf("h", act, (R, de)), buf("y", bf, (R, d))
+    hs = buf("hs", act, (T, ds)) if ds else None
     ys = buf("ys", bf, (T, d)) if ds else None
+    x16 = buf("x16", act, (T, d)) if (fp8 and ds) else None
+    # the layer's kernel choice: the small-M kernel (shared expert merged
+    # into its launches) when the mean rows per expert is at most 32, and
+    # always with e4m3 weights
+    skinny = fp8 or T * k <= 32 * E
     status_word = buf("status", i32, (1,))
     nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
     router_partial = buf("router_partial", f32, (nsplit,)) if nsplit else None
@@ -296,11 +308,19 @@ def run_ours(args, shape, rank, world, local):
                               row_gate, offs_ws)
         if ev is not None:
             ev[2].record()
-        if args.permute == "separate":
+        if fp8:
+            moe.moe_permute_f16(cfg, x, perm_row, x_perm, x16, status_word)
+        elif args.permute == "separate":
             moe.moe_permute(cfg, x, perm_row, x_perm)
         if ev is not None:
             ev[3].record()
-        if args.permute == "separate":
+        if fp8:
+            moe.moe_grouped_gemm_swiglu_fp8(cfg, x_perm, layer.W13q, layer.s13, layer.W2q, layer.s2,
+                                            meta, nb, row_gate, h, y, status_word)
+        elif skinny:
+            moe.moe_grouped_gemm_swiglu_skinny(cfg, x_perm, layer.W13, layer.W2_t, meta, nb,
+                                               row_gate, h, y, status_word)
+        elif args.permute == "separate":
             moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate,
                                         h, y, status_word)
         else:
@@ -308,7 +328,10 @@ def run_ours(args, shape, rank, world, local):
                                                row_gate, h, y, status_word)
         if ev is not None:
             ev[4].record()
-        if ds:
+        if ds and fp8:
+            moe.moe_shared_expert_fp8(cfg, x16, layer.Ws13q, layer.ss13, layer.Ws2q, layer.ss2, hs,
+                                      ys, status_word)
+        elif ds:
             moe.moe_shared_expert(cfg, x, layer.Ws13, layer.Ws2_t, hs, ys, status_word)
         if ev is not None:
             ev[5].record()
@@ -317,11 +340,13 @@ def run_ours(args, shape, rank, world, local):
             ev[6].record()
 
     # kernels per layer forward: router (2 when split-K), offsets (1 or 3),
-    # permute (or none when fused), 2 routed GEMMs, 2 shared-expert GEMMs,
+    # permute (or none when fused), 2 routed GEMMs, 2 shared-expert GEMMs
+    # (none on the small-M kernel, whose launches carry the shared tiles),
     # combine
     offsets_launches = 1 if A <= 4096 else 3  # one-CTA offsets kernel for small batches
     launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
-                         + (1 if args.permute == "separate" else 0) + 2 + (2 if ds else 0) + 1)
+                         + (1 if args.permute == "separate" else 0) + 2
+                         + (2 if ds and not skinny else 0) + 1)
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():
@@ -407,7 +432,7 @@ def run_ours(args, shape, rank, world, local):
     pk = peaks()
     gemm_flops = ledger.routed_flops(A, d, de)
     active = sum(1 for c in counts_h if c > 0)
-    gemm_bytes = ledger.grouped_gemm_bytes_alg(A, active, d, de)
+    gemm_bytes = ledger.grouped_gemm_bytes_alg(A, active, d, de, fp8_weights=fp8)
     gemm_s = stage_ms["grouped_gemm"] / 1e3
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     # the stage is tensor-bound when its FLOP per byte exceeds the machine
@@ -427,16 +452,21 @@ def run_ours(args, shape, rank, world, local):
     comb_gbs = comb_bytes / (stage_ms["combine"] / 1e3) / 1e9
     traffic = recorded_traffic("grouped_gemm", shape.name)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_dict(shape, args.permute),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights, f16 MMA" if fp8 else "bf16",
+        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": dict(roof, kernel="grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
-                         timing="stage pass: CUDA events around moe_grouped_gemm_swiglu",
+                         timing="stage pass: CUDA events around " + (
+                             "moe_grouped_gemm_swiglu_fp8" if fp8 else
+                             "moe_grouped_gemm_swiglu_skinny" if skinny else
+                             "moe_grouped_gemm_swiglu"),
                          traffic=traffic),
         "stages": {"ms": {n: round(v, 4) for n, v in stage_ms.items()},
                    "serial_sum_ms": round(sum(stage_ms.values()), 4),
@@ -456,7 +486,9 @@ def run_ours(args, shape, rank, world, local):
         tf, dt, threads = oracle_sample_tflops(shape, host, n)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {n} tokens of the workload: router, routed "
-                                          f"experts and shared expert ({dt:.1f} s)"}
+                                          f"experts and shared expert ({dt:.1f} s)"
+                                          + (", bf16 weights (the e4m3 evaluation does the same "
+                                             "fp64 work)" if fp8 else "")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -488,6 +520,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--permute", choices=["separate", "fused"], default="separate",
                     help="permute as its own kernel, or fused into GEMM1's A load")
+    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                    help="expert weights in bf16, or e4m3 with per-output-channel scales")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     shape = synth.WORKLOADS[args.workload]

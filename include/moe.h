@@ -357,6 +357,17 @@ moe_status_t moe_shared_expert(const moe_config_t *cfg, const void *x, const voi
                                const void *Ws2_t, void *hs, void *ys, uint32_t *status,
                                void *stream);
 
+/* a6 with e4m3 weights (moe_pack_experts_fp8 with E = 1), on the kernel of
+ * moe_grouped_gemm_swiglu_fp8 with a dense tile list: chunks of 128 token
+ * rows times panels of 256 weight rows.
+ *   x16 f16 [T, d] (moe_permute_f16), hs16 f16 [T, d_shared] holding
+ *   bf16-rounded values, ys bf16 [T, d]; status as above.
+ * The layer (moe_layer_fwd_fp8) puts these tiles into its routed launches
+ * instead, where they fill SMs that this call alone would leave idle. */
+moe_status_t moe_shared_expert_fp8(const moe_config_t *cfg, const void *x16, const void *Ws13q,
+                                   const float *ss13, const void *Ws2q, const float *ss2,
+                                   void *hs16, void *ys, uint32_t *status, void *stream);
+
 /* a7. Combine ("MoE & MLA operators", sec. 2.5 and 6.4: k-way sum back into
  * token order in a fixed order, with wide accumulation):
  *   out[t] = bf16( sum_{j=0..k-1} y[perm_row[t*k + j]] + shared_out[t] )

@@ -31,6 +31,7 @@ __all__ = [
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
     "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_f16", "moe_grouped_gemm_swiglu_skinny",
     "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
+    "moe_shared_expert_fp8",
 ]
 
 MOE_OK = 0
@@ -112,6 +113,7 @@ def load():
         "moe_permute_f16": (ctypes.c_int, [CP] + [P] * 6),
         "moe_grouped_gemm_swiglu_skinny": (ctypes.c_int, [CP] + [P] * 10),
         "moe_grouped_gemm_swiglu_fp8": (ctypes.c_int, [CP] + [P] * 12),
+        "moe_shared_expert_fp8": (ctypes.c_int, [CP] + [P] * 9),
         "moe_layer_fwd_fp8": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P, SZ, P]),
         "moe_layer_fwd_fp8_prerouted": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P,
                                                        P, P, SZ, P]),
@@ -279,6 +281,13 @@ def moe_grouped_gemm_swiglu_fp8(cfg, x_perm16, W13q, s13, W2q, s2, block_metadat
         ctypes.byref(cfg), _ptr(x_perm16), _ptr(W13q), _ptr(s13), _ptr(W2q), _ptr(s2),
         _ptr(block_metadata), _ptr(num_blocks), _ptr(row_gate), _ptr(h16), _ptr(y), _ptr(status),
         _stream(stream)))
+
+
+def moe_shared_expert_fp8(cfg, x16, Ws13q, ss13, Ws2q, ss2, hs16, ys, status=None,
+                          stream=None) -> None:
+    _check(load().moe_shared_expert_fp8(ctypes.byref(cfg), _ptr(x16), _ptr(Ws13q), _ptr(ss13),
+                                        _ptr(Ws2q), _ptr(ss2), _ptr(hs16), _ptr(ys), _ptr(status),
+                                        _stream(stream)))
 
 
 def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:

@@ -831,7 +831,7 @@ static bool make_tmap_box(CUtensorMap* tm, const void* ptr, int64_t rows, int64_
 }
 
 bool make_tensor_map_2d(void* tmap, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
-                        int dtype, int box_cols, int box_rows, bool swizzle128) {
+                        int dtype, int box_cols, int box_rows, int swizzle_bytes) {
     PFN_encodeTiled enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -840,7 +840,9 @@ bool make_tensor_map_2d(void* tmap, const void* ptr, int64_t rows, int64_t cols,
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(static_cast<CUtensorMap*>(tmap), static_cast<CUtensorMapDataType>(dtype), 2,
                      const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

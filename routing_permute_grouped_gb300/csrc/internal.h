@@ -101,10 +101,11 @@ int num_sms();
 // rows) follow the routed tiles when s_rows > 0.
 struct SkinnyArgs {
     const int32_t* block_metadata;  // [nb_cap, 3] [expert, m_start, valid_m]
-    const int32_t* num_blocks;      // [1]
+    const int32_t* num_blocks;      // [1], or null for a launch of shared-expert tiles only
     int32_t nb_cap;                 // capacity of the block table
     int32_t n_experts;              // valid expert ids are [0, n_experts)
     int32_t n_panels;               // routed panels of 256 weight rows per block
+    int32_t n_chunks;               // token-row chunks per block (e4m3 tiles hold <= 64 rows)
     int32_t rows_per_expert;        // weight rows per expert (2 d_e or d)
     int32_t k_blocks;               // routed K / 64
     void* out;                      // routed output [out_rows, ldo] (bf16, or f16 h)
@@ -123,6 +124,10 @@ struct SkinnyArgs {
     uint32_t* status;               // device error word, may be null
 };
 
+// Token rows per tile of the small-M kernel (a block with more valid rows is
+// split into n_chunks chunks of this many rows).
+int skinny_tile_rows(bool fp8);
+
 // Small-M grouped GEMM (epi = kEpiSwiGLU or kEpiGate).  W / Ws: weights
 // [rows, K] K-major, bf16 or (fp8) e4m3 codes; X / Xs: token rows [rows, K],
 // bf16 or (fp8) f16.  max_tiles bounds the tile count (grid size).
@@ -133,9 +138,10 @@ cudaError_t launch_grouped_gemm_skinny(int epi, bool fp8, const void* W, int64_t
 
 // 2D tensor map of a row-major [rows, cols] matrix of elem_bytes-wide
 // elements (dtype: a CUtensorMapDataType value) with a {box_cols, box_rows}
-// box, the 128-byte swizzle or none.  False if the driver refuses it.
+// box and the 128-byte, 64-byte or no (0) swizzle.  False if the driver
+// refuses it.
 bool make_tensor_map_2d(void* tmap, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
-                        int dtype, int box_cols, int box_rows, bool swizzle128);
+                        int dtype, int box_cols, int box_rows, int swizzle_bytes);
 
 // e4m3 packing: per-output-channel scales of W [batch][rows][cols] (column c
 // = output channel c), written to scale[b * scale_bstride + packed_row(c,

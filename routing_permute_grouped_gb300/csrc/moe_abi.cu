@@ -4,6 +4,7 @@
 // the device, except moe_get_device_status().
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -275,8 +276,13 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const voi
                                       void* hs = nullptr, void* ys = nullptr) {
     const Sizes s = sizes_of(c);
     const bool shared = c.d_shared > 0 && Ws13 != nullptr;
-    const int64_t chunks = (static_cast<int64_t>(c.T) + 127) / 128;
+    const int rows = skinny_tile_rows(fp8);
+    const int64_t chunks = (static_cast<int64_t>(c.T) + rows - 1) / rows;  // shared-expert tiles
+    // a block holds at most min(P, T*k) valid rows (T*k: an expert may repeat
+    // within a token of pre-routed input)
+    const int64_t max_rows = std::min<int64_t>(c.pad_multiple, static_cast<int64_t>(c.T) * c.k);
     SkinnyArgs a{};
+    a.n_chunks = static_cast<int32_t>((max_rows + rows - 1) / rows);
     a.block_metadata = meta;
     a.num_blocks = nb;
     a.nb_cap = static_cast<int32_t>(s.NB);
@@ -299,7 +305,7 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const voi
         a.s_ldo = c.d_shared;
         a.s_scale = ss13;
     }
-    int64_t tiles = s.NB * a.n_panels + (shared ? chunks * a.s_panels : 0);
+    int64_t tiles = s.NB * a.n_panels * a.n_chunks + (shared ? chunks * a.s_panels : 0);
     cudaError_t e = launch_grouped_gemm_skinny(
         kEpiSwiGLU, fp8, W13, static_cast<int64_t>(c.E) * 2 * c.d_e, X, s.R, c.d, Ws13,
         2 * static_cast<int64_t>(c.d_shared), Xs, c.T, c.d, a,
@@ -321,7 +327,7 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const voi
         a.s_ldo = c.d;
         a.s_scale = ss2;
     }
-    tiles = s.NB * a.n_panels + (shared ? chunks * a.s_panels : 0);
+    tiles = s.NB * a.n_panels * a.n_chunks + (shared ? chunks * a.s_panels : 0);
     e = launch_grouped_gemm_skinny(kEpiGate, fp8, W2, static_cast<int64_t>(c.E) * c.d, h, s.R, c.d_e,
                                    Ws2, c.d, hs, c.T, c.d_shared, a,
                                    static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
@@ -676,6 +682,23 @@ moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const voi
     if (!x || !Ws13 || !Ws2_t || !hs || !ys) return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
     return do_shared(*cfg, x, Ws13, Ws2_t, hs, ys, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_shared_expert_fp8(const moe_config_t* cfg, const void* x16, const void* Ws13q,
+                                   const float* ss13, const void* Ws2q, const float* ss2, void* hs16,
+                                   void* ys, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (!x16 || !Ws13q || !ss13 || !Ws2q || !ss2 || !hs16 || !ys)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    // the routed part of the launch is empty: no block table, only the dense
+    // shared-expert tiles
+    moe_config_t c = *cfg;
+    return do_experts_skinny(c, true, x16, Ws13q, ss13, Ws2q, ss2, nullptr, nullptr, nullptr, nullptr,
+                             nullptr, status, static_cast<cudaStream_t>(stream), x16, Ws13q, ss13,
+                             Ws2q, ss2, hs16, ys);
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y, const int32_t* perm_row,

@@ -78,12 +78,17 @@ def grouped_gemm_bytes_page(A: int, E: int, d: int, d_e: int, b: int = BF16) -> 
     return b * (3 * A * d + 3 * E * d * d_e)
 
 
-def grouped_gemm_bytes_alg(A: int, active_experts: int, d: int, d_e: int, b: int = BF16) -> int:
+def grouped_gemm_bytes_alg(A: int, active_experts: int, d: int, d_e: int, b: int = BF16,
+                           fp8_weights: bool = False) -> int:
     """Algorithmic bytes of the two grouped GEMMs (padding excluded): x_perm
     rows read and y rows written (A*d each), h written and read back
     (2*A*d_e), and the weights of every expert that received a row
-    (3*d*d_e each)."""
-    return b * (2 * A * d + 2 * A * d_e + active_experts * 3 * d * d_e)
+    (3*d*d_e each, b bytes; with e4m3 weights one byte each plus one fp32
+    scale per output channel, 2*d_e + d per expert)."""
+    act = b * (2 * A * d + 2 * A * d_e)
+    if fp8_weights:
+        return act + active_experts * (3 * d * d_e + 4 * (2 * d_e + d))
+    return act + b * active_experts * 3 * d * d_e
 
 
 def gemm1_flops(rows: int, d: int, d_e: int) -> int:

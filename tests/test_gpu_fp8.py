@@ -208,6 +208,27 @@ def test_fp8_stage(name):
     _compare_rows(shape, ref, h16, y)
 
 
+def test_shared_expert_fp8_stage():
+    shape, inp, oin, ref = prepared("full_blocks", True)
+    cfg = moe.config_of(shape)
+    T, d, ds = shape.T, shape.d, shape.d_shared
+    q13 = torch.empty((1, 2 * ds, d), dtype=torch.uint8, device="cuda")
+    s13 = torch.empty((1, 2 * ds), dtype=torch.float32, device="cuda")
+    q2 = torch.empty((1, d, ds), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty((1, d), dtype=torch.float32, device="cuda")
+    moe.moe_pack_experts_fp8(cuda(inp["Ws1"]).unsqueeze(0), cuda(inp["Ws3"]).unsqueeze(0),
+                             cuda(inp["Ws2"]).unsqueeze(0), q13, s13, q2, s2)
+    x16 = cuda(inp["x"]).half()
+    hs16 = torch.full((T, ds), float("nan"), dtype=torch.float16, device="cuda")
+    ys = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_shared_expert_fp8(cfg, x16, q13, s13, q2, s2, hs16, ys, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(hs16.double().cpu().numpy(), ref["hs"], "hs (e4m3)")
+    assert_close(ys.double().cpu().numpy(), ref["ys"], "ys (e4m3)")
+
+
 # -------------------------------------------------------------- layer ----
 def _make_layer(shape, inp, fp8):
     cfg = moe.config_of(shape)

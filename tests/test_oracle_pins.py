@@ -358,3 +358,14 @@ def test_grouped_gemm_algorithmic_bytes():
     b = ledger.grouped_gemm_bytes_alg(8192 * 4, 8, 7168, 2048)
     assert round(b / 1e9, 3) == 1.913
     assert ledger.grouped_gemm_bytes_alg(0, 3, 64, 32) == 2 * 3 * 3 * 64 * 32
+
+
+def test_grouped_bytes_with_e4m3_weights():
+    """e4m3 weights: one byte per weight plus a 4-byte scale per output
+    channel; the activation bytes are those of the bf16 ledger."""
+    A, act, d, de = 512, 217, 7168, 2048
+    b16 = ledger.grouped_gemm_bytes_alg(A, act, d, de)
+    b8 = ledger.grouped_gemm_bytes_alg(A, act, d, de, fp8_weights=True)
+    acts = 2 * (2 * A * d + 2 * A * de)
+    assert b16 - acts == act * 3 * d * de * 2
+    assert b8 - acts == act * (3 * d * de + 4 * (2 * de + d))
