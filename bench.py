@@ -450,7 +450,8 @@ def run_ours(args, shape, rank, world, local):
     comb_bytes = ledger.combine_bytes_alg(T, k, d, bool(ds))
     perm_gbs = perm_bytes / (stage_ms["permute"] / 1e3) / 1e9
     comb_gbs = comb_bytes / (stage_ms["combine"] / 1e3) / 1e9
-    traffic = recorded_traffic("grouped_gemm", shape.name)
+    traffic = recorded_traffic("skinny_gemm" if skinny else "grouped_gemm",
+                               shape.name + ("_fp8" if fp8 else ""))
     line = {
         "metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps,
@@ -505,7 +506,7 @@ def recorded_traffic(kernel: str, workload: str):
     from routing_permute_grouped_gb300 import build as moe_build
 
     ent = rec.get(kernel, {}).get(workload)
-    if not ent or ent.get("source_digest") != moe_build._digest():
+    if not ent or ent.get("source_digest") != moe_build.kernel_digest(moe_build.KERNEL_SOURCES[kernel]):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -41,6 +41,21 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def kernel_digest(sources) -> str:
+    """Digest of the named csrc files (plus the shared headers and the flags):
+    identifies the code of one kernel, for counters recorded against it."""
+    h = hashlib.sha256()
+    for name in sorted(set(sources) | {"ptx.cuh", "internal.h"}):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
+# the translation unit that defines each profiled kernel
+KERNEL_SOURCES = {"grouped_gemm": ["grouped_gemm.cu"], "skinny_gemm": ["skinny_gemm.cu"]}
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     stamp = os.path.join(BUILD, "stamp")
