@@ -19,6 +19,9 @@ Workloads (the shapes of the pages' running examples):
   imbalance  T=16384, d=4096, de=1024, E=64, k=6, Zipf(s) logit bias with
              s set for a hottest-expert load of 1x / 2x / 4x the mean,
              padding multiple 64 or 128
+  decode_e32 the decode layer's expert width with E=32, k=2, no shared
+             expert: 2.8 GB of bf16 weights, every expert active; small
+             enough for hardware-counter captures of the small-M kernel
 
 Distributions: x ~ N(0, 1); every weight ~ N(0, std = 1/sqrt(fan_in)); all
 bf16 (torch's round-to-nearest-even conversion from fp32 draws).  Each tensor
@@ -80,6 +83,7 @@ WORKLOADS = {
                           prerouted=(21733, 15004, 17982, 10817), seed=1234 + 2),
     "decode": MoeShape("decode", T=64, d=7168, d_e=2048, E=256, k=8, n_groups=8, topk_groups=4,
                        d_shared=2048, seed=1234 + 3),
+    "decode_e32": MoeShape("decode_e32", T=64, d=7168, d_e=2048, E=32, k=2, seed=5),
 }
 for _t in (1.0, 2.0, 4.0):
     for _p in (64, 128):

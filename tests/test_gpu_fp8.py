@@ -295,3 +295,22 @@ def test_fp8_layer_captures_into_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
     assert_close(out.double().cpu().numpy(), ref["out"], "out (graph replay)")
+
+
+@pytest.mark.parametrize("fill", [0x00, 0x7F, 0xFF])
+@pytest.mark.parametrize("name,fp8", [("decode_like", False), ("decode_like", True),
+                                      ("full_blocks", False)])
+def test_layer_ignores_stale_workspace(name, fp8, fill):
+    """Every kernel reads data of the earlier kernels of the launch chain only
+    after waiting for them: a workspace holding zeros or stale bytes before
+    the call gives the same result, call after call."""
+    shape, inp, oin, ref = prepared(name, fp8)
+    _, layer = _make_layer(shape, inp, fp8)
+    x = cuda(inp["x"])
+    for _ in range(3):
+        layer.ws.fill_(fill)
+        layer.ws[:256].zero_()
+        out = layer(x)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        assert_close(out.double().cpu().numpy(), ref["out"], f"out after a 0x{fill:02x} fill")
