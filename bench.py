@@ -280,11 +280,21 @@ def run_ours(args, shape, rank, world, local):
     meta, nb = buf("block_metadata", i32, (NB, 3)), buf("num_blocks", i32, (1,))
     perm_row, row_src = buf("perm_row", i32, (A,)), buf("row_src", i32, (R,))
     row_gate = buf("row_gate", f32, (R,))
-    act = torch.float16 if fp8 else bf  # the e4m3 path keeps activations in f16
-    x_perm, h, y = buf("x_perm", act, (R, d)), buf("h", act, (R, de)), buf("y", bf, (R, d))
-    hs = buf("hs", act, (T, ds)) if ds else None
+    h, y = buf("h", bf, (R, de)), buf("y", bf, (R, d))
+    hs = buf("hs", bf, (T, ds)) if ds else None
     ys = buf("ys", bf, (T, d)) if ds else None
-    x16 = buf("x16", act, (T, d)) if (fp8 and ds) else None
+    if fp8:  # e4m3 pairs of the activations and their row scales
+        u8 = torch.uint8
+        x_perm = buf("x_perm", u8, (2 * R, d))
+        h8 = buf("h8", u8, (2 * R, de))
+        x_scale = buf("row_scale", f32, (R,))
+        h_scale = buf("row_scale", f32, (R,), offset=4 * R)
+        xs8 = buf("xs8", u8, (2 * T, d)) if ds else None
+        hs8 = buf("h8", u8, (2 * T, ds), offset=2 * R * de) if ds else None
+        xs_scale = buf("row_scale", f32, (T,), offset=8 * R) if ds else None
+        hs_scale = buf("row_scale", f32, (T,), offset=8 * R + 4 * T) if ds else None
+    else:
+        x_perm = buf("x_perm", bf, (R, d))
     # the layer's kernel choice: the small-M kernel (shared expert merged
     # into its launches) when the mean rows per expert is at most 32, and
     # always with e4m3 weights
@@ -309,14 +319,15 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[2].record()
         if fp8:
-            moe.moe_permute_f16(cfg, x, perm_row, x_perm, x16, status_word)
+            moe.moe_permute_fp8(cfg, x, perm_row, x_perm, x_scale, xs8, xs_scale)
         elif args.permute == "separate":
             moe.moe_permute(cfg, x, perm_row, x_perm)
         if ev is not None:
             ev[3].record()
         if fp8:
-            moe.moe_grouped_gemm_swiglu_fp8(cfg, x_perm, layer.W13q, layer.s13, layer.W2q, layer.s2,
-                                            meta, nb, row_gate, h, y, status_word)
+            moe.moe_grouped_gemm_swiglu_fp8(cfg, x_perm, x_scale, layer.W13q, layer.s13, layer.W2q,
+                                            layer.s2, meta, nb, row_gate, h, h8, h_scale, y,
+                                            status_word)
         elif skinny:
             moe.moe_grouped_gemm_swiglu_skinny(cfg, x_perm, layer.W13, layer.W2_t, meta, nb,
                                                row_gate, h, y, status_word)
@@ -329,8 +340,8 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[4].record()
         if ds and fp8:
-            moe.moe_shared_expert_fp8(cfg, x16, layer.Ws13q, layer.ss13, layer.Ws2q, layer.ss2, hs,
-                                      ys, status_word)
+            moe.moe_shared_expert_fp8(cfg, xs8, xs_scale, layer.Ws13q, layer.ss13, layer.Ws2q,
+                                      layer.ss2, hs, hs8, hs_scale, ys, status_word)
         elif ds:
             moe.moe_shared_expert(cfg, x, layer.Ws13, layer.Ws2_t, hs, ys, status_word)
         if ev is not None:
@@ -346,7 +357,8 @@ def run_ours(args, shape, rank, world, local):
     offsets_launches = 1 if A <= 4096 else 3  # one-CTA offsets kernel for small batches
     launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
                          + (1 if args.permute == "separate" else 0) + 2
-                         + (2 if ds and not skinny else 0) + 1)
+                         + (2 if ds and not skinny else 0) + 1
+                         + (1 if fp8 else 0))  # e4m3: the split of h between the GEMMs
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():
@@ -457,7 +469,7 @@ def run_ours(args, shape, rank, world, local):
         "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 weights, f16 MMA" if fp8 else "bf16",
+        "dtype": "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16",
         "data": "synthetic", "config": config_dict(shape, args.permute, args.weights),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -58,7 +58,6 @@ typedef enum {
 /* Device error bits reported by moe_get_device_status(). */
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* an expert id outside [0, E) was skipped */
 #define MOE_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel gave up */
-#define MOE_DEVERR_F16_RANGE 0x4u    /* e4m3 path: an activation beyond f16's range */
 
 typedef struct {
     int32_t T;            /* tokens */
@@ -118,8 +117,10 @@ typedef struct {
     size_t hs;             /* bf16 [T, d_shared] */
     size_t ys;             /* bf16 [T, d] */
     size_t router_partial; /* fp32 [S, T, E] split-K router logits (S > 1 only) */
-    size_t x16;            /* f16 [T, d] token rows for the shared expert
-                              (moe_layer_fwd_fp8 with d_shared > 0 only) */
+    /* e4m3-weight layer only (moe_workspace_layout_fp8; empty otherwise): */
+    size_t xs8;            /* e4m3 pairs of the token rows [2T, d] (d_shared > 0) */
+    size_t h8;             /* e4m3 pairs of h [2R_max, d_e], then of hs [2T, d_shared] */
+    size_t row_scale;      /* fp32 row scales: x [R_max], h [R_max], xs [T], hs [T] */
 } moe_workspace_layout_t;
 
 /* ---------------------------------------------------------------- sizes -- */
@@ -132,6 +133,12 @@ size_t moe_workspace_size(const moe_config_t *cfg);
 
 /* Fills *layout with the moe_layer_fwd workspace layout. */
 moe_status_t moe_workspace_layout(const moe_config_t *cfg, moe_workspace_layout_t *layout);
+
+/* The same for moe_layer_fwd_fp8, whose workspace adds the xs8, h8 and
+ * row_scale regions (x_perm then holds the e4m3 pairs of the permuted rows,
+ * [2R_max, d] bytes). */
+size_t moe_workspace_size_fp8(const moe_config_t *cfg);
+moe_status_t moe_workspace_layout_fp8(const moe_config_t *cfg, moe_workspace_layout_t *layout);
 
 /* Bytes of the scratch that moe_build_offsets needs (status word + per-chunk
  * expert counts); 0 if cfg is invalid. */
@@ -263,15 +270,22 @@ moe_status_t moe_build_offsets_noalloc(const moe_config_t *cfg, const int32_t *t
 moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
                          void *x_perm, void *stream);
 
-/* a3 for the e4m3-weight path: the same scatter writing f16 rows (x_perm16
- * [R_max, d]); every bf16 value is copied exactly when its magnitude is in
- * [2^-17, 65504] or zero (smaller magnitudes round to a multiple of 2^-24);
- * a finite value beyond f16's range sets MOE_DEVERR_F16_RANGE in *status.
- *   x16     f16 [T, d] device, written (the dense copy for the shared
- *           expert), or NULL
- *   status  uint32 [1] device word, or NULL */
-moe_status_t moe_permute_f16(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
-                             void *x_perm16, void *x16, uint32_t *status, void *stream);
+/* a3 for the e4m3-weight path.  The 8-bit MMAs take 8-bit operands on both
+ * sides, so every 16-bit activation row v enters as an e4m3 pair with a
+ * power-of-two row scale: 2^sig is the largest power of two with
+ * max|v| * 2^sig <= 448, hi = e4m3(v * 2^sig) and lo = e4m3(v * 2^sig - hi)
+ * (nearest, ties to even).  hi + lo equals v * 2^sig for every element within
+ * a factor 2^10 of the row's largest magnitude and differs by at most 2^-10
+ * below that, so the products keep the 16-bit activations' accuracy.
+ *   x         bf16 [T, d]           device, read
+ *   perm_row  int32 [A]             device, read
+ *   x8        e4m3 [2 R_max, d]     device, written: rows 2r (hi) and 2r+1 (lo)
+ *                                   of padded row r = perm_row[t*k + j]
+ *   x_scale   fp32 [R_max]          device, written: 2^-sig of padded row r
+ *   xs8, xs_scale  e4m3 [2T, d], fp32 [T]: the same pairs per token for the
+ *                  shared expert, or both NULL */
+moe_status_t moe_permute_fp8(const moe_config_t *cfg, const void *x, const int32_t *perm_row,
+                             void *x8, float *x_scale, void *xs8, float *xs_scale, void *stream);
 
 /* a4 + a5. Grouped SwiGLU expert GEMMs over the block table ("MoE & MLA
  * operators", sec. 2.4; "Dropless and grouped GEMM", sec. 5: one tile reads
@@ -316,21 +330,25 @@ moe_status_t moe_grouped_gemm_swiglu_skinny(const moe_config_t *cfg, const void 
                                             const int32_t *num_blocks, const float *row_gate,
                                             void *h, void *y, uint32_t *status, void *stream);
 
-/* a4 + a5 with e4m3 expert weights (moe_pack_experts_fp8), on the kernel of
- * moe_grouped_gemm_swiglu_skinny: converter warps widen each staged e4m3
- * panel to f16 (exact) for f16 x f16 -> fp32 MMAs, and the epilogues apply the
- * channel scales to the fp32 accumulators:
- *   h[r] = bf16( silu(s13_g * (x W1q)) * (s13_u * (x W3q)) )  stored as f16
- *   y[r] = bf16( row_gate[r] * s2 * (h W2q) )
- *   x_perm16 f16 [R_max, d] (moe_permute_f16), h16 f16 [R_max, d_e] holding
- *   the bf16-rounded values, y bf16 [R_max, d]; other arguments as
- *   moe_grouped_gemm_swiglu_skinny.  h values beyond f16's range set
- *   MOE_DEVERR_F16_RANGE. */
-moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t *cfg, const void *x_perm16,
-                                         const void *W13q, const float *s13, const void *W2q,
-                                         const float *s2, const int32_t *block_metadata,
-                                         const int32_t *num_blocks, const float *row_gate,
-                                         void *h16, void *y, uint32_t *status, void *stream);
+/* a4 + a5 with e4m3 expert weights (moe_pack_experts_fp8) on the kernel of
+ * moe_grouped_gemm_swiglu_skinny with 8-bit MMAs (tcgen05 kind::f8f6f4,
+ * K = 32): the weight codes and the token-row pairs of moe_permute_fp8 are
+ * multiplied as they are; the epilogue adds the hi and lo columns of a token
+ * and applies its row scale and the weights' per-output-channel scales:
+ *   h[r] = bf16( silu(s13_g * x_scale[r] * (x8 W1q)) * (s13_u * x_scale[r] * (x8 W3q)) )
+ * A split kernel then writes the e4m3 pairs of h (h8, h_scale), and GEMM2
+ *   y[r] = bf16( row_gate[r] * s2 * h_scale[r] * (h8 W2q) ).
+ *   x8, x_scale    moe_permute_fp8 outputs      device, read
+ *   h              bf16 [R_max, d_e]            device, written
+ *   h8, h_scale    e4m3 [2 R_max, d_e], fp32 [R_max]  device, written
+ *   y              bf16 [R_max, d]              device, written
+ * Other arguments as moe_grouped_gemm_swiglu_skinny. */
+moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t *cfg, const void *x8,
+                                         const float *x_scale, const void *W13q, const float *s13,
+                                         const void *W2q, const float *s2,
+                                         const int32_t *block_metadata, const int32_t *num_blocks,
+                                         const float *row_gate, void *h, void *h8, float *h_scale,
+                                         void *y, uint32_t *status, void *stream);
 
 /* a3 + a4 + a5 fused: the grouped GEMMs of moe_grouped_gemm_swiglu with the
  * permute folded into GEMM1's A load ("Dropless and grouped GEMM", sec. 4:
@@ -357,16 +375,18 @@ moe_status_t moe_shared_expert(const moe_config_t *cfg, const void *x, const voi
                                const void *Ws2_t, void *hs, void *ys, uint32_t *status,
                                void *stream);
 
-/* a6 with e4m3 weights (moe_pack_experts_fp8 with E = 1), on the kernel of
- * moe_grouped_gemm_swiglu_fp8 with a dense tile list: chunks of 128 token
- * rows times panels of 256 weight rows.
- *   x16 f16 [T, d] (moe_permute_f16), hs16 f16 [T, d_shared] holding
- *   bf16-rounded values, ys bf16 [T, d]; status as above.
+/* a6 with e4m3 weights (moe_pack_experts_fp8 with E = 1) on the kernel of
+ * moe_grouped_gemm_swiglu_fp8 with a dense tile list (chunks of 64 token rows
+ * times panels of 256 weight rows).
+ *   xs8, xs_scale  e4m3 [2T, d], fp32 [T] (moe_permute_fp8)
+ *   hs             bf16 [T, d_shared]; hs8, hs_scale  e4m3 [2T, d_shared], fp32 [T]
+ *   ys             bf16 [T, d]; status as above.
  * The layer (moe_layer_fwd_fp8) puts these tiles into its routed launches
  * instead, where they fill SMs that this call alone would leave idle. */
-moe_status_t moe_shared_expert_fp8(const moe_config_t *cfg, const void *x16, const void *Ws13q,
-                                   const float *ss13, const void *Ws2q, const float *ss2,
-                                   void *hs16, void *ys, uint32_t *status, void *stream);
+moe_status_t moe_shared_expert_fp8(const moe_config_t *cfg, const void *xs8, const float *xs_scale,
+                                   const void *Ws13q, const float *ss13, const void *Ws2q,
+                                   const float *ss2, void *hs, void *hs8, float *hs_scale,
+                                   void *ys, uint32_t *status, void *stream);
 
 /* a7. Combine ("MoE & MLA operators", sec. 2.5 and 6.4: k-way sum back into
  * token order in a fixed order, with wide accumulation):
@@ -405,13 +425,12 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
                                      void *out, void *ws, size_t ws_bytes, void *stream);
 
 /* The layer with e4m3 expert weights (routed and shared): router and
- * offsets as moe_layer_fwd, then moe_permute_f16 (x_perm and, with a shared
- * expert, x16 regions of the workspace), the e4m3 grouped GEMMs with the
- * shared expert's tiles in the same two launches, and the combine.  The
- * workspace is the moe_layer_fwd one (moe_workspace_size); x_perm, h and hs
- * hold f16 there.  Requires w->W13q/s13/W2q/s2, w->Wg_t, and the shared codes
- * and scales when d_shared > 0.  Bits of the device status word as above,
- * plus MOE_DEVERR_F16_RANGE. */
+ * offsets as moe_layer_fwd, then moe_permute_fp8, the e4m3 grouped GEMMs
+ * with the shared expert's tiles in the same launches (GEMM1, the split of h
+ * and hs into e4m3 pairs, GEMM2), and the combine.  ws must hold
+ * moe_workspace_size_fp8(cfg) bytes (layout: moe_workspace_layout_fp8).
+ * Requires w->W13q/s13/W2q/s2, w->Wg_t, and the shared codes and scales when
+ * d_shared > 0. */
 moe_status_t moe_layer_fwd_fp8(const moe_config_t *cfg, const moe_weights_fp8_t *w,
                                const void *x, void *out, void *ws, size_t ws_bytes, void *stream);
 

@@ -29,15 +29,14 @@ __all__ = [
     "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
-    "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_f16", "moe_grouped_gemm_swiglu_skinny",
+    "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_fp8", "moe_grouped_gemm_swiglu_skinny",
     "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
-    "moe_shared_expert_fp8",
+    "moe_shared_expert_fp8", "moe_workspace_size_fp8", "moe_workspace_layout_fp8",
 ]
 
 MOE_OK = 0
 DEVERR_EXPERT_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
-DEVERR_F16_RANGE = 0x4
 
 
 class MoeError(RuntimeError):
@@ -63,7 +62,7 @@ class MoeWeightsFp8(ctypes.Structure):
 
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
                   "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
-                  "y", "hs", "ys", "router_partial", "x16")
+                  "y", "hs", "ys", "router_partial", "xs8", "h8", "row_scale")
 
 
 class _Layout(ctypes.Structure):
@@ -110,10 +109,12 @@ def load():
         "moe_layer_fwd_prerouted": (ctypes.c_int,
                                     [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ, P]),
         "moe_pack_experts_fp8": (ctypes.c_int, [I32, I32, I32] + [P] * 8),
-        "moe_permute_f16": (ctypes.c_int, [CP] + [P] * 6),
+        "moe_workspace_size_fp8": (SZ, [CP]),
+        "moe_workspace_layout_fp8": (ctypes.c_int, [CP, ctypes.POINTER(_Layout)]),
+        "moe_permute_fp8": (ctypes.c_int, [CP] + [P] * 7),
         "moe_grouped_gemm_swiglu_skinny": (ctypes.c_int, [CP] + [P] * 10),
-        "moe_grouped_gemm_swiglu_fp8": (ctypes.c_int, [CP] + [P] * 12),
-        "moe_shared_expert_fp8": (ctypes.c_int, [CP] + [P] * 9),
+        "moe_grouped_gemm_swiglu_fp8": (ctypes.c_int, [CP] + [P] * 15),
+        "moe_shared_expert_fp8": (ctypes.c_int, [CP] + [P] * 12),
         "moe_layer_fwd_fp8": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P, SZ, P]),
         "moe_layer_fwd_fp8_prerouted": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P,
                                                        P, P, SZ, P]),
@@ -178,6 +179,16 @@ def moe_workspace_size(cfg: MoeConfig) -> int:
 def moe_workspace_layout(cfg: MoeConfig) -> dict:
     L = _Layout()
     _check(load().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)))
+    return {n: int(getattr(L, n)) for n in _LAYOUT_FIELDS}
+
+
+def moe_workspace_size_fp8(cfg: MoeConfig) -> int:
+    return int(load().moe_workspace_size_fp8(ctypes.byref(cfg)))
+
+
+def moe_workspace_layout_fp8(cfg: MoeConfig) -> dict:
+    L = _Layout()
+    _check(load().moe_workspace_layout_fp8(ctypes.byref(cfg), ctypes.byref(L)))
     return {n: int(getattr(L, n)) for n in _LAYOUT_FIELDS}
 
 
@@ -263,9 +274,9 @@ def moe_grouped_gemm_swiglu_gather(cfg, x, row_src, W13, W2_t, block_metadata, n
         _stream(stream)))
 
 
-def moe_permute_f16(cfg, x, perm_row, x_perm16, x16=None, status=None, stream=None) -> None:
-    _check(load().moe_permute_f16(ctypes.byref(cfg), _ptr(x), _ptr(perm_row), _ptr(x_perm16),
-                                  _ptr(x16), _ptr(status), _stream(stream)))
+def moe_permute_fp8(cfg, x, perm_row, x8, x_scale, xs8=None, xs_scale=None, stream=None) -> None:
+    _check(load().moe_permute_fp8(ctypes.byref(cfg), _ptr(x), _ptr(perm_row), _ptr(x8),
+                                  _ptr(x_scale), _ptr(xs8), _ptr(xs_scale), _stream(stream)))
 
 
 def moe_grouped_gemm_swiglu_skinny(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, row_gate,
@@ -275,19 +286,19 @@ def moe_grouped_gemm_swiglu_skinny(cfg, x_perm, W13, W2_t, block_metadata, num_b
         _ptr(num_blocks), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
 
 
-def moe_grouped_gemm_swiglu_fp8(cfg, x_perm16, W13q, s13, W2q, s2, block_metadata, num_blocks,
-                                row_gate, h16, y, status=None, stream=None) -> None:
+def moe_grouped_gemm_swiglu_fp8(cfg, x8, x_scale, W13q, s13, W2q, s2, block_metadata, num_blocks,
+                                row_gate, h, h8, h_scale, y, status=None, stream=None) -> None:
     _check(load().moe_grouped_gemm_swiglu_fp8(
-        ctypes.byref(cfg), _ptr(x_perm16), _ptr(W13q), _ptr(s13), _ptr(W2q), _ptr(s2),
-        _ptr(block_metadata), _ptr(num_blocks), _ptr(row_gate), _ptr(h16), _ptr(y), _ptr(status),
-        _stream(stream)))
+        ctypes.byref(cfg), _ptr(x8), _ptr(x_scale), _ptr(W13q), _ptr(s13), _ptr(W2q), _ptr(s2),
+        _ptr(block_metadata), _ptr(num_blocks), _ptr(row_gate), _ptr(h), _ptr(h8), _ptr(h_scale),
+        _ptr(y), _ptr(status), _stream(stream)))
 
 
-def moe_shared_expert_fp8(cfg, x16, Ws13q, ss13, Ws2q, ss2, hs16, ys, status=None,
-                          stream=None) -> None:
-    _check(load().moe_shared_expert_fp8(ctypes.byref(cfg), _ptr(x16), _ptr(Ws13q), _ptr(ss13),
-                                        _ptr(Ws2q), _ptr(ss2), _ptr(hs16), _ptr(ys), _ptr(status),
-                                        _stream(stream)))
+def moe_shared_expert_fp8(cfg, xs8, xs_scale, Ws13q, ss13, Ws2q, ss2, hs, hs8, hs_scale, ys,
+                          status=None, stream=None) -> None:
+    _check(load().moe_shared_expert_fp8(ctypes.byref(cfg), _ptr(xs8), _ptr(xs_scale), _ptr(Ws13q),
+                                        _ptr(ss13), _ptr(Ws2q), _ptr(ss2), _ptr(hs), _ptr(hs8),
+                                        _ptr(hs_scale), _ptr(ys), _ptr(status), _stream(stream)))
 
 
 def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:
@@ -389,7 +400,7 @@ class MoeLayer:
         self._init_ws(cfg, dev)
 
     def _init_ws(self, cfg, dev):
-        self.layout = moe_workspace_layout(cfg)
+        self.layout = moe_workspace_layout_fp8(cfg) if self.fp8 else moe_workspace_layout(cfg)
         self.ws = torch.empty(self.layout["total"], dtype=torch.uint8, device=dev)
         self.ws[:256].zero_()
 
@@ -444,9 +455,10 @@ class MoeLayer:
 
     __call__ = forward
 
-    def buffer(self, name: str, dtype, shape) -> torch.Tensor:
-        """A view of one intermediate of the workspace (see moe_workspace_layout)."""
-        off = self.layout[name]
+    def buffer(self, name: str, dtype, shape, offset: int = 0) -> torch.Tensor:
+        """A view of one intermediate of the workspace (see moe_workspace_layout),
+        starting ``offset`` bytes into its region."""
+        off = self.layout[name] + offset
         n = 1
         for s in shape:
             n *= s

@@ -113,6 +113,7 @@ struct SkinnyArgs {
     int64_t out_rows;
     const float* row_gate;          // routed gate per padded row (gate epilogue), may be null
     const float* scale;             // e4m3 weights: fp32 scale per weight row
+    const float* xscale;            // e4m3: scale of each token row pair (per padded row)
     // shared expert (dense tiles after the routed ones)
     int32_t s_rows;                 // token rows (0 = no shared tiles)
     int32_t s_panels;
@@ -121,16 +122,20 @@ struct SkinnyArgs {
     void* s_out;                    // [s_rows, s_ldo]
     int64_t s_ldo;
     const float* s_scale;
+    const float* s_xscale;
     uint32_t* status;               // device error word, may be null
 };
 
 // Token rows per tile of the small-M kernel (a block with more valid rows is
 // split into n_chunks chunks of this many rows).
 int skinny_tile_rows(bool fp8);
+// K per pipeline stage of the small-M kernel (128 bytes of each row).
+int skinny_k_step(bool fp8);
 
 // Small-M grouped GEMM (epi = kEpiSwiGLU or kEpiGate).  W / Ws: weights
-// [rows, K] K-major, bf16 or (fp8) e4m3 codes; X / Xs: token rows [rows, K],
-// bf16 or (fp8) f16.  max_tiles bounds the tile count (grid size).
+// [rows, K] K-major, bf16 or (fp8) e4m3 codes; X / Xs: token rows [rows, K]
+// bf16, or (fp8) their e4m3 pairs [2 rows, K].  max_tiles bounds the tile
+// count (grid size).
 cudaError_t launch_grouped_gemm_skinny(int epi, bool fp8, const void* W, int64_t rowsW,
                                        const void* X, int64_t rowsX, int64_t K, const void* Ws,
                                        int64_t rowsWs, const void* Xs, int64_t rowsXs, int64_t Ks,
@@ -151,11 +156,20 @@ cudaError_t launch_pack_fp8(const void* in, uint8_t* out, float* scale, int rows
                             int64_t in_bstride, int64_t out_bstride, int64_t scale_bstride,
                             int out_ld, int mode, int batch, cudaStream_t stream);
 
-// Permute into f16 rows (exact copies of the bf16 values in f16's range);
-// x16, if not null, also receives the dense f16 copy of every token row.
-// Values beyond f16's range set bit 0x4 of *status.
-cudaError_t launch_permute_f16(const void* x, const int32_t* perm_row, void* x_perm16, void* x16,
-                               int T, int d, int k, uint32_t* status, cudaStream_t stream);
+// Permute of the e4m3-weight path: token rows as e4m3 pairs (x8 [2 R, d]:
+// rows 2r, 2r + 1) with per-row scales; xs8 [2 T, d] / xs_scale [T], if not
+// null, receive the dense pairs for the shared expert.
+cudaError_t launch_permute_fp8(const void* x, const int32_t* perm_row, uint8_t* x8, float* x_scale,
+                               uint8_t* xs8, float* xs_scale, int T, int d, int k,
+                               cudaStream_t stream);
+
+// e4m3 pairs of bf16 rows between the expert GEMMs: the valid rows of the
+// block table's blocks of h [R, K] (h8 [2 R, K], h_scale [R]) and, if hs is
+// not null, the Ts dense rows of hs [Ts, Ks] (hs8, hs_scale).
+cudaError_t launch_split_rows_e4m3(const void* h, const int32_t* block_metadata,
+                                   const int32_t* num_blocks, int nb_cap, int K, uint8_t* h8,
+                                   float* h_scale, const void* hs, int Ts, int Ks, uint8_t* hs8,
+                                   float* hs_scale, cudaStream_t stream);
 
 // Sums S fp32 partial-logit slices in slice order, adds the bias and does the
 // (group-limited) top-k and softmax of each token.

@@ -114,7 +114,7 @@ static int router_splits(const moe_config_t& c) {
     return (k_blocks + per - 1) / per;
 }
 
-static moe_workspace_layout_t layout_of(const moe_config_t& c) {
+static moe_workspace_layout_t layout_of(const moe_config_t& c, bool fp8 = false) {
     const Sizes s = sizes_of(c);
     moe_workspace_layout_t L{};
     size_t off = 0;
@@ -140,7 +140,12 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c) {
     L.ys = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
     const int S = router_splits(c);
     L.router_partial = take(S > 1 ? static_cast<size_t>(S) * c.T * c.E * 4 : 0);
-    L.x16 = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
+    // e4m3-weight layer only: token-row pairs for the shared expert, the pairs
+    // of h (routed then shared) and the row scales (x, h, shared x, shared h)
+    const size_t ds = c.d_shared ? static_cast<size_t>(c.d_shared) : 0;
+    L.xs8 = take(fp8 && ds ? static_cast<size_t>(c.T) * c.d * 2 : 0);
+    L.h8 = take(fp8 ? (static_cast<size_t>(s.R) * c.d_e + static_cast<size_t>(c.T) * ds) * 2 : 0);
+    L.row_scale = take(fp8 ? (2 * static_cast<size_t>(s.R) + 2 * static_cast<size_t>(c.T)) * 4 : 0);
     L.total = off;
     return L;
 }
@@ -262,21 +267,32 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2 (down + gate)");
 }
 
-// The expert GEMMs on the swapped-operand kernel for blocks with few rows,
-// bf16 weights or (fp8) e4m3 codes with per-row scales.  When Ws13 is given
-// and d_shared > 0, the shared expert's dense tiles (token rows Xs) are
-// appended to the same two launches.
-static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const void* X,
-                                      const void* W13, const float* s13, const void* W2,
-                                      const float* s2, const int32_t* meta, const int32_t* nb,
-                                      const float* row_gate, void* h, void* y, uint32_t* status,
-                                      cudaStream_t st, const void* Xs = nullptr,
-                                      const void* Ws13 = nullptr, const float* ss13 = nullptr,
-                                      const void* Ws2 = nullptr, const float* ss2 = nullptr,
-                                      void* hs = nullptr, void* ys = nullptr) {
+// Operands of one expert (or of the shared expert) on the small-M kernel.
+struct SkinnyIO {
+    const void* x;         // token rows: bf16 [rows, d], or (e4m3) their pairs [2 rows, d]
+    const float* x_scale;  // e4m3: scale of each token-row pair
+    const void* W13;       // packed gate/up: bf16 or e4m3 codes
+    const float* s13;      // e4m3: per-row scales
+    const void* W2;        // packed down
+    const float* s2;
+    void* h;               // bf16 [rows, width]
+    uint8_t* h8;           // e4m3: pairs of h [2 rows, width]
+    float* h_scale;        // e4m3: their scales
+    void* y;               // bf16 [rows, d]
+};
+
+// The expert GEMMs on the swapped-operand kernel for blocks with few rows.
+// With sh, the shared expert's dense tiles (T token rows) are appended to the
+// same launches.  e4m3 weights: GEMM1 writes h in bf16, a split kernel turns
+// the rows of h (and hs) into e4m3 pairs, GEMM2 multiplies those.
+static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const SkinnyIO& r,
+                                      const int32_t* meta, const int32_t* nb,
+                                      const float* row_gate, uint32_t* status, cudaStream_t st,
+                                      const SkinnyIO* sh = nullptr) {
     const Sizes s = sizes_of(c);
-    const bool shared = c.d_shared > 0 && Ws13 != nullptr;
+    const bool shared = c.d_shared > 0 && sh != nullptr;
     const int rows = skinny_tile_rows(fp8);
+    const int ks = skinny_k_step(fp8);
     const int64_t chunks = (static_cast<int64_t>(c.T) + rows - 1) / rows;  // shared-expert tiles
     // a block holds at most min(P, T*k) valid rows (T*k: an expert may repeat
     // within a token of pre-routed input)
@@ -292,44 +308,56 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const voi
     // GEMM1: panels of 128 gate + 128 up rows, K = d
     a.n_panels = c.d_e / 128;
     a.rows_per_expert = 2 * c.d_e;
-    a.k_blocks = c.d / 64;
-    a.out = h;
+    a.k_blocks = c.d / ks;
+    a.out = r.h;
     a.ldo = c.d_e;
-    a.scale = s13;
+    a.scale = r.s13;
+    a.xscale = r.x_scale;
     if (shared) {
         a.s_rows = c.T;
         a.s_panels = c.d_shared / 128;
         a.s_rows_per_expert = 2 * c.d_shared;
-        a.s_k_blocks = c.d / 64;
-        a.s_out = hs;
+        a.s_k_blocks = c.d / ks;
+        a.s_out = sh->h;
         a.s_ldo = c.d_shared;
-        a.s_scale = ss13;
+        a.s_scale = sh->s13;
+        a.s_xscale = sh->x_scale;
     }
     int64_t tiles = s.NB * a.n_panels * a.n_chunks + (shared ? chunks * a.s_panels : 0);
     cudaError_t e = launch_grouped_gemm_skinny(
-        kEpiSwiGLU, fp8, W13, static_cast<int64_t>(c.E) * 2 * c.d_e, X, s.R, c.d, Ws13,
-        2 * static_cast<int64_t>(c.d_shared), Xs, c.T, c.d, a,
-        static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
+        kEpiSwiGLU, fp8, r.W13, static_cast<int64_t>(c.E) * 2 * c.d_e, r.x, s.R, c.d,
+        shared ? sh->W13 : nullptr, 2 * static_cast<int64_t>(c.d_shared), shared ? sh->x : nullptr,
+        c.T, c.d, a, static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1, small-M kernel");
+    if (fp8) {
+        e = launch_split_rows_e4m3(r.h, meta, nb, meta ? static_cast<int>(s.NB) : 0, c.d_e, r.h8,
+                                   r.h_scale, shared ? sh->h : nullptr, c.T, c.d_shared,
+                                   shared ? sh->h8 : nullptr, shared ? sh->h_scale : nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(e, "e4m3 pairs of h");
+    }
     // GEMM2: panels of 256 output rows, K = d_e (d_shared for the shared tiles)
     a.n_panels = (c.d + 255) / 256;
     a.rows_per_expert = c.d;
-    a.k_blocks = c.d_e / 64;
-    a.out = y;
+    a.k_blocks = c.d_e / ks;
+    a.out = r.y;
     a.ldo = c.d;
     a.row_gate = row_gate;
-    a.scale = s2;
+    a.scale = r.s2;
+    a.xscale = r.h_scale;
     if (shared) {
         a.s_panels = (c.d + 255) / 256;
         a.s_rows_per_expert = c.d;
-        a.s_k_blocks = c.d_shared / 64;
-        a.s_out = ys;
+        a.s_k_blocks = c.d_shared / ks;
+        a.s_out = sh->y;
         a.s_ldo = c.d;
-        a.s_scale = ss2;
+        a.s_scale = sh->s2;
+        a.s_xscale = sh->h_scale;
     }
     tiles = s.NB * a.n_panels * a.n_chunks + (shared ? chunks * a.s_panels : 0);
-    e = launch_grouped_gemm_skinny(kEpiGate, fp8, W2, static_cast<int64_t>(c.E) * c.d, h, s.R, c.d_e,
-                                   Ws2, c.d, hs, c.T, c.d_shared, a,
+    const void* h_in = fp8 ? static_cast<const void*>(r.h8) : r.h;
+    const void* hs_in = shared ? (fp8 ? static_cast<const void*>(sh->h8) : sh->h) : nullptr;
+    e = launch_grouped_gemm_skinny(kEpiGate, fp8, r.W2, static_cast<int64_t>(c.E) * c.d, h_in, s.R,
+                                   c.d_e, shared ? sh->W2 : nullptr, c.d, hs_in, c.T, c.d_shared, a,
                                    static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2, small-M kernel");
 }
@@ -403,13 +431,13 @@ static moe_status_t layer_front(const moe_config_t& c, const void* Wg_t, const f
 
 static moe_status_t check_layer_args(const moe_config_t* cfg, bool routed, const void* Wg_t,
                                      const void* x, const float* pre_w, void* out, void* ws,
-                                     size_t ws_bytes) {
+                                     size_t ws_bytes, bool fp8 = false) {
     moe_status_t r = check_cfg(cfg, routed);
     if (r != MOE_OK) return r;
     if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "null x or out");
     if (routed && !Wg_t) return fail(MOE_ERR_INVALID_ARG, "null router weight");
     if (!routed && !pre_w) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
-    const size_t need = layout_of(*cfg).total;
+    const size_t need = layout_of(*cfg, fp8).total;
     if (!ws || ws_bytes < need)
         return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
     return MOE_OK;
@@ -434,10 +462,12 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     if (e != cudaSuccess) return cuda_fail(e, "permute");
     const void* shared = c.d_shared ? B.at(L.ys) : nullptr;
     if (use_skinny(c)) {
-        r = do_experts_skinny(c, false, B.at(L.x_perm), w->W13, nullptr, w->W2, nullptr, B.meta(),
-                              B.nb(), B.row_gate(), B.at(L.h), B.at(L.y), B.status(), st, x,
-                              c.d_shared ? w->Ws13 : nullptr, nullptr, w->Ws2, nullptr, B.at(L.hs),
-                              B.at(L.ys));
+        const SkinnyIO ro{B.at(L.x_perm), nullptr, w->W13, nullptr, w->W2, nullptr,
+                          B.at(L.h), nullptr, nullptr, B.at(L.y)};
+        const SkinnyIO so{x, nullptr, w->Ws13, nullptr, w->Ws2, nullptr,
+                          B.at(L.hs), nullptr, nullptr, B.at(L.ys)};
+        r = do_experts_skinny(c, false, ro, B.meta(), B.nb(), B.row_gate(), B.status(), st,
+                              c.d_shared ? &so : nullptr);
         if (r != MOE_OK) return r;
     } else {
         r = do_experts(c, B.at(L.x_perm), w->W13, w->W2, B.meta(), B.nb(), B.po(), B.row_gate(),
@@ -456,7 +486,8 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
                               const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
                               size_t ws_bytes, cudaStream_t st) {
     if (!w) return fail(MOE_ERR_INVALID_ARG, "null weights");
-    moe_status_t r = check_layer_args(cfg, pre_idx == nullptr, w->Wg_t, x, pre_w, out, ws, ws_bytes);
+    moe_status_t r =
+        check_layer_args(cfg, pre_idx == nullptr, w->Wg_t, x, pre_w, out, ws, ws_bytes, true);
     if (r != MOE_OK) return r;
     const moe_config_t& c = *cfg;
     if (!w->W13q || !w->s13 || !w->W2q || !w->s2)
@@ -464,18 +495,25 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
     if (c.d_shared && (!w->Ws13q || !w->ss13 || !w->Ws2q || !w->ss2))
         return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared expert codes or scales");
     if (c.T == 0) return MOE_OK;
-    const LayerBufs B{layout_of(c), static_cast<uint8_t*>(ws)};
+    const LayerBufs B{layout_of(c, true), static_cast<uint8_t*>(ws)};
     const moe_workspace_layout_t& L = B.L;
     r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
     if (r != MOE_OK) return r;
-    void* x16 = c.d_shared ? B.at(L.x16) : nullptr;
-    cudaError_t e = launch_permute_f16(x, B.perm_row(), B.at(L.x_perm), x16, c.T, c.d, c.k,
-                                       B.status(), st);
-    if (e != cudaSuccess) return cuda_fail(e, "permute (f16)");
-    r = do_experts_skinny(c, true, B.at(L.x_perm), w->W13q, w->s13, w->W2q, w->s2, B.meta(), B.nb(),
-                          B.row_gate(), B.at(L.h), B.at(L.y), B.status(), st, x16,
-                          c.d_shared ? w->Ws13q : nullptr, w->ss13, w->Ws2q, w->ss2, B.at(L.hs),
-                          B.at(L.ys));
+    const Sizes s = sizes_of(c);
+    float* scales = static_cast<float*>(B.at(L.row_scale));  // x [R], h [R], xs [T], hs [T]
+    uint8_t* h8 = static_cast<uint8_t*>(B.at(L.h8));
+    uint8_t* x8 = static_cast<uint8_t*>(B.at(L.x_perm));
+    uint8_t* xs8 = c.d_shared ? static_cast<uint8_t*>(B.at(L.xs8)) : nullptr;
+    cudaError_t e = launch_permute_fp8(x, B.perm_row(), x8, scales, xs8,
+                                       c.d_shared ? scales + 2 * s.R : nullptr, c.T, c.d, c.k, st);
+    if (e != cudaSuccess) return cuda_fail(e, "permute (e4m3 pairs)");
+    const SkinnyIO ro{x8, scales, w->W13q, w->s13, w->W2q, w->s2,
+                      B.at(L.h), h8, scales + s.R, B.at(L.y)};
+    const SkinnyIO so{xs8, scales + 2 * s.R, w->Ws13q, w->ss13, w->Ws2q, w->ss2,
+                      B.at(L.hs), h8 + static_cast<size_t>(s.R) * c.d_e * 2,
+                      scales + 2 * s.R + c.T, B.at(L.ys)};
+    r = do_experts_skinny(c, true, ro, B.meta(), B.nb(), B.row_gate(), B.status(), st,
+                          c.d_shared ? &so : nullptr);
     if (r != MOE_OK) return r;
     e = launch_combine(B.at(L.y), B.perm_row(), c.d_shared ? B.at(L.ys) : nullptr, out, c.T, c.d,
                        c.k, st);
@@ -493,6 +531,19 @@ moe_status_t moe_check_config(const moe_config_t* cfg) { return check_cfg(cfg, f
 size_t moe_workspace_size(const moe_config_t* cfg) {
     if (check_cfg(cfg, false) != MOE_OK) return 0;
     return layout_of(*cfg).total;
+}
+
+size_t moe_workspace_size_fp8(const moe_config_t* cfg) {
+    if (check_cfg(cfg, false) != MOE_OK) return 0;
+    return layout_of(*cfg, true).total;
+}
+
+moe_status_t moe_workspace_layout_fp8(const moe_config_t* cfg, moe_workspace_layout_t* layout) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!layout) return fail(MOE_ERR_INVALID_ARG, "layout is NULL");
+    *layout = layout_of(*cfg, true);
+    return MOE_OK;
 }
 
 moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout) {
@@ -618,15 +669,18 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
                       h, y, status, static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_permute_f16(const moe_config_t* cfg, const void* x, const int32_t* perm_row,
-                             void* x_perm16, void* x16, uint32_t* status, void* stream) {
+moe_status_t moe_permute_fp8(const moe_config_t* cfg, const void* x, const int32_t* perm_row,
+                             void* x8, float* x_scale, void* xs8, float* xs_scale, void* stream) {
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
-    if (!x || !perm_row || !x_perm16) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (!x || !perm_row || !x8 || !x_scale) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if ((xs8 == nullptr) != (xs_scale == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "xs8 and xs_scale must both be given or both be NULL");
     if (cfg->T == 0) return MOE_OK;
-    cudaError_t e = launch_permute_f16(x, perm_row, x_perm16, x16, cfg->T, cfg->d, cfg->k, status,
+    cudaError_t e = launch_permute_fp8(x, perm_row, static_cast<uint8_t*>(x8), x_scale,
+                                       static_cast<uint8_t*>(xs8), xs_scale, cfg->T, cfg->d, cfg->k,
                                        static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute (f16)");
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute (e4m3 pairs)");
 }
 
 moe_status_t moe_grouped_gemm_swiglu_skinny(const moe_config_t* cfg, const void* x_perm,
@@ -639,22 +693,26 @@ moe_status_t moe_grouped_gemm_swiglu_skinny(const moe_config_t* cfg, const void*
     if (!x_perm || !W13 || !W2_t || !block_metadata || !num_blocks || !h || !y)
         return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
-    return do_experts_skinny(*cfg, false, x_perm, W13, nullptr, W2_t, nullptr, block_metadata,
-                             num_blocks, row_gate, h, y, status, static_cast<cudaStream_t>(stream));
+    const SkinnyIO ro{x_perm, nullptr, W13, nullptr, W2_t, nullptr, h, nullptr, nullptr, y};
+    return do_experts_skinny(*cfg, false, ro, block_metadata, num_blocks, row_gate, status,
+                             static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t* cfg, const void* x_perm16,
-                                         const void* W13q, const float* s13, const void* W2q,
-                                         const float* s2, const int32_t* block_metadata,
-                                         const int32_t* num_blocks, const float* row_gate,
-                                         void* h16, void* y, uint32_t* status, void* stream) {
+moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t* cfg, const void* x8,
+                                         const float* x_scale, const void* W13q, const float* s13,
+                                         const void* W2q, const float* s2,
+                                         const int32_t* block_metadata, const int32_t* num_blocks,
+                                         const float* row_gate, void* h, void* h8, float* h_scale,
+                                         void* y, uint32_t* status, void* stream) {
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
-    if (!x_perm16 || !W13q || !s13 || !W2q || !s2 || !block_metadata || !num_blocks || !h16 || !y)
+    if (!x8 || !x_scale || !W13q || !s13 || !W2q || !s2 || !block_metadata || !num_blocks || !h ||
+        !h8 || !h_scale || !y)
         return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
-    return do_experts_skinny(*cfg, true, x_perm16, W13q, s13, W2q, s2, block_metadata, num_blocks,
-                             row_gate, h16, y, status, static_cast<cudaStream_t>(stream));
+    const SkinnyIO ro{x8, x_scale, W13q, s13, W2q, s2, h, static_cast<uint8_t*>(h8), h_scale, y};
+    return do_experts_skinny(*cfg, true, ro, block_metadata, num_blocks, row_gate, status,
+                             static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_grouped_gemm_swiglu_gather(const moe_config_t* cfg, const void* x,
@@ -684,21 +742,23 @@ moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const voi
     return do_shared(*cfg, x, Ws13, Ws2_t, hs, ys, status, static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_shared_expert_fp8(const moe_config_t* cfg, const void* x16, const void* Ws13q,
-                                   const float* ss13, const void* Ws2q, const float* ss2, void* hs16,
-                                   void* ys, uint32_t* status, void* stream) {
+moe_status_t moe_shared_expert_fp8(const moe_config_t* cfg, const void* xs8, const float* xs_scale,
+                                   const void* Ws13q, const float* ss13, const void* Ws2q,
+                                   const float* ss2, void* hs, void* hs8, float* hs_scale, void* ys,
+                                   uint32_t* status, void* stream) {
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
     if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
-    if (!x16 || !Ws13q || !ss13 || !Ws2q || !ss2 || !hs16 || !ys)
+    if (!xs8 || !xs_scale || !Ws13q || !ss13 || !Ws2q || !ss2 || !hs || !hs8 || !hs_scale || !ys)
         return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
-    // the routed part of the launch is empty: no block table, only the dense
-    // shared-expert tiles
-    moe_config_t c = *cfg;
-    return do_experts_skinny(c, true, x16, Ws13q, ss13, Ws2q, ss2, nullptr, nullptr, nullptr, nullptr,
-                             nullptr, status, static_cast<cudaStream_t>(stream), x16, Ws13q, ss13,
-                             Ws2q, ss2, hs16, ys);
+    // no block table: a launch of the shared expert's dense tiles only
+    const SkinnyIO none{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, nullptr};
+    const SkinnyIO so{xs8, xs_scale, Ws13q, ss13, Ws2q, ss2, hs, static_cast<uint8_t*>(hs8), hs_scale,
+                      ys};
+    return do_experts_skinny(*cfg, true, none, nullptr, nullptr, nullptr, status,
+                             static_cast<cudaStream_t>(stream), &so);
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y, const int32_t* perm_row,

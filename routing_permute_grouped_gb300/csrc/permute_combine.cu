@@ -11,7 +11,6 @@
 //          (sec. 6.4: fixed summation order, wide accumulation, no atomics).
 //          Bytes per token: (k + 1 [+1]) * d * 2.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -54,64 +53,135 @@ __global__ void __launch_bounds__(kPCWarps * 32)
     }
 }
 
-// Eight bf16 values -> eight f16 values (exact for magnitudes in [2^-17,
-// 65504] and zero); sets ovf for a finite value past f16's range.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v, bool& ovf) {
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-        ovf |= (fabsf(lo) >= 65520.0f && !isinf(lo)) || (fabsf(hi) >= 65520.0f && !isinf(hi));
-        const __half2 h = __floats2half2_rn(lo, hi);
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Largest magnitude of a bf16 row of nvec 16-byte vectors, over the warp.
+__device__ __forceinline__ float row_amax(const uint4* src, int nvec, int lane) {
+    float m = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+        float f[8];
+        bf16x8_to_f32(ld_dep(src + v), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+    return warp_max(m);
+}
+
+// Eight bf16 values of a row -> their e4m3 pair (hi, lo) under the row scale.
+__device__ __forceinline__ void split_vec(const uint4& v, float scale, uint2& hi, uint2& lo) {
+    float f[8];
+    bf16x8_to_f32(v, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] *= scale;  // exact: a power of two
+    e4m3_split8(f, hi, lo);
 }
 
 // The permute of the e4m3-weight path: the same token-major scatter, each row
-// written as f16; x16 (if given) also receives the token's dense f16 row for
-// the shared expert.
+// written as its e4m3 pair (rows 2r and 2r + 1 of x8, d bytes each) with the
+// row's scale factor 2^-sig in x_scale[r]; xs8 / xs_scale (if given) also
+// receive the dense pairs of every token row for the shared expert.  The
+// pair and its scale are those of ptx.cuh (e4m3_row_scale, e4m3_split8).
 __global__ void __launch_bounds__(kPCWarps * 32)
-    k_permute_f16(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
-                  uint4* __restrict__ x_perm, uint4* __restrict__ x16, int T, int nvec, int k,
-                  uint32_t* status) {
+    k_permute_fp8(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
+                  uint8_t* __restrict__ x8, float* __restrict__ x_scale, uint8_t* __restrict__ xs8,
+                  float* __restrict__ xs_scale, int T, int d, int k) {
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
+    const int nvec = d / 8;
     int rows[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
     const uint4* src = x + (int64_t)t * nvec;
-    bool ovf = false;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
-        uint4 buf[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int v = v0 + u * 32;
-            if (v < nvec) buf[u] = bf16x8_to_f16x8(ld_dep(src + v), ovf);
-        }
+    const float scale = e4m3_row_scale(row_amax(src, nvec, lane));
+    for (int v = lane; v < nvec; v += 32) {
+        uint2 hi, lo;
+        split_vec(ld_dep(src + v), scale, hi, lo);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (rows[j] < 0) continue;
-            uint4* dst = x_perm + (int64_t)rows[j] * nvec;
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int v = v0 + u * 32;
-                if (v < nvec) dst[v] = buf[u];
-            }
+            uint8_t* dst = x8 + (int64_t)rows[j] * 2 * d + (int64_t)v * 8;
+            *reinterpret_cast<uint2*>(dst) = hi;
+            *reinterpret_cast<uint2*>(dst + d) = lo;
         }
-        if (x16) {
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int v = v0 + u * 32;
-                if (v < nvec) x16[(int64_t)t * nvec + v] = buf[u];
-            }
+        if (xs8) {
+            uint8_t* dst = xs8 + (int64_t)t * 2 * d + (int64_t)v * 8;
+            *reinterpret_cast<uint2*>(dst) = hi;
+            *reinterpret_cast<uint2*>(dst + d) = lo;
         }
     }
-    if (ovf && status) atomicOr(status, 0x4u);
+    if (lane == 0) {
+        const float inv = 1.0f / scale;  // exact: a power of two
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (rows[j] >= 0) x_scale[rows[j]] = inv;
+        if (xs_scale) xs_scale[t] = inv;
+    }
+}
+
+// The e4m3 pairs of the rows of h between the two expert GEMMs: CTA b <
+// nb_cap takes block b of the table (its valid rows only, if b < num_blocks);
+// CTA nb_cap + c takes dense rows [128 c, 128 c + 128) of hs.  A warp per row:
+// its largest magnitude, the row scale, then the pair.
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_split_rows_e4m3(const uint4* __restrict__ h, const int32_t* __restrict__ block_metadata,
+                      const int32_t* __restrict__ num_blocks, int nb_cap, int K,
+                      uint8_t* __restrict__ h8, float* __restrict__ h_scale,
+                      const uint4* __restrict__ hs, int Ts, int Ks, uint8_t* __restrict__ hs8,
+                      float* __restrict__ hs_scale) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint4* src;
+    uint8_t* dst;
+    float* scl;
+    int r0, nrows, width;
+    if (static_cast<int>(blockIdx.x) < nb_cap) {
+        const int nb = num_blocks ? ld_dep(num_blocks) : 0;
+        if (static_cast<int>(blockIdx.x) >= nb) return;
+        r0 = ld_dep(block_metadata + 3 * blockIdx.x + 1);
+        nrows = ld_dep(block_metadata + 3 * blockIdx.x + 2);
+        src = h;
+        dst = h8;
+        scl = h_scale;
+        width = K;
+    } else {
+        r0 = (blockIdx.x - nb_cap) * 128;
+        nrows = min(128, Ts - r0);
+        src = hs;
+        dst = hs8;
+        scl = hs_scale;
+        width = Ks;
+    }
+    const int nvec = width / 8;
+    for (int i = warp; i < nrows; i += kPCWarps) {
+        const int64_t r = r0 + i;
+        const uint4* row = src + r * nvec;
+        const float scale = e4m3_row_scale(row_amax(row, nvec, lane));
+        for (int v = lane; v < nvec; v += 32) {
+            uint2 hi, lo;
+            split_vec(ld_dep(row + v), scale, hi, lo);
+            uint8_t* o = dst + r * 2 * width + (int64_t)v * 8;
+            *reinterpret_cast<uint2*>(o) = hi;
+            *reinterpret_cast<uint2*>(o + width) = lo;
+        }
+        if (lane == 0) scl[r] = 1.0f / scale;
+    }
 }
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
@@ -215,13 +285,24 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
                       k);
 }
 
-cudaError_t launch_permute_f16(const void* x, const int32_t* perm_row, void* x_perm16, void* x16,
-                               int T, int d, int k, uint32_t* status, cudaStream_t stream) {
-    const int nvec = d / 8;
+cudaError_t launch_permute_fp8(const void* x, const int32_t* perm_row, uint8_t* x8, float* x_scale,
+                               uint8_t* xs8, float* xs_scale, int T, int d, int k,
+                               cudaStream_t stream) {
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    return launch_pdl(k_permute_f16, dim3(grid), dim3(kPCWarps * 32), 0, stream,
-                      static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm16),
-                      static_cast<uint4*>(x16), T, nvec, k, status);
+    return launch_pdl(k_permute_fp8, dim3(grid), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), perm_row, x8, x_scale, xs8, xs_scale, T, d, k);
+}
+
+cudaError_t launch_split_rows_e4m3(const void* h, const int32_t* block_metadata,
+                                   const int32_t* num_blocks, int nb_cap, int K, uint8_t* h8,
+                                   float* h_scale, const void* hs, int Ts, int Ks, uint8_t* hs8,
+                                   float* hs_scale, cudaStream_t stream) {
+    const int dense = hs ? (Ts + 127) / 128 : 0;
+    const int grid = nb_cap + dense;
+    if (grid <= 0) return cudaSuccess;
+    return launch_pdl(k_split_rows_e4m3, dim3(grid), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(h), block_metadata, num_blocks, nb_cap, K, h8, h_scale,
+                      static_cast<const uint4*>(hs), Ts, Ks, hs8, hs_scale);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace moe {
 
@@ -157,8 +158,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// The same with f16 A and B (format code 0 in bits [7,10) and [10,13)).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B
+// (format code 0 in bits [7,10) and [10,13)), fp32 accumulator, K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -173,15 +175,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// The same MMA with A read from tensor memory (M = 128 lanes, 16 K-elements
-// in 8 consecutive 32-bit columns per lane) instead of shared memory.
-__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit operands (kind::f8f6f4),
+// M = 128, K = 32 (32 bytes of each 128-byte swizzled row).
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -222,26 +224,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
-// Each thread of the warp writes 32 consecutive 32-bit columns of its own TMEM
-// lane; tmem_st_wait() returns once the warp's stores have completed.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 
 // ------------------------------------------------ CTA pairs (clusters of 2) --
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -404,11 +386,49 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
     return r;
 }
 
-// Nearest e4m3 code of v, ties to even, saturating at +-448.
-__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+// Nearest e4m3 codes of two values (v0 in the low byte), ties to even,
+// saturating at +-448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float v0, float v1) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
-    return static_cast<uint8_t>(r & 0xFFu);  // the second source lands in the low byte
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+    return r;
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+    return static_cast<uint8_t>(f32x2_to_e4m3x2(v, 0.0f) & 0xFFu);
+}
+
+// ------------------------------------------------ e4m3 activation pairs --
+// A 16-bit activation row v enters the 8-bit MMA as two e4m3 rows with one
+// power-of-two row scale 2^sig:  v * 2^sig = hi + lo,  hi = e4m3(v * 2^sig),
+// lo = e4m3(v * 2^sig - hi).  With 2^sig the largest power of two that keeps
+// the row's largest magnitude within 448, hi carries the top 4 significant
+// bits and lo the rest: the pair is exact for every element within 2^10 of
+// the row's largest and off by at most 2^-10 (before the 2^-sig) below that.
+__device__ __forceinline__ float e4m3_row_scale(float amax) {
+    if (!(amax > 0.0f) || !(amax <= 3.0e38f)) return 1.0f;  // zero or non-finite row
+    int e;
+    const float m = frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1); 448 = 0.875 * 2^9
+    int sig = (m <= 0.875f ? 9 : 8) - e;
+    sig = sig < -120 ? -120 : (sig > 120 ? 120 : sig);
+    return ldexpf(1.0f, sig);
+}
+
+// Eight values (already multiplied by the row scale) -> eight hi codes and
+// eight lo codes, element i in byte i.
+__device__ __forceinline__ void e4m3_split8(const float (&a)[8], uint2& hi, uint2& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint16_t hc = f32x2_to_e4m3x2(a[2 * i], a[2 * i + 1]);
+        const uint32_t hf = e4m3x2_to_f16x2(hc);
+        const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hf));
+        const uint16_t lc = f32x2_to_e4m3x2(a[2 * i] - hv.x, a[2 * i + 1] - hv.y);
+        h[i] = hc;
+        l[i] = lc;
+    }
+    hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
 
 }  // namespace moe

@@ -114,7 +114,10 @@ def test_empty_batch_is_a_noop(lib):
 def test_fp8_entry_points_check_arguments_before_launch(lib):
     cfg = _cfg()
     fake = ctypes.c_void_p(0x1000)
-    need = moe.moe_workspace_size(cfg)
+    need = moe.moe_workspace_size_fp8(cfg)
+    assert need > moe.moe_workspace_size(cfg)  # the e4m3 layer needs its extra regions
+    L8 = moe.moe_workspace_layout_fp8(cfg)
+    assert L8["total"] == need and L8["row_scale"] > L8["h8"] >= L8["xs8"] > L8["router_partial"]
     w = moe.MoeWeightsFp8(Wg_t=0x1000, bias=None, W13q=0x1000, s13=0x1000, W2q=0x1000, s2=0x1000)
     assert lib.moe_layer_fwd_fp8(ctypes.byref(cfg), ctypes.byref(w), fake, fake, fake, need - 1,
                                  None) == 3
@@ -123,17 +126,20 @@ def test_fp8_entry_points_check_arguments_before_launch(lib):
                                  need, None) == 1
     assert "scales" in lib.moe_last_error().decode()
     cfg_s = _cfg(d_shared=256)
-    need_s = moe.moe_workspace_size(cfg_s)
+    need_s = moe.moe_workspace_size_fp8(cfg_s)
     assert lib.moe_layer_fwd_fp8(ctypes.byref(cfg_s), ctypes.byref(w), fake, fake, fake, need_s,
                                  None) == 1
     assert lib.moe_layer_fwd_fp8_prerouted(ctypes.byref(cfg), ctypes.byref(w), fake, None, fake,
                                            fake, fake, need, None) == 1
     # null operands of the stage calls
-    assert lib.moe_grouped_gemm_swiglu_fp8(ctypes.byref(cfg), fake, fake, None, fake, fake, fake,
-                                           fake, None, fake, fake, None, None) == 1
+    args15 = [fake] * 15
+    args15[11] = None  # h8
+    assert lib.moe_grouped_gemm_swiglu_fp8(ctypes.byref(cfg), *args15) == 1
     assert lib.moe_grouped_gemm_swiglu_skinny(ctypes.byref(cfg), fake, fake, fake, None, fake,
                                               None, fake, fake, None, None) == 1
-    assert lib.moe_permute_f16(ctypes.byref(cfg), fake, fake, None, None, None, None) == 1
+    assert lib.moe_permute_fp8(ctypes.byref(cfg), fake, fake, fake, None, None, None, None) == 1
+    assert lib.moe_permute_fp8(ctypes.byref(cfg), fake, fake, fake, fake, fake, None, None) == 1
+    assert lib.moe_shared_expert_fp8(ctypes.byref(cfg_s), *([fake] * 9), None, None, None) == 1
     # packing: shape rules
     assert lib.moe_pack_experts_fp8(2, 200, 128, fake, fake, fake, fake, fake, fake, fake,
                                     None) == 2
@@ -142,6 +148,8 @@ def test_fp8_entry_points_check_arguments_before_launch(lib):
     # T = 0 is a no-op
     cfg0 = _cfg(T=0)
     assert lib.moe_layer_fwd_fp8(ctypes.byref(cfg0), ctypes.byref(w), fake, fake, fake,
-                                 moe.moe_workspace_size(cfg0), None) == 0
-    assert lib.moe_grouped_gemm_swiglu_fp8(ctypes.byref(cfg0), fake, fake, fake, fake, fake, fake,
-                                           fake, None, fake, fake, None, None) == 0
+                                 moe.moe_workspace_size_fp8(cfg0), None) == 0
+    args15 = [fake] * 15
+    args15[13] = None  # status
+    args15[14] = None  # stream
+    assert lib.moe_grouped_gemm_swiglu_fp8(ctypes.byref(cfg0), *args15) == 0

@@ -3,7 +3,8 @@ expert-weight path, against the CPU oracle on the same seeded inputs.
 
   - moe_pack_experts_fp8: codes and scales bit-exact against the oracle's
     quantizer (the integer codes are decided in fp32 on both sides);
-  - moe_permute_f16: f16 rows bit-exact against the bf16 -> f16 conversion;
+  - moe_permute_fp8 and the split of h: the e4m3 pairs and row scales
+    byte-exact against torch's float8 casts under the same row scale;
   - moe_grouped_gemm_swiglu_skinny (bf16 weights) and
     moe_grouped_gemm_swiglu_fp8: h and y of every valid row within the
     tolerances of the bf16 path (relative Frobenius <= 5e-3, max error
@@ -119,28 +120,49 @@ def test_pack_fp8_matches_oracle():
     assert np.array_equal(s2.cpu().numpy(), ref["S2"])
 
 
-def test_permute_f16_copies_rows_and_flags_range():
+def _pairs_ref(rows_f32: torch.Tensor):
+    """Expected e4m3 pairs of float32 rows (CPU): the row scale 2^sig is the
+    largest power of two with max|v| * 2^sig <= 448, hi and lo are torch's
+    nearest-even float8_e4m3fn casts of v * 2^sig and of the remainder."""
+    v = rows_f32.double()
+    amax = v.abs().amax(dim=1)
+    sig = torch.where(amax > 0, torch.floor(torch.log2(448.0 / amax)), torch.zeros_like(amax))
+    # guard the floor of a log against rounding at exact powers of two
+    sig = torch.where(amax * 2.0 ** (sig + 1) <= 448.0, sig + 1, sig)
+    sig = torch.where(amax * 2.0 ** sig > 448.0, sig - 1, sig)
+    a = (v * 2.0 ** sig[:, None]).float()
+    hi = a.to(torch.float8_e4m3fn)
+    lo = (a - hi.float()).to(torch.float8_e4m3fn)
+    return hi.view(torch.uint8), lo.view(torch.uint8), (2.0 ** -sig).float()
+
+
+def test_permute_fp8_pairs_match_float8_casts():
     shape, inp, oin, ref = prepared("full_blocks", False)
     cfg = moe.config_of(shape)
     x = cuda(inp["x"])
-    R, d = shape.rows_capacity, shape.d
+    T, d, R = shape.T, shape.d, shape.rows_capacity
     perm_row = torch.as_tensor(ref["perm_row"], device="cuda")
-    xp16 = torch.zeros((R, d), dtype=torch.float16, device="cuda")
-    x16 = torch.zeros((shape.T, d), dtype=torch.float16, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    moe.moe_permute_f16(cfg, x, perm_row, xp16, x16, status)
+    x8 = torch.zeros((2 * R, d), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros(R, dtype=torch.float32, device="cuda")
+    xs8 = torch.zeros((2 * T, d), dtype=torch.uint8, device="cuda")
+    xss = torch.zeros(T, dtype=torch.float32, device="cuda")
+    moe.moe_permute_fp8(cfg, x, perm_row, x8, xs, xs8, xss)
     torch.cuda.synchronize()
-    assert int(status.item()) == 0
-    assert torch.equal(x16, x.half())
-    rs = torch.as_tensor(ref["row_src"], device="cuda")
-    valid = rs >= 0
-    assert torch.equal(xp16[valid], x.half()[(rs[valid] // shape.k).long()])
-    # a finite bf16 value past f16's range is flagged (the data, not a fault)
-    x2 = x.clone()
-    x2[3, 5] = 65536.0
-    moe.moe_permute_f16(cfg, x2, perm_row, xp16, None, status)
-    torch.cuda.synchronize()
-    assert int(status.item()) == moe.DEVERR_F16_RANGE
+    hi, lo, sc = _pairs_ref(inp["x"].float())
+    assert torch.equal(xs8[0::2].cpu(), hi) and torch.equal(xs8[1::2].cpu(), lo)
+    assert torch.equal(xss.cpu(), sc)
+    rs = ref["row_src"]
+    valid = np.flatnonzero(rs >= 0)
+    tok = torch.as_tensor(rs[valid] // shape.k)
+    vr = torch.as_tensor(valid, device="cuda")
+    assert torch.equal(x8[2 * vr].cpu(), hi[tok]) and torch.equal(x8[2 * vr + 1].cpu(), lo[tok])
+    assert torch.equal(xs[vr].cpu(), sc[tok])
+    # hi + lo carries the bf16 values: exact within 2^10 of the row maximum
+    recon = (hi.view(torch.float8_e4m3fn).double() + lo.view(torch.float8_e4m3fn).double()) * \
+        sc.double()[:, None]
+    xv = inp["x"].double()
+    err = (recon - xv).abs()
+    assert float((err / xv.abs().amax(dim=1, keepdim=True)).max()) < 2.0 ** -17
 
 
 # ------------------------------------------------------------- stages ----
@@ -181,51 +203,64 @@ def test_skinny_stage_bf16(name):
     _compare_rows(shape, ref, h, y)
 
 
+def _fp8_weights(inp, E, d, de, key=("W1", "W3", "W2")):
+    q13 = torch.empty((E, 2 * de, d), dtype=torch.uint8, device="cuda")
+    s13 = torch.empty((E, 2 * de), dtype=torch.float32, device="cuda")
+    q2 = torch.empty((E, d, de), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty((E, d), dtype=torch.float32, device="cuda")
+    w = [cuda(inp[k_]) for k_ in key]
+    if w[0].dim() == 2:
+        w = [t.unsqueeze(0).contiguous() for t in w]
+    moe.moe_pack_experts_fp8(w[0], w[1], w[2], q13, s13, q2, s2)
+    return q13, s13, q2, s2
+
+
 @pytest.mark.parametrize("name", ["decode_like", "full_blocks", "half_panel_p64"])
 def test_fp8_stage(name):
     shape, inp, oin, ref = prepared(name, True)
     cfg = moe.config_of(shape)
     E, d, de, R = shape.E, shape.d, shape.d_e, shape.rows_capacity
-    q13 = torch.empty((E, 2 * de, d), dtype=torch.uint8, device="cuda")
-    s13 = torch.empty((E, 2 * de), dtype=torch.float32, device="cuda")
-    q2 = torch.empty((E, d, de), dtype=torch.uint8, device="cuda")
-    s2 = torch.empty((E, d), dtype=torch.float32, device="cuda")
-    moe.moe_pack_experts_fp8(cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), q13, s13, q2, s2)
-    xp16 = torch.zeros((R, d), dtype=torch.float16, device="cuda")
+    q13, s13, q2, s2 = _fp8_weights(inp, E, d, de)
+    x8 = torch.zeros((2 * R, d), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros(R, dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    moe.moe_permute_f16(cfg, cuda(inp["x"]), torch.as_tensor(ref["perm_row"], device="cuda"),
-                        xp16, None, status)
+    moe.moe_permute_fp8(cfg, cuda(inp["x"]), torch.as_tensor(ref["perm_row"], device="cuda"), x8, xs)
     meta, nb, row_gate = _stage_tables(shape, ref)
-    h16 = torch.full((R, de), float("nan"), dtype=torch.float16, device="cuda")
+    h = torch.full((R, de), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h8 = torch.zeros((2 * R, de), dtype=torch.uint8, device="cuda")
+    hsc = torch.zeros(R, dtype=torch.float32, device="cuda")
     y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    moe.moe_grouped_gemm_swiglu_fp8(cfg, xp16, q13, s13, q2, s2, meta, nb, row_gate, h16, y,
+    moe.moe_grouped_gemm_swiglu_fp8(cfg, x8, xs, q13, s13, q2, s2, meta, nb, row_gate, h, h8, hsc, y,
                                     status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    # h holds bf16-rounded values in f16
+    _compare_rows(shape, ref, h, y)
+    # the pairs of h that GEMM2 multiplied are those of the GPU's own h
     vt = torch.as_tensor(np.flatnonzero(ref["row_src"] >= 0), device="cuda")
-    assert torch.equal(h16[vt].float().bfloat16().float(), h16[vt].float())
-    _compare_rows(shape, ref, h16, y)
+    hi, lo, sc = _pairs_ref(h[vt].float().cpu())
+    assert torch.equal(h8[2 * vt].cpu(), hi) and torch.equal(h8[2 * vt + 1].cpu(), lo)
+    assert torch.equal(hsc[vt].cpu(), sc)
 
 
 def test_shared_expert_fp8_stage():
     shape, inp, oin, ref = prepared("full_blocks", True)
     cfg = moe.config_of(shape)
-    T, d, ds = shape.T, shape.d, shape.d_shared
-    q13 = torch.empty((1, 2 * ds, d), dtype=torch.uint8, device="cuda")
-    s13 = torch.empty((1, 2 * ds), dtype=torch.float32, device="cuda")
-    q2 = torch.empty((1, d, ds), dtype=torch.uint8, device="cuda")
-    s2 = torch.empty((1, d), dtype=torch.float32, device="cuda")
-    moe.moe_pack_experts_fp8(cuda(inp["Ws1"]).unsqueeze(0), cuda(inp["Ws3"]).unsqueeze(0),
-                             cuda(inp["Ws2"]).unsqueeze(0), q13, s13, q2, s2)
-    x16 = cuda(inp["x"]).half()
-    hs16 = torch.full((T, ds), float("nan"), dtype=torch.float16, device="cuda")
+    T, d, ds, R = shape.T, shape.d, shape.d_shared, shape.rows_capacity
+    q13, s13, q2, s2 = _fp8_weights(inp, 1, d, ds, key=("Ws1", "Ws3", "Ws2"))
+    xs8 = torch.zeros((2 * T, d), dtype=torch.uint8, device="cuda")
+    xss = torch.zeros(T, dtype=torch.float32, device="cuda")
+    moe.moe_permute_fp8(cfg, cuda(inp["x"]), torch.as_tensor(ref["perm_row"], device="cuda"),
+                        torch.zeros((2 * R, d), dtype=torch.uint8, device="cuda"),
+                        torch.zeros(R, dtype=torch.float32, device="cuda"), xs8, xss)
+    hs = torch.full((T, ds), float("nan"), dtype=torch.bfloat16, device="cuda")
+    hs8 = torch.zeros((2 * T, ds), dtype=torch.uint8, device="cuda")
+    hss = torch.zeros(T, dtype=torch.float32, device="cuda")
     ys = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    moe.moe_shared_expert_fp8(cfg, x16, q13, s13, q2, s2, hs16, ys, status)
+    moe.moe_shared_expert_fp8(cfg, xs8, xss, q13, s13, q2, s2, hs, hs8, hss, ys, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert_close(hs16.double().cpu().numpy(), ref["hs"], "hs (e4m3)")
+    assert_close(hs.double().cpu().numpy(), ref["hs"], "hs (e4m3)")
     assert_close(ys.double().cpu().numpy(), ref["ys"], "ys (e4m3)")
 
 
