@@ -147,3 +147,87 @@ def test_full_size_layer(name):
     got = out[torch.as_tensor(toks, device=dev, dtype=torch.long)].double().cpu().numpy()
     assert_close(got, ref_out, "out (sampled tokens)")
     assert torch.isfinite(out.float()).all()
+
+
+def _packed_rows(de):
+    """Packed W13 row r -> (0 gate / 1 up, output column)."""
+    r = np.arange(2 * de)
+    return (r % 256 >= 128).astype(np.int64), (r // 256) * 128 + r % 128
+
+
+@pytest.mark.parametrize("name", ["decode"])
+def test_full_size_layer_fp8(name):
+    """The e4m3-weight layer at the full decode size, in the bench's launch
+    configuration: routing and tables bit-exact, the packed codes and scales of
+    the sampled experts bit-exact against the oracle's quantizer, sampled h, y
+    and token outputs within the tolerances against the oracle evaluating the
+    dequantized weights."""
+    shape = synth.WORKLOADS[name]
+    dev = torch.device("cuda")
+    inp = synth.make_inputs(shape, device="cpu", weights_device=dev)
+    enforce_margin(inp, shape)
+    cfg = moe.config_of(shape)
+    g = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=g(inp.get("Wg")),
+                         bias=g(inp.get("bias")), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
+                         Ws2=inp.get("Ws2"), fp8=True)
+    x = g(inp["x"])
+    out = layer(x)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    T, k, E, d, de = shape.T, shape.k, shape.E, shape.d, shape.d_e
+    A, R = shape.A, shape.rows_capacity
+    x_bits = bits(inp["x"])
+    bias = None if inp.get("bias") is None else inp["bias"].numpy()
+    lg = oracle.router_logits(x_bits, bits(inp["Wg"]), bias)
+    idx, w, margin = oracle.route(lg, k, shape.n_groups, shape.topk_groups)
+    assert margin.min() >= 1e-3
+    i32 = torch.int32
+    assert np.array_equal(layer.buffer("topk_idx", i32, (T, k)).cpu().numpy(), idx)
+    off = oracle.build_offsets(idx, w, E, shape.pad)
+    perm_row = layer.buffer("perm_row", i32, (A,)).cpu().numpy()
+    assert np.array_equal(perm_row, off["perm_row"])
+
+    rng = np.random.default_rng(11)
+    row_src = off["row_src"]
+    samp = np.sort(rng.choice(np.flatnonzero(row_src >= 0), size=6, replace=False))
+    seg = np.searchsorted(off["padded_offsets"], samp, side="right") - 1
+    toks = np.sort(rng.choice(T, size=2, replace=False)).astype(np.int32)
+    used = np.unique(np.concatenate([seg, idx[toks].reshape(-1)]))
+    remap = {e: i for i, e in enumerate(used)}
+    q = oracle.quantize_experts(dict(W1=_expert_subset(inp["W1"], used),
+                                     W3=_expert_subset(inp["W3"], used),
+                                     W2=_expert_subset(inp["W2"], used)))
+    # the GPU's packed codes and scales of these experts
+    ut = torch.as_tensor(used, device=dev, dtype=torch.long)
+    which, col = _packed_rows(de)
+    q13 = layer.W13q[ut].cpu().numpy()
+    exp13 = np.where(which[None, :, None] == 0, q["Q1"].transpose(0, 2, 1)[:, col, :],
+                     q["Q3"].transpose(0, 2, 1)[:, col, :])
+    assert np.array_equal(q13, exp13)
+    assert np.array_equal(layer.s13[ut].cpu().numpy(),
+                          np.where(which[None, :] == 0, q["S1"][:, col], q["S3"][:, col]))
+    assert np.array_equal(layer.W2q[ut].cpu().numpy(), q["Q2"].transpose(0, 2, 1))
+    assert np.array_equal(layer.s2[ut].cpu().numpy(), q["S2"])
+
+    # h, y of sampled padded rows
+    ref_xp = oracle.permute(x_bits, np.where(np.isin(np.arange(R), samp), row_src, -1), k)
+    eh, ey = oracle.expert_rows_w8(ref_xp[samp], np.array([remap[e] for e in seg], np.int32),
+                                   off["row_gate"][samp], q)
+    st = torch.as_tensor(samp, device=dev)
+    h = layer.buffer("h", torch.bfloat16, (R, de))
+    y = layer.buffer("y", torch.bfloat16, (R, d))
+    assert_close(h[st].double().cpu().numpy(), eh, "h (sampled rows, e4m3)")
+    assert_close(y[st].double().cpu().numpy(), ey, "y (sampled rows, e4m3)")
+
+    # sampled tokens: routed experts through the oracle's rows, plus the shared expert
+    qs = oracle.quantize_shared(dict(Ws1=bits(inp["Ws1"].cpu()), Ws3=bits(inp["Ws3"].cpu()),
+                                     Ws2=bits(inp["Ws2"].cpu())))
+    _, ys = oracle.shared_expert_w8(x_bits[toks], qs)
+    rows = np.repeat(toks, k)
+    _, yr = oracle.expert_rows_w8(x_bits[rows], np.array([remap[e] for e in idx[toks].reshape(-1)],
+                                                          np.int32), w[toks].reshape(-1), q)
+    ref_out = yr.reshape(toks.size, k, d).sum(axis=1) + ys
+    got = out[torch.as_tensor(toks, device=dev, dtype=torch.long)].double().cpu().numpy()
+    assert_close(got, ref_out, "out (sampled tokens, e4m3)")
+    assert torch.isfinite(out.float()).all()
