@@ -80,6 +80,7 @@ def _L():
                 "or_expert_rows_w8": (I, [I, I, I, I] + [P] * 11),
                 "or_e4m3_to_double_array": (None, [LL, P, P]),
                 "or_double_to_e4m3_array": (None, [LL, P, P]),
+                "or_layer_backward": (I, [I] * 6 + [P] * 22),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -357,6 +358,40 @@ def grouped_experts_w8(x_perm, q: dict, block_metadata, row_gate):
         h[rows] = hh
         y[rows] = yy
     return h, y
+
+
+# ------------------------------------------------------------- backward ----
+def layer_backward(inp: dict, cfg, fwd: dict, dout) -> dict:
+    """Gradients of the layer forward (``layer_forward``'s routing, fixed) for
+    an upstream gradient dout [T, d] (fp64): dx, dgates [T, k], dW1, dW3,
+    dW2, and with a router dlogits [T, E], dWg [d, E], dbias [E], with a
+    shared expert dWs1, dWs3, dWs2 -- all fp64.  The top-k choice is held
+    constant and the bf16 rounding of h passes its gradient through."""
+    x = _c(inp["x"], np.uint16)
+    T, d = x.shape
+    W1, W3, W2 = (_c(inp[n], np.uint16) for n in ("W1", "W3", "W2"))
+    E, _, de = W1.shape
+    k = cfg.k
+    ds = cfg.d_shared
+    idx = _c(fwd["topk_idx"], np.int32)
+    gates = _c(fwd["topk_w"], np.float64)
+    routed = inp.get("Wg") is not None and inp.get("topk_idx") is None
+    Wg = _c(inp["Wg"], np.uint16) if routed else None
+    Ws = [(_c(inp[n], np.uint16) if ds else None) for n in ("Ws1", "Ws3", "Ws2")]
+    g = _c(dout, np.float64)
+    out = dict(dx=np.empty((T, d)), dgates=np.empty((T, k)), dW1=np.empty((E, d, de)),
+               dW3=np.empty((E, d, de)), dW2=np.empty((E, de, d)))
+    if routed:
+        out.update(dlogits=np.empty((T, E)), dWg=np.empty((d, E)), dbias=np.empty(E))
+    if ds:
+        out.update(dWs1=np.empty((d, ds)), dWs3=np.empty((d, ds)), dWs2=np.empty((ds, d)))
+    gp = lambda n: _p(out.get(n))  # noqa: E731
+    _check(_L().or_layer_backward(T, d, de, E, k, ds, _p(x), _p(Wg), _p(idx), _p(gates), _p(W1),
+                                  _p(W3), _p(W2), _p(Ws[0]), _p(Ws[1]), _p(Ws[2]), _p(g),
+                                  gp("dx"), gp("dgates"), gp("dlogits"), gp("dWg"), gp("dbias"),
+                                  gp("dW1"), gp("dW3"), gp("dW2"), gp("dWs1"), gp("dWs3"),
+                                  gp("dWs2")), "layer_backward")
+    return out
 
 
 # ---------------------------------------------------------- whole layer ----

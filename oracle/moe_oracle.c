@@ -30,6 +30,9 @@
  *    weight) and "Dropless and grouped GEMM", sec. 12 (the scale multiplies
  *    the product when one scale covers the whole contraction): e4m3 codes
  *    with one fp32 scale per output channel.
+ *  - the backward: "Dropless and grouped GEMM", sec. 4 (only the sort
+ *    indices need saving; the permutation is undone by the transposed
+ *    gather).
  *
  * Readings where the pages are silent or disagree (each one is listed with
  * its reason in the design notes of the repository):
@@ -665,6 +668,232 @@ int or_direct_layer(int n, const int32_t *tok, int d, int de, int E, int k, cons
         free(au);
         free(yy);
     }
+    return bad ? OR_ERR_ARG : OR_OK;
+}
+
+/* ------------------------------------------------------------- backward -- */
+/*
+ * Gradient of the layer forward above for an upstream gradient dout [T, d]:
+ *   out[t] = sum_j p[t,j] * (h_a W2[e]) + ys[t],  a = t*k + j, e = idx[a],
+ *   h_a = bf16(silu(x_t W1[e]) * (x_t W3[e])),  p = routing weights.
+ * Readings: the expert choice (top-k) is a constant of the step; the bf16
+ * rounding of h is passed straight through (its derivative is taken as 1, and
+ * the rounded value is the one multiplied by W2 and by the gradient); with a
+ * router the weights are a softmax over the k chosen logits, so
+ *   dlogit[t, idx[t,j]] = p_j * (dp_j - sum_i p_i dp_i),  other experts 0,
+ * and the logit bias receives the sum over tokens.  ("Dropless and grouped
+ * GEMM", sec. 4 notes that the backward only needs the sort indices saved
+ * from the forward: the permutation is undone by the transposed gather.)
+ * Outputs (fp64, every array overwritten): dx [T, d]; dgates [T, k];
+ * dW1, dW3 [E, d, de]; dW2 [E, de, d]; with Wg: dlogits [T, E], dWg [d, E],
+ * dbias [E]; with a shared expert (ds > 0): dWs1, dWs3 [d, ds], dWs2 [ds, d]. */
+static double or_sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+/* One SwiGLU expert's backward for one row: given x [d] (bf16), the expert's
+ * W1/W3 [d][de], W2 [de][d], the row's weight p and the upstream dout [d]:
+ * hr [de] (bf16-rounded h), dz = p * dout [d], dp = <dout, h W2>, dg, du [de],
+ * and dxa [d] = dg W1^T + du W3^T. */
+static void expert_row_bwd(int d, int de, const uint16_t *x, const uint16_t *W1,
+                           const uint16_t *W3, const uint16_t *W2, double p, const double *dout,
+                           double *g, double *u, double *hr, double *dz, double *dp, double *dg,
+                           double *du, double *dxa)
+{
+    for (int j = 0; j < de; ++j) g[j] = u[j] = 0.0;
+    for (int i = 0; i < d; ++i) {
+        double xi = or_bf16_to_double(x[i]);
+        for (int j = 0; j < de; ++j) {
+            g[j] += xi * or_bf16_to_double(W1[(size_t)i * de + j]);
+            u[j] += xi * or_bf16_to_double(W3[(size_t)i * de + j]);
+        }
+    }
+    for (int j = 0; j < de; ++j) hr[j] = or_round_bf16(g[j] * or_sigmoid(g[j]) * u[j]);
+    double s = 0.0;
+    for (int n = 0; n < d; ++n) {
+        double z = 0.0;
+        for (int j = 0; j < de; ++j) z += hr[j] * or_bf16_to_double(W2[(size_t)j * d + n]);
+        s += dout[n] * z;
+        dz[n] = p * dout[n];
+    }
+    *dp = s;
+    for (int j = 0; j < de; ++j) {
+        double dh = 0.0;
+        for (int n = 0; n < d; ++n) dh += dz[n] * or_bf16_to_double(W2[(size_t)j * d + n]);
+        double sg = or_sigmoid(g[j]);
+        dg[j] = dh * u[j] * sg * (1.0 + g[j] * (1.0 - sg));
+        du[j] = dh * g[j] * sg;
+    }
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < de; ++j)
+            acc += dg[j] * or_bf16_to_double(W1[(size_t)i * de + j]) +
+                   du[j] * or_bf16_to_double(W3[(size_t)i * de + j]);
+        dxa[i] = acc;
+    }
+}
+
+int or_layer_backward(int T, int d, int de, int E, int k, int ds, const uint16_t *x,
+                      const uint16_t *Wg, const int32_t *idx, const double *gates,
+                      const uint16_t *W1, const uint16_t *W3, const uint16_t *W2,
+                      const uint16_t *Ws1, const uint16_t *Ws3, const uint16_t *Ws2,
+                      const double *dout, double *dx, double *dgates, double *dlogits, double *dWg,
+                      double *dbias, double *dW1, double *dW3, double *dW2, double *dWs1,
+                      double *dWs3, double *dWs2)
+{
+    const long long A = (long long)T * k;
+    for (long long a = 0; a < A; ++a)
+        if (idx[a] < 0 || idx[a] >= E) return OR_ERR_DATA;
+    double *hr = (double *)malloc(sizeof(double) * (size_t)A * de);
+    double *dz = (double *)malloc(sizeof(double) * (size_t)A * d);
+    double *dg = (double *)malloc(sizeof(double) * (size_t)A * de);
+    double *du = (double *)malloc(sizeof(double) * (size_t)A * de);
+    double *dxa = (double *)malloc(sizeof(double) * (size_t)A * d);
+    if (!hr || !dz || !dg || !du || !dxa) {
+        free(hr); free(dz); free(dg); free(du); free(dxa);
+        return OR_ERR_ARG;
+    }
+    int bad = 0;
+    /* per assignment */
+#pragma omp parallel
+    {
+        double *g = (double *)malloc(sizeof(double) * (size_t)de);
+        double *u = (double *)malloc(sizeof(double) * (size_t)de);
+        if (!g || !u) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long long a = 0; a < A; ++a) {
+                size_t e = (size_t)idx[a], t = (size_t)(a / k);
+                expert_row_bwd(d, de, x + t * d, W1 + e * d * de, W3 + e * d * de, W2 + e * de * d,
+                               gates[a], dout + t * d, g, u, hr + a * de, dz + a * d, dgates + a,
+                               dg + a * de, du + a * de, dxa + a * d);
+            }
+        }
+        free(g);
+        free(u);
+    }
+    if (bad) {
+        free(hr); free(dz); free(dg); free(du); free(dxa);
+        return OR_ERR_ARG;
+    }
+    /* expert weight gradients: sums over the expert's rows, ascending a */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e) {
+        double *w1 = dW1 + (size_t)e * d * de, *w3 = dW3 + (size_t)e * d * de;
+        double *w2 = dW2 + (size_t)e * de * d;
+        memset(w1, 0, sizeof(double) * (size_t)d * de);
+        memset(w3, 0, sizeof(double) * (size_t)d * de);
+        memset(w2, 0, sizeof(double) * (size_t)de * d);
+        for (long long a = 0; a < A; ++a) {
+            if (idx[a] != e) continue;
+            const uint16_t *xt = x + (size_t)(a / k) * d;
+            for (int j = 0; j < de; ++j)
+                for (int n = 0; n < d; ++n) w2[(size_t)j * d + n] += hr[a * de + j] * dz[a * d + n];
+            for (int i = 0; i < d; ++i) {
+                double xi = or_bf16_to_double(xt[i]);
+                for (int j = 0; j < de; ++j) {
+                    w1[(size_t)i * de + j] += xi * dg[a * de + j];
+                    w3[(size_t)i * de + j] += xi * du[a * de + j];
+                }
+            }
+        }
+    }
+    /* dx: the routed rows of each token (ascending j) */
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        double *o = dx + (size_t)t * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        for (int j = 0; j < k; ++j)
+            for (int i = 0; i < d; ++i) o[i] += dxa[((size_t)t * k + j) * d + i];
+    }
+    /* router */
+    if (Wg) {
+        for (size_t q = 0; q < (size_t)T * E; ++q) dlogits[q] = 0.0;
+        for (int t = 0; t < T; ++t) {
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) s += gates[(size_t)t * k + j] * dgates[(size_t)t * k + j];
+            for (int j = 0; j < k; ++j) {
+                size_t a = (size_t)t * k + j;
+                dlogits[(size_t)t * E + idx[a]] += gates[a] * (dgates[a] - s);
+            }
+        }
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int t = 0; t < T; ++t) s += dlogits[(size_t)t * E + e];
+            dbias[e] = s;
+        }
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < d; ++i)
+            for (int e = 0; e < E; ++e) {
+                double s = 0.0;
+                for (int t = 0; t < T; ++t)
+                    s += or_bf16_to_double(x[(size_t)t * d + i]) * dlogits[(size_t)t * E + e];
+                dWg[(size_t)i * E + e] = s;
+            }
+#pragma omp parallel for schedule(static)
+        for (int t = 0; t < T; ++t)
+            for (int i = 0; i < d; ++i) {
+                double s = 0.0;
+                for (int e = 0; e < E; ++e)
+                    s += dlogits[(size_t)t * E + e] * or_bf16_to_double(Wg[(size_t)i * E + e]);
+                dx[(size_t)t * d + i] += s;
+            }
+    }
+    /* shared expert: the same row backward with weight 1 for every token */
+    if (ds > 0) {
+        double *shr = (double *)malloc(sizeof(double) * (size_t)T * ds);
+        double *sdg = (double *)malloc(sizeof(double) * (size_t)T * ds);
+        double *sdu = (double *)malloc(sizeof(double) * (size_t)T * ds);
+        double *sdx = (double *)malloc(sizeof(double) * (size_t)T * d);
+        double *sdz = (double *)malloc(sizeof(double) * (size_t)T * d);
+        if (!shr || !sdg || !sdu || !sdx || !sdz) {
+            bad = 1;
+        } else {
+#pragma omp parallel
+            {
+                double *g = (double *)malloc(sizeof(double) * (size_t)ds);
+                double *u = (double *)malloc(sizeof(double) * (size_t)ds);
+                double dp;
+                if (g && u) {
+#pragma omp for schedule(dynamic, 1)
+                    for (int t = 0; t < T; ++t)
+                        expert_row_bwd(d, ds, x + (size_t)t * d, Ws1, Ws3, Ws2, 1.0,
+                                       dout + (size_t)t * d, g, u, shr + (size_t)t * ds,
+                                       sdz + (size_t)t * d, &dp, sdg + (size_t)t * ds,
+                                       sdu + (size_t)t * ds, sdx + (size_t)t * d);
+                } else {
+#pragma omp atomic write
+                    bad = 1;
+                }
+                free(g);
+                free(u);
+            }
+            if (!bad) {
+#pragma omp parallel for schedule(static)
+                for (int j = 0; j < ds; ++j)
+                    for (int n = 0; n < d; ++n) {
+                        double s = 0.0;
+                        for (int t = 0; t < T; ++t) s += shr[(size_t)t * ds + j] * sdz[(size_t)t * d + n];
+                        dWs2[(size_t)j * d + n] = s;
+                    }
+#pragma omp parallel for schedule(static)
+                for (int i = 0; i < d; ++i)
+                    for (int j = 0; j < ds; ++j) {
+                        double s1 = 0.0, s3 = 0.0;
+                        for (int t = 0; t < T; ++t) {
+                            double xi = or_bf16_to_double(x[(size_t)t * d + i]);
+                            s1 += xi * sdg[(size_t)t * ds + j];
+                            s3 += xi * sdu[(size_t)t * ds + j];
+                        }
+                        dWs1[(size_t)i * ds + j] = s1;
+                        dWs3[(size_t)i * ds + j] = s3;
+                    }
+                for (size_t q = 0; q < (size_t)T * d; ++q) dx[q] += sdx[q];
+            }
+        }
+        free(shr); free(sdg); free(sdu); free(sdx); free(sdz);
+    }
+    free(hr); free(dz); free(dg); free(du); free(dxa);
     return bad ? OR_ERR_ARG : OR_OK;
 }
 
