@@ -194,6 +194,52 @@ def oracle_sample_tflops(shape, inp_host: dict, n_tokens: int):
     return flops / dt / 1e12, dt, oracle.num_threads()
 
 
+def oracle_train_sample_tflops(shape, inp_host: dict, n_tokens: int):
+    """fp64 CPU oracle forward + backward of the layer on the first n_tokens
+    tokens of the workload (the same weights; upstream gradient seeded).
+    Returns (useful TFLOP/s, seconds, threads)."""
+    import dataclasses
+
+    import numpy as np
+
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    sub = dataclasses.replace(shape, T=n_tokens)
+    oi = {}
+    for key, v in inp_host.items():
+        if v is None:
+            oi[key] = None
+        elif key in ("topk_idx", "topk_w", "x"):
+            v = v[:n_tokens]
+            oi[key] = bits(v) if v.dtype == torch.bfloat16 else (
+                v.double().numpy() if key == "topk_w" else v.numpy())
+        elif v.dtype == torch.bfloat16:
+            oi[key] = bits(v)
+        else:
+            oi[key] = v.numpy()
+    gen = torch.Generator().manual_seed(shape.seed + 1000)
+    dout = torch.randn((n_tokens, shape.d), generator=gen).to(torch.bfloat16).double().numpy()
+    t0 = time.perf_counter()
+    fwd = oracle.layer_forward(oi, sub)
+    oracle.layer_backward(oi, sub, fwd, dout)
+    dt = time.perf_counter() - t0
+    flops = train_useful_flops(sub)
+    return flops / dt / 1e12, dt, oracle.num_threads()
+
+
+def train_useful_flops(shape) -> int:
+    """Forward + backward useful FLOP of one layer step (router included when
+    the layer routes)."""
+    E = 0 if shape.prerouted else shape.E
+    fwd = ledger.layer_useful_flops(shape.T, shape.k, shape.d, shape.d_e, shape.d_shared)
+    fwd += ledger.router_flops(shape.T, shape.d, E) if E else 0
+    return fwd + ledger.layer_backward_useful_flops(shape.T, shape.k, shape.d, shape.d_e,
+                                                    shape.d_shared, E)
+
+
 def host_inputs(shape):
     """CPU copies of the workload (seeded; same generator as the GPU run)."""
     return synth.make_inputs(shape, device="cpu")
@@ -206,6 +252,8 @@ def run_reference(args, shape, rank, world):
     import oracle
 
     inp = host_inputs(shape)
+    if args.pass_ == "train":
+        return run_reference_train(args, shape, inp)
     n_tok = max(1, oracle.num_threads())  # one token per oracle thread per step
     for _ in range(args.warmup):
         oracle_sample_tflops(shape, inp, n_tok)
@@ -232,7 +280,36 @@ def run_reference(args, shape, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_train(args, shape, inp):
+    import oracle
+
+    n_tok = max(1, oracle.num_threads())
+    for _ in range(args.warmup):
+        oracle_train_sample_tflops(shape, inp, n_tok)
+    t0 = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        _, _, threads = oracle_train_sample_tflops(shape, inp, n_tok)
+    dt = time.perf_counter() - t0
+    flops = train_useful_flops(__import__("dataclasses").replace(shape, T=n_tok)) * args.steps
+    val = flops / dt / 1e12
+    sample = (f"{n_tok} token(s) of the workload per step: the oracle's layer forward and "
+              f"backward on them")
+    line = {
+        "impl": "reference", "metric": METRIC_TRAIN, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(config_dict(shape, weights=args.weights), **{"pass": "train"}),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 METRIC = "MoE layer fwd useful TFLOP/s (bf16, fp32 accumulate)"
+METRIC_TRAIN = "MoE layer fwd+bwd useful TFLOP/s (bf16, fp32 accumulate)"
 METRIC_FP8 = "MoE layer fwd useful TFLOP/s (e4m3 expert weights, fp32 accumulate)"
 
 
@@ -350,15 +427,7 @@ def run_ours(args, shape, rank, world, local):
         if ev is not None:
             ev[6].record()
 
-    # kernels per layer forward: router (2 when split-K), offsets (1 or 3),
-    # permute (or none when fused), 2 routed GEMMs, 2 shared-expert GEMMs
-    # (none on the small-M kernel, whose launches carry the shared tiles),
-    # combine
-    offsets_launches = 1 if A <= 4096 else 3  # one-CTA offsets kernel for small batches
-    launches_per_step = ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
-                         + (1 if args.permute == "separate" else 0) + 2
-                         + (2 if ds and not skinny else 0) + 1
-                         + (1 if fp8 else 0))  # e4m3: the split of h between the GEMMs
+    launches_per_step = forward_launches(shape, skinny, fp8, args.permute == "separate")
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():
@@ -506,6 +575,185 @@ def run_ours(args, shape, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: bool = True) -> int:
+    """Kernels of one layer forward: router (2 when split-K), offsets (1 or
+    3), permute (none when fused), 2 routed GEMMs, 2 shared-expert GEMMs (none
+    on the small-M kernel, whose launches carry the shared tiles), combine,
+    and with e4m3 weights the split of h between the GEMMs."""
+    import routing_permute_grouped_gb300 as moe
+
+    cfg = moe.config_of(shape)
+    nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
+    offsets_launches = 1 if shape.A <= 4096 else 3  # one-CTA offsets kernel for small batches
+    return ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
+            + (1 if separate_permute else 0) + 2
+            + (2 if shape.d_shared and not skinny else 0) + 1 + (1 if fp8 else 0))
+
+
+def backward_launches(shape, router_grads: bool = True) -> int:
+    """Kernels of one moe_layer_bwd call."""
+    n = 1 + 4 + 4 + 2 + 1  # permute of dout; dh, gu, SwiGLU bwd, dx_perm; 4 transposes; dW2, dW13; interleave
+    routed = not shape.prerouted
+    if (routed and router_grads) or shape.d_shared:
+        n += 1  # x transpose
+    if routed:
+        n += 2 + 1  # router backward + dbias column sums; dx from the router
+        n += 2 if router_grads else 0  # dlogit transpose, dWg
+    if shape.d_shared:
+        n += 4 + 3 + 2 + 1  # gate/up, dh, SwiGLU bwd, dx; 3 transposes; 2 wgrads; interleave
+    return n + 1  # dx combine
+
+
+def run_train(args, shape, rank, world, local):
+    """Forward + backward of the layer per step (moe_layer_fwd, moe_layer_bwd)."""
+    import routing_permute_grouped_gb300 as moe
+    from routing_permute_grouped_gb300 import build as moe_build
+
+    if args.weights != "bf16":
+        raise SystemExit("--pass train runs with bf16 expert weights")
+    moe_build.build()
+    moe.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.make_inputs(shape, device="cpu", weights_device=dev)
+    for key in ("x", "Wg", "bias", "topk_idx", "topk_w"):
+        if inp.get(key) is not None:
+            inp[key] = inp[key].to(dev)
+    cfg = moe.config_of(shape)
+    layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
+                         bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
+                         Ws2=inp.get("Ws2"))
+    T, k, d, de, ds = shape.T, shape.k, shape.d, shape.d_e, shape.d_shared
+    x = inp["x"]
+    out = torch.empty_like(x)
+    gen = torch.Generator().manual_seed(shape.seed + 1000)
+    dout = torch.randn((T, d), generator=gen).to(torch.bfloat16).to(dev)
+    pre = bool(shape.prerouted)
+    kw = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if pre else {}
+    layer(x, out, **kw)
+    grads = layer.backward(x, dout, prerouted=pre)
+
+    def train_step():
+        layer(x, out, **kw)
+        layer.backward(x, dout, grads=grads, prerouted=pre)
+
+    for _ in range(max(args.warmup, 3)):
+        train_step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        train_step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_max = reduce_max(t0.elapsed_time(t1), world)
+    # split pass: forward and backward bracketed separately
+    n_split = min(args.steps, 20)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_split)]
+    for i in range(n_split):
+        evs[i][0].record()
+        layer(x, out, **kw)
+        evs[i][1].record()
+        layer.backward(x, dout, grads=grads, prerouted=pre)
+        evs[i][2].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    st = layer.device_status()
+    if st:
+        raise RuntimeError(f"device status bits {st:#x}")
+    useful = train_useful_flops(shape)
+    value = reduce_sum(useful * args.steps, world) / (ms_max / 1e3) / 1e12
+
+    # e2e: token rows and the output gradient from pinned host memory, dx
+    # back to the host, every step (weight gradients stay on the device)
+    x_host = x.cpu().pin_memory()
+    dout_host = dout.cpu().pin_memory()
+    dx_host = torch.empty_like(x_host).pin_memory()
+    xd, dd = torch.empty_like(x), torch.empty_like(dout)
+    h2d = x_host.numel() * 2 + dout_host.numel() * 2
+    kw_host = {}
+    if pre:
+        kw_host = dict(topk_idx=torch.empty_like(inp["topk_idx"]),
+                       topk_w=torch.empty_like(inp["topk_w"]))
+        idx_host = inp["topk_idx"].cpu().pin_memory()
+        w_host = inp["topk_w"].cpu().pin_memory()
+        h2d += idx_host.numel() * 4 + w_host.numel() * 4
+    d2h = dx_host.numel() * 2
+
+    def e2e_step():
+        xd.copy_(x_host, non_blocking=True)
+        dd.copy_(dout_host, non_blocking=True)
+        if pre:
+            kw_host["topk_idx"].copy_(idx_host, non_blocking=True)
+            kw_host["topk_w"].copy_(w_host, non_blocking=True)
+        layer(xd, out, **kw_host)
+        layer.backward(xd, dd, grads=grads, prerouted=pre)
+        dx_host.copy_(grads["dx"], non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+
+    pk = peaks()
+    E_r = 0 if pre else shape.E
+    bwd_flops = ledger.layer_backward_gemm_flops(T, k, d, de, ds, E_r)
+    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved = bwd_flops / (bwd_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": achieved / peak_t, "peak_source": pk["source"] + " sustained bf16",
+            "kernel": "layer backward (moe_layer_bwd: all its kernels; GEMM FLOP incl. the "
+                      "gate/up recomputation)",
+            "timing": "split pass: CUDA events around moe_layer_bwd",
+            "algorithmic": {"flop": bwd_flops}, "traffic": None}
+    skinny = T * k <= 32 * shape.E
+    line = {
+        "metric": METRIC_TRAIN, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(config_dict(shape, weights="bf16"), **{"pass": "train"}),
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": (forward_launches(shape, skinny) + backward_launches(shape)) * args.steps,
+        "roofline": roof,
+        "stages": {"ms": {"forward": round(fwd_ms, 4), "backward": round(bwd_ms, 4)}},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
+        import oracle
+
+        n0 = max(1, oracle.num_threads())
+        _, dt1, _ = oracle_train_sample_tflops(shape, host, n0)
+        n = max(n0, min(T, n0 * int(round(20.0 / max(dt1, 1e-3)))))
+        tf, dt, threads = oracle_train_sample_tflops(shape, host, n)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {n} tokens of the workload: the oracle's "
+                                          f"layer forward and backward ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources."""
@@ -535,11 +783,15 @@ def main():
                     help="permute as its own kernel, or fused into GEMM1's A load")
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weights in bf16, or e4m3 with per-output-channel scales")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",
+                    help="fwd: the layer forward; train: forward + backward per step")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     shape = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, shape, rank, world)
+    elif args.pass_ == "train":
+        run_train(args, shape, rank, world, local)
     else:
         run_ours(args, shape, rank, world, local)
     if world > 1:

@@ -97,6 +97,37 @@ typedef struct {
     const float *ss2;    /* fp32 [d] */
 } moe_weights_fp8_t;
 
+/* Extra weight layouts the backward pass multiplies by (device pointers).
+ * The data gradients run on the same K-major grouped GEMMs as the forward,
+ * so they need the weights with the other dimension as K.  W2 and Ws2 are
+ * the caller's own arrays; W13t/Ws13t come from moe_pack_experts_bwd (the
+ * gate and up weights interleaved per 128 columns, the order of the packed
+ * W13); WgP from moe_pack_router_bwd. */
+typedef struct {
+    const void *W13t;   /* bf16 [E, d, 2*d_e]: row i = (W1[e][i], W3[e][i]) interleaved */
+    const void *W2;     /* bf16 [E, d_e, d]: the unpacked W2 */
+    const void *WgP;    /* bf16 [d, Ep], Ep = E rounded up to 64, columns >= E zero;
+                         * NULL for a pre-routed forward (no router to
+                         * differentiate through) */
+    const void *Ws13t;  /* bf16 [d, 2*d_shared] (d_shared > 0), else NULL */
+    const void *Ws2;    /* bf16 [d_shared, d]: the unpacked Ws2 (d_shared > 0), else NULL */
+} moe_weights_bwd_t;
+
+/* Gradients written by moe_layer_bwd (device pointers, caller-owned, fully
+ * overwritten when T > 0; nothing is accumulated into them). */
+typedef struct {
+    void *dx;        /* bf16 [T, d] */
+    float *dgates;   /* fp32 [T, k]: gradient of the routing weights (the
+                      * topk_w of the forward), or NULL to keep it internal */
+    float *dWg;      /* fp32 [d, E] router weight gradient, or NULL (a frozen
+                      * router: dx still gets the router's term) */
+    float *dbias;    /* fp32 [E] logit-bias gradient, or NULL */
+    void *dW1, *dW3; /* bf16 [E, d, d_e] */
+    void *dW2;       /* bf16 [E, d_e, d] */
+    void *dWs1, *dWs3; /* bf16 [d, d_shared] (d_shared > 0), else NULL */
+    void *dWs2;      /* bf16 [d_shared, d] (d_shared > 0), else NULL */
+} moe_grads_t;
+
 /* Offsets (bytes) of every intermediate inside the moe_layer_fwd workspace,
  * so a caller can read them back.  All offsets are multiples of 1024. */
 typedef struct {
@@ -439,6 +470,61 @@ moe_status_t moe_layer_fwd_fp8_prerouted(const moe_config_t *cfg, const moe_weig
                                          const void *x, const int32_t *topk_idx,
                                          const float *topk_w, void *out, void *ws,
                                          size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------- backward -- */
+
+/* Backward weight layout of the routed experts: W13t [E, d, 2*d_e] from the
+ * caller's W1, W3 bf16 [E, d, d_e] (row i of expert e holds W1[e][i] and
+ * W3[e][i] interleaved per 128 columns).  d, d_e multiples of 128.  Also
+ * packs the shared expert (E = 1, W1 = Ws1, W3 = Ws3, d_e = d_shared). */
+moe_status_t moe_pack_experts_bwd(int32_t E, int32_t d, int32_t de, const void *W1,
+                                  const void *W3, void *W13t, void *stream);
+
+/* WgP bf16 [d, Ep] from the caller's router weight Wg bf16 [d, E]; Ep = E
+ * rounded up to 64, the extra columns zero. */
+moe_status_t moe_pack_router_bwd(int32_t d, int32_t E, const void *Wg, void *WgP, void *stream);
+
+/* Bytes of the moe_layer_bwd workspace; 0 if cfg is invalid. */
+size_t moe_backward_workspace_size(const moe_config_t *cfg);
+
+/* Backward of the bf16 layer.  The only state it keeps from the forward is
+ * the routing: the sort indices and what derives from them ("Dropless and
+ * grouped GEMM", sec. 4: the sort's residual is its indices, not the
+ * T*k x d copy).  It reads the first moe_workspace_layout(cfg).x_perm bytes
+ * of the forward workspace fwd_ws -- status word, topk_idx, topk_w, counts,
+ * padded offsets, block table, perm_row, row_src, row_gate -- as the
+ * moe_layer_fwd (or _prerouted) call that produced the output left them;
+ * fwd_ws_bytes may be just that prefix, so a caller training several layers
+ * can keep the prefix per layer and share the rest of the workspace.  The
+ * permuted token rows are gathered again from x, the gate/up products and h
+ * recomputed.  dout bf16 [T, d] is the gradient of out.  Nothing in fwd_ws
+ * is written but the device error word.
+ *
+ * Gradients (the routing choice is a constant; the bf16 rounding of h passes
+ * its gradient through):
+ *   dW2[e]  = sum over e's rows a of h_a^T (p_a dout[t])
+ *   dW1/dW3 from the SwiGLU backward of the recomputed g, u
+ *   dgates  = <dout[t], h_a W2[e]> for each of the k choices
+ *   dWg, dbias through the softmax over the k chosen logits (when
+ *           wb->WgP is given: a routed forward)
+ *   dx      = the k rows' dx_perm + the router's term (routed forward) + the
+ *           shared expert's term (d_shared > 0)
+ * Accumulation is fp32 inside each GEMM; GEMM outputs, dW1/dW3/dW2 and the
+ * shared weight gradients are rounded to bf16 once, dWg and dbias stay fp32.
+ *
+ * T = 0 returns MOE_OK without enqueuing anything (the gradient arrays are
+ * not touched).
+ *
+ * Returns MOE_ERR_INVALID_ARG on NULL buffers a gradient needs,
+ * MOE_ERR_WORKSPACE when bws_bytes < moe_backward_workspace_size(cfg) or
+ * fwd_ws_bytes is shorter than the routing state, the shape errors of
+ * moe_check_config, MOE_ERR_CUDA on a launch error.  Asynchronous on
+ * `stream`; bounded waits inside the kernels set MOE_DEVERR_TIMEOUT in the
+ * forward workspace's device error word. */
+moe_status_t moe_layer_bwd(const moe_config_t *cfg, const moe_weights_t *w,
+                           const moe_weights_bwd_t *wb, const void *x, const void *dout,
+                           const void *fwd_ws, size_t fwd_ws_bytes, const moe_grads_t *grads,
+                           void *bws, size_t bws_bytes, void *stream);
 
 /* ---------------------------------------------------------- diagnostics -- */
 

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) dropless MoE layer forward pass: Python binding.
+"""GB300 (sm_103a) dropless MoE layer, forward and backward: Python binding.
 
 Every compute step runs in the CUDA library ``_build/libmoe_gb300.so``
 (C ABI in ``include/moe.h``); this module only marshals torch tensors into
@@ -32,6 +32,8 @@ __all__ = [
     "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_fp8", "moe_grouped_gemm_swiglu_skinny",
     "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
     "moe_shared_expert_fp8", "moe_workspace_size_fp8", "moe_workspace_layout_fp8",
+    "MoeWeightsBwd", "MoeGrads", "moe_pack_experts_bwd", "moe_pack_router_bwd",
+    "moe_backward_workspace_size", "moe_layer_bwd",
 ]
 
 MOE_OK = 0
@@ -58,6 +60,17 @@ class MoeWeights(ctypes.Structure):
 class MoeWeightsFp8(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("Wg_t", "bias", "W13q", "s13", "W2q", "s2", "Ws13q", "ss13", "Ws2q", "ss2")]
+
+
+class MoeWeightsBwd(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W13t", "W2", "WgP", "Ws13t", "Ws2")]
+
+
+_GRAD_FIELDS = ("dx", "dgates", "dWg", "dbias", "dW1", "dW3", "dW2", "dWs1", "dWs3", "dWs2")
+
+
+class MoeGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _GRAD_FIELDS]
 
 
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
@@ -118,6 +131,12 @@ def load():
         "moe_layer_fwd_fp8": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P, SZ, P]),
         "moe_layer_fwd_fp8_prerouted": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeightsFp8), P, P, P,
                                                        P, P, SZ, P]),
+        "moe_pack_experts_bwd": (ctypes.c_int, [I32, I32, I32, P, P, P, P]),
+        "moe_pack_router_bwd": (ctypes.c_int, [I32, I32, P, P, P]),
+        "moe_backward_workspace_size": (SZ, [CP]),
+        "moe_layer_bwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights),
+                                         ctypes.POINTER(MoeWeightsBwd), P, P, P, SZ,
+                                         ctypes.POINTER(MoeGrads), P, SZ, P]),
         "moe_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -335,6 +354,35 @@ def moe_layer_fwd_fp8_prerouted(cfg, weights: MoeWeightsFp8, x, topk_idx, topk_w
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+# ---------------------------------------------------------- backward ------
+def moe_pack_experts_bwd(W1, W3, W13t, stream=None) -> None:
+    """W13t [E, d, 2*d_e] from W1, W3 [E, d, d_e] (bf16, CUDA)."""
+    E, d, de = W1.shape
+    _check(load().moe_pack_experts_bwd(E, d, de, _ptr(W1), _ptr(W3), _ptr(W13t), _stream(stream)))
+
+
+def moe_pack_router_bwd(Wg, WgP, stream=None) -> None:
+    """WgP [d, Ep] (Ep = E rounded up to 64, zero past E) from Wg [d, E]."""
+    d, E = Wg.shape
+    _check(load().moe_pack_router_bwd(d, E, _ptr(Wg), _ptr(WgP), _stream(stream)))
+
+
+def moe_backward_workspace_size(cfg: MoeConfig) -> int:
+    return int(load().moe_backward_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_layer_bwd(cfg, weights: MoeWeights, wbwd: MoeWeightsBwd, x, dout, ws, grads: dict, bws,
+                  stream=None) -> None:
+    """Backward of moe_layer_fwd(_prerouted); ``grads`` maps the moe_grads_t
+    field names to caller-owned CUDA tensors (missing or None = NULL)."""
+    g = MoeGrads(**{n: (None if grads.get(n) is None else _ptr(grads[n]).value)
+                    for n in _GRAD_FIELDS})
+    _check(load().moe_layer_bwd(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(wbwd),
+                                _ptr(x), _ptr(dout), _ptr(ws), ws.numel() * ws.element_size(),
+                                ctypes.byref(g), _ptr(bws), bws.numel() * bws.element_size(),
+                                _stream(stream)))
+
+
 def moe_get_device_status(ws, stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error bits."""
     bits = ctypes.c_uint32(0)
@@ -376,6 +424,9 @@ class MoeLayer:
         if fp8:
             self._init_fp8(cfg, W1, W3, W2, Wg, bias, Ws1, Ws3, Ws2, stream)
             return
+        # the caller's weights, kept by reference for the backward packs
+        self._user = dict(W1=W1, W3=W3, W2=W2, Wg=Wg, Ws1=Ws1, Ws3=Ws3, Ws2=Ws2)
+        self.wbwd = None
         self.W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device=dev)
         self.W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device=dev)
         moe_pack_experts(W1, W3, W2, self.W13, self.W2_t, stream)
@@ -454,6 +505,64 @@ class MoeLayer:
         return out
 
     __call__ = forward
+
+    def _init_bwd(self, stream=None):
+        u = self._user
+        dev = u["W1"].device
+        E, d, de = u["W1"].shape
+        self.W13t = torch.empty((E, d, 2 * de), dtype=torch.bfloat16, device=dev)
+        moe_pack_experts_bwd(u["W1"], u["W3"], self.W13t, stream)
+        self.WgP = None
+        if u["Wg"] is not None:
+            self.WgP = torch.empty((d, (E + 63) // 64 * 64), dtype=torch.bfloat16, device=dev)
+            moe_pack_router_bwd(u["Wg"], self.WgP, stream)
+        self.Ws13t = None
+        if self.cfg.d_shared:
+            self.Ws13t = torch.empty((1, d, 2 * self.cfg.d_shared), dtype=torch.bfloat16,
+                                     device=dev)
+            moe_pack_experts_bwd(u["Ws1"].unsqueeze(0).contiguous(),
+                                 u["Ws3"].unsqueeze(0).contiguous(), self.Ws13t, stream)
+
+        def p(t):
+            return None if t is None else t.data_ptr()
+
+        self.wbwd = MoeWeightsBwd(W13t=p(self.W13t), W2=p(u["W2"]), WgP=p(self.WgP),
+                                  Ws13t=p(self.Ws13t), Ws2=p(u["Ws2"]))
+        self.bws = torch.empty(moe_backward_workspace_size(self.cfg), dtype=torch.uint8,
+                               device=dev)
+
+    def backward(self, x, dout, grads: Optional[dict] = None, prerouted: bool = False,
+                 stream=None) -> dict:
+        """Gradients of the last ``forward(x)`` (its workspace must be unchanged)
+        for the output gradient ``dout`` [T, d] bf16: a dict with dx, dgates,
+        dW1, dW3, dW2, the shared dWs1/dWs3/dWs2 and, for a routed forward,
+        dWg and dbias (``moe_layer_bwd``).  ``prerouted`` marks a forward that
+        was given its routing (no router term)."""
+        if self.fp8:
+            raise NotImplementedError("the backward runs on bf16 expert weights")
+        if self.wbwd is None:
+            self._init_bwd(stream)
+        cfg, dev = self.cfg, x.device
+        T, d, de, E, k = cfg.T, cfg.d, cfg.d_e, cfg.E, cfg.k
+        if grads is None:
+            bf = dict(dtype=torch.bfloat16, device=dev)
+            f32 = dict(dtype=torch.float32, device=dev)
+            grads = dict(dx=torch.empty((T, d), **bf), dgates=torch.empty((T, k), **f32),
+                         dW1=torch.empty((E, d, de), **bf), dW3=torch.empty((E, d, de), **bf),
+                         dW2=torch.empty((E, de, d), **bf))
+            routed = self.WgP is not None and not prerouted
+            if routed:
+                grads["dWg"] = torch.empty((d, E), **f32)
+                grads["dbias"] = torch.empty((E,), **f32)
+            if cfg.d_shared:
+                ds = cfg.d_shared
+                grads.update(dWs1=torch.empty((d, ds), **bf), dWs3=torch.empty((d, ds), **bf),
+                             dWs2=torch.empty((ds, d), **bf))
+        wb = self.wbwd
+        if prerouted and wb.WgP is not None:
+            wb = MoeWeightsBwd(W13t=wb.W13t, W2=wb.W2, WgP=None, Ws13t=wb.Ws13t, Ws2=wb.Ws2)
+        moe_layer_bwd(self.cfg, self.weights, wb, x, dout, self.ws, grads, self.bws, stream)
+        return grads
 
     def buffer(self, name: str, dtype, shape, offset: int = 0) -> torch.Tensor:
         """A view of one intermediate of the workspace (see moe_workspace_layout),

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
 SOURCES = ["moe_abi.cu", "grouped_gemm.cu", "offsets.cu", "permute_combine.cu", "pack.cu",
-           "offsets_noalloc.cu", "router_reduce.cu", "skinny_gemm.cu"]
+           "offsets_noalloc.cu", "router_reduce.cu", "skinny_gemm.cu",
+           "backward.cu", "wgrad_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]

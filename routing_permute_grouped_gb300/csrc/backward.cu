@@ -1,0 +1,237 @@
+// backward.cu -- the element-wise and data-movement kernels of the layer
+// backward (the GEMMs run on the grouped kernels of grouped_gemm.cu and
+// wgrad_gemm.cu).  With out[t] = sum_j p_j (h_a W2) + ys[t], the routed rows
+// of dout are permuted like x (dz_a = dout[t]) and dh_a = dz_a W2^T is the
+// gradient before the routing weight:
+//   k_router_bwd    dlogit = p_j (dp_j - sum_i p_i dp_i) for the k chosen
+//                   experts of a token, 0 for the others (softmax over the
+//                   chosen logits; the choice itself is a constant)
+//   k_colsum        the logit-bias gradient: column sums in token order
+//   k_swiglu_bwd    h = silu(g) u recomputed from the recomputed g, u;
+//                   dg = p dh * u * silu'(g), du = p dh * silu(g) in the
+//                   gate/up interleaved column order of the packed weights;
+//                   the routing-weight gradient dp_a = <dh_a, h_a>
+//   k_transpose     [rows, C] -> [C, ld] with an optional row scale, pad rows
+//                   (and columns past rows) zero: the K-major operands of the
+//                   weight gradients
+//   k_interleave    row-wise (de)interleave of gate and up blocks of 128
+//                   columns ([.., w] x 2 <-> [.., 2w])
+// Reads of data written by earlier kernels of the stream use ld_dep.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// One thread per token: dl[t][e] (fp32, and bf16 with row stride ld16).
+__global__ void k_router_bwd(const float* __restrict__ dgates, const int32_t* __restrict__ idx,
+                             const float* __restrict__ gates, float* __restrict__ dl,
+                             __nv_bfloat16* __restrict__ dl16, int T, int E, int k, int ld16) {
+    pdl_trigger();
+    pdl_wait();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float s = 0.0f;
+    for (int j = 0; j < k; ++j) s += ld_dep(gates + (int64_t)t * k + j) * ld_dep(dgates + (int64_t)t * k + j);
+    float* row = dl + (int64_t)t * E;
+    __nv_bfloat16* row16 = dl16 + (int64_t)t * ld16;
+    for (int e = 0; e < E; ++e) row[e] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        const int e = ld_dep(idx + (int64_t)t * k + j);
+        if (e >= 0 && e < E) {
+            const float pj = ld_dep(gates + (int64_t)t * k + j);
+            row[e] += pj * (ld_dep(dgates + (int64_t)t * k + j) - s);
+        }
+    }
+    for (int e = 0; e < ld16; ++e) row16[e] = __float2bfloat16_rn(e < E ? row[e] : 0.0f);
+}
+
+// One thread per column, rows summed in order.
+__global__ void k_colsum(const float* __restrict__ m, float* __restrict__ out, int rows, int cols) {
+    pdl_trigger();
+    pdl_wait();
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float s = 0.0f;
+    for (int r = 0; r < rows; ++r) s += ld_dep(m + (int64_t)r * cols + c);
+    out[c] = s;
+}
+
+// One warp per row of h.  gu and dgu are [rows, 2w] in the interleaved
+// order (block j of 256: 128 gate columns, 128 up columns); dh is the row's
+// gradient before its routing weight p.  Recomputes h = silu(g) u (bf16,
+// written to h when not null), writes dgu = f'(g, u) * (p dh) and, when
+// dgates is not null, dgates[a] = <dh, h> for the assignment a the row
+// holds.  Pad rows (row_src < 0) are skipped.
+__global__ void __launch_bounds__(kWarps * 32)
+    k_swiglu_bwd(const __nv_bfloat16* __restrict__ gu, const __nv_bfloat16* __restrict__ dh,
+                 const int32_t* __restrict__ row_src, const float* __restrict__ row_gate,
+                 __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ dgu,
+                 float* __restrict__ dgates, int64_t rows, int w) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(kWarps) + (threadIdx.x >> 5); r < rows;
+         r += nwarps) {
+        const int a = row_src ? ld_dep(row_src + r) : static_cast<int>(r);
+        if (a < 0) continue;
+        const float p = row_gate ? ld_dep(row_gate + r) : 1.0f;
+        float dot = 0.0f;
+        for (int c = lane * 8; c < w; c += 256) {
+            const int64_t gcol = (c / 128) * 256 + (c % 128);
+            float g[8], u[8], d[8], hv[8], dg[8], du[8];
+            unpack8(ld_dep(reinterpret_cast<const uint4*>(gu + r * 2 * w + gcol)), g);
+            unpack8(ld_dep(reinterpret_cast<const uint4*>(gu + r * 2 * w + gcol + 128)), u);
+            unpack8(ld_dep(reinterpret_cast<const uint4*>(dh + r * w + c)), d);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float s = 1.0f / (1.0f + expf(-g[q]));
+                hv[q] = g[q] * s * u[q];
+                const float pd = p * d[q];
+                dg[q] = pd * u[q] * s * (1.0f + g[q] * (1.0f - s));
+                du[q] = pd * g[q] * s;
+            }
+            const uint4 hb = pack8(hv);
+            if (h) *reinterpret_cast<uint4*>(h + r * w + c) = hb;
+            if (dgates) {
+                unpack8(hb, hv);  // the bf16 h that the weight gradient sees
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dot += d[q] * hv[q];
+            }
+            *reinterpret_cast<uint4*>(dgu + r * 2 * w + gcol) = pack8(dg);
+            *reinterpret_cast<uint4*>(dgu + r * 2 * w + gcol + 128) = pack8(du);
+        }
+        if (dgates) {
+            dot = warp_sum(dot);
+            if (lane == 0) dgates[a] = dot;
+        }
+    }
+}
+
+// dst[c][r] = scale[r] * src[r][c] (scale 1 when null; 0 for a row with
+// row_src[r] < 0 and for r >= rows); 32 x 32 tiles through shared memory,
+// grid (ceil(C/32), ceil(ld/32)).
+__global__ void k_transpose(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ row_src,
+                            const float* __restrict__ scale, __nv_bfloat16* __restrict__ dst,
+                            int64_t rows, int C, int64_t ld) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ __nv_bfloat16 tile[32][33];
+    const int c0 = blockIdx.x * 32;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t r = r0 + i;
+        const int c = c0 + threadIdx.x;
+        __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+        if (r < rows && c < C && !(row_src && ld_dep(row_src + r) < 0)) {
+            v = ld_dep(src + r * C + c);
+            if (scale) v = __float2bfloat16_rn(__bfloat162float(v) * ld_dep(scale + r));
+        }
+        tile[i][threadIdx.x] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i;
+        const int64_t r = r0 + threadIdx.x;
+        if (c < C && r < ld) dst[static_cast<int64_t>(c) * ld + r] = tile[threadIdx.x][i];
+    }
+}
+
+// mode 0: out2 [n, 2w] <- (a, b) [n, w] interleaved per 128 columns;
+// mode 1: (a, b) [n, w] <- out2 [n, 2w].  One thread per 8 columns.
+__global__ void k_interleave(__nv_bfloat16* __restrict__ a, __nv_bfloat16* __restrict__ b,
+                             __nv_bfloat16* __restrict__ out2, int64_t n, int w, int mode) {
+    pdl_trigger();
+    pdl_wait();
+    const int gpr = w / 8;
+    const int64_t total = n * gpr;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / gpr;
+        const int c = static_cast<int>(i - r * gpr) * 8;
+        const int64_t g = r * 2 * w + (c / 128) * 256 + (c % 128);
+        uint4* pa = reinterpret_cast<uint4*>(a + r * w + c);
+        uint4* pb = reinterpret_cast<uint4*>(b + r * w + c);
+        uint4* po = reinterpret_cast<uint4*>(out2 + g);
+        uint4* pu = reinterpret_cast<uint4*>(out2 + g + 128);
+        if (mode == 0) {
+            *po = ld_dep(pa);
+            *pu = ld_dep(pb);
+        } else {
+            *pa = ld_dep(po);
+            *pb = ld_dep(pu);
+        }
+    }
+}
+
+int grid_for(int64_t work, int per_block) {
+    int64_t g = (work + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+    if (g > cap) g = cap;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_router_bwd(const float* dgates, const int32_t* idx, const float* gates, float* dl,
+                              void* dl16, int T, int E, int k, int ld16, float* dbias,
+                              cudaStream_t st) {
+    cudaError_t e = launch_pdl(k_router_bwd, dim3((T + 127) / 128), dim3(128), 0, st, dgates, idx, gates,
+                               dl, static_cast<__nv_bfloat16*>(dl16), T, E, k, ld16);
+    if (e != cudaSuccess || !dbias) return e;
+    return launch_pdl(k_colsum, dim3((E + 127) / 128), dim3(128), 0, st,
+                      static_cast<const float*>(dl), dbias, T, E);
+}
+
+cudaError_t launch_swiglu_bwd(const void* gu, const void* dh, const int32_t* row_src,
+                              const float* row_gate, void* h, void* dgu, float* dgates, int64_t rows,
+                              int w, cudaStream_t st) {
+    return launch_pdl(k_swiglu_bwd, dim3(grid_for(rows, kWarps)), dim3(kWarps * 32), 0, st,
+                      static_cast<const __nv_bfloat16*>(gu), static_cast<const __nv_bfloat16*>(dh),
+                      row_src, row_gate, static_cast<__nv_bfloat16*>(h),
+                      static_cast<__nv_bfloat16*>(dgu), dgates, rows, w);
+}
+
+cudaError_t launch_transpose(const void* src, const int32_t* row_src, const float* scale, void* dst,
+                             int64_t rows, int C, int64_t ld, cudaStream_t st) {
+    dim3 grid((C + 31) / 32, static_cast<unsigned>((ld + 31) / 32));
+    return launch_pdl(k_transpose, grid, dim3(32, 8), 0, st, static_cast<const __nv_bfloat16*>(src),
+                      row_src, scale, static_cast<__nv_bfloat16*>(dst), rows, C, ld);
+}
+
+cudaError_t launch_interleave(void* a, void* b, void* out2, int64_t n, int w, int mode,
+                              cudaStream_t st) {
+    const int64_t work = n * (w / 8);
+    return launch_pdl(k_interleave, dim3(grid_for(work, 256)), dim3(256), 0, st,
+                      static_cast<__nv_bfloat16*>(a), static_cast<__nv_bfloat16*>(b),
+                      static_cast<__nv_bfloat16*>(out2), n, w, mode);
+}
+
+}  // namespace moe

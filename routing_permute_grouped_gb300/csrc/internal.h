@@ -83,8 +83,11 @@ int64_t offsets_num_chunks(int64_t A);
 
 cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,
                            int k, cudaStream_t stream);
+// out[t] = sum_j y[perm_row[t*k + j]] (+ extra[t]) (+ extra2[t]), fp32, in
+// that order.
 cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,
-                           void* out, int T, int d, int k, cudaStream_t stream);
+                           void* out, int T, int d, int k, cudaStream_t stream,
+                           const void* extra2 = nullptr);
 
 // out[c, r] = in[r, c] with the output row of column c remapped by `mode`:
 // 0: row c; 1: gate rows of W13; 2: up rows of W13.  Batched over `batch`.
@@ -93,6 +96,42 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
                                   cudaStream_t stream);
 
 int num_sms();
+
+// ------------------------------------------------------------- backward --
+// Weight-gradient GEMM: out[e][m][n] = sum over rows r in [seg[e], seg[e+1])
+// of A[m][r] * B[n][r]; A [M, ldk] and B [N, ldk] bf16 K-major (row stride
+// ldk elements, ldk % 8 == 0, pad rows zero), out bf16 [n_experts, M, N].
+struct WgradArgs {
+    const int32_t* seg;  // [n_experts + 1] row offsets (device), or null: rows [0, dense_rows)
+    int32_t dense_rows;
+    int32_t n_experts, M, N, m_tiles, n_tiles;
+    void* out;
+    uint32_t* status;
+};
+cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int64_t ldk,
+                         const int32_t* seg, int n_experts, int dense_rows, void* out,
+                         uint32_t* status, cudaStream_t stream);
+// dl [T, E] (fp32) and dl16 [T, ld16] (bf16, zero past E) from dgates; dbias
+// (if not null) = column sums of dl.
+cudaError_t launch_router_bwd(const float* dgates, const int32_t* idx, const float* gates, float* dl,
+                              void* dl16, int T, int E, int k, int ld16, float* dbias,
+                              cudaStream_t st);
+// From gu [rows, 2w]: h [rows, w] = silu(g) u (bf16, if h is not null) and
+// dgu [rows, 2w] = the SwiGLU backward for the gradient row_gate[r] * dh
+// [rows, w]; dgates[row_src[r]] = <dh[r], h[r]> when dgates is not null.
+// Rows with row_src < 0 are skipped (row_src null: row r holds r);
+// row_gate null means 1.
+cudaError_t launch_swiglu_bwd(const void* gu, const void* dh, const int32_t* row_src,
+                              const float* row_gate, void* h, void* dgu, float* dgates, int64_t rows,
+                              int w, cudaStream_t st);
+// dst [C, ld] = (scale[r] * src [rows, C]) transposed; masked rows and
+// r >= rows are zero; scale null means 1.
+cudaError_t launch_transpose(const void* src, const int32_t* row_src, const float* scale, void* dst,
+                             int64_t rows, int C, int64_t ld, cudaStream_t st);
+// mode 0: out2 [n, 2w] <- gate a, up b [n, w] (interleaved per 128 columns);
+// mode 1: the inverse.
+cudaError_t launch_interleave(void* a, void* b, void* out2, int64_t n, int w, int mode,
+                              cudaStream_t st);
 
 // Device-side description of one launch of the small-M (swapped-operand)
 // grouped GEMM.  A tile multiplies 256 rows of one expert's K-major weight

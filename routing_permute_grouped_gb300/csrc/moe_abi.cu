@@ -520,6 +520,251 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
 }
 
+// ------------------------------------------------------------ backward --
+
+struct BwdLayout {
+    size_t total;
+    size_t dgates, dz, xp, gu, h, dh, dgu, dxp, xpT, hT, dzT, dguT, dW13i;  // routed experts
+    size_t dl32, dl16, dlT, xT, dxr;                                   // router
+    size_t gus, hs, dhs, dgus, dxs, hsT, doT, dgusT, dWs13i;           // shared expert
+    int64_t R64, T64, Ep;
+};
+
+static inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+static BwdLayout bwd_layout_of(const moe_config_t& c) {
+    const Sizes s = sizes_of(c);
+    BwdLayout B{};
+    B.R64 = round_up(s.R, 64);
+    B.T64 = round_up(c.T, 64);
+    B.Ep = round_up(c.E, 64);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    const size_t R = static_cast<size_t>(s.R), T = static_cast<size_t>(c.T);
+    const size_t d = c.d, de = c.d_e, ds = c.d_shared, E = c.E;
+    B.dgates = take(T * c.k * 4);
+    B.dz = take(R * d * 2);
+    B.xp = take(R * d * 2);
+    B.gu = take(R * 2 * de * 2);
+    B.h = take(R * de * 2);
+    B.dh = take(R * de * 2);
+    B.dgu = take(R * 2 * de * 2);
+    B.dxp = take(R * d * 2);
+    B.xpT = take(d * B.R64 * 2);
+    B.hT = take(de * B.R64 * 2);
+    B.dzT = take(d * B.R64 * 2);
+    B.dguT = take(2 * de * B.R64 * 2);
+    B.dW13i = take(E * d * 2 * de * 2);
+    B.dl32 = take(T * E * 4);
+    B.dl16 = take(T * B.Ep * 2);
+    B.dlT = take(B.Ep * B.T64 * 2);
+    B.xT = take(d * B.T64 * 2);
+    B.dxr = take(T * d * 2);
+    B.gus = take(T * 2 * ds * 2);
+    B.hs = take(T * ds * 2);
+    B.dhs = take(T * ds * 2);
+    B.dgus = take(T * 2 * ds * 2);
+    B.dxs = take(T * d * 2);
+    B.hsT = take(ds * B.T64 * 2);
+    B.doT = take(d * B.T64 * 2);
+    B.dgusT = take(2 * ds * B.T64 * 2);
+    B.dWs13i = take(d * 2 * ds * 2);
+    B.total = off;
+    return B;
+}
+
+// A plain bf16 GEMM on the CTA-pair kernel: out[r] = A[r] B[e]^T for the
+// blocks of the table (meta != null) or for `rows` dense rows.
+static cudaError_t pair_gemm(const moe_config_t& c, const void* A, int64_t rowsA, const void* B,
+                             int64_t rowsB_per_expert, int64_t K, int64_t N, void* out,
+                             int64_t out_rows, const int32_t* meta, const int32_t* nb,
+                             const int32_t* po, uint32_t* status, cudaStream_t st) {
+    const Sizes s = sizes_of(c);
+    const int bn = N % 256 == 0 ? 256 : 128;
+    GemmArgs a{};
+    a.status = status;
+    a.n_tiles = static_cast<int32_t>(N / bn);
+    a.k_blocks = static_cast<int32_t>((K + 63) / 64);
+    a.out = out;
+    a.ldo = N;
+    a.out_rows = out_rows;
+    int64_t tiles;
+    int64_t rowsB;
+    if (meta) {
+        a.block_metadata = meta;
+        a.num_blocks = nb;
+        a.nb_cap = static_cast<int32_t>(s.NB);
+        a.padded_offsets = po;
+        a.block_rows = c.pad_multiple;
+        a.n_experts = c.E;
+        a.b_rows_per_expert = static_cast<int32_t>(rowsB_per_expert);
+        tiles = s.NB * a.n_tiles;
+        rowsB = rowsB_per_expert * c.E;
+    } else {
+        a.dense_rows = static_cast<int32_t>(rowsA);
+        a.block_rows = 256;
+        tiles = ((rowsA + 255) / 256) * a.n_tiles;
+        rowsB = rowsB_per_expert;
+    }
+    return launch_grouped_gemm(kEpiGate, bn, A, rowsA, B, rowsB, K, a,
+                               static_cast<int>(tiles < (1 << 30) ? tiles : (1 << 30)), st);
+}
+
+static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
+                              const moe_weights_bwd_t* wb, const void* x, const void* dout,
+                              const void* fwd_ws, size_t fwd_ws_bytes, const moe_grads_t* g,
+                              void* bws, size_t bws_bytes, cudaStream_t st) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    const moe_config_t& c = *cfg;
+    if (!w || !wb || !g || !x || !dout || !fwd_ws)
+        return fail(MOE_ERR_INVALID_ARG, "null weights, gradients, x, dout or forward workspace");
+    if (!w->W13 || !wb->W13t || !wb->W2 || !g->dx || !g->dW1 || !g->dW3 || !g->dW2)
+        return fail(MOE_ERR_INVALID_ARG, "null routed expert weights or gradients");
+    const bool router = wb->WgP != nullptr;
+    if ((g->dWg || g->dbias) && !router)
+        return fail(MOE_ERR_INVALID_ARG, "router gradients asked for without WgP");
+    const bool shared = c.d_shared > 0;
+    if (shared && (!w->Ws13 || !wb->Ws13t || !wb->Ws2 || !g->dWs1 || !g->dWs3 || !g->dWs2))
+        return fail(MOE_ERR_INVALID_ARG, "d_shared > 0 but null shared weights or gradients");
+    // the backward reads only the routing state at the front of the forward
+    // workspace (everything before x_perm)
+    const moe_workspace_layout_t L = layout_of(c);
+    if (fwd_ws_bytes < L.x_perm)
+        return fail(MOE_ERR_WORKSPACE, "forward routing state of %zu bytes, %zu expected",
+                    fwd_ws_bytes, L.x_perm);
+    const BwdLayout B = bwd_layout_of(c);
+    if (!bws || bws_bytes < B.total)
+        return fail(MOE_ERR_WORKSPACE, "backward workspace of %zu bytes, %zu needed", bws_bytes,
+                    B.total);
+    if (c.T == 0) return MOE_OK;
+    const Sizes s = sizes_of(c);
+    const uint8_t* fw = static_cast<const uint8_t*>(fwd_ws);
+    uint8_t* bw = static_cast<uint8_t*>(bws);
+    auto F = [&](size_t o) { return const_cast<void*>(static_cast<const void*>(fw + o)); };
+    auto W = [&](size_t o) { return static_cast<void*>(bw + o); };
+    uint32_t* status = static_cast<uint32_t*>(F(L.status));
+    const int32_t* meta = static_cast<const int32_t*>(F(L.block_metadata));
+    const int32_t* nb = static_cast<const int32_t*>(F(L.num_blocks));
+    const int32_t* po = static_cast<const int32_t*>(F(L.padded_offsets));
+    const int32_t* perm_row = static_cast<const int32_t*>(F(L.perm_row));
+    const int32_t* row_src = static_cast<const int32_t*>(F(L.row_src));
+    const float* row_gate = static_cast<const float*>(F(L.row_gate));
+    float* dgates = g->dgates ? g->dgates : static_cast<float*>(W(B.dgates));
+    const int d = c.d, de = c.d_e, E = c.E;
+    cudaError_t e;
+#define MOE_BWD_CHECK(what)                  \
+    if (e != cudaSuccess) return cuda_fail(e, what)
+    // combine backward: the rows of dout in the padded order (dz_a = dout[t]);
+    // the permuted token rows again, from x and the sort indices
+    e = launch_permute(dout, perm_row, W(B.dz), c.T, d, c.k, st);
+    if (e == cudaSuccess) e = launch_permute(x, perm_row, W(B.xp), c.T, d, c.k, st);
+    MOE_BWD_CHECK("permutes of dout and x");
+    // routed experts, data gradients: dh = dz W2^T (before the routing
+    // weight), [g|u] and h recomputed, dgu and dgates, dx_perm
+    e = pair_gemm(c, W(B.dz), s.R, wb->W2, de, d, de, W(B.dh), s.R, meta, nb, po, status, st);
+    MOE_BWD_CHECK("dh = dz W2^T");
+    e = pair_gemm(c, W(B.xp), s.R, w->W13, 2 * de, d, 2 * de, W(B.gu), s.R, meta, nb, po, status,
+                  st);
+    MOE_BWD_CHECK("gate/up recomputation");
+    e = launch_swiglu_bwd(W(B.gu), W(B.dh), row_src, row_gate, W(B.h), W(B.dgu), dgates, s.R, de,
+                          st);
+    MOE_BWD_CHECK("SwiGLU backward");
+    e = pair_gemm(c, W(B.dgu), s.R, wb->W13t, d, 2 * de, d, W(B.dxp), s.R, meta, nb, po, status, st);
+    MOE_BWD_CHECK("dx_perm = dgu W13");
+    // routed experts, weight gradients over each expert's rows
+    e = launch_transpose(W(B.dz), row_src, row_gate, W(B.dzT), s.R, d, B.R64, st);
+    if (e == cudaSuccess) e = launch_transpose(W(B.h), row_src, nullptr, W(B.hT), s.R, de, B.R64, st);
+    if (e == cudaSuccess)
+        e = launch_transpose(W(B.dgu), row_src, nullptr, W(B.dguT), s.R, 2 * de, B.R64, st);
+    if (e == cudaSuccess)
+        e = launch_transpose(W(B.xp), row_src, nullptr, W(B.xpT), s.R, d, B.R64, st);
+    MOE_BWD_CHECK("transposes");
+    e = launch_wgrad(W(B.hT), de, W(B.dzT), d, B.R64, po, E, 0, g->dW2, status, st);
+    MOE_BWD_CHECK("dW2");
+    e = launch_wgrad(W(B.xpT), d, W(B.dguT), 2 * de, B.R64, po, E, 0, W(B.dW13i), status, st);
+    if (e == cudaSuccess)
+        e = launch_interleave(g->dW1, g->dW3, W(B.dW13i), static_cast<int64_t>(E) * d, de, 1, st);
+    MOE_BWD_CHECK("dW1, dW3");
+    if ((router && g->dWg) || shared) {
+        e = launch_transpose(x, nullptr, nullptr, W(B.xT), c.T, d, B.T64, st);
+        MOE_BWD_CHECK("x transpose");
+    }
+    const void* dxr = nullptr;
+    if (router) {
+        const int32_t* idx = static_cast<const int32_t*>(F(L.topk_idx));
+        const float* gates = static_cast<const float*>(F(L.topk_w));
+        e = launch_router_bwd(dgates, idx, gates, static_cast<float*>(W(B.dl32)), W(B.dl16), c.T, E,
+                              c.k, static_cast<int>(B.Ep), g->dbias, st);
+        MOE_BWD_CHECK("router backward");
+    }
+    if (router && g->dWg) {
+        e = launch_transpose(W(B.dl16), nullptr, nullptr, W(B.dlT), c.T, static_cast<int>(B.Ep), B.T64,
+                             st);
+        MOE_BWD_CHECK("dlogit transpose");
+        // dWg [d, E] = x^T dl on the 1-CTA kernel (fp32 rows of E)
+        GemmArgs a{};
+        a.dense_rows = d;
+        a.n_tiles = 1;
+        a.k_blocks = static_cast<int32_t>(B.T64 / 64);
+        a.k_per_split = a.k_blocks;
+        a.E = E;
+        a.partial = g->dWg;
+        a.status = status;
+        e = launch_grouped_gemm(kEpiPartial, router_bn(E), W(B.xT), d, W(B.dlT), B.Ep, B.T64, a,
+                                (d + 127) / 128, st);
+        MOE_BWD_CHECK("dWg");
+    }
+    if (router) {
+        e = pair_gemm(c, W(B.dl16), c.T, wb->WgP, d, B.Ep, d, W(B.dxr), c.T, nullptr, nullptr,
+                      nullptr, status, st);
+        MOE_BWD_CHECK("dx from the router");
+        dxr = W(B.dxr);
+    }
+    const void* dxs = nullptr;
+    if (shared) {
+        const int ds = c.d_shared;
+        e = pair_gemm(c, x, c.T, w->Ws13, 2 * ds, d, 2 * ds, W(B.gus), c.T, nullptr, nullptr, nullptr,
+                      status, st);
+        if (e == cudaSuccess)
+            e = pair_gemm(c, dout, c.T, wb->Ws2, ds, d, ds, W(B.dhs), c.T, nullptr, nullptr, nullptr,
+                          status, st);
+        if (e == cudaSuccess)
+            e = launch_swiglu_bwd(W(B.gus), W(B.dhs), nullptr, nullptr, W(B.hs), W(B.dgus), nullptr,
+                                  c.T, ds, st);
+        if (e == cudaSuccess)
+            e = pair_gemm(c, W(B.dgus), c.T, wb->Ws13t, d, 2 * ds, d, W(B.dxs), c.T, nullptr, nullptr,
+                          nullptr, status, st);
+        MOE_BWD_CHECK("shared expert data gradients");
+        e = launch_transpose(W(B.hs), nullptr, nullptr, W(B.hsT), c.T, ds, B.T64, st);
+        if (e == cudaSuccess) e = launch_transpose(dout, nullptr, nullptr, W(B.doT), c.T, d, B.T64, st);
+        if (e == cudaSuccess)
+            e = launch_transpose(W(B.dgus), nullptr, nullptr, W(B.dgusT), c.T, 2 * ds, B.T64, st);
+        if (e == cudaSuccess)
+            e = launch_wgrad(W(B.hsT), ds, W(B.doT), d, B.T64, nullptr, 1, c.T, g->dWs2, status, st);
+        if (e == cudaSuccess)
+            e = launch_wgrad(W(B.xT), d, W(B.dgusT), 2 * ds, B.T64, nullptr, 1, c.T, W(B.dWs13i), status,
+                             st);
+        if (e == cudaSuccess) e = launch_interleave(g->dWs1, g->dWs3, W(B.dWs13i), d, ds, 1, st);
+        MOE_BWD_CHECK("shared expert weight gradients");
+        dxs = W(B.dxs);
+    }
+    // dx: the k rows of each token (permute backward), then the router and
+    // shared-expert terms, in that order
+    if (!dxr) {
+        dxr = dxs;
+        dxs = nullptr;
+    }
+    e = launch_combine(W(B.dxp), perm_row, dxr, g->dx, c.T, d, c.k, st, dxs);
+    MOE_BWD_CHECK("dx");
+#undef MOE_BWD_CHECK
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -796,6 +1041,41 @@ moe_status_t moe_layer_fwd_fp8_prerouted(const moe_config_t* cfg, const moe_weig
                                          size_t ws_bytes, void* stream) {
     if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "null pre-routed indices");
     return layer_fp8(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_pack_experts_bwd(int32_t E, int32_t d, int32_t de, const void* W1, const void* W3,
+                                  void* W13t, void* stream) {
+    if (E <= 0 || d <= 0 || de <= 0 || !W1 || !W3 || !W13t)
+        return fail(MOE_ERR_INVALID_ARG, "bad backward expert pack args");
+    if (d % 128 || de % 128) return fail(MOE_ERR_UNSUPPORTED, "d and de must be multiples of 128");
+    cudaError_t e = launch_interleave(const_cast<void*>(W1), const_cast<void*>(W3), W13t,
+                                      static_cast<int64_t>(E) * d, de, 0,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack experts (backward)");
+}
+
+moe_status_t moe_pack_router_bwd(int32_t d, int32_t E, const void* Wg, void* WgP, void* stream) {
+    if (d <= 0 || E <= 0 || !Wg || !WgP) return fail(MOE_ERR_INVALID_ARG, "bad router pack args");
+    const size_t ep = static_cast<size_t>((E + 63) / 64 * 64);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemset2DAsync(WgP, ep * 2, 0, ep * 2, d, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(WgP, ep * 2, Wg, static_cast<size_t>(E) * 2, static_cast<size_t>(E) * 2, d,
+                              cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack router (backward)");
+}
+
+size_t moe_backward_workspace_size(const moe_config_t* cfg) {
+    if (check_cfg(cfg, false) != MOE_OK) return 0;
+    return bwd_layout_of(*cfg).total;
+}
+
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
+                           const moe_weights_bwd_t* wb, const void* x, const void* dout,
+                           const void* fwd_ws, size_t fwd_ws_bytes, const moe_grads_t* grads,
+                           void* bws, size_t bws_bytes, void* stream) {
+    return layer_bwd(cfg, w, wb, x, dout, fwd_ws, fwd_ws_bytes, grads, bws, bws_bytes,
                      static_cast<cudaStream_t>(stream));
 }
 

@@ -212,7 +212,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 template <int K>
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ perm_row,
-              const uint4* __restrict__ shared_out, uint4* __restrict__ out, int T, int nvec) {
+              const uint4* __restrict__ shared_out, const uint4* __restrict__ extra2,
+              uint4* __restrict__ out, int T, int nvec) {
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,6 +251,10 @@ __global__ void __launch_bounds__(kPCWarps * 32)
         if (shared_out) {
             add_bf16x8(a0, sh0);
             add_bf16x8(a1, sh1);
+        }
+        if (extra2) {
+            add_bf16x8(a0, ld_dep(extra2 + (int64_t)t * nvec + v0));
+            if (has1) add_bf16x8(a1, ld_dep(extra2 + (int64_t)t * nvec + v1));
         }
         __stcs(out + (int64_t)t * nvec + v0, pack_bf16x8(a0));
         if (has1) __stcs(out + (int64_t)t * nvec + v1, pack_bf16x8(a1));
@@ -306,16 +311,17 @@ cudaError_t launch_split_rows_e4m3(const void* h, const int32_t* block_metadata,
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* shared_out,
-                           void* out, int T, int d, int k, cudaStream_t stream) {
+                           void* out, int T, int d, int k, cudaStream_t stream, const void* extra2) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
     const uint4* y4 = static_cast<const uint4*>(y);
     const uint4* s4 = static_cast<const uint4*>(shared_out);
+    const uint4* x4 = static_cast<const uint4*>(extra2);
     uint4* o4 = static_cast<uint4*>(out);
     switch (k) {
 #define MOE_COMBINE_K(KK) \
     case KK: return launch_pdl(k_combine<KK>, dim3(grid), dim3(kPCWarps * 32), 0, stream, y4, perm_row, \
-                               s4, o4, T, nvec);
+                               s4, x4, o4, T, nvec);
         MOE_COMBINE_K(1) MOE_COMBINE_K(2) MOE_COMBINE_K(3) MOE_COMBINE_K(4)
         MOE_COMBINE_K(5) MOE_COMBINE_K(6) MOE_COMBINE_K(7) MOE_COMBINE_K(8)
 #undef MOE_COMBINE_K

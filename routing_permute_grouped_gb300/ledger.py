@@ -107,3 +107,21 @@ def padding_waste(counts, P: int) -> float:
     """(sum of padded sizes - assignments) / assignments."""
     A = sum(counts)
     return (padded_rows(counts, P) - A) / A if A else 0.0
+
+
+def layer_backward_useful_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0,
+                                E: int = 0) -> int:
+    """Useful FLOP of the layer backward: every forward GEMM C = A B has a data
+    gradient dA = dC B^T and a weight gradient dB = A^T dC of its own cost, so
+    twice the forward's routed + shared FLOP, plus twice the router GEMM when
+    the router is differentiated (E > 0).  The gate/up recomputation is not
+    useful work and is not counted."""
+    return 2 * layer_useful_flops(T, k, d, d_e, d_s) + (2 * router_flops(T, d, E) if E else 0)
+
+
+def layer_backward_gemm_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0, E: int = 0) -> int:
+    """FLOP the backward's GEMMs execute on unpadded rows: the useful FLOP plus
+    the recomputed gate/up products (2 * d * 2 d_e per routed row, the same
+    for the shared expert)."""
+    recompute = T * k * 2 * d * 2 * d_e + (T * 2 * d * 2 * d_s if d_s else 0)
+    return layer_backward_useful_flops(T, k, d, d_e, d_s, E) + recompute

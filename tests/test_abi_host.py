@@ -153,3 +153,39 @@ def test_fp8_entry_points_check_arguments_before_launch(lib):
     args15[13] = None  # status
     args15[14] = None  # stream
     assert lib.moe_grouped_gemm_swiglu_fp8(ctypes.byref(cfg0), *args15) == 0
+
+
+def test_backward_entry_points_check_arguments_before_launch(lib):
+    cfg = _cfg(d_shared=256)
+    fake = 0x1000
+    fp = ctypes.c_void_p(fake)
+    need_f = moe.moe_workspace_size(cfg)
+    need_b = moe.moe_backward_workspace_size(cfg)
+    assert need_b > 0 and moe.moe_backward_workspace_size(_cfg(d=500)) == 0
+    w = moe.MoeWeights(Wg_t=fake, bias=None, W13=fake, W2=fake, Ws13=fake, Ws2=fake)
+    wb = moe.MoeWeightsBwd(W13t=fake, W2=fake, WgP=fake, Ws13t=fake, Ws2=fake)
+    full = {n: fake for n in moe._GRAD_FIELDS}
+    g = moe.MoeGrads(**full)
+
+    def call(c=cfg, w=w, wb=wb, g=g, fwd_bytes=need_f, bws_bytes=need_b, x=fp):
+        return lib.moe_layer_bwd(ctypes.byref(c), ctypes.byref(w), ctypes.byref(wb), x, fp, fp,
+                                 fwd_bytes, ctypes.byref(g), fp, bws_bytes, None)
+
+    assert call(bws_bytes=need_b - 1) == 3
+    # the backward needs only the routing state at the front of the forward workspace
+    assert call(fwd_bytes=moe.moe_workspace_layout(cfg)["x_perm"] - 1) == 3
+    assert call(x=None) == 1
+    assert call(g=moe.MoeGrads(**dict(full, dW2=None))) == 1
+    assert call(g=moe.MoeGrads(**dict(full, dWs3=None))) == 1
+    assert "shared" in lib.moe_last_error().decode()
+    assert call(wb=moe.MoeWeightsBwd(W13t=fake, W2=fake, WgP=None, Ws13t=fake, Ws2=fake)) == 1
+    assert "WgP" in lib.moe_last_error().decode()
+    assert call(c=_cfg(d_shared=256, d_e=200)) == 2
+    # T = 0: nothing to do, nothing enqueued
+    c0 = _cfg(T=0, d_shared=256)
+    assert call(c=c0, fwd_bytes=moe.moe_workspace_size(c0),
+                bws_bytes=moe.moe_backward_workspace_size(c0)) == 0
+    # packs: shape rules
+    assert lib.moe_pack_experts_bwd(2, 200, 128, fp, fp, fp, None) == 2
+    assert lib.moe_pack_experts_bwd(2, 256, 128, fp, None, fp, None) == 1
+    assert lib.moe_pack_router_bwd(256, 0, fp, fp, None) == 1

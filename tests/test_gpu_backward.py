@@ -1,0 +1,185 @@
+"""GPU parity of the layer backward (moe_layer_bwd) against the oracle's fp64
+layer backward, on the same seeded inputs and the same routing.
+
+The backward runs bf16 GEMMs with fp32 accumulation and rounds each GEMM
+output to bf16 once, so a gradient passes through at most five bf16
+roundings (dz scaled by the routing weight, dh, the recomputed gate/up
+values, dgu, the output itself), each a relative error of at most 2^-9 per
+element.  Random rounding errors add in quadrature: the bound below,
+a relative Frobenius error of 1e-2 and a max error of 5e-2 * max|ref|, is
+about three times that sum.  The fp32 outputs (dgates, dWg, dbias) follow
+bf16 operands and are held to the same bound.
+
+Shapes: routed with a logit bias and a shared expert (several row tiles per
+expert, ragged tails), group-limited routing with padding 64 and a model
+width that is not a multiple of 256, a pre-routed batch with an empty expert
+and repeated experts within a token, many experts (E = 100, most of them
+empty), a decode-sized batch whose forward runs on the small-M kernel, and
+a single token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import routing_permute_grouped_gb300 as moe
+from routing_permute_grouped_gb300 import build as moe_build
+from routing_permute_grouped_gb300 import synth
+from routing_permute_grouped_gb300.synth import MoeShape
+from tests.helpers import enforce_margin, oracle_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 1e-2
+MAX_REL = 5e-2
+
+SHAPES = {
+    "routed_shared": MoeShape("routed_shared", T=777, d=1024, d_e=384, E=8, k=4, bias_std=0.5,
+                              d_shared=256, seed=201),
+    "groups_p64_d384": MoeShape("groups_p64_d384", T=400, d=384, d_e=256, E=16, k=4, n_groups=4,
+                                topk_groups=2, pad=64, seed=202),
+    "prerouted_empty": MoeShape("prerouted_empty", T=150, d=256, d_e=256, E=4, k=8,
+                                prerouted=(500, 0, 600, 100), seed=203),
+    "e100": MoeShape("e100", T=300, d=384, d_e=128, E=100, k=3, bias_std=0.3, seed=204),
+    "decode_small_m": MoeShape("decode_small_m", T=37, d=512, d_e=256, E=64, k=8, n_groups=8,
+                               topk_groups=4, d_shared=128, seed=205),
+    "one_token": MoeShape("one_token", T=1, d=256, d_e=128, E=8, k=2, d_shared=128, seed=206),
+}
+
+_cache = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU backward tests need a CUDA device")
+    moe_build.build()
+    moe.load()
+
+
+def _dout(shape):
+    g = torch.Generator().manual_seed(shape.seed + 1000)
+    return torch.randn((shape.T, shape.d), generator=g).to(torch.bfloat16)
+
+
+def prepared(name):
+    """(shape, CPU inputs, dout bf16, oracle forward, oracle backward)."""
+    if name not in _cache:
+        shape = SHAPES[name]
+        inp = synth.make_inputs(shape)
+        enforce_margin(inp, shape)
+        oi = oracle_inputs(inp)
+        fwd = oracle.layer_forward(oi, shape)
+        dout = _dout(shape)
+        bwd = oracle.layer_backward(oi, shape, fwd, dout.double().numpy())
+        _cache[name] = (shape, inp, dout, fwd, bwd)
+    return _cache[name]
+
+
+def cuda(t):
+    return None if t is None else t.cuda().contiguous()
+
+
+def f64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def assert_close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, what
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / (nref if nref > 0 else 1.0)
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    bound = MAX_REL * (np.abs(ref).max() if ref.size else 0.0)
+    assert rel <= REL_FRO, f"{what}: relative Frobenius error {rel:.3e}"
+    assert mx <= bound + 1e-30, f"{what}: max error {mx:.3e} > {bound:.3e}"
+
+
+def run(shape, inp, dout):
+    cfg = moe.config_of(shape)
+    layer = moe.MoeLayer(cfg, cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]),
+                         Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")),
+                         Ws1=cuda(inp.get("Ws1")), Ws3=cuda(inp.get("Ws3")),
+                         Ws2=cuda(inp.get("Ws2")))
+    x = cuda(inp["x"])
+    if shape.prerouted:
+        layer(x, topk_idx=cuda(inp["topk_idx"]), topk_w=cuda(inp["topk_w"]))
+    else:
+        layer(x)
+    g = layer.backward(x, cuda(dout), prerouted=bool(shape.prerouted))
+    torch.cuda.synchronize()
+    return layer, x, g
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_backward_matches_oracle(name):
+    shape, inp, dout, fwd, ref = prepared(name)
+    layer, x, g = run(shape, inp, dout)
+    assert layer.device_status() == 0
+    for key in ("dx", "dgates", "dW1", "dW3", "dW2"):
+        assert_close(f64(g[key]), ref[key], key)
+    if not shape.prerouted:
+        assert_close(f64(g["dWg"]), ref["dWg"], "dWg")
+        assert_close(f64(g["dbias"]), ref["dbias"], "dbias")
+    else:
+        assert "dWg" not in g
+    if shape.d_shared:
+        for key in ("dWs1", "dWs3", "dWs2"):
+            assert_close(f64(g[key]), ref[key], key)
+    # experts that received no rows have exactly zero weight gradients
+    empty = np.flatnonzero(fwd["counts"] == 0)
+    for key in ("dW1", "dW3", "dW2"):
+        assert not g[key][torch.as_tensor(empty)].any() if empty.size else True
+
+
+def test_backward_needs_only_the_routing_state():
+    """The backward reads the forward workspace's routing state (everything
+    before x_perm) and nothing else: overwriting the rest changes nothing, the
+    state itself is left as it was, and a second run is bit-identical."""
+    shape, inp, dout, _, _ = prepared("routed_shared")
+    layer, x, g1 = run(shape, inp, dout)
+    front = layer.layout["x_perm"]
+    before = layer.ws[256:front].clone()
+    layer.ws[front:].fill_(0xFF)
+    g2 = layer.backward(x, cuda(dout))
+    torch.cuda.synchronize()
+    assert torch.equal(before, layer.ws[256:front])
+    for key in g1:
+        assert torch.equal(g1[key], g2[key]), key
+    assert layer.device_status() == 0
+
+
+def test_frozen_router_still_differentiates_through_it():
+    """dWg/dbias left NULL: dx keeps the router's term."""
+    shape, inp, dout, _, ref = prepared("e100")
+    layer, x, g = run(shape, inp, dout)
+    grads = {k: torch.empty_like(v) for k, v in g.items() if k not in ("dWg", "dbias")}
+    layer.backward(x, cuda(dout), grads=grads)
+    torch.cuda.synchronize()
+    assert_close(f64(grads["dx"]), ref["dx"], "dx, frozen router")
+    assert torch.equal(grads["dx"], g["dx"])
+
+
+def test_backward_captures_into_a_cuda_graph():
+    shape, inp, dout, _, ref = prepared("groups_p64_d384")
+    layer, x, g = run(shape, inp, dout)
+    dz = cuda(dout)
+    grads = {k: torch.zeros_like(v) for k, v in g.items()}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.backward(x, dz, grads=grads, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.backward(x, dz, grads=grads)
+    for v in grads.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for key in g:
+        assert torch.equal(grads[key], g[key]), key
+    assert layer.device_status() == 0
