@@ -592,7 +592,7 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: b
 
 def backward_launches(shape, router_grads: bool = True) -> int:
     """Kernels of one moe_layer_bwd call."""
-    n = 1 + 4 + 4 + 2 + 1  # permute of dout; dh, gu, SwiGLU bwd, dx_perm; 4 transposes; dW2, dW13; interleave
+    n = 2 + 4 + 4 + 2  # permutes of dout and x; dh, gu, SwiGLU bwd, dx_perm; 4 transposes; dW2, dW13
     routed = not shape.prerouted
     if (routed and router_grads) or shape.d_shared:
         n += 1  # x transpose
@@ -600,7 +600,7 @@ def backward_launches(shape, router_grads: bool = True) -> int:
         n += 2 + 1  # router backward + dbias column sums; dx from the router
         n += 2 if router_grads else 0  # dlogit transpose, dWg
     if shape.d_shared:
-        n += 4 + 3 + 2 + 1  # gate/up, dh, SwiGLU bwd, dx; 3 transposes; 2 wgrads; interleave
+        n += 4 + 3 + 2  # gate/up, dh, SwiGLU bwd, dx; 3 transposes; 2 wgrads
     return n + 1  # dx combine
 
 

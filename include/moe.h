@@ -58,6 +58,8 @@ typedef enum {
 /* Device error bits reported by moe_get_device_status(). */
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* an expert id outside [0, E) was skipped */
 #define MOE_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel gave up */
+#define MOE_DEVERR_SEGMENT 0x4u      /* backward: a segment offset outside the padded rows
+                                      * was skipped */
 
 typedef struct {
     int32_t T;            /* tokens */
@@ -106,7 +108,7 @@ typedef struct {
 typedef struct {
     const void *W13t;   /* bf16 [E, d, 2*d_e]: row i = (W1[e][i], W3[e][i]) interleaved */
     const void *W2;     /* bf16 [E, d_e, d]: the unpacked W2 */
-    const void *WgP;    /* bf16 [d, Ep], Ep = E rounded up to 64, columns >= E zero;
+    const void *WgP;    /* bf16 [d, Ep], Ep = E rounded up to 128, columns >= E zero;
                          * NULL for a pre-routed forward (no router to
                          * differentiate through) */
     const void *Ws13t;  /* bf16 [d, 2*d_shared] (d_shared > 0), else NULL */
@@ -481,7 +483,7 @@ moe_status_t moe_pack_experts_bwd(int32_t E, int32_t d, int32_t de, const void *
                                   const void *W3, void *W13t, void *stream);
 
 /* WgP bf16 [d, Ep] from the caller's router weight Wg bf16 [d, E]; Ep = E
- * rounded up to 64, the extra columns zero. */
+ * rounded up to 128, the extra columns zero. */
 moe_status_t moe_pack_router_bwd(int32_t d, int32_t E, const void *Wg, void *WgP, void *stream);
 
 /* Bytes of the moe_layer_bwd workspace; 0 if cfg is invalid. */

@@ -362,7 +362,7 @@ def moe_pack_experts_bwd(W1, W3, W13t, stream=None) -> None:
 
 
 def moe_pack_router_bwd(Wg, WgP, stream=None) -> None:
-    """WgP [d, Ep] (Ep = E rounded up to 64, zero past E) from Wg [d, E]."""
+    """WgP [d, Ep] (Ep = E rounded up to 128, zero past E) from Wg [d, E]."""
     d, E = Wg.shape
     _check(load().moe_pack_router_bwd(d, E, _ptr(Wg), _ptr(WgP), _stream(stream)))
 
@@ -514,7 +514,7 @@ class MoeLayer:
         moe_pack_experts_bwd(u["W1"], u["W3"], self.W13t, stream)
         self.WgP = None
         if u["Wg"] is not None:
-            self.WgP = torch.empty((d, (E + 63) // 64 * 64), dtype=torch.bfloat16, device=dev)
+            self.WgP = torch.empty((d, (E + 127) // 128 * 128), dtype=torch.bfloat16, device=dev)
             moe_pack_router_bwd(u["Wg"], self.WgP, stream)
         self.Ws13t = None
         if self.cfg.d_shared:

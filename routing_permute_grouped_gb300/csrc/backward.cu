@@ -7,15 +7,13 @@
 //                   experts of a token, 0 for the others (softmax over the
 //                   chosen logits; the choice itself is a constant)
 //   k_colsum        the logit-bias gradient: column sums in token order
-//   k_swiglu_bwd    h = silu(g) u recomputed from the recomputed g, u;
-//                   dg = p dh * u * silu'(g), du = p dh * silu(g) in the
-//                   gate/up interleaved column order of the packed weights;
-//                   the routing-weight gradient dp_a = <dh_a, h_a>
-//   k_transpose     [rows, C] -> [C, ld] with an optional row scale, pad rows
-//                   (and columns past rows) zero: the K-major operands of the
-//                   weight gradients
-//   k_interleave    row-wise (de)interleave of gate and up blocks of 128
-//                   columns ([.., w] x 2 <-> [.., 2w])
+//   k_swiglu_bwd    h = silu(g) u recomputed from the recomputed g, u, stored
+//                   as p h; dg = p dh * u * silu'(g), du = p dh * silu(g) in
+//                   the gate/up interleaved column order of the packed
+//                   weights; the routing-weight gradient dp_a = <dh_a, h_a>;
+//                   pad rows of the weight-gradient operands zeroed
+//   k_interleave    row-wise interleave of gate and up blocks of 128 columns
+//                   ([.., w] x 2 -> [.., 2w]): the backward weight layout
 // Reads of data written by earlier kernels of the stream use ld_dep.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -72,36 +70,64 @@ __global__ void k_router_bwd(const float* __restrict__ dgates, const int32_t* __
     for (int e = 0; e < ld16; ++e) row16[e] = __float2bfloat16_rn(e < E ? row[e] : 0.0f);
 }
 
-// One thread per column, rows summed in order.
-__global__ void k_colsum(const float* __restrict__ m, float* __restrict__ out, int rows, int cols) {
+// One block of 256 threads per column: thread i sums rows i, i + 256, ... in
+// order, then a fixed tree over the threads (deterministic).
+__global__ void __launch_bounds__(256)
+    k_colsum(const float* __restrict__ m, float* __restrict__ out, int rows, int cols) {
     pdl_trigger();
     pdl_wait();
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= cols) return;
+    __shared__ float part[8];
+    const int c = blockIdx.x;
     float s = 0.0f;
-    for (int r = 0; r < rows; ++r) s += ld_dep(m + (int64_t)r * cols + c);
-    out[c] = s;
+    for (int r = threadIdx.x; r < rows; r += 256) s += ld_dep(m + (int64_t)r * cols + c);
+    s = warp_sum(s);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int i = 0; i < 8; ++i) t += part[i];
+        out[c] = t;
+    }
 }
 
-// One warp per row of h.  gu and dgu are [rows, 2w] in the interleaved
-// order (block j of 256: 128 gate columns, 128 up columns); dh is the row's
-// gradient before its routing weight p.  Recomputes h = silu(g) u (bf16,
-// written to h when not null), writes dgu = f'(g, u) * (p dh) and, when
-// dgates is not null, dgates[a] = <dh, h> for the assignment a the row
-// holds.  Pad rows (row_src < 0) are skipped.
+// One warp per padded row r < *used_rows (all rows when used_rows is null).
+// gu and dgu are [rows, 2w] in the interleaved order (block j of 256: 128
+// gate columns, 128 up columns); dh is the row's gradient before its routing
+// weight p.  For a row that holds assignment a: recomputes h = silu(g) u and
+// writes hp = p h (bf16, the weight-gradient operand of the down projection),
+// dgu = f'(g, u) * (p dh) and, when dgates is not null, dgates[a] = <dh, h>
+// with h rounded to bf16.  A pad row (row_src < 0) is zeroed in hp, dgu and
+// the two extra row-major buffers z0, z1 (width zw; may be null), so that the
+// weight-gradient GEMMs can reduce over whole segments.
 __global__ void __launch_bounds__(kWarps * 32)
     k_swiglu_bwd(const __nv_bfloat16* __restrict__ gu, const __nv_bfloat16* __restrict__ dh,
                  const int32_t* __restrict__ row_src, const float* __restrict__ row_gate,
-                 __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ dgu,
-                 float* __restrict__ dgates, int64_t rows, int w) {
+                 const int32_t* __restrict__ used_rows, __nv_bfloat16* __restrict__ hp,
+                 __nv_bfloat16* __restrict__ dgu, float* __restrict__ dgates,
+                 __nv_bfloat16* __restrict__ z0, __nv_bfloat16* __restrict__ z1, int zw,
+                 int64_t rows, int w) {
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    if (used_rows) {
+        const int64_t u = ld_dep(used_rows);
+        rows = u < rows ? u : rows;
+    }
+    const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int64_t r = blockIdx.x * static_cast<int64_t>(kWarps) + (threadIdx.x >> 5); r < rows;
          r += nwarps) {
         const int a = row_src ? ld_dep(row_src + r) : static_cast<int>(r);
-        if (a < 0) continue;
+        if (a < 0) {
+            for (int c = lane * 8; c < w; c += 256) *reinterpret_cast<uint4*>(hp + r * w + c) = zero;
+            for (int c = lane * 8; c < 2 * w; c += 256)
+                *reinterpret_cast<uint4*>(dgu + r * 2 * w + c) = zero;
+            for (int c = lane * 8; c < zw; c += 256) {
+                if (z0) *reinterpret_cast<uint4*>(z0 + r * zw + c) = zero;
+                if (z1) *reinterpret_cast<uint4*>(z1 + r * zw + c) = zero;
+            }
+            continue;
+        }
         const float p = row_gate ? ld_dep(row_gate + r) : 1.0f;
         float dot = 0.0f;
         for (int c = lane * 8; c < w; c += 256) {
@@ -118,13 +144,15 @@ __global__ void __launch_bounds__(kWarps * 32)
                 dg[q] = pd * u[q] * s * (1.0f + g[q] * (1.0f - s));
                 du[q] = pd * g[q] * s;
             }
-            const uint4 hb = pack8(hv);
-            if (h) *reinterpret_cast<uint4*>(h + r * w + c) = hb;
             if (dgates) {
-                unpack8(hb, hv);  // the bf16 h that the weight gradient sees
+                float hb[8];
+                unpack8(pack8(hv), hb);  // h as the forward stored it: bf16
 #pragma unroll
-                for (int q = 0; q < 8; ++q) dot += d[q] * hv[q];
+                for (int q = 0; q < 8; ++q) dot += d[q] * hb[q];
             }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hv[q] *= p;
+            *reinterpret_cast<uint4*>(hp + r * w + c) = pack8(hv);
             *reinterpret_cast<uint4*>(dgu + r * 2 * w + gcol) = pack8(dg);
             *reinterpret_cast<uint4*>(dgu + r * 2 * w + gcol + 128) = pack8(du);
         }
@@ -132,35 +160,6 @@ __global__ void __launch_bounds__(kWarps * 32)
             dot = warp_sum(dot);
             if (lane == 0) dgates[a] = dot;
         }
-    }
-}
-
-// dst[c][r] = scale[r] * src[r][c] (scale 1 when null; 0 for a row with
-// row_src[r] < 0 and for r >= rows); 32 x 32 tiles through shared memory,
-// grid (ceil(C/32), ceil(ld/32)).
-__global__ void k_transpose(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ row_src,
-                            const float* __restrict__ scale, __nv_bfloat16* __restrict__ dst,
-                            int64_t rows, int C, int64_t ld) {
-    pdl_trigger();
-    pdl_wait();
-    __shared__ __nv_bfloat16 tile[32][33];
-    const int c0 = blockIdx.x * 32;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int64_t r = r0 + i;
-        const int c = c0 + threadIdx.x;
-        __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-        if (r < rows && c < C && !(row_src && ld_dep(row_src + r) < 0)) {
-            v = ld_dep(src + r * C + c);
-            if (scale) v = __float2bfloat16_rn(__bfloat162float(v) * ld_dep(scale + r));
-        }
-        tile[i][threadIdx.x] = v;
-    }
-    __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int c = c0 + i;
-        const int64_t r = r0 + threadIdx.x;
-        if (c < C && r < ld) dst[static_cast<int64_t>(c) * ld + r] = tile[threadIdx.x][i];
     }
 }
 
@@ -206,24 +205,19 @@ cudaError_t launch_router_bwd(const float* dgates, const int32_t* idx, const flo
     cudaError_t e = launch_pdl(k_router_bwd, dim3((T + 127) / 128), dim3(128), 0, st, dgates, idx, gates,
                                dl, static_cast<__nv_bfloat16*>(dl16), T, E, k, ld16);
     if (e != cudaSuccess || !dbias) return e;
-    return launch_pdl(k_colsum, dim3((E + 127) / 128), dim3(128), 0, st,
-                      static_cast<const float*>(dl), dbias, T, E);
+    return launch_pdl(k_colsum, dim3(E), dim3(256), 0, st, static_cast<const float*>(dl), dbias, T,
+                      E);
 }
 
 cudaError_t launch_swiglu_bwd(const void* gu, const void* dh, const int32_t* row_src,
-                              const float* row_gate, void* h, void* dgu, float* dgates, int64_t rows,
-                              int w, cudaStream_t st) {
+                              const float* row_gate, const int32_t* used_rows, void* hp, void* dgu,
+                              float* dgates, void* z0, void* z1, int zw, int64_t rows, int w,
+                              cudaStream_t st) {
     return launch_pdl(k_swiglu_bwd, dim3(grid_for(rows, kWarps)), dim3(kWarps * 32), 0, st,
                       static_cast<const __nv_bfloat16*>(gu), static_cast<const __nv_bfloat16*>(dh),
-                      row_src, row_gate, static_cast<__nv_bfloat16*>(h),
-                      static_cast<__nv_bfloat16*>(dgu), dgates, rows, w);
-}
-
-cudaError_t launch_transpose(const void* src, const int32_t* row_src, const float* scale, void* dst,
-                             int64_t rows, int C, int64_t ld, cudaStream_t st) {
-    dim3 grid((C + 31) / 32, static_cast<unsigned>((ld + 31) / 32));
-    return launch_pdl(k_transpose, grid, dim3(32, 8), 0, st, static_cast<const __nv_bfloat16*>(src),
-                      row_src, scale, static_cast<__nv_bfloat16*>(dst), rows, C, ld);
+                      row_src, row_gate, used_rows, static_cast<__nv_bfloat16*>(hp),
+                      static_cast<__nv_bfloat16*>(dgu), dgates, static_cast<__nv_bfloat16*>(z0),
+                      static_cast<__nv_bfloat16*>(z1), zw, rows, w);
 }
 
 cudaError_t launch_interleave(void* a, void* b, void* out2, int64_t n, int w, int mode,

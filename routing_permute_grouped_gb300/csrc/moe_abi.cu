@@ -524,10 +524,10 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
 
 struct BwdLayout {
     size_t total;
-    size_t dgates, dz, xp, gu, h, dh, dgu, dxp, xpT, hT, dzT, dguT, dW13i;  // routed experts
-    size_t dl32, dl16, dlT, xT, dxr;                                   // router
-    size_t gus, hs, dhs, dgus, dxs, hsT, doT, dgusT, dWs13i;           // shared expert
-    int64_t R64, T64, Ep;
+    size_t dgates, dz, xp, gu, hp, dh, dgu, dxp;                     // routed experts
+    size_t dl32, dl16, dxr;                                            // router
+    size_t gus, hs, dhs, dgus, dxs;                                  // shared expert
+    int64_t Ep;
 };
 
 static inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -535,9 +535,7 @@ static inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * 
 static BwdLayout bwd_layout_of(const moe_config_t& c) {
     const Sizes s = sizes_of(c);
     BwdLayout B{};
-    B.R64 = round_up(s.R, 64);
-    B.T64 = round_up(c.T, 64);
-    B.Ep = round_up(c.E, 64);
+    B.Ep = round_up(c.E, 128);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -550,29 +548,18 @@ static BwdLayout bwd_layout_of(const moe_config_t& c) {
     B.dz = take(R * d * 2);
     B.xp = take(R * d * 2);
     B.gu = take(R * 2 * de * 2);
-    B.h = take(R * de * 2);
+    B.hp = take(R * de * 2);
     B.dh = take(R * de * 2);
     B.dgu = take(R * 2 * de * 2);
     B.dxp = take(R * d * 2);
-    B.xpT = take(d * B.R64 * 2);
-    B.hT = take(de * B.R64 * 2);
-    B.dzT = take(d * B.R64 * 2);
-    B.dguT = take(2 * de * B.R64 * 2);
-    B.dW13i = take(E * d * 2 * de * 2);
     B.dl32 = take(T * E * 4);
     B.dl16 = take(T * B.Ep * 2);
-    B.dlT = take(B.Ep * B.T64 * 2);
-    B.xT = take(d * B.T64 * 2);
     B.dxr = take(T * d * 2);
     B.gus = take(T * 2 * ds * 2);
     B.hs = take(T * ds * 2);
     B.dhs = take(T * ds * 2);
     B.dgus = take(T * 2 * ds * 2);
     B.dxs = take(T * d * 2);
-    B.hsT = take(ds * B.T64 * 2);
-    B.doT = take(d * B.T64 * 2);
-    B.dgusT = take(2 * ds * B.T64 * 2);
-    B.dWs13i = take(d * 2 * ds * 2);
     B.total = off;
     return B;
 }
@@ -671,29 +658,17 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     e = pair_gemm(c, W(B.xp), s.R, w->W13, 2 * de, d, 2 * de, W(B.gu), s.R, meta, nb, po, status,
                   st);
     MOE_BWD_CHECK("gate/up recomputation");
-    e = launch_swiglu_bwd(W(B.gu), W(B.dh), row_src, row_gate, W(B.h), W(B.dgu), dgates, s.R, de,
-                          st);
+    e = launch_swiglu_bwd(W(B.gu), W(B.dh), row_src, row_gate, po + E, W(B.hp), W(B.dgu), dgates,
+                          W(B.dz), W(B.xp), d, s.R, de, st);
     MOE_BWD_CHECK("SwiGLU backward");
     e = pair_gemm(c, W(B.dgu), s.R, wb->W13t, d, 2 * de, d, W(B.dxp), s.R, meta, nb, po, status, st);
     MOE_BWD_CHECK("dx_perm = dgu W13");
-    // routed experts, weight gradients over each expert's rows
-    e = launch_transpose(W(B.dz), row_src, row_gate, W(B.dzT), s.R, d, B.R64, st);
-    if (e == cudaSuccess) e = launch_transpose(W(B.h), row_src, nullptr, W(B.hT), s.R, de, B.R64, st);
-    if (e == cudaSuccess)
-        e = launch_transpose(W(B.dgu), row_src, nullptr, W(B.dguT), s.R, 2 * de, B.R64, st);
-    if (e == cudaSuccess)
-        e = launch_transpose(W(B.xp), row_src, nullptr, W(B.xpT), s.R, d, B.R64, st);
-    MOE_BWD_CHECK("transposes");
-    e = launch_wgrad(W(B.hT), de, W(B.dzT), d, B.R64, po, E, 0, g->dW2, status, st);
+    // routed experts, weight gradients over each expert's rows (pad rows
+    // zeroed above): dW2 = (p h)^T dz, [dW1 | dW3] = x_perm^T dgu
+    e = launch_wgrad(W(B.hp), de, W(B.dz), d, s.R, po, E, 0, g->dW2, nullptr, status, st);
     MOE_BWD_CHECK("dW2");
-    e = launch_wgrad(W(B.xpT), d, W(B.dguT), 2 * de, B.R64, po, E, 0, W(B.dW13i), status, st);
-    if (e == cudaSuccess)
-        e = launch_interleave(g->dW1, g->dW3, W(B.dW13i), static_cast<int64_t>(E) * d, de, 1, st);
+    e = launch_wgrad(W(B.xp), d, W(B.dgu), 2 * de, s.R, po, E, 0, g->dW1, g->dW3, status, st);
     MOE_BWD_CHECK("dW1, dW3");
-    if ((router && g->dWg) || shared) {
-        e = launch_transpose(x, nullptr, nullptr, W(B.xT), c.T, d, B.T64, st);
-        MOE_BWD_CHECK("x transpose");
-    }
     const void* dxr = nullptr;
     if (router) {
         const int32_t* idx = static_cast<const int32_t*>(F(L.topk_idx));
@@ -703,20 +678,8 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
         MOE_BWD_CHECK("router backward");
     }
     if (router && g->dWg) {
-        e = launch_transpose(W(B.dl16), nullptr, nullptr, W(B.dlT), c.T, static_cast<int>(B.Ep), B.T64,
-                             st);
-        MOE_BWD_CHECK("dlogit transpose");
-        // dWg [d, E] = x^T dl on the 1-CTA kernel (fp32 rows of E)
-        GemmArgs a{};
-        a.dense_rows = d;
-        a.n_tiles = 1;
-        a.k_blocks = static_cast<int32_t>(B.T64 / 64);
-        a.k_per_split = a.k_blocks;
-        a.E = E;
-        a.partial = g->dWg;
-        a.status = status;
-        e = launch_grouped_gemm(kEpiPartial, router_bn(E), W(B.xT), d, W(B.dlT), B.Ep, B.T64, a,
-                                (d + 127) / 128, st);
+        // dWg [d, E] = x^T dlogits (fp32), on the weight-gradient kernel
+        e = launch_wgrad(x, d, W(B.dl16), B.Ep, c.T, nullptr, 1, c.T, g->dWg, nullptr, status, st, E);
         MOE_BWD_CHECK("dWg");
     }
     if (router) {
@@ -734,22 +697,17 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
             e = pair_gemm(c, dout, c.T, wb->Ws2, ds, d, ds, W(B.dhs), c.T, nullptr, nullptr, nullptr,
                           status, st);
         if (e == cudaSuccess)
-            e = launch_swiglu_bwd(W(B.gus), W(B.dhs), nullptr, nullptr, W(B.hs), W(B.dgus), nullptr,
-                                  c.T, ds, st);
+            e = launch_swiglu_bwd(W(B.gus), W(B.dhs), nullptr, nullptr, nullptr, W(B.hs), W(B.dgus),
+                                  nullptr, nullptr, nullptr, 0, c.T, ds, st);
         if (e == cudaSuccess)
             e = pair_gemm(c, W(B.dgus), c.T, wb->Ws13t, d, 2 * ds, d, W(B.dxs), c.T, nullptr, nullptr,
                           nullptr, status, st);
         MOE_BWD_CHECK("shared expert data gradients");
-        e = launch_transpose(W(B.hs), nullptr, nullptr, W(B.hsT), c.T, ds, B.T64, st);
-        if (e == cudaSuccess) e = launch_transpose(dout, nullptr, nullptr, W(B.doT), c.T, d, B.T64, st);
         if (e == cudaSuccess)
-            e = launch_transpose(W(B.dgus), nullptr, nullptr, W(B.dgusT), c.T, 2 * ds, B.T64, st);
+            e = launch_wgrad(W(B.hs), ds, dout, d, c.T, nullptr, 1, c.T, g->dWs2, nullptr, status, st);
         if (e == cudaSuccess)
-            e = launch_wgrad(W(B.hsT), ds, W(B.doT), d, B.T64, nullptr, 1, c.T, g->dWs2, status, st);
-        if (e == cudaSuccess)
-            e = launch_wgrad(W(B.xT), d, W(B.dgusT), 2 * ds, B.T64, nullptr, 1, c.T, W(B.dWs13i), status,
+            e = launch_wgrad(x, d, W(B.dgus), 2 * ds, c.T, nullptr, 1, c.T, g->dWs1, g->dWs3, status,
                              st);
-        if (e == cudaSuccess) e = launch_interleave(g->dWs1, g->dWs3, W(B.dWs13i), d, ds, 1, st);
         MOE_BWD_CHECK("shared expert weight gradients");
         dxs = W(B.dxs);
     }
@@ -1057,7 +1015,7 @@ moe_status_t moe_pack_experts_bwd(int32_t E, int32_t d, int32_t de, const void* 
 
 moe_status_t moe_pack_router_bwd(int32_t d, int32_t E, const void* Wg, void* WgP, void* stream) {
     if (d <= 0 || E <= 0 || !Wg || !WgP) return fail(MOE_ERR_INVALID_ARG, "bad router pack args");
-    const size_t ep = static_cast<size_t>((E + 63) / 64 * 64);
+    const size_t ep = static_cast<size_t>((E + 127) / 128 * 128);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemset2DAsync(WgP, ep * 2, 0, ep * 2, d, st);
     if (e == cudaSuccess)

@@ -1,21 +1,27 @@
 // wgrad_gemm.cu -- weight gradients of the grouped expert GEMMs.
 //
-//   C[e][m][n] = sum over the rows r of expert e's segment of A[m][r] * B[n][r]
+//   C[e][m][n] = sum over the rows r of expert e's segment of A[r][m] * B[r][n]
 //
-// A [M, Rtot] and B [N, Rtot] are K-major copies of two activation matrices
-// transposed so that the padded rows run along K (pad rows hold zeros), and
-// expert e owns rows [seg[e], seg[e+1]) of the padded layout.  For the down
-// projection A = h^T, B = dz^T give dW2[e] = h_e^T dz_e; for gate/up A = x^T,
-// B = dgu^T give the gradient of the packed gate/up weights.  ("Dropless and
-// grouped GEMM", sec. 5: a tile reads exactly one expert's rows; here the
-// reduction, not the output, runs over them.)
+// A [rows, M] and B [rows, N] are the row-major activations of the padded
+// layout as the backward produces them (pad rows hold zeros), and expert e
+// owns rows [seg[e], seg[e+1]).  For the down projection A = p h, B = dz give
+// dW2[e] = (p h)_e^T dz_e; for gate/up A = x_perm, B = dgu give the gradient
+// of the packed gate/up weights.  ("Dropless and grouped GEMM", sec. 5: a
+// tile reads exactly one expert's rows; here the reduction, not the output,
+// runs over them.)
 //
-// Tiles are (expert, 256-row block of M, BN-column block of N) on CTA pairs
-// (cta_group::2, M = 256 split over the pair, B split along N), the K loop
-// over the expert's rows in 64-row steps.  An expert without rows gets a zero
-// gradient.  Warp roles as in the forward kernels: warp 0 TMA producer,
-// warp 1 TMEM allocation and MMA issue (even CTA), warps 2..5 epilogue
-// (bf16 stores of the fp32 accumulators).  Every wait is bounded.
+// The reduction runs along the rows, so both operands are MN-major: TMA
+// copies boxes of 64 rows x 64 columns (128-byte swizzle, one 128-byte row
+// per k) and the MMA reads them through MN-major shared-memory descriptors,
+// no transposed copy.  Tiles are (expert, 256 rows of M over the CTA pair
+// (cta_group::2), BN columns split over the pair), the K loop over the
+// expert's segment in 64-row steps.  An expert without rows gets a zero
+// gradient.  For the packed gate/up operand the epilogue splits every
+// 256-column tile (128 gate, 128 up columns) straight into the two gradients;
+// the router's gradient (N = the expert count rounded up to 128) is written
+// as fp32 for its first E columns.  Warp roles as in the forward kernels: warp 0 TMA producer, warp 1 TMEM
+// allocation and MMA issue (even CTA), warps 2..5 epilogue (bf16 stores of
+// the fp32 accumulators).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -30,9 +36,29 @@ namespace {
 constexpr int kBM = 128;  // rows of A per CTA
 constexpr int kBK = 64;
 constexpr uint32_t kTimeout = 0x2u;
+// bits [15] and [16] of the instruction descriptor: A and B are MN-major
+constexpr uint32_t kIdescMnMajorAB = (1u << 15) | (1u << 16);
+// output staging: 4 epilogue warps x 2 buffers x (32 rows x 128 bytes)
+constexpr int kOutStage = 4 * 2 * 4096;
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
+// rows of 128 bytes (64 bf16 along M or N) per k, 8-row groups 1024 bytes
+// apart (stride byte offset), 64-column chunks `chunk_bytes` apart (leading
+// byte offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t chunk_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((chunk_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+constexpr uint32_t kBadSegment = 0x4u;
 
 struct WTile {
     int e, mt, nt, kb0, kb1;
+    bool bad;  // the segment lies outside [0, rows): skipped as empty and flagged
 };
 
 __device__ __forceinline__ WTile wg_tile(const WgradArgs& a, int t) {
@@ -43,27 +69,31 @@ __device__ __forceinline__ WTile wg_tile(const WgradArgs& a, int t) {
     w.e = r / a.m_tiles;
     const int s0 = a.seg ? ld_dep(a.seg + w.e) : 0;
     const int s1 = a.seg ? ld_dep(a.seg + w.e + 1) : a.dense_rows;
-    w.kb0 = s0 / kBK;
-    w.kb1 = s1 > s0 ? (s1 + kBK - 1) / kBK : w.kb0;
+    w.bad = s0 < 0 || s1 < s0 || s1 > a.rows;
+    w.kb0 = w.bad ? 0 : s0 / kBK;
+    w.kb1 = (!w.bad && s1 > s0) ? (s1 + kBK - 1) / kBK : w.kb0;
     return w;
 }
 
 template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_wgrad_pair(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                 const __grid_constant__ CUtensorMap tO, const __grid_constant__ CUtensorMap tO2,
                  const WgradArgs args) {
     constexpr int BH = BN / 2;
+    constexpr int BOX = 64 * kBK * 2;  // one TMA box: 64 columns x 64 rows, 8 KB
     constexpr int A_BYTES = kBM * kBK * 2;
     constexpr int B_BYTES = BH * kBK * 2;
     constexpr int STAGE = A_BYTES + B_BYTES;
-    constexpr int S = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
+    constexpr int S = (160 * 1024) / STAGE > 8 ? 8 : (160 * 1024) / STAGE;
     constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * B_BYTES);
+    uint8_t* sOut = sB + S * B_BYTES;  // 4 epilogue warps x 2 x 4 KB staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kOutStage);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* tfull = bars + 2 * S;
@@ -92,8 +122,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         tma_prefetch_desc(&tA);
         tma_prefetch_desc(&tB);
     }
-    if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    // tensor memory is taken only once the kernels before this one have
+    // finished (and released theirs)
     pdl_wait();
+    if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the peer's barriers are initialised before any remote use
@@ -113,8 +145,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t armed = 0, armed_par = 0;
             for (int t = cluster; t < total && !timed_out; t += nclusters) {
                 const WTile w = wg_tile(args, t);
-                const int arow = w.mt * 256 + kBM * static_cast<int>(rank);
-                const int brow = w.nt * BN + BH * static_cast<int>(rank);
+                const int acol = w.mt * 256 + kBM * static_cast<int>(rank);
+                const int bcol = w.nt * BN + BH * static_cast<int>(rank);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
                         timed_out = true;
@@ -123,8 +155,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t full_leader = mapa_shared(smem_u32(full + s), 0);
                     armed &= ~(1u << s);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE);
-                    tma_load_2d_pair(sA + s * A_BYTES, &tA, kb * kBK, arow, full_leader);
-                    tma_load_2d_pair(sB + s * B_BYTES, &tB, kb * kBK, brow, full_leader);
+#pragma unroll
+                    for (int i = 0; i < kBM / 64; ++i)
+                        tma_load_2d_pair(sA + s * A_BYTES + i * BOX, &tA, acol + 64 * i, kb * kBK,
+                                         full_leader);
+#pragma unroll
+                    for (int i = 0; i < BH / 64; ++i)
+                        tma_load_2d_pair(sB + s * B_BYTES + i * BOX, &tB, bcol + 64 * i, kb * kBK,
+                                         full_leader);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -145,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ----------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, BN);
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, BN) | kIdescMnMajorAB;
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
@@ -168,10 +206,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
                     const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+                    // K = 16 rows per MMA: two 8-row groups of 1024 bytes
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
-                                      idesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
+                        mma_bf16_pair(d_tmem, sdesc_sw128_mn(a_addr + kk * 2048, BOX),
+                                      sdesc_sw128_mn(b_addr + kk * 2048, BOX), idesc,
+                                      (kb != w.kb0 || kk != 0) ? 1u : 0u);
                     issued = true;
                     mma_commit_pair(empty + s, 0x3);
                     if (++s == S) {
@@ -193,50 +233,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        // Each warp owns 32 rows of M.  bf16 outputs leave through TMA bulk
+        // stores of 32 x 64 boxes staged in shared memory (128-byte swizzle,
+        // two 4 KB buffers per warp); the fp32 router gradient (a few
+        // columns) is stored per thread.
         const int q = warp & 3;
         int acc = 0;
         uint32_t aph = 0;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+        int buf = 0;
+        uint8_t* stage = sOut + (q & 3) * 2 * 4096;
+        float* outf = static_cast<float*>(args.out);
+        const bool split = args.out2 != nullptr;
         for (int t = cluster; t < total; t += nclusters) {
             const WTile w = wg_tile(args, t);
-            const int m = w.mt * 256 + kBM * static_cast<int>(rank) + q * 32 + lane;
-            __nv_bfloat16* dst = out + (static_cast<int64_t>(w.e) * args.M + m) * args.N +
-                                 static_cast<int64_t>(w.nt) * BN;
-            if (w.kb1 <= w.kb0) {  // an expert without rows: zero gradient
-                if (m < args.M)
-                    for (int c = 0; c < BN; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-                continue;
+            const int mb = w.mt * 256 + kBM * static_cast<int>(rank) + q * 32;  // warp's first row
+            const int m = mb + lane;
+            const int col0 = w.nt * BN;
+            const int64_t orow = static_cast<int64_t>(w.e) * args.M + mb;  // row in the output map
+            const bool empty_tile = w.kb1 <= w.kb0;
+            if (empty_tile && w.bad && q == 2 && lane == 0 && args.status)
+                atomicOr(args.status, kBadSegment);
+            uint32_t taddr = 0;
+            if (!empty_tile) {
+                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
+                if (!ok) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             }
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
-            if (!ok) {
-                timed_out = true;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * BN);
+            if (args.f32) {
+                const int64_t row_off = (static_cast<int64_t>(w.e) * args.M + m) * args.n_valid;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr + c, v);
-                tmem_ld_wait();
-                if (m < args.M) {
-                    uint32_t p[16];
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    if (!empty_tile) {
+                        tmem_ld32(taddr + c, v);
+                        tmem_ld_wait();
+                    }
+                    if (m < args.M) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + c + i < args.n_valid)
+                                outf[row_off + col0 + c + i] = empty_tile ? 0.0f : __uint_as_float(v[i]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 64) {
+                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+                    __syncwarp();
+                    uint8_t* sb = stage + buf * 4096 + lane * 128;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        if (!empty_tile) {
+                            tmem_ld32(taddr + c + half * 32, v);
+                            tmem_ld_wait();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = 0u;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int chunk = half * 4 + j;  // 16-byte chunk of the 128-byte row
+                            const int i = 8 * j;
+                            *reinterpret_cast<uint4*>(sb + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                pack_bf16x2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])),
+                                pack_bf16x2(__uint_as_float(v[i + 4]), __uint_as_float(v[i + 5])),
+                                pack_bf16x2(__uint_as_float(v[i + 6]), __uint_as_float(v[i + 7])));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && mb < args.M) {
+                        // split: tile columns [0, 128) are gate, [128, 256) up
+                        const bool up = split && c >= 128;
+                        const int x = split ? w.nt * 128 + (c & 127) : col0 + c;
+                        tma_store_2d(up ? &tO2 : &tO, stage + buf * 4096, x, static_cast<int32_t>(orow));
+                        bulk_commit();
+                    }
+                    buf ^= 1;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + acc), 0));
-            acc ^= 1;
-            if (acc == 0) aph ^= 1u;
+            if (!empty_tile) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + acc), 0));
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
         }
+        if (lane == 0) bulk_wait_all();  // the stores have left shared memory and landed
         if (timed_out) *abort_flag = 1;
     }
 
@@ -251,11 +341,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 }
 
 template <int BN>
-cudaError_t launch_wg(const CUtensorMap& tA, const CUtensorMap& tB, const WgradArgs& args,
-                      cudaStream_t stream) {
+cudaError_t launch_wg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tO,
+                      const CUtensorMap& tO2, const WgradArgs& args, cudaStream_t stream) {
     constexpr int STAGE = kBM * kBK * 2 + (BN / 2) * kBK * 2;
-    constexpr int S = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
-    constexpr int SMEM = 1024 + S * STAGE + 512;
+    constexpr int S = (160 * 1024) / STAGE > 8 ? 8 : (160 * 1024) / STAGE;
+    constexpr int SMEM = 1024 + S * STAGE + kOutStage + 512;
     static_assert(SMEM <= 232448, "shared memory budget");
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -271,31 +361,53 @@ cudaError_t launch_wg(const CUtensorMap& tA, const CUtensorMap& tB, const WgradA
     int clusters = num_sms() / 2;
     if (total < clusters) clusters = total;
     if (clusters <= 0) return cudaSuccess;
-    return launch_pdl(k_wgrad_pair<BN>, dim3(2 * clusters), dim3(192), SMEM, stream, tA, tB, args);
+    return launch_pdl(k_wgrad_pair<BN>, dim3(2 * clusters), dim3(192), SMEM, stream, tA, tB, tO, tO2,
+                      args);
 }
 
 }  // namespace
 
-cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int64_t ldk,
-                         const int32_t* seg, int n_experts, int dense_rows, void* out,
-                         uint32_t* status, cudaStream_t stream) {
-    if (N % 128 || M <= 0 || ldk % 8) return cudaErrorInvalidValue;
+cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int64_t rows,
+                         const int32_t* seg, int n_experts, int dense_rows, void* out, void* out2,
+                         uint32_t* status, cudaStream_t stream, int f32_cols) {
+    if (N % 128 || M % 64 || M <= 0 || rows <= 0 || f32_cols < 0 || f32_cols > N)
+        return cudaErrorInvalidValue;
     const int bn = N % 256 == 0 ? 256 : 128;
+    if (out2 && (bn != 256 || f32_cols)) return cudaErrorInvalidValue;  // split: 256-column tiles
     CUtensorMap tA, tB;
-    if (!make_tensor_map_2d(&tA, A, M, ldk, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kBK, kBM, 128) ||
-        !make_tensor_map_2d(&tB, B, N, ldk, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kBK, bn / 2, 128))
+    if (!make_tensor_map_2d(&tA, A, rows, M, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, kBK, 128) ||
+        !make_tensor_map_2d(&tB, B, rows, N, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, kBK, 128))
         return cudaErrorInvalidValue;
     WgradArgs a{};
     a.seg = seg;
     a.dense_rows = dense_rows;
+    a.rows = static_cast<int32_t>(rows);
     a.n_experts = n_experts;
     a.M = static_cast<int32_t>(M);
     a.N = static_cast<int32_t>(N);
     a.m_tiles = static_cast<int32_t>((M + 255) / 256);
     a.n_tiles = static_cast<int32_t>(N / bn);
     a.out = out;
+    a.out2 = out2;
+    a.f32 = f32_cols > 0;
+    a.n_valid = f32_cols > 0 ? f32_cols : static_cast<int32_t>(N);
     a.status = status;
-    return bn == 256 ? launch_wg<256>(tA, tB, a, stream) : launch_wg<128>(tA, tB, a, stream);
+    // bf16 outputs as [n_experts * M, ldo] maps stored in 64 x 32 boxes (the
+    // fp32 output is stored per thread and needs none)
+    CUtensorMap tO, tO2;
+    const int64_t ldo = out2 ? N / 2 : N;
+    const int64_t orows = static_cast<int64_t>(n_experts) * M;
+    if (f32_cols) {
+        tO = tA;
+        tO2 = tA;
+    } else if (!make_tensor_map_2d(&tO, out, orows, ldo, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, 32,
+                                   128) ||
+               !make_tensor_map_2d(&tO2, out2 ? out2 : out, orows, ldo, 2,
+                                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, 32, 128)) {
+        return cudaErrorInvalidValue;
+    }
+    return bn == 256 ? launch_wg<256>(tA, tB, tO, tO2, a, stream)
+                     : launch_wg<128>(tA, tB, tO, tO2, a, stream);
 }
 
 }  // namespace moe
