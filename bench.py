@@ -716,15 +716,27 @@ def run_train(args, shape, rank, world, local):
 
     pk = peaks()
     E_r = 0 if pre else shape.E
+    counts_h = layer.buffer("counts", torch.int32, (shape.E,)).cpu().tolist()
+    active = sum(1 for c in counts_h if c > 0)
     bwd_flops = ledger.layer_backward_gemm_flops(T, k, d, de, ds, E_r)
+    bwd_bytes = ledger.layer_backward_bytes_alg(T, k, d, de, ds, shape.E, active, not pre)
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    achieved = bwd_flops / (bwd_ms / 1e3) / 1e12
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
-            "frac": achieved / peak_t, "peak_source": pk["source"] + " sustained bf16",
-            "kernel": "layer backward (moe_layer_bwd: all its kernels; GEMM FLOP incl. the "
-                      "gate/up recomputation)",
-            "timing": "split pass: CUDA events around moe_layer_bwd",
-            "algorithmic": {"flop": bwd_flops}, "traffic": None}
+    bwd_s = bwd_ms / 1e3
+    # tensor-bound when the backward's FLOP per byte exceeds the machine
+    # balance (measured bf16 FLOP/s over measured HBM bytes/s), else HBM-bound
+    if bwd_flops / bwd_bytes < peak_t * 1e12 / (pk["hbm_gbs"] * 1e9):
+        roof = {"bound": "hbm", "achieved": bwd_bytes / bwd_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "peak_source": pk["source"] + " copy bandwidth"}
+    else:
+        roof = {"bound": "tensor", "achieved": bwd_flops / bwd_s / 1e12, "peak": peak_t,
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " sustained bf16"}
+    roof.update({"frac": roof["achieved"] / roof["peak"],
+                 "kernel": "layer backward (moe_layer_bwd: all its kernels; GEMM FLOP incl. the "
+                           "gate/up recomputation; bytes: weights read, weight gradients "
+                           "written, token rows)",
+                 "timing": "split pass: CUDA events around moe_layer_bwd",
+                 "algorithmic": {"flop": bwd_flops, "bytes": bwd_bytes, "active_experts": active},
+                 "traffic": None})
     skinny = T * k <= 32 * shape.E
     line = {
         "metric": METRIC_TRAIN, "value": value, "unit": "TFLOP/s", "n_gpus": world,

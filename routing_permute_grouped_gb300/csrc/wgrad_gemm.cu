@@ -19,9 +19,10 @@
 // gradient.  For the packed gate/up operand the epilogue splits every
 // 256-column tile (128 gate, 128 up columns) straight into the two gradients;
 // the router's gradient (N = the expert count rounded up to 128) is written
-// as fp32 for its first E columns.  Warp roles as in the forward kernels: warp 0 TMA producer, warp 1 TMEM
-// allocation and MMA issue (even CTA), warps 2..5 epilogue (bf16 stores of
-// the fp32 accumulators).  Every wait is bounded.
+// as fp32 for its first E columns.  Warp roles: warp 0 TMA producer, warp 1
+// TMEM allocation and MMA issue (even CTA), warps 2..9 epilogue (two per
+// TMEM lane quarter, each half of the columns; bf16 stores of the fp32
+// accumulators).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,8 +39,12 @@ constexpr int kBK = 64;
 constexpr uint32_t kTimeout = 0x2u;
 // bits [15] and [16] of the instruction descriptor: A and B are MN-major
 constexpr uint32_t kIdescMnMajorAB = (1u << 15) | (1u << 16);
-// output staging: 4 epilogue warps x 2 buffers x (32 rows x 128 bytes)
-constexpr int kOutStage = 4 * 2 * 4096;
+// warps: TMA producer, MMA issuer, then two epilogue warps per TMEM lane
+// quarter (each takes half of the tile's columns)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+// output staging: epilogue warps x 2 buffers x (32 rows x 128 bytes)
+constexpr int kOutStage = kEpiWarps * 2 * 4096;
 
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
 // rows of 128 bytes (64 bf16 along M or N) per k, 8-row groups 1024 bytes
@@ -76,7 +81,7 @@ __device__ __forceinline__ WTile wg_tile(const WgradArgs& a, int t) {
 }
 
 template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_wgrad_pair(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                  const __grid_constant__ CUtensorMap tO, const __grid_constant__ CUtensorMap tO2,
                  const WgradArgs args) {
@@ -92,7 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * A_BYTES;
-    uint8_t* sOut = sB + S * B_BYTES;  // 4 epilogue warps x 2 x 4 KB staging
+    uint8_t* sOut = sB + S * B_BYTES;  // epilogue warps x 2 x 4 KB staging
     uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kOutStage);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
@@ -114,7 +119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull + i, 1);
-            mbar_init(tempty + i, 8);  // one arrival per epilogue warp of both CTAs
+            mbar_init(tempty + i, 2 * kEpiWarps);  // one arrival per epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -233,15 +238,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
-        // Each warp owns 32 rows of M.  bf16 outputs leave through TMA bulk
-        // stores of 32 x 64 boxes staged in shared memory (128-byte swizzle,
-        // two 4 KB buffers per warp); the fp32 router gradient (a few
-        // columns) is stored per thread.
+        // Each warp owns 32 rows of M (its TMEM lane quarter) and half of the
+        // tile's columns.  bf16 outputs leave through TMA bulk stores of
+        // 32 x 64 boxes staged in shared memory (128-byte swizzle, two 4 KB
+        // buffers per warp); the fp32 router gradient (a few columns) is
+        // stored per thread.
         const int q = warp & 3;
+        const int ew = warp - 2;            // epilogue warp 0 .. kEpiWarps - 1
+        const int c_lo = (ew >> 2) * (BN / 2), c_hi = c_lo + BN / 2;
         int acc = 0;
         uint32_t aph = 0;
         int buf = 0;
-        uint8_t* stage = sOut + (q & 3) * 2 * 4096;
+        uint8_t* stage = sOut + ew * 2 * 4096;
         float* outf = static_cast<float*>(args.out);
         const bool split = args.out2 != nullptr;
         for (int t = cluster; t < total; t += nclusters) {
@@ -251,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const int col0 = w.nt * BN;
             const int64_t orow = static_cast<int64_t>(w.e) * args.M + mb;  // row in the output map
             const bool empty_tile = w.kb1 <= w.kb0;
-            if (empty_tile && w.bad && q == 2 && lane == 0 && args.status)
+            if (empty_tile && w.bad && ew == 0 && lane == 0 && args.status)
                 atomicOr(args.status, kBadSegment);
             uint32_t taddr = 0;
             if (!empty_tile) {
@@ -266,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             if (args.f32) {
                 const int64_t row_off = (static_cast<int64_t>(w.e) * args.M + m) * args.n_valid;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = c_lo; c < c_hi; c += 32) {
                     uint32_t v[32];
                     if (!empty_tile) {
                         tmem_ld32(taddr + c, v);
@@ -281,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 64) {
+                for (int c = c_lo; c < c_hi; c += 64) {
                     if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
                     __syncwarp();
                     uint8_t* sb = stage + buf * 4096 + lane * 128;
@@ -361,7 +369,7 @@ cudaError_t launch_wg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtens
     int clusters = num_sms() / 2;
     if (total < clusters) clusters = total;
     if (clusters <= 0) return cudaSuccess;
-    return launch_pdl(k_wgrad_pair<BN>, dim3(2 * clusters), dim3(192), SMEM, stream, tA, tB, tO, tO2,
+    return launch_pdl(k_wgrad_pair<BN>, dim3(2 * clusters), dim3(kThreads), SMEM, stream, tA, tB, tO, tO2,
                       args);
 }
 
