@@ -440,9 +440,8 @@ def run_ours(args, shape, rank, world, local):
         layer_step()
         step()
     torch.cuda.synchronize()
-    # timed region: K whole-layer forwards (moe_layer_fwd, which runs the
-    # shared expert on a side stream beside the routing chain), bracketed by
-    # CUDA events on the calling stream
+    # timed region: K whole-layer forwards (moe_layer_fwd: every stage on the
+    # calling stream), bracketed by CUDA events on that stream
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
