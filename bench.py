@@ -672,44 +672,33 @@ def run_train(args, shape, rank, world, local):
     useful = train_useful_flops(shape)
     value = reduce_sum(useful * args.steps, world) / (ms_max / 1e3) / 1e12
 
-    # e2e: token rows and the output gradient from pinned host memory, dx
-    # back to the host, every step (weight gradients stay on the device)
+    # e2e through the public API with host buffers: every step copies its
+    # token rows and output gradient from pinned host memory and dx back
+    # (weight gradients stay on the device); HostPipeline.submit_train
+    # overlaps the copies of neighbouring steps with the compute
     x_host = x.cpu().pin_memory()
     dout_host = dout.cpu().pin_memory()
-    dx_host = torch.empty_like(x_host).pin_memory()
-    xd, dd = torch.empty_like(x), torch.empty_like(dout)
+    dx_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
     h2d = x_host.numel() * 2 + dout_host.numel() * 2
     kw_host = {}
     if pre:
-        kw_host = dict(topk_idx=torch.empty_like(inp["topk_idx"]),
-                       topk_w=torch.empty_like(inp["topk_w"]))
-        idx_host = inp["topk_idx"].cpu().pin_memory()
-        w_host = inp["topk_w"].cpu().pin_memory()
-        h2d += idx_host.numel() * 4 + w_host.numel() * 4
-    d2h = dx_host.numel() * 2
-
-    def e2e_step():
-        xd.copy_(x_host, non_blocking=True)
-        dd.copy_(dout_host, non_blocking=True)
-        if pre:
-            kw_host["topk_idx"].copy_(idx_host, non_blocking=True)
-            kw_host["topk_w"].copy_(w_host, non_blocking=True)
-        layer(xd, out, **kw_host)
-        layer.backward(xd, dd, grads=grads, prerouted=pre)
-        dx_host.copy_(grads["dx"], non_blocking=True)
-
+        kw_host = dict(topk_idx=inp["topk_idx"].cpu().pin_memory(),
+                       topk_w=inp["topk_w"].cpu().pin_memory())
+        h2d += kw_host["topk_idx"].numel() * 4 + kw_host["topk_w"].numel() * 4
+    d2h = x_host.numel() * 2
     e2e_steps = max(1, min(args.steps, 50))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
+    pipe = moe.HostPipeline(layer)
+    for i in range(3):
+        pipe.submit_train(x_host, dout_host, dx_host[i % 2], grads, **kw_host)
+    pipe.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record()
-    torch.cuda.synchronize()
+    e0.record(pipe.s_in)
+    for i in range(e2e_steps):
+        pipe.submit_train(x_host, dout_host, dx_host[i % 2], grads, **kw_host)
+    e1.record(pipe.s_out)
+    pipe.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
 

@@ -24,7 +24,8 @@
  *    that only the device can see (an expert id outside [0, E), a wait that
  *    timed out) set a word in the workspace, readable with
  *    moe_get_device_status().
- *  - A call with T == 0 enqueues nothing and returns MOE_OK.
+ *  - A call with T == 0 enqueues nothing and returns MOE_OK; its token-row
+ *    buffers (x, out, dout, dx, the given routing) may be NULL.
  *  - Requirements on shapes: d % 128 == 0, d_e % 128 == 0,
  *    d_shared % 128 == 0 (or 0), 1 <= E <= 256, 1 <= k <= 8, pad_multiple 64
  *    or 128, group-limited routing needs E % n_groups == 0,
@@ -514,8 +515,8 @@ size_t moe_backward_workspace_size(const moe_config_t *cfg);
  * Accumulation is fp32 inside each GEMM; GEMM outputs, dW1/dW3/dW2 and the
  * shared weight gradients are rounded to bf16 once, dWg and dbias stay fp32.
  *
- * T = 0 returns MOE_OK without enqueuing anything (the gradient arrays are
- * not touched).
+ * T = 0 returns MOE_OK after the shape checks, without reading any pointer
+ * or enqueuing anything (the gradient arrays are not touched).
  *
  * Returns MOE_ERR_INVALID_ARG on NULL buffers a gradient needs,
  * MOE_ERR_WORKSPACE when bws_bytes < moe_backward_workspace_size(cfg) or

@@ -634,6 +634,49 @@ class HostPipeline:
             out_host.copy_(self.o_dev[k], non_blocking=True)
             self.ev_out[k].record(self.s_out)
 
+    def submit_train(self, x_host: torch.Tensor, dout_host: torch.Tensor, dx_host: torch.Tensor,
+                     grads: dict, topk_idx=None, topk_w=None):
+        """Forward and backward of one batch: x and the output gradient dout
+        copied in from pinned host memory, dx copied back; the weight
+        gradients (and dgates) land in the device tensors of ``grads``,
+        overwritten by every batch.  Copies overlap the compute of the
+        neighbouring batches as in ``submit``."""
+        k = self.i % self.depth
+        self.i += 1
+        if not hasattr(self, "dout_dev"):
+            self.dout_dev = [torch.empty_like(x) for x in self.x_dev]
+            self.dx_dev = [torch.empty_like(x) for x in self.x_dev]
+        if self.used[k]:
+            self.s_in.wait_event(self.ev_run[k])    # x and dout buffers no longer read
+            self.s_run.wait_event(self.ev_out[k])   # dx buffer copied back
+        self.used[k] = True
+        prerouted = topk_idx is not None
+        with torch.cuda.stream(self.s_in):
+            self.x_dev[k].copy_(x_host, non_blocking=True)
+            self.dout_dev[k].copy_(dout_host, non_blocking=True)
+            if prerouted and not topk_idx.is_cuda:
+                if not hasattr(self, "idx_dev"):
+                    self.idx_dev = [torch.empty_like(topk_idx, device=self.x_dev[0].device)
+                                    for _ in range(self.depth)]
+                    self.w_dev = [torch.empty_like(topk_w, device=self.x_dev[0].device)
+                                  for _ in range(self.depth)]
+                self.idx_dev[k].copy_(topk_idx, non_blocking=True)
+                self.w_dev[k].copy_(topk_w, non_blocking=True)
+                topk_idx, topk_w = self.idx_dev[k], self.w_dev[k]
+            self.ev_in[k].record(self.s_in)
+        self.s_run.wait_event(self.ev_in[k])
+        self.layer.forward(self.x_dev[k], self.o_dev[k], topk_idx=topk_idx, topk_w=topk_w,
+                           stream=self.s_run)
+        g = dict(grads)
+        g["dx"] = self.dx_dev[k]
+        self.layer.backward(self.x_dev[k], self.dout_dev[k], grads=g, prerouted=prerouted,
+                            stream=self.s_run)
+        self.ev_run[k].record(self.s_run)
+        self.s_out.wait_event(self.ev_run[k])
+        with torch.cuda.stream(self.s_out):
+            dx_host.copy_(self.dx_dev[k], non_blocking=True)
+            self.ev_out[k].record(self.s_out)
+
     def synchronize(self):
         for s in (self.s_in, self.s_run, self.s_out):
             s.synchronize()

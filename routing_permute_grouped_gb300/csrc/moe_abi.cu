@@ -434,9 +434,10 @@ static moe_status_t check_layer_args(const moe_config_t* cfg, bool routed, const
                                      size_t ws_bytes, bool fp8 = false) {
     moe_status_t r = check_cfg(cfg, routed);
     if (r != MOE_OK) return r;
-    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "null x or out");
+    // an empty batch has no token rows: x, out and the gates may be null
+    if (cfg->T > 0 && (!x || !out)) return fail(MOE_ERR_INVALID_ARG, "null x or out");
     if (routed && !Wg_t) return fail(MOE_ERR_INVALID_ARG, "null router weight");
-    if (!routed && !pre_w) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
+    if (!routed && !pre_w && cfg->T > 0) return fail(MOE_ERR_INVALID_ARG, "null pre-routed gates");
     const size_t need = layout_of(*cfg, fp8).total;
     if (!ws || ws_bytes < need)
         return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
@@ -608,6 +609,7 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
     const moe_config_t& c = *cfg;
+    if (c.T == 0) return MOE_OK;  // nothing to differentiate; no pointer is read
     if (!w || !wb || !g || !x || !dout || !fwd_ws)
         return fail(MOE_ERR_INVALID_ARG, "null weights, gradients, x, dout or forward workspace");
     if (!w->W13 || !wb->W13t || !wb->W2 || !g->dx || !g->dW1 || !g->dW3 || !g->dW2)
@@ -628,7 +630,6 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     if (!bws || bws_bytes < B.total)
         return fail(MOE_ERR_WORKSPACE, "backward workspace of %zu bytes, %zu needed", bws_bytes,
                     B.total);
-    if (c.T == 0) return MOE_OK;
     const Sizes s = sizes_of(c);
     const uint8_t* fw = static_cast<const uint8_t*>(fwd_ws);
     uint8_t* bw = static_cast<uint8_t*>(bws);

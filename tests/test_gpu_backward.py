@@ -19,8 +19,9 @@ Shapes: routed with a logit bias and a shared expert (several row tiles per
 expert, ragged tails), group-limited routing with padding 64 and a model
 width that is not a multiple of 256, a pre-routed batch with an empty expert
 and repeated experts within a token, many experts (E = 100, most of them
-empty), a decode-sized batch whose forward runs on the small-M kernel, and
-a single token.
+empty), a decode-sized batch whose forward runs on the small-M kernel, a
+single token, a single expert (k = 1: every gate is 1 and the router gets no
+gradient) and k = E (every expert chosen by every token).
 """
 import numpy as np
 import pytest
@@ -49,6 +50,9 @@ SHAPES = {
     "decode_small_m": MoeShape("decode_small_m", T=37, d=512, d_e=256, E=64, k=8, n_groups=8,
                                topk_groups=4, d_shared=128, seed=205),
     "one_token": MoeShape("one_token", T=1, d=256, d_e=128, E=8, k=2, d_shared=128, seed=206),
+    "single_expert": MoeShape("single_expert", T=300, d=384, d_e=256, E=1, k=1, d_shared=128,
+                              seed=207),
+    "k_equals_E": MoeShape("k_equals_E", T=130, d=256, d_e=128, E=4, k=4, bias_std=0.5, seed=208),
 }
 
 _cache = {}
@@ -208,4 +212,57 @@ def test_backward_captures_into_a_cuda_graph():
     torch.cuda.synchronize()
     for key in g:
         assert torch.equal(grads[key], g[key]), key
+    assert layer.device_status() == 0
+
+
+def test_backward_weight_packs():
+    """moe_pack_experts_bwd interleaves W1 and W3 per 128 columns along d_e;
+    moe_pack_router_bwd pads Wg to a multiple of 128 columns with zeros."""
+    g = torch.Generator().manual_seed(11)
+    E, d, de = 3, 256, 384
+    W1 = torch.randn((E, d, de), generator=g).to(torch.bfloat16).cuda()
+    W3 = torch.randn((E, d, de), generator=g).to(torch.bfloat16).cuda()
+    W13t = torch.empty((E, d, 2 * de), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts_bwd(W1, W3, W13t)
+    expect = torch.stack([W1.view(E, d, de // 128, 128), W3.view(E, d, de // 128, 128)], dim=3)
+    assert torch.equal(W13t, expect.reshape(E, d, 2 * de))
+    Wg = torch.randn((d, 5), generator=g).to(torch.bfloat16).cuda()
+    WgP = torch.full((d, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_router_bwd(Wg, WgP)
+    torch.cuda.synchronize()
+    assert torch.equal(WgP[:, :5], Wg) and not WgP[:, 5:].any()
+
+
+def test_empty_batch_backward_is_a_noop():
+    shape = MoeShape("t0", T=0, d=256, d_e=128, E=4, k=2, d_shared=128, seed=209)
+    cfg = moe.config_of(shape)
+    inp = synth.make_inputs(MoeShape("t1", T=1, d=256, d_e=128, E=4, k=2, d_shared=128, seed=209))
+    layer = moe.MoeLayer(cfg, cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), Wg=cuda(inp["Wg"]),
+                         Ws1=cuda(inp["Ws1"]), Ws3=cuda(inp["Ws3"]), Ws2=cuda(inp["Ws2"]))
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    layer(x)
+    grads = layer.backward(x, torch.empty_like(x))
+    torch.cuda.synchronize()
+    assert grads["dx"].shape == (0, 256)
+    assert layer.device_status() == 0
+
+
+def test_host_pipeline_train_matches_the_direct_calls():
+    """HostPipeline.submit_train: x and dout from pinned host memory, dx back;
+    the same bits as forward + backward called directly."""
+    shape, inp, dout, _, _ = prepared("groups_p64_d384")
+    layer, x, g = run(shape, inp, dout)
+    x_host = inp["x"].pin_memory()
+    dout_host = dout.pin_memory()
+    dx_host = [torch.empty_like(x_host).pin_memory() for _ in range(3)]
+    grads = {k: torch.empty_like(v) for k, v in g.items()}
+    pipe = moe.HostPipeline(layer)
+    for i in range(3):
+        pipe.submit_train(x_host, dout_host, dx_host[i], grads)
+    pipe.synchronize()
+    for i in range(3):
+        assert torch.equal(dx_host[i], g["dx"].cpu()), i
+    for key in g:
+        if key != "dx":
+            assert torch.equal(grads[key], g[key]), key
     assert layer.device_status() == 0
