@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "backward.h"
 #include "ptx.cuh"
 
 namespace moe {

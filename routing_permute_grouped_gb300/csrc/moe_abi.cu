@@ -11,6 +11,7 @@
 
 #include "../../include/moe.h"
 #include "internal.h"
+#include "backward.h"
 
 namespace moe {
 

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "backward.h"
 #include "ptx.cuh"
 
 namespace moe {

@@ -84,6 +84,9 @@ WORKLOADS = {
     "decode": MoeShape("decode", T=64, d=7168, d_e=2048, E=256, k=8, n_groups=8, topk_groups=4,
                        d_shared=2048, seed=1234 + 3),
     "decode_e32": MoeShape("decode_e32", T=64, d=7168, d_e=2048, E=32, k=2, seed=5),
+    # a mid-size layer (a few GB with its backward) for counter captures
+    "mid_e8": MoeShape("mid_e8", T=4096, d=4096, d_e=1024, E=8, k=4, d_shared=1024,
+                       bias_std=0.5, seed=6),
 }
 for _t in (1.0, 2.0, 4.0):
     for _p in (64, 128):
