@@ -589,9 +589,11 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: b
             + (2 if shape.d_shared and not skinny else 0) + 1 + (1 if fp8 else 0))
 
 
-def backward_launches(shape, router_grads: bool = True) -> int:
+def backward_launches(shape, router_grads: bool = True, recompute: bool = True) -> int:
     """Kernels of one moe_layer_bwd call."""
-    n = 2 + 4 + 4 + 2  # permutes of dout and x; dh, gu, SwiGLU bwd, dx_perm; 4 transposes; dW2, dW13
+    n = 2 + 4 + 2  # permutes of dout and x; dh, gate/up, SwiGLU bwd, dx_perm; dW2, dW13
+    if not recompute:
+        n -= 1  # the gate/up values come from the forward
     routed = not shape.prerouted
     if (routed and router_grads) or shape.d_shared:
         n += 1  # x transpose
@@ -599,7 +601,7 @@ def backward_launches(shape, router_grads: bool = True) -> int:
         n += 2 + 1  # router backward + dbias column sums; dx from the router
         n += 2 if router_grads else 0  # dlogit transpose, dWg
     if shape.d_shared:
-        n += 4 + 3 + 2  # gate/up, dh, SwiGLU bwd, dx; 3 transposes; 2 wgrads
+        n += (4 if recompute else 3) + 2  # gate/up, dh, SwiGLU bwd, dx; 2 weight gradients
     return n + 1  # dx combine
 
 
@@ -620,7 +622,7 @@ def run_train(args, shape, rank, world, local):
     cfg = moe.config_of(shape)
     layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
                          bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
-                         Ws2=inp.get("Ws2"))
+                         Ws2=inp.get("Ws2"), keep_gate_up=args.keep_gate_up)
     T, k, d, de, ds = shape.T, shape.k, shape.d, shape.d_e, shape.d_shared
     x = inp["x"]
     out = torch.empty_like(x)
@@ -706,8 +708,10 @@ def run_train(args, shape, rank, world, local):
     E_r = 0 if pre else shape.E
     counts_h = layer.buffer("counts", torch.int32, (shape.E,)).cpu().tolist()
     active = sum(1 for c in counts_h if c > 0)
-    bwd_flops = ledger.layer_backward_gemm_flops(T, k, d, de, ds, E_r)
-    bwd_bytes = ledger.layer_backward_bytes_alg(T, k, d, de, ds, shape.E, active, not pre)
+    bwd_flops = ledger.layer_backward_gemm_flops(T, k, d, de, ds, E_r,
+                                                 recompute=not args.keep_gate_up)
+    bwd_bytes = ledger.layer_backward_bytes_alg(T, k, d, de, ds, shape.E, active, not pre,
+                                                recompute=not args.keep_gate_up)
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     bwd_s = bwd_ms / 1e3
     # tensor-bound when the backward's FLOP per byte exceeds the machine
@@ -731,11 +735,14 @@ def run_train(args, shape, rank, world, local):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": dict(config_dict(shape, weights="bf16"), **{"pass": "train"}),
+        "config": dict(config_dict(shape, weights="bf16"), **{
+            "pass": "train",
+            "gate_up": "saved by the forward" if args.keep_gate_up else "recomputed"}),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": (forward_launches(shape, skinny) + backward_launches(shape)) * args.steps,
+        "gpu_launches": (forward_launches(shape, skinny)
+                         + backward_launches(shape, recompute=not args.keep_gate_up)) * args.steps,
         "roofline": roof,
         "stages": {"ms": {"forward": round(fwd_ms, 4), "backward": round(bwd_ms, 4)}},
     }
@@ -785,6 +792,9 @@ def main():
                     help="expert weights in bf16, or e4m3 with per-output-channel scales")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",
                     help="fwd: the layer forward; train: forward + backward per step")
+    ap.add_argument("--keep-gate-up", action="store_true",
+                    help="train: the forward saves the gate/up values, the backward skips "
+                         "recomputing them")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     shape = synth.WORKLOADS[args.workload]

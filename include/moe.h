@@ -487,6 +487,23 @@ moe_status_t moe_pack_experts_bwd(int32_t E, int32_t d, int32_t de, const void *
  * rounded up to 128, the extra columns zero. */
 moe_status_t moe_pack_router_bwd(int32_t d, int32_t E, const void *Wg, void *WgP, void *stream);
 
+/* Bytes of a gate/up save (moe_layer_fwd_save); 0 if cfg is invalid.  The
+ * routed rows' values come first, bf16 [R_max, 2*d_e] in the padded order and
+ * the packed gate/up column order (pad rows unwritten), then the shared
+ * expert's, bf16 [T, 2*d_shared], at the next 1024-byte boundary. */
+size_t moe_gate_up_save_size(const moe_config_t *cfg);
+
+/* moe_layer_fwd (topk_idx NULL) or moe_layer_fwd_prerouted (topk_idx and
+ * topk_w given) that also stores the gate/up GEMM's values x W13 (bf16, as
+ * the backward's recomputation would produce them) into gu_save, which must
+ * hold moe_gate_up_save_size(cfg) bytes.  Handing gu_save to moe_layer_bwd
+ * spares it the recomputation: memory for time, against the pages' choice
+ * of keeping only the routing ("Dropless and grouped GEMM", sec. 4). */
+moe_status_t moe_layer_fwd_save(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
+                                const int32_t *topk_idx, const float *topk_w, void *out, void *ws,
+                                size_t ws_bytes, void *gu_save, size_t gu_save_bytes,
+                                void *stream);
+
 /* Bytes of the moe_layer_bwd workspace; 0 if cfg is invalid. */
 size_t moe_backward_workspace_size(const moe_config_t *cfg);
 
@@ -499,9 +516,11 @@ size_t moe_backward_workspace_size(const moe_config_t *cfg);
  * moe_layer_fwd (or _prerouted) call that produced the output left them;
  * fwd_ws_bytes may be just that prefix, so a caller training several layers
  * can keep the prefix per layer and share the rest of the workspace.  The
- * permuted token rows are gathered again from x, the gate/up products and h
- * recomputed.  dout bf16 [T, d] is the gradient of out.  Nothing in fwd_ws
- * is written but the device error word.
+ * permuted token rows are gathered again from x, the gate/up products
+ * recomputed (or, when gu_saved is not NULL, read from the save that
+ * moe_layer_fwd_save wrote, gu_saved_bytes >= moe_gate_up_save_size(cfg)),
+ * and h recomputed from them.  dout bf16 [T, d] is the gradient of out.
+ * Nothing in fwd_ws is written but the device error word.
  *
  * Gradients (the routing choice is a constant; the bf16 rounding of h passes
  * its gradient through):
@@ -519,15 +538,17 @@ size_t moe_backward_workspace_size(const moe_config_t *cfg);
  * or enqueuing anything (the gradient arrays are not touched).
  *
  * Returns MOE_ERR_INVALID_ARG on NULL buffers a gradient needs,
- * MOE_ERR_WORKSPACE when bws_bytes < moe_backward_workspace_size(cfg) or
- * fwd_ws_bytes is shorter than the routing state, the shape errors of
+ * MOE_ERR_WORKSPACE when bws_bytes < moe_backward_workspace_size(cfg),
+ * fwd_ws_bytes is shorter than the routing state or a gate/up save is too
+ * short, the shape errors of
  * moe_check_config, MOE_ERR_CUDA on a launch error.  Asynchronous on
  * `stream`; bounded waits inside the kernels set MOE_DEVERR_TIMEOUT in the
  * forward workspace's device error word. */
 moe_status_t moe_layer_bwd(const moe_config_t *cfg, const moe_weights_t *w,
                            const moe_weights_bwd_t *wb, const void *x, const void *dout,
-                           const void *fwd_ws, size_t fwd_ws_bytes, const moe_grads_t *grads,
-                           void *bws, size_t bws_bytes, void *stream);
+                           const void *fwd_ws, size_t fwd_ws_bytes, const void *gu_saved,
+                           size_t gu_saved_bytes, const moe_grads_t *grads, void *bws,
+                           size_t bws_bytes, void *stream);
 
 /* ---------------------------------------------------------- diagnostics -- */
 

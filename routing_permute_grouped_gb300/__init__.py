@@ -33,7 +33,7 @@ __all__ = [
     "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
     "moe_shared_expert_fp8", "moe_workspace_size_fp8", "moe_workspace_layout_fp8",
     "MoeWeightsBwd", "MoeGrads", "moe_pack_experts_bwd", "moe_pack_router_bwd",
-    "moe_backward_workspace_size", "moe_layer_bwd",
+    "moe_backward_workspace_size", "moe_layer_bwd", "moe_gate_up_save_size", "moe_layer_fwd_save",
 ]
 
 MOE_OK = 0
@@ -134,8 +134,11 @@ def load():
         "moe_pack_experts_bwd": (ctypes.c_int, [I32, I32, I32, P, P, P, P]),
         "moe_pack_router_bwd": (ctypes.c_int, [I32, I32, P, P, P]),
         "moe_backward_workspace_size": (SZ, [CP]),
+        "moe_gate_up_save_size": (SZ, [CP]),
+        "moe_layer_fwd_save": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ,
+                                              P, SZ, P]),
         "moe_layer_bwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights),
-                                         ctypes.POINTER(MoeWeightsBwd), P, P, P, SZ,
+                                         ctypes.POINTER(MoeWeightsBwd), P, P, P, SZ, P, SZ,
                                          ctypes.POINTER(MoeGrads), P, SZ, P]),
         "moe_get_device_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, P, P]),
@@ -371,16 +374,33 @@ def moe_backward_workspace_size(cfg: MoeConfig) -> int:
     return int(load().moe_backward_workspace_size(ctypes.byref(cfg)))
 
 
+def moe_gate_up_save_size(cfg: MoeConfig) -> int:
+    return int(load().moe_gate_up_save_size(ctypes.byref(cfg)))
+
+
+def moe_layer_fwd_save(cfg, weights: MoeWeights, x, out, ws, gu_save, topk_idx=None, topk_w=None,
+                       stream=None) -> None:
+    """moe_layer_fwd (or the pre-routed form) that also saves the gate/up
+    values for moe_layer_bwd in gu_save (moe_gate_up_save_size bytes)."""
+    _check(load().moe_layer_fwd_save(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(out),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(gu_save),
+        gu_save.numel() * gu_save.element_size(), _stream(stream)))
+
+
 def moe_layer_bwd(cfg, weights: MoeWeights, wbwd: MoeWeightsBwd, x, dout, ws, grads: dict, bws,
-                  stream=None) -> None:
-    """Backward of moe_layer_fwd(_prerouted); ``grads`` maps the moe_grads_t
-    field names to caller-owned CUDA tensors (missing or None = NULL)."""
+                  gu_saved=None, stream=None) -> None:
+    """Backward of moe_layer_fwd(_prerouted / _save); ``grads`` maps the
+    moe_grads_t field names to caller-owned CUDA tensors (missing or None =
+    NULL); ``gu_saved`` is the gate/up save of moe_layer_fwd_save, or None to
+    recompute it."""
     g = MoeGrads(**{n: (None if grads.get(n) is None else _ptr(grads[n]).value)
                     for n in _GRAD_FIELDS})
+    gu_bytes = 0 if gu_saved is None else gu_saved.numel() * gu_saved.element_size()
     _check(load().moe_layer_bwd(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(wbwd),
                                 _ptr(x), _ptr(dout), _ptr(ws), ws.numel() * ws.element_size(),
-                                ctypes.byref(g), _ptr(bws), bws.numel() * bws.element_size(),
-                                _stream(stream)))
+                                _ptr(gu_saved), gu_bytes, ctypes.byref(g), _ptr(bws),
+                                bws.numel() * bws.element_size(), _stream(stream)))
 
 
 def moe_get_device_status(ws, stream=None) -> int:
@@ -415,10 +435,17 @@ class MoeLayer:
     """
 
     def __init__(self, cfg: MoeConfig, W1, W3, W2, Wg=None, bias=None, Ws1=None, Ws3=None, Ws2=None,
-                 stream=None, fp8: bool = False):
+                 stream=None, fp8: bool = False, keep_gate_up: bool = False):
         moe_check_config(cfg)
         self.cfg = cfg
         self.fp8 = fp8
+        # keep_gate_up: every forward saves the gate/up values (moe_layer_fwd_save)
+        # and the backward reads them instead of recomputing them
+        self.keep_gate_up = keep_gate_up and not fp8
+        self.gu_save = None
+        if self.keep_gate_up:
+            self.gu_save = torch.empty(moe_gate_up_save_size(cfg), dtype=torch.uint8,
+                                       device=W1.device)
         dev = W1.device
         E, d, de = W1.shape
         if fp8:
@@ -497,6 +524,9 @@ class MoeLayer:
             else:
                 moe_layer_fwd_fp8_prerouted(self.cfg, self.weights, x, topk_idx, topk_w, out,
                                             self.ws, stream)
+        elif self.keep_gate_up:
+            moe_layer_fwd_save(self.cfg, self.weights, x, out, self.ws, self.gu_save,
+                               topk_idx=topk_idx, topk_w=topk_w, stream=stream)
         elif topk_idx is None:
             moe_layer_fwd(self.cfg, self.weights, x, out, self.ws, stream)
         else:
@@ -561,7 +591,8 @@ class MoeLayer:
         wb = self.wbwd
         if prerouted and wb.WgP is not None:
             wb = MoeWeightsBwd(W13t=wb.W13t, W2=wb.W2, WgP=None, Ws13t=wb.Ws13t, Ws2=wb.Ws2)
-        moe_layer_bwd(self.cfg, self.weights, wb, x, dout, self.ws, grads, self.bws, stream)
+        moe_layer_bwd(self.cfg, self.weights, wb, x, dout, self.ws, grads, self.bws,
+                      gu_saved=self.gu_save, stream=stream)
         return grads
 
     def buffer(self, name: str, dtype, shape, offset: int = 0) -> torch.Tensor:

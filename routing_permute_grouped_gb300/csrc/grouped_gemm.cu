@@ -84,6 +84,28 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 
 // GEMM1: columns [0, 128) of the tile are gate, [128, 256) up, for the 128
 // SwiGLU outputs [nb*128, nb*128 + 128) of row m0 + row.
+// Stores 32 gate and 32 up accumulators of one row as bf16 at column c of
+// the tile in the saved gate/up array (packed order: the tile's 128 gate
+// columns, then its 128 up columns).
+__device__ __forceinline__ void save_gate_up(const GemmArgs& a, const TileInfo& ti, int row, int c,
+                                             const uint32_t (&g)[32], const uint32_t (&u)[32]) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.gu_out) + (int64_t)(ti.m0 + row) * a.ld_gu +
+                         (int64_t)ti.nb * 256 + c;
+    uint32_t pg[16], pu[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        pg[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+        pu[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+    }
+    uint4* dg = reinterpret_cast<uint4*>(dst);
+    uint4* du = reinterpret_cast<uint4*>(dst + 128);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dg[i] = make_uint4(pg[4 * i], pg[4 * i + 1], pg[4 * i + 2], pg[4 * i + 3]);
+        du[i] = make_uint4(pu[4 * i], pu[4 * i + 1], pu[4 * i + 2], pu[4 * i + 3]);
+    }
+}
+
 __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
                                            int row) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
@@ -95,6 +117,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, const TileInfo& ti
         tmem_ld32(taddr + c * 32, g);
         tmem_ld32(taddr + 128 + c * 32, u);
         tmem_ld_wait();
+        if (valid && a.gu_out) save_gate_up(a, ti, row, c * 32, g, u);
         if (valid) {
             uint32_t p[16];
 #pragma unroll
@@ -514,6 +537,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
                 tmem_ld32(taddr + c * 64 + half * 32, g);
                 tmem_ld32(taddr + 128 + c * 64 + half * 32, u);
                 tmem_ld_wait();
+                if (a.gu_out) save_gate_up(a, ti, row, c * 64 + half * 32, g, u);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);

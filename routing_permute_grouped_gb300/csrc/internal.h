@@ -58,6 +58,10 @@ struct GemmArgs {
     int64_t ldo;                    // output row stride (elements)
     int64_t out_rows;               // rows of the output tensor
     const float* row_gate;          // per padded row (gate epilogue), may be null
+    // SwiGLU epilogue only: also store the gate/up values (bf16) of the tile,
+    // in the packed interleaved column order, at gu_out[row * ld_gu + col]
+    void* gu_out;
+    int64_t ld_gu;
     uint32_t* status;               // device error word, may be null
     // router epilogue
     const float* bias;
@@ -117,6 +121,8 @@ struct SkinnyArgs {
     const float* row_gate;          // routed gate per padded row (gate epilogue), may be null
     const float* scale;             // e4m3 weights: fp32 scale per weight row
     const float* xscale;            // e4m3: scale of each token row pair (per padded row)
+    void* gu_out;                   // SwiGLU: gate/up values saved [out_rows, ld_gu], or null
+    int64_t ld_gu;
     // shared expert (dense tiles after the routed ones)
     int32_t s_rows;                 // token rows (0 = no shared tiles)
     int32_t s_panels;
@@ -126,6 +132,8 @@ struct SkinnyArgs {
     int64_t s_ldo;
     const float* s_scale;
     const float* s_xscale;
+    void* s_gu_out;                 // SwiGLU: the shared expert's gate/up values, or null
+    int64_t s_ld_gu;
     uint32_t* status;               // device error word, may be null
 };
 

@@ -229,7 +229,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
                                const void* W2_t, const int32_t* meta, const int32_t* nb,
                                const int32_t* po, const float* row_gate, void* h, void* y,
                                uint32_t* status, cudaStream_t st, const void* x = nullptr,
-                               const int32_t* row_src = nullptr) {
+                               const int32_t* row_src = nullptr, void* gu = nullptr) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
     a.block_metadata = meta;
@@ -246,6 +246,8 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.out = h;
     a.ldo = c.d_e;
     a.out_rows = s.R;
+    a.gu_out = gu;  // the gate/up values saved for the backward, or null
+    a.ld_gu = 2 * c.d_e;
     const bool gather = x_perm == nullptr;
     a.gather_x = x;
     a.row_src = row_src;
@@ -257,6 +259,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 (gate/up + SwiGLU)");
     // GEMM2: N = d, K = d_e
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
+    a.gu_out = nullptr;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_e / 64;
     a.b_rows_per_expert = c.d;
@@ -280,6 +283,7 @@ struct SkinnyIO {
     uint8_t* h8;           // e4m3: pairs of h [2 rows, width]
     float* h_scale;        // e4m3: their scales
     void* y;               // bf16 [rows, d]
+    void* gu;              // bf16 [rows, 2 width]: GEMM1's gate/up values saved, or null
 };
 
 // The expert GEMMs on the swapped-operand kernel for blocks with few rows.
@@ -314,6 +318,8 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const Ski
     a.ldo = c.d_e;
     a.scale = r.s13;
     a.xscale = r.x_scale;
+    a.gu_out = r.gu;
+    a.ld_gu = 2 * c.d_e;
     if (shared) {
         a.s_rows = c.T;
         a.s_panels = c.d_shared / 128;
@@ -323,6 +329,8 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const Ski
         a.s_ldo = c.d_shared;
         a.s_scale = sh->s13;
         a.s_xscale = sh->x_scale;
+        a.s_gu_out = sh->gu;
+        a.s_ld_gu = 2 * c.d_shared;
     }
     int64_t tiles = s.NB * a.n_panels * a.n_chunks + (shared ? chunks * a.s_panels : 0);
     cudaError_t e = launch_grouped_gemm_skinny(
@@ -337,6 +345,8 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const Ski
         if (e != cudaSuccess) return cuda_fail(e, "e4m3 pairs of h");
     }
     // GEMM2: panels of 256 output rows, K = d_e (d_shared for the shared tiles)
+    a.gu_out = nullptr;
+    a.s_gu_out = nullptr;
     a.n_panels = (c.d + 255) / 256;
     a.rows_per_expert = c.d;
     a.k_blocks = c.d_e / ks;
@@ -371,7 +381,7 @@ static bool use_skinny(const moe_config_t& c) {
 
 static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
                               const void* Ws2_t, void* hs, void* ys, uint32_t* status,
-                              cudaStream_t st) {
+                              cudaStream_t st, void* gus = nullptr) {
     GemmArgs a{};
     a.dense_rows = c.T;
     a.status = status;
@@ -382,11 +392,14 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     a.out = hs;
     a.ldo = c.d_shared;
     a.out_rows = c.T;
+    a.gu_out = gus;
+    a.ld_gu = 2 * c.d_shared;
     const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
                                         mblocks * a.n_tiles, st);
     if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
+    a.gu_out = nullptr;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_shared / 64;
     a.out = ys;
@@ -445,9 +458,18 @@ static moe_status_t check_layer_args(const moe_config_t* cfg, bool routed, const
     return MOE_OK;
 }
 
+// Bytes of the routed part of a gate/up save (the shared expert's follows).
+static size_t gate_up_routed_bytes(const moe_config_t& c) {
+    return align_up(static_cast<size_t>(sizes_of(c).R) * 2 * c.d_e * 2, 1024);
+}
+
+static size_t gate_up_save_bytes(const moe_config_t& c) {
+    return gate_up_routed_bytes(c) + static_cast<size_t>(c.T) * 2 * c.d_shared * 2;
+}
+
 static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
                           const int32_t* pre_idx, const float* pre_w, void* out, void* ws,
-                          size_t ws_bytes, cudaStream_t st) {
+                          size_t ws_bytes, cudaStream_t st, void* gu_save = nullptr) {
     if (!w) return fail(MOE_ERR_INVALID_ARG, "null weights");
     moe_status_t r = check_layer_args(cfg, pre_idx == nullptr, w->Wg_t, x, pre_w, out, ws, ws_bytes);
     if (r != MOE_OK) return r;
@@ -463,20 +485,24 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     cudaError_t e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
     if (e != cudaSuccess) return cuda_fail(e, "permute");
     const void* shared = c.d_shared ? B.at(L.ys) : nullptr;
+    // gate/up values saved for the backward: routed rows, then the shared expert's
+    void* gu = gu_save;
+    void* gus = gu_save && c.d_shared ? static_cast<uint8_t*>(gu_save) + gate_up_routed_bytes(c)
+                                      : nullptr;
     if (use_skinny(c)) {
         const SkinnyIO ro{B.at(L.x_perm), nullptr, w->W13, nullptr, w->W2, nullptr,
-                          B.at(L.h), nullptr, nullptr, B.at(L.y)};
+                          B.at(L.h), nullptr, nullptr, B.at(L.y), gu};
         const SkinnyIO so{x, nullptr, w->Ws13, nullptr, w->Ws2, nullptr,
-                          B.at(L.hs), nullptr, nullptr, B.at(L.ys)};
+                          B.at(L.hs), nullptr, nullptr, B.at(L.ys), gus};
         r = do_experts_skinny(c, false, ro, B.meta(), B.nb(), B.row_gate(), B.status(), st,
                               c.d_shared ? &so : nullptr);
         if (r != MOE_OK) return r;
     } else {
         r = do_experts(c, B.at(L.x_perm), w->W13, w->W2, B.meta(), B.nb(), B.po(), B.row_gate(),
-                       B.at(L.h), B.at(L.y), B.status(), st);
+                       B.at(L.h), B.at(L.y), B.status(), st, nullptr, nullptr, gu);
         if (r != MOE_OK) return r;
         if (c.d_shared) {
-            r = do_shared(c, x, w->Ws13, w->Ws2, B.at(L.hs), B.at(L.ys), B.status(), st);
+            r = do_shared(c, x, w->Ws13, w->Ws2, B.at(L.hs), B.at(L.ys), B.status(), st, gus);
             if (r != MOE_OK) return r;
         }
     }
@@ -605,8 +631,9 @@ static cudaError_t pair_gemm(const moe_config_t& c, const void* A, int64_t rowsA
 
 static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
                               const moe_weights_bwd_t* wb, const void* x, const void* dout,
-                              const void* fwd_ws, size_t fwd_ws_bytes, const moe_grads_t* g,
-                              void* bws, size_t bws_bytes, cudaStream_t st) {
+                              const void* fwd_ws, size_t fwd_ws_bytes, const void* gu_saved,
+                              size_t gu_saved_bytes, const moe_grads_t* g, void* bws,
+                              size_t bws_bytes, cudaStream_t st) {
     moe_status_t r = check_cfg(cfg, false);
     if (r != MOE_OK) return r;
     const moe_config_t& c = *cfg;
@@ -627,6 +654,9 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     if (fwd_ws_bytes < L.x_perm)
         return fail(MOE_ERR_WORKSPACE, "forward routing state of %zu bytes, %zu expected",
                     fwd_ws_bytes, L.x_perm);
+    if (gu_saved && gu_saved_bytes < gate_up_save_bytes(c))
+        return fail(MOE_ERR_WORKSPACE, "gate/up save of %zu bytes, %zu expected", gu_saved_bytes,
+                    gate_up_save_bytes(c));
     const BwdLayout B = bwd_layout_of(c);
     if (!bws || bws_bytes < B.total)
         return fail(MOE_ERR_WORKSPACE, "backward workspace of %zu bytes, %zu needed", bws_bytes,
@@ -657,10 +687,15 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     // weight), [g|u] and h recomputed, dgu and dgates, dx_perm
     e = pair_gemm(c, W(B.dz), s.R, wb->W2, de, d, de, W(B.dh), s.R, meta, nb, po, status, st);
     MOE_BWD_CHECK("dh = dz W2^T");
-    e = pair_gemm(c, W(B.xp), s.R, w->W13, 2 * de, d, 2 * de, W(B.gu), s.R, meta, nb, po, status,
-                  st);
-    MOE_BWD_CHECK("gate/up recomputation");
-    e = launch_swiglu_bwd(W(B.gu), W(B.dh), row_src, row_gate, po + E, W(B.hp), W(B.dgu), dgates,
+    // the gate/up values: saved by the forward, or recomputed
+    const void* gu = gu_saved;
+    if (!gu) {
+        e = pair_gemm(c, W(B.xp), s.R, w->W13, 2 * de, d, 2 * de, W(B.gu), s.R, meta, nb, po, status,
+                      st);
+        MOE_BWD_CHECK("gate/up recomputation");
+        gu = W(B.gu);
+    }
+    e = launch_swiglu_bwd(gu, W(B.dh), row_src, row_gate, po + E, W(B.hp), W(B.dgu), dgates,
                           W(B.dz), W(B.xp), d, s.R, de, st);
     MOE_BWD_CHECK("SwiGLU backward");
     e = pair_gemm(c, W(B.dgu), s.R, wb->W13t, d, 2 * de, d, W(B.dxp), s.R, meta, nb, po, status, st);
@@ -693,13 +728,18 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     const void* dxs = nullptr;
     if (shared) {
         const int ds = c.d_shared;
-        e = pair_gemm(c, x, c.T, w->Ws13, 2 * ds, d, 2 * ds, W(B.gus), c.T, nullptr, nullptr, nullptr,
-                      status, st);
+        const void* gus = gu_saved ? static_cast<const uint8_t*>(gu_saved) + gate_up_routed_bytes(c)
+                                   : nullptr;
+        if (!gus) {
+            e = pair_gemm(c, x, c.T, w->Ws13, 2 * ds, d, 2 * ds, W(B.gus), c.T, nullptr, nullptr,
+                          nullptr, status, st);
+            gus = W(B.gus);
+        }
         if (e == cudaSuccess)
             e = pair_gemm(c, dout, c.T, wb->Ws2, ds, d, ds, W(B.dhs), c.T, nullptr, nullptr, nullptr,
                           status, st);
         if (e == cudaSuccess)
-            e = launch_swiglu_bwd(W(B.gus), W(B.dhs), nullptr, nullptr, nullptr, W(B.hs), W(B.dgus),
+            e = launch_swiglu_bwd(gus, W(B.dhs), nullptr, nullptr, nullptr, W(B.hs), W(B.dgus),
                                   nullptr, nullptr, nullptr, 0, c.T, ds, st);
         if (e == cudaSuccess)
             e = pair_gemm(c, W(B.dgus), c.T, wb->Ws13t, d, 2 * ds, d, W(B.dxs), c.T, nullptr, nullptr,
@@ -989,6 +1029,23 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t* cfg, const moe_weights_
     return layer(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_gate_up_save_size(const moe_config_t* cfg) {
+    if (check_cfg(cfg, false) != MOE_OK) return 0;
+    return gate_up_save_bytes(*cfg);
+}
+
+moe_status_t moe_layer_fwd_save(const moe_config_t* cfg, const moe_weights_t* w, const void* x,
+                                const int32_t* topk_idx, const float* topk_w, void* out, void* ws,
+                                size_t ws_bytes, void* gu_save, size_t gu_save_bytes, void* stream) {
+    moe_status_t r = check_cfg(cfg, topk_idx == nullptr);
+    if (r != MOE_OK) return r;
+    if (cfg->T > 0 && (!gu_save || gu_save_bytes < gate_up_save_bytes(*cfg)))
+        return fail(MOE_ERR_WORKSPACE, "gate/up save of %zu bytes, %zu needed", gu_save_bytes,
+                    gate_up_save_bytes(*cfg));
+    return layer(cfg, w, x, topk_idx, topk_w, out, ws, ws_bytes, static_cast<cudaStream_t>(stream),
+                 gu_save);
+}
+
 moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* w, const void* x,
                                void* out, void* ws, size_t ws_bytes, void* stream) {
     return layer_fp8(cfg, w, x, nullptr, nullptr, out, ws, ws_bytes,
@@ -1033,10 +1090,11 @@ size_t moe_backward_workspace_size(const moe_config_t* cfg) {
 
 moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
                            const moe_weights_bwd_t* wb, const void* x, const void* dout,
-                           const void* fwd_ws, size_t fwd_ws_bytes, const moe_grads_t* grads,
-                           void* bws, size_t bws_bytes, void* stream) {
-    return layer_bwd(cfg, w, wb, x, dout, fwd_ws, fwd_ws_bytes, grads, bws, bws_bytes,
-                     static_cast<cudaStream_t>(stream));
+                           const void* fwd_ws, size_t fwd_ws_bytes, const void* gu_saved,
+                           size_t gu_saved_bytes, const moe_grads_t* grads, void* bws,
+                           size_t bws_bytes, void* stream) {
+    return layer_bwd(cfg, w, wb, x, dout, fwd_ws, fwd_ws_bytes, gu_saved, gu_saved_bytes, grads, bws,
+                     bws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_get_device_status(void* ws, uint32_t* bits, void* stream) {

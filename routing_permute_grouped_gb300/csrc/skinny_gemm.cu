@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(192, 1)
             const float* xsc = x.shared ? args.s_xscale : args.xscale;  // e4m3: token row scales
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(x.shared ? args.s_out : args.out);
             const int64_t ldo = x.shared ? args.s_ldo : args.ldo;
+            __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(x.shared ? args.s_gu_out : args.gu_out);
+            const int64_t ld_gu = x.shared ? args.s_ld_gu : args.ld_gu;
             constexpr int TPC = FP8 ? 8 : 16;  // tokens per 16 accumulator columns
             const bool two = EPI == kEpiSwiGLU || x.p * kWRows + kWRows <= rpe;
             const float s0 = FP8 ? ld_dep(sc + wrow) : 1.0f;
@@ -346,6 +348,12 @@ __global__ void __launch_bounds__(192, 1)
                             const float h = silu(v0 * s0) * (v1 * s1);
                             out[(x.m0 + tt) * ldo + static_cast<int64_t>(x.p) * 128 + row] =
                                 __float2bfloat16_rn(h);
+                            if (gu) {  // the gate/up values, packed order
+                                __nv_bfloat16* gr = gu + (x.m0 + tt) * ld_gu +
+                                                    static_cast<int64_t>(x.p) * kWRows + row;
+                                gr[0] = __float2bfloat16_rn(v0 * s0);
+                                gr[128] = __float2bfloat16_rn(v1 * s1);
+                            }
                         } else {
                             const float gate = (!x.shared && args.row_gate)
                                                    ? ld_dep(args.row_gate + x.m0 + tt)

@@ -119,26 +119,29 @@ def layer_backward_useful_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0,
     return 2 * layer_useful_flops(T, k, d, d_e, d_s) + (2 * router_flops(T, d, E) if E else 0)
 
 
-def layer_backward_gemm_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0, E: int = 0) -> int:
-    """FLOP the backward's GEMMs execute on unpadded rows: the useful FLOP plus
-    the recomputed gate/up products (2 * d * 2 d_e per routed row, the same
-    for the shared expert)."""
-    recompute = T * k * 2 * d * 2 * d_e + (T * 2 * d * 2 * d_s if d_s else 0)
-    return layer_backward_useful_flops(T, k, d, d_e, d_s, E) + recompute
+def layer_backward_gemm_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0, E: int = 0,
+                              recompute: bool = True) -> int:
+    """FLOP the backward's GEMMs execute on unpadded rows: the useful FLOP plus,
+    unless the forward saved them, the recomputed gate/up products
+    (2 * d * 2 d_e per routed row, the same for the shared expert)."""
+    extra = T * k * 2 * d * 2 * d_e + (T * 2 * d * 2 * d_s if d_s else 0)
+    return layer_backward_useful_flops(T, k, d, d_e, d_s, E) + (extra if recompute else 0)
 
 
 def layer_backward_bytes_alg(T: int, k: int, d: int, d_e: int, d_s: int, E: int, active: int,
-                             router: bool, b: int = BF16) -> int:
+                             router: bool, b: int = BF16, recompute: bool = True) -> int:
     """A lower bound of the bytes the layer backward moves: the weights its
     data gradients and the gate/up recomputation read (W2, W13 and W13 in
-    the other orientation: 5 * d * d_e per expert that received a row), the
-    weight gradients it writes (3 * d * d_e for every expert, zero for the
-    others), the shared expert's weights and gradients likewise, the router
-    weight and its fp32 gradient, and the token rows x and dout read and dx
-    written once.  The activations of the padded layout are not counted."""
-    n = b * (active * 5 * d * d_e + E * 3 * d * d_e + 3 * T * d)
+    the other orientation: 5 * d * d_e per expert that received a row; 3 *
+    d * d_e without the recomputation), the weight gradients it writes (3 *
+    d * d_e for every expert, zero for the others), the shared expert's
+    weights and gradients likewise, the router weight and its fp32 gradient,
+    and the token rows x and dout read and dx written once.  The activations
+    of the padded layout are not counted."""
+    wr = 5 if recompute else 3
+    n = b * (active * wr * d * d_e + E * 3 * d * d_e + 3 * T * d)
     if d_s:
-        n += b * 8 * d * d_s
+        n += b * (wr + 3) * d * d_s
     if router:
         n += b * d * E + 4 * d * E
     return n

@@ -167,9 +167,9 @@ def test_backward_entry_points_check_arguments_before_launch(lib):
     full = {n: fake for n in moe._GRAD_FIELDS}
     g = moe.MoeGrads(**full)
 
-    def call(c=cfg, w=w, wb=wb, g=g, fwd_bytes=need_f, bws_bytes=need_b, x=fp):
+    def call(c=cfg, w=w, wb=wb, g=g, fwd_bytes=need_f, bws_bytes=need_b, x=fp, gu=None, gu_bytes=0):
         return lib.moe_layer_bwd(ctypes.byref(c), ctypes.byref(w), ctypes.byref(wb), x, fp, fp,
-                                 fwd_bytes, ctypes.byref(g), fp, bws_bytes, None)
+                                 fwd_bytes, gu, gu_bytes, ctypes.byref(g), fp, bws_bytes, None)
 
     assert call(bws_bytes=need_b - 1) == 3
     # the backward needs only the routing state at the front of the forward workspace
@@ -181,6 +181,13 @@ def test_backward_entry_points_check_arguments_before_launch(lib):
     assert call(wb=moe.MoeWeightsBwd(W13t=fake, W2=fake, WgP=None, Ws13t=fake, Ws2=fake)) == 1
     assert "WgP" in lib.moe_last_error().decode()
     assert call(c=_cfg(d_shared=256, d_e=200)) == 2
+    # a gate/up save shorter than its size
+    need_gu = moe.moe_gate_up_save_size(cfg)
+    R = 256 * 2 + 8 * 127
+    assert need_gu >= R * 2 * 256 * 2 + 256 * 2 * 256 * 2
+    assert call(gu=fp, gu_bytes=need_gu - 1) == 3
+    assert lib.moe_layer_fwd_save(ctypes.byref(cfg), ctypes.byref(w), fp, None, None, fp, fp,
+                                  moe.moe_workspace_size(cfg), fp, need_gu - 1, None) == 3
     # T = 0: nothing to do, nothing enqueued
     c0 = _cfg(T=0, d_shared=256)
     assert call(c=c0, fwd_bytes=moe.moe_workspace_size(c0),

@@ -266,3 +266,42 @@ def test_host_pipeline_train_matches_the_direct_calls():
         if key != "dx":
             assert torch.equal(grads[key], g[key]), key
     assert layer.device_status() == 0
+
+
+def _layer(shape, inp, **kw):
+    cfg = moe.config_of(shape)
+    return moe.MoeLayer(cfg, cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]),
+                        Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")),
+                        Ws1=cuda(inp.get("Ws1")), Ws3=cuda(inp.get("Ws3")),
+                        Ws2=cuda(inp.get("Ws2")), **kw)
+
+
+@pytest.mark.parametrize("name", ["routed_shared", "prerouted_empty", "decode_small_m"])
+def test_saved_gate_up_matches_the_recomputation(name):
+    """moe_layer_fwd_save keeps [g|u]; the backward that reads it gives the
+    forward output and gradients of the recomputing one, bit for bit where the
+    forward and the recomputation run the same GEMM kernel (the CTA-pair
+    kernel), and within the parity bound where the forward ran the small-M
+    kernel (decode sizes)."""
+    shape, inp, dout, _, ref = prepared(name)
+    pre = bool(shape.prerouted)
+    kw = dict(topk_idx=cuda(inp["topk_idx"]), topk_w=cuda(inp["topk_w"])) if pre else {}
+    x, dz = cuda(inp["x"]), cuda(dout)
+    plain, keep = _layer(shape, inp), _layer(shape, inp, keep_gate_up=True)
+    out_p, out_k = plain(x, **kw), keep(x, **kw)
+    g_p = plain.backward(x, dz, prerouted=pre)
+    g_k = keep.backward(x, dz, prerouted=pre)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, out_k)
+    assert keep.device_status() == 0
+    if shape.T * shape.k > 32 * shape.E:  # the forward ran the CTA-pair kernel
+        for key in g_p:
+            assert torch.equal(g_p[key], g_k[key]), key
+        return
+    for key in ("dx", "dgates", "dW1", "dW3", "dW2", "dWs1", "dWs3", "dWs2"):
+        if key in ref:
+            assert_close(f64(g_k[key]), ref[key], key)
+    if not pre:
+        s_wg, s_bias = router_scales(inp, _cache[name][3], ref)
+        assert_close(f64(g_k["dWg"]), ref["dWg"], "dWg", s_wg)
+        assert_close(f64(g_k["dbias"]), ref["dbias"], "dbias", s_bias)
