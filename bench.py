@@ -360,7 +360,18 @@ def run_ours(args, shape, rank, world, local):
     h, y = buf("h", bf, (R, de)), buf("y", bf, (R, d))
     hs = buf("hs", bf, (T, ds)) if ds else None
     ys = buf("ys", bf, (T, d)) if ds else None
-    if fp8:  # e4m3 pairs of the activations and their row scales
+    # the layer's kernel choice: the small-M kernel (shared expert merged
+    # into its launches) when the mean rows per expert is at most 32; above
+    # that, e4m3 weights are widened to bf16 for the CTA-pair kernel
+    skinny = T * k <= 32 * E
+    wide = fp8 and not skinny
+    if wide:  # the widened codes: routed W13, W2, then shared Ws13, Ws2
+        n13, n2, ns13 = E * 2 * de * d, E * d * de, 2 * ds * d
+        W13w = buf("w16", bf, (n13,))
+        W2w = buf("w16", bf, (n2,), offset=2 * n13)
+        Ws13w = buf("w16", bf, (ns13,), offset=2 * (n13 + n2)) if ds else None
+        Ws2w = buf("w16", bf, (ns13 // 2,), offset=2 * (n13 + n2 + ns13)) if ds else None
+    if fp8 and not wide:  # e4m3 pairs of the activations and their row scales
         u8 = torch.uint8
         x_perm = buf("x_perm", u8, (2 * R, d))
         h8 = buf("h8", u8, (2 * R, de))
@@ -372,10 +383,6 @@ def run_ours(args, shape, rank, world, local):
         hs_scale = buf("row_scale", f32, (T,), offset=8 * R + 4 * T) if ds else None
     else:
         x_perm = buf("x_perm", bf, (R, d))
-    # the layer's kernel choice: the small-M kernel (shared expert merged
-    # into its launches) when the mean rows per expert is at most 32, and
-    # always with e4m3 weights
-    skinny = fp8 or T * k <= 32 * E
     status_word = buf("status", i32, (1,))
     nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
     router_partial = buf("router_partial", f32, (nsplit,)) if nsplit else None
@@ -395,13 +402,18 @@ def run_ours(args, shape, rank, world, local):
                               row_gate, offs_ws)
         if ev is not None:
             ev[2].record()
-        if fp8:
+        if fp8 and not wide:
             moe.moe_permute_fp8(cfg, x, perm_row, x_perm, x_scale, xs8, xs_scale)
         elif args.permute == "separate":
             moe.moe_permute(cfg, x, perm_row, x_perm)
         if ev is not None:
             ev[3].record()
-        if fp8:
+        if wide:  # widen the routed codes, then the scaled bf16 GEMMs
+            moe.moe_widen_e4m3(layer.W13q, W13w)
+            moe.moe_widen_e4m3(layer.W2q, W2w)
+            moe.moe_grouped_gemm_swiglu_scaled(cfg, x_perm, W13w, layer.s13, W2w, layer.s2, meta,
+                                               nb, po, row_gate, h, y, status_word)
+        elif fp8:
             moe.moe_grouped_gemm_swiglu_fp8(cfg, x_perm, x_scale, layer.W13q, layer.s13, layer.W2q,
                                             layer.s2, meta, nb, row_gate, h, h8, h_scale, y,
                                             status_word)
@@ -416,7 +428,12 @@ def run_ours(args, shape, rank, world, local):
                                                row_gate, h, y, status_word)
         if ev is not None:
             ev[4].record()
-        if ds and fp8:
+        if ds and wide:
+            moe.moe_widen_e4m3(layer.Ws13q, Ws13w)
+            moe.moe_widen_e4m3(layer.Ws2q, Ws2w)
+            moe.moe_shared_expert_scaled(cfg, x, Ws13w, layer.ss13, Ws2w, layer.ss2, hs, ys,
+                                         status_word)
+        elif ds and fp8:
             moe.moe_shared_expert_fp8(cfg, xs8, xs_scale, layer.Ws13q, layer.ss13, layer.Ws2q,
                                       layer.ss2, hs, hs8, hs_scale, ys, status_word)
         elif ds:
@@ -537,7 +554,9 @@ def run_ours(args, shape, rank, world, local):
         "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16",
+        "dtype": ("e4m3 (weights, widened to bf16 for the MMAs; per-channel scales on the fp32 "
+                  "accumulators)" if wide else
+                  "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16"),
         "data": "synthetic", "config": config_dict(shape, args.permute, args.weights),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -545,6 +564,8 @@ def run_ours(args, shape, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": dict(roof, kernel="grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
                          timing="stage pass: CUDA events around " + (
+                             "moe_widen_e4m3 (routed codes) + moe_grouped_gemm_swiglu_scaled"
+                             if wide else
                              "moe_grouped_gemm_swiglu_fp8" if fp8 else
                              "moe_grouped_gemm_swiglu_skinny" if skinny else
                              "moe_grouped_gemm_swiglu"),
@@ -584,9 +605,12 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: b
     cfg = moe.config_of(shape)
     nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
     offsets_launches = 1 if shape.A <= 4096 else 3  # one-CTA offsets kernel for small batches
+    widen = (2 + (2 if shape.d_shared else 0)) if fp8 and not skinny else 0
     return ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
             + (1 if separate_permute else 0) + 2
-            + (2 if shape.d_shared and not skinny else 0) + 1 + (1 if fp8 else 0))
+            + (2 if shape.d_shared and not skinny else 0) + 1
+            + (1 if fp8 and skinny else 0)  # e4m3 pairs of h between the small-M GEMMs
+            + widen)
 
 
 def backward_launches(shape, router_grads: bool = True, recompute: bool = True) -> int:

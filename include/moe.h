@@ -155,6 +155,8 @@ typedef struct {
     size_t xs8;            /* e4m3 pairs of the token rows [2T, d] (d_shared > 0) */
     size_t h8;             /* e4m3 pairs of h [2R_max, d_e], then of hs [2T, d_shared] */
     size_t row_scale;      /* fp32 row scales: x [R_max], h [R_max], xs [T], hs [T] */
+    size_t w16;            /* e4m3 layer with T*k > 32*E: the expert codes widened to bf16
+                            * (routed W13, W2, shared Ws13, Ws2), empty otherwise */
 } moe_workspace_layout_t;
 
 /* ---------------------------------------------------------------- sizes -- */
@@ -458,10 +460,36 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
                                      const void *x, const int32_t *topk_idx, const float *topk_w,
                                      void *out, void *ws, size_t ws_bytes, void *stream);
 
-/* The layer with e4m3 expert weights (routed and shared): router and
- * offsets as moe_layer_fwd, then moe_permute_fp8, the e4m3 grouped GEMMs
- * with the shared expert's tiles in the same launches (GEMM1, the split of h
- * and hs into e4m3 pairs, GEMM2), and the combine.  ws must hold
+/* out[i] = the e4m3 code q[i] widened to bf16 (exact: every e4m3 value is a
+ * bf16 value); n % 16 == 0.  The e4m3 layer's first step above the small-M
+ * regime. */
+moe_status_t moe_widen_e4m3(const void *q, void *out, int64_t n, void *stream);
+
+/* moe_grouped_gemm_swiglu on e4m3 codes widened to bf16 (moe_widen_e4m3 of
+ * W13q, W2q): every accumulator is multiplied by its weight row's scale
+ * (s13 [E, 2*d_e], s2 [E, d] as moe_pack_experts_fp8 wrote them) before the
+ * SwiGLU or gate epilogue. */
+moe_status_t moe_grouped_gemm_swiglu_scaled(const moe_config_t *cfg, const void *x_perm,
+                                            const void *W13, const float *s13, const void *W2_t,
+                                            const float *s2, const int32_t *block_metadata,
+                                            const int32_t *num_blocks,
+                                            const int32_t *padded_offsets, const float *row_gate,
+                                            void *h, void *y, uint32_t *status, void *stream);
+
+/* moe_shared_expert on widened e4m3 codes with per-row scales ss13 [2*d_s],
+ * ss2 [d]. */
+moe_status_t moe_shared_expert_scaled(const moe_config_t *cfg, const void *x, const void *Ws13,
+                                      const float *ss13, const void *Ws2_t, const float *ss2,
+                                      void *hs, void *ys, uint32_t *status, void *stream);
+
+/* The layer with e4m3 expert weights (routed and shared).  When T*k <=
+ * 32*E (few rows per expert: the weight bytes set the pace): router and
+ * offsets as moe_layer_fwd, then moe_permute_fp8, the e4m3 grouped GEMMs on
+ * 8-bit MMAs with the shared expert's tiles in the same launches (GEMM1, the
+ * split of h and hs into e4m3 pairs, GEMM2), and the combine.  Above that
+ * (the tensor pipe sets the pace): the codes are widened to bf16 (exact)
+ * into the workspace's w16 region, and the layer runs as moe_layer_fwd with
+ * the accumulators of every GEMM scaled per output channel.  ws must hold
  * moe_workspace_size_fp8(cfg) bytes (layout: moe_workspace_layout_fp8).
  * Requires w->W13q/s13/W2q/s2, w->Wg_t, and the shared codes and scales when
  * d_shared > 0. */

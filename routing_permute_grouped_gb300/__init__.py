@@ -34,6 +34,7 @@ __all__ = [
     "moe_shared_expert_fp8", "moe_workspace_size_fp8", "moe_workspace_layout_fp8",
     "MoeWeightsBwd", "MoeGrads", "moe_pack_experts_bwd", "moe_pack_router_bwd",
     "moe_backward_workspace_size", "moe_layer_bwd", "moe_gate_up_save_size", "moe_layer_fwd_save",
+    "moe_widen_e4m3", "moe_grouped_gemm_swiglu_scaled", "moe_shared_expert_scaled",
 ]
 
 MOE_OK = 0
@@ -75,7 +76,7 @@ class MoeGrads(ctypes.Structure):
 
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
                   "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
-                  "y", "hs", "ys", "router_partial", "xs8", "h8", "row_scale")
+                  "y", "hs", "ys", "router_partial", "xs8", "h8", "row_scale", "w16")
 
 
 class _Layout(ctypes.Structure):
@@ -135,6 +136,9 @@ def load():
         "moe_pack_router_bwd": (ctypes.c_int, [I32, I32, P, P, P]),
         "moe_backward_workspace_size": (SZ, [CP]),
         "moe_gate_up_save_size": (SZ, [CP]),
+        "moe_widen_e4m3": (ctypes.c_int, [P, P, ctypes.c_int64, P]),
+        "moe_grouped_gemm_swiglu_scaled": (ctypes.c_int, [CP] + [P] * 13),
+        "moe_shared_expert_scaled": (ctypes.c_int, [CP] + [P] * 9),
         "moe_layer_fwd_save": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ,
                                               P, SZ, P]),
         "moe_layer_bwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights),
@@ -372,6 +376,27 @@ def moe_pack_router_bwd(Wg, WgP, stream=None) -> None:
 
 def moe_backward_workspace_size(cfg: MoeConfig) -> int:
     return int(load().moe_backward_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_widen_e4m3(q, out, stream=None) -> None:
+    """bf16 out (same element count) from e4m3 codes q (uint8)."""
+    _check(load().moe_widen_e4m3(_ptr(q), _ptr(out), q.numel(), _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_scaled(cfg, x_perm, W13, s13, W2_t, s2, block_metadata, num_blocks,
+                                   padded_offsets, row_gate, h, y, status=None,
+                                   stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu_scaled(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(s13), _ptr(W2_t), _ptr(s2),
+        _ptr(block_metadata), _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate), _ptr(h),
+        _ptr(y), _ptr(status), _stream(stream)))
+
+
+def moe_shared_expert_scaled(cfg, x, Ws13, ss13, Ws2_t, ss2, hs, ys, status=None,
+                             stream=None) -> None:
+    _check(load().moe_shared_expert_scaled(ctypes.byref(cfg), _ptr(x), _ptr(Ws13), _ptr(ss13),
+                                           _ptr(Ws2_t), _ptr(ss2), _ptr(hs), _ptr(ys), _ptr(status),
+                                           _stream(stream)))
 
 
 def moe_gate_up_save_size(cfg: MoeConfig) -> int:

@@ -84,6 +84,26 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 
 // GEMM1: columns [0, 128) of the tile are gate, [128, 256) up, for the 128
 // SwiGLU outputs [nb*128, nb*128 + 128) of row m0 + row.
+// Multiplies 32 accumulators by the scales of their columns (cs: the first
+// of them, 16-byte aligned; null = no scale).  The scales were written by a
+// packing kernel that finished long before this launch: read-only loads.
+__device__ __forceinline__ void scale_cols(uint32_t (&v)[32], const float* cs) {
+    if (!cs) return;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(cs + i));
+        v[i] = __float_as_uint(__uint_as_float(v[i]) * s4.x);
+        v[i + 1] = __float_as_uint(__uint_as_float(v[i + 1]) * s4.y);
+        v[i + 2] = __float_as_uint(__uint_as_float(v[i + 2]) * s4.z);
+        v[i + 3] = __float_as_uint(__uint_as_float(v[i + 3]) * s4.w);
+    }
+}
+
+// Scales of the tile's first B row (packed row col0 of expert e), or null.
+__device__ __forceinline__ const float* tile_scales(const GemmArgs& a, const TileInfo& ti, int col0) {
+    return a.col_scale ? a.col_scale + (int64_t)ti.e * a.b_rows_per_expert + col0 : nullptr;
+}
+
 // Stores 32 gate and 32 up accumulators of one row as bf16 at column c of
 // the tile in the saved gate/up array (packed order: the tile's 128 gate
 // columns, then its 128 up columns).
@@ -111,12 +131,17 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, const TileInfo& ti
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     const bool valid = row >= ti.lo && row < ti.hi;
     __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * 128;
+    const float* cs = tile_scales(a, ti, ti.nb * 256);
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         uint32_t g[32], u[32];
         tmem_ld32(taddr + c * 32, g);
         tmem_ld32(taddr + 128 + c * 32, u);
         tmem_ld_wait();
+        if (cs) {
+            scale_cols(g, cs + c * 32);
+            scale_cols(u, cs + 128 + c * 32);
+        }
         if (valid && a.gu_out) save_gate_up(a, ti, row, c * 32, g, u);
         if (valid) {
             uint32_t p[16];
@@ -141,11 +166,13 @@ __device__ __forceinline__ void epi_gate(const GemmArgs& a, const TileInfo& ti, 
     const bool valid = row >= ti.lo && row < ti.hi;
     const float gate = (valid && a.row_gate) ? ld_dep(a.row_gate + ti.m0 + row) : 1.0f;
     __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * BN;
+    const float* cs = tile_scales(a, ti, ti.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(taddr + c * 32, v);
         tmem_ld_wait();
+        if (cs) scale_cols(v, cs + c * 32);
         if (valid) {
             uint32_t p[16];
 #pragma unroll
@@ -524,6 +551,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
     constexpr int NCH = EPI == kEpiSwiGLU ? 2 : BN / 64;  // 64-column output boxes
     const int col0 = EPI == kEpiSwiGLU ? ti.nb * 128 : ti.nb * BN;
     const float gate = (EPI == kEpiGate && a.row_gate) ? ld_dep(a.row_gate + ti.m0 + row) : 1.0f;
+    const float* cs = tile_scales(a, ti, EPI == kEpiSwiGLU ? ti.nb * 256 : ti.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < NCH; ++c) {
         if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
@@ -537,6 +565,10 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
                 tmem_ld32(taddr + c * 64 + half * 32, g);
                 tmem_ld32(taddr + 128 + c * 64 + half * 32, u);
                 tmem_ld_wait();
+                if (cs) {
+                    scale_cols(g, cs + c * 64 + half * 32);
+                    scale_cols(u, cs + 128 + c * 64 + half * 32);
+                }
                 if (a.gu_out) save_gate_up(a, ti, row, c * 64 + half * 32, g, u);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -548,6 +580,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
                 uint32_t v[32];
                 tmem_ld32(taddr + c * 64 + half * 32, v);
                 tmem_ld_wait();
+                if (cs) scale_cols(v, cs + c * 64 + half * 32);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     p[i] = pack_bf16x2(gate * __uint_as_float(v[2 * i]), gate * __uint_as_float(v[2 * i + 1]));

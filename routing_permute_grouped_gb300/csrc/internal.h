@@ -62,6 +62,10 @@ struct GemmArgs {
     // in the packed interleaved column order, at gu_out[row * ld_gu + col]
     void* gu_out;
     int64_t ld_gu;
+    // per-column scale of the accumulators (e4m3 weights widened to bf16:
+    // the weights' per-output-channel scales), indexed like the B rows:
+    // col_scale[e * b_rows_per_expert + packed row]; null = 1
+    const float* col_scale;
     uint32_t* status;               // device error word, may be null
     // router epilogue
     const float* bias;
@@ -100,6 +104,9 @@ cudaError_t launch_pack_transpose(const void* in, void* out, int rows, int cols,
                                   cudaStream_t stream);
 
 int num_sms();
+
+// out[i] = the value of e4m3 code q[i] as bf16 (exact), n % 16 == 0.
+cudaError_t launch_widen_e4m3(const void* q, void* out, int64_t n, cudaStream_t stream);
 
 // Device-side description of one launch of the small-M (swapped-operand)
 // grouped GEMM.  A tile multiplies 256 rows of one expert's K-major weight

@@ -115,6 +115,20 @@ static int router_splits(const moe_config_t& c) {
     return (k_blocks + per - 1) / per;
 }
 
+// The small-M kernel serves the layer when the mean rows per expert is small
+// enough that 256-row visits would mostly multiply padding.
+static bool use_skinny(const moe_config_t& c) {
+    return static_cast<int64_t>(c.T) * c.k <= 32ll * c.E;
+}
+
+// Elements of the routed and of the shared expert weights (gate/up + down).
+static size_t routed_weight_elems(const moe_config_t& c) {
+    return static_cast<size_t>(c.E) * 3 * c.d * c.d_e;
+}
+static size_t shared_weight_elems(const moe_config_t& c) {
+    return static_cast<size_t>(3) * c.d * (c.d_shared ? c.d_shared : 0);
+}
+
 static moe_workspace_layout_t layout_of(const moe_config_t& c, bool fp8 = false) {
     const Sizes s = sizes_of(c);
     moe_workspace_layout_t L{};
@@ -147,6 +161,10 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c, bool fp8 = false)
     L.xs8 = take(fp8 && ds ? static_cast<size_t>(c.T) * c.d * 2 : 0);
     L.h8 = take(fp8 ? (static_cast<size_t>(s.R) * c.d_e + static_cast<size_t>(c.T) * ds) * 2 : 0);
     L.row_scale = take(fp8 ? (2 * static_cast<size_t>(s.R) + 2 * static_cast<size_t>(c.T)) * 4 : 0);
+    // e4m3 layer above the small-M regime: the codes widened to bf16 for the
+    // CTA-pair GEMMs (routed W13, W2, then shared Ws13, Ws2)
+    const bool wide = fp8 && !use_skinny(c);
+    L.w16 = take(wide ? (routed_weight_elems(c) + shared_weight_elems(c)) * 2 : 0);
     L.total = off;
     return L;
 }
@@ -229,7 +247,8 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
                                const void* W2_t, const int32_t* meta, const int32_t* nb,
                                const int32_t* po, const float* row_gate, void* h, void* y,
                                uint32_t* status, cudaStream_t st, const void* x = nullptr,
-                               const int32_t* row_src = nullptr, void* gu = nullptr) {
+                               const int32_t* row_src = nullptr, void* gu = nullptr,
+                               const float* s13 = nullptr, const float* s2 = nullptr) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
     a.block_metadata = meta;
@@ -248,6 +267,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.out_rows = s.R;
     a.gu_out = gu;  // the gate/up values saved for the backward, or null
     a.ld_gu = 2 * c.d_e;
+    a.col_scale = s13;  // widened e4m3 weights: their per-channel scales
     const bool gather = x_perm == nullptr;
     a.gather_x = x;
     a.row_src = row_src;
@@ -260,6 +280,7 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     // GEMM2: N = d, K = d_e
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
     a.gu_out = nullptr;
+    a.col_scale = s2;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_e / 64;
     a.b_rows_per_expert = c.d;
@@ -373,15 +394,10 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const Ski
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2, small-M kernel");
 }
 
-// The small-M kernel serves the layer when the mean rows per expert is small
-// enough that 128-row tiles would mostly multiply padding.
-static bool use_skinny(const moe_config_t& c) {
-    return static_cast<int64_t>(c.T) * c.k <= 32ll * c.E;
-}
-
 static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
                               const void* Ws2_t, void* hs, void* ys, uint32_t* status,
-                              cudaStream_t st, void* gus = nullptr) {
+                              cudaStream_t st, void* gus = nullptr, const float* ss13 = nullptr,
+                              const float* ss2 = nullptr) {
     GemmArgs a{};
     a.dense_rows = c.T;
     a.status = status;
@@ -394,12 +410,14 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     a.out_rows = c.T;
     a.gu_out = gus;
     a.ld_gu = 2 * c.d_shared;
+    a.col_scale = ss13;
     const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
                                         mblocks * a.n_tiles, st);
     if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
     a.gu_out = nullptr;
+    a.col_scale = ss2;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_shared / 64;
     a.out = ys;
@@ -525,6 +543,43 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
     if (c.T == 0) return MOE_OK;
     const LayerBufs B{layout_of(c, true), static_cast<uint8_t*>(ws)};
     const moe_workspace_layout_t& L = B.L;
+    if (!use_skinny(c)) {
+        // Enough rows per expert that the tensor pipe, not the weight bytes,
+        // sets the pace: widen the codes to bf16 (exact) and run the CTA-pair
+        // GEMMs, which scale their accumulators per output channel ("Dropless
+        // and grouped GEMM", sec. 12: a scale covering the whole contraction
+        // multiplies the product).
+        uint8_t* w16 = static_cast<uint8_t*>(B.at(L.w16));
+        const size_t n13 = static_cast<size_t>(c.E) * 2 * c.d_e * c.d;
+        const size_t n2 = static_cast<size_t>(c.E) * c.d * c.d_e;
+        const size_t ns13 = static_cast<size_t>(2) * c.d_shared * c.d;
+        void* W13w = w16;
+        void* W2w = w16 + n13 * 2;
+        void* Ws13w = w16 + (n13 + n2) * 2;
+        void* Ws2w = w16 + (n13 + n2 + ns13) * 2;
+        cudaError_t e = launch_widen_e4m3(w->W13q, W13w, static_cast<int64_t>(n13), st);
+        if (e == cudaSuccess) e = launch_widen_e4m3(w->W2q, W2w, static_cast<int64_t>(n2), st);
+        if (e == cudaSuccess && c.d_shared) {
+            e = launch_widen_e4m3(w->Ws13q, Ws13w, static_cast<int64_t>(ns13), st);
+            if (e == cudaSuccess) e = launch_widen_e4m3(w->Ws2q, Ws2w, static_cast<int64_t>(ns13 / 2), st);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "widen e4m3 weights");
+        r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
+        if (r != MOE_OK) return r;
+        e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
+        if (e != cudaSuccess) return cuda_fail(e, "permute");
+        r = do_experts(c, B.at(L.x_perm), W13w, W2w, B.meta(), B.nb(), B.po(), B.row_gate(),
+                       B.at(L.h), B.at(L.y), B.status(), st, nullptr, nullptr, nullptr, w->s13, w->s2);
+        if (r != MOE_OK) return r;
+        if (c.d_shared) {
+            r = do_shared(c, x, Ws13w, Ws2w, B.at(L.hs), B.at(L.ys), B.status(), st, nullptr, w->ss13,
+                          w->ss2);
+            if (r != MOE_OK) return r;
+        }
+        e = launch_combine(B.at(L.y), B.perm_row(), c.d_shared ? B.at(L.ys) : nullptr, out, c.T, c.d,
+                           c.k, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine");
+    }
     r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
     if (r != MOE_OK) return r;
     const Sizes s = sizes_of(c);
@@ -912,6 +967,45 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
     if (cfg->T == 0) return MOE_OK;
     return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
                       h, y, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_widen_e4m3(const void* q, void* out, int64_t n, void* stream) {
+    if (n < 0 || (n > 0 && (!q || !out))) return fail(MOE_ERR_INVALID_ARG, "bad widen args");
+    if (n % 16) return fail(MOE_ERR_UNSUPPORTED, "n = %lld is not a multiple of 16",
+                            static_cast<long long>(n));
+    if (n == 0) return MOE_OK;
+    cudaError_t e = launch_widen_e4m3(q, out, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "widen e4m3");
+}
+
+moe_status_t moe_grouped_gemm_swiglu_scaled(const moe_config_t* cfg, const void* x_perm,
+                                            const void* W13, const float* s13, const void* W2_t,
+                                            const float* s2, const int32_t* block_metadata,
+                                            const int32_t* num_blocks, const int32_t* padded_offsets,
+                                            const float* row_gate, void* h, void* y,
+                                            uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x_perm || !W13 || !s13 || !W2_t || !s2 || !block_metadata || !num_blocks ||
+        !padded_offsets || !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
+                      h, y, status, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, s13,
+                      s2);
+}
+
+moe_status_t moe_shared_expert_scaled(const moe_config_t* cfg, const void* x, const void* Ws13,
+                                      const float* ss13, const void* Ws2_t, const float* ss2,
+                                      void* hs, void* ys, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (!x || !Ws13 || !ss13 || !Ws2_t || !ss2 || !hs || !ys)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_shared(*cfg, x, Ws13, Ws2_t, hs, ys, status, static_cast<cudaStream_t>(stream), nullptr,
+                     ss13, ss2);
 }
 
 moe_status_t moe_permute_fp8(const moe_config_t* cfg, const void* x, const int32_t* perm_row,

@@ -111,4 +111,41 @@ cudaError_t launch_pack_fp8(const void* in, uint8_t* out, float* scale, int rows
     return cudaGetLastError();
 }
 
+// Widens e4m3 codes to bf16 (every e4m3 value is a bf16 value: exact), 16
+// codes per thread, grid-stride.  For the e4m3 layer at batch sizes where the
+// tensor pipe, not the weight bytes, sets the pace: the bf16 GEMMs then run
+// on the widened codes and scale their accumulators per output channel.
+__global__ void k_widen_e4m3(const uint4* __restrict__ q, uint4* __restrict__ out, int64_t n16) {
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 c = ld_dep(q + i);
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t hf = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> (16 * h)));
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hf));
+                o[2 * j + h] = pack_bf16x2(f.x, f.y);
+            }
+        }
+        out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+cudaError_t launch_widen_e4m3(const void* q, void* out, int64_t n, cudaStream_t stream) {
+    if (n % 16) return cudaErrorInvalidValue;
+    const int64_t n16 = n / 16;
+    int64_t grid = (n16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    return launch_pdl(k_widen_e4m3, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                      static_cast<const uint4*>(q), static_cast<uint4*>(out), n16);
+}
+
 }  // namespace moe

@@ -334,7 +334,7 @@ def test_fp8_layer_captures_into_a_cuda_graph():
 
 @pytest.mark.parametrize("fill", [0x00, 0x7F, 0xFF])
 @pytest.mark.parametrize("name,fp8", [("decode_like", False), ("decode_like", True),
-                                      ("full_blocks", False)])
+                                      ("full_blocks", False), ("full_blocks", True)])
 def test_layer_ignores_stale_workspace(name, fp8, fill):
     """Every kernel reads data of the earlier kernels of the launch chain only
     after waiting for them: a workspace holding zeros or stale bytes before
