@@ -349,3 +349,17 @@ def test_layer_ignores_stale_workspace(name, fp8, fill):
         torch.cuda.synchronize()
         assert layer.device_status() == 0
         assert_close(out.double().cpu().numpy(), ref["out"], f"out after a 0x{fill:02x} fill")
+
+
+def test_widen_e4m3_is_exact():
+    """moe_widen_e4m3: every code to the bf16 of its e4m3 value (torch's
+    float8_e4m3fn cast), NaN codes to NaN."""
+    codes = torch.arange(256, dtype=torch.uint8).repeat(4).cuda()
+    out = torch.empty(codes.numel(), dtype=torch.bfloat16, device="cuda")
+    moe.moe_widen_e4m3(codes, out)
+    torch.cuda.synchronize()
+    ref = codes.cpu().view(torch.float8_e4m3fn).to(torch.bfloat16)
+    got = out.cpu()
+    nan = torch.isnan(ref)
+    assert torch.equal(torch.isnan(got), nan)
+    assert torch.equal(got[~nan].view(torch.int16), ref[~nan].view(torch.int16))
