@@ -486,7 +486,8 @@ def run_ours(args, shape, rank, world, local):
         step(evs[i])
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    stage_ms = {n: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
+    # per-stage median over the stage-pass steps
+    stage_ms = {n: statistics.median(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
                 for j, n in enumerate(stage_names)}
 
     counts_h = counts.cpu().tolist()
@@ -690,8 +691,8 @@ def run_train(args, shape, rank, world, local):
         evs[i][2].record()
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     st = layer.device_status()
     if st:
         raise RuntimeError(f"device status bits {st:#x}")
