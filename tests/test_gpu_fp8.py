@@ -363,3 +363,43 @@ def test_widen_e4m3_is_exact():
     nan = torch.isnan(ref)
     assert torch.equal(torch.isnan(got), nan)
     assert torch.equal(got[~nan].view(torch.int16), ref[~nan].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["full_blocks", "half_panel_p64"])
+def test_widened_scaled_stage(name):
+    """The stage calls of the e4m3 layer above the small-M regime:
+    moe_widen_e4m3 of the codes, then moe_grouped_gemm_swiglu_scaled (the
+    per-channel scales on the accumulators) against the oracle's e4m3
+    evaluation; moe_shared_expert_scaled likewise."""
+    shape, inp, oin, ref = prepared(name, True)
+    cfg = moe.config_of(shape)
+    E, d, de, R = shape.E, shape.d, shape.d_e, shape.rows_capacity
+    q13, s13, q2, s2 = _fp8_weights(inp, E, d, de)
+    w13 = torch.empty(q13.shape, dtype=torch.bfloat16, device="cuda")
+    w2 = torch.empty(q2.shape, dtype=torch.bfloat16, device="cuda")
+    moe.moe_widen_e4m3(q13, w13)
+    moe.moe_widen_e4m3(q2, w2)
+    x_perm = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, cuda(inp["x"]), torch.as_tensor(ref["perm_row"], device="cuda"), x_perm)
+    meta, nb, row_gate = _stage_tables(shape, ref)
+    po = cuda(torch.as_tensor(ref["padded_offsets"], dtype=torch.int32))
+    h = torch.full((R, de), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_swiglu_scaled(cfg, x_perm, w13, s13, w2, s2, meta, nb, po, row_gate, h, y,
+                                       status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _compare_rows(shape, ref, h, y)
+    if shape.d_shared:
+        ds, T = shape.d_shared, shape.T
+        qs13, ss13, qs2, ss2 = _fp8_weights(inp, 1, d, ds, key=("Ws1", "Ws3", "Ws2"))
+        ws13 = torch.empty(qs13.shape, dtype=torch.bfloat16, device="cuda")
+        ws2 = torch.empty(qs2.shape, dtype=torch.bfloat16, device="cuda")
+        moe.moe_widen_e4m3(qs13, ws13)
+        moe.moe_widen_e4m3(qs2, ws2)
+        hs = torch.empty((T, ds), dtype=torch.bfloat16, device="cuda")
+        ys = torch.empty((T, shape.d), dtype=torch.bfloat16, device="cuda")
+        moe.moe_shared_expert_scaled(cfg, cuda(inp["x"]), ws13, ss13, ws2, ss2, hs, ys, status)
+        torch.cuda.synchronize()
+        assert_close(ys.double().cpu().numpy(), ref["ys"], "shared ys (widened)")
