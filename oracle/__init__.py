@@ -81,6 +81,7 @@ def _L():
                 "or_e4m3_to_double_array": (None, [LL, P, P]),
                 "or_double_to_e4m3_array": (None, [LL, P, P]),
                 "or_layer_backward": (I, [I] * 6 + [P] * 22),
+                "or_weight_grad_columns": (I, [I] * 3 + [P] * 6 + [I] + [P] * 4),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -361,6 +362,26 @@ def grouped_experts_w8(x_perm, q: dict, block_metadata, row_gate):
 
 
 # ------------------------------------------------------------- backward ----
+def weight_grad_columns(x_rows, dout_rows, p, W1, W3, W2, J):
+    """Columns J of one expert's weight gradients over the given rows (token
+    rows x_rows bf16 bits [n, d], upstream rows dout_rows fp64 [n, d],
+    routing weights p [n]; W1/W3 [d, de], W2 [de, d] bf16 bits): returns
+    (dW1[:, J], dW3[:, J], dW2[J, :]) in fp64."""
+    x = _c(x_rows, np.uint16)
+    n, d = x.shape
+    de = W1.shape[-1]
+    J = _c(J, np.int32)
+    dW1c = np.empty((d, J.size))
+    dW3c = np.empty((d, J.size))
+    dW2r = np.empty((J.size, d))
+    _check(_L().or_weight_grad_columns(n, d, de, _p(x), _p(_c(dout_rows, np.float64)),
+                                       _p(_c(p, np.float64)), _p(_c(W1, np.uint16)),
+                                       _p(_c(W3, np.uint16)), _p(_c(W2, np.uint16)), J.size,
+                                       _p(J), _p(dW1c), _p(dW3c), _p(dW2r)),
+           "weight_grad_columns")
+    return dW1c, dW3c, dW2r
+
+
 def layer_backward(inp: dict, cfg, fwd: dict, dout) -> dict:
     """Gradients of the layer forward (``layer_forward``'s routing, fixed) for
     an upstream gradient dout [T, d] (fp64): dx, dgates [T, k], dW1, dW3,

@@ -897,6 +897,54 @@ int or_layer_backward(int T, int d, int de, int E, int k, int ds, const uint16_t
     return bad ? OR_ERR_ARG : OR_OK;
 }
 
+/* Selected columns of one SwiGLU expert's weight gradients over a set of
+ * rows ("Dropless and grouped GEMM", sec. 4: the backward of the expert GEMMs
+ * over the rows routed to the expert; the layer backward above, restricted
+ * to columns).  Row r brings its token row x_r (bf16 [d]), its upstream
+ * gradient dout_r (fp64 [d]) and its routing weight p_r.  For each column j
+ * of J (0 <= j < de):
+ *   g = x_r . W1[:, j], u = x_r . W3[:, j], h = bf16(silu(g) u),
+ *   dh = p_r dout_r . W2[j, :],
+ *   dW2[j][n]  = sum_r h p_r dout_r[n]
+ *   dW1[i][jj] = sum_r x_r[i] dh u silu'(g),  dW3[i][jj] = sum_r x_r[i] dh silu(g)
+ * Outputs (fp64, overwritten): dW1c, dW3c [d][nj], dW2r [nj][d]. */
+int or_weight_grad_columns(int n, int d, int de, const uint16_t *x, const double *dout,
+                           const double *p, const uint16_t *W1, const uint16_t *W3,
+                           const uint16_t *W2, int nj, const int32_t *J, double *dW1c,
+                           double *dW3c, double *dW2r)
+{
+    if (n < 0 || d <= 0 || de <= 0 || nj <= 0) return OR_ERR_ARG;
+    for (int jj = 0; jj < nj; ++jj)
+        if (J[jj] < 0 || J[jj] >= de) return OR_ERR_ARG;
+    for (size_t q = 0; q < (size_t)d * nj; ++q) dW1c[q] = dW3c[q] = 0.0;
+    for (size_t q = 0; q < (size_t)nj * d; ++q) dW2r[q] = 0.0;
+    for (int r = 0; r < n; ++r) {
+        const uint16_t *xr = x + (size_t)r * d;
+        const double *dr = dout + (size_t)r * d;
+        for (int jj = 0; jj < nj; ++jj) {
+            const int j = J[jj];
+            double g = 0.0, u = 0.0, dh = 0.0;
+            for (int i = 0; i < d; ++i) {
+                const double xi = or_bf16_to_double(xr[i]);
+                g += xi * or_bf16_to_double(W1[(size_t)i * de + j]);
+                u += xi * or_bf16_to_double(W3[(size_t)i * de + j]);
+            }
+            for (int i = 0; i < d; ++i) dh += p[r] * dr[i] * or_bf16_to_double(W2[(size_t)j * d + i]);
+            const double sg = or_sigmoid(g);
+            const double h = or_round_bf16(g * sg * u);
+            const double dg = dh * u * sg * (1.0 + g * (1.0 - sg));
+            const double du = dh * g * sg;
+            for (int i = 0; i < d; ++i) {
+                const double xi = or_bf16_to_double(xr[i]);
+                dW1c[(size_t)i * nj + jj] += xi * dg;
+                dW3c[(size_t)i * nj + jj] += xi * du;
+                dW2r[(size_t)jj * d + i] += h * p[r] * dr[i];
+            }
+        }
+    }
+    return OR_OK;
+}
+
 /* Element-wise bf16 rounding of an fp64 array (test helper). */
 void or_round_bf16_array(long long n, const double *in, double *out)
 {

@@ -155,3 +155,33 @@ def test_top1_router_has_no_gradient():
     g = oracle.layer_backward(inp, shape, fwd, np.ones((shape.T, shape.d)))
     assert np.all(fwd["topk_w"] == 1.0)
     assert not g["dlogits"].any() and not g["dWg"].any() and not g["dbias"].any()
+
+
+@pytest.mark.parametrize("name", ["routed_shared", "prerouted_repeat"])
+def test_weight_grad_columns_match_autograd(name):
+    """oracle.weight_grad_columns (columns of one expert's weight gradients
+    over the rows routed to it) against torch fp64 autograd, for every expert
+    and the shared expert."""
+    shape = SHAPES[name]
+    inp = _inputs(shape)
+    fwd = oracle.layer_forward(inp, shape)
+    dout = np.random.default_rng(shape.seed + 77).standard_normal((shape.T, shape.d))
+    _, L = _torch_grads(inp, shape, fwd, dout)
+    idx, gates = fwd["topk_idx"], fwd["topk_w"]
+    J = np.array([0, shape.d_e - 1, shape.d_e // 2 + 1], np.int32)
+    for e in range(shape.E):
+        t, j = np.nonzero(idx == e)
+        if t.size == 0:
+            continue
+        dW1c, dW3c, dW2r = oracle.weight_grad_columns(inp["x"][t], dout[t], gates[t, j],
+                                                      inp["W1"][e], inp["W3"][e], inp["W2"][e], J)
+        _close(dW1c, L["W1"].grad[e][:, J].numpy(), f"dW1[{e}] columns")
+        _close(dW3c, L["W3"].grad[e][:, J].numpy(), f"dW3[{e}] columns")
+        _close(dW2r, L["W2"].grad[e][J, :].numpy(), f"dW2[{e}] rows")
+    if shape.d_shared:
+        Js = np.array([1, shape.d_shared - 2], np.int32)
+        dW1c, dW3c, dW2r = oracle.weight_grad_columns(inp["x"], dout, np.ones(shape.T),
+                                                      inp["Ws1"], inp["Ws3"], inp["Ws2"], Js)
+        _close(dW1c, L["Ws1"].grad[:, Js].numpy(), "dWs1 columns")
+        _close(dW3c, L["Ws3"].grad[:, Js].numpy(), "dWs3 columns")
+        _close(dW2r, L["Ws2"].grad[Js, :].numpy(), "dWs2 rows")
