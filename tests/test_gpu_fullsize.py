@@ -231,3 +231,92 @@ def test_full_size_layer_fp8(name):
     got = out[torch.as_tensor(toks, device=dev, dtype=torch.long)].double().cpu().numpy()
     assert_close(got, ref_out, "out (sampled tokens, e4m3)")
     assert torch.isfinite(out.float()).all()
+
+
+def _close_bwd(got, ref, what, rel_fro=1e-2, max_rel=5e-2):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(got).all(), what
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    mx = np.abs(got - ref).max()
+    assert rel <= rel_fro, f"{what}: relative Frobenius error {rel:.3e}"
+    assert mx <= max_rel * np.abs(ref).max(), f"{what}: max error {mx:.3e}"
+
+
+@pytest.mark.parametrize("name", ["default", "prerouted"])
+def test_full_size_backward(name):
+    """moe_layer_bwd at the full workload sizes, as bench.py --pass train runs
+    it.  Sampled from the oracle: dx and dgates of sampled tokens (the
+    oracle's layer backward on those tokens alone: dx of a token depends on
+    that token only), and three columns of the weight gradients of two
+    experts and of the shared expert (the oracle over every row routed to the
+    expert).  Tolerances as the small-size backward parity."""
+    import dataclasses
+
+    shape = synth.WORKLOADS[name]
+    dev = torch.device("cuda")
+    inp = synth.make_inputs(shape, device="cpu", weights_device=dev)
+    enforce_margin(inp, shape)
+    cfg = moe.config_of(shape)
+    g = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=g(inp.get("Wg")),
+                         bias=g(inp.get("bias")), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
+                         Ws2=inp.get("Ws2"))
+    x = g(inp["x"])
+    pre = bool(shape.prerouted)
+    if pre:
+        layer(x, topk_idx=g(inp["topk_idx"]), topk_w=g(inp["topk_w"]))
+    else:
+        layer(x)
+    T, k, E, d, de = shape.T, shape.k, shape.E, shape.d, shape.d_e
+    gen = torch.Generator().manual_seed(shape.seed + 1000)
+    dout = torch.randn((T, d), generator=gen).to(torch.bfloat16)
+    grads = layer.backward(x, dout.to(dev), prerouted=pre)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    for key, t in grads.items():
+        assert torch.isfinite(t.float()).all(), key
+    x_bits = bits(inp["x"])
+    dout64 = dout.double().numpy()
+    idx = layer.buffer("topk_idx", torch.int32, (T, k)).cpu().numpy() if not pre \
+        else inp["topk_idx"].numpy()
+    gates = layer.buffer("topk_w", torch.float32, (T, k)).cpu().double().numpy() if not pre \
+        else inp["topk_w"].double().numpy()
+    host = lambda key: None if inp.get(key) is None else bits(inp[key].cpu())  # noqa: E731
+    W1, W3, W2 = host("W1"), host("W3"), host("W2")
+
+    # sampled tokens: the oracle's layer backward on those tokens alone
+    rng = np.random.default_rng(11)
+    toks = np.sort(rng.choice(T, size=8, replace=False))
+    sub = dict(x=x_bits[toks], W1=W1, W3=W3, W2=W2, Wg=host("Wg"),
+               bias=None if inp.get("bias") is None else inp["bias"].numpy(),
+               Ws1=host("Ws1"), Ws3=host("Ws3"), Ws2=host("Ws2"))
+    if pre:
+        sub.update(Wg=None, topk_idx=idx[toks], topk_w=gates[toks])
+    sub_shape = dataclasses.replace(shape, T=toks.size)
+    fwd = oracle.layer_forward(sub, sub_shape)
+    if not pre:
+        assert np.array_equal(fwd["topk_idx"], idx[toks])
+    ref = oracle.layer_backward(sub, sub_shape, fwd, dout64[toks])
+    tt = torch.as_tensor(toks, device=dev, dtype=torch.long)
+    _close_bwd(grads["dx"][tt].double().cpu().numpy(), ref["dx"], "dx (sampled tokens)")
+    _close_bwd(grads["dgates"][tt].double().cpu().numpy(), ref["dgates"], "dgates (sampled)")
+
+    # three columns of the weight gradients of two experts, over all their rows
+    J = np.array([3, de // 2, de - 1], np.int32)
+    for e in (0, E - 1):
+        t, j = np.nonzero(idx == e)
+        dW1c, dW3c, dW2r = oracle.weight_grad_columns(x_bits[t], dout64[t], gates[t, j],
+                                                      W1[e], W3[e], W2[e], J)
+        Jt = torch.as_tensor(J, device=dev, dtype=torch.long)
+        _close_bwd(grads["dW1"][e][:, Jt].double().cpu().numpy(), dW1c, f"dW1[{e}] columns")
+        _close_bwd(grads["dW3"][e][:, Jt].double().cpu().numpy(), dW3c, f"dW3[{e}] columns")
+        _close_bwd(grads["dW2"][e][Jt, :].double().cpu().numpy(), dW2r, f"dW2[{e}] rows")
+    if shape.d_shared:
+        Js = np.array([5, shape.d_shared - 3], np.int32)
+        dW1c, dW3c, dW2r = oracle.weight_grad_columns(x_bits, dout64, np.ones(T), host("Ws1"),
+                                                      host("Ws3"), host("Ws2"), Js)
+        Jt = torch.as_tensor(Js, device=dev, dtype=torch.long)
+        _close_bwd(grads["dWs1"][:, Jt].double().cpu().numpy(), dW1c, "dWs1 columns")
+        _close_bwd(grads["dWs3"][:, Jt].double().cpu().numpy(), dW3c, "dWs3 columns")
+        _close_bwd(grads["dWs2"][Jt, :].double().cpu().numpy(), dW2r, "dWs2 rows")
