@@ -174,3 +174,155 @@ class EpLayerBase:
             yr[src:src + n].copy_(ye[dst:dst + n])
         ys = self._all_to_all(yr, plan.recv_rows, plan.send_rows, (d,))
         return self.finish(x, ys, tables)
+
+
+class GpuEp(EpLayerBase):
+    """The expert-parallel layer forward on the CUDA library: this rank's
+    slice of the routed experts (W1/W3 [El, d, d_e], W2 [El, d_e, d], bf16,
+    CUDA), the router and the shared expert replicated (the pages'
+    orientations, as MoeLayer).  ``cfg`` is the global config (E = all
+    experts, T = this rank's tokens per call).  Buffers are sized once: the
+    expert-major layout holds at most W * T * k rows plus W * El * P of
+    padding."""
+
+    def __init__(self, cfg, W1_local, W3_local, W2_local, Wg=None, bias=None, Ws1=None, Ws3=None,
+                 Ws2=None, group=None, stream=None):
+        import math
+
+        import torch
+
+        from . import (config_of, moe_check_config, moe_pack_experts, moe_pack_router,
+                       moe_route_splitk_scratch_size, moe_workspace_layout)
+
+        moe_check_config(cfg)
+        super().__init__(cfg.E, cfg.k, cfg.pad_multiple, group)
+        El, dev = self.El, W1_local.device
+        if W1_local.shape[0] != El:
+            raise ValueError(f"this rank holds {El} experts, got {W1_local.shape[0]}")
+        self.cfg, self.dev = cfg, dev
+        d, de, ds = cfg.d, cfg.d_e, cfg.d_shared
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.W13 = torch.empty((El, 2 * de, d), **bf)
+        self.W2_t = torch.empty((El, d, de), **bf)
+        moe_pack_experts(W1_local, W3_local, W2_local, self.W13, self.W2_t, stream)
+        self.Wg_t = None
+        if Wg is not None:
+            self.Wg_t = torch.empty((cfg.E, d), **bf)
+            moe_pack_router(Wg, self.Wg_t, stream)
+        self.bias = None if bias is None else bias.to(device=dev, dtype=torch.float32).contiguous()
+        self.Ws13 = self.Ws2_t = None
+        if ds:
+            self.Ws13 = torch.empty((1, 2 * ds, d), **bf)
+            self.Ws2_t = torch.empty((1, d, ds), **bf)
+            moe_pack_experts(Ws1.unsqueeze(0).contiguous(), Ws3.unsqueeze(0).contiguous(),
+                             Ws2.unsqueeze(0).contiguous(), self.Ws13, self.Ws2_t, stream)
+        # this rank's forward workspace over the global experts (routing,
+        # offsets, its padded layout, y, the shared expert's rows)
+        self.L = moe_workspace_layout(cfg)
+        self.ws = torch.empty(self.L["total"], dtype=torch.uint8, device=dev)
+        self.ws[:256].zero_()
+        n_split = moe_route_splitk_scratch_size(cfg) // 4
+        self.partial = self._buf("router_partial", torch.float32, (n_split,)) if n_split else None
+        # the expert-major layout of the received rows: capacity R_cap rows
+        self.R_cap = self.world * cfg.T * cfg.k + self.world * El * cfg.pad_multiple
+        self.cfg_local = config_of(T=math.ceil(self.R_cap / cfg.k), d=d, d_e=de, E=El, k=cfg.k,
+                                   pad_multiple=cfg.pad_multiple)
+        R_loc = self.cfg_local.T * cfg.k + El * (cfg.pad_multiple - 1)  # the GEMMs' row capacity
+        NB_loc = self.cfg_local.T * cfg.k // cfg.pad_multiple + El
+        self.xe = torch.zeros((R_loc, d), **bf)
+        self.ge = torch.zeros((R_loc,), dtype=torch.float32, device=dev)
+        self.he = torch.empty((R_loc, de), **bf)
+        self.ye = torch.empty((R_loc, d), **bf)
+        self.meta = torch.zeros((NB_loc, 3), dtype=torch.int32, device=dev)
+        self.nb = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.po = torch.zeros((El + 1,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def _buf(self, name, dtype, shape):
+        import torch
+
+        n = 1
+        for v in shape:
+            n *= v
+        off = self.L[name]
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def front(self, x, topk_idx=None, topk_w=None):
+        import torch
+
+        from . import moe_build_offsets, moe_permute, moe_route, moe_route_splitk
+
+        c = self.cfg
+        T, k, E, d = c.T, c.k, c.E, c.d
+        A, R = T * k, T * k + E * (c.pad_multiple - 1)
+        NB = A // c.pad_multiple + E
+        i32, f32 = torch.int32, torch.float32
+        if topk_idx is None:
+            topk_idx = self._buf("topk_idx", i32, (T, k))
+            topk_w = self._buf("topk_w", f32, (T, k))
+            if self.partial is not None:
+                moe_route_splitk(c, x, self.Wg_t, self.bias, topk_idx, topk_w, self.partial)
+            else:
+                moe_route(c, x, self.Wg_t, self.bias, topk_idx, topk_w)
+        t = dict(counts=self._buf("counts", i32, (E,)), po=self._buf("padded_offsets", i32, (E + 1,)),
+                 meta=self._buf("block_metadata", i32, (NB, 3)), nb=self._buf("num_blocks", i32, (1,)),
+                 perm_row=self._buf("perm_row", i32, (A,)), row_src=self._buf("row_src", i32, (R,)),
+                 row_gate=self._buf("row_gate", f32, (R,)))
+        moe_build_offsets(c, topk_idx, topk_w, t["counts"], t["po"], t["meta"], t["nb"],
+                          t["perm_row"], t["row_src"], t["row_gate"],
+                          self.ws[self.L["status"]:self.L["topk_idx"]])
+        x_perm = self._buf("x_perm", torch.bfloat16, (R, d))
+        moe_permute(c, x, t["perm_row"], x_perm)
+        return t["counts"], x_perm, t["row_gate"], t
+
+    def expert_major_buffers(self, rows, d, like_x, like_g):
+        if rows > self.xe.shape[0]:
+            raise RuntimeError(f"{rows} received rows exceed the capacity {self.xe.shape[0]}")
+        return self.xe, self.ge
+
+    def local_experts(self, xe, ge, plan):
+        import torch
+
+        from . import moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_skinny
+
+        nb = plan.block_metadata.shape[0]
+        if nb == 0:
+            return self.ye[:0]
+        if nb > self.meta.shape[0]:
+            raise RuntimeError("block table exceeds its capacity")
+        self.meta[:nb].copy_(torch.from_numpy(plan.block_metadata), non_blocking=False)
+        self.nb.fill_(nb)
+        self.po.copy_(torch.from_numpy(plan.padded_offsets.astype(np.int32)))
+        c = self.cfg_local
+        valid = int(plan.block_metadata[:, 2].sum())
+        if valid <= 32 * self.El:  # few rows per expert: the small-M kernel, as the layer
+            moe_grouped_gemm_swiglu_skinny(c, xe, self.W13, self.W2_t, self.meta, self.nb, ge,
+                                           self.he, self.ye, self.status)
+        else:
+            moe_grouped_gemm_swiglu(c, xe, self.W13, self.W2_t, self.meta, self.nb, self.po, ge,
+                                    self.he, self.ye, self.status)
+        return self.ye[:plan.rows]
+
+    def finish(self, x, y, t):
+        import torch
+
+        from . import moe_combine, moe_shared_expert
+
+        c = self.cfg
+        R = t["row_src"].shape[0]
+        yy = self._buf("y", torch.bfloat16, (R, c.d))
+        yy[:y.shape[0]].copy_(y)
+        ys = None
+        if c.d_shared:
+            hs = self._buf("hs", torch.bfloat16, (c.T, c.d_shared))
+            ys = self._buf("ys", torch.bfloat16, (c.T, c.d))
+            moe_shared_expert(c, x, self.Ws13, self.Ws2_t, hs, ys, self.status)
+        out = torch.empty_like(x)
+        moe_combine(c, yy, t["perm_row"], ys, out)
+        return out
+
+    def device_status(self) -> int:
+        from . import moe_get_device_status
+
+        return moe_get_device_status(self.status) | moe_get_device_status(self.ws)
