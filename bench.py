@@ -786,6 +786,107 @@ def run_train(args, shape, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ep(args, shape, rank, world, local):
+    """Expert parallelism (ep.GpuEp): rank r holds experts [r E/W, (r+1) E/W)
+    and routes its own T tokens (the workload's token rows on every rank);
+    dispatch and combine are NCCL all-to-alls.  At N = 1 the group has one
+    rank and the exchange stays on the GPU."""
+    import socket
+
+    import torch.distributed as dist
+
+    import routing_permute_grouped_gb300 as moe
+    from routing_permute_grouped_gb300 import build as moe_build
+    from routing_permute_grouped_gb300 import ep
+
+    moe_build.build()
+    moe.load()
+    if not dist.is_initialized():
+        s = socket.socket()
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+        s.close()
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.make_inputs(shape, device="cpu", weights_device=dev)
+    for key in ("x", "Wg", "bias", "topk_idx", "topk_w"):
+        if inp.get(key) is not None:
+            inp[key] = inp[key].to(dev)
+    cfg = moe.config_of(shape)
+    W = dist.get_world_size()
+    if shape.E % W:
+        raise SystemExit(f"--parallel ep needs E ({shape.E}) divisible by the ranks ({W})")
+    El = shape.E // W
+    sl = slice(dist.get_rank() * El, (dist.get_rank() + 1) * El)
+    layer = ep.GpuEp(cfg, inp["W1"][sl].contiguous(), inp["W3"][sl].contiguous(),
+                     inp["W2"][sl].contiguous(), Wg=inp.get("Wg"), bias=inp.get("bias"),
+                     Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"), Ws2=inp.get("Ws2"))
+    x = inp["x"]
+    kw = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(x, **kw)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        layer.forward(x, **kw)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms_max = reduce_max(t0.elapsed_time(t1), world)
+    assert layer.device_status() == 0
+    T, k, d, de, ds = shape.T, shape.k, shape.d, shape.d_e, shape.d_shared
+    useful = ledger.layer_useful_flops(T, k, d, de, ds)
+    value = reduce_sum(useful * args.steps, world) / (ms_max / 1e3) / 1e12
+    # e2e: token rows in from pinned host memory, the output back, every step
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    xd = torch.empty_like(x)
+    e2e_steps = max(1, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(e2e_steps):
+        xd.copy_(x_host, non_blocking=True)
+        out_host.copy_(layer.forward(xd, **kw), non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+    pk = peaks()
+    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved = useful / (ms_max / args.steps / 1e3) / 1e12
+    skinny = T * k <= 32 * shape.E
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(config_dict(shape), parallelism=f"expert parallel over {world} rank(s)"),
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": x_host.numel() * 2,
+                "d2h_bytes_per_step": x_host.numel() * 2},
+        "gpu_launches": forward_launches(shape, skinny) * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": achieved / peak_t, "peak_source": pk["source"] + " sustained bf16",
+                     "kernel": "the whole expert-parallel layer per rank (its kernels, the two "
+                               "all-to-alls, the host sync for the split sizes)",
+                     "timing": "CUDA events around the K layer calls", "traffic": None},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources."""
@@ -817,6 +918,9 @@ def main():
                     help="expert weights in bf16, or e4m3 with per-output-channel scales")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",
                     help="fwd: the layer forward; train: forward + backward per step")
+    ap.add_argument("--parallel", choices=["replicas", "ep"], default="replicas",
+                    help="replicas: every rank runs the whole layer on its tokens; ep: the "
+                         "routed experts are split over the ranks (NCCL all-to-alls)")
     ap.add_argument("--keep-gate-up", action="store_true",
                     help="train: the forward saves the gate/up values, the backward skips "
                          "recomputing them")
@@ -825,13 +929,15 @@ def main():
     shape = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, shape, rank, world)
+    elif args.parallel == "ep":
+        run_ep(args, shape, rank, world, local)
     elif args.pass_ == "train":
         run_train(args, shape, rank, world, local)
     else:
         run_ours(args, shape, rank, world, local)
-    if world > 1:
-        import torch.distributed as dist
+    import torch.distributed as dist
 
+    if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
 
 

@@ -460,6 +460,15 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
                                      const void *x, const int32_t *topk_idx, const float *topk_w,
                                      void *out, void *ws, size_t ws_bytes, void *stream);
 
+/* dst[i] = src[idx[i]] for i < n: bf16 rows of d elements (d % 8 == 0);
+ * with src_gate/dst_gate (both or neither), fp32 dst_gate[i] =
+ * src_gate[idx[i]] too; idx[i] < 0 gives a zero row (and gate).  The
+ * reorder of the expert-parallel exchange ("Dropless and grouped GEMM",
+ * sec. 14) between the senders' order and the expert-major layout.  src,
+ * idx, dst device; ranges must not overlap. */
+moe_status_t moe_gather_rows(const void *src, const int32_t *idx, void *dst, int64_t n,
+                             int32_t d, const float *src_gate, float *dst_gate, void *stream);
+
 /* out[i] = the e4m3 code q[i] widened to bf16 (exact: every e4m3 value is a
  * bf16 value); n % 16 == 0.  The e4m3 layer's first step above the small-M
  * regime. */

@@ -35,6 +35,7 @@ __all__ = [
     "MoeWeightsBwd", "MoeGrads", "moe_pack_experts_bwd", "moe_pack_router_bwd",
     "moe_backward_workspace_size", "moe_layer_bwd", "moe_gate_up_save_size", "moe_layer_fwd_save",
     "moe_widen_e4m3", "moe_grouped_gemm_swiglu_scaled", "moe_shared_expert_scaled",
+    "moe_gather_rows",
 ]
 
 MOE_OK = 0
@@ -137,6 +138,7 @@ def load():
         "moe_backward_workspace_size": (SZ, [CP]),
         "moe_gate_up_save_size": (SZ, [CP]),
         "moe_widen_e4m3": (ctypes.c_int, [P, P, ctypes.c_int64, P]),
+        "moe_gather_rows": (ctypes.c_int, [P, P, P, ctypes.c_int64, I32, P, P, P]),
         "moe_grouped_gemm_swiglu_scaled": (ctypes.c_int, [CP] + [P] * 13),
         "moe_shared_expert_scaled": (ctypes.c_int, [CP] + [P] * 9),
         "moe_layer_fwd_save": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ,
@@ -376,6 +378,12 @@ def moe_pack_router_bwd(Wg, WgP, stream=None) -> None:
 
 def moe_backward_workspace_size(cfg: MoeConfig) -> int:
     return int(load().moe_backward_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_gather_rows(src, idx, dst, src_gate=None, dst_gate=None, stream=None) -> None:
+    """dst[i] = src[idx[i]] (bf16 rows; gates too when given)."""
+    _check(load().moe_gather_rows(_ptr(src), _ptr(idx), _ptr(dst), idx.numel(), src.shape[-1],
+                                  _ptr(src_gate), _ptr(dst_gate), _stream(stream)))
 
 
 def moe_widen_e4m3(q, out, stream=None) -> None:

@@ -12,6 +12,7 @@
 #include "../../include/moe.h"
 #include "internal.h"
 #include "backward.h"
+#include "ep.h"
 
 namespace moe {
 
@@ -967,6 +968,19 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
     if (cfg->T == 0) return MOE_OK;
     return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
                       h, y, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_gather_rows(const void* src, const int32_t* idx, void* dst, int64_t n, int32_t d,
+                             const float* src_gate, float* dst_gate, void* stream) {
+    if (n < 0 || d <= 0) return fail(MOE_ERR_INVALID_ARG, "bad gather sizes");
+    if (d % 8) return fail(MOE_ERR_UNSUPPORTED, "d = %d is not a multiple of 8", d);
+    if ((src_gate == nullptr) != (dst_gate == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "src_gate and dst_gate must both be given or both be NULL");
+    if (n == 0) return MOE_OK;
+    if (!src || !idx || !dst) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    cudaError_t e = launch_gather_rows(src, idx, dst, n, d, src_gate, dst_gate,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gather rows");
 }
 
 moe_status_t moe_widen_e4m3(const void* q, void* out, int64_t n, void* stream) {

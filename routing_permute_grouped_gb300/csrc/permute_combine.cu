@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "ep.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -288,6 +289,38 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
     return launch_pdl(k_permute, dim3(grid), dim3(kPCWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm), T, nvec,
                       k);
+}
+
+// One warp per destination row: dst[i] = src[idx[i]] with 16-byte loads and
+// stores (the expert-parallel exchange's reorder between the senders' order
+// and the expert-major layout).
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_gather_rows(const uint4* __restrict__ src, const int32_t* __restrict__ idx,
+                  uint4* __restrict__ dst, int64_t n, int nvec, const float* __restrict__ sgate,
+                  float* __restrict__ dgate) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t i = blockIdx.x * static_cast<int64_t>(kPCWarps) + (threadIdx.x >> 5);
+    if (i >= n) return;
+    const int r = ld_dep(idx + i);
+    uint4* d = dst + i * nvec;
+    if (r < 0) {
+        for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+    } else {
+        const uint4* sr = src + static_cast<int64_t>(r) * nvec;
+        for (int v = lane; v < nvec; v += 32) d[v] = ld_dep(sr + v);
+    }
+    if (dgate && lane == 0) dgate[i] = r < 0 ? 0.0f : ld_dep(sgate + r);
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* idx, void* dst, int64_t n, int d,
+                               const float* sgate, float* dgate, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t grid = (n + kPCWarps - 1) / kPCWarps;
+    return launch_pdl(k_gather_rows, dim3(static_cast<unsigned>(grid)), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(src), idx, static_cast<uint4*>(dst), n, d / 8, sgate,
+                      dgate);
 }
 
 cudaError_t launch_permute_fp8(const void* x, const int32_t* perm_row, uint8_t* x8, float* x_scale,

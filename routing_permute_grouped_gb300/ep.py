@@ -49,6 +49,9 @@ class DispatchPlan:
     padded_offsets  [El + 1] of the expert-major layout
     block_metadata  [num_blocks, 3] = [local expert, m_start, valid_m]
     rows            rows of the expert-major layout (= padded_offsets[-1])
+    gather_idx      [rows]: the received row each expert-major row takes
+    return_idx      [received rows]: the expert-major row each received row
+                    returns from (the combine exchange's reorder)
     """
     send_rows: np.ndarray
     recv_rows: np.ndarray
@@ -56,6 +59,8 @@ class DispatchPlan:
     padded_offsets: np.ndarray
     block_metadata: np.ndarray
     rows: int
+    gather_idx: np.ndarray
+    return_idx: np.ndarray
 
 
 def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> DispatchPlan:
@@ -86,7 +91,13 @@ def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> Dispat
                 meta.append((e, dst + m, min(P, c - m)))
             dst += n
     block_metadata = np.array(meta, np.int32).reshape(-1, 3)
-    return DispatchPlan(send_rows, recv_rows, copies, po, block_metadata, int(po[-1]))
+    gather_idx = np.zeros(int(po[-1]), np.int32)
+    return_idx = np.zeros(int(recv_rows.sum()), np.int32)
+    for src, dst, n in copies:
+        gather_idx[dst:dst + n] = np.arange(src, src + n, dtype=np.int32)
+        return_idx[src:src + n] = np.arange(dst, dst + n, dtype=np.int32)
+    return DispatchPlan(send_rows, recv_rows, copies, po, block_metadata, int(po[-1]), gather_idx,
+                        return_idx)
 
 
 class EpLayerBase:
@@ -133,11 +144,23 @@ class EpLayerBase:
         return (torch.empty((rows, d), dtype=like_x.dtype, device=like_x.device),
                 torch.empty((rows,), dtype=like_g.dtype, device=like_g.device))
 
-    # -- the exchange -------------------------------------------------------
-    def _all_to_all(self, inp, send, recv, trailing):
+    def gather_rows(self, src, idx: np.ndarray, dst, sgate=None, dgate=None):
+        """dst[i] = src[idx[i]] (and the gates) for i < len(idx)."""
         import torch
 
-        out = torch.empty((int(sum(recv)),) + trailing, dtype=inp.dtype, device=inp.device)
+        ii = torch.as_tensor(idx.astype(np.int64), device=src.device)
+        dst[:idx.size].copy_(src.index_select(0, ii))
+        if sgate is not None:
+            dgate[:idx.size].copy_(sgate.index_select(0, ii))
+
+    # -- the exchange -------------------------------------------------------
+    def _all_to_all(self, inp, send, recv, trailing, out=None):
+        import torch
+
+        if out is None:
+            out = torch.empty((int(sum(recv)),) + trailing, dtype=inp.dtype, device=inp.device)
+        else:
+            out = out[:int(sum(recv))]
         self.dist.all_to_all_single(out, inp[:int(sum(send))].contiguous(),
                                     [int(v) for v in recv], [int(v) for v in send],
                                     group=self.group)
@@ -164,16 +187,17 @@ class EpLayerBase:
         xr = self._all_to_all(x_perm, plan.send_rows, plan.recv_rows, (d,))
         gr = self._all_to_all(row_gate, plan.send_rows, plan.recv_rows, ())
         xe, ge = self.expert_major_buffers(plan.rows, d, x_perm, row_gate)
-        for src, dst, n in plan.copies:
-            xe[dst:dst + n].copy_(xr[src:src + n])
-            ge[dst:dst + n].copy_(gr[src:src + n])
+        self.gather_rows(xr, plan.gather_idx, xe, gr, ge)
         ye = self.local_experts(xe, ge, plan)
         # combine exchange: y rows back to their senders' layout
         yr = torch.empty((int(plan.recv_rows.sum()), d), dtype=ye.dtype, device=x.device)
-        for src, dst, n in plan.copies:
-            yr[src:src + n].copy_(ye[dst:dst + n])
-        ys = self._all_to_all(yr, plan.recv_rows, plan.send_rows, (d,))
+        self.gather_rows(ye, plan.return_idx, yr)
+        ys = self._all_to_all(yr, plan.recv_rows, plan.send_rows, (d,), self.combine_buffer(tables))
         return self.finish(x, ys, tables)
+
+    def combine_buffer(self, tables):
+        """Where the returning y rows land (None: a new tensor)."""
+        return None
 
 
 class GpuEp(EpLayerBase):
@@ -281,6 +305,16 @@ class GpuEp(EpLayerBase):
             raise RuntimeError(f"{rows} received rows exceed the capacity {self.xe.shape[0]}")
         return self.xe, self.ge
 
+    def gather_rows(self, src, idx, dst, sgate=None, dgate=None):
+        import torch
+
+        from . import moe_gather_rows
+
+        if idx.size == 0:
+            return
+        ii = torch.from_numpy(idx).pin_memory().to(self.dev, non_blocking=True)
+        moe_gather_rows(src, ii, dst, sgate, dgate)
+
     def local_experts(self, xe, ge, plan):
         import torch
 
@@ -304,15 +338,20 @@ class GpuEp(EpLayerBase):
                                     self.he, self.ye, self.status)
         return self.ye[:plan.rows]
 
+    def combine_buffer(self, t):
+        import torch
+
+        return self._buf("y", torch.bfloat16, (t["row_src"].shape[0], self.cfg.d))
+
     def finish(self, x, y, t):
         import torch
 
         from . import moe_combine, moe_shared_expert
 
         c = self.cfg
-        R = t["row_src"].shape[0]
-        yy = self._buf("y", torch.bfloat16, (R, c.d))
-        yy[:y.shape[0]].copy_(y)
+        yy = self.combine_buffer(t)
+        if y.shape[0] and y.data_ptr() != yy.data_ptr():
+            yy[:y.shape[0]].copy_(y)
         ys = None
         if c.d_shared:
             hs = self._buf("hs", torch.bfloat16, (c.T, c.d_shared))
