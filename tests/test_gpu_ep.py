@@ -82,3 +82,24 @@ def test_ep_world1_matches_the_layer(name):
     _close(out_e.double().cpu().numpy(), ref["out"], "out (expert parallel)")
     if shape.T * shape.k > 32 * shape.E:  # both on the CTA-pair kernel
         assert torch.equal(out_e, out_l)
+
+
+def test_gather_rows():
+    """moe_gather_rows: dst[i] = src[idx[i]] bit for bit, gates alongside,
+    negative indices give zero rows and zero gates."""
+    g = torch.Generator().manual_seed(9)
+    src = torch.randn((300, 264), generator=g).to(torch.bfloat16).cuda()
+    sg = torch.rand(300, generator=g).cuda()
+    idx = torch.randint(-1, 300, (517,), generator=g, dtype=torch.int32)
+    dst = torch.full((517, 264), 7.0, dtype=torch.bfloat16, device="cuda")
+    dg = torch.full((517,), 7.0, device="cuda")
+    moe.moe_gather_rows(src, idx.cuda(), dst, sg, dg)
+    torch.cuda.synchronize()
+    ii = idx.long()
+    ok = ii >= 0
+    expect = torch.zeros((517, 264), dtype=torch.bfloat16)
+    expect[ok] = src.cpu()[ii[ok]]
+    assert torch.equal(dst.cpu(), expect)
+    eg = torch.zeros(517)
+    eg[ok] = sg.cpu()[ii[ok]]
+    assert torch.equal(dg.cpu(), eg)
