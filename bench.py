@@ -876,8 +876,10 @@ def run_ep(args, shape, rank, world, local):
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": x_host.numel() * 2},
-        # the layer's kernels plus the two gathers of the exchange's reorder
-        "gpu_launches": (forward_launches(shape, skinny) + 2) * args.steps,
+        # the layer's kernels (the routed GEMMs are two launches on either
+        # kernel; the shared expert always runs its own two) plus the two
+        # gathers of the exchange's reorder
+        "gpu_launches": (forward_launches(shape, False) + 2) * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                      "frac": achieved / peak_t, "peak_source": pk["source"] + " sustained bf16",
                      "kernel": "the whole expert-parallel layer per rank (its kernels, the two "
