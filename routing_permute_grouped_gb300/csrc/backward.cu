@@ -48,27 +48,44 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One thread per token: dl[t][e] (fp32, and bf16 with row stride ld16).
-__global__ void k_router_bwd(const float* __restrict__ dgates, const int32_t* __restrict__ idx,
-                             const float* __restrict__ gates, float* __restrict__ dl,
-                             __nv_bfloat16* __restrict__ dl16, int T, int E, int k, int ld16) {
+// One warp per token.  Lanes j < k hold choice j: its expert, its routing
+// weight p_j and dp_j = dgates[t][j]; s = sum_j p_j dp_j (a fixed shuffle
+// tree); then lane c writes column c of dl[t] (fp32, [T, E]) and of dl16[t]
+// (bf16, row stride ld16, zero past E): p_j (dp_j - s) summed over the j that
+// chose expert c, 0 for the others.
+__global__ void __launch_bounds__(kWarps * 32)
+    k_router_bwd(const float* __restrict__ dgates, const int32_t* __restrict__ idx,
+                 const float* __restrict__ gates, float* __restrict__ dl,
+                 __nv_bfloat16* __restrict__ dl16, int T, int E, int k, int ld16) {
     pdl_trigger();
     pdl_wait();
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x * static_cast<int64_t>(kWarps) + (threadIdx.x >> 5);
     if (t >= T) return;
-    float s = 0.0f;
-    for (int j = 0; j < k; ++j) s += ld_dep(gates + (int64_t)t * k + j) * ld_dep(dgates + (int64_t)t * k + j);
-    float* row = dl + (int64_t)t * E;
-    __nv_bfloat16* row16 = dl16 + (int64_t)t * ld16;
-    for (int e = 0; e < E; ++e) row[e] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        const int e = ld_dep(idx + (int64_t)t * k + j);
-        if (e >= 0 && e < E) {
-            const float pj = ld_dep(gates + (int64_t)t * k + j);
-            row[e] += pj * (ld_dep(dgates + (int64_t)t * k + j) - s);
-        }
+    float p = 0.0f, dp = 0.0f;
+    int ex = -1;
+    if (lane < k) {
+        p = ld_dep(gates + t * k + lane);
+        dp = ld_dep(dgates + t * k + lane);
+        ex = ld_dep(idx + t * k + lane);
     }
-    for (int e = 0; e < ld16; ++e) row16[e] = __float2bfloat16_rn(e < E ? row[e] : 0.0f);
+    const float s = warp_sum(p * dp);
+    const float gj = p * (dp - s);
+    int ej[8];
+    float vj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        ej[j] = __shfl_sync(0xFFFFFFFFu, ex, j);
+        vj[j] = __shfl_sync(0xFFFFFFFFu, gj, j);
+    }
+    for (int c = lane; c < ld16; c += 32) {
+        float v = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < k && ej[j] == c && c < E) v += vj[j];
+        if (c < E) dl[t * E + c] = v;
+        dl16[t * ld16 + c] = __float2bfloat16_rn(v);
+    }
 }
 
 // One block of 256 threads per column: thread i sums rows i, i + 256, ... in
@@ -203,11 +220,18 @@ int grid_for(int64_t work, int per_block) {
 cudaError_t launch_router_bwd(const float* dgates, const int32_t* idx, const float* gates, float* dl,
                               void* dl16, int T, int E, int k, int ld16, float* dbias,
                               cudaStream_t st) {
-    cudaError_t e = launch_pdl(k_router_bwd, dim3((T + 127) / 128), dim3(128), 0, st, dgates, idx, gates,
-                               dl, static_cast<__nv_bfloat16*>(dl16), T, E, k, ld16);
+    // Plain launches (no programmatic dependent launch): these grids are
+    // small and come right behind the weight-gradient kernel, which fills
+    // every SM.  Launched early, their CTAs would be packed onto the first
+    // SMs that free up and run there with a few SMs' share of the machine
+    // (measured: 395 us instead of 24 us at T = 8192); launched plainly they
+    // start once the SMs are free and spread over all of them.
+    k_router_bwd<<<static_cast<unsigned>((T + kWarps - 1) / kWarps), kWarps * 32, 0, st>>>(
+        dgates, idx, gates, dl, static_cast<__nv_bfloat16*>(dl16), T, E, k, ld16);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !dbias) return e;
-    return launch_pdl(k_colsum, dim3(E), dim3(256), 0, st, static_cast<const float*>(dl), dbias, T,
-                      E);
+    k_colsum<<<E, 256, 0, st>>>(static_cast<const float*>(dl), dbias, T, E);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_bwd(const void* gu, const void* dh, const int32_t* row_src,

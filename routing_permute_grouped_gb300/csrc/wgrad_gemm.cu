@@ -62,6 +62,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t chun
 }
 constexpr uint32_t kBadSegment = 0x4u;
 
+// Arrive on an mbarrier of the pair's leader CTA without release semantics,
+// for a hand-back that publishes no data: the epilogue returning an
+// accumulator whose tensor-memory reads it has completed (tcgen05.wait::ld).
+// A release arrive also waits for the thread's earlier stores to land.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 struct WTile {
     int e, mt, nt, kb0, kb1;
     bool bad;  // the segment lies outside [0, rows): skipped as empty and flagged
@@ -289,43 +298,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-#pragma unroll 1
-                for (int c = c_lo; c < c_hi; c += 64) {
+                // The warp's BN / 2 columns are read out of tensor memory and
+                // packed to bf16 pairs first, and the accumulator is handed
+                // back before any store of this tile is issued, with a
+                // relaxed arrive: the reads are complete (wait::ld) and the
+                // MMA side reads nothing this warp wrote.  A release arrive
+                // waits for the warp's earlier stores to land, which at
+                // decode sizes (a K loop of two steps per tile) paced the
+                // whole kernel at 1.7x its store-bound time.
+                uint32_t pk[BN / 4];
+                if (!empty_tile) {
+#pragma unroll
+                    for (int c = 0; c < BN / 2; c += 64) {
+                        uint32_t v[2][32];
+                        tmem_ld32(taddr + c_lo + c, v[0]);
+                        tmem_ld32(taddr + c_lo + c + 32, v[1]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pk[c / 2 + i] = pack_bf16x2(__uint_as_float(v[i >> 4][2 * (i & 15)]),
+                                                        __uint_as_float(v[i >> 4][2 * (i & 15) + 1]));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(tempty + acc), 0));
+                    acc ^= 1;
+                    if (acc == 0) aph ^= 1u;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BN / 4; ++i) pk[i] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 64) {
                     if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
                     __syncwarp();
                     uint8_t* sb = stage + buf * 4096 + lane * 128;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t v[32];
-                        if (!empty_tile) {
-                            tmem_ld32(taddr + c + half * 32, v);
-                            tmem_ld_wait();
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = 0u;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int chunk = half * 4 + j;  // 16-byte chunk of the 128-byte row
-                            const int i = 8 * j;
-                            *reinterpret_cast<uint4*>(sb + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
-                                pack_bf16x2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])),
-                                pack_bf16x2(__uint_as_float(v[i + 4]), __uint_as_float(v[i + 5])),
-                                pack_bf16x2(__uint_as_float(v[i + 6]), __uint_as_float(v[i + 7])));
-                        }
+                    for (int chunk = 0; chunk < 8; ++chunk) {  // 16-byte chunks of the 128-byte row
+                        const uint32_t* u = pk + c / 2 + 4 * chunk;
+                        *reinterpret_cast<uint4*>(sb + ((chunk ^ (lane & 7)) << 4)) =
+                            make_uint4(u[0], u[1], u[2], u[3]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && mb < args.M) {
                         // split: tile columns [0, 128) are gate, [128, 256) up
-                        const bool up = split && c >= 128;
-                        const int x = split ? w.nt * 128 + (c & 127) : col0 + c;
+                        const int cc = c_lo + c;
+                        const bool up = split && cc >= 128;
+                        const int x = split ? w.nt * 128 + (cc & 127) : col0 + cc;
                         tma_store_2d(up ? &tO2 : &tO, stage + buf * 4096, x, static_cast<int32_t>(orow));
                         bulk_commit();
                     }
                     buf ^= 1;
                 }
+                continue;  // the accumulator went back above
             }
             if (!empty_tile) {
                 tc_fence_before();
@@ -381,6 +407,7 @@ cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int
                          uint32_t* status, cudaStream_t stream, int f32_cols) {
     if (N % 128 || M % 64 || M <= 0 || rows <= 0 || f32_cols < 0 || f32_cols > N)
         return cudaErrorInvalidValue;
+    if (n_experts <= 0) return cudaErrorInvalidValue;
     const int bn = N % 256 == 0 ? 256 : 128;
     if (out2 && (bn != 256 || f32_cols)) return cudaErrorInvalidValue;  // split: 256-column tiles
     CUtensorMap tA, tB;

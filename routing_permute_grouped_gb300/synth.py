@@ -22,6 +22,10 @@ Workloads (the shapes of the pages' running examples):
   decode_e32 the decode layer's expert width with E=32, k=2, no shared
              expert: 2.8 GB of bf16 weights, every expert active; small
              enough for hardware-counter captures of the small-M kernel
+  decode_e8  the same expert shapes with E=8, k=2, T=16: a small backward
+             in the decode regime for captures of the weight-gradient kernel
+  mid_e8     T=4096, d=4096, de=1024, E=8, k=4, shared 1024: a mid-size
+             layer for captures of the backward kernels
 
 Distributions: x ~ N(0, 1); every weight ~ N(0, std = 1/sqrt(fan_in)); all
 bf16 (torch's round-to-nearest-even conversion from fp32 draws).  Each tensor
@@ -84,6 +88,10 @@ WORKLOADS = {
     "decode": MoeShape("decode", T=64, d=7168, d_e=2048, E=256, k=8, n_groups=8, topk_groups=4,
                        d_shared=2048, seed=1234 + 3),
     "decode_e32": MoeShape("decode_e32", T=64, d=7168, d_e=2048, E=32, k=2, seed=5),
+    # the decode expert shapes with 8 experts and 4 rows each: a small
+    # backward (about 2.5 GB) for counter captures of the weight-gradient
+    # kernel in the decode regime
+    "decode_e8": MoeShape("decode_e8", T=16, d=7168, d_e=2048, E=8, k=2, seed=7),
     # a mid-size layer (a few GB with its backward) for counter captures
     "mid_e8": MoeShape("mid_e8", T=4096, d=4096, d_e=1024, E=8, k=4, d_shared=1024,
                        bias_std=0.5, seed=6),
