@@ -20,10 +20,14 @@ struct WgradArgs {
     bool f32;    // fp32 output [n_experts, M, n_valid] (columns >= n_valid dropped)
     int32_t n_valid;
     uint32_t* status;
+    // null, or [n_experts]: rows of each segment that hold data; the rest of
+    // the segment is zero pad rows, and whole 64-row steps of them are skipped
+    const int32_t* valid;
 };
 cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int64_t rows,
                          const int32_t* seg, int n_experts, int dense_rows, void* out, void* out2,
-                         uint32_t* status, cudaStream_t stream, int f32_cols = 0);
+                         uint32_t* status, cudaStream_t stream, int f32_cols = 0,
+                         const int32_t* valid = nullptr);
 // dl [T, E] (fp32) and dl16 [T, ld16] (bf16, zero past E) from dgates; dbias
 // (if not null) = column sums of dl.
 cudaError_t launch_router_bwd(const float* dgates, const int32_t* idx, const float* gates, float* dl,

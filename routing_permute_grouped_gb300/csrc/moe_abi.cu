@@ -758,9 +758,11 @@ static moe_status_t layer_bwd(const moe_config_t* cfg, const moe_weights_t* w,
     MOE_BWD_CHECK("dx_perm = dgu W13");
     // routed experts, weight gradients over each expert's rows (pad rows
     // zeroed above): dW2 = (p h)^T dz, [dW1 | dW3] = x_perm^T dgu
-    e = launch_wgrad(W(B.hp), de, W(B.dz), d, s.R, po, E, 0, g->dW2, nullptr, status, st);
+    const int32_t* counts = static_cast<const int32_t*>(F(L.counts));
+    e = launch_wgrad(W(B.hp), de, W(B.dz), d, s.R, po, E, 0, g->dW2, nullptr, status, st, 0, counts);
     MOE_BWD_CHECK("dW2");
-    e = launch_wgrad(W(B.xp), d, W(B.dgu), 2 * de, s.R, po, E, 0, g->dW1, g->dW3, status, st);
+    e = launch_wgrad(W(B.xp), d, W(B.dgu), 2 * de, s.R, po, E, 0, g->dW1, g->dW3, status, st, 0,
+                     counts);
     MOE_BWD_CHECK("dW1, dW3");
     const void* dxr = nullptr;
     if (router) {

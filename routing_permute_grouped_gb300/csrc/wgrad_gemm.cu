@@ -83,8 +83,15 @@ __device__ __forceinline__ WTile wg_tile(const WgradArgs& a, int t) {
     w.mt = r % a.m_tiles;
     w.e = r / a.m_tiles;
     const int s0 = a.seg ? ld_dep(a.seg + w.e) : 0;
-    const int s1 = a.seg ? ld_dep(a.seg + w.e + 1) : a.dense_rows;
+    int s1 = a.seg ? ld_dep(a.seg + w.e + 1) : a.dense_rows;
     w.bad = s0 < 0 || s1 < s0 || s1 > a.rows;
+    if (a.seg && a.valid && !w.bad) {
+        // rows past the valid ones are zero: stop at the last 64-row step
+        // that holds data (at decode sizes that halves a tile's K loop)
+        const int v = ld_dep(a.valid + w.e);
+        w.bad = v < 0 || v > s1 - s0;
+        s1 = s0 + v;
+    }
     w.kb0 = w.bad ? 0 : s0 / kBK;
     w.kb1 = (!w.bad && s1 > s0) ? (s1 + kBK - 1) / kBK : w.kb0;
     return w;
@@ -404,7 +411,7 @@ cudaError_t launch_wg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtens
 
 cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int64_t rows,
                          const int32_t* seg, int n_experts, int dense_rows, void* out, void* out2,
-                         uint32_t* status, cudaStream_t stream, int f32_cols) {
+                         uint32_t* status, cudaStream_t stream, int f32_cols, const int32_t* valid) {
     if (N % 128 || M % 64 || M <= 0 || rows <= 0 || f32_cols < 0 || f32_cols > N)
         return cudaErrorInvalidValue;
     if (n_experts <= 0) return cudaErrorInvalidValue;
@@ -428,6 +435,7 @@ cudaError_t launch_wgrad(const void* A, int64_t M, const void* B, int64_t N, int
     a.f32 = f32_cols > 0;
     a.n_valid = f32_cols > 0 ? f32_cols : static_cast<int32_t>(N);
     a.status = status;
+    a.valid = valid;
     // bf16 outputs as [n_experts * M, ldo] maps stored in 64 x 32 boxes (the
     // fp32 output is stored per thread and needs none)
     CUtensorMap tO, tO2;
