@@ -114,9 +114,13 @@ __global__ void __launch_bounds__(256)
 // weight p.  For a row that holds assignment a: recomputes h = silu(g) u and
 // writes hp = p h (bf16, the weight-gradient operand of the down projection),
 // dgu = f'(g, u) * (p dh) and, when dgates is not null, dgates[a] = <dh, h>
-// with h rounded to bf16.  A pad row (row_src < 0) is zeroed in hp, dgu and
-// the two extra row-major buffers z0, z1 (width zw; may be null), so that the
-// weight-gradient GEMMs can reduce over whole segments.
+// with h rounded to bf16.  A pad row (row_src < 0) inside a 64-row block that
+// holds data is zeroed in hp, dgu and the two extra row-major buffers z0, z1
+// (width zw; may be null): the weight-gradient GEMMs reduce over every
+// 64-row step of a segment up to its last valid row.  Segments start on
+// 64-row boundaries and hold their valid rows first, so a block holds data
+// exactly when its first row is valid; pad rows of all-pad blocks are not
+// read by anyone and are left as they are.
 __global__ void __launch_bounds__(kWarps * 32)
     k_swiglu_bwd(const __nv_bfloat16* __restrict__ gu, const __nv_bfloat16* __restrict__ dh,
                  const int32_t* __restrict__ row_src, const float* __restrict__ row_gate,
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int64_t r = blockIdx.x * static_cast<int64_t>(kWarps) + (threadIdx.x >> 5); r < rows;
          r += nwarps) {
         const int a = row_src ? ld_dep(row_src + r) : static_cast<int>(r);
+        if (a < 0 && ld_dep(row_src + (r & ~static_cast<int64_t>(63))) < 0) continue;  // all-pad block
         if (a < 0) {
             for (int c = lane * 8; c < w; c += 256) *reinterpret_cast<uint4*>(hp + r * w + c) = zero;
             for (int c = lane * 8; c < 2 * w; c += 256)

@@ -181,6 +181,22 @@ def test_backward_needs_only_the_routing_state():
     assert layer.device_status() == 0
 
 
+@pytest.mark.parametrize("name", ["routed_shared", "groups_p64_d384", "decode_small_m", "e100"])
+def test_backward_workspace_contents_do_not_matter(name):
+    """The backward workspace filled with NaN bit patterns before a run gives
+    the same gradients bit for bit: every row a kernel reads is written
+    first in the same call (pad rows of 64-row blocks that hold data are
+    zeroed; all-pad blocks are never read)."""
+    shape, inp, dout, _, _ = prepared(name)
+    layer, x, g1 = run(shape, inp, dout)
+    layer.bws.fill_(0xFF)
+    g2 = layer.backward(x, cuda(dout))
+    torch.cuda.synchronize()
+    for key in g1:
+        assert torch.equal(g1[key], g2[key]), key
+    assert layer.device_status() == 0
+
+
 def test_frozen_router_still_differentiates_through_it():
     """dWg/dbias left NULL: dx keeps the router's term."""
     shape, inp, dout, _, ref = prepared("e100")
