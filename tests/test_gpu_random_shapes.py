@@ -8,6 +8,7 @@ CTA-pair paths run).  Each layer's forward output and backward gradients are
 compared with the oracle under the tolerances of the dedicated parity files
 (forward 5e-3 / 3e-2, backward 1e-2 / 5e-2, relative Frobenius / max over
 max|ref|); routing indices are compared bit-exactly after the margin filter.
+The same layers also run with e4m3 expert weights, forward only.
 """
 import numpy as np
 import pytest
@@ -98,3 +99,29 @@ def test_random_layer_forward_and_backward(name):
     for key in ("dx", "dW1", "dW3", "dW2", "dWs1", "dWs3", "dWs2"):
         if key in bref:
             _close(grads[key].double().cpu().numpy(), bref[key], key, 1e-2, 5e-2)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_random_layer_e4m3_forward(name):
+    """The same layers with e4m3 expert weights (the small-M kernel's 8-bit
+    MMAs below T*k = 32*E, the widened codes on the CTA-pair kernel above),
+    against the oracle's evaluation of the quantized weights."""
+    shape = SHAPES[name]
+    inp = synth.make_inputs(shape)
+    enforce_margin(inp, shape)
+    oi = oracle_inputs(inp)
+    oi.update(oracle.quantize_experts(oi))
+    if shape.d_shared:
+        oi.update(oracle.quantize_shared(oi))
+    ref = oracle.layer_forward(oi, shape)
+    cuda = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+    layer = moe.MoeLayer(moe.config_of(shape), cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]),
+                         Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")),
+                         Ws1=cuda(inp.get("Ws1")), Ws3=cuda(inp.get("Ws3")),
+                         Ws2=cuda(inp.get("Ws2")), fp8=True)
+    out = layer(cuda(inp["x"]))
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    idx = layer.buffer("topk_idx", torch.int32, (shape.T, shape.k)).cpu().numpy()
+    assert np.array_equal(idx, ref["topk_idx"])
+    _close(out.double().cpu().numpy(), ref["out"], "out (e4m3)", 5e-3, 3e-2)
