@@ -55,6 +55,26 @@ __global__ void __launch_bounds__(kScatterThreads)
         chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
+// The pad rows of every segment, [offset + count, offset + padded size):
+// row_src = -1, row_gate = 0.  A warp per expert, its lanes over the rows,
+// so that the stores are coalesced.  s_incl holds the inclusive scan of the
+// padded sizes and cnt the counts (both in shared memory, final).
+__device__ __forceinline__ void fill_pad_rows(const int* s_incl, const int* cnt, int E, int P,
+                                              int32_t* __restrict__ row_src,
+                                              float* __restrict__ row_gate) {
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    for (int e = threadIdx.x >> 5; e < E; e += nw) {
+        const int c = cnt[e];
+        const int size = ((c + P - 1) / P) * P;
+        const int po = s_incl[e] - size;
+        for (int r = po + c + lane; r < po + size; r += 32) {
+            row_src[r] = -1;
+            row_gate[r] = 0.0f;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kScanThreads)
     k_scan(int n_chunks, int E, int P, int64_t R_max, int32_t* __restrict__ chunk_counts,
            int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets,
@@ -64,6 +84,7 @@ __global__ void __launch_bounds__(kScanThreads)
     pdl_wait();
     __shared__ int s_size[kMaxE];
     __shared__ int s_nblk[kMaxE];
+    __shared__ int s_cnt[kMaxE];
     __shared__ int s_total[2];
     const int e = threadIdx.x;
     int cnt = 0;
@@ -76,6 +97,7 @@ __global__ void __launch_bounds__(kScanThreads)
         }
         s_size[e] = ((cnt + P - 1) / P) * P;  // ceil(c/P)*P, 0 for an empty expert
         s_nblk[e] = (cnt + P - 1) / P;
+        s_cnt[e] = cnt;
     }
     __syncthreads();
     // inclusive Hillis-Steele scans of sizes and block counts over E <= 256
@@ -111,12 +133,9 @@ __global__ void __launch_bounds__(kScanThreads)
             block_metadata[3 * (b0 + i) + 1] = po + i * P;
             block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
         }
-        for (int r = po + cnt; r < po + size; ++r) {
-            row_src[r] = -1;
-            row_gate[r] = 0.0f;
-        }
     }
     if (e == 0) *num_blocks = s_total[1];
+    fill_pad_rows(s_size, s_cnt, E, P, row_src, row_gate);
     for (int64_t r = s_total[0] + threadIdx.x; r < R_max; r += blockDim.x) {
         row_src[r] = -1;
         row_gate[r] = 0.0f;
@@ -249,12 +268,9 @@ __global__ void __launch_bounds__(kSmallThreads)
             block_metadata[3 * (b0 + i) + 1] = po + i * P;
             block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
         }
-        for (int r = po + cnt; r < po + size; ++r) {
-            row_src[r] = -1;
-            row_gate[r] = 0.0f;
-        }
     }
     if (tid == 0) *num_blocks = s_total[1];
+    fill_pad_rows(s_size, hist, E, P, row_src, row_gate);
     for (int64_t r = s_total[0] + tid; r < R_max; r += blockDim.x) {
         row_src[r] = -1;
         row_gate[r] = 0.0f;

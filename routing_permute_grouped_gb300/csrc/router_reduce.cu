@@ -20,6 +20,7 @@
 namespace moe {
 
 constexpr int kReduceWarps = 8;
+constexpr int kMaxSlices = 16;
 
 // (value, index) maximum over the warp; the lower index wins a tie
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
@@ -50,8 +51,17 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
         const int e = lane + 32 * i;
         l[i] = -FLT_MAX;
         if (e < E) {
+            // every slice's load issued before the first add (a loop of
+            // dependent load-add steps would pay one memory latency per
+            // slice); the sum still runs in slice order
+            float p[kMaxSlices];
+#pragma unroll
+            for (int sl = 0; sl < kMaxSlices; ++sl)
+                p[sl] = sl < S ? ld_dep(partial + (static_cast<int64_t>(sl) * T + t) * E + e) : 0.0f;
             float v = 0.0f;
-            for (int sl = 0; sl < S; ++sl) v += ld_dep(partial + (static_cast<int64_t>(sl) * T + t) * E + e);
+#pragma unroll
+            for (int sl = 0; sl < kMaxSlices; ++sl)
+                if (sl < S) v += p[sl];
             if (bias) v += ld_dep(bias + e);
             l[i] = v;
             s_logit[warp][e] = v;
@@ -121,7 +131,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
 cudaError_t launch_router_reduce(const float* partial, int S, int T, int E, int k, int n_groups,
                                  int topk_groups, const float* bias, int32_t* topk_idx,
                                  float* topk_w, cudaStream_t stream) {
-    if (E > 256 || k > 8 || (n_groups > 32)) return cudaErrorInvalidValue;
+    if (E > 256 || k > 8 || n_groups > 32 || S < 1 || S > kMaxSlices) return cudaErrorInvalidValue;
     const int grid = (T + kReduceWarps - 1) / kReduceWarps;
     return launch_pdl(k_router_reduce, dim3(grid), dim3(kReduceWarps * 32), 0, stream, partial, S, T,
                       E, k, n_groups, topk_groups, bias, topk_idx, topk_w);
