@@ -10,6 +10,9 @@
 //          the fixed order j = 0..k-1 then shared, and writes one bf16 row
 //          (sec. 6.4: fixed summation order, wide accumulation, no atomics).
 //          Bytes per token: (k + 1 [+1]) * d * 2.
+// Few tokens (decode): the rows are also split into column chunks over
+// grid.y, so that the grid still covers the SMs (8 tokens per CTA would
+// otherwise leave a 64-token batch on 8 of them).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -24,22 +27,24 @@ constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_permute(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
-              uint4* __restrict__ x_perm, int T, int nvec, int k) {
+              uint4* __restrict__ x_perm, int T, int nvec, int k, int chunk) {
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
+    const int vb = blockIdx.y * chunk;
+    const int ve = min(nvec, vb + chunk);
     int rows[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
     const uint4* src = x + (int64_t)t * nvec;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+    for (int v0 = vb + lane; v0 < ve; v0 += 32 * kUnroll) {
         uint4 buf[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int v = v0 + u * 32;
-            if (v < nvec) buf[u] = ld_dep(src + v);
+            if (v < ve) buf[u] = ld_dep(src + v);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -48,7 +53,7 @@ __global__ void __launch_bounds__(kPCWarps * 32)
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int v = v0 + u * 32;
-                if (v < nvec) dst[v] = buf[u];
+                if (v < ve) dst[v] = buf[u];
             }
         }
     }
@@ -214,18 +219,20 @@ template <int K>
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ perm_row,
               const uint4* __restrict__ shared_out, const uint4* __restrict__ extra2,
-              uint4* __restrict__ out, int T, int nvec) {
+              uint4* __restrict__ out, int T, int nvec, int chunk) {
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kPCWarps + warp;
     if (t >= T) return;
+    const int vb = blockIdx.y * chunk;
+    const int ve = min(nvec, vb + chunk);
     int rows[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) rows[j] = ld_dep(perm_row + (int64_t)t * K + j);
-    for (int v0 = lane; v0 < nvec; v0 += 64) {
+    for (int v0 = vb + lane; v0 < ve; v0 += 64) {
         const int v1 = v0 + 32;
-        const bool has1 = v1 < nvec;
+        const bool has1 = v1 < ve;
         uint4 in0[K], in1[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
@@ -282,13 +289,27 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream
     return cudaGetLastError();
 }
 
+// Column chunks (in 16-byte vectors, a multiple of 32) for a grid of
+// `rows_grid` CTAs along the tokens: one chunk (the whole row) once the
+// token CTAs alone cover the SMs twice, else enough chunks to do so.
+static int column_chunk(int rows_grid, int nvec) {
+    const int want = 2 * num_sms();
+    if (rows_grid >= want) return nvec;
+    const int split = (want + rows_grid - 1) / rows_grid;
+    int chunk = (nvec + split - 1) / split;
+    chunk = ((chunk + 31) / 32) * 32;
+    return chunk < nvec ? chunk : nvec;
+}
+
 cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,
                            int k, cudaStream_t stream) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    return launch_pdl(k_permute, dim3(grid), dim3(kPCWarps * 32), 0, stream,
+    const int chunk = column_chunk(grid, nvec);
+    const int ny = (nvec + chunk - 1) / chunk;
+    return launch_pdl(k_permute, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm), T, nvec,
-                      k);
+                      k, chunk);
 }
 
 // One warp per destination row: dst[i] = src[idx[i]] with 16-byte loads and
@@ -347,14 +368,16 @@ cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* s
                            void* out, int T, int d, int k, cudaStream_t stream, const void* extra2) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
+    const int chunk = column_chunk(grid, nvec);
+    const int ny = (nvec + chunk - 1) / chunk;
     const uint4* y4 = static_cast<const uint4*>(y);
     const uint4* s4 = static_cast<const uint4*>(shared_out);
     const uint4* x4 = static_cast<const uint4*>(extra2);
     uint4* o4 = static_cast<uint4*>(out);
     switch (k) {
-#define MOE_COMBINE_K(KK) \
-    case KK: return launch_pdl(k_combine<KK>, dim3(grid), dim3(kPCWarps * 32), 0, stream, y4, perm_row, \
-                               s4, x4, o4, T, nvec);
+#define MOE_COMBINE_K(KK)                                                                           \
+    case KK: return launch_pdl(k_combine<KK>, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream, y4, \
+                               perm_row, s4, x4, o4, T, nvec, chunk);
         MOE_COMBINE_K(1) MOE_COMBINE_K(2) MOE_COMBINE_K(3) MOE_COMBINE_K(4)
         MOE_COMBINE_K(5) MOE_COMBINE_K(6) MOE_COMBINE_K(7) MOE_COMBINE_K(8)
 #undef MOE_COMBINE_K
