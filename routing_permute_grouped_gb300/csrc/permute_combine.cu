@@ -74,14 +74,24 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Largest magnitude of a bf16 row of nvec 16-byte vectors, over the warp.
+// Largest magnitude of a bf16 row of nvec 16-byte vectors, over the warp
+// (kUnroll loads in flight per lane; absent vectors count as zeros).
 __device__ __forceinline__ float row_amax(const uint4* src, int nvec, int lane) {
     float m = 0.0f;
-    for (int v = lane; v < nvec; v += 32) {
-        float f[8];
-        bf16x8_to_f32(ld_dep(src + v), f);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 b[kUnroll];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + 32 * u;
+            b[u] = v < nvec ? ld_dep(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float f[8];
+            bf16x8_to_f32(b[u], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+        }
     }
     return warp_max(m);
 }
@@ -115,23 +125,109 @@ __global__ void __launch_bounds__(kPCWarps * 32)
     for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
     const uint4* src = x + (int64_t)t * nvec;
     const float scale = e4m3_row_scale(row_amax(src, nvec, lane));
-    for (int v = lane; v < nvec; v += 32) {
-        uint2 hi, lo;
-        split_vec(ld_dep(src + v), scale, hi, lo);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 b[kUnroll];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (rows[j] < 0) continue;
-            uint8_t* dst = x8 + (int64_t)rows[j] * 2 * d + (int64_t)v * 8;
-            *reinterpret_cast<uint2*>(dst) = hi;
-            *reinterpret_cast<uint2*>(dst + d) = lo;
-        }
-        if (xs8) {
-            uint8_t* dst = xs8 + (int64_t)t * 2 * d + (int64_t)v * 8;
-            *reinterpret_cast<uint2*>(dst) = hi;
-            *reinterpret_cast<uint2*>(dst + d) = lo;
+        for (int u = 0; u < kUnroll; ++u)
+            if (v0 + 32 * u < nvec) b[u] = ld_dep(src + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + 32 * u;
+            if (v >= nvec) break;
+            uint2 hi, lo;
+            split_vec(b[u], scale, hi, lo);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (rows[j] < 0) continue;
+                uint8_t* dst = x8 + (int64_t)rows[j] * 2 * d + (int64_t)v * 8;
+                *reinterpret_cast<uint2*>(dst) = hi;
+                *reinterpret_cast<uint2*>(dst + d) = lo;
+            }
+            if (xs8) {
+                uint8_t* dst = xs8 + (int64_t)t * 2 * d + (int64_t)v * 8;
+                *reinterpret_cast<uint2*>(dst) = hi;
+                *reinterpret_cast<uint2*>(dst + d) = lo;
+            }
         }
     }
     if (lane == 0) {
+        const float inv = 1.0f / scale;  // exact: a power of two
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (rows[j] >= 0) x_scale[rows[j]] = inv;
+        if (xs_scale) xs_scale[t] = inv;
+    }
+}
+
+// The same permute with a CTA per token (few tokens: a warp per token would
+// leave the batch on a handful of SMs).  The eight warps split the row; the
+// row's largest magnitude is reduced over them in shared memory.
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_permute_fp8_cta(const uint4* __restrict__ x, const int32_t* __restrict__ perm_row,
+                      uint8_t* __restrict__ x8, float* __restrict__ x_scale,
+                      uint8_t* __restrict__ xs8, float* __restrict__ xs_scale, int T, int d, int k) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float s_max[kPCWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x;
+    if (t >= T) return;
+    const int nvec = d / 8;
+    int rows[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rows[j] = (j < k) ? ld_dep(perm_row + (int64_t)t * k + j) : -1;
+    const uint4* src = x + (int64_t)t * nvec;
+    // this warp's vectors: v = warp * 32 + lane + 256 * i
+    constexpr int kStride = kPCWarps * 32;
+    float m = 0.0f;
+    for (int v0 = warp * 32 + lane; v0 < nvec; v0 += kStride * kUnroll) {
+        uint4 b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + kStride * u;
+            b[u] = v < nvec ? ld_dep(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float f[8];
+            bf16x8_to_f32(b[u], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(f[q]));
+        }
+    }
+    m = warp_max(m);
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    float amax = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kPCWarps; ++w) amax = fmaxf(amax, s_max[w]);
+    const float scale = e4m3_row_scale(amax);
+    for (int v0 = warp * 32 + lane; v0 < nvec; v0 += kStride * kUnroll) {
+        uint4 b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (v0 + kStride * u < nvec) b[u] = ld_dep(src + v0 + kStride * u);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + kStride * u;
+            if (v >= nvec) break;
+            uint2 hi, lo;
+            split_vec(b[u], scale, hi, lo);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (rows[j] < 0) continue;
+                uint8_t* dst = x8 + (int64_t)rows[j] * 2 * d + (int64_t)v * 8;
+                *reinterpret_cast<uint2*>(dst) = hi;
+                *reinterpret_cast<uint2*>(dst + d) = lo;
+            }
+            if (xs8) {
+                uint8_t* dst = xs8 + (int64_t)t * 2 * d + (int64_t)v * 8;
+                *reinterpret_cast<uint2*>(dst) = hi;
+                *reinterpret_cast<uint2*>(dst + d) = lo;
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
         const float inv = 1.0f / scale;  // exact: a power of two
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -179,12 +275,21 @@ __global__ void __launch_bounds__(kPCWarps * 32)
         const int64_t r = r0 + i;
         const uint4* row = src + r * nvec;
         const float scale = e4m3_row_scale(row_amax(row, nvec, lane));
-        for (int v = lane; v < nvec; v += 32) {
-            uint2 hi, lo;
-            split_vec(ld_dep(row + v), scale, hi, lo);
-            uint8_t* o = dst + r * 2 * width + (int64_t)v * 8;
-            *reinterpret_cast<uint2*>(o) = hi;
-            *reinterpret_cast<uint2*>(o + width) = lo;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+            uint4 b[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                if (v0 + 32 * u < nvec) b[u] = ld_dep(row + v0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= nvec) break;
+                uint2 hi, lo;
+                split_vec(b[u], scale, hi, lo);
+                uint8_t* o = dst + r * 2 * width + (int64_t)v * 8;
+                *reinterpret_cast<uint2*>(o) = hi;
+                *reinterpret_cast<uint2*>(o + width) = lo;
+            }
         }
         if (lane == 0) scl[r] = 1.0f / scale;
     }
@@ -348,6 +453,10 @@ cudaError_t launch_permute_fp8(const void* x, const int32_t* perm_row, uint8_t* 
                                uint8_t* xs8, float* xs_scale, int T, int d, int k,
                                cudaStream_t stream) {
     const int grid = (T + kPCWarps - 1) / kPCWarps;
+    if (grid < 2 * num_sms())  // few tokens: a CTA per token
+        return launch_pdl(k_permute_fp8_cta, dim3(T), dim3(kPCWarps * 32), 0, stream,
+                          static_cast<const uint4*>(x), perm_row, x8, x_scale, xs8, xs_scale, T, d,
+                          k);
     return launch_pdl(k_permute_fp8, dim3(grid), dim3(kPCWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), perm_row, x8, x_scale, xs8, xs_scale, T, d, k);
 }

@@ -40,6 +40,10 @@ SHAPES = {
                                bias_std=0.3, seed=93),
     "prerouted": MoeShape("prerouted", T=120, d=512, d_e=256, E=4, k=8,
                           prerouted=(400, 121, 300, 139), seed=94),
+    # enough tokens for the warp-per-token form of the e4m3 permute (fewer
+    # take a CTA per token)
+    "many_tokens": MoeShape("many_tokens", T=3000, d=640, d_e=128, E=8, k=2, d_shared=128,
+                            seed=95),
 }
 
 _cache = {}
@@ -136,8 +140,9 @@ def _pairs_ref(rows_f32: torch.Tensor):
     return hi.view(torch.uint8), lo.view(torch.uint8), (2.0 ** -sig).float()
 
 
-def test_permute_fp8_pairs_match_float8_casts():
-    shape, inp, oin, ref = prepared("full_blocks", False)
+@pytest.mark.parametrize("name", ["full_blocks", "many_tokens"])
+def test_permute_fp8_pairs_match_float8_casts(name):
+    shape, inp, oin, ref = prepared(name, False)
     cfg = moe.config_of(shape)
     x = cuda(inp["x"])
     T, d, R = shape.T, shape.d, shape.rows_capacity
