@@ -616,17 +616,17 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: b
 
 def backward_launches(shape, router_grads: bool = True, recompute: bool = True) -> int:
     """Kernels of one moe_layer_bwd call."""
-    n = 2 + 4 + 2  # permutes of dout and x; dh, gate/up, SwiGLU bwd, dx_perm; dW2, dW13
-    if not recompute:
-        n -= 1  # the gate/up values come from the forward
-    routed = not shape.prerouted
-    if (routed and router_grads) or shape.d_shared:
-        n += 1  # x transpose
-    if routed:
-        n += 2 + 1  # router backward + dbias column sums; dx from the router
-        n += 2 if router_grads else 0  # dlogit transpose, dWg
+    # permutes of dout and x; dh, SwiGLU backward, dx_perm; dW2, dW1 + dW3
+    n = 2 + 3 + 2
+    if recompute:
+        n += 1  # the gate/up values recomputed (else read from the forward's save)
+    if not shape.prerouted:
+        n += 2  # router backward; dx from the router
+        if router_grads:
+            n += 2  # dbias column sums; dWg
     if shape.d_shared:
-        n += (4 if recompute else 3) + 2  # gate/up, dh, SwiGLU bwd, dx; 2 weight gradients
+        # [gate/up,] dh, SwiGLU backward, dx; 2 weight gradients
+        n += (6 if recompute else 5)
     return n + 1  # dx combine
 
 
