@@ -830,7 +830,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             epi_pair<BN, EPI>(args, ti, taddr, q, lane, stage, &tmOut, buf);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + acc), 0));
+            // relaxed: the accumulator's reads are complete and the MMA warp
+            // reads nothing this warp wrote (a release arrive would wait for
+            // the tile's stores to land)
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(tempty + acc), 0));
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }

@@ -250,6 +250,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// The same arrive without release semantics, for a hand-back that publishes
+// no data: an epilogue returning a tensor-memory accumulator whose reads it
+// has completed (tcgen05.wait::ld) to the MMA warp.  A release arrive also
+// waits for the thread's earlier stores to land.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
 
 // 2D tiled load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may live in the peer CTA of the pair (shared::cluster

@@ -62,15 +62,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t chun
 }
 constexpr uint32_t kBadSegment = 0x4u;
 
-// Arrive on an mbarrier of the pair's leader CTA without release semantics,
-// for a hand-back that publishes no data: the epilogue returning an
-// accumulator whose tensor-memory reads it has completed (tcgen05.wait::ld).
-// A release arrive also waits for the thread's earlier stores to land.
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
 struct WTile {
     int e, mt, nt, kb0, kb1;
     bool bad;  // the segment lies outside [0, rows): skipped as empty and flagged
