@@ -789,8 +789,10 @@ def run_train(args, shape, rank, world, local):
 def run_ep(args, shape, rank, world, local):
     """Expert parallelism (ep.GpuEp): rank r holds experts [r E/W, (r+1) E/W)
     and routes its own T tokens (the workload's token rows on every rank);
-    dispatch and combine are NCCL all-to-alls.  At N = 1 the group has one
-    rank and the exchange stays on the GPU."""
+    dispatch and combine move one piece per (rank, expert): batched NCCL
+    point-to-point operations between ranks, one gather kernel for the
+    pieces a rank keeps.  At N = 1 the group has one rank and the exchange
+    is that gather in each direction."""
     import socket
 
     import torch.distributed as dist

@@ -462,10 +462,11 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
 
 /* dst[i] = src[idx[i]] for i < n: bf16 rows of d elements (d % 8 == 0);
  * with src_gate/dst_gate (both or neither), fp32 dst_gate[i] =
- * src_gate[idx[i]] too; idx[i] < 0 gives a zero row (and gate).  The
- * reorder of the expert-parallel exchange ("Dropless and grouped GEMM",
- * sec. 14) between the senders' order and the expert-major layout.  src,
- * idx, dst device; ranges must not overlap. */
+ * src_gate[idx[i]] too; idx[i] < 0 leaves row i (and its gate) as it is.
+ * The local part of the expert-parallel exchange ("Dropless and grouped
+ * GEMM", sec. 14): the row pieces a rank keeps move between its senders'
+ * layout and its expert-major layout here, the others arrive from its
+ * peers.  src, idx, dst device; ranges must not overlap. */
 moe_status_t moe_gather_rows(const void *src, const int32_t *idx, void *dst, int64_t n,
                              int32_t d, const float *src_gate, float *dst_gate, void *stream);
 

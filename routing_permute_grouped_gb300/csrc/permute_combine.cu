@@ -418,8 +418,9 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
 }
 
 // One warp per destination row: dst[i] = src[idx[i]] with 16-byte loads and
-// stores (the expert-parallel exchange's reorder between the senders' order
-// and the expert-major layout).
+// stores; a negative idx[i] leaves row i untouched (the expert-parallel
+// exchange: the rows a rank keeps are gathered here, the others arrive from
+// its peers).
 __global__ void __launch_bounds__(kPCWarps * 32)
     k_gather_rows(const uint4* __restrict__ src, const int32_t* __restrict__ idx,
                   uint4* __restrict__ dst, int64_t n, int nvec, const float* __restrict__ sgate,
@@ -430,14 +431,11 @@ __global__ void __launch_bounds__(kPCWarps * 32)
     const int64_t i = blockIdx.x * static_cast<int64_t>(kPCWarps) + (threadIdx.x >> 5);
     if (i >= n) return;
     const int r = ld_dep(idx + i);
+    if (r < 0) return;  // a row that another path fills: left as it is
     uint4* d = dst + i * nvec;
-    if (r < 0) {
-        for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
-    } else {
-        const uint4* sr = src + static_cast<int64_t>(r) * nvec;
-        for (int v = lane; v < nvec; v += 32) d[v] = ld_dep(sr + v);
-    }
-    if (dgate && lane == 0) dgate[i] = r < 0 ? 0.0f : ld_dep(sgate + r);
+    const uint4* sr = src + static_cast<int64_t>(r) * nvec;
+    for (int v = lane; v < nvec; v += 32) d[v] = ld_dep(sr + v);
+    if (dgate && lane == 0) dgate[i] = ld_dep(sgate + r);
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* idx, void* dst, int64_t n, int d,

@@ -6,21 +6,23 @@ a copy of the router and of the shared expert.  One layer forward:
   1. each rank routes its own tokens and permutes them into the padded
      expert-major layout over all E experts (the single-GPU stages);
   2. the per-expert counts are exchanged, then each rank sends rank r' the
-     contiguous rows of r''s experts, padded segments included, with their
-     routing weights ("Dropless and grouped GEMM", sec. 14: the dispatch
-     all-to-all, whose landing write does the permute and the padding);
-  3. the receiver lays the W senders' pieces of each local expert out as one
-     padded segment per expert (pieces in rank order: every piece is a
-     multiple of P rows, so the concatenation is again a padded segment) and
-     runs the grouped GEMMs on them with a block table built from the counts;
-  4. the rows of y go back into the senders' layout (the combine all-to-all)
-     and each rank combines its tokens with its shared expert's rows, as the
-     single-GPU layer does.
+     padded segment of each of r''s experts, one piece per expert, with
+     their routing weights ("Dropless and grouped GEMM", sec. 14: the
+     dispatch, whose landing write does the permute and the padding);
+  3. the pieces land straight in the receiver's expert-major layout: the W
+     senders' pieces of each local expert, in rank order, make one padded
+     segment (every piece is a multiple of P rows, so the concatenation is
+     again a padded segment), and the grouped GEMMs run on them with a
+     block table built from the counts;
+  4. the rows of y go back, piece by piece, into the senders' layout (the
+     combine exchange) and each rank combines its tokens with its shared
+     expert's rows, as the single-GPU layer does.
 
-The summation order of the combine is the single-GPU one, so a token's
-output does not depend on W.  NCCL's all-to-all takes its split sizes on the
-host: the per-expert counts cross to the host once per layer (a few hundred
-bytes).  The plan functions below are plain host logic over those counts;
+Pieces between ranks travel as batched point-to-point sends and receives
+(NCCL between GPUs); the pieces a rank keeps move in one gather.  The
+summation order of the combine is the single-GPU one, so a token's output
+does not depend on W.  The piece sizes are needed on the host: the
+per-expert counts cross to the host once per layer (a few hundred bytes).  The plan functions below are plain host logic over those counts;
 the compute steps go through a backend object (the CUDA library in
 ``GpuEp``), so the exchange logic can be exercised on CPU process groups.
 """
@@ -43,24 +45,23 @@ class DispatchPlan:
 
     send_rows[r']   rows this rank sends to rank r' (padded, r''s experts)
     recv_rows[s]    rows this rank receives from rank s
-    copies          (src_row, dst_row, rows): the received (source-major)
-                    buffer into the expert-major layout, one per non-empty
-                    (source, local expert) piece
     padded_offsets  [El + 1] of the expert-major layout
     block_metadata  [num_blocks, 3] = [local expert, m_start, valid_m]
     rows            rows of the expert-major layout (= padded_offsets[-1])
-    gather_idx      [rows]: the received row each expert-major row takes
-    return_idx      [received rows]: the expert-major row each received row
-                    returns from (the combine exchange's reorder)
+    send_pieces     (peer, row, rows): this rank's padded segments in its own
+                    layout, one per expert with rows, peers in order and each
+                    peer's experts in order (the dispatch's sends)
+    recv_pieces     (peer, row, rows): where each arriving piece lands in the
+                    expert-major layout; for every peer in the order that
+                    peer sends them
     """
     send_rows: np.ndarray
     recv_rows: np.ndarray
-    copies: list
     padded_offsets: np.ndarray
     block_metadata: np.ndarray
     rows: int
-    gather_idx: np.ndarray
-    return_idx: np.ndarray
+    send_pieces: list
+    recv_pieces: list
 
 
 def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> DispatchPlan:
@@ -74,37 +75,34 @@ def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> Dispat
     send_rows = padded(counts, P).reshape(W, El).sum(axis=1)
     pieces = padded(recv_counts, P)                      # [W, El]
     recv_rows = pieces.sum(axis=1)
-    src_start = np.concatenate([[0], np.cumsum(recv_rows)[:-1]])
     seg_rows = pieces.sum(axis=0)                        # per local expert
     po = np.concatenate([[0], np.cumsum(seg_rows)]).astype(np.int32)
-    copies, meta = [], []
+    meta, recv_pieces = [], []
     for e in range(El):
         dst = int(po[e])
         for s in range(W):
             n = int(pieces[s, e])
             if n == 0:
                 continue
-            src = int(src_start[s] + pieces[s, :e].sum())
-            copies.append((src, dst, n))
+            recv_pieces.append((s, dst, n))
             c = int(recv_counts[s, e])
             for m in range(0, c, P):
                 meta.append((e, dst + m, min(P, c - m)))
             dst += n
+    own = padded(counts, P)
+    own_po = np.concatenate([[0], np.cumsum(own)])
+    send_pieces = [(g // El, int(own_po[g]), int(own[g])) for g in range(W * El) if own[g]]
     block_metadata = np.array(meta, np.int32).reshape(-1, 3)
-    gather_idx = np.zeros(int(po[-1]), np.int32)
-    return_idx = np.zeros(int(recv_rows.sum()), np.int32)
-    for src, dst, n in copies:
-        gather_idx[dst:dst + n] = np.arange(src, src + n, dtype=np.int32)
-        return_idx[src:src + n] = np.arange(dst, dst + n, dtype=np.int32)
-    return DispatchPlan(send_rows, recv_rows, copies, po, block_metadata, int(po[-1]), gather_idx,
-                        return_idx)
+    return DispatchPlan(send_rows, recv_rows, po, block_metadata, int(po[-1]), send_pieces,
+                        recv_pieces)
 
 
 class EpLayerBase:
     """The exchange of an expert-parallel layer forward over a process group;
     subclasses supply the compute steps (``front``, ``local_experts``,
-    ``finish``) and the tensors' device.  Data moves with
-    torch.distributed.all_to_all_single (NCCL between GPUs)."""
+    ``finish``) and the tensors' device.  Row pieces move with
+    torch.distributed's batched point-to-point operations (NCCL between
+    GPUs), the per-expert counts with one all_to_all_single."""
 
     def __init__(self, E: int, k: int, P: int, group=None):
         import torch.distributed as dist
@@ -145,26 +143,49 @@ class EpLayerBase:
                 torch.empty((rows,), dtype=like_g.dtype, device=like_g.device))
 
     def gather_rows(self, src, idx: np.ndarray, dst, sgate=None, dgate=None):
-        """dst[i] = src[idx[i]] (and the gates) for i < len(idx)."""
+        """dst[i] = src[idx[i]] (and the gates) for the i < len(idx) with
+        idx[i] >= 0; the other rows are left as they are."""
         import torch
 
-        ii = torch.as_tensor(idx.astype(np.int64), device=src.device)
-        dst[:idx.size].copy_(src.index_select(0, ii))
+        keep = np.flatnonzero(idx >= 0)
+        di = torch.as_tensor(keep, device=src.device)
+        si = torch.as_tensor(idx[keep].astype(np.int64), device=src.device)
+        dst.index_copy_(0, di, src.index_select(0, si))
         if sgate is not None:
-            dgate[:idx.size].copy_(sgate.index_select(0, ii))
+            dgate.index_copy_(0, di, sgate.index_select(0, si))
 
     # -- the exchange -------------------------------------------------------
-    def _all_to_all(self, inp, send, recv, trailing, out=None):
-        import torch
-
-        if out is None:
-            out = torch.empty((int(sum(recv)),) + trailing, dtype=inp.dtype, device=inp.device)
-        else:
-            out = out[:int(sum(recv))]
-        self.dist.all_to_all_single(out, inp[:int(sum(send))].contiguous(),
-                                    [int(v) for v in recv], [int(v) for v in send],
-                                    group=self.group)
-        return out
+    def _exchange(self, src, dst, sends, recvs, sgate=None, dgate=None):
+        """Moves row pieces of src to the peers (sends: (peer, row, rows)) and
+        lands the peers' pieces in dst (recvs: (peer, row, rows)), the gates
+        alongside.  Per pair of ranks the pieces pair up in list order.  The
+        pieces between this rank and itself are one gather; the others go
+        through batched point-to-point operations."""
+        own_s = [(r, n) for p, r, n in sends if p == self.rank]
+        own_r = [(r, n) for p, r, n in recvs if p == self.rank]
+        if own_s:
+            rows = max(r + n for r, n in own_r)
+            idx = np.full(rows, -1, np.int32)
+            for (rs, n), (rd, n2) in zip(own_s, own_r):
+                if n != n2:
+                    raise RuntimeError("mismatched local pieces")
+                idx[rd:rd + n] = np.arange(rs, rs + n, dtype=np.int32)
+            self.gather_rows(src, idx, dst, sgate, dgate)
+        ops = []
+        P2POp, dist = self.dist.P2POp, self.dist
+        for p, r, n in sends:
+            if p != self.rank:
+                ops.append(P2POp(dist.isend, src[r:r + n], p, self.group))
+                if sgate is not None:
+                    ops.append(P2POp(dist.isend, sgate[r:r + n], p, self.group))
+        for p, r, n in recvs:
+            if p != self.rank:
+                ops.append(P2POp(dist.irecv, dst[r:r + n], p, self.group))
+                if dgate is not None:
+                    ops.append(P2POp(dist.irecv, dgate[r:r + n], p, self.group))
+        if ops:
+            for req in dist.batch_isend_irecv(ops):
+                req.wait()
 
     def exchange_counts(self, counts_host: np.ndarray, device) -> np.ndarray:
         """[W, El]: what every rank routes to this rank's experts."""
@@ -183,16 +204,16 @@ class EpLayerBase:
         recv_counts = self.exchange_counts(counts_host, x.device)
         plan = plan_dispatch(counts_host, recv_counts, self.P)
         d = x_perm.shape[1]
-        # dispatch: token rows and their routing weights
-        xr = self._all_to_all(x_perm, plan.send_rows, plan.recv_rows, (d,))
-        gr = self._all_to_all(row_gate, plan.send_rows, plan.recv_rows, ())
+        # dispatch: token rows and their routing weights, piece by piece,
+        # straight into the expert-major layout
         xe, ge = self.expert_major_buffers(plan.rows, d, x_perm, row_gate)
-        self.gather_rows(xr, plan.gather_idx, xe, gr, ge)
+        self._exchange(x_perm, xe, plan.send_pieces, plan.recv_pieces, row_gate, ge)
         ye = self.local_experts(xe, ge, plan)
-        # combine exchange: y rows back to their senders' layout
-        yr = torch.empty((int(plan.recv_rows.sum()), d), dtype=ye.dtype, device=x.device)
-        self.gather_rows(ye, plan.return_idx, yr)
-        ys = self._all_to_all(yr, plan.recv_rows, plan.send_rows, (d,), self.combine_buffer(tables))
+        # combine exchange: the y pieces back into their senders' layout
+        ys = self.combine_buffer(tables)
+        if ys is None:
+            ys = torch.empty((int(plan.send_rows.sum()), d), dtype=ye.dtype, device=x.device)
+        self._exchange(ye, ys, plan.recv_pieces, plan.send_pieces)
         return self.finish(x, ys, tables)
 
     def combine_buffer(self, tables):

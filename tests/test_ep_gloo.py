@@ -1,8 +1,8 @@
 """Expert parallelism (routing_permute_grouped_gb300/ep.py) on CPU process
 groups.
 
-The exchange logic (split sizes, the receiver's expert-major layout and block
-table, the two all-to-alls) runs with world size 2 over gloo, with the
+The exchange logic (piece sizes, the receiver's expert-major layout and block
+table, the two piece-by-piece exchanges) runs with world size 2 over gloo, with the
 oracle as the compute backend on each rank: rank r holds experts
 [r*E/2, (r+1)*E/2) and its own half of the tokens.  Every rank's output must
 equal, bit for bit, the single-process oracle's output for the same tokens:
@@ -32,8 +32,12 @@ def test_plan_dispatch_worked_example():
     assert plan.recv_rows.tolist() == [12, 4]
     assert plan.padded_offsets.tolist() == [0, 8, 16]
     assert plan.rows == 16
-    assert plan.copies == [(0, 0, 4), (12, 4, 4), (4, 8, 8)]
     assert plan.block_metadata.tolist() == [[0, 0, 2], [0, 4, 4], [1, 8, 4], [1, 12, 3]]
+    # this rank's padded segments (8, 0, 4, 12 rows) go out one per expert:
+    # experts 0, 1 to rank 0, experts 2, 3 to rank 1
+    assert plan.send_pieces == [(0, 0, 8), (1, 8, 4), (1, 12, 12)]
+    # arriving pieces land expert-major, senders in rank order within an expert
+    assert plan.recv_pieces == [(0, 0, 4), (1, 4, 4), (0, 8, 8)]
 
 
 def test_plan_dispatch_conserves_rows():
@@ -45,15 +49,14 @@ def test_plan_dispatch_conserves_rows():
     assert plan.send_rows.sum() == ep.padded(counts, P).sum()
     assert plan.rows == plan.recv_rows.sum() == ep.padded(recv, P).sum()
     assert plan.block_metadata[:, 2].sum() == recv.sum()
-    # the copies tile both layouts exactly once
-    src = sorted((s, n) for s, _, n in plan.copies)
-    dst = sorted((d, n) for _, d, n in plan.copies)
-    for spans in (src, dst):
+    # the arriving pieces tile the expert-major layout exactly once, and the
+    # sent pieces tile this rank's own padded layout
+    for pieces, total in ((plan.recv_pieces, plan.rows), (plan.send_pieces, plan.send_rows.sum())):
         pos = 0
-        for start, n in spans:
+        for _, start, n in sorted(pieces, key=lambda p: p[1]):
             assert start == pos
             pos += n
-        assert pos == plan.rows
+        assert pos == total
     assert (plan.padded_offsets % P == 0).all()
 
 

@@ -85,8 +85,8 @@ def test_ep_world1_matches_the_layer(name):
 
 
 def test_gather_rows():
-    """moe_gather_rows: dst[i] = src[idx[i]] bit for bit, gates alongside,
-    negative indices give zero rows and zero gates."""
+    """moe_gather_rows: dst[i] = src[idx[i]] bit for bit, gates alongside;
+    a negative index leaves the row and its gate as they were."""
     g = torch.Generator().manual_seed(9)
     src = torch.randn((300, 264), generator=g).to(torch.bfloat16).cuda()
     sg = torch.rand(300, generator=g).cuda()
@@ -97,9 +97,9 @@ def test_gather_rows():
     torch.cuda.synchronize()
     ii = idx.long()
     ok = ii >= 0
-    expect = torch.zeros((517, 264), dtype=torch.bfloat16)
+    expect = torch.full((517, 264), 7.0, dtype=torch.bfloat16)
     expect[ok] = src.cpu()[ii[ok]]
     assert torch.equal(dst.cpu(), expect)
-    eg = torch.zeros(517)
+    eg = torch.full((517,), 7.0)
     eg[ok] = sg.cpu()[ii[ok]]
     assert torch.equal(dg.cpu(), eg)
