@@ -77,22 +77,22 @@ def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> Dispat
     recv_rows = pieces.sum(axis=1)
     seg_rows = pieces.sum(axis=0)                        # per local expert
     po = np.concatenate([[0], np.cumsum(seg_rows)]).astype(np.int32)
-    meta, recv_pieces = [], []
-    for e in range(El):
-        dst = int(po[e])
-        for s in range(W):
-            n = int(pieces[s, e])
-            if n == 0:
-                continue
-            recv_pieces.append((s, dst, n))
-            c = int(recv_counts[s, e])
-            for m in range(0, c, P):
-                meta.append((e, dst + m, min(P, c - m)))
-            dst += n
+    # arriving pieces: expert-major, senders in rank order within an expert
+    n = pieces.T                                         # [El, W]
+    dst = po[:-1, None].astype(np.int64) + np.cumsum(n, axis=1) - n
+    ee, ss = np.nonzero(n)                               # row-major: e outer, s inner
+    recv_pieces = list(zip(ss.tolist(), dst[ee, ss].tolist(), n[ee, ss].tolist()))
+    # the block table: a piece of c rows holds ceil(c / P) blocks of P rows
+    c = recv_counts.T[ee, ss]
+    nblk = -(-c // P)
+    first = np.repeat(np.cumsum(nblk) - nblk, nblk)
+    m = (np.arange(int(nblk.sum())) - first) * P
+    block_metadata = np.stack([np.repeat(ee, nblk), np.repeat(dst[ee, ss], nblk) + m,
+                               np.minimum(P, np.repeat(c, nblk) - m)], axis=1).astype(np.int32)
     own = padded(counts, P)
     own_po = np.concatenate([[0], np.cumsum(own)])
-    send_pieces = [(g // El, int(own_po[g]), int(own[g])) for g in range(W * El) if own[g]]
-    block_metadata = np.array(meta, np.int32).reshape(-1, 3)
+    g = np.flatnonzero(own)
+    send_pieces = list(zip((g // El).tolist(), own_po[g].tolist(), own[g].tolist()))
     return DispatchPlan(send_rows, recv_rows, po, block_metadata, int(po[-1]), send_pieces,
                         recv_pieces)
 
@@ -164,12 +164,13 @@ class EpLayerBase:
         own_s = [(r, n) for p, r, n in sends if p == self.rank]
         own_r = [(r, n) for p, r, n in recvs if p == self.rank]
         if own_s:
-            rows = max(r + n for r, n in own_r)
-            idx = np.full(rows, -1, np.int32)
-            for (rs, n), (rd, n2) in zip(own_s, own_r):
-                if n != n2:
-                    raise RuntimeError("mismatched local pieces")
-                idx[rd:rd + n] = np.arange(rs, rs + n, dtype=np.int32)
+            rs, ns = np.array(own_s, np.int64).T
+            rd, nd = np.array(own_r, np.int64).T
+            if not np.array_equal(ns, nd):
+                raise RuntimeError("mismatched local pieces")
+            idx = np.full(int((rd + nd).max()), -1, np.int32)
+            step = np.arange(int(ns.sum())) - np.repeat(np.cumsum(ns) - ns, ns)
+            idx[np.repeat(rd, ns) + step] = np.repeat(rs, ns) + step
             self.gather_rows(src, idx, dst, sgate, dgate)
         ops = []
         P2POp, dist = self.dist.P2POp, self.dist
@@ -282,6 +283,7 @@ class GpuEp(EpLayerBase):
         self.nb = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.po = torch.zeros((El + 1,), dtype=torch.int32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self._staging = {}
 
     def _buf(self, name, dtype, shape):
         import torch
@@ -326,15 +328,34 @@ class GpuEp(EpLayerBase):
             raise RuntimeError(f"{rows} received rows exceed the capacity {self.xe.shape[0]}")
         return self.xe, self.ge
 
-    def gather_rows(self, src, idx, dst, sgate=None, dgate=None):
+    def _stage(self, slot: str, a: np.ndarray, out=None):
+        """The int32 host array ``a`` on the device (in ``out``, or in the
+        slot's own device buffer), through the slot's pinned staging buffer;
+        the buffer is reused once its previous copy has finished."""
         import torch
 
+        st = self._staging.get(slot)
+        if st is None or st[0].numel() < a.size:
+            n = max(2 * a.size, 1024)
+            st = (torch.empty(n, dtype=torch.int32).pin_memory(),
+                  torch.empty(n, dtype=torch.int32, device=self.dev), torch.cuda.Event())
+            self._staging[slot] = st
+        else:
+            st[2].synchronize()
+        host, dev, ev = st
+        host[:a.size].numpy()[:] = a.reshape(-1)
+        dst = dev[:a.size] if out is None else out.view(-1)[:a.size]
+        dst.copy_(host[:a.size], non_blocking=True)
+        ev.record()
+        return dst
+
+    def gather_rows(self, src, idx, dst, sgate=None, dgate=None):
         from . import moe_gather_rows
 
         if idx.size == 0:
             return
-        ii = torch.from_numpy(idx).pin_memory().to(self.dev, non_blocking=True)
-        moe_gather_rows(src, ii, dst, sgate, dgate)
+        slot = "idx_x" if sgate is not None else "idx_y"
+        moe_gather_rows(src, self._stage(slot, idx), dst, sgate, dgate)
 
     def local_experts(self, xe, ge, plan):
         import torch
@@ -346,9 +367,9 @@ class GpuEp(EpLayerBase):
             return self.ye[:0]
         if nb > self.meta.shape[0]:
             raise RuntimeError("block table exceeds its capacity")
-        self.meta[:nb].copy_(torch.from_numpy(plan.block_metadata), non_blocking=False)
+        self._stage("meta", plan.block_metadata, self.meta)
         self.nb.fill_(nb)
-        self.po.copy_(torch.from_numpy(plan.padded_offsets.astype(np.int32)))
+        self._stage("po", plan.padded_offsets.astype(np.int32), self.po)
         c = self.cfg_local
         valid = int(plan.block_metadata[:, 2].sum())
         if valid <= 32 * self.El:  # few rows per expert: the small-M kernel, as the layer
