@@ -155,10 +155,11 @@ def _packed_rows(de):
     return (r % 256 >= 128).astype(np.int64), (r // 256) * 128 + r % 128
 
 
-@pytest.mark.parametrize("name", ["decode"])
+@pytest.mark.parametrize("name", ["decode", "default"])
 def test_full_size_layer_fp8(name):
-    """The e4m3-weight layer at the full decode size, in the bench's launch
-    configuration: routing and tables bit-exact, the packed codes and scales of
+    """The e4m3-weight layer at the full decode size (8-bit MMAs on the small-M
+    kernel) and the full default size (the codes widened to bf16 for the
+    CTA-pair kernel), in the bench's launch configuration: routing and tables bit-exact, the packed codes and scales of
     the sampled experts bit-exact against the oracle's quantizer, sampled h, y
     and token outputs within the tolerances against the oracle evaluating the
     dequantized weights."""
