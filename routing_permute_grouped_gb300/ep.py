@@ -284,6 +284,10 @@ class GpuEp(EpLayerBase):
         self.po = torch.zeros((El + 1,), dtype=torch.int32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self._staging = {}
+        # the shared expert needs only x: it runs on a side stream while the
+        # routing, the exchange (and its host syncs) and the routed experts run
+        self.s_shared = torch.cuda.Stream(device=dev)
+        self.ev_shared = torch.cuda.Event()
 
     def _buf(self, name, dtype, shape):
         import torch
@@ -300,11 +304,19 @@ class GpuEp(EpLayerBase):
 
         from . import moe_build_offsets, moe_permute, moe_route, moe_route_splitk
 
+        from . import moe_shared_expert
+
         c = self.cfg
         T, k, E, d = c.T, c.k, c.E, c.d
         A, R = T * k, T * k + E * (c.pad_multiple - 1)
         NB = A // c.pad_multiple + E
         i32, f32 = torch.int32, torch.float32
+        if c.d_shared:
+            self.s_shared.wait_stream(torch.cuda.current_stream(self.dev))
+            hs = self._buf("hs", torch.bfloat16, (T, c.d_shared))
+            ys = self._buf("ys", torch.bfloat16, (T, d))
+            moe_shared_expert(c, x, self.Ws13, self.Ws2_t, hs, ys, self.status, stream=self.s_shared)
+            self.ev_shared.record(self.s_shared)
         if topk_idx is None:
             topk_idx = self._buf("topk_idx", i32, (T, k))
             topk_w = self._buf("topk_w", f32, (T, k))
@@ -388,17 +400,16 @@ class GpuEp(EpLayerBase):
     def finish(self, x, y, t):
         import torch
 
-        from . import moe_combine, moe_shared_expert
+        from . import moe_combine
 
         c = self.cfg
         yy = self.combine_buffer(t)
         if y.shape[0] and y.data_ptr() != yy.data_ptr():
             yy[:y.shape[0]].copy_(y)
         ys = None
-        if c.d_shared:
-            hs = self._buf("hs", torch.bfloat16, (c.T, c.d_shared))
+        if c.d_shared:  # computed on the side stream since front()
+            torch.cuda.current_stream(self.dev).wait_event(self.ev_shared)
             ys = self._buf("ys", torch.bfloat16, (c.T, c.d))
-            moe_shared_expert(c, x, self.Ws13, self.Ws2_t, hs, ys, self.status)
         out = torch.empty_like(x)
         moe_combine(c, yy, t["perm_row"], ys, out)
         return out
