@@ -8,7 +8,8 @@ CTA-pair paths run).  Each layer's forward output and backward gradients are
 compared with the oracle under the tolerances of the dedicated parity files
 (forward 5e-3 / 3e-2, backward 1e-2 / 5e-2, relative Frobenius / max over
 max|ref|); routing indices are compared bit-exactly after the margin filter.
-The same layers also run with e4m3 expert weights, forward only.
+The same layers also run with e4m3 expert weights (forward) and with the
+gate/up values kept from the forward (backward).
 """
 import numpy as np
 import pytest
@@ -125,3 +126,39 @@ def test_random_layer_e4m3_forward(name):
     idx = layer.buffer("topk_idx", torch.int32, (shape.T, shape.k)).cpu().numpy()
     assert np.array_equal(idx, ref["topk_idx"])
     _close(out.double().cpu().numpy(), ref["out"], "out (e4m3)", 5e-3, 3e-2)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_random_layer_backward_with_saved_gate_up(name):
+    """The same layers with the gate/up values kept from the forward
+    (keep_gate_up): the gradients equal the recomputing layer's bit for bit
+    where the forward ran the CTA-pair kernel, and stay within the backward
+    tolerances of the oracle where it ran the small-M kernel."""
+    shape = SHAPES[name]
+    inp = synth.make_inputs(shape)
+    enforce_margin(inp, shape)
+    cuda = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+    g = torch.Generator().manual_seed(shape.seed + 1000)
+    dout = torch.randn((shape.T, shape.d), generator=g).to(torch.bfloat16)
+    kw = dict(Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")), Ws1=cuda(inp.get("Ws1")),
+              Ws3=cuda(inp.get("Ws3")), Ws2=cuda(inp.get("Ws2")))
+    cfg = moe.config_of(shape)
+    W = [cuda(inp[n]) for n in ("W1", "W3", "W2")]
+    plain = moe.MoeLayer(cfg, *W, **kw)
+    keep = moe.MoeLayer(cfg, *W, keep_gate_up=True, **kw)
+    x, dz = cuda(inp["x"]), cuda(dout)
+    out_p, out_k = plain(x), keep(x)
+    g_p, g_k = plain.backward(x, dz), keep.backward(x, dz)
+    torch.cuda.synchronize()
+    assert keep.device_status() == 0
+    assert torch.equal(out_p, out_k)
+    if shape.T * shape.k > 32 * shape.E:
+        for key in g_p:
+            assert torch.equal(g_p[key], g_k[key]), key
+        return
+    oi = oracle_inputs(inp)
+    ref = oracle.layer_forward(oi, shape)
+    bref = oracle.layer_backward(oi, shape, ref, dout.double().numpy())
+    for key in ("dx", "dW1", "dW3", "dW2", "dWs1", "dWs3", "dWs2"):
+        if key in bref:
+            _close(g_k[key].double().cpu().numpy(), bref[key], key, 1e-2, 5e-2)
