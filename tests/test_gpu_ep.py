@@ -103,3 +103,35 @@ def test_gather_rows():
     eg = torch.full((517,), 7.0)
     eg[ok] = sg.cpu()[ii[ok]]
     assert torch.equal(dg.cpu(), eg)
+
+
+def _random_shapes():
+    from tests.test_gpu_random_shapes import SHAPES as RANDOM
+
+    return {k: v for k, v in RANDOM.items() if k in ("r0", "r2", "r3", "r6", "r7", "r11")}
+
+
+@pytest.mark.parametrize("name", list(_random_shapes()))
+def test_ep_world1_random_layers(name):
+    """Seeded random layers (E from 2 to 64, shared expert or not, both GEMM
+    paths) through the piece-by-piece exchange at world size 1: bit-identical
+    to MoeLayer where both run the CTA-pair kernel, within the parity bound
+    of the oracle everywhere."""
+    shape = _random_shapes()[name]
+    inp = synth.make_inputs(shape)
+    enforce_margin(inp, shape)
+    ref = oracle.layer_forward(oracle_inputs(inp), shape)
+    cuda = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+    cfg = moe.config_of(shape)
+    kw = dict(Wg=cuda(inp.get("Wg")), bias=cuda(inp.get("bias")), Ws1=cuda(inp.get("Ws1")),
+              Ws3=cuda(inp.get("Ws3")), Ws2=cuda(inp.get("Ws2")))
+    W1, W3, W2 = cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"])
+    x = cuda(inp["x"])
+    out_l = moe.MoeLayer(cfg, W1, W3, W2, **kw)(x)
+    eplayer = ep.GpuEp(cfg, W1, W3, W2, **kw)
+    out_e = eplayer.forward(x)
+    torch.cuda.synchronize()
+    assert eplayer.device_status() == 0
+    _close(out_e.double().cpu().numpy(), ref["out"], "out (expert parallel)")
+    if shape.T * shape.k > 32 * shape.E:
+        assert torch.equal(out_e, out_l)
