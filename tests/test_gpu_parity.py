@@ -145,6 +145,34 @@ def test_layer_is_deterministic():
     assert torch.equal(a, b)
 
 
+def test_layers_on_concurrent_streams():
+    """Two layers (different shapes, one on the CTA-pair and one on the
+    small-M path) enqueued alternately on two streams, each several times:
+    every output equals the same layer's output run alone.  The library
+    keeps no per-call state outside the caller's workspaces."""
+    runs = []
+    for name in ("small_default", "small_decode"):
+        shape, inp, _ = prepared(name)
+        cfg, layer = make_layer(shape, inp)
+        x = cuda(inp["x"])
+        alone = layer(x).clone()
+        torch.cuda.synchronize()
+        runs.append((layer, x, alone))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    for _ in range(4):
+        for i, (layer, x, _) in enumerate(runs):
+            with torch.cuda.stream(streams[i]):
+                out = torch.empty_like(x)
+                layer.forward(x, out, stream=streams[i])
+                outs[i].append(out)
+    torch.cuda.synchronize()
+    for i, (layer, _, alone) in enumerate(runs):
+        assert layer.device_status() == 0
+        for out in outs[i]:
+            assert torch.equal(out, alone)
+
+
 # --------------------------------------------------------------- stages ----
 @pytest.mark.parametrize("name", ["tiny", "small_decode", "small_e100_d384", "small_imbalance_p64"])
 def test_route_stage(name):
