@@ -196,3 +196,30 @@ def test_backward_entry_points_check_arguments_before_launch(lib):
     assert lib.moe_pack_experts_bwd(2, 200, 128, fp, fp, fp, None) == 2
     assert lib.moe_pack_experts_bwd(2, 256, 128, fp, None, fp, None) == 1
     assert lib.moe_pack_router_bwd(256, 0, fp, fp, None) == 1
+
+
+def test_exchange_and_widened_entry_points_check_arguments_before_launch(lib):
+    """moe_gather_rows, moe_widen_e4m3 and the scaled (widened e4m3) stage
+    calls reject bad sizes and null operands before any launch, and are
+    no-ops for empty inputs."""
+    fake = ctypes.c_void_p(0x1000)
+    # gather: sizes, d % 8, gates both or neither; n = 0 touches nothing
+    assert lib.moe_gather_rows(fake, fake, fake, ctypes.c_int64(-1), 64, None, None, None) == 1
+    assert lib.moe_gather_rows(fake, fake, fake, ctypes.c_int64(4), 60, None, None, None) == 2
+    assert lib.moe_gather_rows(fake, fake, fake, ctypes.c_int64(4), 64, fake, None, None) == 1
+    assert lib.moe_gather_rows(None, None, None, ctypes.c_int64(0), 64, None, None, None) == 0
+    assert lib.moe_gather_rows(None, fake, fake, ctypes.c_int64(4), 64, None, None, None) == 1
+    # widen: n % 16, null buffers; n = 0 is a no-op
+    assert lib.moe_widen_e4m3(fake, fake, ctypes.c_int64(24), None) == 2
+    assert lib.moe_widen_e4m3(None, fake, ctypes.c_int64(32), None) == 1
+    assert lib.moe_widen_e4m3(None, None, ctypes.c_int64(0), None) == 0
+    # scaled stages: null operands; the shared one needs d_shared > 0
+    cfg = _cfg()
+    args = [fake] * 13
+    args[2] = None  # s13
+    assert lib.moe_grouped_gemm_swiglu_scaled(ctypes.byref(cfg), *args) == 1
+    assert lib.moe_shared_expert_scaled(ctypes.byref(cfg), *([fake] * 7), None, None) == 1
+    cfg_s = _cfg(d_shared=256)
+    sargs = [fake] * 7
+    sargs[2] = None  # ss13
+    assert lib.moe_shared_expert_scaled(ctypes.byref(cfg_s), *sargs, None, None) == 1
