@@ -1,0 +1,47 @@
+"""CPU tests of bench.py's host-side accounting: the kernel launches it
+claims per layer call match the launch lists ncu recorded for the same
+workloads (the forward: router, offsets, permute, GEMMs, combine; the
+backward: 19 kernels at the default and decode workloads), and the
+algorithmic FLOP and byte counts follow the definitions of the counting
+rules (useful FLOP exclude padding rows)."""
+import sys
+
+import pytest
+
+from routing_permute_grouped_gb300 import ledger, synth
+
+
+@pytest.fixture(scope="module")
+def bench():
+    import os
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench as b
+
+    return b
+
+
+@pytest.mark.parametrize("name, skinny, fp8, expect", [
+    ("default", False, False, 11),     # split-K router 2, offsets 3, permute, 2 + 2 GEMMs, combine
+    ("decode", True, False, 7),        # split-K router 2, small offsets 1, permute, 2 GEMMs, combine
+    ("decode", True, True, 8),         # + the e4m3 pairs of h between the GEMMs
+    ("prerouted", False, False, 7),    # no router: offsets 3, permute, 2 GEMMs, combine
+    ("default", False, True, 15),      # + widening routed and shared W13, W2
+])
+def test_forward_launch_counts(bench, name, skinny, fp8, expect):
+    assert bench.forward_launches(synth.WORKLOADS[name], skinny, fp8) == expect
+
+
+@pytest.mark.parametrize("name, recompute, expect", [
+    ("default", True, 19), ("decode", True, 19), ("default", False, 17), ("prerouted", True, 9),
+])
+def test_backward_launch_counts(bench, name, recompute, expect):
+    assert bench.backward_launches(synth.WORKLOADS[name], recompute=recompute) == expect
+
+
+def test_useful_flops_exclude_padding():
+    s = synth.WORKLOADS["default"]
+    # 2 * T*k * d * 3 d_e routed + 2 * T * d * 3 d_s shared
+    routed = 2 * s.A * s.d * 3 * s.d_e
+    assert ledger.routed_flops(s.A, s.d, s.d_e) == routed
+    assert routed == 2_886_218_022_912
