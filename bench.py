@@ -57,58 +57,160 @@ def peaks():
 
 
 # ------------------------------------------------------------ clocks ------
+# NVML clock-event reason bits (nvml.h): the ones a measurement must report
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """SM clock and clock-event reasons of one GPU, read every ``period_s``
+    seconds on a background thread while a region runs.
+
+    NVML is read through ctypes (libnvidia-ml ships with the driver); where
+    it cannot be loaded, ``nvidia-smi -lms`` is the fallback.  Readings only:
+    nothing here changes a setting of the GPU.  ``mark(name)`` / ``window``
+    record wall-clock spans (the host enqueues far ahead and synchronises at
+    the end of each span, so the device is busy during it) and ``summary``
+    reports the samples taken inside a span."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, period_s: float = 0.001):
         self.idx = device_index
+        self.period = period_s
+        self.samples = []  # (wall time, sm MHz, reason bits)
+        self.sm_max = None
+        self.spans = {}
+        self._stop = threading.Event()
+        self.thread = None
         self.proc = None
-        self.lines = []
+        self.source = None
+
+    # -- NVML through ctypes
+    def _nvml_open(self):
+        import ctypes
+
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        try:  # the CUDA device's own GPU, matched by UUID
+            uuid = str(torch.cuda.get_device_properties(self.idx).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+        except Exception:  # noqa: BLE001
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.idx, ctypes.byref(h)) != 0:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.sm_max = float(mx.value)
+        return lib, h
+
+    def _nvml_loop(self, lib, h):
+        import ctypes
+
+        mhz = ctypes.c_uint()
+        bits = ctypes.c_ulonglong()
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            t = time.time()
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                r = bits.value if reasons(h, ctypes.byref(bits)) == 0 else 0
+                self.samples.append((t, float(mhz.value), int(r)))
+            time.sleep(self.period)
+
+    # -- nvidia-smi fallback
+    def _smi_read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm = float(parts[0])
+                self.sm_max = float(parts[1])
+            except ValueError:
+                continue
+            bits = 0
+            for b, v in zip((0x8, 0x40, 0x20, 0x4), parts[4:8]):
+                if v.lower().startswith("active"):
+                    bits |= b
+            self.samples.append((time.time(), sm, bits))
 
     def start(self):
+        nv = None
+        try:
+            nv = self._nvml_open()
+        except Exception:  # noqa: BLE001
+            nv = None
+        if nv is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._nvml_loop, args=nv, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._smi_read, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+    def window(self, name: str, t0: float, t1: float):
+        self.spans[name] = (t0, t1)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for _, line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
+        self._stop.set()
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
             try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, span: str = None):
+        """Median SM MHz and the reasons seen among the samples inside the
+        span (all samples when span is None)."""
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock readings unavailable"]}
+        sel = self.samples
+        if span is not None and span in self.spans:
+            t0, t1 = self.spans[span]
+            sel = [x for x in self.samples if t0 <= x[0] <= t1]
+        reasons = sorted({n for _, _, b in sel for bit, n in _NVML_REASONS.items() if b & bit})
+        sm = [x[1] for x in sel]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.sm_max,
+                "reasons": reasons, "samples": len(sm), "source": self.source,
+                "period_ms": self.period * 1e3 if self.source == "nvml" else 100.0}
+
+
+def clock_normalised(stage_ms: float, roof: dict, clk):
+    """Stage time against the SM clock seen while it ran: ms x median MHz
+    (thousands of SM cycles) and the rate the same cycles would give at the
+    maximum SM clock.  A stage held back by the power cap shows a median
+    below the maximum; one held back by its code does not."""
+    if not clk or not clk.get("sm_mhz") or not clk.get("sm_max_mhz"):
+        return None
+    scale = clk["sm_max_mhz"] / clk["sm_mhz"]
+    return {"sm_mhz_median": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+            "samples": clk.get("samples"), "stage_ms_x_mhz": stage_ms * clk["sm_mhz"],
+            "achieved_at_max_clock": roof["achieved"] * scale,
+            "frac_at_max_clock": roof["achieved"] * scale / roof["peak"]}
 
 
 # --------------------------------------------------------- distributed ----
@@ -467,11 +569,13 @@ def run_ours(args, shape, rank, world, local):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     t_start.record()
     for i in range(args.steps):
         layer_step()
     t_end.record()
     torch.cuda.synchronize()
+    w1 = time.time()
     barrier(world)
     ms_total = t_start.elapsed_time(t_end)
     ms_max = reduce_max(ms_total, world)
@@ -482,10 +586,18 @@ def run_ours(args, shape, rank, world, local):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
            for _ in range(n_stage)]
     torch.cuda.synchronize()
+    w2 = time.time()
     for i in range(n_stage):
         step(evs[i])
     torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
+    w3 = time.time()
+    clocks = stage_clocks = None
+    if sampler:
+        sampler.stop()
+        sampler.window("timed", w0, w1)
+        sampler.window("stages", w2, w3)
+        clocks = sampler.summary("timed")
+        stage_clocks = sampler.summary("stages")
     # per-stage median over the stage-pass steps
     stage_ms = {n: statistics.median(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
                 for j, n in enumerate(stage_names)}
@@ -532,7 +644,10 @@ def run_ours(args, shape, rank, world, local):
     active = sum(1 for c in counts_h if c > 0)
     gemm_bytes = ledger.grouped_gemm_bytes_alg(A, active, d, de, fp8_weights=fp8)
     gemm_s = stage_ms["grouped_gemm"] / 1e3
-    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # the stage is timed by CUDA events launch by launch (about 2 ms each,
+    # well under a second), so its peak is the burst bf16 figure; the
+    # sustained one (a seconds-long loop under the power cap) is context
+    peak_t = pk["bf16_tflops"]
     # the stage is tensor-bound when its FLOP per byte exceeds the machine
     # balance (measured bf16 FLOP/s over measured HBM bytes/s), else HBM-bound
     hbm_bound = gemm_flops / gemm_bytes < peak_t * 1e12 / (pk["hbm_gbs"] * 1e9)
@@ -541,8 +656,11 @@ def run_ours(args, shape, rank, world, local):
                 "unit": "GB/s", "peak_source": pk["source"] + " copy bandwidth"}
     else:
         roof = {"bound": "tensor", "achieved": gemm_flops / gemm_s / 1e12, "peak": peak_t,
-                "unit": "TFLOP/s", "peak_source": pk["source"] + " sustained bf16"}
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " burst bf16"}
+        if "bf16_tflops_sustained" in pk:
+            roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
     roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["clock"] = clock_normalised(stage_ms["grouped_gemm"], roof, stage_clocks)
     roof["algorithmic"] = {"flop": gemm_flops, "bytes": gemm_bytes, "active_experts": active}
     perm_bytes = ledger.permute_bytes_alg(T, k, d)
     comb_bytes = ledger.combine_bytes_alg(T, k, d, bool(ds))
@@ -572,6 +690,7 @@ def run_ours(args, shape, rank, world, local):
                              "moe_grouped_gemm_swiglu"),
                          traffic=traffic),
         "stages": {"ms": {n: round(v, 4) for n, v in stage_ms.items()},
+                   "clocks": stage_clocks,
                    "serial_sum_ms": round(sum(stage_ms.values()), 4),
                    "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],
                    "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm_gbs"],
@@ -673,16 +792,19 @@ def run_train(args, shape, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     t0.record()
     for _ in range(args.steps):
         train_step()
     t1.record()
     torch.cuda.synchronize()
+    w1 = time.time()
     barrier(world)
     ms_max = reduce_max(t0.elapsed_time(t1), world)
     # split pass: forward and backward bracketed separately
     n_split = min(args.steps, 20)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_split)]
+    w2 = time.time()
     for i in range(n_split):
         evs[i][0].record()
         layer(x, out, **kw)
@@ -690,7 +812,14 @@ def run_train(args, shape, rank, world, local):
         layer.backward(x, dout, grads=grads, prerouted=pre)
         evs[i][2].record()
     torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
+    w3 = time.time()
+    clocks = split_clocks = None
+    if sampler:
+        sampler.stop()
+        sampler.window("timed", w0, w1)
+        sampler.window("split", w2, w3)
+        clocks = sampler.summary("timed")
+        split_clocks = sampler.summary("split")
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     st = layer.device_status()
@@ -737,7 +866,9 @@ def run_train(args, shape, rank, world, local):
                                                  recompute=not args.keep_gate_up)
     bwd_bytes = ledger.layer_backward_bytes_alg(T, k, d, de, ds, shape.E, active, not pre,
                                                 recompute=not args.keep_gate_up)
-    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # the backward is timed call by call (a few ms each, well under a
+    # second): the burst bf16 peak applies; the sustained one is context
+    peak_t = pk["bf16_tflops"]
     bwd_s = bwd_ms / 1e3
     # tensor-bound when the backward's FLOP per byte exceeds the machine
     # balance (measured bf16 FLOP/s over measured HBM bytes/s), else HBM-bound
@@ -746,7 +877,10 @@ def run_train(args, shape, rank, world, local):
                 "unit": "GB/s", "peak_source": pk["source"] + " copy bandwidth"}
     else:
         roof = {"bound": "tensor", "achieved": bwd_flops / bwd_s / 1e12, "peak": peak_t,
-                "unit": "TFLOP/s", "peak_source": pk["source"] + " sustained bf16"}
+                "unit": "TFLOP/s", "peak_source": pk["source"] + " burst bf16"}
+        if "bf16_tflops_sustained" in pk:
+            roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
+    roof["clock"] = clock_normalised(bwd_ms, dict(roof, frac=None), split_clocks)
     roof.update({"frac": roof["achieved"] / roof["peak"],
                  "kernel": "layer backward (moe_layer_bwd: all its kernels; GEMM FLOP incl. the "
                            "gate/up recomputation; bytes: weights read, weight gradients "
@@ -769,7 +903,8 @@ def run_train(args, shape, rank, world, local):
         "gpu_launches": (forward_launches(shape, skinny)
                          + backward_launches(shape, recompute=not args.keep_gate_up)) * args.steps,
         "roofline": roof,
-        "stages": {"ms": {"forward": round(fwd_ms, 4), "backward": round(bwd_ms, 4)}},
+        "stages": {"ms": {"forward": round(fwd_ms, 4), "backward": round(bwd_ms, 4)},
+                   "clocks": split_clocks},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
@@ -837,13 +972,19 @@ def run_ep(args, shape, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     t0.record()
     for _ in range(args.steps):
         layer.forward(x, **kw)
     t1.record()
     torch.cuda.synchronize()
+    w1 = time.time()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
+    clocks = None
+    if sampler:
+        sampler.stop()
+        sampler.window("timed", w0, w1)
+        clocks = sampler.summary("timed")
     ms_max = reduce_max(t0.elapsed_time(t1), world)
     assert layer.device_status() == 0
     T, k, d, de, ds = shape.T, shape.k, shape.d, shape.d_e, shape.d_shared
@@ -866,7 +1007,7 @@ def run_ep(args, shape, rank, world, local):
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
     pk = peaks()
-    peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak_t = pk["bf16_tflops"]  # K calls of a few ms: the burst figure
     achieved = useful / (ms_max / args.steps / 1e3) / 1e12
     skinny = T * k <= 32 * shape.E
     line = {
@@ -883,7 +1024,7 @@ def run_ep(args, shape, rank, world, local):
         # gathers of the exchange's reorder
         "gpu_launches": (forward_launches(shape, False) + 2) * args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": achieved / peak_t, "peak_source": pk["source"] + " sustained bf16",
+                     "frac": achieved / peak_t, "peak_source": pk["source"] + " burst bf16",
                      "kernel": "the whole expert-parallel layer per rank (its kernels, the two "
                                "all-to-alls, the host sync for the split sizes)",
                      "timing": "CUDA events around the K layer calls", "traffic": None},

@@ -199,6 +199,21 @@ moe_status_t moe_pack_router(int32_t d, int32_t E, const void *Wg, void *Wg_t, v
 moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void *W1, const void *W3,
                               const void *W2, void *W13, void *W2_t, void *stream);
 
+/* The gate/up half of moe_pack_experts for one layer's config, in the form
+ * the layer's scope names: W1 (gate) and W3 (up), bf16 [E, d, d_e] each,
+ * row-major as the pages write x W -> W13_packed bf16 [E, 2*d_e, d], K-major,
+ * gate and up rows interleaved per 128 output columns exactly as
+ * moe_pack_experts writes them ("MoE & MLA operators", sec. 2.4(c): the dual
+ * GEMM of gate and up over one read of the activations).  The config is
+ * checked like every other entry point's (d % 128, d_e % 128, E <= 256);
+ * only d, d_e and E are used.  The down projection needs its own K-major
+ * copy, which moe_pack_experts writes (it also packs a shared expert with
+ * E = 1), and the router weight is packed by moe_pack_router.
+ *   W1, W3      bf16 [E, d, d_e]   device, read
+ *   W13_packed  bf16 [E, 2*d_e, d] device, written */
+moe_status_t moe_pack_weights(const moe_config_t *cfg, const void *W1, const void *W3,
+                              void *W13_packed, void *stream);
+
 /* The same packing into e4m3 codes with one fp32 scale per output channel
  * ("MoE & MLA operators", sec. 6.1: fp8 expert weights, one byte each;
  * "Dropless and grouped GEMM", sec. 12: a scale that covers the whole
@@ -286,6 +301,9 @@ moe_status_t moe_build_offsets(const moe_config_t *cfg, const int32_t *topk_idx,
  * larger configs return MOE_ERR_WORKSPACE before anything is enqueued.
  * The first call on a device looks up the array's device address (with that
  * device current), so make that first call before any stream capture begins.
+ * The address is kept per device and per CUDA context: after the device's
+ * context is torn down and made again (cudaDeviceReset), the next call looks
+ * it up again and counts as a first call.
  * All calls share the one array and it keeps the last call's contents (none
  * of it needs to start at zero); calls whose work overlaps on the GPU (on
  * different streams, or from different threads) race on it and must be

@@ -25,7 +25,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "MoeConfig", "MoeWeights", "MoeLayer", "config_of", "load",
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
-    "moe_pack_router", "moe_pack_experts", "moe_route", "moe_route_splitk",
+    "moe_pack_router", "moe_pack_experts", "moe_pack_weights", "moe_route", "moe_route_splitk",
     "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
     "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
@@ -110,6 +110,7 @@ def load():
         "moe_offsets_workspace_size": (SZ, [CP]),
         "moe_pack_router": (ctypes.c_int, [I32, I32, P, P, P]),
         "moe_pack_experts": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P]),
+        "moe_pack_weights": (ctypes.c_int, [CP, P, P, P, P]),
         "moe_route": (ctypes.c_int, [CP, P, P, P, P, P, P]),
         "moe_route_splitk_scratch_size": (SZ, [CP]),
         "moe_route_splitk": (ctypes.c_int, [CP, P, P, P, P, P, P, SZ, P]),
@@ -233,6 +234,11 @@ def moe_pack_router(Wg: torch.Tensor, Wg_t: torch.Tensor, stream=None) -> None:
 def moe_pack_experts(W1, W3, W2, W13, W2_t, stream=None) -> None:
     E, d, de = W1.shape
     _check(load().moe_pack_experts(E, d, de, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(W13), _ptr(W2_t),
+                                   _stream(stream)))
+
+
+def moe_pack_weights(cfg: MoeConfig, W1, W3, W13_packed, stream=None) -> None:
+    _check(load().moe_pack_weights(ctypes.byref(cfg), _ptr(W1), _ptr(W3), _ptr(W13_packed),
                                    _stream(stream)))
 
 

@@ -342,12 +342,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    // Inputs written by earlier kernels are visible after pdl_wait().  Tensor
+    // memory is taken only after it too: by then every earlier kernel of the
+    // stream has finished and released its own, and no later kernel has
+    // allocated (each of them waits in the same place first).  Allocating
+    // before the wait could deadlock a chain A -> B -> C of tensor-memory
+    // kernels: a CTA of C, let in early by B's trigger, could take the
+    // columns A frees while a CTA of B on the same SM still waits for them,
+    // and then wait for B to finish.
+    pdl_wait();
     if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    pdl_wait();  // inputs written by earlier kernels are visible from here on
 
     const int total = ((args.dense_rows + BM - 1) / BM) * args.n_tiles;
     bool timed_out = false;
@@ -655,8 +663,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmB);
     }
     if (threadIdx.x == 32) tma_prefetch_desc(&tmOut);
+    // inputs written by earlier kernels are visible from here on; tensor
+    // memory is taken after the wait, as in k_grouped_gemm
+    pdl_wait();
     if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
-    pdl_wait();  // inputs written by earlier kernels are visible from here on
     if (warp == 2 && args.block_metadata) {
         // per-expert visit counts from the segment sizes, exclusive warp scan
         const int per = 256 / args.block_rows;

@@ -882,6 +882,21 @@ moe_status_t moe_pack_experts(int32_t E, int32_t d, int32_t de, const void* W1, 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack experts");
 }
 
+moe_status_t moe_pack_weights(const moe_config_t* cfg, const void* W1, const void* W3,
+                              void* W13_packed, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!W1 || !W3 || !W13_packed) return fail(MOE_ERR_INVALID_ARG, "null gate/up weights");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t dd = cfg->d, dde = cfg->d_e;
+    cudaError_t e = launch_pack_transpose(W1, W13_packed, cfg->d, cfg->d_e, dd * dde, 2 * dde * dd,
+                                          cfg->d, 1, cfg->E, st);
+    if (e == cudaSuccess)
+        e = launch_pack_transpose(W3, W13_packed, cfg->d, cfg->d_e, dd * dde, 2 * dde * dd, cfg->d,
+                                  2, cfg->E, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "pack gate/up weights");
+}
+
 moe_status_t moe_pack_experts_fp8(int32_t E, int32_t d, int32_t de, const void* W1, const void* W3,
                                   const void* W2, void* W13q, float* s13, void* W2q, float* s2,
                                   void* stream) {

@@ -8,6 +8,7 @@
 // forbid any allocation on the serving path.  This variant keeps its
 // scratch in a fixed-size array in the library's own device memory instead,
 // so the caller passes inputs and outputs only.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,19 +23,45 @@ namespace moe {
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;
 static __device__ __align__(256) unsigned char g_offsets_scratch[kNoAllocScratchBytes];
 
-// Device address of g_offsets_scratch on the current device.  In host code
+// Device address of g_offsets_scratch in the current context.  In host code
 // the symbol name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with the device current and cached per device together with the context it
+// was found in: after cudaDeviceReset (or any teardown of the primary
+// context) the module is loaded again, possibly at another address, so a
+// call in a new context looks the address up afresh.
+typedef CUresult (*PFN_ctxGetCurrent)(CUcontext*);
+
+static PFN_ctxGetCurrent ctx_get_current() {
+    static PFN_ctxGetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_ctxGetCurrent>(p);
+    });
+    return fn;
+}
+
 static void* noalloc_scratch(int dev, cudaError_t* err) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static CUcontext ctx_of[kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
     *err = cudaSuccess;
-    if (addr[dev]) return addr[dev];
+    PFN_ctxGetCurrent get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    if (addr[dev] && ctx && ctx == ctx_of[dev]) return addr[dev];
     void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_offsets_scratch);
+    *err = cudaGetSymbolAddress(&p, g_offsets_scratch);  // sets the context up if needed
     if (*err != cudaSuccess) return nullptr;
+    ctx = nullptr;
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
     return p;
 }
 

@@ -170,12 +170,15 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tBs);
         }
     }
+    // The block table and the token rows are visible after pdl_wait().
+    // Tensor memory is taken after the wait: every earlier kernel of the
+    // stream has then released its own, and no later one holds any yet.
+    pdl_wait();
     if (warp == 1) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    pdl_wait();  // the block table and the token rows are visible from here on
 
     int nb = args.num_blocks ? ld_dep(args.num_blocks) : 0;  // null: shared-expert tiles only
     nb = nb < 0 ? 0 : (nb > args.nb_cap ? args.nb_cap : nb);

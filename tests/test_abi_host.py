@@ -223,3 +223,14 @@ def test_exchange_and_widened_entry_points_check_arguments_before_launch(lib):
     sargs = [fake] * 7
     sargs[2] = None  # ss13
     assert lib.moe_shared_expert_scaled(ctypes.byref(cfg_s), *sargs, None, None) == 1
+
+
+def test_pack_weights_checks_arguments_before_launch(lib):
+    """moe_pack_weights takes the layer's config: the config rules and null
+    operands are rejected before anything is enqueued."""
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.moe_pack_weights(ctypes.byref(_cfg(d=500)), fake, fake, fake, None) == 2
+    assert lib.moe_pack_weights(ctypes.byref(_cfg(d_e=200)), fake, fake, fake, None) == 2
+    assert lib.moe_pack_weights(ctypes.byref(_cfg()), fake, None, fake, None) == 1
+    assert lib.moe_pack_weights(ctypes.byref(_cfg()), fake, fake, None, None) == 1
+    assert lib.moe_pack_weights(None, fake, fake, fake, None) == 1

@@ -51,8 +51,9 @@ def _expert_subset(W, experts):
     return bits(W[torch.as_tensor(experts, device=W.device, dtype=torch.long)].cpu())
 
 
-@pytest.mark.parametrize("name", ["default", "prerouted", "decode", "imbalance_x4_p128",
-                                  "imbalance_x2_p64"])
+@pytest.mark.parametrize("name", ["default", "prerouted", "decode", "imbalance_x1_p64",
+                                  "imbalance_x1_p128", "imbalance_x2_p64", "imbalance_x2_p128",
+                                  "imbalance_x4_p64", "imbalance_x4_p128"])
 def test_full_size_layer(name):
     shape = synth.WORKLOADS[name]
     dev = torch.device("cuda")
@@ -112,7 +113,7 @@ def test_full_size_layer(name):
     assert torch.equal(xp[valid], x[src_tok[valid]])
     rng = np.random.default_rng(7)
     vrows = np.flatnonzero(row_src >= 0)
-    n_rows, n_tok = (6, 2) if E > 64 else (24, 8)  # bounds the expert weights copied to the host
+    n_rows, n_tok = (16, 4) if E > 64 else (24, 8)  # bounds the expert weights copied to the host
     samp = np.sort(rng.choice(vrows, size=min(n_rows, vrows.size), replace=False))
     ref_xp = oracle.permute(x_bits, np.where(np.isin(np.arange(R), samp), row_src, -1), k)
     assert np.array_equal(bits(xp[torch.as_tensor(samp, device=dev)].cpu()), ref_xp[samp])

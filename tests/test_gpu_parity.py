@@ -93,6 +93,31 @@ def make_layer(shape, inp):
     return cfg, layer
 
 
+# ------------------------------------------------------------- packing ----
+def test_pack_weights_interleaves_gate_and_up():
+    """moe_pack_weights (the config form of the gate/up pack): row 256 j + c
+    of expert e's packed matrix is gate column 128 j + c and row
+    256 j + 128 + c the matching up column, K (= d) contiguous; the same bytes
+    as moe_pack_experts writes."""
+    E, d, de = 3, 384, 256
+    W1 = torch.randn(E, d, de).to(torch.bfloat16)
+    W3 = torch.randn(E, d, de).to(torch.bfloat16)
+    W2 = torch.randn(E, de, d).to(torch.bfloat16)
+    cfg = moe.config_of(T=1, d=d, d_e=de, E=E, k=1)
+    W13 = torch.empty(E, 2 * de, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_weights(cfg, cuda(W1), cuda(W3), W13)
+    ref = torch.empty(E, 2 * de, d, dtype=torch.bfloat16)
+    for j in range(de // 128):
+        ref[:, 256 * j:256 * j + 128] = W1[:, :, 128 * j:128 * j + 128].transpose(1, 2)
+        ref[:, 256 * j + 128:256 * j + 256] = W3[:, :, 128 * j:128 * j + 128].transpose(1, 2)
+    assert torch.equal(W13.cpu(), ref)
+    W13b = torch.empty_like(W13)
+    W2t = torch.empty(E, d, de, dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(W1), cuda(W3), cuda(W2), W13b, W2t)
+    assert torch.equal(W13b, W13)
+    assert torch.equal(W2t.cpu(), W2.transpose(1, 2))
+
+
 # ---------------------------------------------------------------- layer ----
 @pytest.mark.parametrize("name", list(SHAPES))
 def test_layer_matches_oracle(name):

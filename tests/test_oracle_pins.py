@@ -55,6 +55,34 @@ def test_bf16_rounding_matches_torch_rne():
     np.testing.assert_array_equal(got, ref)
 
 
+def test_bf16_rounding_subnormal_overflow_and_ties_match_torch():
+    # the corners of the rounding: bf16 subnormals (quantum 2^-133, below the
+    # smallest normal 2^-126), values that overflow to infinity (at and above
+    # the midpoint (2 - 2^-8) * 2^127 between the largest finite bf16 and the
+    # next power of two), and exact ties in both ranges.  Every input is an
+    # fp32 value, which torch converts with round-to-nearest-even.
+    g = torch.Generator().manual_seed(4)
+    tiny = torch.ldexp(torch.rand(20000, generator=g) * 2 - 1,
+                       torch.randint(-149, -120, (20000,), generator=g))
+    k = torch.randint(-300, 300, (4000,), generator=g).to(torch.float32)
+    q = 2.0 ** -133
+    sub_ties = torch.cat([(k + 0.5) * q, (k + 0.25) * q, (k + 0.75) * q])
+    fmax = torch.finfo(torch.float32).max
+    top = torch.tensor([(2 - 2 ** -8) * 2.0 ** 127, (2 - 2 ** -7) * 2.0 ** 127,
+                        (2 - 2 ** -7 - 2 ** -9) * 2.0 ** 127, (2 - 2 ** -8 - 2 ** -20) * 2.0 ** 127,
+                        fmax, 2.0 ** 127, (2 - 2 ** -8 + 2 ** -20) * 2.0 ** 127],
+                       dtype=torch.float64).to(torch.float32)
+    big = torch.ldexp(1 + torch.rand(4000, generator=g), torch.full((4000,), 127))
+    f = torch.cat([tiny, sub_ties, top, big, -top, -sub_ties,
+                   torch.tensor([2.0 ** -126, 2.0 ** -127, 2.0 ** -133, 2.0 ** -134,
+                                 1.5 * 2.0 ** -134, 2.0 ** -135, 2.0 ** -149])])
+    ref = f.to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(f.to(torch.float64).numpy())
+    np.testing.assert_array_equal(got, ref)
+    assert np.isinf(got).sum() > 0 and (np.abs(got[np.isfinite(got)]) > 0).any()
+    assert ((got != 0) & (np.abs(got) < 2.0 ** -126)).sum() > 1000  # subnormal results
+
+
 # ---------------------------------------------------------- offsets --------
 def _prerouted_idx(counts, seed=0):
     labels = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])
@@ -183,6 +211,49 @@ def test_route_brute_force(case):
                                       np.take_along_axis(lg, idx[:, -1:].astype(np.int64), 1)[:, 0]),
                                rtol=1e-12)
     assert (m > 0).all()
+
+
+def _brute_margin(l, k, n_groups, topk_groups):
+    """The smallest gap between two values whose order decides the routing,
+    by enumerating pairs: every kept group against every rejected group
+    (group scores), every chosen expert against every eligible rejected one,
+    and every pair of chosen experts (their order is part of the output)."""
+    E = l.size
+    chosen = _brute_topk(l, k, n_groups, topk_groups)
+    gaps = []
+    elig = set(range(E))
+    if n_groups:
+        gsz = E // n_groups
+        gs = [l[g * gsz:(g + 1) * gsz].max() for g in range(n_groups)]
+        kept = max(itertools.combinations(range(n_groups), topk_groups),
+                   key=lambda c: sum(gs[g] for g in c))
+        gaps += [gs[a] - gs[b] for a in kept for b in range(n_groups) if b not in kept]
+        elig = {e for e in range(E) if e // gsz in kept}
+    gaps += [l[a] - l[b] for a in chosen for b in elig if b not in chosen]
+    gaps += [l[chosen[i]] - l[chosen[j]] for i in range(k) for j in range(i + 1, k)]
+    return min(gaps) if gaps else np.inf
+
+
+@pytest.mark.parametrize("case", [(8, 2, 0, 0), (8, 3, 4, 2), (6, 1, 0, 0), (8, 4, 2, 1),
+                                  (8, 8, 0, 0), (8, 5, 4, 3), (12, 3, 6, 2), (9, 2, 3, 1)])
+def test_route_margin_brute_force(case):
+    # the margin that the tie filter of the parity tests rests on: equal to
+    # the pairwise brute force, and no perturbation of the logits smaller
+    # than half of it (in every coordinate) changes the routing.  Logits on a
+    # coarse grid make near-ties and exact ties (margin 0) frequent.
+    E, k, ng, tg = case
+    rng = np.random.default_rng(E * 1000 + k * 10 + ng)
+    lg = np.concatenate([rng.normal(size=(24, E)), np.round(rng.normal(size=(24, E)) * 4) / 4])
+    idx, _, m = oracle.route(lg, k, ng, tg)
+    for t in range(lg.shape[0]):
+        want = _brute_margin(lg[t], k, ng, tg)
+        assert m[t] == want, (t, m[t], want)
+        if not np.isfinite(want) or want == 0:
+            continue
+        for _ in range(20):
+            d = rng.uniform(-1, 1, E) * want * 0.49
+            assert _brute_topk(lg[t] + d, k, ng, tg) == idx[t].tolist()
+    assert (m == 0).any() and (m > 0).any()
 
 
 def test_route_ties_go_to_lower_index():
@@ -369,3 +440,33 @@ def test_grouped_bytes_with_e4m3_weights():
     acts = 2 * (2 * A * d + 2 * A * de)
     assert b16 - acts == act * 3 * d * de * 2
     assert b8 - acts == act * (3 * d * de + 4 * (2 * de + d))
+
+
+# ------------------------------------------------------ imbalance sweep ----
+def test_zipf_exponents_give_the_stored_loads():
+    # the Zipf exponents of the imbalance workloads (constants in synth) are
+    # the ones tests/golden/make_zipf_s.py stored, and with them the oracle's
+    # routing of the seeded token rows puts the recorded multiple of the mean
+    # load on the hottest expert (within 2 % of 1x / 2x / 4x for 2x and 4x)
+    import json
+
+    from routing_permute_grouped_gb300 import synth
+
+    with open(os.path.join(GOLDEN, "zipf_s.json")) as f:
+        stored = json.load(f)
+    shape = synth.WORKLOADS["imbalance_x1_p128"]
+    inp = synth.make_inputs(shape, zipf_s=0.0)
+    L0 = oracle.router_logits(bits(inp["x"]), bits(inp["Wg"]), None)
+    for target in (1, 2, 4):
+        for pad in (64, 128):
+            name = f"imbalance_x{target}_p{pad}"
+            assert synth.ZIPF_S[name] == stored[name]
+            assert synth.ZIPF_HOT_OVER_MEAN[name] == stored[name + "_hot_over_mean"]
+        name = f"imbalance_x{target}_p128"
+        bias = synth.zipf_bias(shape.E, synth.ZIPF_S[name], shape.seed).numpy().astype(np.float64)
+        idx, _, _ = oracle.route(L0 + bias[None, :], shape.k)
+        counts = np.bincount(idx.reshape(-1), minlength=shape.E)
+        ratio = counts.max() / counts.mean()
+        assert round(float(ratio), 4) == synth.ZIPF_HOT_OVER_MEAN[name]
+        if target > 1:
+            assert abs(ratio - target) <= 0.02 * target

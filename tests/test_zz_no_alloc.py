@@ -39,12 +39,19 @@ def test_noalloc_matches_allocating_entry_point_twice():
     moe.load()
     dev = "cuda"
     # the larger scratch user first, so stale counts from it would show in
-    # the second, smaller call
-    cases = [(256, 1111, 8, 64, 11), (8, 4097, 4, 128, 12)]
-    for E, T, k, P, seed in cases:
+    # the later, smaller calls; the third case (T*k <= 4096) takes the
+    # one-CTA offsets kernel, the fourth carries expert ids outside [0, E),
+    # which both entry points skip and flag in their status words
+    cases = [(256, 1111, 8, 64, 11, False), (8, 4097, 4, 128, 12, False),
+             (16, 300, 6, 64, 13, False), (32, 2500, 4, 128, 14, True)]
+    for E, T, k, P, seed, bad in cases:
         rng = np.random.default_rng(seed)
         p = rng.dirichlet(np.full(E, 0.2))
-        idx = torch.from_numpy(rng.choice(E, size=(T, k), p=p).astype(np.int32)).to(dev)
+        idx_h = rng.choice(E, size=(T, k), p=p).astype(np.int32)
+        if bad:
+            idx_h[3, 1] = E
+            idx_h[T - 1, 0] = E + 7
+        idx = torch.from_numpy(idx_h).to(dev)
         w = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(dev)
         cfg = moe.config_of(T=T, d=128, d_e=128, E=E, k=k, pad_multiple=P)
         ref = _tables(E, T, k, P, dev)
@@ -54,7 +61,9 @@ def test_noalloc_matches_allocating_entry_point_twice():
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         moe.moe_build_offsets_noalloc(cfg, idx, w, *_order(got), status=status)
         torch.cuda.synchronize()
-        assert int(status.item()) == 0
+        want = moe.DEVERR_EXPERT_RANGE if bad else 0
+        assert int(status.item()) == want
+        assert int(ws[:4].view(torch.int32).item()) == want
         nb = int(ref["num_blocks"].item())
         assert nb == int(got["num_blocks"].item()) and nb > 0
         for key in ("counts", "padded_offsets", "perm_row", "row_src", "row_gate"):
