@@ -716,7 +716,8 @@ def run_ours(args, shape, rank, world, local):
 
 
 def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: bool = True) -> int:
-    """Kernels of one layer forward: router (2 when split-K), offsets (1 or
+    """Kernels of one layer forward: router (2 when split-K with a scratch:
+    partial logits + reduce; 1 fused or clustered), offsets (1 or
     3), permute (none when fused), 2 routed GEMMs, 2 shared-expert GEMMs (none
     on the small-M kernel, whose launches carry the shared tiles), combine,
     and with e4m3 weights the split of h between the GEMMs."""

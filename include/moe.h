@@ -245,11 +245,17 @@ moe_status_t moe_route(const moe_config_t *cfg, const void *x, const void *Wg_t,
 
 /* a1 for small batches: the router GEMM with K split into S slices (S from
  * the config: enough slices that the 128-token tiles x slices cover the GPU,
- * at most 16) writes fp32 partial logits to `partial`; a second kernel sums
- * them in slice order, adds the bias and does the same group-limited top-k
- * and softmax as moe_route.  Returns the same outputs as moe_route.  When
- * moe_route_splitk_scratch_size(cfg) is 0 (the batch already fills the GPU)
- * it runs moe_route's single kernel and ignores `partial`.
+ * at most 16), the partial logits summed in slice order, then the bias, the
+ * same group-limited top-k and softmax as moe_route.  Returns the same
+ * outputs as moe_route.  Two forms, chosen from the config:
+ *  - up to 4 slices and E <= 64 (within the kernel's shared memory): the S
+ *    CTAs of a 128-token tile form a thread-block cluster and the slices
+ *    meet in the first CTA's shared memory, one launch, no scratch
+ *    (moe_route_splitk_scratch_size is 0 and `partial` is ignored);
+ *  - otherwise fp32 partial logits go to `partial` and a second kernel sums
+ *    them.
+ * When the batch already fills the GPU (S = 1) it runs moe_route's single
+ * kernel; the scratch size is 0 then too.
  *   partial  fp32 [S, T, E] device scratch, partial_bytes >= the size above */
 size_t moe_route_splitk_scratch_size(const moe_config_t *cfg);
 moe_status_t moe_route_splitk(const moe_config_t *cfg, const void *x, const void *Wg_t,
@@ -487,6 +493,48 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
  * peers.  src, idx, dst device; ranges must not overlap. */
 moe_status_t moe_gather_rows(const void *src, const int32_t *idx, void *dst, int64_t n,
                              int32_t d, const float *src_gate, float *dst_gate, void *stream);
+
+/* The receiving side of the expert-parallel dispatch ("Dropless and grouped
+ * GEMM", sec. 4 step 5: the dispatch lands rows already grouped by expert and
+ * padded to the alignment, and hands the receiver its per-expert counts;
+ * sec. 14: expert parallelism with all-to-all).  counts[s * E + e] rows of
+ * sender s for local expert e (e.g. the result of the counts all-to-all).
+ * Expert e's segment holds the senders' rows back to back in sender order,
+ * padded like any segment to ceil(c_e / P) * P rows, c_e = sum over s of
+ * counts[s, e]; its valid rows are therefore a prefix of the segment, as in
+ * the single-GPU layout, and the grouped GEMM entry points run on it as they
+ * are.  This is a2's arithmetic for a batch that arrives as counts instead
+ * of expert ids.
+ *   counts          int32 [n_src, E] device, read (negative entries count
+ *                   as 0 and set MOE_DEVERR_SEGMENT)
+ *   padded_offsets  int32 [E + 1]    device, written
+ *   block_metadata  int32 [nb_cap,3] device, written: [expert, first row,
+ *                   valid rows] of blocks [0, num_blocks)
+ *   num_blocks      int32 [1]        device, written (at most nb_cap; blocks
+ *                   past nb_cap set MOE_DEVERR_SEGMENT)
+ *   piece_row       int32 [n_src, E] device, written: the first row of sender
+ *                   s's rows for expert e, or NULL
+ *   status          uint32 [1] device error word, or NULL
+ * 1 <= E <= 256, P in {64, 128}.  One launch; nothing goes to the host. */
+moe_status_t moe_build_blocks_from_counts(const int32_t *counts, int32_t n_src, int32_t E,
+                                          int32_t P, int32_t *padded_offsets,
+                                          int32_t *block_metadata, int32_t *num_blocks,
+                                          int32_t nb_cap, int32_t *piece_row, uint32_t *status,
+                                          void *stream);
+
+/* Row pieces between two row-major bf16 [*, d] buffers (d % 8 == 0): for
+ * piece i < n, rows [src_row[i], src_row[i] + rows[i]) of src go to rows
+ * [dst_row[i], dst_row[i] + rows[i]) of dst, and with src_gate/dst_gate
+ * (both or neither) their fp32 gates too.  The piece descriptors are device
+ * arrays, so the pieces an expert-parallel rank keeps ("Dropless and grouped
+ * GEMM", sec. 14) move between its own layout and its expert-major layout
+ * with nothing built on the host.  max_rows >= every rows[i] (sizes the
+ * grid; larger pieces are not copied beyond it); n <= 65535; pieces must not
+ * overlap in dst, and src and dst ranges must not overlap. */
+moe_status_t moe_copy_pieces(const void *src, void *dst, int32_t d, const int32_t *src_row,
+                             const int32_t *dst_row, const int32_t *rows, int32_t n,
+                             int32_t max_rows, const float *src_gate, float *dst_gate,
+                             void *stream);
 
 /* out[i] = the e4m3 code q[i] widened to bf16 (exact: every e4m3 value is a
  * bf16 value); n % 16 == 0.  The e4m3 layer's first step above the small-M

@@ -65,6 +65,7 @@ def _L():
                 "or_rows_capacity": (LL, [LL, I, I]),
                 "or_blocks_capacity": (LL, [LL, I, I]),
                 "or_build_offsets": (I, [LL, I, I, P, P, P, P, P, P, P, P, P]),
+                "or_blocks_from_counts": (I, [I, I, I, P, P, P, P, P]),
                 "or_permute": (None, [LL, I, I, P, P, P]),
                 "or_grouped_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P]),
                 "or_expert_rows": (I, [I, I, I, I, P, P, P, P, P, P, P, P]),
@@ -177,6 +178,24 @@ def build_offsets(topk_idx, topk_w, E: int, P: int) -> dict:
     return dict(counts=counts, padded_offsets=po, block_metadata=meta[:n].copy(), num_blocks=n,
                 perm_row=perm_row, row_src=row_src, row_gate=row_gate, rows_capacity=R,
                 blocks_capacity=NB)
+
+
+def blocks_from_counts(counts, P: int) -> dict:
+    """The receiver's expert-major layout of an expert-parallel dispatch from
+    counts [n_src, E] (rows of sender s for local expert e): padded offsets,
+    block table, and piece_row [n_src, E], where sender s's rows for e land."""
+    c = _c(counts, np.int32)
+    n_src, E = c.shape
+    po = np.empty(E + 1, np.int32)
+    cap = int(c.sum()) // P + E
+    meta = np.empty((max(cap, 1), 3), np.int32)
+    nb = np.zeros(1, np.int32)
+    piece_row = np.empty((n_src, E), np.int32)
+    _check(_L().or_blocks_from_counts(n_src, E, P, _p(c), _p(po), _p(meta), _p(nb),
+                                      _p(piece_row)), "blocks_from_counts")
+    n = int(nb[0])
+    return dict(padded_offsets=po, block_metadata=meta[:n].copy(), num_blocks=n,
+                piece_row=piece_row)
 
 
 def permute(x, row_src, k: int) -> np.ndarray:

@@ -278,6 +278,47 @@ int or_build_offsets(long long A, int E, int P, const int32_t *idx, const double
     return OR_OK;
 }
 
+/* The receiving side of the expert-parallel dispatch ("Dropless and grouped
+ * GEMM", sec. 4 step 5 and sec. 14: the exchange lands rows already grouped by
+ * expert and padded; the receiver learns how many rows each sender has for
+ * each of its experts).  counts[s * E + e] rows of sender s for local expert
+ * e.  Expert e's segment holds the senders' rows back to back, in sender
+ * order, and is padded like any segment: size ceil(c_e / P) * P with
+ * c_e = sum over s of counts[s, e].  piece_row[s * E + e] is where sender
+ * s's rows for e begin.  The block table follows the segments exactly as in
+ * or_build_offsets (its valid rows form a prefix of each segment). */
+int or_blocks_from_counts(int n_src, int E, int P, const int32_t *counts, int32_t *padded_offsets,
+                          int32_t *block_metadata, int32_t *num_blocks, int32_t *piece_row)
+{
+    if (n_src <= 0 || E <= 0 || P <= 0) return OR_ERR_ARG;
+    padded_offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        long long c = 0;
+        for (int s = 0; s < n_src; ++s) {
+            if (counts[(size_t)s * E + e] < 0) return OR_ERR_DATA;
+            c += counts[(size_t)s * E + e];
+        }
+        padded_offsets[e + 1] = padded_offsets[e] + (int32_t)(((c + P - 1) / P) * P);
+    }
+    int nb = 0;
+    for (int e = 0; e < E; ++e) {
+        int row = padded_offsets[e];
+        for (int s = 0; s < n_src; ++s) {
+            piece_row[(size_t)s * E + e] = row;
+            row += counts[(size_t)s * E + e];
+        }
+        int c = row - padded_offsets[e];
+        for (int m = 0; m < c; m += P) {
+            block_metadata[3 * nb + 0] = e;
+            block_metadata[3 * nb + 1] = padded_offsets[e] + m;
+            block_metadata[3 * nb + 2] = c - m < P ? c - m : P;
+            ++nb;
+        }
+    }
+    *num_blocks = nb;
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------- permute -- */
 
 /* x_perm[r] = x[row_src[r] / k] for every valid padded row r; pad rows are

@@ -35,7 +35,7 @@ __all__ = [
     "MoeWeightsBwd", "MoeGrads", "moe_pack_experts_bwd", "moe_pack_router_bwd",
     "moe_backward_workspace_size", "moe_layer_bwd", "moe_gate_up_save_size", "moe_layer_fwd_save",
     "moe_widen_e4m3", "moe_grouped_gemm_swiglu_scaled", "moe_shared_expert_scaled",
-    "moe_gather_rows",
+    "moe_gather_rows", "moe_build_blocks_from_counts", "moe_copy_pieces",
 ]
 
 MOE_OK = 0
@@ -140,6 +140,8 @@ def load():
         "moe_gate_up_save_size": (SZ, [CP]),
         "moe_widen_e4m3": (ctypes.c_int, [P, P, ctypes.c_int64, P]),
         "moe_gather_rows": (ctypes.c_int, [P, P, P, ctypes.c_int64, I32, P, P, P]),
+        "moe_build_blocks_from_counts": (ctypes.c_int, [P, I32, I32, I32, P, P, P, I32, P, P, P]),
+        "moe_copy_pieces": (ctypes.c_int, [P, P, I32, P, P, P, I32, I32, P, P, P]),
         "moe_grouped_gemm_swiglu_scaled": (ctypes.c_int, [CP] + [P] * 13),
         "moe_shared_expert_scaled": (ctypes.c_int, [CP] + [P] * 9),
         "moe_layer_fwd_save": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ,
@@ -389,6 +391,25 @@ def moe_backward_workspace_size(cfg: MoeConfig) -> int:
 def moe_gather_rows(src, idx, dst, src_gate=None, dst_gate=None, stream=None) -> None:
     """dst[i] = src[idx[i]] (bf16 rows; gates too when given)."""
     _check(load().moe_gather_rows(_ptr(src), _ptr(idx), _ptr(dst), idx.numel(), src.shape[-1],
+                                  _ptr(src_gate), _ptr(dst_gate), _stream(stream)))
+
+
+def moe_build_blocks_from_counts(counts, P: int, padded_offsets, block_metadata, num_blocks,
+                                 piece_row=None, status=None, stream=None) -> None:
+    """The expert-major layout of rows that arrive as counts [n_src, E] (int32,
+    device): padded offsets, block table, and where each sender's rows land."""
+    n_src, E = counts.shape
+    _check(load().moe_build_blocks_from_counts(
+        _ptr(counts), n_src, E, P, _ptr(padded_offsets), _ptr(block_metadata), _ptr(num_blocks),
+        block_metadata.shape[0], _ptr(piece_row), _ptr(status), _stream(stream)))
+
+
+def moe_copy_pieces(src, dst, src_row, dst_row, rows, max_rows: int, src_gate=None, dst_gate=None,
+                    stream=None) -> None:
+    """Row pieces src[src_row[i] : + rows[i]] -> dst[dst_row[i] : + rows[i]]
+    (device int32 descriptors; gates alongside when given)."""
+    _check(load().moe_copy_pieces(_ptr(src), _ptr(dst), src.shape[-1], _ptr(src_row),
+                                  _ptr(dst_row), _ptr(rows), rows.numel(), int(max_rows),
                                   _ptr(src_gate), _ptr(dst_gate), _stream(stream)))
 
 

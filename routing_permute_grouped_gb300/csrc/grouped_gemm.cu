@@ -302,6 +302,19 @@ __device__ __forceinline__ void epi_partial(const GemmArgs& a, const TileInfo& t
     }
 }
 
+// Where a CTA of the dense router GEMMs starts its K loop.  Every CTA streams
+// its own 128 token rows, and with a power-of-two row pitch the rows of all
+// CTAs at the same K offset fall on few DRAM channels; starting each CTA at
+// a different K block (and wrapping around) spreads the concurrent reads.
+// The MMAs accumulate in the rotated order: a fixed order per CTA.
+__device__ __forceinline__ int k_rotation(int nk) {
+    return nk > 1 ? static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(nk)) : 0;
+}
+__device__ __forceinline__ int rotated_k(int kb, int kb0, int kb1, int rot) {
+    int k = kb + rot;
+    return k >= kb1 ? k - (kb1 - kb0) : k;
+}
+
 // -------------------------------------------------------------- kernel --
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -372,15 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int brow = split ? 0 : ti.e * args.b_rows_per_expert + ti.nb * BN;
                 const int kb0 = split ? ti.nb * args.k_per_split : 0;
                 const int kb1 = split ? min(kb0 + args.k_per_split, args.k_blocks) : args.k_blocks;
+                const int rot = k_rotation(kb1 - kb0);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
                         timed_out = true;
                         break;
                     }
                     armed &= ~(1u << s);
+                    const int kx = rotated_k(kb, kb0, kb1, rot) * BK;
                     mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
-                    tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, ti.m0, full + s);
-                    tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * BK, brow, full + s);
+                    tma_load_2d(sA + s * C::A_BYTES, &tmA, kx, ti.m0, full + s);
+                    tma_load_2d(sB + s * C::B_BYTES, &tmB, kx, brow, full + s);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -482,6 +497,288 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (timed_out) *abort_flag = 1;
     }
 
+    if (timed_out && args.status) atomicOr(args.status, kDevErrTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------- split-K router over a cluster --
+//
+// The router GEMM for batches whose 128-token tiles cannot fill the GPU
+// ("MoE & MLA operators", sec. 2.2: logits = x W_g, then top-k and softmax):
+// the K range is split into S slices, and the S CTAs that share one 128-token
+// tile form a thread-block cluster (rank = slice).  Each CTA accumulates its
+// slice's fp32 partial logits in tensor memory; slices 1..S-1 store theirs
+// into slice 0's shared memory (distributed shared memory), and slice 0 sums
+// them in slice order, adds the bias and picks the experts.  One launch, no
+// global scratch, and a fixed summation order.
+
+// Group limit, top-k and softmax of one token's logits held in registers (the
+// bias already added).  The same rules as epi_router: a group's score is its
+// largest logit, the topk_groups best groups stay eligible, top-k runs over
+// the eligible experts in ascending index order with strict comparisons (the
+// lower index wins a tie), the gates are a softmax over the k chosen logits.
+template <int BN>
+__device__ __forceinline__ void route_row(const GemmArgs& a, const float (&l)[BN], int token) {
+    const int E = a.E, k = a.k;
+    uint32_t gmask = 0xFFFFFFFFu;
+    int gsz = E;
+    if (a.n_groups > 0) {
+        gsz = E / a.n_groups;
+        float gs[32];
+#pragma unroll
+        for (int g = 0; g < 32; ++g) gs[g] = -FLT_MAX;
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+            if (e < E) gs[e / gsz] = fmaxf(gs[e / gsz], l[e]);
+        gmask = 0;
+        for (int r = 0; r < a.topk_groups; ++r) {
+            int bi = -1;
+            float bv = -FLT_MAX;
+            for (int g = 0; g < a.n_groups; ++g) {
+                if (gmask & (1u << g)) continue;
+                if (bi < 0 || gs[g] > bv) {
+                    bi = g;
+                    bv = gs[g];
+                }
+            }
+            gmask |= 1u << bi;
+        }
+    }
+    float tv[8];
+    int te[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        tv[s] = -FLT_MAX;
+        te[s] = -1;
+    }
+#pragma unroll
+    for (int e = 0; e < BN; ++e) {
+        if (e < E && ((gmask >> (e / gsz)) & 1u)) {
+            float cv = l[e];
+            int ci = e;
+            bool shifting = false;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                if (s < k && (shifting || te[s] < 0 || cv > tv[s])) {
+                    const float tf = tv[s];
+                    const int tix = te[s];
+                    tv[s] = cv;
+                    te[s] = ci;
+                    cv = tf;
+                    ci = tix;
+                    shifting = true;
+                }
+            }
+        }
+    }
+    float sum = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+        if (s < k) sum += expf(tv[s] - tv[0]);
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        if (s < k) {
+            a.topk_idx[(int64_t)token * k + s] = te[s];
+            a.topk_w[(int64_t)token * k + s] = expf(tv[s] - tv[0]) * inv;
+        }
+    }
+}
+
+// Shared memory of k_router_cluster beyond the GEMM ring: the partial logits
+// that slices 1..S-1 hand to slice 0 ([S-1][128 rows][BN] fp32) and one flag
+// per (slice, epilogue warp) saying that the warp's rows arrived.
+template <int BN>
+constexpr int router_cluster_smem(int S) {
+    return GemmCfg<BN>::SMEM + (S - 1) * BM * BN * 4 + 4 * 8 * 4;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_router_cluster(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args) {
+    using C = GemmCfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* tfull = bars + 2 * S;
+    uint64_t* drain = tfull + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_holder + 1;
+    const int nsl = args.n_tiles;  // slices = CTAs of the cluster
+    float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + C::BAR_BYTES);
+    int* arrived = reinterpret_cast<int*>(red + (nsl - 1) * BM * BN);  // [S-1][4]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int m0 = (blockIdx.x / nsl) * BM;
+    pdl_trigger();
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        if (rank == 0)
+            for (int i = 0; i < (nsl - 1) * 4; ++i) arrived[i] = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    // inputs written by earlier kernels are visible after the wait; tensor
+    // memory is taken after it (see k_grouped_gemm)
+    pdl_wait();
+    if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // every CTA of the cluster runs (and slice 0's flags are clear)
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int kb0 = static_cast<int>(rank) * args.k_per_split;
+    const int kb1 = min(kb0 + args.k_per_split, args.k_blocks);
+    bool timed_out = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t armed = 0, armed_par = 0;
+            const int rot = k_rotation(kb1 - kb0);
+            for (int kb = kb0, s = 0, ph = 0; kb < kb1; ++kb) {
+                if (!mbar_wait(empty + s, ph ^ 1u, abort_flag)) {
+                    timed_out = true;
+                    break;
+                }
+                const int kx = rotated_k(kb, kb0, kb1, rot) * BK;
+                mbar_arrive_expect_tx(full + s, C::STAGE_BYTES);
+                tma_load_2d(sA + s * C::A_BYTES, &tmA, kx, m0, full + s);
+                tma_load_2d(sB + s * C::B_BYTES, &tmB, kx, 0, full + s);
+                armed |= 1u << s;
+                armed_par = (armed_par & ~(1u << s)) | (static_cast<uint32_t>(ph) << s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (timed_out || *abort_flag) {
+                *abort_flag = 1;
+                for (int i = 0; i < S; ++i)
+                    if (armed & (1u << i)) {
+                        volatile uint32_t never = 0;
+                        (void)mbar_wait(full + i, (armed_par >> i) & 1u, &never);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            bool issued = false;
+            for (int kb = kb0, s = 0, ph = 0; kb < kb1; ++kb) {
+                if (!mbar_wait(full + s, ph, abort_flag)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + s * C::A_BYTES);
+                const uint32_t b_addr = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(tmem_base, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32),
+                             idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+                issued = true;
+                mma_commit(empty + s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (!timed_out) mma_commit(tfull);
+            if ((timed_out || *abort_flag) && issued) {
+                *abort_flag = 1;
+                mma_commit(drain);
+                volatile uint32_t never = 0;
+                (void)mbar_wait(drain, 0, &never);
+            }
+        }
+    }
+
+    // epilogue warps: this thread's row of partial logits, out of tensor memory
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    float v[BN];
+    bool have = false;
+    if (warp >= 2) {
+        have = __all_sync(0xFFFFFFFFu, mbar_wait(tfull, 0, abort_flag));
+        if (have) {
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < BN / 16; ++c) {
+                uint32_t r[16];
+                tmem_ld16(taddr + c * 16, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+            }
+            if (rank != 0) {
+                // hand the row to slice 0, then flag the warp's rows as there
+                const uint32_t dst =
+                    mapa_shared(smem_u32(red + ((static_cast<int>(rank) - 1) * BM + row) * BN), 0);
+#pragma unroll
+                for (int i = 0; i < BN; i += 4) st_cluster_v4(dst + 4 * i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t f = mapa_shared(smem_u32(arrived + (static_cast<int>(rank) - 1) * 4 + q), 0);
+                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(f), "r"(1) : "memory");
+                }
+            }
+        } else {
+            timed_out = true;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the partial rows are in slice 0's shared memory
+    if (warp >= 2 && rank == 0 && have) {
+        bool all = true;
+        for (int i = 0; i < (nsl - 1); ++i) all = all && arrived[i * 4 + q] != 0;
+        if (all) {
+            // slice order: own slice (0), then 1 .. S-1
+            for (int sl = 1; sl < nsl; ++sl) {
+                const float4* p = reinterpret_cast<const float4*>(red + ((sl - 1) * BM + row) * BN);
+#pragma unroll
+                for (int i = 0; i < BN / 4; ++i) {
+                    const float4 w = p[i];
+                    v[4 * i] += w.x;
+                    v[4 * i + 1] += w.y;
+                    v[4 * i + 2] += w.z;
+                    v[4 * i + 3] += w.w;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < BN; ++e)
+                if (args.bias && e < args.E) v[e] += ld_dep(args.bias + e);
+            if (m0 + row < args.dense_rows) route_row<BN>(args, v, m0 + row);
+        } else {
+            timed_out = true;  // a slice gave up: its rows never arrived
+        }
+    }
     if (timed_out && args.status) atomicOr(args.status, kDevErrTimeout);
     tc_fence_before();
     __syncthreads();
@@ -715,8 +1012,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // an expert's weight panels are re-read by every visit of that
         // expert: keep them in L2 ahead of the streamed activation rows
         const uint64_t keep = l2_policy_evict_last();
-        for (int t = cluster; t < total && !timed_out; t += nclusters) {
+        // Consecutive waves of the pair grid run the K loop in opposite
+        // directions: a wave's CTA pairs share the weight panels of one expert
+        // with the wave before, and starting where that wave stopped finds the
+        // panels' last-loaded K blocks still in L2 (GEMM1 at the default
+        // workload read 19 % fewer DRAM bytes).  The accumulation order of a
+        // tile is fixed by its position in the visit list.
+        int wave = 0;
+        for (int t = cluster; t < total && !timed_out; t += nclusters, ++wave) {
             const PairTile p = decode_pair(args, t, vpref);
+            const bool rev = wave & 1;
             const int arow = p.m0 + BM * static_cast<int>(rank);
             const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
             int grow[4] = {0, 0, 0, 0};
@@ -741,13 +1046,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     armed &= ~(1u << s);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
-                    if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, arow, full_leader);
-                    tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, kb * BK, brow, full_leader, keep);
+                    const int kx = (rev ? args.k_blocks - 1 - kb : kb) * BK;
+                    if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kx, arow, full_leader);
+                    tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, kx, brow, full_leader, keep);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                 }
                 if (GATHER)
-                    tma_gather4_pair(smem_u32(sA + s * A_BYTES) + lane * 512u, &tmA, kb * BK, grow[0],
+                    tma_gather4_pair(smem_u32(sA + s * A_BYTES) + lane * 512u, &tmA,
+                                     (rev ? args.k_blocks - 1 - kb : kb) * BK, grow[0],
                                      grow[1], grow[2], grow[3], full_leader);
                 if (++s == S) {
                     s = 0;
@@ -940,6 +1247,64 @@ static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const 
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(k_grouped_gemm<BN, EPI>, dim3(grid), dim3(kThreads), C::SMEM, stream, tA, tB,
                       args);
+}
+
+template <int BN>
+static cudaError_t launch_router_cluster_t(const CUtensorMap& tA, const CUtensorMap& tB,
+                                           const GemmArgs& args, int m_tiles, int slices,
+                                           cudaStream_t stream) {
+    const int smem = router_cluster_smem<BN>(slices);
+    static int attr_smem[64] = {};  // per device: the largest size set so far
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (attr_smem[dev] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_router_cluster<BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_smem[dev] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(m_tiles * slices, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = slices;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_router_cluster<BN>, tA, tB, args);
+}
+
+bool router_cluster_fits(int bn, int slices) {
+    // up to 4 slices: with 8 the clustered launch (8 co-scheduled CTAs of up
+    // to 206 KB each) measured slower than partial logits + a reduce kernel
+    if (slices < 2 || slices > 4) return false;
+    switch (bn) {
+        case 16: return router_cluster_smem<16>(slices) <= 232448;
+        case 32: return router_cluster_smem<32>(slices) <= 232448;
+        case 64: return router_cluster_smem<64>(slices) <= 232448;
+        default: return false;
+    }
+}
+
+cudaError_t launch_router_cluster(int bn, const void* x, int64_t T, const void* Wg_t, int64_t E,
+                                  int64_t K, const GemmArgs& args, int slices, cudaStream_t stream) {
+    if (!router_cluster_fits(bn, slices)) return cudaErrorInvalidValue;
+    CUtensorMap tA, tB;
+    if (!make_tmap(&tA, x, T, K, BM) || !make_tmap(&tB, Wg_t, E, K, bn)) return cudaErrorInvalidValue;
+    const int m_tiles = static_cast<int>((T + BM - 1) / BM);
+    switch (bn) {
+        case 16: return launch_router_cluster_t<16>(tA, tB, args, m_tiles, slices, stream);
+        case 32: return launch_router_cluster_t<32>(tA, tB, args, m_tiles, slices, stream);
+        case 64: return launch_router_cluster_t<64>(tA, tB, args, m_tiles, slices, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int BN, int EPI, bool GATHER>

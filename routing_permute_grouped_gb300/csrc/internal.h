@@ -74,6 +74,14 @@ struct GemmArgs {
     float* topk_w;
 };
 
+// The split-K router on clusters of `slices` CTAs (one per K slice of a
+// 128-token tile; top-k fused after a distributed-shared-memory reduction).
+// router_cluster_fits says whether a router of tile width bn with that many
+// slices takes the kernel (2..4 slices, bn <= 64, shared-memory budget).
+bool router_cluster_fits(int bn, int slices);
+cudaError_t launch_router_cluster(int bn, const void* x, int64_t T, const void* Wg_t, int64_t E,
+                                  int64_t K, const GemmArgs& args, int slices, cudaStream_t stream);
+
 enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 3, kEpiPartial = 4 };
 
 // Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
@@ -195,6 +203,13 @@ cudaError_t launch_router_reduce(const float* partial, int S, int T, int E, int 
                                  int topk_groups, const float* bias, int32_t* topk_idx,
                                  float* topk_w, cudaStream_t stream);
 
+cudaError_t launch_blocks_from_counts(const int32_t* counts, int n_src, int E, int P,
+                                      int32_t* padded_offsets, int32_t* block_metadata,
+                                      int32_t* num_blocks, int nb_cap, int32_t* piece_row,
+                                      uint32_t* status, cudaStream_t stream);
+cudaError_t launch_copy_pieces(const void* src, void* dst, int d, const int32_t* src_row,
+                               const int32_t* dst_row, const int32_t* rows, int n, int max_rows,
+                               const float* sgate, float* dgate, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 
 constexpr int kMaxDevices = 64;

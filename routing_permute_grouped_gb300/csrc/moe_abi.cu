@@ -116,6 +116,16 @@ static int router_splits(const moe_config_t& c) {
     return (k_blocks + per - 1) / per;
 }
 
+static int router_bn(int E);
+
+// The split-K router runs as one clustered kernel (slices reduced through
+// distributed shared memory, no scratch) when its slices and tile width fit
+// that kernel; otherwise as partial logits in a scratch + a reduce kernel.
+static bool router_uses_cluster(const moe_config_t& c) {
+    const int S = router_splits(c);
+    return S > 1 && router_cluster_fits(router_bn(c.E), S);
+}
+
 // The small-M kernel serves the layer when the mean rows per expert is small
 // enough that 256-row visits would mostly multiply padding.
 static bool use_skinny(const moe_config_t& c) {
@@ -155,7 +165,8 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c, bool fp8 = false)
     L.hs = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d_shared : 0) * 2);
     L.ys = take(static_cast<size_t>(c.T) * (c.d_shared ? c.d : 0) * 2);
     const int S = router_splits(c);
-    L.router_partial = take(S > 1 ? static_cast<size_t>(S) * c.T * c.E * 4 : 0);
+    L.router_partial =
+        take(S > 1 && !router_uses_cluster(c) ? static_cast<size_t>(S) * c.T * c.E * 4 : 0);
     // e4m3-weight layer only: token-row pairs for the shared expert, the pairs
     // of h (routed then shared) and the row scales (x, h, shared x, shared h)
     const size_t ds = c.d_shared ? static_cast<size_t>(c.d_shared) : 0;
@@ -209,7 +220,7 @@ static moe_status_t do_route(const moe_config_t& c, const void* x, const void* W
 // fills the GPU, otherwise split-K partial logits + a reduce/top-k kernel.
 static moe_status_t do_route_layer(const moe_config_t& c, const void* x, const void* Wg_t,
                                    const float* bias, int32_t* topk_idx, float* topk_w,
-                                   float* partial, cudaStream_t st) {
+                                   float* partial, cudaStream_t st, uint32_t* status = nullptr) {
     const int S = router_splits(c);
     if (S <= 1) return do_route(c, x, Wg_t, bias, topk_idx, topk_w, st);
     GemmArgs a{};
@@ -218,6 +229,17 @@ static moe_status_t do_route_layer(const moe_config_t& c, const void* x, const v
     a.k_blocks = c.d / 64;
     a.k_per_split = (a.k_blocks + S - 1) / S;
     a.E = c.E;
+    if (router_uses_cluster(c)) {
+        a.bias = bias;
+        a.k = c.k;
+        a.n_groups = c.n_groups;
+        a.topk_groups = c.topk_groups;
+        a.topk_idx = topk_idx;
+        a.topk_w = topk_w;
+        a.status = status;
+        cudaError_t e = launch_router_cluster(router_bn(c.E), x, c.T, Wg_t, c.E, c.d, a, S, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router GEMM (split K over a cluster)");
+    }
     a.partial = partial;
     const int tiles = ((c.T + 127) / 128) * S;
     cudaError_t e = launch_grouped_gemm(kEpiPartial, router_bn(c.E), x, c.T, Wg_t, c.E, c.d, a,
@@ -450,7 +472,8 @@ static moe_status_t layer_front(const moe_config_t& c, const void* Wg_t, const f
     float* topk_w = static_cast<float*>(B.at(B.L.topk_w));
     if (!pre_idx) {
         moe_status_t r = do_route_layer(c, x, Wg_t, bias, topk_idx, topk_w,
-                                        static_cast<float*>(B.at(B.L.router_partial)), st);
+                                        static_cast<float*>(B.at(B.L.router_partial)), st,
+                                        B.status());
         if (r != MOE_OK) return r;
     } else {
         topk_idx = const_cast<int32_t*>(pre_idx);
@@ -926,7 +949,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg_t,
 size_t moe_route_splitk_scratch_size(const moe_config_t* cfg) {
     if (check_cfg(cfg, true) != MOE_OK) return 0;
     const int S = router_splits(*cfg);
-    return S > 1 ? static_cast<size_t>(S) * cfg->T * cfg->E * 4 : 0;
+    return S > 1 && !router_uses_cluster(*cfg) ? static_cast<size_t>(S) * cfg->T * cfg->E * 4 : 0;
 }
 
 moe_status_t moe_route_splitk(const moe_config_t* cfg, const void* x, const void* Wg_t,
@@ -998,6 +1021,38 @@ moe_status_t moe_gather_rows(const void* src, const int32_t* idx, void* dst, int
     cudaError_t e = launch_gather_rows(src, idx, dst, n, d, src_gate, dst_gate,
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gather rows");
+}
+
+moe_status_t moe_build_blocks_from_counts(const int32_t* counts, int32_t n_src, int32_t E,
+                                          int32_t P, int32_t* padded_offsets,
+                                          int32_t* block_metadata, int32_t* num_blocks,
+                                          int32_t nb_cap, int32_t* piece_row, uint32_t* status,
+                                          void* stream) {
+    if (n_src <= 0 || E <= 0 || nb_cap < 0) return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+    if (E > 256) return fail(MOE_ERR_UNSUPPORTED, "E = %d > 256", E);
+    if (P != 64 && P != 128) return fail(MOE_ERR_UNSUPPORTED, "P = %d must be 64 or 128", P);
+    if (!counts || !padded_offsets || !num_blocks || (nb_cap > 0 && !block_metadata))
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    cudaError_t e = launch_blocks_from_counts(counts, n_src, E, P, padded_offsets, block_metadata,
+                                              num_blocks, nb_cap, piece_row, status,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "blocks from counts");
+}
+
+moe_status_t moe_copy_pieces(const void* src, void* dst, int32_t d, const int32_t* src_row,
+                             const int32_t* dst_row, const int32_t* rows, int32_t n,
+                             int32_t max_rows, const float* src_gate, float* dst_gate,
+                             void* stream) {
+    if (n < 0 || d <= 0 || max_rows < 0) return fail(MOE_ERR_INVALID_ARG, "bad piece sizes");
+    if (d % 8) return fail(MOE_ERR_UNSUPPORTED, "d = %d is not a multiple of 8", d);
+    if (n > 65535) return fail(MOE_ERR_UNSUPPORTED, "n = %d pieces > 65535", n);
+    if ((src_gate == nullptr) != (dst_gate == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "src_gate and dst_gate must both be given or both be NULL");
+    if (n == 0 || max_rows == 0) return MOE_OK;
+    if (!src || !dst || !src_row || !dst_row || !rows) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    cudaError_t e = launch_copy_pieces(src, dst, d, src_row, dst_row, rows, n, max_rows, src_gate,
+                                       dst_gate, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "copy pieces");
 }
 
 moe_status_t moe_widen_e4m3(const void* q, void* out, int64_t n, void* stream) {

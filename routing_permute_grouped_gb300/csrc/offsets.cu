@@ -24,10 +24,12 @@
 namespace moe {
 
 constexpr int kChunk = 2048;     // assignments per chunk
-constexpr int kScatterThreads = 256;
+constexpr int kScatterThreads = 1024;  // two passes over a chunk
 constexpr int kScanThreads = 1024;
 constexpr int kMaxE = 256;
+constexpr int kScanStaged = 8192;  // chunk counts k_scan stages in shared memory (32 KB)
 constexpr uint32_t kDevErrExpert = 0x1u;
+constexpr uint32_t kDevErrSegment = 0x4u;  // counts that do not fit the layout
 
 int64_t offsets_num_chunks(int64_t A) { return (A + kChunk - 1) / kChunk; }
 
@@ -85,21 +87,54 @@ __global__ void __launch_bounds__(kScanThreads)
     __shared__ int s_size[kMaxE];
     __shared__ int s_nblk[kMaxE];
     __shared__ int s_cnt[kMaxE];
+    __shared__ int s_po[kMaxE];
     __shared__ int s_total[2];
+    extern __shared__ int s_cc[];  // [n_chunks][E] when it fits (staged), else unused
+    const bool staged = static_cast<int64_t>(n_chunks) * E <= kScanStaged;
     const int e = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (staged) {
+        // exclusive prefix over the chunks of every expert: the counts come in
+        // with one coalesced pass, a warp scans an expert's column 32 chunks
+        // at a time, the first ranks go back out with one coalesced pass
+        const int n = n_chunks * E;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) s_cc[i] = chunk_counts[i];
+        __syncthreads();
+        for (int ex = warp; ex < E; ex += blockDim.x >> 5) {
+            int running = 0;
+            for (int base = 0; base < n_chunks; base += 32) {
+                const int c = base + lane;
+                const int v = c < n_chunks ? s_cc[c * E + ex] : 0;
+                int x = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (c < n_chunks) s_cc[c * E + ex] = running + x - v;
+                running += __shfl_sync(0xFFFFFFFFu, x, 31);
+            }
+            if (lane == 0) s_cnt[ex] = running;
+        }
+        __syncthreads();
+    }
     int cnt = 0;
     if (e < E) {
-        // exclusive prefix over the chunks, in place: chunk c's first rank
-        for (int c = 0; c < n_chunks; ++c) {
-            const int v = chunk_counts[(int64_t)c * E + e];
-            chunk_counts[(int64_t)c * E + e] = cnt;
-            cnt += v;
+        if (staged) {
+            cnt = s_cnt[e];
+        } else {
+            // exclusive prefix over the chunks, in place: chunk c's first rank
+            for (int c = 0; c < n_chunks; ++c) {
+                const int v = chunk_counts[(int64_t)c * E + e];
+                chunk_counts[(int64_t)c * E + e] = cnt;
+                cnt += v;
+            }
         }
         s_size[e] = ((cnt + P - 1) / P) * P;  // ceil(c/P)*P, 0 for an empty expert
         s_nblk[e] = (cnt + P - 1) / P;
-        s_cnt[e] = cnt;
     }
     __syncthreads();
+    if (e < E) s_cnt[e] = cnt;
     // inclusive Hillis-Steele scans of sizes and block counts over E <= 256
     for (int off = 1; off < E; off <<= 1) {
         int vs = 0, vb = 0;
@@ -126,8 +161,10 @@ __global__ void __launch_bounds__(kScanThreads)
         const int b0 = s_nblk[e] - nblk;   // exclusive
         counts[e] = cnt;
         padded_offsets[e] = po;
+        s_po[e] = po;
         if (e == E - 1) padded_offsets[E] = s_total[0];
-        for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += po;
+        if (!staged)
+            for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += po;
         for (int i = 0; i < nblk; ++i) {
             block_metadata[3 * (b0 + i) + 0] = e;
             block_metadata[3 * (b0 + i) + 1] = po + i * P;
@@ -135,6 +172,11 @@ __global__ void __launch_bounds__(kScanThreads)
         }
     }
     if (e == 0) *num_blocks = s_total[1];
+    if (staged) {
+        __syncthreads();
+        const int n = n_chunks * E;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) chunk_counts[i] = s_cc[i] + s_po[i % E];
+    }
     fill_pad_rows(s_size, s_cnt, E, P, row_src, row_gate);
     for (int64_t r = s_total[0] + threadIdx.x; r < R_max; r += blockDim.x) {
         row_src[r] = -1;
@@ -310,6 +352,90 @@ __global__ void __launch_bounds__(kSmallThreads)
     }
 }
 
+// The receiving side of an expert-parallel dispatch: from counts [n_src, E]
+// (rows of sender s for local expert e) the padded offsets, the block table
+// and piece_row [n_src, E] (where sender s's rows for e begin).  Expert e's
+// segment holds the senders' rows back to back in sender order and is
+// padded to a multiple of P, so its valid rows form a prefix, as in the
+// single-GPU layout.  One CTA, a thread per expert.
+__global__ void __launch_bounds__(kScanThreads)
+    k_blocks_from_counts(const int32_t* __restrict__ counts, int n_src, int E, int P,
+                         int32_t* __restrict__ padded_offsets, int32_t* __restrict__ block_metadata,
+                         int32_t* __restrict__ num_blocks, int nb_cap,
+                         int32_t* __restrict__ piece_row, uint32_t* status) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int s_size[kMaxE];
+    __shared__ int s_nblk[kMaxE];
+    __shared__ int s_total[2];
+    const int e = threadIdx.x;
+    int cnt = 0;
+    bool bad = false;
+    if (e < E) {
+        for (int s = 0; s < n_src; ++s) {
+            const int v = ld_dep(counts + static_cast<int64_t>(s) * E + e);
+            if (v < 0) bad = true;
+            cnt += v > 0 ? v : 0;
+        }
+        s_size[e] = ((cnt + P - 1) / P) * P;
+        s_nblk[e] = (cnt + P - 1) / P;
+    }
+    __syncthreads();
+    for (int off = 1; off < E; off <<= 1) {
+        int vs = 0, vb = 0;
+        if (e < E && e >= off) {
+            vs = s_size[e - off];
+            vb = s_nblk[e - off];
+        }
+        __syncthreads();
+        if (e < E && e >= off) {
+            s_size[e] += vs;
+            s_nblk[e] += vb;
+        }
+        __syncthreads();
+    }
+    if (e == E - 1) {
+        s_total[0] = s_size[e];
+        s_total[1] = s_nblk[e];
+    }
+    __syncthreads();
+    if (e < E) {
+        const int size = ((cnt + P - 1) / P) * P;
+        const int nblk = (cnt + P - 1) / P;
+        const int po = s_size[e] - size;
+        const int b0 = s_nblk[e] - nblk;
+        padded_offsets[e] = po;
+        if (e == E - 1) padded_offsets[E] = s_total[0];
+        if (piece_row) {
+            int row = po;
+            for (int s = 0; s < n_src; ++s) {
+                piece_row[static_cast<int64_t>(s) * E + e] = row;
+                const int v = ld_dep(counts + static_cast<int64_t>(s) * E + e);
+                row += v > 0 ? v : 0;
+            }
+        }
+        for (int i = 0; i < nblk; ++i) {
+            if (b0 + i >= nb_cap) {
+                bad = true;
+                break;
+            }
+            block_metadata[3 * (b0 + i) + 0] = e;
+            block_metadata[3 * (b0 + i) + 1] = po + i * P;
+            block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
+        }
+    }
+    if (e == 0) *num_blocks = min(s_total[1], nb_cap);
+    if (bad && status) atomicOr(status, kDevErrSegment);
+}
+
+cudaError_t launch_blocks_from_counts(const int32_t* counts, int n_src, int E, int P,
+                                      int32_t* padded_offsets, int32_t* block_metadata,
+                                      int32_t* num_blocks, int nb_cap, int32_t* piece_row,
+                                      uint32_t* status, cudaStream_t stream) {
+    return launch_pdl(k_blocks_from_counts, dim3(1), dim3(kScanThreads), 0, stream, counts, n_src, E,
+                      P, padded_offsets, block_metadata, num_blocks, nb_cap, piece_row, status);
+}
+
 cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t A, int E, int P,
                            int64_t R_max, int32_t* counts, int32_t* padded_offsets,
                            int32_t* block_metadata, int32_t* num_blocks, int32_t* perm_row,
@@ -326,7 +452,9 @@ cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t
                                    topk_idx, A, E, chunk_scratch, status);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = launch_pdl(k_scan, dim3(1), dim3(kScanThreads), 0, stream, n_chunks, E, P,
+    const size_t scan_smem = static_cast<int64_t>(n_chunks) * E <= kScanStaged
+                                 ? static_cast<size_t>(n_chunks) * E * 4 : 0;
+    cudaError_t e = launch_pdl(k_scan, dim3(1), dim3(kScanThreads), scan_smem, stream, n_chunks, E, P,
                                R_max, chunk_scratch, counts, padded_offsets, block_metadata,
                                num_blocks, row_src, row_gate);
     if (e != cudaSuccess) return e;

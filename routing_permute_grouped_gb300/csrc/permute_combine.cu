@@ -447,6 +447,40 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* idx, void* dst, i
                       dgate);
 }
 
+// Row pieces between two row-major buffers: piece i moves rows
+// [src_row[i], src_row[i] + rows[i]) of src to [dst_row[i], ...) of dst (and
+// their gates).  Grid (row groups, pieces); one warp per row, 16-byte
+// accesses.  The piece descriptors live in device memory, so the local part
+// of an expert-parallel exchange needs no index array from the host.
+__global__ void __launch_bounds__(kPCWarps * 32)
+    k_copy_pieces(const uint4* __restrict__ src, uint4* __restrict__ dst, int nvec,
+                  const int32_t* __restrict__ src_row, const int32_t* __restrict__ dst_row,
+                  const int32_t* __restrict__ rows, const float* __restrict__ sgate,
+                  float* __restrict__ dgate) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int p = blockIdx.y;
+    const int r = blockIdx.x * kPCWarps + (threadIdx.x >> 5);
+    if (r >= ld_dep(rows + p)) return;
+    const int64_t s = ld_dep(src_row + p) + static_cast<int64_t>(r);
+    const int64_t d = ld_dep(dst_row + p) + static_cast<int64_t>(r);
+    const uint4* sr = src + s * nvec;
+    uint4* dr = dst + d * nvec;
+    for (int v = lane; v < nvec; v += 32) dr[v] = ld_dep(sr + v);
+    if (dgate && lane == 0) dgate[d] = ld_dep(sgate + s);
+}
+
+cudaError_t launch_copy_pieces(const void* src, void* dst, int d, const int32_t* src_row,
+                               const int32_t* dst_row, const int32_t* rows, int n, int max_rows,
+                               const float* sgate, float* dgate, cudaStream_t stream) {
+    if (n <= 0 || max_rows <= 0) return cudaSuccess;
+    const int gx = (max_rows + kPCWarps - 1) / kPCWarps;
+    return launch_pdl(k_copy_pieces, dim3(gx, n), dim3(kPCWarps * 32), 0, stream,
+                      static_cast<const uint4*>(src), static_cast<uint4*>(dst), d / 8, src_row,
+                      dst_row, rows, sgate, dgate);
+}
+
 cudaError_t launch_permute_fp8(const void* x, const int32_t* perm_row, uint8_t* x8, float* x_scale,
                                uint8_t* xs8, float* xs_scale, int T, int d, int k,
                                cudaStream_t stream) {

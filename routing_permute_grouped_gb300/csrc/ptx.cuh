@@ -245,6 +245,15 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
+// 16-byte store into the shared memory of a CTA of the cluster (own or peer),
+// given its shared::cluster address
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c,
+                                              float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a),
+                 "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // arrive on an mbarrier given by its shared::cluster address (own or peer CTA)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

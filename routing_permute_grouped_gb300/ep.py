@@ -5,103 +5,68 @@ a copy of the router and of the shared expert.  One layer forward:
 
   1. each rank routes its own tokens and permutes them into the padded
      expert-major layout over all E experts (the single-GPU stages);
-  2. the per-expert counts are exchanged, then each rank sends rank r' the
-     padded segment of each of r''s experts, one piece per expert, with
-     their routing weights ("Dropless and grouped GEMM", sec. 14: the
-     dispatch, whose landing write does the permute and the padding);
-  3. the pieces land straight in the receiver's expert-major layout: the W
-     senders' pieces of each local expert, in rank order, make one padded
-     segment (every piece is a multiple of P rows, so the concatenation is
-     again a padded segment), and the grouped GEMMs run on them with a
-     block table built from the counts;
+  2. the per-expert counts are exchanged with one all-to-all on the device,
+     and the receiver builds its expert-major layout from them on the device
+     (moe_build_blocks_from_counts: the padded offsets, the block table and
+     where each sender's rows land);
+  3. each rank sends rank r' its rows of each of r''s experts, one piece per
+     expert, with their routing weights ("Dropless and grouped GEMM", sec.
+     14: the dispatch, whose landing write does the permute and the padding);
+     the pieces land back to back, in sender order, in the receiver's segment
+     of that expert, so every segment holds its valid rows first, as in the
+     single-GPU layout, and the grouped GEMMs run on it as they are;
   4. the rows of y go back, piece by piece, into the senders' layout (the
      combine exchange) and each rank combines its tokens with its shared
      expert's rows, as the single-GPU layer does.
 
 Pieces between ranks travel as batched point-to-point sends and receives
-(NCCL between GPUs); the pieces a rank keeps move in one gather.  The
+(NCCL between GPUs); the pieces a rank keeps move with one device copy
+(moe_copy_pieces) whose descriptors are the device tables.  NCCL takes its
+sizes and offsets from the host, so the counts and the landing rows cross to
+the host once per layer (one copy of a few hundred bytes); the host only
+reads positions out of them (``plan_pieces``), it computes no layout.  The
 summation order of the combine is the single-GPU one, so a token's output
-does not depend on W.  The piece sizes are needed on the host: the
-per-expert counts cross to the host once per layer (a few hundred bytes).  The plan functions below are plain host logic over those counts;
-the compute steps go through a backend object (the CUDA library in
-``GpuEp``), so the exchange logic can be exercised on CPU process groups.
+does not depend on W.  The compute steps go through a backend object (the
+CUDA library in ``GpuEp``), so the exchange logic can be exercised on CPU
+process groups.
 """
 from __future__ import annotations
-
-from dataclasses import dataclass
 
 import numpy as np
 
 
-def padded(c, P: int):
-    """Padded segment size(s): ceil(c / P) * P, 0 for an empty expert."""
-    c = np.asarray(c, np.int64)
-    return -(-c // P) * P
+def plan_pieces(rank: int, El: int, counts, own_po, recv, piece_row):
+    """The pieces of both exchanges, read from the tables the devices made
+    (host copies).
 
+    counts     [E]      this rank's rows per global expert
+    own_po     [E + 1]  this rank's padded offsets (its own layout)
+    recv       [W, El]  rows every rank sends to this rank's experts
+    piece_row  [W, El]  where those rows land in this rank's expert-major
+                        layout
 
-@dataclass
-class DispatchPlan:
-    """Split sizes and the receiver's layout for one exchange.
-
-    send_rows[r']   rows this rank sends to rank r' (padded, r''s experts)
-    recv_rows[s]    rows this rank receives from rank s
-    padded_offsets  [El + 1] of the expert-major layout
-    block_metadata  [num_blocks, 3] = [local expert, m_start, valid_m]
-    rows            rows of the expert-major layout (= padded_offsets[-1])
-    send_pieces     (peer, row, rows): this rank's padded segments in its own
-                    layout, one per expert with rows, peers in order and each
-                    peer's experts in order (the dispatch's sends)
-    recv_pieces     (peer, row, rows): where each arriving piece lands in the
-                    expert-major layout; for every peer in the order that
-                    peer sends them
-    """
-    send_rows: np.ndarray
-    recv_rows: np.ndarray
-    padded_offsets: np.ndarray
-    block_metadata: np.ndarray
-    rows: int
-    send_pieces: list
-    recv_pieces: list
-
-
-def plan_dispatch(counts: np.ndarray, recv_counts: np.ndarray, P: int) -> DispatchPlan:
-    """counts [E]: this rank's assignments per global expert; recv_counts
-    [W, El]: what every rank s routes to this rank's local experts."""
-    recv_counts = np.asarray(recv_counts, np.int64)
-    W, El = recv_counts.shape
-    counts = np.asarray(counts, np.int64)
-    if counts.size != W * El:
-        raise ValueError("counts must cover W * El experts")
-    send_rows = padded(counts, P).reshape(W, El).sum(axis=1)
-    pieces = padded(recv_counts, P)                      # [W, El]
-    recv_rows = pieces.sum(axis=1)
-    seg_rows = pieces.sum(axis=0)                        # per local expert
-    po = np.concatenate([[0], np.cumsum(seg_rows)]).astype(np.int32)
-    # arriving pieces: expert-major, senders in rank order within an expert
-    n = pieces.T                                         # [El, W]
-    dst = po[:-1, None].astype(np.int64) + np.cumsum(n, axis=1) - n
-    ee, ss = np.nonzero(n)                               # row-major: e outer, s inner
-    recv_pieces = list(zip(ss.tolist(), dst[ee, ss].tolist(), n[ee, ss].tolist()))
-    # the block table: a piece of c rows holds ceil(c / P) blocks of P rows
-    c = recv_counts.T[ee, ss]
-    nblk = -(-c // P)
-    first = np.repeat(np.cumsum(nblk) - nblk, nblk)
-    m = (np.arange(int(nblk.sum())) - first) * P
-    block_metadata = np.stack([np.repeat(ee, nblk), np.repeat(dst[ee, ss], nblk) + m,
-                               np.minimum(P, np.repeat(c, nblk) - m)], axis=1).astype(np.int32)
-    own = padded(counts, P)
-    own_po = np.concatenate([[0], np.cumsum(own)])
-    g = np.flatnonzero(own)
-    send_pieces = list(zip((g // El).tolist(), own_po[g].tolist(), own[g].tolist()))
-    return DispatchPlan(send_rows, recv_rows, po, block_metadata, int(po[-1]), send_pieces,
-                        recv_pieces)
+    send_pieces (peer, row, rows): this rank's rows of expert g (from its own
+        segment start) go to rank g // El; peers in order, each peer's experts
+        in order.
+    recv_pieces (peer, row, rows): for every local expert (outer) and sender
+        (inner), where that sender's rows land.  Between two ranks the pieces
+        pair up in list order: both lists follow the receiver's experts."""
+    counts = np.asarray(counts, np.int64).reshape(-1)
+    own_po = np.asarray(own_po, np.int64).reshape(-1)
+    recv = np.asarray(recv, np.int64)
+    piece_row = np.asarray(piece_row, np.int64)
+    g = np.flatnonzero(counts > 0)
+    send_pieces = list(zip((g // El).tolist(), own_po[g].tolist(), counts[g].tolist()))
+    ee, ss = np.nonzero(recv.T > 0)  # expert outer, sender inner
+    recv_pieces = list(zip(ss.tolist(), piece_row[ss, ee].tolist(), recv[ss, ee].tolist()))
+    return send_pieces, recv_pieces
 
 
 class EpLayerBase:
     """The exchange of an expert-parallel layer forward over a process group;
-    subclasses supply the compute steps (``front``, ``local_experts``,
-    ``finish``) and the tensors' device.  Row pieces move with
-    torch.distributed's batched point-to-point operations (NCCL between
+    subclasses supply the compute steps (``front``, ``layout``,
+    ``local_experts``, ``finish``) and the tensors' device.  Row pieces move
+    with torch.distributed's batched point-to-point operations (NCCL between
     GPUs), the per-expert counts with one all_to_all_single."""
 
     def __init__(self, E: int, k: int, P: int, group=None):
@@ -119,13 +84,20 @@ class EpLayerBase:
     # -- compute steps (subclasses) ------------------------------------------
     def front(self, x, topk_idx=None, topk_w=None):
         """Route x (or take the given routing) and permute it into the padded
-        expert-major layout over all E experts.  Returns (counts [E] device
-        int32, x_perm [R, d], row_gate [R], tables for finish)."""
+        expert-major layout over all E experts.  Returns (counts [E] int32,
+        padded offsets [E + 1] int32, x_perm [R, d], row_gate [R], tables for
+        finish)."""
         raise NotImplementedError
 
-    def local_experts(self, xe, ge, plan: DispatchPlan):
-        """y rows [plan.rows, d] of the local experts for the expert-major rows
-        xe with routing weights ge (the GEMM2 epilogue multiplies by them)."""
+    def layout(self, recv):
+        """The expert-major layout of the arriving rows from recv [W * El]
+        (int32, rows of sender s for local expert e at s * El + e): a dict
+        with at least ``piece_row`` [W, El]."""
+        raise NotImplementedError
+
+    def local_experts(self, xe, ge, lay, valid_rows: int):
+        """y rows of the local experts for the expert-major rows xe with routing
+        weights ge (the GEMM2 epilogue multiplies by them)."""
         raise NotImplementedError
 
     def finish(self, x, y, tables):
@@ -142,36 +114,38 @@ class EpLayerBase:
         return (torch.empty((rows, d), dtype=like_x.dtype, device=like_x.device),
                 torch.empty((rows,), dtype=like_g.dtype, device=like_g.device))
 
-    def gather_rows(self, src, idx: np.ndarray, dst, sgate=None, dgate=None):
-        """dst[i] = src[idx[i]] (and the gates) for the i < len(idx) with
-        idx[i] >= 0; the other rows are left as they are."""
+    def host_tables(self, counts, own_po, recv, piece_row):
+        """Host copies of the four tables (numpy)."""
+        return tuple(np.asarray(t.cpu() if hasattr(t, "cpu") else t)
+                     for t in (counts, own_po, recv, piece_row))
+
+    def move_local(self, src, dst, pieces, sgate=None, dgate=None, combine=False, lay=None):
+        """The pieces this rank keeps: pieces = [(src row, dst row, rows)]."""
         import torch
 
-        keep = np.flatnonzero(idx >= 0)
-        di = torch.as_tensor(keep, device=src.device)
-        si = torch.as_tensor(idx[keep].astype(np.int64), device=src.device)
+        if not pieces:
+            return
+        rs, rd, n = (np.array(v, np.int64) for v in zip(*pieces))
+        step = np.arange(int(n.sum())) - np.repeat(np.cumsum(n) - n, n)
+        si = torch.as_tensor(np.repeat(rs, n) + step, device=src.device)
+        di = torch.as_tensor(np.repeat(rd, n) + step, device=src.device)
         dst.index_copy_(0, di, src.index_select(0, si))
         if sgate is not None:
             dgate.index_copy_(0, di, sgate.index_select(0, si))
 
     # -- the exchange -------------------------------------------------------
-    def _exchange(self, src, dst, sends, recvs, sgate=None, dgate=None):
+    def _exchange(self, src, dst, sends, recvs, sgate=None, dgate=None, combine=False, lay=None):
         """Moves row pieces of src to the peers (sends: (peer, row, rows)) and
         lands the peers' pieces in dst (recvs: (peer, row, rows)), the gates
         alongside.  Per pair of ranks the pieces pair up in list order.  The
-        pieces between this rank and itself are one gather; the others go
-        through batched point-to-point operations."""
+        pieces between this rank and itself are one local move; the others
+        go through batched point-to-point operations."""
         own_s = [(r, n) for p, r, n in sends if p == self.rank]
         own_r = [(r, n) for p, r, n in recvs if p == self.rank]
-        if own_s:
-            rs, ns = np.array(own_s, np.int64).T
-            rd, nd = np.array(own_r, np.int64).T
-            if not np.array_equal(ns, nd):
-                raise RuntimeError("mismatched local pieces")
-            idx = np.full(int((rd + nd).max()), -1, np.int32)
-            step = np.arange(int(ns.sum())) - np.repeat(np.cumsum(ns) - ns, ns)
-            idx[np.repeat(rd, ns) + step] = np.repeat(rs, ns) + step
-            self.gather_rows(src, idx, dst, sgate, dgate)
+        if [n for _, n in own_s] != [n for _, n in own_r]:
+            raise RuntimeError("mismatched local pieces")
+        self.move_local(src, dst, [(a, b, n) for (a, n), (b, _) in zip(own_s, own_r)], sgate,
+                        dgate, combine, lay)
         ops = []
         P2POp, dist = self.dist.P2POp, self.dist
         for p, r, n in sends:
@@ -188,33 +162,38 @@ class EpLayerBase:
             for req in dist.batch_isend_irecv(ops):
                 req.wait()
 
-    def exchange_counts(self, counts_host: np.ndarray, device) -> np.ndarray:
-        """[W, El]: what every rank routes to this rank's experts."""
+    def exchange_counts(self, counts):
+        """[W * El] on counts' device: what every rank routes to this rank's
+        experts (sender s's counts at s * El + e)."""
         import torch
 
-        send = torch.as_tensor(counts_host.astype(np.int64), device=device)
-        recv = torch.empty_like(send)
-        self.dist.all_to_all_single(recv, send, group=self.group)
-        return recv.cpu().numpy().reshape(self.world, self.El)
+        recv = torch.empty_like(counts)
+        self.dist.all_to_all_single(recv, counts.contiguous(), group=self.group)
+        return recv
 
     def forward(self, x, topk_idx=None, topk_w=None):
         import torch
 
-        counts, x_perm, row_gate, tables = self.front(x, topk_idx, topk_w)
-        counts_host = counts.cpu().numpy().astype(np.int64)  # the split sizes
-        recv_counts = self.exchange_counts(counts_host, x.device)
-        plan = plan_dispatch(counts_host, recv_counts, self.P)
+        counts, own_po, x_perm, row_gate, tables = self.front(x, topk_idx, topk_w)
+        recv = self.exchange_counts(counts)
+        lay = self.layout(recv)
+        h_counts, h_po, h_recv, h_piece = self.host_tables(counts, own_po, recv,
+                                                           lay["piece_row"])
+        h_recv = h_recv.reshape(self.world, self.El)
+        sends, recvs = plan_pieces(self.rank, self.El, h_counts, h_po, h_recv,
+                                   h_piece.reshape(self.world, self.El))
         d = x_perm.shape[1]
+        rows = int(h_recv.sum())
         # dispatch: token rows and their routing weights, piece by piece,
         # straight into the expert-major layout
-        xe, ge = self.expert_major_buffers(plan.rows, d, x_perm, row_gate)
-        self._exchange(x_perm, xe, plan.send_pieces, plan.recv_pieces, row_gate, ge)
-        ye = self.local_experts(xe, ge, plan)
+        xe, ge = self.expert_major_buffers(max(rows, 1), d, x_perm, row_gate)
+        self._exchange(x_perm, xe, sends, recvs, row_gate, ge, lay=lay)
+        ye = self.local_experts(xe, ge, lay, rows)
         # combine exchange: the y pieces back into their senders' layout
         ys = self.combine_buffer(tables)
         if ys is None:
-            ys = torch.empty((int(plan.send_rows.sum()), d), dtype=ye.dtype, device=x.device)
-        self._exchange(ye, ys, plan.recv_pieces, plan.send_pieces)
+            ys = torch.empty((int(h_po[-1]), d), dtype=ye.dtype, device=x.device)
+        self._exchange(ye, ys, recvs, sends, combine=True, lay=lay)
         return self.finish(x, ys, tables)
 
     def combine_buffer(self, tables):
@@ -228,8 +207,10 @@ class GpuEp(EpLayerBase):
     CUDA), the router and the shared expert replicated (the pages'
     orientations, as MoeLayer).  ``cfg`` is the global config (E = all
     experts, T = this rank's tokens per call).  Buffers are sized once: the
-    expert-major layout holds at most W * T * k rows plus W * El * P of
-    padding."""
+    expert-major layout holds at most W * T * k rows plus El * P of padding.
+    At world size 1 the expert-major layout is the rank's own layout (one
+    sender, its rows already back to back per expert), so the layer's own
+    buffers serve both sides and no row moves."""
 
     def __init__(self, cfg, W1_local, W3_local, W2_local, Wg=None, bias=None, Ws1=None, Ws3=None,
                  Ws2=None, group=None, stream=None):
@@ -248,6 +229,7 @@ class GpuEp(EpLayerBase):
         self.cfg, self.dev = cfg, dev
         d, de, ds = cfg.d, cfg.d_e, cfg.d_shared
         bf = dict(dtype=torch.bfloat16, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
         self.W13 = torch.empty((El, 2 * de, d), **bf)
         self.W2_t = torch.empty((El, d, de), **bf)
         moe_pack_experts(W1_local, W3_local, W2_local, self.W13, self.W2_t, stream)
@@ -270,22 +252,25 @@ class GpuEp(EpLayerBase):
         n_split = moe_route_splitk_scratch_size(cfg) // 4
         self.partial = self._buf("router_partial", torch.float32, (n_split,)) if n_split else None
         # the expert-major layout of the received rows: capacity R_cap rows
-        self.R_cap = self.world * cfg.T * cfg.k + self.world * El * cfg.pad_multiple
+        self.R_cap = self.world * cfg.T * cfg.k + El * cfg.pad_multiple
         self.cfg_local = config_of(T=math.ceil(self.R_cap / cfg.k), d=d, d_e=de, E=El, k=cfg.k,
                                    pad_multiple=cfg.pad_multiple)
         R_loc = self.cfg_local.T * cfg.k + El * (cfg.pad_multiple - 1)  # the GEMMs' row capacity
         NB_loc = self.cfg_local.T * cfg.k // cfg.pad_multiple + El
-        self.xe = torch.zeros((R_loc, d), **bf)
-        self.ge = torch.zeros((R_loc,), dtype=torch.float32, device=dev)
-        self.he = torch.empty((R_loc, de), **bf)
-        self.ye = torch.empty((R_loc, d), **bf)
-        self.meta = torch.zeros((NB_loc, 3), dtype=torch.int32, device=dev)
-        self.nb = torch.zeros((1,), dtype=torch.int32, device=dev)
-        self.po = torch.zeros((El + 1,), dtype=torch.int32, device=dev)
-        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
-        self._staging = {}
+        if self.world > 1:
+            self.xe = torch.zeros((R_loc, d), **bf)
+            self.ge = torch.zeros((R_loc,), dtype=torch.float32, device=dev)
+            self.he = torch.empty((R_loc, de), **bf)
+            self.ye = torch.empty((R_loc, d), **bf)
+        # the receiver's tables, built on the device from the exchanged counts
+        self.meta = torch.zeros((NB_loc, 3), **i32)
+        self.nb = torch.zeros((1,), **i32)
+        self.po = torch.zeros((El + 1,), **i32)
+        self.piece_row = torch.zeros((self.world, El), **i32)
+        self.status = torch.zeros((1,), **i32)
+        self._recv = None
         # the shared expert needs only x: it runs on a side stream while the
-        # routing, the exchange (and its host syncs) and the routed experts run
+        # routing, the exchange (and its host sync) and the routed experts run
         self.s_shared = torch.cuda.Stream(device=dev)
         self.ev_shared = torch.cuda.Event()
 
@@ -302,9 +287,7 @@ class GpuEp(EpLayerBase):
     def front(self, x, topk_idx=None, topk_w=None):
         import torch
 
-        from . import moe_build_offsets, moe_permute, moe_route, moe_route_splitk
-
-        from . import moe_shared_expert
+        from . import moe_build_offsets, moe_permute, moe_route_splitk, moe_shared_expert
 
         c = self.cfg
         T, k, E, d = c.T, c.k, c.E, c.d
@@ -320,10 +303,10 @@ class GpuEp(EpLayerBase):
         if topk_idx is None:
             topk_idx = self._buf("topk_idx", i32, (T, k))
             topk_w = self._buf("topk_w", f32, (T, k))
-            if self.partial is not None:
-                moe_route_splitk(c, x, self.Wg_t, self.bias, topk_idx, topk_w, self.partial)
-            else:
-                moe_route(c, x, self.Wg_t, self.bias, topk_idx, topk_w)
+            # the layer's own router form (fused, clustered split-K, or split-K
+            # with partial logits in the scratch), so that the routing weights
+            # carry the same bits as MoeLayer's
+            moe_route_splitk(c, x, self.Wg_t, self.bias, topk_idx, topk_w, self.partial)
         t = dict(counts=self._buf("counts", i32, (E,)), po=self._buf("padded_offsets", i32, (E + 1,)),
                  meta=self._buf("block_metadata", i32, (NB, 3)), nb=self._buf("num_blocks", i32, (1,)),
                  perm_row=self._buf("perm_row", i32, (A,)), row_src=self._buf("row_src", i32, (R,)),
@@ -333,64 +316,77 @@ class GpuEp(EpLayerBase):
                           self.ws[self.L["status"]:self.L["topk_idx"]])
         x_perm = self._buf("x_perm", torch.bfloat16, (R, d))
         moe_permute(c, x, t["perm_row"], x_perm)
-        return t["counts"], x_perm, t["row_gate"], t
+        return t["counts"], t["po"], x_perm, t["row_gate"], t
+
+    def layout(self, recv):
+        from . import moe_build_blocks_from_counts
+
+        self._recv = recv.view(self.world, self.El)
+        moe_build_blocks_from_counts(self._recv, self.P, self.po, self.meta, self.nb,
+                                     self.piece_row, self.status)
+        return dict(po=self.po, meta=self.meta, nb=self.nb, piece_row=self.piece_row)
+
+    def host_tables(self, counts, own_po, recv, piece_row):
+        """One device-to-host copy of the four tables (the host sync of the
+        layer: NCCL takes its sizes and offsets from the host)."""
+        import torch
+
+        parts = (counts, own_po, recv, piece_row)
+        packed = torch.cat([t.reshape(-1) for t in parts]).cpu().numpy()
+        out, o = [], 0
+        for t in parts:
+            out.append(packed[o:o + t.numel()])
+            o += t.numel()
+        return tuple(out)
 
     def expert_major_buffers(self, rows, d, like_x, like_g):
+        if self.world == 1:
+            return like_x, like_g  # the rank's own layout is the expert-major one
         if rows > self.xe.shape[0]:
             raise RuntimeError(f"{rows} received rows exceed the capacity {self.xe.shape[0]}")
         return self.xe, self.ge
 
-    def _stage(self, slot: str, a: np.ndarray, out=None):
-        """The int32 host array ``a`` on the device (in ``out``, or in the
-        slot's own device buffer), through the slot's pinned staging buffer;
-        the buffer is reused once its previous copy has finished."""
-        import torch
+    def move_local(self, src, dst, pieces, sgate=None, dgate=None, combine=False, lay=None):
+        """The pieces this rank keeps, with device descriptors: its own
+        segment starts (padded offsets of its experts), the landing rows, the
+        counts from the exchange."""
+        from . import moe_copy_pieces
 
-        st = self._staging.get(slot)
-        if st is None or st[0].numel() < a.size:
-            n = max(2 * a.size, 1024)
-            st = (torch.empty(n, dtype=torch.int32).pin_memory(),
-                  torch.empty(n, dtype=torch.int32, device=self.dev), torch.cuda.Event())
-            self._staging[slot] = st
-        else:
-            st[2].synchronize()
-        host, dev, ev = st
-        host[:a.size].numpy()[:] = a.reshape(-1)
-        dst = dev[:a.size] if out is None else out.view(-1)[:a.size]
-        dst.copy_(host[:a.size], non_blocking=True)
-        ev.record()
-        return dst
-
-    def gather_rows(self, src, idx, dst, sgate=None, dgate=None):
-        from . import moe_gather_rows
-
-        if idx.size == 0:
+        if not pieces:
             return
-        slot = "idx_x" if sgate is not None else "idx_y"
-        moe_gather_rows(src, self._stage(slot, idx), dst, sgate, dgate)
+        if src.data_ptr() == dst.data_ptr():
+            if any(a != b for a, b, _ in pieces):
+                raise RuntimeError("aliased exchange buffers with moving pieces")
+            return
+        r, El = self.rank, self.El
+        own = self._buf("padded_offsets", __import__("torch").int32, (self.E + 1,))[r * El:(r + 1) * El]
+        land = self.piece_row[r]
+        rows = self._recv[r]
+        src_row, dst_row = (land, own) if combine else (own, land)
+        moe_copy_pieces(src, dst, src_row, dst_row, rows, max(n for _, _, n in pieces), sgate, dgate)
 
-    def local_experts(self, xe, ge, plan):
+    def local_experts(self, xe, ge, lay, valid_rows):
         import torch
 
         from . import moe_grouped_gemm_swiglu, moe_grouped_gemm_swiglu_skinny
 
-        nb = plan.block_metadata.shape[0]
-        if nb == 0:
-            return self.ye[:0]
-        if nb > self.meta.shape[0]:
-            raise RuntimeError("block table exceeds its capacity")
-        self._stage("meta", plan.block_metadata, self.meta)
-        self.nb.fill_(nb)
-        self._stage("po", plan.padded_offsets.astype(np.int32), self.po)
-        c = self.cfg_local
-        valid = int(plan.block_metadata[:, 2].sum())
-        if valid <= 32 * self.El:  # few rows per expert: the small-M kernel, as the layer
-            moe_grouped_gemm_swiglu_skinny(c, xe, self.W13, self.W2_t, self.meta, self.nb, ge,
-                                           self.he, self.ye, self.status)
+        if self.world == 1:
+            # the layer's own config and buffers: x_perm, h, y of the workspace
+            c = self.cfg
+            R = c.T * c.k + c.E * (c.pad_multiple - 1)
+            he = self._buf("h", torch.bfloat16, (R, c.d_e))
+            ye = self._buf("y", torch.bfloat16, (R, c.d))
         else:
-            moe_grouped_gemm_swiglu(c, xe, self.W13, self.W2_t, self.meta, self.nb, self.po, ge,
-                                    self.he, self.ye, self.status)
-        return self.ye[:plan.rows]
+            c, he, ye = self.cfg_local, self.he, self.ye
+        if valid_rows == 0:
+            return ye
+        if valid_rows <= 32 * self.El:  # few rows per expert: the small-M kernel, as the layer
+            moe_grouped_gemm_swiglu_skinny(c, xe, self.W13, self.W2_t, lay["meta"], lay["nb"], ge,
+                                           he, ye, self.status)
+        else:
+            moe_grouped_gemm_swiglu(c, xe, self.W13, self.W2_t, lay["meta"], lay["nb"], lay["po"],
+                                    ge, he, ye, self.status)
+        return ye
 
     def combine_buffer(self, t):
         import torch

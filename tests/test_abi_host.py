@@ -117,7 +117,7 @@ def test_fp8_entry_points_check_arguments_before_launch(lib):
     need = moe.moe_workspace_size_fp8(cfg)
     assert need > moe.moe_workspace_size(cfg)  # the e4m3 layer needs its extra regions
     L8 = moe.moe_workspace_layout_fp8(cfg)
-    assert L8["total"] == need and L8["row_scale"] > L8["h8"] >= L8["xs8"] > L8["router_partial"]
+    assert L8["total"] == need and L8["row_scale"] > L8["h8"] >= L8["xs8"] >= L8["router_partial"]
     w = moe.MoeWeightsFp8(Wg_t=0x1000, bias=None, W13q=0x1000, s13=0x1000, W2q=0x1000, s2=0x1000)
     assert lib.moe_layer_fwd_fp8(ctypes.byref(cfg), ctypes.byref(w), fake, fake, fake, need - 1,
                                  None) == 3
@@ -234,3 +234,20 @@ def test_pack_weights_checks_arguments_before_launch(lib):
     assert lib.moe_pack_weights(ctypes.byref(_cfg()), fake, None, fake, None) == 1
     assert lib.moe_pack_weights(ctypes.byref(_cfg()), fake, fake, None, None) == 1
     assert lib.moe_pack_weights(None, fake, fake, fake, None) == 1
+
+
+def test_exchange_table_entry_points_check_arguments_before_launch(lib):
+    """moe_build_blocks_from_counts and moe_copy_pieces reject bad sizes and
+    null operands before any launch."""
+    fake = ctypes.c_void_p(0x1000)
+    f = lib.moe_build_blocks_from_counts
+    assert f(fake, 0, 8, 128, fake, fake, fake, 10, None, None, None) == 1   # no sender
+    assert f(fake, 2, 300, 128, fake, fake, fake, 10, None, None, None) == 2  # E > 256
+    assert f(fake, 2, 8, 96, fake, fake, fake, 10, None, None, None) == 2    # P
+    assert f(None, 2, 8, 128, fake, fake, fake, 10, None, None, None) == 1
+    assert f(fake, 2, 8, 128, fake, None, fake, 10, None, None, None) == 1
+    c = lib.moe_copy_pieces
+    assert c(fake, fake, 60, fake, fake, fake, 3, 8, None, None, None) == 2  # d % 8
+    assert c(fake, fake, 64, fake, fake, fake, 3, 8, fake, None, None) == 1  # gates both or neither
+    assert c(fake, fake, 64, None, fake, fake, 3, 8, None, None, None) == 1
+    assert c(None, None, 64, None, None, None, 0, 0, None, None, None) == 0  # nothing to move

@@ -22,11 +22,16 @@ def bench():
 
 
 @pytest.mark.parametrize("name, skinny, fp8, expect", [
-    ("default", False, False, 11),     # split-K router 2, offsets 3, permute, 2 + 2 GEMMs, combine
-    ("decode", True, False, 7),        # split-K router 2, small offsets 1, permute, 2 GEMMs, combine
+    ("default", False, False, 10),     # clustered split-K router 1, offsets 3, permute, 2 + 2 GEMMs,
+                                       # combine
+    ("decode", True, False, 7),        # split-K router 2 (partials + reduce: E = 256), small offsets
+                                       # 1, permute, 2 GEMMs, combine
     ("decode", True, True, 8),         # + the e4m3 pairs of h between the GEMMs
     ("prerouted", False, False, 7),    # no router: offsets 3, permute, 2 GEMMs, combine
-    ("default", False, True, 15),      # + widening routed and shared W13, W2
+    ("default", False, True, 14),      # + widening routed and shared W13, W2
+    ("imbalance_x4_p128", False, False, 8),  # fused router 1, offsets 3, permute, 2 GEMMs, combine
+    ("tiny", False, False, 7),         # split-K router 2 (8 slices), small offsets 1, permute, 2
+                                       # GEMMs, combine
 ])
 def test_forward_launch_counts(bench, name, skinny, fp8, expect):
     assert bench.forward_launches(synth.WORKLOADS[name], skinny, fp8) == expect

@@ -1,13 +1,17 @@
 """Expert parallelism (routing_permute_grouped_gb300/ep.py) on CPU process
 groups.
 
-The exchange logic (piece sizes, the receiver's expert-major layout and block
-table, the two piece-by-piece exchanges) runs with world size 2 over gloo, with the
-oracle as the compute backend on each rank: rank r holds experts
+The exchange logic (the counts all-to-all, the receiver's expert-major layout
+built from the counts, the piece lists read off it, the two piece-by-piece
+exchanges) runs with world size 2 over gloo, with the oracle as the compute
+backend on each rank: rank r holds experts
 [r*E/2, (r+1)*E/2) and its own half of the tokens.  Every rank's output must
 equal, bit for bit, the single-process oracle's output for the same tokens:
 dispatch and combine only move rows, and the combine keeps its order.  The
-plan itself is also checked on a hand-worked example.
+receiver's layout (the oracle's definition, which the device entry point
+moe_build_blocks_from_counts is compared with on the GPU) and the piece lists
+are checked on hand-worked examples and against the single-GPU offsets of
+the same rows.
 """
 import os
 import socket
@@ -23,41 +27,81 @@ from routing_permute_grouped_gb300.synth import MoeShape
 from tests.helpers import enforce_margin, oracle_inputs
 
 
-def test_plan_dispatch_worked_example():
-    # this rank (of W = 2, El = 2, P = 4) routes 5, 0, 3, 9 rows to experts
-    # 0..3; it receives 2 and 7 rows (experts 0, 1 of its own) from rank 0,
-    # 4 and 0 from rank 1
-    plan = ep.plan_dispatch(np.array([5, 0, 3, 9]), np.array([[2, 7], [4, 0]]), 4)
-    assert plan.send_rows.tolist() == [8, 16]
-    assert plan.recv_rows.tolist() == [12, 4]
-    assert plan.padded_offsets.tolist() == [0, 8, 16]
-    assert plan.rows == 16
-    assert plan.block_metadata.tolist() == [[0, 0, 2], [0, 4, 4], [1, 8, 4], [1, 12, 3]]
-    # this rank's padded segments (8, 0, 4, 12 rows) go out one per expert:
-    # experts 0, 1 to rank 0, experts 2, 3 to rank 1
-    assert plan.send_pieces == [(0, 0, 8), (1, 8, 4), (1, 12, 12)]
-    # arriving pieces land expert-major, senders in rank order within an expert
-    assert plan.recv_pieces == [(0, 0, 4), (1, 4, 4), (0, 8, 8)]
+def test_receiver_layout_worked_example():
+    # this rank (0 of W = 2, El = 2, P = 4) keeps experts 0, 1 and receives
+    # 5 rows for expert 0 from itself; 4 for expert 0 and 7 for expert 1 from
+    # rank 1.  Expert 0's segment: 5 + 4 = 9 rows, padded to 12; expert 1: 7,
+    # padded to 8.  Sender 1's rows of expert 0 land right after sender 0's.
+    lay = oracle.blocks_from_counts(np.array([[5, 0], [4, 7]]), 4)
+    assert lay["padded_offsets"].tolist() == [0, 12, 20]
+    assert lay["piece_row"].tolist() == [[0, 12], [5, 12]]
+    assert lay["num_blocks"] == 5
+    assert lay["block_metadata"].tolist() == [[0, 0, 4], [0, 4, 4], [0, 8, 1], [1, 12, 4],
+                                              [1, 16, 3]]
 
 
-def test_plan_dispatch_conserves_rows():
+def test_receiver_layout_is_the_single_gpu_layout_of_the_arriving_rows():
+    # the expert-major layout built from counts equals the offsets stage's
+    # layout of the arriving assignments concatenated in sender order: the
+    # same segments and blocks, and sender s's first row of expert e sits
+    # where the stable order puts it
+    rng = np.random.default_rng(5)
+    for W, El, P in ((1, 8, 128), (3, 5, 64), (4, 2, 128)):
+        per_src = [rng.choice(El, size=int(rng.integers(0, 400)),
+                              p=rng.dirichlet(np.full(El, 0.4))).astype(np.int32)
+                   for _ in range(W)]
+        counts = np.stack([np.bincount(a, minlength=El) for a in per_src]).astype(np.int32)
+        lay = oracle.blocks_from_counts(counts, P)
+        cat = np.concatenate(per_src + [np.zeros(0, np.int32)])
+        if cat.size == 0:
+            continue
+        off = oracle.build_offsets(cat, None, El, P)
+        assert np.array_equal(lay["padded_offsets"], off["padded_offsets"])
+        assert lay["num_blocks"] == off["num_blocks"]
+        assert np.array_equal(lay["block_metadata"], off["block_metadata"])
+        start = np.cumsum([0] + [a.size for a in per_src])
+        for s_ in range(W):
+            for e in range(El):
+                hit = np.flatnonzero(per_src[s_] == e)
+                if hit.size:
+                    assert lay["piece_row"][s_, e] == off["perm_row"][start[s_] + hit[0]]
+        if W == 1:
+            assert np.array_equal(lay["piece_row"][0], off["padded_offsets"][:-1])
+
+
+def test_plan_pieces_worked_example():
+    # rank 0 of W = 2, El = 2: it routes 5, 0, 3, 9 rows to experts 0..3
+    # (its own padded segments start at 0, 8, 8, 12); it receives [5, 0] from
+    # itself and [4, 7] from rank 1, landing as in the worked layout above
+    sends, recvs = ep.plan_pieces(0, 2, [5, 0, 3, 9], [0, 8, 8, 12, 24], [[5, 0], [4, 7]],
+                                  [[0, 12], [5, 12]])
+    # expert 0 to itself; experts 2, 3 to rank 1, each from its segment start
+    assert sends == [(0, 0, 5), (1, 8, 3), (1, 12, 9)]
+    # expert-major: expert 0 from ranks 0 and 1, expert 1 from rank 1
+    assert recvs == [(0, 0, 5), (1, 5, 4), (1, 12, 7)]
+
+
+def test_plan_pieces_conserves_rows():
     rng = np.random.default_rng(3)
     W, El, P = 4, 3, 64
     counts = rng.integers(0, 300, W * El)
     recv = rng.integers(0, 300, (W, El))
-    plan = ep.plan_dispatch(counts, recv, P)
-    assert plan.send_rows.sum() == ep.padded(counts, P).sum()
-    assert plan.rows == plan.recv_rows.sum() == ep.padded(recv, P).sum()
-    assert plan.block_metadata[:, 2].sum() == recv.sum()
-    # the arriving pieces tile the expert-major layout exactly once, and the
-    # sent pieces tile this rank's own padded layout
-    for pieces, total in ((plan.recv_pieces, plan.rows), (plan.send_pieces, plan.send_rows.sum())):
-        pos = 0
-        for _, start, n in sorted(pieces, key=lambda p: p[1]):
-            assert start == pos
-            pos += n
-        assert pos == total
-    assert (plan.padded_offsets % P == 0).all()
+    own_po = np.concatenate([[0], np.cumsum(-(-counts // P) * P)])
+    lay = oracle.blocks_from_counts(recv.astype(np.int32), P)
+    sends, recvs = ep.plan_pieces(1, El, counts, own_po, recv, lay["piece_row"])
+    assert sum(n for _, _, n in sends) == counts.sum()
+    assert sum(n for _, _, n in recvs) == recv.sum()
+    # pieces to each peer follow that peer's experts; arrivals fill each
+    # segment's valid prefix exactly once
+    for peer in range(W):
+        assert [n for p, _, n in sends if p == peer] == [c for c in counts[peer * El:(peer + 1) * El]
+                                                        if c > 0]
+    covered = np.zeros(int(lay["padded_offsets"][-1]), np.int32)
+    for _, r, n in recvs:
+        covered[r:r + n] += 1
+    for e in range(El):
+        a, c = lay["padded_offsets"][e], recv[:, e].sum()
+        assert (covered[a:a + c] == 1).all() and (covered[a + c:lay["padded_offsets"][e + 1]] == 0).all()
 
 
 class OracleEp(ep.EpLayerBase):
@@ -79,13 +123,26 @@ class OracleEp(ep.EpLayerBase):
         off = oracle.build_offsets(topk_idx, topk_w, s.E, s.pad)
         x_perm = oracle.permute(xb, off["row_src"], s.k)
         # bf16 bits carried as int32 (gloo's all-to-all has no 16-bit type)
-        return (torch.as_tensor(off["counts"]), torch.from_numpy(x_perm.astype(np.int32)),
+        return (torch.as_tensor(off["counts"]), torch.as_tensor(off["padded_offsets"]),
+                torch.from_numpy(x_perm.astype(np.int32)),
                 torch.from_numpy(off["row_gate"].astype(np.float64)), off)
 
-    def local_experts(self, xe, ge, plan):
+    def layout(self, recv):
+        lay = oracle.blocks_from_counts(recv.numpy().reshape(self.world, self.El), self.P)
+        return dict(lay, piece_row=torch.from_numpy(lay["piece_row"]))
+
+    def local_experts(self, xe, ge, lay, valid_rows):
         _, y = oracle.grouped_experts(xe.numpy().astype(np.uint16), self.W1, self.W3, self.W2,
-                                      plan.block_metadata, ge.numpy())
+                                      lay["block_metadata"], ge.numpy())
         return torch.from_numpy(y)
+
+    def expert_major_buffers(self, rows, d, like_x, like_g):
+        # the oracle reads only the valid rows of each block: any buffer that
+        # holds the padded segments will do
+        import torch as _t
+
+        n = rows + self.El * self.P
+        return (_t.zeros((n, d), dtype=like_x.dtype), _t.zeros((n,), dtype=like_g.dtype))
 
     def finish(self, x, y, off):
         s = self.shape

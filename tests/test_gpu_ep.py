@@ -1,10 +1,13 @@
 """The expert-parallel layer forward (ep.GpuEp) on the CUDA library, through
 NCCL, with world size 1: the one GPU of a box holds every expert, so the
-all-to-alls move rows within the rank, and the dispatch plan, the receiver's
-block table and the stage calls run exactly as they do across ranks.  The
-output must be bit-identical to MoeLayer's where both run the CTA-pair
-kernel, and within the parity bound of the oracle everywhere.  (The exchange
-between ranks is tested on CPU process groups in tests/test_ep_gloo.py.)
+counts all-to-all stays within the rank, the receiver's layout is built on
+the device from the exchanged counts, and the rank's own layout serves as the
+expert-major one.  The output must be bit-identical to MoeLayer's where both
+run the CTA-pair kernel, and within the parity bound of the oracle
+everywhere.  The device entry points of the exchange with several senders
+(the receiver's layout from counts, the piece copies) are compared with the
+oracle's layout and with plain indexing here; the exchange between ranks is
+tested on CPU process groups in tests/test_ep_gloo.py.
 """
 import socket
 
@@ -102,6 +105,67 @@ def test_gather_rows():
     assert torch.equal(dst.cpu(), expect)
     eg = torch.full((517,), 7.0)
     eg[ok] = sg.cpu()[ii[ok]]
+    assert torch.equal(dg.cpu(), eg)
+
+
+@pytest.mark.parametrize("W, El, P", [(1, 8, 128), (2, 4, 64), (4, 32, 128), (8, 256, 64),
+                                      (3, 1, 128)])
+def test_blocks_from_counts_match_the_oracle(W, El, P):
+    """moe_build_blocks_from_counts: padded offsets, block table and landing
+    rows bit-exact against the oracle's layout of the same counts (empty
+    experts and senders included), twice on stale outputs."""
+    rng = np.random.default_rng(W * 1000 + El)
+    counts = rng.integers(0, 3 * P, (W, El)).astype(np.int32)
+    counts[rng.random((W, El)) < 0.2] = 0
+    ref = oracle.blocks_from_counts(counts, P)
+    cap = int(counts.sum()) // P + El
+    dev = "cuda"
+    po = torch.full((El + 1,), -9, dtype=torch.int32, device=dev)
+    meta = torch.full((cap, 3), -9, dtype=torch.int32, device=dev)
+    nb = torch.full((1,), -9, dtype=torch.int32, device=dev)
+    pr = torch.full((W, El), -9, dtype=torch.int32, device=dev)
+    st = torch.zeros((1,), dtype=torch.int32, device=dev)
+    for _ in range(2):
+        moe.moe_build_blocks_from_counts(torch.from_numpy(counts).to(dev), P, po, meta, nb, pr, st)
+        torch.cuda.synchronize()
+        n = int(nb.item())
+        assert n == ref["num_blocks"] and int(st.item()) == 0
+        assert np.array_equal(po.cpu().numpy(), ref["padded_offsets"])
+        assert np.array_equal(meta.cpu().numpy()[:n], ref["block_metadata"])
+        assert np.array_equal(pr.cpu().numpy(), ref["piece_row"])
+
+
+def test_blocks_from_counts_flags_overflow():
+    """A table that does not fit its capacity is cut at nb_cap and flagged."""
+    counts = torch.tensor([[300, 5]], dtype=torch.int32, device="cuda")
+    meta = torch.zeros((2, 3), dtype=torch.int32, device="cuda")
+    po = torch.zeros((3,), dtype=torch.int32, device="cuda")
+    nb = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    moe.moe_build_blocks_from_counts(counts, 128, po, meta, nb, None, st)
+    torch.cuda.synchronize()
+    assert int(nb.item()) == 2 and int(st.item()) & 0x4
+    assert po.cpu().tolist() == [0, 384, 512]
+
+
+def test_copy_pieces():
+    """moe_copy_pieces: each piece's rows (and gates) land at its destination
+    bit for bit; rows outside the pieces keep their contents."""
+    g = torch.Generator().manual_seed(11)
+    src = torch.randn((500, 264), generator=g).to(torch.bfloat16).cuda()
+    sg = torch.rand(500, generator=g).cuda()
+    pieces = [(0, 40, 17), (100, 0, 33), (300, 90, 0), (37, 200, 64), (450, 300, 50)]
+    s_row, d_row, rows = (torch.tensor(v, dtype=torch.int32, device="cuda") for v in zip(*pieces))
+    dst = torch.full((400, 264), 3.0, dtype=torch.bfloat16, device="cuda")
+    dg = torch.full((400,), 3.0, device="cuda")
+    moe.moe_copy_pieces(src, dst, s_row, d_row, rows, 64, sg, dg)
+    torch.cuda.synchronize()
+    expect = torch.full((400, 264), 3.0, dtype=torch.bfloat16)
+    eg = torch.full((400,), 3.0)
+    for a, b, n in pieces:
+        expect[b:b + n] = src.cpu()[a:a + n]
+        eg[b:b + n] = sg.cpu()[a:a + n]
+    assert torch.equal(dst.cpu(), expect)
     assert torch.equal(dg.cpu(), eg)
 
 

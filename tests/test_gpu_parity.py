@@ -210,15 +210,62 @@ def test_route_stage(name):
     moe.moe_route(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(w.cpu().double().numpy(), ref["topk_w"], rtol=0, atol=2e-5)
-    # the split-K router (partial logits + reduce/top-k kernel) decides the same
+    # the split-K router (slices over a cluster, or partial logits + a
+    # reduce/top-k kernel) decides the same
     nbytes = moe.moe_route_splitk_scratch_size(cfg)
-    assert nbytes > 0  # these batches are small enough to split
-    partial = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    partial = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device="cuda")
     idx.fill_(-7)
     w.zero_()
     moe.moe_route_splitk(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w, partial)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(w.cpu().double().numpy(), ref["topk_w"], rtol=0, atol=2e-5)
+
+
+# Router shapes for the split-K paths: K slices x 128-token tiles.  Up to 4
+# slices with E <= 64 run as one clustered kernel (tile width 16, 32 or 64);
+# more slices, or more experts, take partial logits and a reduce kernel.
+ROUTER_SHAPES = {
+    "partial_bn16_s8": MoeShape("partial_bn16_s8", T=2000, d=512, d_e=128, E=8, k=2,
+                                bias_std=0.5, seed=90),
+    "cluster_bn16_s3": MoeShape("cluster_bn16_s3", T=5000, d=384, d_e=128, E=8, k=2,
+                                bias_std=0.5, seed=95),
+    "cluster_bn16_s2": MoeShape("cluster_bn16_s2", T=8000, d=1024, d_e=128, E=16, k=4, seed=91),
+    "cluster_bn32_s4": MoeShape("cluster_bn32_s4", T=4000, d=1024, d_e=128, E=32, k=3,
+                                bias_std=0.3, seed=92),
+    "cluster_bn64_s2": MoeShape("cluster_bn64_s2", T=8100, d=768, d_e=128, E=64, k=6,
+                                n_groups=8, topk_groups=4, seed=93),
+    "partial_bn64_s8": MoeShape("partial_bn64_s8", T=1500, d=1024, d_e=128, E=48, k=5,
+                                n_groups=4, topk_groups=2, bias_std=0.2, seed=94),
+}
+
+
+@pytest.mark.parametrize("name", list(ROUTER_SHAPES))
+def test_route_splitk_paths(name):
+    """moe_route_splitk against the oracle's routing (indices bit-exact after
+    the margin filter, gates to 2e-5) on each form of the split-K router, and
+    the scratch size that each form asks for."""
+    shape = ROUTER_SHAPES[name]
+    inp = synth.make_inputs(shape)
+    enforce_margin(inp, shape)
+    bias = None if inp.get("bias") is None else inp["bias"].numpy()
+    lg = oracle.router_logits(bits(inp["x"]), bits(inp["Wg"]), bias)
+    ref_idx, ref_w, margin = oracle.route(lg, shape.k, shape.n_groups, shape.topk_groups)
+    assert margin.min() >= 1e-3
+    cfg = moe.config_of(shape)
+    nbytes = moe.moe_route_splitk_scratch_size(cfg)
+    assert (nbytes == 0) == name.startswith("cluster"), nbytes
+    Wg_t = torch.empty((shape.E, shape.d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_router(cuda(inp["Wg"]), Wg_t)
+    partial = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device="cuda")
+    idx = torch.full((shape.T, shape.k), -7, dtype=torch.int32, device="cuda")
+    w = torch.zeros((shape.T, shape.k), dtype=torch.float32, device="cuda")
+    for _ in range(2):  # twice: nothing may depend on what a previous call left
+        moe.moe_route_splitk(cfg, cuda(inp["x"]), Wg_t, cuda(inp.get("bias")), idx, w, partial)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), ref_idx)
+        np.testing.assert_allclose(w.cpu().double().numpy(), ref_w, rtol=0, atol=2e-5)
+        idx.fill_(-7)
+        w.zero_()
 
 
 def _offsets_case(idx, w, E, P):
