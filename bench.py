@@ -415,11 +415,11 @@ METRIC_TRAIN = "MoE layer fwd+bwd useful TFLOP/s (bf16, fp32 accumulate)"
 METRIC_FP8 = "MoE layer fwd useful TFLOP/s (e4m3 expert weights, fp32 accumulate)"
 
 
-def config_dict(shape, permute="separate", weights="bf16"):
+def config_dict(shape, permute="separate", weights="bf16", schedule="padded"):
     return {"workload": f"{shape.name}: T={shape.T} d={shape.d} d_e={shape.d_e} E={shape.E} "
                         f"k={shape.k} groups={shape.n_groups}/{shape.topk_groups} "
                         f"pad={shape.pad} shared={shape.d_shared}",
-            "permute": permute, "expert_weights": weights,
+            "permute": permute, "expert_weights": weights, "schedule": schedule,
             "l2": "inputs larger than L2 (expert weights and permuted rows exceed 129 MB)",
             "parallelism": "replicas"}
 
@@ -442,6 +442,11 @@ def run_ours(args, shape, rank, world, local):
     fp8 = args.weights == "fp8"
     if fp8 and args.permute != "separate":
         raise SystemExit("--weights fp8 runs with the separate permute")
+    unpadded = args.schedule == "unpadded"
+    if unpadded and (fp8 or args.permute != "separate" or
+                     shape.T * shape.k <= 32 * shape.E):
+        raise SystemExit("--schedule unpadded runs the CTA-pair GEMMs with bf16 weights and the "
+                         "separate permute")
     layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
                          bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
                          Ws2=inp.get("Ws2"), fp8=fp8)
@@ -500,8 +505,12 @@ def run_ours(args, shape, rank, world, local):
             moe.moe_route_splitk(cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w, router_partial)
         if ev is not None:
             ev[1].record()
-        moe.moe_build_offsets(cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src,
-                              row_gate, offs_ws)
+        if unpadded:  # group offsets in po, no block table
+            moe.moe_build_offsets_unpadded(cfg, topk_idx, topk_w, counts, po, perm_row, row_src,
+                                           row_gate, offs_ws)
+        else:
+            moe.moe_build_offsets(cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src,
+                                  row_gate, offs_ws)
         if ev is not None:
             ev[2].record()
         if fp8 and not wide:
@@ -519,6 +528,9 @@ def run_ours(args, shape, rank, world, local):
             moe.moe_grouped_gemm_swiglu_fp8(cfg, x_perm, x_scale, layer.W13q, layer.s13, layer.W2q,
                                             layer.s2, meta, nb, row_gate, h, h8, h_scale, y,
                                             status_word)
+        elif unpadded:
+            moe.moe_grouped_gemm_swiglu_unpadded(cfg, x_perm, layer.W13, layer.W2_t, po, row_gate,
+                                                 h, y, status_word)
         elif skinny:
             moe.moe_grouped_gemm_swiglu_skinny(cfg, x_perm, layer.W13, layer.W2_t, meta, nb,
                                                row_gate, h, y, status_word)
@@ -550,7 +562,7 @@ def run_ours(args, shape, rank, world, local):
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():
-        if args.permute == "separate":
+        if args.permute == "separate" and not unpadded:
             layer(x, out, **topk_kw_dev)  # moe_layer_fwd: the whole layer, one call
         else:
             step()
@@ -676,7 +688,7 @@ def run_ours(args, shape, rank, world, local):
         "dtype": ("e4m3 (weights, widened to bf16 for the MMAs; per-channel scales on the fp32 "
                   "accumulators)" if wide else
                   "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16"),
-        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights),
+        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights, args.schedule),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -695,7 +707,10 @@ def run_ours(args, shape, rank, world, local):
                    "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],
                    "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm_gbs"],
                    "expert_counts": counts_h,
-                   "padded_rows": ledger.padded_rows(counts_h, shape.pad)},
+                   "padded_rows": ledger.padded_rows(counts_h, shape.pad),
+                   # 256-row windows the CTA pairs execute under each schedule
+                   "visits": {"padded": ledger.padded_tiles(counts_h, shape.pad, 256),
+                              "unpadded": ledger.unpadded_tiles(counts_h, 256)}},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
@@ -1068,6 +1083,10 @@ def main():
     ap.add_argument("--parallel", choices=["replicas", "ep"], default="replicas",
                     help="replicas: every rank runs the whole layer on its tokens; ep: the "
                          "routed experts are split over the ranks (NCCL all-to-alls)")
+    ap.add_argument("--schedule", choices=["padded", "unpadded"], default="padded",
+                    help="padded: segments padded to the block multiple (the layer); unpadded: "
+                         "no padding, windows cut by an expert boundary visited once per "
+                         "expert (stage calls)")
     ap.add_argument("--keep-gate-up", action="store_true",
                     help="train: the forward saves the gate/up values, the backward skips "
                          "recomputing them")

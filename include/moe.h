@@ -494,6 +494,35 @@ moe_status_t moe_layer_fwd_prerouted(const moe_config_t *cfg, const moe_weights_
 moe_status_t moe_gather_rows(const void *src, const int32_t *idx, void *dst, int64_t n,
                              int32_t d, const float *src_gate, float *dst_gate, void *stream);
 
+/* The unpadded schedule ("Dropless and grouped GEMM", sec. 11: instead of
+ * padding each segment to a block multiple, a row tile that an expert
+ * boundary cuts is executed once for each expert whose rows it holds; the
+ * waste becomes repeated tiles instead of zero rows, at most E - 1 of them).
+ *
+ * a2 without padding: counts, and group_offsets [E + 1] = the exclusive
+ * prefix sum of the counts; the assignments of expert e take rows
+ * [group_offsets[e], group_offsets[e + 1]) in ascending assignment order.
+ * perm_row [A], row_src [A] (the unpadded layout has A rows; -1 for rows
+ * left over by out-of-range expert ids), row_gate [A] as moe_build_offsets
+ * writes them; no block table.  ws as for moe_build_offsets. */
+moe_status_t moe_build_offsets_unpadded(const moe_config_t *cfg, const int32_t *topk_idx,
+                                        const float *topk_w, int32_t *counts,
+                                        int32_t *group_offsets, int32_t *perm_row,
+                                        int32_t *row_src, float *row_gate, void *ws,
+                                        size_t ws_bytes, void *stream);
+
+/* a4 + a5 on the unpadded layout: x_perm, h, y have A = T*k rows (bf16
+ * [A, d], [A, d_e], [A, d]); the CTA pairs visit, for every expert, the
+ * 256-row windows of the rows that its rows touch, and store only the rows of
+ * that expert, so a window cut by an expert boundary is computed twice, once
+ * with each expert's weights.  Weights, gates and epilogues as
+ * moe_grouped_gemm_swiglu.  moe_permute and moe_combine run on this layout
+ * unchanged (with the perm_row of moe_build_offsets_unpadded). */
+moe_status_t moe_grouped_gemm_swiglu_unpadded(const moe_config_t *cfg, const void *x_perm,
+                                              const void *W13, const void *W2_t,
+                                              const int32_t *group_offsets, const float *row_gate,
+                                              void *h, void *y, uint32_t *status, void *stream);
+
 /* The receiving side of the expert-parallel dispatch ("Dropless and grouped
  * GEMM", sec. 4 step 5: the dispatch lands rows already grouped by expert and
  * padded to the alignment, and hands the receiver its per-expert counts;

@@ -36,6 +36,7 @@ __all__ = [
     "moe_backward_workspace_size", "moe_layer_bwd", "moe_gate_up_save_size", "moe_layer_fwd_save",
     "moe_widen_e4m3", "moe_grouped_gemm_swiglu_scaled", "moe_shared_expert_scaled",
     "moe_gather_rows", "moe_build_blocks_from_counts", "moe_copy_pieces",
+    "moe_build_offsets_unpadded", "moe_grouped_gemm_swiglu_unpadded",
 ]
 
 MOE_OK = 0
@@ -142,6 +143,8 @@ def load():
         "moe_gather_rows": (ctypes.c_int, [P, P, P, ctypes.c_int64, I32, P, P, P]),
         "moe_build_blocks_from_counts": (ctypes.c_int, [P, I32, I32, I32, P, P, P, I32, P, P, P]),
         "moe_copy_pieces": (ctypes.c_int, [P, P, I32, P, P, P, I32, I32, P, P, P]),
+        "moe_build_offsets_unpadded": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_grouped_gemm_swiglu_unpadded": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_swiglu_scaled": (ctypes.c_int, [CP] + [P] * 13),
         "moe_shared_expert_scaled": (ctypes.c_int, [CP] + [P] * 9),
         "moe_layer_fwd_save": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, P, P, SZ,
@@ -411,6 +414,25 @@ def moe_copy_pieces(src, dst, src_row, dst_row, rows, max_rows: int, src_gate=No
     _check(load().moe_copy_pieces(_ptr(src), _ptr(dst), src.shape[-1], _ptr(src_row),
                                   _ptr(dst_row), _ptr(rows), rows.numel(), int(max_rows),
                                   _ptr(src_gate), _ptr(dst_gate), _stream(stream)))
+
+
+def moe_build_offsets_unpadded(cfg, topk_idx, topk_w, counts, group_offsets, perm_row, row_src,
+                               row_gate, ws, stream=None) -> None:
+    """Counts, group offsets [E + 1] and the permutation of the unpadded
+    layout (A rows, no padding, no block table)."""
+    _check(load().moe_build_offsets_unpadded(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(group_offsets),
+        _ptr(perm_row), _ptr(row_src), _ptr(row_gate), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_unpadded(cfg, x_perm, W13, W2_t, group_offsets, row_gate, h, y,
+                                     status=None, stream=None) -> None:
+    """The grouped GEMMs on the unpadded layout (windows cut by an expert
+    boundary run once per expert)."""
+    _check(load().moe_grouped_gemm_swiglu_unpadded(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(group_offsets),
+        _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
 
 
 def moe_widen_e4m3(q, out, stream=None) -> None:

@@ -804,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // visits are enumerated, so the round-robin over CTA pairs stays balanced.
 
 struct PairTile {
-    int e, m0, hi, nb;  // rows [m0, m0 + hi) of the visit are valid
+    int e, m0, lo, hi, nb;  // rows [m0 + lo, m0 + hi) of the visit are valid
 };
 
 // Visits of expert e are numbered from vpref[e] (exclusive prefix over the
@@ -815,7 +815,8 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
     PairTile p;
     const int v = t / a.n_tiles;
     p.nb = t - v * a.n_tiles;
-    if (!a.block_metadata) {
+    p.lo = 0;
+    if (!a.block_metadata && !a.unpadded) {
         p.e = 0;
         p.m0 = v * 256;
         p.hi = min(256, a.dense_rows - p.m0);
@@ -827,6 +828,18 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
         if (vpref[mid] <= v) lo = mid; else hi = mid;
     }
     p.e = lo;
+    if (a.unpadded) {
+        // the experts' rows lie back to back (padded_offsets holds the plain
+        // group offsets): visit v of expert e is the 256-row window
+        // first + (v - vpref[e]) of the rows, of which the rows inside
+        // [start_e, end_e) are stored; a window cut by an expert boundary
+        // is visited once for each expert it holds
+        const int s0 = ld_dep(a.padded_offsets + lo), s1 = ld_dep(a.padded_offsets + lo + 1);
+        p.m0 = (s0 / 256 + (v - vpref[lo])) * 256;
+        p.lo = max(s0 - p.m0, 0);
+        p.hi = min(s1 - p.m0, 256);
+        return p;
+    }
     const int per = 256 / a.block_rows;
     const int mb = ld_dep(a.padded_offsets + lo) / a.block_rows + (v - vpref[lo]) * per;
     const int32_t* bm = a.block_metadata;
@@ -848,7 +861,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
                                          int q, int lane, uint8_t* stage, const CUtensorMap* tmOut,
                                          int& buf) {
     const int row = q * 32 + lane;
-    if (q * 32 + 32 > ti.hi) {
+    if (q * 32 < ti.lo || q * 32 + 32 > ti.hi) {
         if constexpr (EPI == kEpiSwiGLU) epi_swiglu(a, ti, taddr, row);
         else epi_gate<BN>(a, ti, taddr, row);
         return;
@@ -964,17 +977,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // memory is taken after the wait, as in k_grouped_gemm
     pdl_wait();
     if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
-    if (warp == 2 && args.block_metadata) {
+    if (warp == 2 && (args.block_metadata || args.unpadded)) {
         // per-expert visit counts from the segment sizes, exclusive warp scan
-        const int per = 256 / args.block_rows;
+        const int per = args.unpadded ? 1 : 256 / args.block_rows;
         int running = 0;
         for (int base = 0; base < args.n_experts; base += 32) {
             const int e = base + lane;
             int nv = 0;
             if (e < args.n_experts) {
-                const int nblk = (ld_dep(args.padded_offsets + e + 1) - ld_dep(args.padded_offsets + e)) /
-                                 args.block_rows;
-                nv = (nblk + per - 1) / per;
+                const int s0 = ld_dep(args.padded_offsets + e), s1 = ld_dep(args.padded_offsets + e + 1);
+                if (args.unpadded) {
+                    nv = s1 > s0 ? (s1 - 1) / 256 - s0 / 256 + 1 : 0;  // windows the rows touch
+                } else {
+                    const int nblk = (s1 - s0) / args.block_rows;
+                    nv = (nblk + per - 1) / per;
+                }
             }
             int x = nv;
 #pragma unroll
@@ -993,7 +1010,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int nvisits = args.block_metadata ? vpref[args.n_experts] : (args.dense_rows + 255) / 256;
+    const int nvisits = (args.block_metadata || args.unpadded) ? vpref[args.n_experts]
+                                                                : (args.dense_rows + 255) / 256;
     const int total = nvisits * args.n_tiles;
     const int cluster = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
@@ -1138,7 +1156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ti.e = p.e;
             ti.nb = p.nb;
             ti.m0 = p.m0 + BM * static_cast<int>(rank);
-            ti.lo = 0;
+            ti.lo = max(0, p.lo - BM * static_cast<int>(rank));
             ti.hi = min(BM, p.hi - BM * static_cast<int>(rank));
             ti.skip = false;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +

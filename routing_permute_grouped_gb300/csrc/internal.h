@@ -40,6 +40,10 @@ struct GemmArgs {
     const int32_t* padded_offsets;  // [E + 1] segment starts (CTA-pair kernel)
     int32_t block_rows;             // rows per block of the table (P)
     int32_t n_experts;              // E (CTA-pair kernel)
+    // CTA-pair kernel on the unpadded layout: padded_offsets holds the plain
+    // group offsets, no block table; visits are the 256-row windows of each
+    // expert's rows (a window cut by a boundary is visited once per expert)
+    int32_t unpadded;
     // A rows gathered from token rows (permute fused into GEMM1's A load):
     // padded row r reads gather_x[row_src[r] / gather_k], pad rows read zeros
     const void* gather_x;

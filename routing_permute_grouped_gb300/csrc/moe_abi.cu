@@ -315,6 +315,42 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2 (down + gate)");
 }
 
+// The grouped GEMMs on the unpadded layout: rows [group_offsets[e],
+// group_offsets[e + 1]) belong to expert e, with no padding between experts.
+static moe_status_t do_experts_unpadded(const moe_config_t& c, const void* x_perm, const void* W13,
+                                        const void* W2_t, const int32_t* group_offsets,
+                                        const float* row_gate, void* h, void* y, uint32_t* status,
+                                        cudaStream_t st) {
+    const int64_t A = static_cast<int64_t>(c.T) * c.k;
+    const int64_t windows = (A + 255) / 256 + c.E;  // at most: one more per expert boundary
+    GemmArgs a{};
+    a.unpadded = 1;
+    a.padded_offsets = group_offsets;
+    a.block_rows = c.pad_multiple;
+    a.n_experts = c.E;
+    a.status = status;
+    a.n_tiles = (2 * c.d_e) / 256;
+    a.k_blocks = c.d / 64;
+    a.b_rows_per_expert = 2 * c.d_e;
+    a.out = h;
+    a.ldo = c.d_e;
+    a.out_rows = A;
+    cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x_perm, A, W13,
+                                        static_cast<int64_t>(c.E) * 2 * c.d_e, c.d, a,
+                                        static_cast<int>(windows * a.n_tiles), st);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1, unpadded");
+    const int bn2 = (c.d % 256 == 0) ? 256 : 128;
+    a.n_tiles = c.d / bn2;
+    a.k_blocks = c.d_e / 64;
+    a.b_rows_per_expert = c.d;
+    a.out = y;
+    a.ldo = c.d;
+    a.row_gate = row_gate;
+    e = launch_grouped_gemm(kEpiGate, bn2, h, A, W2_t, static_cast<int64_t>(c.E) * c.d, c.d_e, a,
+                            static_cast<int>(windows * a.n_tiles), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2, unpadded");
+}
+
 // Operands of one expert (or of the shared expert) on the small-M kernel.
 struct SkinnyIO {
     const void* x;         // token rows: bf16 [rows, d], or (e4m3) their pairs [2 rows, d]
@@ -1021,6 +1057,42 @@ moe_status_t moe_gather_rows(const void* src, const int32_t* idx, void* dst, int
     cudaError_t e = launch_gather_rows(src, idx, dst, n, d, src_gate, dst_gate,
                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gather rows");
+}
+
+moe_status_t moe_build_offsets_unpadded(const moe_config_t* cfg, const int32_t* topk_idx,
+                                        const float* topk_w, int32_t* counts,
+                                        int32_t* group_offsets, int32_t* perm_row,
+                                        int32_t* row_src, float* row_gate, void* ws,
+                                        size_t ws_bytes, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!topk_idx || !counts || !group_offsets || !perm_row || !row_src || !row_gate || !ws)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (ws_bytes < offsets_ws_bytes(*cfg))
+        return fail(MOE_ERR_WORKSPACE, "offsets scratch of %zu bytes, %zu needed", ws_bytes,
+                    offsets_ws_bytes(*cfg));
+    if (cfg->T == 0) return MOE_OK;
+    const int64_t A = static_cast<int64_t>(cfg->T) * cfg->k;
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    cudaError_t e = launch_offsets(topk_idx, topk_w, A, cfg->E, 1, A, counts, group_offsets, nullptr,
+                                   nullptr, perm_row, row_src, row_gate,
+                                   reinterpret_cast<uint32_t*>(w8),
+                                   reinterpret_cast<int32_t*>(w8 + 256),
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "offsets kernels (unpadded)");
+}
+
+moe_status_t moe_grouped_gemm_swiglu_unpadded(const moe_config_t* cfg, const void* x_perm,
+                                              const void* W13, const void* W2_t,
+                                              const int32_t* group_offsets, const float* row_gate,
+                                              void* h, void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (!x_perm || !W13 || !W2_t || !group_offsets || !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    if (cfg->T == 0) return MOE_OK;
+    return do_experts_unpadded(*cfg, x_perm, W13, W2_t, group_offsets, row_gate, h, y, status,
+                               static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_build_blocks_from_counts(const int32_t* counts, int32_t n_src, int32_t E,

@@ -165,13 +165,14 @@ __global__ void __launch_bounds__(kScanThreads)
         if (e == E - 1) padded_offsets[E] = s_total[0];
         if (!staged)
             for (int c = 0; c < n_chunks; ++c) chunk_counts[(int64_t)c * E + e] += po;
-        for (int i = 0; i < nblk; ++i) {
-            block_metadata[3 * (b0 + i) + 0] = e;
-            block_metadata[3 * (b0 + i) + 1] = po + i * P;
-            block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
-        }
+        if (block_metadata)  // null: the unpadded layout, which has no block table
+            for (int i = 0; i < nblk; ++i) {
+                block_metadata[3 * (b0 + i) + 0] = e;
+                block_metadata[3 * (b0 + i) + 1] = po + i * P;
+                block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
+            }
     }
-    if (e == 0) *num_blocks = s_total[1];
+    if (e == 0 && num_blocks) *num_blocks = s_total[1];
     if (staged) {
         __syncthreads();
         const int n = n_chunks * E;
@@ -305,13 +306,14 @@ __global__ void __launch_bounds__(kSmallThreads)
         padded_offsets[tid] = po;
         if (tid == E - 1) padded_offsets[E] = s_total[0];
         running[tid] = po;
-        for (int i = 0; i < nblk; ++i) {
-            block_metadata[3 * (b0 + i) + 0] = tid;
-            block_metadata[3 * (b0 + i) + 1] = po + i * P;
-            block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
-        }
+        if (block_metadata)
+            for (int i = 0; i < nblk; ++i) {
+                block_metadata[3 * (b0 + i) + 0] = tid;
+                block_metadata[3 * (b0 + i) + 1] = po + i * P;
+                block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
+            }
     }
-    if (tid == 0) *num_blocks = s_total[1];
+    if (tid == 0 && num_blocks) *num_blocks = s_total[1];
     fill_pad_rows(s_size, hist, E, P, row_src, row_gate);
     for (int64_t r = s_total[0] + tid; r < R_max; r += blockDim.x) {
         row_src[r] = -1;

@@ -109,6 +109,26 @@ def padding_waste(counts, P: int) -> float:
     return (padded_rows(counts, P) - A) / A if A else 0.0
 
 
+def padded_tiles(counts, P: int, tile: int) -> int:
+    """Row tiles of height `tile` that the padded layout executes: each
+    expert's segment (ceil(c / P) * P rows) split into tiles on its own."""
+    return sum(-(-(-(-c // P) * P) // tile) for c in counts if c > 0)
+
+
+def unpadded_tiles(counts, tile: int) -> int:
+    """Row tiles of height `tile` that the unpadded schedule executes
+    ("Dropless and grouped GEMM", sec. 11): the experts' rows lie back to
+    back without padding, and a tile is executed once for every expert whose
+    rows it holds, so a tile that an expert boundary cuts runs twice.
+    Between the tile count of the rows and that count + E - 1."""
+    n, start = 0, 0
+    for c in counts:
+        if c > 0:
+            n += (start + c - 1) // tile - start // tile + 1
+        start += c
+    return n
+
+
 def layer_backward_useful_flops(T: int, k: int, d: int, d_e: int, d_s: int = 0,
                                 E: int = 0) -> int:
     """Useful FLOP of the layer backward: every forward GEMM C = A B has a data

@@ -251,3 +251,17 @@ def test_exchange_table_entry_points_check_arguments_before_launch(lib):
     assert c(fake, fake, 64, fake, fake, fake, 3, 8, fake, None, None) == 1  # gates both or neither
     assert c(fake, fake, 64, None, fake, fake, 3, 8, None, None, None) == 1
     assert c(None, None, 64, None, None, None, 0, 0, None, None, None) == 0  # nothing to move
+
+
+def test_unpadded_entry_points_check_arguments_before_launch(lib):
+    fake = ctypes.c_void_p(0x1000)
+    cfg = _cfg()
+    small = moe.moe_offsets_workspace_size(cfg) - 1
+    assert lib.moe_build_offsets_unpadded(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake,
+                                          fake, fake, small, None) == 3
+    assert lib.moe_build_offsets_unpadded(ctypes.byref(cfg), fake, fake, None, fake, fake, fake,
+                                          fake, fake, small + 1, None) == 1
+    assert lib.moe_grouped_gemm_swiglu_unpadded(ctypes.byref(cfg), fake, fake, fake, None, fake,
+                                                fake, fake, None, None) == 1
+    assert lib.moe_grouped_gemm_swiglu_unpadded(ctypes.byref(_cfg(d_e=200)), fake, fake, fake,
+                                                fake, fake, fake, fake, None, None) == 2

@@ -470,3 +470,36 @@ def test_zipf_exponents_give_the_stored_loads():
         assert round(float(ratio), 4) == synth.ZIPF_HOT_OVER_MEAN[name]
         if target > 1:
             assert abs(ratio - target) <= 0.02 * target
+
+
+def test_tile_counts_of_the_padded_and_unpadded_schedules():
+    # "Dropless and grouped GEMM", sec. 11: the pre-routed sizes at tile
+    # height 128 execute 515 tiles unpadded (512 tiles of rows, three
+    # segment starts inside a tile: +0.59 %) against 514 padded (65,792
+    # rows: +0.39 %)
+    g = _golden("unpadded_tiles_sec11.txt")
+    sizes, tile = g["counts"], g["tile"][0]
+    assert np.cumsum([0] + sizes).tolist() == g["group_offsets"]
+    assert ledger.unpadded_tiles(sizes, tile) == g["unpadded_tiles"][0]
+    assert g["unpadded_tiles"][0] == g["tiles_of_rows"][0] + g["extra_visits"][0]
+    assert g["unpadded_tiles"][0] * tile == g["unpadded_rows"][0]
+    assert ledger.padded_rows(sizes, tile) == g["padded_rows"][0]
+    assert ledger.padded_tiles(sizes, 128, tile) * tile == g["padded_rows"][0]
+    A = sum(sizes)
+    assert round(100 * (g["unpadded_rows"][0] / A - 1), 2) == g["unpadded_extra_pct"][0]
+    assert round(100 * (g["padded_rows"][0] / A - 1), 2) == g["padded_extra_pct"][0]
+    # the bounds the page states: rows / tile <= tiles <= rows / tile + E - 1
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        E = int(rng.integers(1, 40))
+        c = rng.integers(0, 700, E)
+        c[rng.random(E) < 0.2] = 0
+        tile = int(rng.choice([64, 128, 256]))
+        A = int(c.sum())
+        n = ledger.unpadded_tiles(c.tolist(), tile)
+        assert -(-A // tile) <= n <= -(-A // tile) + max(int((c > 0).sum()) - 1, 0)
+        # brute force: tiles x experts whose row ranges meet
+        starts = np.concatenate([[0], np.cumsum(c)])
+        brute = sum(1 for t in range(-(-A // tile)) for e in range(E)
+                    if c[e] > 0 and starts[e] < (t + 1) * tile and starts[e + 1] > t * tile)
+        assert n == brute
