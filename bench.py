@@ -603,13 +603,6 @@ def run_ours(args, shape, rank, world, local):
         step(evs[i])
     torch.cuda.synchronize()
     w3 = time.time()
-    clocks = stage_clocks = None
-    if sampler:
-        sampler.stop()
-        sampler.window("timed", w0, w1)
-        sampler.window("stages", w2, w3)
-        clocks = sampler.summary("timed")
-        stage_clocks = sampler.summary("stages")
     # per-stage median over the stage-pass steps
     stage_ms = {n: statistics.median(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
                 for j, n in enumerate(stage_names)}
@@ -643,13 +636,24 @@ def run_ours(args, shape, rank, world, local):
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    w4 = time.time()
     e0.record(pipe.s_in)
     for i in range(e2e_steps):
         pipe.submit(x_host, out_host[i % 2], **topk_kw)
     e1.record(pipe.s_out)
     pipe.synchronize()
+    w5 = time.time()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+    clocks = stage_clocks = e2e_clocks = None
+    if sampler:  # one sampler over the three regions, summarised per region
+        sampler.stop()
+        sampler.window("timed", w0, w1)
+        sampler.window("stages", w2, w3)
+        sampler.window("e2e", w4, w5)
+        clocks = sampler.summary("timed")
+        stage_clocks = sampler.summary("stages")
+        e2e_clocks = sampler.summary("e2e")
 
     pk = peaks()
     gemm_flops = ledger.routed_flops(A, d, de)
@@ -691,7 +695,7 @@ def run_ours(args, shape, rank, world, local):
         "data": "synthetic", "config": config_dict(shape, args.permute, args.weights, args.schedule),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "clocks": e2e_clocks},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": dict(roof, kernel="grouped GEMM stage (GEMM1+SwiGLU, GEMM2+gate)",
                          timing="stage pass: CUDA events around " + (
