@@ -50,3 +50,22 @@ def test_useful_flops_exclude_padding():
     routed = 2 * s.A * s.d * 3 * s.d_e
     assert ledger.routed_flops(s.A, s.d, s.d_e) == routed
     assert routed == 2_886_218_022_912
+
+
+def test_clock_windows_and_normalised_rate(bench):
+    """ClockSampler.summary picks the samples inside a region (median SM MHz,
+    the reasons seen there), and clock_normalised scales a rate by the
+    maximum over the median clock of the region."""
+    c = bench.ClockSampler(0)
+    c.source, c.period, c.sm_max = "nvml", 0.001, 2070.0
+    c.samples = [(0.5, 2070.0, 0), (1.1, 1800.0, 0x4), (1.2, 1900.0, 0x4), (1.3, 2000.0, 0),
+                 (2.5, 1500.0, 0x8)]
+    c.window("timed", 1.0, 1.4)
+    s = c.summary("timed")
+    assert s["samples"] == 3 and s["sm_mhz"] == 1900.0 and s["reasons"] == ["sw_power_cap"]
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    roof = {"achieved": 1700.0, "peak": 1935.5}
+    n = bench.clock_normalised(1.6, roof, s)
+    assert abs(n["stage_ms_x_mhz"] - 1.6 * 1900.0) < 1e-9
+    assert abs(n["achieved_at_max_clock"] - 1700.0 * 2070.0 / 1900.0) < 1e-9
+    assert bench.clock_normalised(1.6, roof, {"sm_mhz": None}) is None
