@@ -929,8 +929,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
     constexpr int BH = BN / 2;  // B rows staged by each CTA
-    constexpr int A_BYTES = BM * BK * 2;
-    constexpr int B_BYTES = BH * BK * 2;
+    // K blocks per stage.  A and B are loaded as 3D tensors [K block][row][64]
+    // whose {64, rows, 2} box lands as two 128-byte-swizzled tiles back to
+    // back: one TMA operation per operand carries two K blocks (3 stages of
+    // 64 KB instead of 6 of 32 KB), half the operations for the same bytes in
+    // flight.  The gather variant keeps one K block per stage.
+    constexpr int KP = GATHER ? 1 : 2;
+    constexpr int A_TILE = BM * BK * 2, B_TILE = BH * BK * 2;
+    constexpr int A_BYTES = A_TILE * KP;
+    constexpr int B_BYTES = B_TILE * KP;
     constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
     constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
@@ -1052,7 +1059,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (rr < p.hi) grow[j] = ld_dep(args.row_src + p.m0 + rr) / args.gather_k;
                 }
             }
-            for (int kb = 0; kb < args.k_blocks; ++kb) {
+            const int n_steps = (args.k_blocks + KP - 1) / KP;
+            for (int kb = 0; kb < n_steps; ++kb) {
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(empty + s, ph ^ 1u, abort_flag);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -1064,15 +1072,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     armed &= ~(1u << s);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * STAGE_BYTES);
-                    const int kx = (rev ? args.k_blocks - 1 - kb : kb) * BK;
-                    if (!GATHER) tma_load_2d_pair(sA + s * A_BYTES, &tmA, kx, arow, full_leader);
-                    tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, kx, brow, full_leader, keep);
+                    const int kstep = rev ? n_steps - 1 - kb : kb;
+                    if constexpr (!GATHER) {
+                        tma_load_3d_pair(sA + s * A_BYTES, &tmA, 0, arow, kstep * KP, full_leader);
+                        tma_load_3d_pair_hint(sB + s * B_BYTES, &tmB, 0, brow, kstep * KP, full_leader,
+                                              keep);
+                    } else {
+                        tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, kstep * BK, brow, full_leader, keep);
+                    }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                 }
                 if (GATHER)
                     tma_gather4_pair(smem_u32(sA + s * A_BYTES) + lane * 512u, &tmA,
-                                     (rev ? args.k_blocks - 1 - kb : kb) * BK, grow[0],
+                                     (rev ? n_steps - 1 - kb : kb) * BK, grow[0],
                                      grow[1], grow[2], grow[3], full_leader);
                 if (++s == S) {
                     s = 0;
@@ -1104,7 +1117,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                const int n_steps = (args.k_blocks + KP - 1) / KP;
+                for (int kb = 0; kb < n_steps; ++kb) {
                     if (!mbar_wait(full + s, ph, abort_flag)) {
                         timed_out = true;
                         break;
@@ -1113,10 +1127,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
                     const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + kk * 32),
-                                      sdesc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kp = 0; kp < KP; ++kp)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + kp * A_TILE + kk * 32),
+                                          sdesc_sw128(b_addr + kp * B_TILE + kk * 32), idesc,
+                                          (kb | kp | kk) != 0 ? 1u : 0u);
+                        }
                     issued = true;
                     mma_commit_pair(empty + s, 0x3);
                     if (++s == S) {
@@ -1247,6 +1264,23 @@ static bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t K,
     return make_tmap_box(tm, ptr, rows, K, BK, box_rows);
 }
 
+// K-major operand [rows, K] seen as [K / 64][rows][64]: a {64, box_rows, 2}
+// box carries two K blocks, landing as two 128-byte-swizzled tiles back to
+// back.  K blocks past the last read as zero.
+static bool make_tmap_kpair(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+    PFN_encodeTiled enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(K / BK)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(BK) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN, int EPI>
 static cudaError_t launch_t(const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
                             int max_tiles, cudaStream_t stream) {
@@ -1329,7 +1363,7 @@ template <int BN, int EPI, bool GATHER>
 static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tO,
                                  const GemmArgs& args, int max_visits, cudaStream_t stream) {
     constexpr int NT = kThreads;
-    constexpr int STAGE_BYTES = BM * BK * 2 + (BN / 2) * BK * 2;
+    constexpr int STAGE_BYTES = (BM * BK * 2 + (BN / 2) * BK * 2) * (GATHER ? 1 : 2);
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
     constexpr int SMEM = 1024 + S * STAGE_BYTES + kOutStageBytes + 512 + 4 * 260;
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -1362,9 +1396,14 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
                                 cudaStream_t stream) {
     CUtensorMap tA, tB;
     const bool pair = epi != kEpiRouter && epi != kEpiPartial;
+    const bool kpair = pair && epi != kEpiSwiGLUGather;
     const int a_box = epi == kEpiSwiGLUGather ? 1 : BM;  // gather4 reads one-row boxes
-    if (!make_tmap(&tA, A, rowsA, K, a_box) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn))
+    if (kpair) {
+        if (!make_tmap_kpair(&tA, A, rowsA, K, BM) || !make_tmap_kpair(&tB, B, rowsB, K, bn / 2))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap(&tA, A, rowsA, K, a_box) || !make_tmap(&tB, B, rowsB, K, pair ? bn / 2 : bn)) {
         return cudaErrorInvalidValue;
+    }
     if (pair) {
         // the output as a [rows, ldo] bf16 tensor for the staged TMA stores
         CUtensorMap tO;

@@ -314,6 +314,27 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* smem_dst, const CUte
         : "memory");
 }
 
+// 3D tiled loads of box {x0.., y0.., z0..} (the pair kernel's operands seen
+// as [K-block][row][64 elements]: one box carries two K blocks)
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* tm, int32_t x0,
+                                                 int32_t y0, int32_t z0, uint32_t bar_cluster_addr) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x0), "r"(y0), "r"(z0), "r"(bar_cluster_addr)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(void* smem_dst, const CUtensorMap* tm,
+                                                      int32_t x0, int32_t y0, int32_t z0,
+                                                      uint32_t bar_cluster_addr, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x0), "r"(y0), "r"(z0), "r"(bar_cluster_addr),
+        "l"(policy)
+        : "memory");
+}
+
 // Tensor memory shared by a CTA pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
