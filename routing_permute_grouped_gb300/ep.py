@@ -350,6 +350,8 @@ class GpuEp(EpLayerBase):
         """The pieces this rank keeps, with device descriptors: its own
         segment starts (padded offsets of its experts), the landing rows, the
         counts from the exchange."""
+        import torch
+
         from . import moe_copy_pieces
 
         if not pieces:
@@ -359,7 +361,7 @@ class GpuEp(EpLayerBase):
                 raise RuntimeError("aliased exchange buffers with moving pieces")
             return
         r, El = self.rank, self.El
-        own = self._buf("padded_offsets", __import__("torch").int32, (self.E + 1,))[r * El:(r + 1) * El]
+        own = self._buf("padded_offsets", torch.int32, (self.E + 1,))[r * El:(r + 1) * El]
         land = self.piece_row[r]
         rows = self._recv[r]
         src_row, dst_row = (land, own) if combine else (own, land)
