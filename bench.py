@@ -415,11 +415,12 @@ METRIC_TRAIN = "MoE layer fwd+bwd useful TFLOP/s (bf16, fp32 accumulate)"
 METRIC_FP8 = "MoE layer fwd useful TFLOP/s (e4m3 expert weights, fp32 accumulate)"
 
 
-def config_dict(shape, permute="separate", weights="bf16", schedule="padded"):
+def config_dict(shape, permute="layer", weights="bf16", schedule="padded", combine="kernel"):
     return {"workload": f"{shape.name}: T={shape.T} d={shape.d} d_e={shape.d_e} E={shape.E} "
                         f"k={shape.k} groups={shape.n_groups}/{shape.topk_groups} "
                         f"pad={shape.pad} shared={shape.d_shared}",
-            "permute": permute, "expert_weights": weights, "schedule": schedule,
+            "permute": permute, "combine": combine, "expert_weights": weights,
+            "schedule": schedule,
             "l2": "inputs larger than L2 (expert weights and permuted rows exceed 129 MB)",
             "parallelism": "replicas"}
 
@@ -440,13 +441,13 @@ def run_ours(args, shape, rank, world, local):
             inp[key] = inp[key].to(dev)
     cfg = moe.config_of(shape)
     fp8 = args.weights == "fp8"
-    if fp8 and args.permute != "separate":
-        raise SystemExit("--weights fp8 runs with the separate permute")
+    if fp8 and (args.permute == "gather" or args.combine != "kernel"):
+        raise SystemExit("--weights fp8 runs with the layer's permute and combine")
     unpadded = args.schedule == "unpadded"
-    if unpadded and (fp8 or args.permute != "separate" or
+    if unpadded and (fp8 or args.permute == "gather" or args.combine != "kernel" or
                      shape.T * shape.k <= 32 * shape.E):
         raise SystemExit("--schedule unpadded runs the CTA-pair GEMMs with bf16 weights and the "
-                         "separate permute")
+                         "permute and combine kernels")
     layer = moe.MoeLayer(cfg, inp["W1"], inp["W3"], inp["W2"], Wg=inp.get("Wg"),
                          bias=inp.get("bias"), Ws1=inp.get("Ws1"), Ws3=inp.get("Ws3"),
                          Ws2=inp.get("Ws2"), fp8=fp8)
@@ -495,30 +496,36 @@ def run_ours(args, shape, rank, world, local):
     router_partial = buf("router_partial", f32, (nsplit,)) if nsplit else None
     offs_ws = ws[L["status"]:L["topk_idx"]]
 
-    stage_names = ["route", "offsets", "permute", "grouped_gemm", "shared", "combine"]
+    # The stages in enqueue order, (name, call).  By default they mirror
+    # moe_layer_fwd: on the bf16 CTA-pair path with a shared expert, the
+    # shared GEMM1 runs before the routed GEMMs with the permute in its
+    # epilogue, the shared GEMM2 after them, then the combine.  (With e4m3
+    # weights widened for the CTA-pair kernel the layer does the same with the
+    # scaled GEMMs; the stage pass there runs the permute kernel and the whole
+    # scaled shared expert after the routed GEMMs.)
+    pair_shared = bool(ds) and not skinny and not fp8 and not unpadded
+    perm_in_shared = pair_shared and args.permute == "layer"
+    stages = []
+    if not shape.prerouted:
+        # the router the layer runs: split-K for small batches
+        stages.append(("route", lambda: moe.moe_route_splitk(
+            cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w, router_partial)))
+    if unpadded:  # group offsets in po, no block table
+        stages.append(("offsets", lambda: moe.moe_build_offsets_unpadded(
+            cfg, topk_idx, topk_w, counts, po, perm_row, row_src, row_gate, offs_ws)))
+    else:
+        stages.append(("offsets", lambda: moe.moe_build_offsets(
+            cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src, row_gate, offs_ws)))
+    if perm_in_shared:
+        stages.append(("shared_up_permute", lambda: moe.moe_shared_expert_up(
+            cfg, x, layer.Ws13, hs, perm_row, x_perm, status_word)))
+    elif fp8 and not wide:
+        stages.append(("permute", lambda: moe.moe_permute_fp8(
+            cfg, x, perm_row, x_perm, x_scale, xs8, xs_scale)))
+    elif args.permute != "gather":
+        stages.append(("permute", lambda: moe.moe_permute(cfg, x, perm_row, x_perm)))
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record()
-        if not shape.prerouted:
-            # the router the layer runs: split-K for small batches
-            moe.moe_route_splitk(cfg, x, layer.Wg_t, layer.bias, topk_idx, topk_w, router_partial)
-        if ev is not None:
-            ev[1].record()
-        if unpadded:  # group offsets in po, no block table
-            moe.moe_build_offsets_unpadded(cfg, topk_idx, topk_w, counts, po, perm_row, row_src,
-                                           row_gate, offs_ws)
-        else:
-            moe.moe_build_offsets(cfg, topk_idx, topk_w, counts, po, meta, nb, perm_row, row_src,
-                                  row_gate, offs_ws)
-        if ev is not None:
-            ev[2].record()
-        if fp8 and not wide:
-            moe.moe_permute_fp8(cfg, x, perm_row, x_perm, x_scale, xs8, xs_scale)
-        elif args.permute == "separate":
-            moe.moe_permute(cfg, x, perm_row, x_perm)
-        if ev is not None:
-            ev[3].record()
+    def grouped():
         if wide:  # widen the routed codes, then the scaled bf16 GEMMs
             moe.moe_widen_e4m3(layer.W13q, W13w)
             moe.moe_widen_e4m3(layer.W2q, W2w)
@@ -534,35 +541,57 @@ def run_ours(args, shape, rank, world, local):
         elif skinny:
             moe.moe_grouped_gemm_swiglu_skinny(cfg, x_perm, layer.W13, layer.W2_t, meta, nb,
                                                row_gate, h, y, status_word)
-        elif args.permute == "separate":
+        elif args.permute != "gather":
             moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate,
                                         h, y, status_word)
         else:
             moe.moe_grouped_gemm_swiglu_gather(cfg, x, row_src, layer.W13, layer.W2_t, meta, nb, po,
                                                row_gate, h, y, status_word)
-        if ev is not None:
-            ev[4].record()
-        if ds and wide:
-            moe.moe_widen_e4m3(layer.Ws13q, Ws13w)
-            moe.moe_widen_e4m3(layer.Ws2q, Ws2w)
-            moe.moe_shared_expert_scaled(cfg, x, Ws13w, layer.ss13, Ws2w, layer.ss2, hs, ys,
-                                         status_word)
-        elif ds and fp8:
-            moe.moe_shared_expert_fp8(cfg, xs8, xs_scale, layer.Ws13q, layer.ss13, layer.Ws2q,
-                                      layer.ss2, hs, hs8, hs_scale, ys, status_word)
-        elif ds:
-            moe.moe_shared_expert(cfg, x, layer.Ws13, layer.Ws2_t, hs, ys, status_word)
-        if ev is not None:
-            ev[5].record()
-        moe.moe_combine(cfg, y, perm_row, ys, out)
-        if ev is not None:
-            ev[6].record()
 
-    launches_per_step = forward_launches(shape, skinny, fp8, args.permute == "separate")
+    stages.append(("grouped_gemm", grouped))
+    fused_combine = pair_shared and args.combine == "fused"
+    if pair_shared:
+        if not perm_in_shared:
+            stages.append(("shared_up", lambda: moe.moe_shared_expert_up(
+                cfg, x, layer.Ws13, hs, None, None, status_word)))
+        if fused_combine:
+            stages.append(("shared_down_combine", lambda: moe.moe_shared_expert_down_combine(
+                cfg, hs, layer.Ws2_t, y, perm_row, out, status_word)))
+        else:
+            stages.append(("shared_down", lambda: moe.moe_shared_expert_down(
+                cfg, hs, layer.Ws2_t, ys, status_word)))
+    elif ds:
+        def shared():
+            if wide:
+                moe.moe_widen_e4m3(layer.Ws13q, Ws13w)
+                moe.moe_widen_e4m3(layer.Ws2q, Ws2w)
+                moe.moe_shared_expert_scaled(cfg, x, Ws13w, layer.ss13, Ws2w, layer.ss2, hs, ys,
+                                             status_word)
+            elif fp8:
+                moe.moe_shared_expert_fp8(cfg, xs8, xs_scale, layer.Ws13q, layer.ss13, layer.Ws2q,
+                                          layer.ss2, hs, hs8, hs_scale, ys, status_word)
+            else:
+                moe.moe_shared_expert(cfg, x, layer.Ws13, layer.Ws2_t, hs, ys, status_word)
+
+        stages.append(("shared", shared))
+    if not fused_combine:
+        stages.append(("combine", lambda: moe.moe_combine(cfg, y, perm_row, ys, out)))
+    stage_names = [n for n, _ in stages]
+
+    def step(ev=None):
+        for i, (_, call) in enumerate(stages):
+            if ev is not None:
+                ev[i].record()
+            call()
+        if ev is not None:
+            ev[len(stages)].record()
+
+    launches_per_step = forward_launches(shape, skinny, fp8,
+                                         "kernel" if unpadded else args.permute, args.combine)
     topk_kw_dev = dict(topk_idx=inp["topk_idx"], topk_w=inp["topk_w"]) if shape.prerouted else {}
 
     def layer_step():
-        if args.permute == "separate" and not unpadded:
+        if args.permute == "layer" and args.combine == "kernel" and not unpadded:
             layer(x, out, **topk_kw_dev)  # moe_layer_fwd: the whole layer, one call
         else:
             step()
@@ -680,8 +709,8 @@ def run_ours(args, shape, rank, world, local):
     roof["algorithmic"] = {"flop": gemm_flops, "bytes": gemm_bytes, "active_experts": active}
     perm_bytes = ledger.permute_bytes_alg(T, k, d)
     comb_bytes = ledger.combine_bytes_alg(T, k, d, bool(ds))
-    perm_gbs = perm_bytes / (stage_ms["permute"] / 1e3) / 1e9
-    comb_gbs = comb_bytes / (stage_ms["combine"] / 1e3) / 1e9
+    perm_gbs = perm_bytes / (stage_ms["permute"] / 1e3) / 1e9 if "permute" in stage_ms else None
+    comb_gbs = comb_bytes / (stage_ms["combine"] / 1e3) / 1e9 if "combine" in stage_ms else None
     traffic = recorded_traffic("skinny_gemm" if skinny else "grouped_gemm",
                                shape.name + ("_fp8" if fp8 else ""))
     line = {
@@ -692,7 +721,8 @@ def run_ours(args, shape, rank, world, local):
         "dtype": ("e4m3 (weights, widened to bf16 for the MMAs; per-channel scales on the fp32 "
                   "accumulators)" if wide else
                   "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16"),
-        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights, args.schedule),
+        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights, args.schedule,
+                                                     args.combine),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "clocks": e2e_clocks},
@@ -708,8 +738,10 @@ def run_ours(args, shape, rank, world, local):
         "stages": {"ms": {n: round(v, 4) for n, v in stage_ms.items()},
                    "clocks": stage_clocks,
                    "serial_sum_ms": round(sum(stage_ms.values()), 4),
-                   "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm_gbs"],
-                   "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm_gbs"],
+                   "permute_gbs": perm_gbs,
+                   "permute_frac_hbm": perm_gbs / pk["hbm_gbs"] if perm_gbs else None,
+                   "combine_gbs": comb_gbs,
+                   "combine_frac_hbm": comb_gbs / pk["hbm_gbs"] if comb_gbs else None,
                    "expert_counts": counts_h,
                    "padded_rows": ledger.padded_rows(counts_h, shape.pad),
                    # 256-row windows the CTA pairs execute under each schedule
@@ -734,21 +766,28 @@ def run_ours(args, shape, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def forward_launches(shape, skinny: bool, fp8: bool = False, separate_permute: bool = True) -> int:
+def forward_launches(shape, skinny: bool, fp8: bool = False, permute: str = "layer",
+                     combine: str = "kernel") -> int:
     """Kernels of one layer forward: router (2 when split-K with a scratch:
-    partial logits + reduce; 1 fused or clustered), offsets (1 or
-    3), permute (none when fused), 2 routed GEMMs, 2 shared-expert GEMMs (none
-    on the small-M kernel, whose launches carry the shared tiles), combine,
-    and with e4m3 weights the split of h between the GEMMs."""
+    partial logits + reduce; 1 fused or clustered), offsets (1 or 3), permute
+    (none when it runs in the shared expert's GEMM1 epilogue, the layer's
+    choice on the CTA-pair kernel with a shared expert, or in GEMM1's A
+    load), 2 routed GEMMs, 2 shared-expert GEMMs (none on the small-M kernel,
+    whose launches carry the shared tiles), combine (none when it runs in the
+    shared expert's GEMM2 epilogue), and with e4m3 weights the split of h
+    between the GEMMs."""
     import routing_permute_grouped_gb300 as moe
 
     cfg = moe.config_of(shape)
     nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
     offsets_launches = 1 if shape.A <= 4096 else 3  # one-CTA offsets kernel for small batches
     widen = (2 + (2 if shape.d_shared else 0)) if fp8 and not skinny else 0
+    pair_shared = bool(shape.d_shared) and not skinny
+    permute_kernel = not (permute == "gather" or (pair_shared and permute == "layer"))
+    fused_combine = pair_shared and not fp8 and combine == "fused"
     return ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
-            + (1 if separate_permute else 0) + 2
-            + (2 if shape.d_shared and not skinny else 0) + 1
+            + (1 if permute_kernel else 0) + 2
+            + (2 if pair_shared else 0) + (0 if fused_combine else 1)
             + (1 if fp8 and skinny else 0)  # e4m3 pairs of h between the small-M GEMMs
             + widen)
 
@@ -1078,8 +1117,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--permute", choices=["separate", "fused"], default="separate",
-                    help="permute as its own kernel, or fused into GEMM1's A load")
+    ap.add_argument("--permute", choices=["layer", "kernel", "gather"], default="layer",
+                    help="layer: as moe_layer_fwd (in the shared expert's GEMM1 epilogue when "
+                         "there is one on the CTA-pair kernel, else its own kernel); kernel: "
+                         "always its own kernel; gather: fused into GEMM1's A load (stage calls)")
+    ap.add_argument("--combine", choices=["kernel", "fused"], default="kernel",
+                    help="kernel: the combine as its own kernel (the layer); fused: in the "
+                         "shared expert's GEMM2 epilogue (stage calls)")
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weights in bf16, or e4m3 with per-output-channel scales")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",

@@ -435,6 +435,43 @@ moe_status_t moe_shared_expert(const moe_config_t *cfg, const void *x, const voi
                                const void *Ws2_t, void *hs, void *ys, uint32_t *status,
                                void *stream);
 
+/* a6 in two halves, with the layer's fusions.  moe_shared_expert_up is
+ * the gate/up GEMM, hs = bf16( silu(x Ws1) * (x Ws3) ); with perm_row and
+ * x_perm (both or neither) it also performs a3, the permute of
+ * moe_permute, in its epilogue: that GEMM's tiles are long (K = d), so
+ * after handing each accumulator back the epilogue warps copy the tile's
+ * column slice of their token rows to the k permuted positions
+ * ("MoE & MLA operators", sec. 2.3) while the next tile's MMAs run.
+ * x_perm then holds exactly what moe_permute writes (pad rows untouched).
+ *   x bf16 [T, d], Ws13 packed (moe_pack_experts with E = 1), hs bf16
+ *   [T, d_shared] written, perm_row int32 [A], x_perm bf16 [R_max, d]
+ *   written; all device.
+ * moe_shared_expert_down is the down projection, ys = bf16( hs Ws2 ).
+ *   hs bf16 [T, d_shared], Ws2_t packed, ys bf16 [T, d] written. */
+moe_status_t moe_shared_expert_up(const moe_config_t *cfg, const void *x, const void *Ws13,
+                                  void *hs, const int32_t *perm_row, void *x_perm,
+                                  uint32_t *status, void *stream);
+moe_status_t moe_shared_expert_down(const moe_config_t *cfg, const void *hs, const void *Ws2_t,
+                                    void *ys, uint32_t *status, void *stream);
+
+/* a6's down projection + a7 fused: the combine in the shared expert's GEMM2
+ * epilogue.  That tile covers token rows in token order, so the thread that
+ * owns output row t adds the token's k routed rows there ("MoE & MLA
+ * operators", sec. 2.5: the down-projection epilogue sums back into token
+ * order; sec. 6.4: a fixed order, no atomics):
+ *   out[t] = bf16( sum_{j=0..k-1} y[perm_row[t*k + j]] + bf16(hs Ws2)[t] )
+ * in fp32 in exactly that order, one rounding at the end: bit for bit
+ * moe_shared_expert_down followed by moe_combine, without writing or
+ * reading ys.  Slower than the two calls at the default workload (the
+ * gathers of the k rows hold up the epilogue of GEMM2's short tiles); the
+ * layer does not use it.
+ *   hs bf16 [T, d_shared], Ws2_t packed, y bf16 [R_max, d], perm_row int32
+ *   [A], out bf16 [T, d] written; all device. */
+moe_status_t moe_shared_expert_down_combine(const moe_config_t *cfg, const void *hs,
+                                            const void *Ws2_t, const void *y,
+                                            const int32_t *perm_row, void *out, uint32_t *status,
+                                            void *stream);
+
 /* a6 with e4m3 weights (moe_pack_experts_fp8 with E = 1) on the kernel of
  * moe_grouped_gemm_swiglu_fp8 with a dense tile list (chunks of 64 token rows
  * times panels of 256 weight rows).
@@ -471,8 +508,12 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y, const int32_t *
  * before the top-k; otherwise it is the single kernel of moe_route.
  * When the mean rows per expert, T*k/E, is at most 32 the expert GEMMs run
  * on the kernel of moe_grouped_gemm_swiglu_skinny, with the shared expert's
- * tiles appended to the same two launches; otherwise on the CTA-pair kernel
- * of moe_grouped_gemm_swiglu followed by moe_shared_expert. */
+ * tiles appended to the same two launches, after moe_permute; otherwise on
+ * the CTA-pair kernel of moe_grouped_gemm_swiglu, with the shared expert
+ * split around it: moe_shared_expert_up (with the permute in its epilogue)
+ * before the routed GEMMs, moe_shared_expert_down after them (with no
+ * shared expert: moe_permute before the routed GEMMs).  moe_combine ends
+ * the layer. */
 moe_status_t moe_layer_fwd(const moe_config_t *cfg, const moe_weights_t *w, const void *x,
                            void *out, void *ws, size_t ws_bytes, void *stream);
 

@@ -27,7 +27,8 @@ __all__ = [
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
     "moe_pack_router", "moe_pack_experts", "moe_pack_weights", "moe_route", "moe_route_splitk",
     "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
-    "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_combine", "moe_layer_fwd",
+    "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_shared_expert_up", "moe_shared_expert_down",
+    "moe_shared_expert_down_combine", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
     "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_fp8", "moe_grouped_gemm_swiglu_skinny",
     "moe_grouped_gemm_swiglu_fp8", "moe_layer_fwd_fp8", "moe_layer_fwd_fp8_prerouted",
@@ -121,6 +122,9 @@ def load():
         "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_swiglu_gather": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
+        "moe_shared_expert_up": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
+        "moe_shared_expert_down": (ctypes.c_int, [CP, P, P, P, P, P]),
+        "moe_shared_expert_down_combine": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
         "moe_combine": (ctypes.c_int, [CP, P, P, P, P, P]),
         "moe_layer_fwd": (ctypes.c_int, [CP, ctypes.POINTER(MoeWeights), P, P, P, SZ, P]),
         "moe_layer_fwd_prerouted": (ctypes.c_int,
@@ -343,6 +347,25 @@ def moe_shared_expert_fp8(cfg, xs8, xs_scale, Ws13q, ss13, Ws2q, ss2, hs, hs8, h
 def moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys, status=None, stream=None) -> None:
     _check(load().moe_shared_expert(ctypes.byref(cfg), _ptr(x), _ptr(Ws13), _ptr(Ws2_t), _ptr(hs),
                                     _ptr(ys), _ptr(status), _stream(stream)))
+
+
+def moe_shared_expert_up(cfg, x, Ws13, hs, perm_row=None, x_perm=None, status=None,
+                         stream=None) -> None:
+    _check(load().moe_shared_expert_up(ctypes.byref(cfg), _ptr(x), _ptr(Ws13), _ptr(hs),
+                                       _ptr(perm_row), _ptr(x_perm), _ptr(status),
+                                       _stream(stream)))
+
+
+def moe_shared_expert_down(cfg, hs, Ws2_t, ys, status=None, stream=None) -> None:
+    _check(load().moe_shared_expert_down(ctypes.byref(cfg), _ptr(hs), _ptr(Ws2_t), _ptr(ys),
+                                         _ptr(status), _stream(stream)))
+
+
+def moe_shared_expert_down_combine(cfg, hs, Ws2_t, y, perm_row, out, status=None,
+                                   stream=None) -> None:
+    _check(load().moe_shared_expert_down_combine(ctypes.byref(cfg), _ptr(hs), _ptr(Ws2_t),
+                                                 _ptr(y), _ptr(perm_row), _ptr(out),
+                                                 _ptr(status), _stream(stream)))
 
 
 def moe_combine(cfg, y, perm_row, shared_out, out, stream=None) -> None:

@@ -185,6 +185,146 @@ __device__ __forceinline__ void epi_gate(const GemmArgs& a, const TileInfo& ti, 
     }
 }
 
+// ---------------------------------------------------- combine epilogue --
+// The shared expert's GEMM2 tile covers token rows in token order, so the
+// layer's combine ("MoE & MLA operators", sec. 2.5: the k weighted expert
+// rows of a token summed back in token order, plus the shared expert's row)
+// can be taken by the thread that owns the token's output row: no atomics,
+// and the same fixed order as the stand-alone combine kernel, so the result
+// is bit for bit the one of GEMM2 followed by the combine.
+
+// The routed rows of the token (comb_perm[token * k + j], j < k), -1 past k
+// or for a row past the tile's valid rows.
+__device__ __forceinline__ void combine_rows_of(const GemmArgs& a, int token, bool valid,
+                                                int (&pr)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        pr[j] = (valid && j < a.comb_k) ? ld_dep(a.comb_perm + (int64_t)token * a.comb_k + j) : -1;
+}
+
+// s[i] = sum over j ascending (rows < 0 skipped) of comb_y[pr[j]][col + i],
+// fp32 from zero, for 32 columns; the loads of two rows are in flight at a
+// time (the rows were fetched into L2 ahead of the epilogue).
+__device__ __forceinline__ void combine_sum32(const GemmArgs& a, const int (&pr)[8], int64_t col,
+                                              float (&s)[32]) {
+    const __nv_bfloat16* y = static_cast<const __nv_bfloat16*>(a.comb_y);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s[i] = 0.0f;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; j0 += 2) {
+        uint4 in[2][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+            if (pr[j0 + jj] >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(y + (int64_t)pr[j0 + jj] * a.comb_ldy + col);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) in[jj][u] = ld_dep(src + u);
+            }
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+            if (pr[j0 + jj] >= 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t w[4] = {in[jj][u].x, in[jj][u].y, in[jj][u].z, in[jj][u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        s[8 * u + 2 * i] += __uint_as_float(w[i] << 16);
+                        s[8 * u + 2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                    }
+                }
+            }
+    }
+}
+
+// The tile's own result rounded to bf16 (as the stand-alone GEMM2 stores it)
+// added last, then one rounding to bf16.
+__device__ __forceinline__ uint32_t combine_pack2(float s0, float s1, uint32_t v0, uint32_t v1) {
+    const float r0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(v0)));
+    const float r1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(v1)));
+    return pack_bf16x2(s0 + r0, s1 + r1);
+}
+
+// Per-thread path of the combine epilogue (rows of a partly valid warp).
+template <int BN>
+__device__ __forceinline__ void epi_combine(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                            int row, const int (&pr)[8]) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    const bool valid = row >= ti.lo && row < ti.hi;
+    __nv_bfloat16* dst = out + (int64_t)(ti.m0 + row) * a.ldo + (int64_t)ti.nb * BN;
+    const float* cs = tile_scales(a, ti, ti.nb * BN);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        float sum[32];
+        combine_sum32(a, pr, (int64_t)ti.nb * BN + c * 32, sum);
+        uint32_t v[32];
+        tmem_ld32(taddr + c * 32, v);
+        tmem_ld_wait();
+        if (cs) scale_cols(v, cs + c * 32);
+        if (valid) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p[i] = combine_pack2(sum[2 * i], sum[2 * i + 1], v[2 * i], v[2 * i + 1]);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        }
+    }
+}
+
+// ---------------------------------------------------- permute epilogue --
+// The permute ("MoE & MLA operators", sec. 2.3: every token row copied to its
+// k expert-major positions) in the slack of the shared expert's GEMM1.  That
+// GEMM's tiles are long (K = d) and its epilogue waits for the next
+// accumulator most of the time; after handing the accumulator back, the warp
+// copies the tile's column slice of its 32 token rows, 8 rows at a time with
+// the lanes across the columns (coalesced 512-byte accesses).  The tiles of
+// one 256-row visit cover the row's columns once between them.
+__device__ __forceinline__ void permute_slice(const GemmArgs& a, const TileInfo& ti, int q, int lane) {
+    const int nvec = a.perm_nvec, k = a.perm_k;
+    const int v0 = static_cast<int>(static_cast<int64_t>(ti.nb) * nvec / a.n_tiles);
+    const int v1 = static_cast<int>(static_cast<int64_t>(ti.nb + 1) * nvec / a.n_tiles);
+    const uint4* x = static_cast<const uint4*>(a.perm_x);
+    uint4* xp = static_cast<uint4*>(a.perm_out);
+    const int row = q * 32 + lane;  // this lane's row of the tile, for the positions
+    const bool valid = row >= ti.lo && row < ti.hi;
+    int dst[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        dst[j] = (valid && j < k) ? ld_dep(a.perm_rows + static_cast<int64_t>(ti.m0 + row) * k + j) : -1;
+#pragma unroll 1
+    for (int vb = v0; vb < v1; vb += 64) {
+#pragma unroll 1
+        for (int r0 = 0; r0 < 32; r0 += 8) {
+            uint4 buf[8][2];
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = q * 32 + r0 + rr;
+                const bool rv = r >= ti.lo && r < ti.hi;  // the same for every lane
+                const uint4* src = x + static_cast<int64_t>(ti.m0 + r) * nvec;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int v = vb + lane + 32 * h;
+                    if (rv && v < v1) buf[rr][h] = ld_dep(src + v);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int dj = __shfl_sync(0xFFFFFFFFu, dst[j], r0 + rr);
+                    if (dj < 0) continue;
+                    uint4* o = xp + static_cast<int64_t>(dj) * nvec;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int v = vb + lane + 32 * h;
+                        if (v < v1) o[v] = buf[rr][h];
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Router: the thread owns token m0 + row and its E logits (TMEM columns
 // [0, E)).  Group-limited routing keeps the topk_groups groups with the
 // largest maximum logit; top-k runs over the eligible experts in ascending
@@ -859,10 +999,11 @@ __device__ __forceinline__ PairTile decode_pair(const GemmArgs& a, int t, const 
 template <int BN, int EPI>
 __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
                                          int q, int lane, uint8_t* stage, const CUtensorMap* tmOut,
-                                         int& buf) {
+                                         int& buf, const int (&pr)[8]) {
     const int row = q * 32 + lane;
     if (q * 32 < ti.lo || q * 32 + 32 > ti.hi) {
         if constexpr (EPI == kEpiSwiGLU) epi_swiglu(a, ti, taddr, row);
+        else if constexpr (EPI == kEpiCombine) epi_combine<BN>(a, ti, taddr, row, pr);
         else epi_gate<BN>(a, ti, taddr, row);
         return;
     }
@@ -894,6 +1035,15 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
                     const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
                     p[i] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
                 }
+            } else if constexpr (EPI == kEpiCombine) {
+                float sum[32];
+                combine_sum32(a, pr, col0 + c * 64 + half * 32, sum);
+                uint32_t v[32];
+                tmem_ld32(taddr + c * 64 + half * 32, v);
+                tmem_ld_wait();
+                if (cs) scale_cols(v, cs + c * 64 + half * 32);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) p[i] = combine_pack2(sum[2 * i], sum[2 * i + 1], v[2 * i], v[2 * i + 1]);
             } else {
                 uint32_t v[32];
                 tmem_ld32(taddr + c * 64 + half * 32, v);
@@ -1163,12 +1313,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t aph = 0;
         for (int t = cluster; t < total; t += nclusters) {
             const PairTile p = decode_pair(args, t, vpref);
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
-            if (!ok) {
-                timed_out = true;
-                break;
-            }
-            tc_fence_after();
             TileInfo ti;
             ti.e = p.e;
             ti.nb = p.nb;
@@ -1176,16 +1320,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ti.lo = max(0, p.lo - BM * static_cast<int>(rank));
             ti.hi = min(BM, p.hi - BM * static_cast<int>(rank));
             ti.skip = false;
+            int pr[8];
+            if constexpr (EPI == kEpiCombine) {
+                // the token's routed rows, and their BN columns of this tile
+                // fetched into L2 while the tile's MMAs run
+                combine_rows_of(args, ti.m0 + row, row >= ti.lo && row < ti.hi, pr);
+                const __nv_bfloat16* y = static_cast<const __nv_bfloat16*>(args.comb_y);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (pr[j] >= 0)
+                        bulk_prefetch_l2(y + (int64_t)pr[j] * args.comb_ldy + (int64_t)ti.nb * BN, BN * 2);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) pr[j] = -1;
+            }
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(tfull + acc, aph, abort_flag));
+            if (!ok) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            (void)row;
-            epi_pair<BN, EPI>(args, ti, taddr, q, lane, stage, &tmOut, buf);
+            epi_pair<BN, EPI>(args, ti, taddr, q, lane, stage, &tmOut, buf, pr);
             tc_fence_before();
             __syncwarp();
             // relaxed: the accumulator's reads are complete and the MMA warp
             // reads nothing this warp wrote (a release arrive would wait for
             // the tile's stores to land)
             if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(tempty + acc), 0));
+            if constexpr (EPI == kEpiSwiGLU) {
+                if (args.perm_out) permute_slice(args, ti, q, lane);
+            }
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
@@ -1408,6 +1574,9 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
         // the output as a [rows, ldo] bf16 tensor for the staged TMA stores
         CUtensorMap tO;
         if (!make_tmap_box(&tO, args.out, args.out_rows, args.ldo, 64, 32)) return cudaErrorInvalidValue;
+        if (epi == kEpiCombine &&
+            (args.comb_k < 1 || args.comb_k > 8 || !args.comb_y || !args.comb_perm))
+            return cudaErrorInvalidValue;
         if (epi == kEpiSwiGLU && bn == 256)
             return launch_pair_t<256, kEpiSwiGLU, false>(tA, tB, tO, args, max_tiles, stream);
         if (epi == kEpiSwiGLUGather && bn == 256)
@@ -1416,6 +1585,10 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const void* A, int64_t rowsA, c
             return launch_pair_t<256, kEpiGate, false>(tA, tB, tO, args, max_tiles, stream);
         if (epi == kEpiGate && bn == 128)
             return launch_pair_t<128, kEpiGate, false>(tA, tB, tO, args, max_tiles, stream);
+        if (epi == kEpiCombine && bn == 256)
+            return launch_pair_t<256, kEpiCombine, false>(tA, tB, tO, args, max_tiles, stream);
+        if (epi == kEpiCombine && bn == 128)
+            return launch_pair_t<128, kEpiCombine, false>(tA, tB, tO, args, max_tiles, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == kEpiPartial) {

@@ -71,6 +71,22 @@ struct GemmArgs {
     // col_scale[e * b_rows_per_expert + packed row]; null = 1
     const float* col_scale;
     uint32_t* status;               // device error word, may be null
+    // combine epilogue (the shared expert's GEMM2 over token rows): output row
+    // t = sum over j of comb_y[comb_perm[t * comb_k + j]] (fp32, j ascending,
+    // rows < 0 skipped) + the tile's own bf16 result, rounded once to bf16
+    const void* comb_y;             // routed GEMM2 output [rows, comb_ldy] bf16
+    const int32_t* comb_perm;       // [T, comb_k]
+    int32_t comb_k;                 // 1..8
+    int64_t comb_ldy;
+    // permute in the SwiGLU epilogue (the shared expert's GEMM1 over token
+    // rows): after its tile, the epilogue copies columns
+    // [nb * nvec / n_tiles, (nb + 1) * nvec / n_tiles) (16-byte vectors) of
+    // its token rows perm_x[t] to perm_out[perm_rows[t * perm_k + j]], j < perm_k
+    const void* perm_x;             // token rows [T, perm_nvec * 8] bf16
+    const int32_t* perm_rows;       // [T, perm_k]
+    void* perm_out;                 // permuted rows (null: no permute)
+    int32_t perm_k;
+    int32_t perm_nvec;
     // router epilogue
     const float* bias;
     int32_t E, k, n_groups, topk_groups;
@@ -86,7 +102,14 @@ bool router_cluster_fits(int bn, int slices);
 cudaError_t launch_router_cluster(int bn, const void* x, int64_t T, const void* Wg_t, int64_t E,
                                   int64_t K, const GemmArgs& args, int slices, cudaStream_t stream);
 
-enum EpiKind { kEpiSwiGLU = 0, kEpiGate = 1, kEpiRouter = 2, kEpiSwiGLUGather = 3, kEpiPartial = 4 };
+enum EpiKind {
+    kEpiSwiGLU = 0,
+    kEpiGate = 1,
+    kEpiRouter = 2,
+    kEpiSwiGLUGather = 3,
+    kEpiPartial = 4,
+    kEpiCombine = 5
+};
 
 // Launch the tcgen05 grouped GEMM: A [rowsA, K] bf16 (K-major), B
 // [rowsB, K] bf16 (K-major), tile N = bn.  Returns a cudaError_t.

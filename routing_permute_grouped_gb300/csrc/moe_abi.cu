@@ -453,10 +453,25 @@ static moe_status_t do_experts_skinny(const moe_config_t& c, bool fp8, const Ski
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "grouped GEMM2, small-M kernel");
 }
 
-static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
-                              const void* Ws2_t, void* hs, void* ys, uint32_t* status,
-                              cudaStream_t st, void* gus = nullptr, const float* ss13 = nullptr,
-                              const float* ss2 = nullptr) {
+// The permute in the shared expert's GEMM1 epilogue (null x_perm: none).
+struct FusedPermute {
+    const int32_t* perm_row;
+    void* x_perm;
+};
+
+// The routed rows that the shared expert's GEMM2 adds into its output rows
+// when the combine is fused there (null y: no fusion).
+struct FusedCombine {
+    const void* y;
+    const int32_t* perm_row;
+    void* out;
+};
+
+// The shared expert's gate/up GEMM: hs = bf16(silu(x Ws1) * (x Ws3)), 256-row
+// visits of the token rows; with perm, the permute in its epilogue.
+static moe_status_t do_shared_up(const moe_config_t& c, const void* x, const void* Ws13, void* hs,
+                                 uint32_t* status, cudaStream_t st, void* gus = nullptr,
+                                 const float* ss13 = nullptr, const FusedPermute* perm = nullptr) {
     GemmArgs a{};
     a.dense_rows = c.T;
     a.status = status;
@@ -470,20 +485,58 @@ static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* 
     a.gu_out = gus;
     a.ld_gu = 2 * c.d_shared;
     a.col_scale = ss13;
+    if (perm && perm->x_perm) {
+        a.perm_x = x;
+        a.perm_rows = perm->perm_row;
+        a.perm_out = perm->x_perm;
+        a.perm_k = c.k;
+        a.perm_nvec = c.d / 8;
+    }
     const int mblocks = (c.T + 255) / 256;  // 256-row visits of the CTA-pair kernel
     cudaError_t e = launch_grouped_gemm(kEpiSwiGLU, 256, x, c.T, Ws13, 2 * c.d_shared, c.d, a,
                                         mblocks * a.n_tiles, st);
-    if (e != cudaSuccess) return cuda_fail(e, "shared GEMM1");
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "shared GEMM1");
+}
+
+// The shared expert's down projection: ys = bf16(hs Ws2); with comb, the
+// combine in its epilogue writes the layer output instead.
+static moe_status_t do_shared_down(const moe_config_t& c, const void* hs, const void* Ws2_t,
+                                   void* ys, uint32_t* status, cudaStream_t st,
+                                   const float* ss2 = nullptr, const FusedCombine* comb = nullptr) {
+    GemmArgs a{};
+    a.dense_rows = c.T;
+    a.status = status;
+    a.block_rows = 256;
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
-    a.gu_out = nullptr;
     a.col_scale = ss2;
     a.n_tiles = c.d / bn2;
     a.k_blocks = c.d_shared / 64;
+    a.b_rows_per_expert = 0;
     a.out = ys;
     a.ldo = c.d;
-    e = launch_grouped_gemm(kEpiGate, bn2, hs, c.T, Ws2_t, c.d, c.d_shared, a,
-                            mblocks * a.n_tiles, st);
+    a.out_rows = c.T;
+    int epi = kEpiGate;
+    if (comb && comb->y) {
+        // the combine in GEMM2's epilogue: the output rows are the layer's
+        a.out = comb->out;
+        a.comb_y = comb->y;
+        a.comb_perm = comb->perm_row;
+        a.comb_k = c.k;
+        a.comb_ldy = c.d;
+        epi = kEpiCombine;
+    }
+    const int mblocks = (c.T + 255) / 256;
+    cudaError_t e = launch_grouped_gemm(epi, bn2, hs, c.T, Ws2_t, c.d, c.d_shared, a,
+                                        mblocks * a.n_tiles, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "shared GEMM2");
+}
+
+static moe_status_t do_shared(const moe_config_t& c, const void* x, const void* Ws13,
+                              const void* Ws2_t, void* hs, void* ys, uint32_t* status,
+                              cudaStream_t st, void* gus = nullptr, const float* ss13 = nullptr,
+                              const float* ss2 = nullptr) {
+    moe_status_t r = do_shared_up(c, x, Ws13, hs, status, st, gus, ss13);
+    return r != MOE_OK ? r : do_shared_down(c, hs, Ws2_t, ys, status, st, ss2);
 }
 
 // Pointers into a layer workspace.
@@ -560,14 +613,15 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
     const moe_workspace_layout_t& L = B.L;
     r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
     if (r != MOE_OK) return r;
-    cudaError_t e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
-    if (e != cudaSuccess) return cuda_fail(e, "permute");
     const void* shared = c.d_shared ? B.at(L.ys) : nullptr;
     // gate/up values saved for the backward: routed rows, then the shared expert's
     void* gu = gu_save;
     void* gus = gu_save && c.d_shared ? static_cast<uint8_t*>(gu_save) + gate_up_routed_bytes(c)
                                       : nullptr;
+    cudaError_t e = cudaSuccess;
     if (use_skinny(c)) {
+        e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
+        if (e != cudaSuccess) return cuda_fail(e, "permute");
         const SkinnyIO ro{B.at(L.x_perm), nullptr, w->W13, nullptr, w->W2, nullptr,
                           B.at(L.h), nullptr, nullptr, B.at(L.y), gu};
         const SkinnyIO so{x, nullptr, w->Ws13, nullptr, w->Ws2, nullptr,
@@ -576,11 +630,21 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
                               c.d_shared ? &so : nullptr);
         if (r != MOE_OK) return r;
     } else {
+        if (c.d_shared) {
+            // the shared expert's GEMM1 first, with the permute in the slack
+            // of its epilogue; its GEMM2 after the routed GEMMs
+            const FusedPermute fp{B.perm_row(), B.at(L.x_perm)};
+            r = do_shared_up(c, x, w->Ws13, B.at(L.hs), B.status(), st, gus, nullptr, &fp);
+        } else {
+            e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
+            r = e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute");
+        }
+        if (r != MOE_OK) return r;
         r = do_experts(c, B.at(L.x_perm), w->W13, w->W2, B.meta(), B.nb(), B.po(), B.row_gate(),
                        B.at(L.h), B.at(L.y), B.status(), st, nullptr, nullptr, gu);
         if (r != MOE_OK) return r;
         if (c.d_shared) {
-            r = do_shared(c, x, w->Ws13, w->Ws2, B.at(L.hs), B.at(L.ys), B.status(), st, gus);
+            r = do_shared_down(c, B.at(L.hs), w->Ws2, B.at(L.ys), B.status(), st);
             if (r != MOE_OK) return r;
         }
     }
@@ -626,14 +690,19 @@ static moe_status_t layer_fp8(const moe_config_t* cfg, const moe_weights_fp8_t* 
         if (e != cudaSuccess) return cuda_fail(e, "widen e4m3 weights");
         r = layer_front(c, w->Wg_t, w->bias, x, pre_idx, pre_w, B, st);
         if (r != MOE_OK) return r;
-        e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
-        if (e != cudaSuccess) return cuda_fail(e, "permute");
+        if (c.d_shared) {  // as the bf16 layer: the permute in the shared GEMM1's epilogue
+            const FusedPermute fp{B.perm_row(), B.at(L.x_perm)};
+            r = do_shared_up(c, x, Ws13w, B.at(L.hs), B.status(), st, nullptr, w->ss13, &fp);
+            if (r != MOE_OK) return r;
+        } else {
+            e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
+            if (e != cudaSuccess) return cuda_fail(e, "permute");
+        }
         r = do_experts(c, B.at(L.x_perm), W13w, W2w, B.meta(), B.nb(), B.po(), B.row_gate(),
                        B.at(L.h), B.at(L.y), B.status(), st, nullptr, nullptr, nullptr, w->s13, w->s2);
         if (r != MOE_OK) return r;
         if (c.d_shared) {
-            r = do_shared(c, x, Ws13w, Ws2w, B.at(L.hs), B.at(L.ys), B.status(), st, nullptr, w->ss13,
-                          w->ss2);
+            r = do_shared_down(c, B.at(L.hs), Ws2w, B.at(L.ys), B.status(), st, w->ss2);
             if (r != MOE_OK) return r;
         }
         e = launch_combine(B.at(L.y), B.perm_row(), c.d_shared ? B.at(L.ys) : nullptr, out, c.T, c.d,
@@ -1237,6 +1306,44 @@ moe_status_t moe_shared_expert(const moe_config_t* cfg, const void* x, const voi
     if (!x || !Ws13 || !Ws2_t || !hs || !ys) return fail(MOE_ERR_INVALID_ARG, "null pointer");
     if (cfg->T == 0) return MOE_OK;
     return do_shared(*cfg, x, Ws13, Ws2_t, hs, ys, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_shared_expert_up(const moe_config_t* cfg, const void* x, const void* Ws13,
+                                  void* hs, const int32_t* perm_row, void* x_perm,
+                                  uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (!x_perm != !perm_row) return fail(MOE_ERR_INVALID_ARG, "perm_row and x_perm: both or neither");
+    if (cfg->T == 0) return MOE_OK;
+    if (!x || !Ws13 || !hs) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    const FusedPermute fp{perm_row, x_perm};
+    return do_shared_up(*cfg, x, Ws13, hs, status, static_cast<cudaStream_t>(stream), nullptr,
+                        nullptr, &fp);
+}
+
+moe_status_t moe_shared_expert_down(const moe_config_t* cfg, const void* hs, const void* Ws2_t,
+                                    void* ys, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (cfg->T == 0) return MOE_OK;
+    if (!hs || !Ws2_t || !ys) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    return do_shared_down(*cfg, hs, Ws2_t, ys, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_shared_expert_down_combine(const moe_config_t* cfg, const void* hs,
+                                            const void* Ws2_t, const void* y,
+                                            const int32_t* perm_row, void* out, uint32_t* status,
+                                            void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->d_shared <= 0) return fail(MOE_ERR_INVALID_ARG, "d_shared must be > 0");
+    if (cfg->T == 0) return MOE_OK;
+    if (!hs || !Ws2_t || !y || !perm_row || !out) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    const FusedCombine fc{y, perm_row, out};
+    return do_shared_down(*cfg, hs, Ws2_t, nullptr, status, static_cast<cudaStream_t>(stream),
+                          nullptr, &fc);
 }
 
 moe_status_t moe_shared_expert_fp8(const moe_config_t* cfg, const void* xs8, const float* xs_scale,

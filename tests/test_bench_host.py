@@ -22,19 +22,30 @@ def bench():
 
 
 @pytest.mark.parametrize("name, skinny, fp8, expect", [
-    ("default", False, False, 10),     # clustered split-K router 1, offsets 3, permute, 2 + 2 GEMMs,
-                                       # combine
+    ("default", False, False, 9),      # clustered split-K router 1, offsets 3, 2 + 2 GEMMs (the
+                                       # permute in the shared GEMM1's epilogue), combine
     ("decode", True, False, 7),        # split-K router 2 (partials + reduce: E = 256), small offsets
                                        # 1, permute, 2 GEMMs, combine
     ("decode", True, True, 8),         # + the e4m3 pairs of h between the GEMMs
     ("prerouted", False, False, 7),    # no router: offsets 3, permute, 2 GEMMs, combine
-    ("default", False, True, 14),      # + widening routed and shared W13, W2
+    ("default", False, True, 13),      # + widening routed and shared W13, W2
     ("imbalance_x4_p128", False, False, 8),  # fused router 1, offsets 3, permute, 2 GEMMs, combine
     ("tiny", False, False, 7),         # split-K router 2 (8 slices), small offsets 1, permute, 2
                                        # GEMMs, combine
 ])
 def test_forward_launch_counts(bench, name, skinny, fp8, expect):
     assert bench.forward_launches(synth.WORKLOADS[name], skinny, fp8) == expect
+
+
+@pytest.mark.parametrize("permute, combine, expect", [
+    ("layer", "kernel", 9), ("kernel", "kernel", 10), ("gather", "kernel", 9),
+    ("layer", "fused", 8), ("kernel", "fused", 9),
+])
+def test_forward_launch_counts_options(bench, permute, combine, expect):
+    # the default workload's stage-call options: the permute as its own kernel
+    # or inside a GEMM, the combine as its own kernel or in the shared GEMM2
+    assert bench.forward_launches(synth.WORKLOADS["default"], False, False, permute,
+                                  combine) == expect
 
 
 @pytest.mark.parametrize("name, recompute, expect", [

@@ -157,7 +157,14 @@ def test_layer_matches_oracle(name):
     y = f64(layer.buffer("y", torch.bfloat16, (R, d)))
     assert_close(y[valid], ref["y"][valid], "y")
     if shape.d_shared:
-        assert_close(f64(layer.buffer("ys", torch.bfloat16, (T, d))), ref["ys"], "shared ys")
+        ys = layer.buffer("ys", torch.bfloat16, (T, d))
+        assert_close(f64(ys), ref["ys"], "shared ys")
+        # the layer's output is the combine of its own buffers, bit for bit
+        out2 = torch.empty_like(out)
+        moe.moe_combine(cfg, layer.buffer("y", torch.bfloat16, (R, d)),
+                        layer.buffer("perm_row", i32, (A,)), ys, out2)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, out)
     assert_close(f64(out), ref["out"], "out")
 
 
@@ -420,6 +427,60 @@ def test_combine_stage(shared):
     ulp = np.ldexp(1.0, np.frexp(np.abs(expect))[1] - 8)
     assert (np.abs(got - expect) <= ulp).all()
     assert np.mean(got == oracle.round_bf16(expect)) > 0.999
+
+
+@pytest.mark.parametrize("T, d, ds, k, R", [
+    (777, 1024, 384, 4, 3500),   # 3 column slices of 42/43 vectors, ragged last visit
+    (300, 384, 128, 3, 1000),    # one slice; d not a multiple of 256 (128-column GEMM2 tiles)
+    (40, 7168, 128, 2, 100),     # one slice of 896 vectors (several 64-vector passes)
+    (1, 256, 128, 8, 64),        # one token, k = 8
+])
+def test_shared_expert_halves(T, d, ds, k, R):
+    """The shared expert split as the layer runs it, against the stand-alone
+    stage calls, bit for bit: moe_shared_expert_up writes the hs of
+    moe_shared_expert and, with the permute in its epilogue, the x_perm of
+    moe_permute (pad rows untouched); moe_shared_expert_down writes its ys;
+    moe_shared_expert_down_combine writes moe_combine's output of those rows.
+    Some perm_row entries are negative (rows that take no copy and add
+    nothing)."""
+    g = torch.Generator().manual_seed(T * 7 + d)
+    cfg = moe.config_of(T=T, d=d, d_e=128, E=8, k=k, d_shared=ds)
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+    x = cuda(rnd(T, d))
+    Ws13 = torch.empty((1, 2 * ds, d), dtype=torch.bfloat16, device="cuda")
+    Ws2_t = torch.empty((1, d, ds), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(rnd(1, d, ds, std=d ** -0.5)), cuda(rnd(1, d, ds, std=d ** -0.5)),
+                         cuda(rnd(1, ds, d, std=ds ** -0.5)), Ws13, Ws2_t)
+    perm = torch.randperm(R, generator=g)[:T * k].to(torch.int32)
+    perm[::5] = -1
+    perm = cuda(perm)
+    hs = torch.empty((T, ds), dtype=torch.bfloat16, device="cuda")
+    ys = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_shared_expert(cfg, x, Ws13, Ws2_t, hs, ys)
+    xp_ref = cuda(rnd(R, d))
+    xp = xp_ref.clone()
+    moe.moe_permute(cfg, x, perm, xp_ref)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs2 = torch.zeros_like(hs)
+    moe.moe_shared_expert_up(cfg, x, Ws13, hs2, perm, xp, status)
+    ys2 = torch.zeros_like(ys)
+    moe.moe_shared_expert_down(cfg, hs2, Ws2_t, ys2, status)
+    y = cuda(rnd(R, d))
+    expect = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(cfg, y, perm, ys, expect)
+    out = torch.zeros_like(expect)
+    moe.moe_shared_expert_down_combine(cfg, hs2, Ws2_t, y, perm, out, status)
+    hs3 = torch.zeros_like(hs)
+    moe.moe_shared_expert_up(cfg, x, Ws13, hs3, None, None, status)  # no permute
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(hs2, hs) and torch.equal(hs3, hs)
+    assert torch.equal(xp, xp_ref)
+    assert torch.equal(ys2, ys)
+    assert torch.equal(out, expect)
 
 
 def test_host_pipeline_matches_layer():
