@@ -63,8 +63,8 @@ _NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slow
 
 
 class ClockSampler:
-    """SM clock and clock-event reasons of one GPU, read every ``period_s``
-    seconds on a background thread while a region runs.
+    """SM clock, clock-event reasons and board power of one GPU, read every
+    ``period_s`` seconds on a background thread while a region runs.
 
     NVML is read through ctypes (libnvidia-ml ships with the driver); where
     it cannot be loaded, ``nvidia-smi -lms`` is the fallback.  Readings only:
@@ -80,8 +80,9 @@ class ClockSampler:
     def __init__(self, device_index: int, period_s: float = 0.001):
         self.idx = device_index
         self.period = period_s
-        self.samples = []  # (wall time, sm MHz, reason bits)
+        self.samples = []  # (wall time, sm MHz, reason bits, power W or None)
         self.sm_max = None
+        self.power_limit = None
         self.spans = {}
         self._stop = threading.Event()
         self.thread = None
@@ -113,12 +114,15 @@ class ClockSampler:
         mx = ctypes.c_uint()
         if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
             self.sm_max = float(mx.value)
+        if lib.nvmlDeviceGetEnforcedPowerLimit(h, ctypes.byref(mx)) == 0:  # milliwatts
+            self.power_limit = mx.value / 1e3
         return lib, h
 
     def _nvml_loop(self, lib, h):
         import ctypes
 
         mhz = ctypes.c_uint()
+        mw = ctypes.c_uint()
         bits = ctypes.c_ulonglong()
         reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             lib.nvmlDeviceGetCurrentClocksThrottleReasons
@@ -126,7 +130,8 @@ class ClockSampler:
             t = time.time()
             if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
                 r = bits.value if reasons(h, ctypes.byref(bits)) == 0 else 0
-                self.samples.append((t, float(mhz.value), int(r)))
+                w = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
+                self.samples.append((t, float(mhz.value), int(r), w))
             time.sleep(self.period)
 
     # -- nvidia-smi fallback
@@ -144,7 +149,11 @@ class ClockSampler:
             for b, v in zip((0x8, 0x40, 0x20, 0x4), parts[4:8]):
                 if v.lower().startswith("active"):
                     bits |= b
-            self.samples.append((time.time(), sm, bits))
+            try:
+                w = float(parts[2])
+            except ValueError:
+                w = None
+            self.samples.append((time.time(), sm, bits, w))
 
     def start(self):
         nv = None
@@ -184,19 +193,24 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, span: str = None):
-        """Median SM MHz and the reasons seen among the samples inside the
-        span (all samples when span is None)."""
+        """Median SM MHz, the reasons seen and the median and largest board
+        power (W) among the samples inside the span (all samples when span is
+        None), with the enforced power limit."""
         if self.source is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock readings unavailable"]}
         sel = self.samples
         if span is not None and span in self.spans:
             t0, t1 = self.spans[span]
             sel = [x for x in self.samples if t0 <= x[0] <= t1]
-        reasons = sorted({n for _, _, b in sel for bit, n in _NVML_REASONS.items() if b & bit})
+        reasons = sorted({n for x in sel for bit, n in _NVML_REASONS.items() if x[2] & bit})
         sm = [x[1] for x in sel]
+        pw = [x[3] for x in sel if len(x) > 3 and x[3] is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.sm_max,
                 "reasons": reasons, "samples": len(sm), "source": self.source,
-                "period_ms": self.period * 1e3 if self.source == "nvml" else 100.0}
+                "period_ms": self.period * 1e3 if self.source == "nvml" else 100.0,
+                "power_w_median": round(statistics.median(pw), 1) if pw else None,
+                "power_w_max": round(max(pw), 1) if pw else None,
+                "power_limit_w": self.power_limit}
 
 
 def clock_normalised(stage_ms: float, roof: dict, clk):

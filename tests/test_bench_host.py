@@ -69,11 +69,14 @@ def test_clock_windows_and_normalised_rate(bench):
     maximum over the median clock of the region."""
     c = bench.ClockSampler(0)
     c.source, c.period, c.sm_max = "nvml", 0.001, 2070.0
-    c.samples = [(0.5, 2070.0, 0), (1.1, 1800.0, 0x4), (1.2, 1900.0, 0x4), (1.3, 2000.0, 0),
-                 (2.5, 1500.0, 0x8)]
+    c.power_limit = 1400.0
+    c.samples = [(0.5, 2070.0, 0, 300.0), (1.1, 1800.0, 0x4, 1390.0), (1.2, 1900.0, 0x4, 1400.0),
+                 (1.3, 2000.0, 0, None), (2.5, 1500.0, 0x8, 900.0)]
     c.window("timed", 1.0, 1.4)
     s = c.summary("timed")
     assert s["samples"] == 3 and s["sm_mhz"] == 1900.0 and s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_median"] == 1395.0 and s["power_w_max"] == 1400.0
+    assert s["power_limit_w"] == 1400.0
     assert c.summary()["reasons"] == ["hw_slowdown", "sw_power_cap"]
     roof = {"achieved": 1700.0, "peak": 1935.5}
     n = bench.clock_normalised(1.6, roof, s)
