@@ -21,7 +21,9 @@
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma into one
 //               of two TMEM accumulators
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
-//               fused SwiGLU / gate / top-k, stores to global memory
+//               fused SwiGLU / gate / top-k, stores to global memory; on the
+//               shared expert's token-major tiles also the permute (GEMM1,
+//               after the accumulator is handed back) or the combine (GEMM2)
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every wait is bounded; on a timeout the CTA flags the status word,
 // drains what it has in flight and returns.
