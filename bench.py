@@ -1063,19 +1063,45 @@ def run_ep(args, shape, rank, world, local):
     T, k, d, de, ds = shape.T, shape.k, shape.d, shape.d_e, shape.d_shared
     useful = ledger.layer_useful_flops(T, k, d, de, ds)
     value = reduce_sum(useful * args.steps, world) / (ms_max / 1e3) / 1e12
-    # e2e: token rows in from pinned host memory, the output back, every step
+    # e2e: token rows in from pinned host memory, the output back, every
+    # step; the copies run on their own streams with two device buffers, so
+    # that they overlap the neighbouring steps' layers (as HostPipeline does
+    # for the single-GPU layer)
     x_host = x.cpu().pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    xd = torch.empty_like(x)
+    out_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step(i):
+        j = i % 2
+        s_in.wait_event(ev_run[j])  # the buffer's previous layer has read it
+        with torch.cuda.stream(s_in):
+            xd[j].copy_(x_host, non_blocking=True)
+            ev_in[j].record(s_in)
+        cur.wait_event(ev_in[j])
+        o = layer.forward(xd[j], **kw)
+        ev_run[j].record(cur)
+        s_out.wait_event(ev_run[j])
+        with torch.cuda.stream(s_out):
+            out_host[j].copy_(o, non_blocking=True)
+        o.record_stream(s_out)
+
+    for j in range(2):
+        ev_run[j].record(cur)
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record()
-    for _ in range(e2e_steps):
-        xd.copy_(x_host, non_blocking=True)
-        out_host.copy_(layer.forward(xd, **kw), non_blocking=True)
-    e1.record()
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e_val = reduce_sum(useful * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
