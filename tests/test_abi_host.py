@@ -265,3 +265,25 @@ def test_unpadded_entry_points_check_arguments_before_launch(lib):
                                                 fake, fake, None, None) == 1
     assert lib.moe_grouped_gemm_swiglu_unpadded(ctypes.byref(_cfg(d_e=200)), fake, fake, fake,
                                                 fake, fake, fake, fake, None, None) == 2
+
+
+def test_shared_expert_halves_check_arguments_before_launch(lib):
+    """moe_shared_expert_up / _down / _down_combine need a shared expert and
+    their operands; the permute of _up takes perm_row and x_perm both or
+    neither; an empty batch is a no-op."""
+    fake = ctypes.c_void_p(0x1000)
+    cfg, cfg_s = _cfg(), _cfg(d_shared=256)
+    up, down, dc = lib.moe_shared_expert_up, lib.moe_shared_expert_down, \
+        lib.moe_shared_expert_down_combine
+    assert up(ctypes.byref(cfg), fake, fake, fake, None, None, None, None) == 1       # no shared
+    assert up(ctypes.byref(cfg_s), fake, fake, fake, fake, None, None, None) == 1     # perm alone
+    assert up(ctypes.byref(cfg_s), fake, fake, fake, None, fake, None, None) == 1     # x_perm alone
+    assert up(ctypes.byref(cfg_s), None, fake, fake, None, None, None, None) == 1
+    assert down(ctypes.byref(cfg_s), fake, fake, None, None, None) == 1
+    assert down(ctypes.byref(cfg), fake, fake, fake, None, None) == 1
+    assert dc(ctypes.byref(cfg_s), fake, fake, fake, None, fake, None, None) == 1     # no perm_row
+    assert dc(ctypes.byref(cfg_s), fake, fake, fake, fake, None, None, None) == 1     # no out
+    empty = _cfg(d_shared=256, T=0)
+    assert up(ctypes.byref(empty), None, None, None, None, None, None, None) == 0
+    assert down(ctypes.byref(empty), None, None, None, None, None) == 0
+    assert dc(ctypes.byref(empty), None, None, None, None, None, None, None) == 0
