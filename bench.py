@@ -121,6 +121,26 @@ class ClockSampler:
     def _nvml_loop(self, lib, h):
         import ctypes
 
+        class FieldValue(ctypes.Structure):  # nvmlFieldValue_t
+            _fields_ = [("fieldId", ctypes.c_uint), ("scopeId", ctypes.c_uint),
+                        ("timestamp", ctypes.c_longlong), ("latencyUsec", ctypes.c_longlong),
+                        ("valueType", ctypes.c_int), ("nvmlReturn", ctypes.c_int),
+                        ("value", ctypes.c_ulonglong)]
+
+        def power_w():
+            # instantaneous board power (NVML_FI_DEV_POWER_INSTANT, milliwatts);
+            # nvmlDeviceGetPowerUsage, a one-second average on recent GPUs,
+            # where the field is not served
+            fv = FieldValue(fieldId=186)
+            if lib.nvmlDeviceGetFieldValues(h, 1, ctypes.byref(fv)) == 0 and fv.nvmlReturn == 0:
+                if fv.valueType == 0:
+                    return ctypes.cast(ctypes.pointer(ctypes.c_ulonglong(fv.value)),
+                                       ctypes.POINTER(ctypes.c_double))[0] / 1e3
+                if fv.valueType in (1, 5):
+                    return (fv.value & 0xFFFFFFFF) / 1e3
+                return fv.value / 1e3
+            return mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
+
         mhz = ctypes.c_uint()
         mw = ctypes.c_uint()
         bits = ctypes.c_ulonglong()
@@ -130,8 +150,7 @@ class ClockSampler:
             t = time.time()
             if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
                 r = bits.value if reasons(h, ctypes.byref(bits)) == 0 else 0
-                w = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
-                self.samples.append((t, float(mhz.value), int(r), w))
+                self.samples.append((t, float(mhz.value), int(r), power_w()))
             time.sleep(self.period)
 
     # -- nvidia-smi fallback
