@@ -293,9 +293,8 @@ moe_status_t moe_build_offsets(const moe_config_t *cfg, const int32_t *topk_idx,
 
 /* Allocation-free variant of moe_build_offsets (the pages have no
  * counterpart; this exists for callers of this library).  Some callers cannot
- * allocate device memory where they run this stage: work recorded into a
- * CUDA graph may not call allocation routines during stream capture, and some
- * serving runtimes only hand out memory from a pool reserved at start-up.
+ * allocate device memory where they run this stage; some serving runtimes,
+ * for one, only hand out memory from a pool reserved at start-up.
  * This call takes the same inputs and outputs as moe_build_offsets but no
  * scratch: its per-chunk counts live in a 64 KiB array in the library's own
  * device memory, which every GPU that loads the library holds until the
@@ -305,8 +304,8 @@ moe_status_t moe_build_offsets(const moe_config_t *cfg, const int32_t *topk_idx,
  *           NULL to leave bad expert ids unreported
  * Limits: ceil(T*k / 2048) * E * 4 <= 65536 bytes (T*k <= 131072 at E = 256);
  * larger configs return MOE_ERR_WORKSPACE before anything is enqueued.
- * The first call on a device looks up the array's device address (with that
- * device current), so make that first call before any stream capture begins.
+ * The first call on a device looks up the array's device address with a
+ * host-side query (with that device current); later calls reuse it.
  * The address is kept per device and per CUDA context: after the device's
  * context is torn down and made again (cudaDeviceReset), the next call looks
  * it up again and counts as a first call.

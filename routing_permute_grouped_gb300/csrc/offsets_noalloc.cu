@@ -2,10 +2,9 @@
 //
 // moe_build_offsets needs a small device scratch (per-chunk expert counts)
 // that its caller allocates.  Some callers cannot allocate device memory at
-// the point where they run this stage: code that is being recorded into a
-// CUDA graph (allocation calls are not allowed during stream capture), and
-// runtimes that hand out memory only from a pool reserved at start-up and
-// forbid any allocation on the serving path.  This variant keeps its
+// the point where they run this stage, for one runtimes that hand out memory
+// only from a pool reserved at start-up and forbid any allocation on the
+// serving path.  This variant keeps its
 // scratch in a fixed-size array in the library's own device memory instead,
 // so the caller passes inputs and outputs only.
 #include <cuda.h>

@@ -1,8 +1,8 @@
 """The allocation-free offsets entry point (moe_build_offsets_noalloc).
 
 It serves callers that cannot allocate device memory where they build the
-routing tables (work recorded into a CUDA graph, runtimes that only use a pool
-reserved at start-up): its scratch is a fixed array inside the library.  The
+routing tables (runtimes that only use a pool reserved at start-up, for one):
+its scratch is a fixed array inside the library.  The
 GPU test checks, through the C ABI, that two calls in a row give the same
 tables as moe_build_offsets with a caller-allocated scratch; tables are
 integer (and copied gates), so the comparison is exact.  The file is named to
