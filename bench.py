@@ -538,6 +538,9 @@ def run_ours(args, shape, rank, world, local):
     # scaled shared expert after the routed GEMMs.)
     pair_shared = bool(ds) and not skinny and not fp8 and not unpadded
     perm_in_shared = pair_shared and args.permute == "layer"
+    # --permute gemm: the permute in GEMM1's copy warps (stage calls)
+    perm_in_gemm = not skinny and not fp8 and not unpadded and args.permute == "gemm"
+    visit_ready = buf("visit_ready", i32, (NB,))
     stages = []
     if not shape.prerouted:
         # the router the layer runs: split-K for small batches
@@ -555,7 +558,7 @@ def run_ours(args, shape, rank, world, local):
     elif fp8 and not wide:
         stages.append(("permute", lambda: moe.moe_permute_fp8(
             cfg, x, perm_row, x_perm, x_scale, xs8, xs_scale)))
-    elif args.permute != "gather":
+    elif args.permute != "gather" and not perm_in_gemm:
         stages.append(("permute", lambda: moe.moe_permute(cfg, x, perm_row, x_perm)))
 
     def grouped():
@@ -574,6 +577,10 @@ def run_ours(args, shape, rank, world, local):
         elif skinny:
             moe.moe_grouped_gemm_swiglu_skinny(cfg, x_perm, layer.W13, layer.W2_t, meta, nb,
                                                row_gate, h, y, status_word)
+        elif perm_in_gemm:
+            moe.moe_grouped_gemm_swiglu_permute(cfg, x, row_src, x_perm, visit_ready, layer.W13,
+                                                layer.W2_t, meta, nb, po, row_gate, h, y,
+                                                status_word)
         elif args.permute != "gather":
             moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, row_gate,
                                         h, y, status_word)
@@ -803,9 +810,10 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, permute: str = "lay
                      combine: str = "kernel") -> int:
     """Kernels of one layer forward: router (2 when split-K with a scratch:
     partial logits + reduce; 1 fused or clustered), offsets (1 or 3), permute
-    (none when it runs in the shared expert's GEMM1 epilogue, the layer's
-    choice on the CTA-pair kernel with a shared expert, or in GEMM1's A
-    load), 2 routed GEMMs, 2 shared-expert GEMMs (none on the small-M kernel,
+    (none where the layer runs it in the shared expert's GEMM1 epilogue,
+    on the CTA-pair path with a shared expert, nor in GEMM1's A load or its
+    copy warps), 2 routed GEMMs, 2 shared-expert GEMMs (none on the small-M
+    kernel,
     whose launches carry the shared tiles), combine (none when it runs in the
     shared expert's GEMM2 epilogue), and with e4m3 weights the split of h
     between the GEMMs."""
@@ -816,7 +824,9 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, permute: str = "lay
     offsets_launches = 1 if shape.A <= 4096 else 3  # one-CTA offsets kernel for small batches
     widen = (2 + (2 if shape.d_shared else 0)) if fp8 and not skinny else 0
     pair_shared = bool(shape.d_shared) and not skinny
-    permute_kernel = not (permute == "gather" or (pair_shared and permute == "layer"))
+    # on the CTA-pair path with a shared expert the layer's permute rides in
+    # the shared GEMM1's epilogue
+    permute_kernel = skinny or permute == "kernel" or (permute == "layer" and not pair_shared)
     fused_combine = pair_shared and not fp8 and combine == "fused"
     return ((0 if shape.prerouted else (2 if nsplit else 1)) + offsets_launches
             + (1 if permute_kernel else 0) + 2
@@ -1176,10 +1186,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--permute", choices=["layer", "kernel", "gather"], default="layer",
+    ap.add_argument("--permute", choices=["layer", "kernel", "gather", "gemm"], default="layer",
                     help="layer: as moe_layer_fwd (in the shared expert's GEMM1 epilogue when "
                          "there is one on the CTA-pair kernel, else its own kernel); kernel: "
-                         "always its own kernel; gather: fused into GEMM1's A load (stage calls)")
+                         "always its own kernel; gather: fused into GEMM1's A load; gemm: in "
+                         "GEMM1's copy warps (stage calls)")
     ap.add_argument("--combine", choices=["kernel", "fused"], default="kernel",
                     help="kernel: the combine as its own kernel (the layer); fused: in the "
                          "shared expert's GEMM2 epilogue (stage calls)")

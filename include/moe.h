@@ -157,6 +157,8 @@ typedef struct {
     size_t row_scale;      /* fp32 row scales: x [R_max], h [R_max], xs [T], hs [T] */
     size_t w16;            /* e4m3 layer with T*k > 32*E: the expert codes widened to bf16
                             * (routed W13, W2, shared Ws13, Ws2), empty otherwise */
+    size_t visit_ready;    /* int32 [NB_max] scratch for moe_grouped_gemm_swiglu_permute (per-visit
+                            * counts of permuted rows in place); not used by the layer */
 } moe_workspace_layout_t;
 
 /* ---------------------------------------------------------------- sizes -- */
@@ -408,6 +410,32 @@ moe_status_t moe_grouped_gemm_swiglu_fp8(const moe_config_t *cfg, const void *x8
                                          const int32_t *block_metadata, const int32_t *num_blocks,
                                          const float *row_gate, void *h, void *h8, float *h_scale,
                                          void *y, uint32_t *status, void *stream);
+
+/* a3 + a4 + a5 in one pair of launches: the grouped GEMMs of
+ * moe_grouped_gemm_swiglu, with the permute of moe_permute done inside GEMM1
+ * ("MoE & MLA operators", sec. 2.3) by two extra warps of every CTA.  They
+ * copy the token rows into x_perm in padded-row order (the order the visits
+ * are loaded in), a whole row per warp, and count the rows of every 256-row
+ * visit in visit_ready; the CTA pair's TMA producer loads a visit's
+ * rows once its count is complete (acquire, then a generic-to-async proxy
+ * fence).  The copy warps wait on nothing, so the loads always come.  x_perm
+ * ends as moe_permute leaves it (pad rows untouched).  This call clears
+ * visit_ready itself (cudaMemsetAsync on the stream).  Measured no faster
+ * than moe_permute followed by moe_grouped_gemm_swiglu (the copies' bytes
+ * cost the GEMM what the permute kernel costs alone); the layer does not use
+ * it.
+ *   x            bf16 [T, d]       device, read
+ *   row_src      int32 [R_max]     device, read (moe_build_offsets)
+ *   x_perm       bf16 [R_max, d]   device, written
+ *   visit_ready  int32 [NB_max]    device scratch
+ * Other arguments as moe_grouped_gemm_swiglu (the CTA-pair kernel). */
+moe_status_t moe_grouped_gemm_swiglu_permute(const moe_config_t *cfg, const void *x,
+                                             const int32_t *row_src, void *x_perm,
+                                             int32_t *visit_ready, const void *W13,
+                                             const void *W2_t, const int32_t *block_metadata,
+                                             const int32_t *num_blocks,
+                                             const int32_t *padded_offsets, const float *row_gate,
+                                             void *h, void *y, uint32_t *status, void *stream);
 
 /* a3 + a4 + a5 fused: the grouped GEMMs of moe_grouped_gemm_swiglu with the
  * permute folded into GEMM1's A load ("Dropless and grouped GEMM", sec. 4:

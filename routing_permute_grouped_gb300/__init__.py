@@ -27,7 +27,8 @@ __all__ = [
     "moe_check_config", "moe_workspace_size", "moe_workspace_layout", "moe_offsets_workspace_size",
     "moe_pack_router", "moe_pack_experts", "moe_pack_weights", "moe_route", "moe_route_splitk",
     "moe_route_splitk_scratch_size", "moe_build_offsets", "moe_build_offsets_noalloc", "moe_permute",
-    "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather", "moe_shared_expert", "moe_shared_expert_up", "moe_shared_expert_down",
+    "moe_grouped_gemm_swiglu", "moe_grouped_gemm_swiglu_gather",
+    "moe_grouped_gemm_swiglu_permute", "moe_shared_expert", "moe_shared_expert_up", "moe_shared_expert_down",
     "moe_shared_expert_down_combine", "moe_combine", "moe_layer_fwd",
     "moe_layer_fwd_prerouted", "moe_get_device_status", "moe_status_string", "HostPipeline",
     "MoeWeightsFp8", "moe_pack_experts_fp8", "moe_permute_fp8", "moe_grouped_gemm_swiglu_skinny",
@@ -79,7 +80,8 @@ class MoeGrads(ctypes.Structure):
 
 _LAYOUT_FIELDS = ("total", "status", "topk_idx", "topk_w", "counts", "padded_offsets",
                   "block_metadata", "num_blocks", "perm_row", "row_src", "row_gate", "x_perm", "h",
-                  "y", "hs", "ys", "router_partial", "xs8", "h8", "row_scale", "w16")
+                  "y", "hs", "ys", "router_partial", "xs8", "h8", "row_scale", "w16",
+                  "visit_ready")
 
 
 class _Layout(ctypes.Structure):
@@ -121,6 +123,7 @@ def load():
         "moe_permute": (ctypes.c_int, [CP, P, P, P, P]),
         "moe_grouped_gemm_swiglu": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_swiglu_gather": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "moe_grouped_gemm_swiglu_permute": (ctypes.c_int, [CP] + [P] * 14),
         "moe_shared_expert": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
         "moe_shared_expert_up": (ctypes.c_int, [CP, P, P, P, P, P, P, P]),
         "moe_shared_expert_down": (ctypes.c_int, [CP, P, P, P, P, P]),
@@ -306,6 +309,15 @@ def moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, block_metadata, num_blocks, 
         ctypes.byref(cfg), _ptr(x_perm), _ptr(W13), _ptr(W2_t), _ptr(block_metadata),
         _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate), _ptr(h), _ptr(y), _ptr(status),
         _stream(stream)))
+
+
+def moe_grouped_gemm_swiglu_permute(cfg, x, row_src, x_perm, visit_ready, W13, W2_t, block_metadata,
+                                    num_blocks, padded_offsets, row_gate, h, y, status=None,
+                                    stream=None) -> None:
+    _check(load().moe_grouped_gemm_swiglu_permute(
+        ctypes.byref(cfg), _ptr(x), _ptr(row_src), _ptr(x_perm), _ptr(visit_ready), _ptr(W13),
+        _ptr(W2_t), _ptr(block_metadata), _ptr(num_blocks), _ptr(padded_offsets), _ptr(row_gate),
+        _ptr(h), _ptr(y), _ptr(status), _stream(stream)))
 
 
 def moe_grouped_gemm_swiglu_gather(cfg, x, row_src, W13, W2_t, block_metadata, num_blocks,

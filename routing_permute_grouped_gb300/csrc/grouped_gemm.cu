@@ -42,6 +42,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
 constexpr int kOutStageBytes = 4 * 2 * 4096;  // pair-kernel epilogue staging
 constexpr int kThreads = 192;
+constexpr int kPairThreads = 256;  // the pair kernel with its 2 copy warps (6 warps without)
 constexpr uint32_t kDevErrTimeout = 0x2u;
 
 template <int BN>
@@ -1076,7 +1077,7 @@ __device__ __forceinline__ void epi_pair(const GemmArgs& a, const TileInfo& ti, 
 // permute fused into GEMM1's A load) instead of a tile load from the
 // permuted buffer.
 template <int BN, int EPI, bool GATHER>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
@@ -1198,6 +1199,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int wave = 0;
         for (int t = cluster; t < total && !timed_out; t += nclusters, ++wave) {
             const PairTile p = decode_pair(args, t, vpref);
+            if (args.cp_out) {
+                // the visit's A rows are written by the copy warps of every
+                // CTA: load them once all of them are in place
+                bool ready = true;
+                if (lane == 0) {
+                    ready = wait_count(args.cp_ready + t / args.n_tiles, p.hi, abort_flag);
+                    fence_proxy_async_global();
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) {
+                    timed_out = true;
+                    break;
+                }
+            }
             const bool rev = wave & 1;
             const int arow = p.m0 + BM * static_cast<int>(rank);
             const int brow = p.e * args.b_rows_per_expert + p.nb * BN + BH * static_cast<int>(rank);
@@ -1359,6 +1373,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) bulk_wait_all();  // staged stores done before shared memory goes
         if (timed_out) *abort_flag = 1;
+    } else if (args.cp_out) {
+        // --------------------------------------------------- copy warps
+        // The permute ("MoE & MLA operators", sec. 2.3) for GEMM1's A
+        // operand: padded row r <- token row row_src[r] / k, the rows dealt
+        // out over the two copy warps of every CTA in ascending order (the
+        // order the visits are loaded in), a warp per row with 16 vectors in
+        // flight per lane.  After each row the warp publishes it (fence,
+        // then a count per visit).  These warps wait on nothing.
+        const int cw = warp - 6;
+        const int R = ld_dep(args.padded_offsets + args.n_experts);
+        const uint4* xs = static_cast<const uint4*>(args.cp_x);
+        uint4* xd = static_cast<uint4*>(args.cp_out);
+        const int nvec = args.cp_nvec;
+        int e = 0, po0 = 0;
+        int po1 = ld_dep(args.padded_offsets + 1);
+        for (int r = static_cast<int>(blockIdx.x) * 2 + cw; r < R; r += 2 * static_cast<int>(gridDim.x)) {
+            while (r >= po1) {  // the expert of row r (rows ascend)
+                ++e;
+                po0 = po1;
+                po1 = ld_dep(args.padded_offsets + e + 1);
+            }
+            const int src = ld_dep(args.cp_row_src + r);
+            if (src < 0) continue;  // a pad row: read by no stored output
+            const uint4* s = xs + static_cast<int64_t>(src / args.cp_k) * nvec;
+            uint4* d = xd + static_cast<int64_t>(r) * nvec;
+            for (int v0 = lane; v0 < nvec; v0 += 32 * 16) {
+                uint4 b[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (v0 + 32 * u < nvec) b[u] = ld_dep(s + v0 + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (v0 + 32 * u < nvec) d[v0 + 32 * u] = b[u];
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                atomicAdd(args.cp_ready + vpref[e] + (r - po0) / 256, 1);
+            }
+        }
     }
 
     if (timed_out && args.status) atomicOr(args.status, kDevErrTimeout);
@@ -1530,7 +1584,7 @@ cudaError_t launch_router_cluster(int bn, const void* x, int64_t T, const void* 
 template <int BN, int EPI, bool GATHER>
 static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tO,
                                  const GemmArgs& args, int max_visits, cudaStream_t stream) {
-    constexpr int NT = kThreads;
+    constexpr int NT = kPairThreads;
     constexpr int STAGE_BYTES = (BM * BK * 2 + (BN / 2) * BK * 2) * (GATHER ? 1 : 2);
     constexpr int S = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
     constexpr int SMEM = 1024 + S * STAGE_BYTES + kOutStageBytes + 512 + 4 * 260;
@@ -1555,7 +1609,9 @@ static cudaError_t launch_pair_t(const CUtensorMap& tA, const CUtensorMap& tB, c
     int clusters = max_clusters[dev];
     if (max_visits < clusters) clusters = max_visits;
     if (clusters <= 0) return cudaSuccess;
-    return launch_pdl(k_grouped_gemm_pair<BN, EPI, GATHER>, dim3(2 * clusters), dim3(NT), SMEM, stream,
+    // the two copy warps only when GEMM1 does the permute
+    const int nt = args.cp_out ? NT : kThreads;
+    return launch_pdl(k_grouped_gemm_pair<BN, EPI, GATHER>, dim3(2 * clusters), dim3(nt), SMEM, stream,
                       tA, tB, tO, args);
 }
 

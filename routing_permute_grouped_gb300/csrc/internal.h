@@ -87,6 +87,18 @@ struct GemmArgs {
     void* perm_out;                 // permuted rows (null: no permute)
     int32_t perm_k;
     int32_t perm_nvec;
+    // permute by copy warps of the routed GEMM1 (CTA-pair kernel, padded
+    // layout): padded row r of cp_out (GEMM1's A operand) is token row
+    // cp_x[cp_row_src[r] / cp_k] (cp_nvec 16-byte vectors); every copied row
+    // adds 1 to cp_ready[its visit], and the producer loads a visit's rows
+    // once its count reaches the visit's valid rows.  cp_ready must start at
+    // zero.
+    const void* cp_x;
+    const int32_t* cp_row_src;
+    void* cp_out;
+    int32_t* cp_ready;
+    int32_t cp_k;
+    int32_t cp_nvec;
     // router epilogue
     const float* bias;
     int32_t E, k, n_groups, topk_groups;

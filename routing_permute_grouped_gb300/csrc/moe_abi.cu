@@ -177,6 +177,7 @@ static moe_workspace_layout_t layout_of(const moe_config_t& c, bool fp8 = false)
     // CTA-pair GEMMs (routed W13, W2, then shared Ws13, Ws2)
     const bool wide = fp8 && !use_skinny(c);
     L.w16 = take(wide ? (routed_weight_elems(c) + shared_weight_elems(c)) * 2 : 0);
+    L.visit_ready = take(static_cast<size_t>(s.NB) * 4);
     L.total = off;
     return L;
 }
@@ -271,7 +272,8 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
                                const int32_t* po, const float* row_gate, void* h, void* y,
                                uint32_t* status, cudaStream_t st, const void* x = nullptr,
                                const int32_t* row_src = nullptr, void* gu = nullptr,
-                               const float* s13 = nullptr, const float* s2 = nullptr) {
+                               const float* s13 = nullptr, const float* s2 = nullptr,
+                               int32_t* visit_ready = nullptr) {
     const Sizes s = sizes_of(c);
     GemmArgs a{};
     a.block_metadata = meta;
@@ -295,11 +297,22 @@ static moe_status_t do_experts(const moe_config_t& c, const void* x_perm, const 
     a.gather_x = x;
     a.row_src = row_src;
     a.gather_k = c.k;
+    if (visit_ready && !gather) {
+        // the permute by GEMM1's copy warps: x_perm is written in the launch
+        // that reads it (visit_ready cleared by the caller)
+        a.cp_x = x;
+        a.cp_row_src = row_src;
+        a.cp_out = const_cast<void*>(x_perm);
+        a.cp_ready = visit_ready;
+        a.cp_k = c.k;
+        a.cp_nvec = c.d / 8;
+    }
     cudaError_t e = launch_grouped_gemm(gather ? kEpiSwiGLUGather : kEpiSwiGLU, 256,
                                         gather ? x : x_perm, gather ? c.T : s.R, W13,
                                         static_cast<int64_t>(c.E) * 2 * c.d_e, c.d, a,
                                         static_cast<int>(s.NB * a.n_tiles), st);
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 (gate/up + SwiGLU)");
+    a.cp_out = nullptr;
     // GEMM2: N = d, K = d_e
     const int bn2 = (c.d % 256 == 0) ? 256 : 128;
     a.gu_out = nullptr;
@@ -636,6 +649,8 @@ static moe_status_t layer(const moe_config_t* cfg, const moe_weights_t* w, const
             const FusedPermute fp{B.perm_row(), B.at(L.x_perm)};
             r = do_shared_up(c, x, w->Ws13, B.at(L.hs), B.status(), st, gus, nullptr, &fp);
         } else {
+            // the permute as its own kernel (in GEMM1's copy warps it was no
+            // faster: moe_grouped_gemm_swiglu_permute)
             e = launch_permute(x, B.perm_row(), B.at(L.x_perm), c.T, c.d, c.k, st);
             r = e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute");
         }
@@ -1113,6 +1128,26 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_config_t* cfg, const void* x_perm
     if (cfg->T == 0) return MOE_OK;
     return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
                       h, y, status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_gemm_swiglu_permute(const moe_config_t* cfg, const void* x,
+                                             const int32_t* row_src, void* x_perm,
+                                             int32_t* visit_ready, const void* W13,
+                                             const void* W2_t, const int32_t* block_metadata,
+                                             const int32_t* num_blocks,
+                                             const int32_t* padded_offsets, const float* row_gate,
+                                             void* h, void* y, uint32_t* status, void* stream) {
+    moe_status_t r = check_cfg(cfg, false);
+    if (r != MOE_OK) return r;
+    if (cfg->T == 0) return MOE_OK;
+    if (!x || !row_src || !x_perm || !visit_ready || !W13 || !W2_t || !block_metadata ||
+        !num_blocks || !padded_offsets || !h || !y)
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(visit_ready, 0, static_cast<size_t>(sizes_of(*cfg).NB) * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing visit_ready");
+    return do_experts(*cfg, x_perm, W13, W2_t, block_metadata, num_blocks, padded_offsets, row_gate,
+                      h, y, status, st, x, row_src, nullptr, nullptr, nullptr, visit_ready);
 }
 
 moe_status_t moe_gather_rows(const void* src, const int32_t* idx, void* dst, int64_t n, int32_t d,

@@ -91,6 +91,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// Acquire load of a counter that threads of other CTAs raise (each after a
+// fence that publishes the data the count stands for).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded wait until *p >= target; false once the limit passes or *abort is
+// set.
+__device__ __forceinline__ bool wait_count(const int* p, int target, const volatile uint32_t* abort,
+                                           uint64_t limit_ns = kWaitLimitNs) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+// Orders this thread's earlier generic-proxy accesses of global memory (the
+// acquire above) before its later async-proxy ones (TMA loads).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");

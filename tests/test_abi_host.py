@@ -287,3 +287,21 @@ def test_shared_expert_halves_check_arguments_before_launch(lib):
     assert up(ctypes.byref(empty), None, None, None, None, None, None, None) == 0
     assert down(ctypes.byref(empty), None, None, None, None, None) == 0
     assert dc(ctypes.byref(empty), None, None, None, None, None, None, None) == 0
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every entry point the binding declares to ctypes takes as many
+    arguments as include/moe.h gives it (a mismatch would only show at the
+    first call on a GPU)."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    decls = dict(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src))
+    checked = 0
+    for name, params in decls.items():
+        argtypes = getattr(getattr(lib, name), "argtypes", None)
+        if argtypes is None:
+            continue
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(argtypes) == n, f"{name}: {len(argtypes)} argtypes, {n} parameters in the header"
+        checked += 1
+    assert checked >= 40

@@ -38,7 +38,7 @@ def test_forward_launch_counts(bench, name, skinny, fp8, expect):
 
 
 @pytest.mark.parametrize("permute, combine, expect", [
-    ("layer", "kernel", 9), ("kernel", "kernel", 10), ("gather", "kernel", 9),
+    ("layer", "kernel", 9), ("kernel", "kernel", 10), ("gather", "kernel", 9), ("gemm", "kernel", 9),
     ("layer", "fused", 8), ("kernel", "fused", 9),
 ])
 def test_forward_launch_counts_options(bench, permute, combine, expect):

@@ -393,6 +393,45 @@ def test_grouped_gemm_stage(name):
     assert (f64(y)[~valid] == 0).all() and (f64(h)[~valid] == 0).all()
 
 
+@pytest.mark.parametrize("name", ["tiny", "small_default", "small_imbalance_p64", "small_e100_d384",
+                                  "small_prerouted"])
+def test_grouped_gemm_permute_stage(name):
+    """The grouped GEMMs with the permute done by GEMM1's copy warps: x_perm
+    equals the oracle's permute on every valid row and keeps its pad rows,
+    and h and y equal the stand-alone grouped GEMMs' on that x_perm, bit for
+    bit; the call clears a stale visit_ready itself."""
+    shape, inp, ref = prepared(name)
+    cfg = moe.config_of(shape)
+    E, d, de, R, NB = shape.E, shape.d, shape.d_e, shape.rows_capacity, shape.blocks_capacity
+    W13 = torch.empty((E, 2 * de, d), dtype=torch.bfloat16, device="cuda")
+    W2_t = torch.empty((E, d, de), dtype=torch.bfloat16, device="cuda")
+    moe.moe_pack_experts(cuda(inp["W1"]), cuda(inp["W3"]), cuda(inp["W2"]), W13, W2_t)
+    meta = cuda(torch.from_numpy(np.resize(ref["block_metadata"], (NB, 3)).astype(np.int32)))
+    nb = cuda(torch.tensor([ref["num_blocks"]], dtype=torch.int32))
+    po = cuda(torch.from_numpy(ref["padded_offsets"]))
+    gate = cuda(torch.from_numpy(ref["row_gate"].astype(np.float32)))
+    row_src = cuda(torch.from_numpy(ref["row_src"]))
+    g = torch.Generator().manual_seed(11)
+    fill = torch.randn((R, d), generator=g).to(torch.bfloat16).cuda()
+    x_perm = fill.clone()
+    ready = torch.full((NB,), 12345, dtype=torch.int32, device="cuda")
+    h = torch.zeros((R, de), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_grouped_gemm_swiglu_permute(cfg, cuda(inp["x"]), row_src, x_perm, ready, W13, W2_t,
+                                        meta, nb, po, gate, h, y, status)
+    h0 = torch.zeros_like(h)
+    y0 = torch.zeros_like(y)
+    moe.moe_grouped_gemm_swiglu(cfg, x_perm, W13, W2_t, meta, nb, po, gate, h0, y0, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    valid = ref["row_src"] >= 0
+    xp = bits(x_perm.cpu())
+    assert np.array_equal(xp[valid], ref["x_perm"][valid])
+    assert torch.equal(x_perm[torch.from_numpy(~valid).cuda()], fill[torch.from_numpy(~valid).cuda()])
+    assert torch.equal(h, h0) and torch.equal(y, y0)
+
+
 @pytest.mark.parametrize("name", ["small_default", "small_decode"])
 def test_shared_expert_stage(name):
     shape, inp, ref = prepared(name)
