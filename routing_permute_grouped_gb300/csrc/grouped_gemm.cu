@@ -24,6 +24,9 @@
 //               fused SwiGLU / gate / top-k, stores to global memory; on the
 //               shared expert's token-major tiles also the permute (GEMM1,
 //               after the accumulator is handed back) or the combine (GEMM2)
+//   warps 6..7  (pair kernel, launched only when GEMM1 does the permute)
+//               copy the token rows into the permuted layout ahead of the
+//               TMA producer, which waits on per-visit counts
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every wait is bounded; on a timeout the CTA flags the status word,
 // drains what it has in flight and returns.
