@@ -168,6 +168,67 @@ def test_layer_matches_oracle(name):
     assert_close(f64(out), ref["out"], "out")
 
 
+@pytest.mark.parametrize("name, permute", [
+    ("small_default", "kernel"), ("small_default", "gemm"),
+    ("small_prerouted", "kernel"), ("small_prerouted", "gemm"),
+    ("small_imbalance_p64", "gemm"),
+])
+def test_layer_equals_its_stages(name, permute):
+    """moe_layer_fwd (on the CTA-pair path: the permute in the shared GEMM1's
+    epilogue with a shared expert, its own kernel without) equals the stage
+    calls composed by hand, bit for bit: router, offsets, then the permute as
+    its own kernel or in GEMM1's copy warps, the grouped GEMMs, the shared
+    expert's two halves and the combine.  The arithmetic is the same
+    whichever kernel moves the rows."""
+    shape, inp, _ = prepared(name)
+    cfg, layer = make_layer(shape, inp)
+    x = cuda(inp["x"])
+    kw = dict(topk_idx=cuda(inp["topk_idx"]), topk_w=cuda(inp["topk_w"])) if shape.prerouted else {}
+    out = layer(x, **kw).clone()
+    T, k, E, d, de, ds = shape.T, shape.k, shape.E, shape.d, shape.d_e, shape.d_shared
+    A, R, NB = shape.A, shape.rows_capacity, shape.blocks_capacity
+    dev = dict(device="cuda")
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    if shape.prerouted:
+        idx, w = kw["topk_idx"], kw["topk_w"]
+    else:
+        idx = torch.empty((T, k), dtype=i32, **dev)
+        w = torch.empty((T, k), dtype=f32, **dev)
+        n = moe.moe_route_splitk_scratch_size(cfg)
+        part = torch.empty(max(n // 4, 1), dtype=f32, **dev) if n else None
+        moe.moe_route_splitk(cfg, x, layer.Wg_t, layer.bias, idx, w, part)
+    counts = torch.empty(E, dtype=i32, **dev)
+    po = torch.empty(E + 1, dtype=i32, **dev)
+    meta = torch.empty((NB, 3), dtype=i32, **dev)
+    nb = torch.empty(1, dtype=i32, **dev)
+    perm = torch.empty(A, dtype=i32, **dev)
+    row_src = torch.empty(R, dtype=i32, **dev)
+    gate = torch.empty(R, dtype=f32, **dev)
+    ws = torch.empty(moe.moe_offsets_workspace_size(cfg), dtype=torch.uint8, **dev)
+    moe.moe_build_offsets(cfg, idx, w, counts, po, meta, nb, perm, row_src, gate, ws)
+    x_perm = torch.zeros((R, d), dtype=bf, **dev)
+    h = torch.zeros((R, de), dtype=bf, **dev)
+    y = torch.zeros((R, d), dtype=bf, **dev)
+    if permute == "kernel":
+        moe.moe_permute(cfg, x, perm, x_perm)
+        moe.moe_grouped_gemm_swiglu(cfg, x_perm, layer.W13, layer.W2_t, meta, nb, po, gate, h, y)
+    else:
+        ready = torch.empty(NB, dtype=i32, **dev)
+        moe.moe_grouped_gemm_swiglu_permute(cfg, x, row_src, x_perm, ready, layer.W13,
+                                            layer.W2_t, meta, nb, po, gate, h, y)
+    ys = None
+    if ds:
+        hs = torch.empty((T, ds), dtype=bf, **dev)
+        ys = torch.empty((T, d), dtype=bf, **dev)
+        moe.moe_shared_expert_up(cfg, x, layer.Ws13, hs)
+        moe.moe_shared_expert_down(cfg, hs, layer.Ws2_t, ys)
+    out2 = torch.empty_like(out)
+    moe.moe_combine(cfg, y, perm, ys, out2)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert torch.equal(out2, out)
+
+
 def test_layer_is_deterministic():
     shape, inp, _ = prepared("small_default")
     cfg, layer = make_layer(shape, inp)
