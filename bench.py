@@ -640,8 +640,31 @@ def run_ours(args, shape, rank, world, local):
         layer_step()
         step()
     torch.cuda.synchronize()
+    timed_step = layer_step
+    if args.graph:
+        # the whole-layer call recorded once into a CUDA graph (the layer only
+        # enqueues kernels: no host sync, no allocation); each timed step
+        # replays it, so the host issues one launch per step instead of one
+        # per kernel
+        if not (args.permute == "layer" and args.combine == "kernel" and not unpadded):
+            raise SystemExit("--graph records the whole-layer call: default --permute, "
+                             "--combine and --schedule only")
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            layer_step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer_step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        timed_step = graph.replay
     # timed region: K whole-layer forwards (moe_layer_fwd: every stage on the
-    # calling stream), bracketed by CUDA events on that stream
+    # calling stream, or the replay of its graph), bracketed by CUDA events on
+    # that stream
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -653,7 +676,7 @@ def run_ours(args, shape, rank, world, local):
     w0 = time.time()
     t_start.record()
     for i in range(args.steps):
-        layer_step()
+        timed_step()
     t_end.record()
     torch.cuda.synchronize()
     w1 = time.time()
@@ -761,8 +784,10 @@ def run_ours(args, shape, rank, world, local):
         "dtype": ("e4m3 (weights, widened to bf16 for the MMAs; per-channel scales on the fp32 "
                   "accumulators)" if wide else
                   "e4m3 (weights; activations as e4m3 pairs), fp32 accumulate" if fp8 else "bf16"),
-        "data": "synthetic", "config": config_dict(shape, args.permute, args.weights, args.schedule,
-                                                     args.combine),
+        "data": "synthetic", "config": dict(config_dict(shape, args.permute, args.weights,
+                                                          args.schedule, args.combine),
+                                              **({"timed_call": "CUDA graph replay of the layer"}
+                                                 if args.graph else {})),
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "clocks": e2e_clocks},
@@ -1205,10 +1230,14 @@ def main():
                     help="padded: segments padded to the block multiple (the layer); unpadded: "
                          "no padding, windows cut by an expert boundary visited once per "
                          "expert (stage calls)")
+    ap.add_argument("--graph", action="store_true",
+                    help="fwd: time replays of one CUDA graph of the whole-layer call")
     ap.add_argument("--keep-gate-up", action="store_true",
                     help="train: the forward saves the gate/up values, the backward skips "
                          "recomputing them")
     args = ap.parse_args()
+    if args.graph and (args.impl != "ours" or args.parallel != "replicas" or args.pass_ != "fwd"):
+        ap.error("--graph applies to the forward of our layer on replicas")
     rank, world, local = dist_setup(args.gpus)
     shape = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -83,3 +83,18 @@ def test_clock_windows_and_normalised_rate(bench):
     assert abs(n["stage_ms_x_mhz"] - 1.6 * 1900.0) < 1e-9
     assert abs(n["achieved_at_max_clock"] - 1700.0 * 2070.0 / 1900.0) < 1e-9
     assert bench.clock_normalised(1.6, roof, {"sm_mhz": None}) is None
+
+
+@pytest.mark.parametrize("extra", [["--pass", "train"], ["--parallel", "ep"],
+                                   ["--impl", "reference"]])
+def test_graph_option_is_for_the_forward_only(extra):
+    """--graph records the whole-layer forward; with another pass, the
+    expert-parallel layer or the reference arm the argument parser refuses it
+    before any device work."""
+    import os
+    import subprocess
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--graph", *extra],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 2 and "--graph" in r.stderr
