@@ -834,7 +834,7 @@ def run_ours(args, shape, rank, world, local):
 def forward_launches(shape, skinny: bool, fp8: bool = False, permute: str = "layer",
                      combine: str = "kernel") -> int:
     """Kernels of one layer forward: router (2 when split-K with a scratch:
-    partial logits + reduce; 1 fused or clustered), offsets (1 or 3), permute
+    partial logits + reduce; 1 fused or clustered), offsets (1 to 3), permute
     (none where the layer runs it in the shared expert's GEMM1 epilogue,
     on the CTA-pair path with a shared expert, nor in GEMM1's A load or its
     copy warps), 2 routed GEMMs, 2 shared-expert GEMMs (none on the small-M
@@ -846,7 +846,11 @@ def forward_launches(shape, skinny: bool, fp8: bool = False, permute: str = "lay
 
     cfg = moe.config_of(shape)
     nsplit = moe.moe_route_splitk_scratch_size(cfg) // 4 if not shape.prerouted else 0
-    offsets_launches = 1 if shape.A <= 4096 else 3  # one-CTA offsets kernel for small batches
+    # one-CTA offsets kernel for small batches; else the chunk histograms and
+    # the scatter (with the scan inside it while chunks x experts <= 8192),
+    # or histograms, scan and scatter
+    n_chunks = (shape.A + 2047) // 2048
+    offsets_launches = 1 if shape.A <= 4096 else (2 if n_chunks * shape.E <= 8192 else 3)
     widen = (2 + (2 if shape.d_shared else 0)) if fp8 and not skinny else 0
     pair_shared = bool(shape.d_shared) and not skinny
     # on the CTA-pair path with a shared expert the layer's permute rides in

@@ -2,7 +2,7 @@
 // built entirely on the device (no host round trip of the per-expert sizes:
 // "Dropless and grouped GEMM", sec. 5 and 7).
 //
-// Three launches over fixed-size chunks of the A = T*k assignments:
+// Up to three launches over fixed-size chunks of the A = T*k assignments:
 //   k_chunk_hist     per-chunk expert histograms (shared-memory counters)
 //   k_scan           one CTA: per-expert totals, ceil(c/P)*P sizes, exclusive
 //                    prefix sums (padded_offsets, block starts), the block
@@ -12,6 +12,9 @@
 //   k_chunk_scatter  stable ranks inside each chunk (warp match + ballot
 //                    prefix, then a prefix over the warps of the CTA) ->
 //                    perm_row, row_src, row_gate
+// When the chunk histograms are small (chunks x experts <= 8192) the scan
+// runs inside the scatter launch instead (k_scan_scatter): each CTA sums
+// the histogram entries it needs, and CTA 0 writes the tables.
 // Ranks depend only on the assignment order, never on atomic ordering, so the
 // permutation is deterministic and rows of a segment stay in ascending
 // assignment order.  Batches of at most 4096 assignments run all three steps
@@ -185,21 +188,15 @@ __global__ void __launch_bounds__(kScanThreads)
     }
 }
 
-__global__ void __launch_bounds__(kScatterThreads)
-    k_chunk_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int E,
-                    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_row,
-                    int32_t* __restrict__ row_src, float* __restrict__ row_gate) {
-    pdl_trigger();
-    pdl_wait();
-    constexpr int W = kScatterThreads / 32;
-    __shared__ int running[kMaxE];
-    __shared__ int wcnt[W][kMaxE];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        running[e] = chunk_base[(int64_t)blockIdx.x * E + e];
-#pragma unroll
-        for (int i = 0; i < W; ++i) wcnt[i][e] = 0;
-    }
-    __syncthreads();
+// Stable ranks of the assignments of this CTA's chunk (blockIdx.x) inside
+// their segments, from running[e] = the chunk's first row in segment e:
+// writes perm_row, row_src and row_gate.  wcnt must start at zero.
+__device__ __forceinline__ void scatter_chunk(const int32_t* __restrict__ idx,
+                                              const float* __restrict__ w, int64_t A, int E,
+                                              int* running, int (*wcnt)[kMaxE],
+                                              int32_t* __restrict__ perm_row,
+                                              int32_t* __restrict__ row_src,
+                                              float* __restrict__ row_gate) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
     const int64_t a0 = (int64_t)blockIdx.x * kChunk;
@@ -234,6 +231,122 @@ __global__ void __launch_bounds__(kScatterThreads)
         }
         __syncthreads();
     }
+}
+
+__global__ void __launch_bounds__(kScatterThreads)
+    k_chunk_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A, int E,
+                    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_row,
+                    int32_t* __restrict__ row_src, float* __restrict__ row_gate) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int W = kScatterThreads / 32;
+    __shared__ int running[kMaxE];
+    __shared__ int wcnt[W][kMaxE];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        running[e] = chunk_base[(int64_t)blockIdx.x * E + e];
+#pragma unroll
+        for (int i = 0; i < W; ++i) wcnt[i][e] = 0;
+    }
+    __syncthreads();
+    scatter_chunk(idx, w, A, E, running, wcnt, perm_row, row_src, row_gate);
+}
+
+// The scan and the scatter in one launch, for up to kScanStaged chunk
+// counts.  Every CTA derives what it needs from the chunk histograms itself
+// (the expert totals, and its own chunk's first row in every segment), so
+// no CTA waits for another.  CTA 0 also writes the tables k_scan writes:
+// counts, padded offsets, the block table, the block count and the pad-row
+// markers.  The results are those of k_scan + k_chunk_scatter.
+__global__ void __launch_bounds__(kScatterThreads)
+    k_scan_scatter(const int32_t* __restrict__ idx, const float* __restrict__ w, int64_t A,
+                   int n_chunks, int E, int P, int64_t R_max,
+                   const int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
+                   int32_t* __restrict__ padded_offsets, int32_t* __restrict__ block_metadata,
+                   int32_t* __restrict__ num_blocks, int32_t* __restrict__ perm_row,
+                   int32_t* __restrict__ row_src, float* __restrict__ row_gate) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int W = kScatterThreads / 32;
+    __shared__ int s_cnt[kMaxE];
+    __shared__ int s_pre[kMaxE];
+    __shared__ int s_size[kMaxE];
+    __shared__ int s_nblk[kMaxE];
+    __shared__ int running[kMaxE];
+    __shared__ int wcnt[W][kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int me = blockIdx.x;
+    // a warp per expert, its lanes over the chunks: the expert's total and
+    // the counts of the chunks before this one
+    for (int ex = warp; ex < E; ex += W) {
+        int tot = 0, pre = 0;
+        for (int c = lane; c < n_chunks; c += 32) {
+            const int v = ld_dep(chunk_counts + (int64_t)c * E + ex);
+            tot += v;
+            if (c < me) pre += v;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+            pre += __shfl_xor_sync(0xFFFFFFFFu, pre, o);
+        }
+        if (lane == 0) {
+            s_cnt[ex] = tot;
+            s_pre[ex] = pre;
+        }
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+#pragma unroll
+        for (int i = 0; i < W; ++i) wcnt[i][e] = 0;
+    __syncthreads();
+    const int e = threadIdx.x;
+    const int cnt = e < E ? s_cnt[e] : 0;
+    const int size = ((cnt + P - 1) / P) * P;  // ceil(c/P)*P, 0 for an empty expert
+    const int nblk = (cnt + P - 1) / P;
+    if (e < E) {
+        s_size[e] = size;
+        s_nblk[e] = nblk;
+    }
+    __syncthreads();
+    // inclusive Hillis-Steele scans of sizes and block counts over E <= 256
+    for (int off = 1; off < E; off <<= 1) {
+        int vs = 0, vb = 0;
+        if (e < E && e >= off) {
+            vs = s_size[e - off];
+            vb = s_nblk[e - off];
+        }
+        __syncthreads();
+        if (e < E && e >= off) {
+            s_size[e] += vs;
+            s_nblk[e] += vb;
+        }
+        __syncthreads();
+    }
+    if (e < E) {
+        const int po = s_size[e] - size;  // exclusive
+        running[e] = po + s_pre[e];
+        if (me == 0) {
+            const int b0 = s_nblk[e] - nblk;  // exclusive
+            counts[e] = cnt;
+            padded_offsets[e] = po;
+            if (e == E - 1) padded_offsets[E] = s_size[e];
+            if (block_metadata)  // null: the unpadded layout, which has no block table
+                for (int i = 0; i < nblk; ++i) {
+                    block_metadata[3 * (b0 + i) + 0] = e;
+                    block_metadata[3 * (b0 + i) + 1] = po + i * P;
+                    block_metadata[3 * (b0 + i) + 2] = min(P, cnt - i * P);
+                }
+        }
+    }
+    if (me == 0 && e == 0 && num_blocks) *num_blocks = s_nblk[E - 1];
+    __syncthreads();
+    if (me == 0) {
+        fill_pad_rows(s_size, s_cnt, E, P, row_src, row_gate);
+        for (int64_t r = s_size[E - 1] + threadIdx.x; r < R_max; r += blockDim.x) {
+            row_src[r] = -1;
+            row_gate[r] = 0.0f;
+        }
+    }
+    scatter_chunk(idx, w, A, E, running, wcnt, perm_row, row_src, row_gate);
 }
 
 // Small batches (A <= kSmallA): the three steps above in one CTA of 1024
@@ -453,6 +566,14 @@ cudaError_t launch_offsets(const int32_t* topk_idx, const float* topk_w, int64_t
         cudaError_t e = launch_pdl(k_chunk_hist, dim3(n_chunks), dim3(kScatterThreads), 0, stream,
                                    topk_idx, A, E, chunk_scratch, status);
         if (e != cudaSuccess) return e;
+    }
+    if (n_chunks > 0 && static_cast<int64_t>(n_chunks) * E <= kScanStaged) {
+        cudaError_t e = launch_pdl(k_scan_scatter, dim3(n_chunks), dim3(kScatterThreads), 0, stream,
+                                   topk_idx, topk_w, A, n_chunks, E, P, R_max,
+                                   static_cast<const int32_t*>(chunk_scratch), counts,
+                                   padded_offsets, block_metadata, num_blocks, perm_row, row_src,
+                                   row_gate);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     const size_t scan_smem = static_cast<int64_t>(n_chunks) * E <= kScanStaged
                                  ? static_cast<size_t>(n_chunks) * E * 4 : 0;

@@ -22,14 +22,16 @@ def bench():
 
 
 @pytest.mark.parametrize("name, skinny, fp8, expect", [
-    ("default", False, False, 9),      # clustered split-K router 1, offsets 3, 2 + 2 GEMMs (the
-                                       # permute in the shared GEMM1's epilogue), combine
+    ("default", False, False, 8),      # clustered split-K router 1, offsets 2 (histograms; scan
+                                       # and scatter), 2 + 2 GEMMs (the permute in the shared
+                                       # GEMM1's epilogue), combine
     ("decode", True, False, 7),        # split-K router 2 (partials + reduce: E = 256), small offsets
                                        # 1, permute, 2 GEMMs, combine
     ("decode", True, True, 8),         # + the e4m3 pairs of h between the GEMMs
-    ("prerouted", False, False, 7),    # no router: offsets 3, permute, 2 GEMMs, combine
-    ("default", False, True, 13),      # + widening routed and shared W13, W2
-    ("imbalance_x4_p128", False, False, 8),  # fused router 1, offsets 3, permute, 2 GEMMs, combine
+    ("prerouted", False, False, 6),    # no router: offsets 2, permute, 2 GEMMs, combine
+    ("default", False, True, 12),      # + widening routed and shared W13, W2
+    ("imbalance_x4_p128", False, False, 7),  # fused router 1, offsets 2 (48 chunks x 64 experts),
+                                             # permute, 2 GEMMs, combine
     ("tiny", False, False, 7),         # split-K router 2 (8 slices), small offsets 1, permute, 2
                                        # GEMMs, combine
 ])
@@ -37,9 +39,18 @@ def test_forward_launch_counts(bench, name, skinny, fp8, expect):
     assert bench.forward_launches(synth.WORKLOADS[name], skinny, fp8) == expect
 
 
+def test_forward_launch_counts_with_large_chunk_tables(bench):
+    # chunks x experts above 8192 (256 chunks of 2048 assignments x 256
+    # experts): histograms, scan and scatter as three launches
+    from routing_permute_grouped_gb300.synth import MoeShape
+
+    s = MoeShape("big_table", T=65536, d=512, d_e=128, E=256, k=8)
+    assert bench.forward_launches(s, False, False) == 1 + 3 + 1 + 2 + 1
+
+
 @pytest.mark.parametrize("permute, combine, expect", [
-    ("layer", "kernel", 9), ("kernel", "kernel", 10), ("gather", "kernel", 9), ("gemm", "kernel", 9),
-    ("layer", "fused", 8), ("kernel", "fused", 9),
+    ("layer", "kernel", 8), ("kernel", "kernel", 9), ("gather", "kernel", 8), ("gemm", "kernel", 8),
+    ("layer", "fused", 7), ("kernel", "fused", 8),
 ])
 def test_forward_launch_counts_options(bench, permute, combine, expect):
     # the default workload's stage-call options: the permute as its own kernel

@@ -359,8 +359,12 @@ def _offsets_case(idx, w, E, P):
 
 
 @pytest.mark.parametrize("P", [64, 128])
-@pytest.mark.parametrize("case", ["uniform", "skewed_empty", "one_expert", "worked_example", "exact_blocks"])
+@pytest.mark.parametrize("case", ["uniform", "skewed_empty", "one_expert", "worked_example", "exact_blocks",
+                                  "large_table"])
 def test_build_offsets_stage(P, case):
+    # A <= 4096 takes the one-CTA kernel; above it, chunk tables of at most
+    # 8192 entries (chunks x experts) the histogram + scan-and-scatter pair,
+    # larger ones (large_table: 36 chunks x 256 experts) three launches
     rng = np.random.default_rng(hash(case) % 1000 + P)
     if case == "uniform":
         E, T, k = 8, 4097, 4  # several chunks, ragged tail
@@ -378,6 +382,10 @@ def test_build_offsets_stage(P, case):
         lab = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(sizes)])
         idx = lab[rng.permutation(lab.size)].reshape(8192, 8)
         E = 4
+    elif case == "large_table":
+        E, T, k = 256, 9000, 8
+        p = rng.dirichlet(np.full(E, 0.1))
+        idx = rng.choice(E, size=(T, k), p=p).astype(np.int32)
     else:
         E, T, k = 4, 128, 4  # 128 rows per expert: one exact block each at P=128
         idx = np.repeat(np.arange(4, dtype=np.int32)[None, :], T, 0)
