@@ -10,9 +10,10 @@
 //          the fixed order j = 0..k-1 then shared, and writes one bf16 row
 //          (sec. 6.4: fixed summation order, wide accumulation, no atomics).
 //          Bytes per token: (k + 1 [+1]) * d * 2.
-// Few tokens (decode): the rows are also split into column chunks over
-// grid.y, so that the grid still covers the SMs (8 tokens per CTA would
-// otherwise leave a 64-token batch on 8 of them).
+// The rows are also split into column chunks over grid.y: for few tokens
+// (decode) so that the grid still covers the SMs (8 tokens per CTA would
+// otherwise leave a 64-token batch on 8 of them), and for grids of only a
+// few waves so that the last wave's per-warp chains stay short.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -394,23 +395,49 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t* status, cudaStream
     return cudaGetLastError();
 }
 
-// Column chunks (in 16-byte vectors, a multiple of 32) for a grid of
-// `rows_grid` CTAs along the tokens: one chunk (the whole row) once the
-// token CTAs alone cover the SMs twice, else enough chunks to do so.
-static int column_chunk(int rows_grid, int nvec) {
-    const int want = 2 * num_sms();
+// Column chunks (in 16-byte vectors) for a grid of `rows_grid` CTAs along
+// the tokens (8 tokens per CTA), over grid.y.
+//  - Few tokens (fewer CTAs than twice the SMs): chunks of a multiple of 32
+//    vectors, enough for twice the SMs.
+//  - Otherwise: a warp walks its token's row one step at a time (`step`
+//    vectors, one memory round trip each), and the grid runs in waves of
+//    the CTAs resident at once (`per_sm` per SM).  With only two or three
+//    waves the last one runs whole-row chains at partial occupancy, so the
+//    rows are split into chunks of a multiple of `step` until the grid spans
+//    about kTargetWaves waves.
+constexpr int kTargetWaves = 6;
+
+static int column_chunk(int rows_grid, int nvec, int step, int per_sm) {
+    const int sms = num_sms();
+    if (rows_grid < 2 * sms) {
+        const int want = 2 * sms;
+        const int split = (want + rows_grid - 1) / rows_grid;
+        int chunk = (nvec + split - 1) / split;
+        chunk = ((chunk + 31) / 32) * 32;
+        return chunk < nvec ? chunk : nvec;
+    }
+    const int want = kTargetWaves * sms * (per_sm > 0 ? per_sm : 1);
     if (rows_grid >= want) return nvec;
     const int split = (want + rows_grid - 1) / rows_grid;
     int chunk = (nvec + split - 1) / split;
-    chunk = ((chunk + 31) / 32) * 32;
+    chunk = ((chunk + step - 1) / step) * step;
     return chunk < nvec ? chunk : nvec;
+}
+
+// Resident CTAs per SM of a permute/combine kernel (256 threads).
+template <typename Kernel>
+static int resident_per_sm(Kernel kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kPCWarps * 32, 0) != cudaSuccess)
+        n = 1;
+    return n > 0 ? n : 1;
 }
 
 cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm, int T, int d,
                            int k, cudaStream_t stream) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    const int chunk = column_chunk(grid, nvec);
+    const int chunk = column_chunk(grid, nvec, 32 * kUnroll, resident_per_sm(k_permute));
     const int ny = (nvec + chunk - 1) / chunk;
     return launch_pdl(k_permute, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), perm_row, static_cast<uint4*>(x_perm), T, nvec,
@@ -509,16 +536,18 @@ cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* s
                            void* out, int T, int d, int k, cudaStream_t stream, const void* extra2) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
-    const int chunk = column_chunk(grid, nvec);
-    const int ny = (nvec + chunk - 1) / chunk;
     const uint4* y4 = static_cast<const uint4*>(y);
     const uint4* s4 = static_cast<const uint4*>(shared_out);
     const uint4* x4 = static_cast<const uint4*>(extra2);
     uint4* o4 = static_cast<uint4*>(out);
     switch (k) {
-#define MOE_COMBINE_K(KK)                                                                           \
-    case KK: return launch_pdl(k_combine<KK>, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream, y4, \
-                               perm_row, s4, x4, o4, T, nvec, chunk);
+#define MOE_COMBINE_K(KK)                                                                       \
+    case KK: {                                                                                  \
+        const int chunk = column_chunk(grid, nvec, 64, resident_per_sm(k_combine<KK>));         \
+        const int ny = (nvec + chunk - 1) / chunk;                                              \
+        return launch_pdl(k_combine<KK>, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream, y4,    \
+                          perm_row, s4, x4, o4, T, nvec, chunk);                                \
+    }
         MOE_COMBINE_K(1) MOE_COMBINE_K(2) MOE_COMBINE_K(3) MOE_COMBINE_K(4)
         MOE_COMBINE_K(5) MOE_COMBINE_K(6) MOE_COMBINE_K(7) MOE_COMBINE_K(8)
 #undef MOE_COMBINE_K
