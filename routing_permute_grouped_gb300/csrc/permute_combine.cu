@@ -409,6 +409,7 @@ constexpr int kTargetWaves = 6;
 
 static int column_chunk(int rows_grid, int nvec, int step, int per_sm) {
     const int sms = num_sms();
+    if (rows_grid <= 0) return nvec;
     if (rows_grid < 2 * sms) {
         const int want = 2 * sms;
         const int split = (want + rows_grid - 1) / rows_grid;
@@ -437,6 +438,7 @@ cudaError_t launch_permute(const void* x, const int32_t* perm_row, void* x_perm,
                            int k, cudaStream_t stream) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
+    if (grid == 0 || nvec == 0) return cudaSuccess;
     const int chunk = column_chunk(grid, nvec, 32 * kUnroll, resident_per_sm(k_permute));
     const int ny = (nvec + chunk - 1) / chunk;
     return launch_pdl(k_permute, dim3(grid, ny), dim3(kPCWarps * 32), 0, stream,
@@ -536,6 +538,7 @@ cudaError_t launch_combine(const void* y, const int32_t* perm_row, const void* s
                            void* out, int T, int d, int k, cudaStream_t stream, const void* extra2) {
     const int nvec = d / 8;
     const int grid = (T + kPCWarps - 1) / kPCWarps;
+    if (grid == 0 || nvec == 0) return cudaSuccess;
     const uint4* y4 = static_cast<const uint4*>(y);
     const uint4* s4 = static_cast<const uint4*>(shared_out);
     const uint4* x4 = static_cast<const uint4*>(extra2);
