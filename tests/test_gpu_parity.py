@@ -518,6 +518,22 @@ def test_shared_expert_stage(name):
     assert_close(f64(ys), ref["ys"], "ys")
 
 
+def assert_combine_bound(got, expect, y, perm_row, k, ys=None):
+    """The combine sums k (+1) bf16 values in fp32 in a fixed order and rounds
+    once to bf16.  Against the exact fp64 sum its error is at most half a
+    bf16 ulp of the result plus the fp32 additions' error, each at most 2^-24
+    of a partial sum, so k (+1) x 2^-24 x the sum of the terms' magnitudes;
+    the second term matters only where the terms cancel.  Nearly every
+    output is the correctly rounded exact sum."""
+    mag = oracle.combine(np.abs(oracle.bf16_to_f64(bits(y))), perm_row, k,
+                         None if ys is None else np.abs(oracle.bf16_to_f64(bits(ys))))
+    n_terms = k + (0 if ys is None else 1)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(expect))[1] - 8)
+    bound = ulp + n_terms * 2.0 ** -24 * mag
+    assert (np.abs(got - expect) <= bound).all()
+    assert np.mean(got == oracle.round_bf16(expect)) > 0.999
+
+
 @pytest.mark.parametrize("shared", [False, True])
 def test_combine_stage(shared):
     shape, inp, ref = prepared("small_default")
@@ -531,10 +547,43 @@ def test_combine_stage(shared):
     expect = oracle.combine(oracle.bf16_to_f64(bits(y)), ref["perm_row"], shape.k,
                             None if ys is None else oracle.bf16_to_f64(bits(ys)))
     got = f64(out)
-    # fp32 sum of at most k+1 bf16 values, one rounding: within one bf16 ulp
-    ulp = np.ldexp(1.0, np.frexp(np.abs(expect))[1] - 8)
-    assert (np.abs(got - expect) <= ulp).all()
-    assert np.mean(got == oracle.round_bf16(expect)) > 0.999
+    assert_combine_bound(got, expect, y, ref["perm_row"], shape.k, ys)
+
+
+@pytest.mark.parametrize("T, d, k, E", [
+    (3000, 1152, 4, 8),   # 375 token CTAs: 3 combine and 2 permute column chunks, the last 16 vectors
+    (2500, 2176, 8, 16),  # 313 token CTAs, k = 8: 5 combine and 3 permute chunks, the last 16 vectors
+])
+def test_permute_combine_column_chunks(T, d, k, E):
+    """Grids of a few hundred token CTAs split their rows into column chunks
+    (over grid.y) until they span about six waves of resident CTAs; the
+    last chunk here is ragged.  The permute copies bit for bit (the
+    oracle's rows, pad rows untouched) and the combine stays within one bf16
+    ulp of the oracle's fp64 sum, with and without a shared row."""
+    rng = np.random.default_rng(T + d)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.random(idx.shape).astype(np.float32)
+    off = oracle.build_offsets(idx, w.astype(np.float64), E, 128)
+    perm, row_src = off["perm_row"], off["row_src"]
+    R = row_src.size
+    cfg = moe.config_of(T=T, d=d, d_e=128, E=E, k=k)
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    x_perm = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, cuda(x), cuda(torch.as_tensor(perm)), x_perm)
+    got = bits(x_perm.cpu())
+    ref = oracle.permute(bits(x), row_src, k)
+    valid = row_src >= 0
+    assert np.array_equal(got[valid], ref[valid])
+    assert (got[~valid] == 0).all()
+    y = torch.randn((R, d), generator=g).to(torch.bfloat16)
+    y64 = oracle.bf16_to_f64(bits(y))
+    for shared in (False, True):
+        ys = torch.randn((T, d), generator=g).to(torch.bfloat16) if shared else None
+        out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+        moe.moe_combine(cfg, cuda(y), cuda(torch.as_tensor(perm)), cuda(ys), out)
+        expect = oracle.combine(y64, perm, k, None if ys is None else oracle.bf16_to_f64(bits(ys)))
+        assert_combine_bound(f64(out), expect, y, perm, k, ys)
 
 
 @pytest.mark.parametrize("T, d, ds, k, R", [
