@@ -558,8 +558,9 @@ def test_permute_combine_column_chunks(T, d, k, E):
     """Grids of a few hundred token CTAs split their rows into column chunks
     (over grid.y) until they span about six waves of resident CTAs; the
     last chunk here is ragged.  The permute copies bit for bit (the
-    oracle's rows, pad rows untouched) and the combine stays within one bf16
-    ulp of the oracle's fp64 sum, with and without a shared row."""
+    oracle's rows, pad rows untouched) and the combine stays within the
+    fp32 summation bound of the oracle's fp64 sum, with and without a shared
+    row."""
     rng = np.random.default_rng(T + d)
     idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     w = rng.random(idx.shape).astype(np.float32)
